@@ -1,0 +1,166 @@
+"""CPU oracle for paged KV-cache attention (fp64).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by ``__graft_entry__.smoke``
+and by the bench's CPU-baseline leg, never by the product library.  It shares
+no code with the CUDA path; ``ref.c`` is compiled here with gcc.
+
+Every function here follows a definition on the pages (see ``ref.c`` for the
+per-step citations):
+  * ``slot_mapping``   - slot of each new token (nano-vllm walkthrough, Step 5)
+  * ``store_kvcache``  - bit copy of K/V rows into their slots, -1 skipped (Step 4)
+  * ``gather_dense``   - block_table[pos // bs], pos % bs resolution (mini-infer §2.2-2.3)
+  * ``paged_attention``- causal softmax(q K^T * scale) V, bottom-right aligned,
+                         in double precision (KV-cache toy of the inference notes)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ref.c into _build/liboracle.so (gcc, OpenMP)."""
+    src = os.path.join(_HERE, "ref.c")
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(src):
+        return _SO
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = _SO + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", src, "-o", tmp, "-lm"])
+    os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            lib.oracle_slot_mapping.restype = ctypes.c_int64
+            lib.oracle_slot_mapping.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_int, P]
+            lib.oracle_store_kvcache.restype = None
+            lib.oracle_store_kvcache.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_int64]
+            lib.oracle_gather_dense.restype = None
+            lib.oracle_gather_dense.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+            lib.oracle_paged_attention.restype = ctypes.c_int64
+            lib.oracle_paged_attention.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_double, P, P, ctypes.c_int]
+            lib.oracle_max_threads.restype = ctypes.c_int
+            lib.oracle_max_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 tensor (torch) or uint16 array -> contiguous uint16 numpy array of the raw bits."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch
+    assert x.dtype == torch.bfloat16
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _i32(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def flatten_blocks(block_lists):
+    """Per-sequence block lists -> (offsets [B+1], flat ids)."""
+    off = np.zeros(len(block_lists) + 1, dtype=np.int32)
+    for i, b in enumerate(block_lists):
+        off[i + 1] = off[i] + len(b)
+    ids = np.concatenate([np.asarray(b, np.int32) for b in block_lists]) if block_lists else np.zeros(0, np.int32)
+    return off, _i32(ids)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def slot_mapping(seq_lens, query_lens, block_lists, block_size: int) -> np.ndarray:
+    lib = _load()
+    seq_lens, query_lens = _i32(seq_lens), _i32(query_lens)
+    off, ids = flatten_blocks(block_lists)
+    out = np.empty(int(query_lens.sum()), dtype=np.int32)
+    n = lib.oracle_slot_mapping(len(seq_lens), _ptr(seq_lens), _ptr(query_lens), _ptr(off), _ptr(ids),
+                                block_size, _ptr(out))
+    if n < 0:
+        raise ValueError("position outside the sequence's block list")
+    return out
+
+
+def store_kvcache(k_cache: np.ndarray, v_cache: np.ndarray, k, v, slots) -> None:
+    """In place on uint16 numpy caches of shape [num_blocks, bs, Hkv, D]."""
+    lib = _load()
+    kb, vb, slots = _bits(k), _bits(v), _i32(slots)
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    row = int(np.prod(k_cache.shape[2:]))
+    assert kb.size == slots.size * row
+    lib.oracle_store_kvcache(_ptr(k_cache), _ptr(v_cache), _ptr(kb), _ptr(vb), _ptr(slots), slots.size, row)
+
+
+def gather_dense(cache, length: int, blocks, block_size: int) -> np.ndarray:
+    """Dense [length, Hkv, D] float64 rows of one sequence."""
+    lib = _load()
+    c = _bits(cache)
+    hkv, d = c.shape[2], c.shape[3]
+    blocks = _i32(blocks)
+    out = np.empty((length, hkv, d), dtype=np.float64)
+    lib.oracle_gather_dense(_ptr(c), length, _ptr(blocks), hkv, d, block_size, _ptr(out))
+    return out
+
+
+def paged_attention(q, k_cache, v_cache, seq_lens, query_lens, block_lists, block_size: int,
+                    scale: float, row_select=None, num_threads: int = 0):
+    """Causal paged attention in fp64.
+
+    Returns (out [T, Hq, D] float64, pairs) where pairs is the number of
+    (query row, head, key) scores computed.  Rows not selected by
+    ``row_select`` (bool/uint8 [T]) are NaN.
+    """
+    lib = _load()
+    qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
+    seq_lens, query_lens = _i32(seq_lens), _i32(query_lens)
+    off, ids = flatten_blocks(block_lists)
+    t, hq, d = qb.shape
+    hkv = kb.shape[2]
+    out = np.full((t, hq, d), np.nan, dtype=np.float64)
+    sel = None
+    if row_select is not None:
+        sel = np.ascontiguousarray(np.asarray(row_select, dtype=np.uint8))
+        assert sel.size == t
+    pairs = lib.oracle_paged_attention(_ptr(qb), _ptr(kb), _ptr(vb), len(seq_lens), _ptr(seq_lens),
+                                       _ptr(query_lens), _ptr(off), _ptr(ids), hq, hkv, d, block_size,
+                                       float(scale), _ptr(sel) if sel is not None else None, _ptr(out),
+                                       int(num_threads))
+    if pairs < 0:
+        raise ValueError("malformed paged-attention input")
+    return out, int(pairs)
+
+
+def run_batch(pool_k: np.ndarray, pool_v: np.ndarray, batch, block_size: int, row_select=None,
+              num_threads: int = 0):
+    """Store the batch's new K/V into the (uint16) pool copies, then attend.
+
+    The two steps in the order the attention layer runs them: store, then
+    attention (nano-vllm walkthrough, Step 4).  Mutates pool_k / pool_v.
+    """
+    slots = slot_mapping(batch.seq_lens, batch.query_lens, batch.block_lists, block_size)
+    store_kvcache(pool_k, pool_v, batch.k, batch.v, slots)
+    return paged_attention(batch.q, pool_k, pool_v, batch.seq_lens, batch.query_lens, batch.block_lists,
+                           block_size, batch.scale, row_select=row_select, num_threads=num_threads)

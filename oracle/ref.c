@@ -1,0 +1,224 @@
+/*
+ * Oracle for attention over a paged (block-table) KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library includes, links
+ * or calls this file; only the tests, the package's smoke check and the
+ * bench's CPU-baseline leg do.  It shares no code, header, table or constant
+ * with the CUDA path.
+ *
+ * Plain, slow, obviously correct: every floating-point step is done in
+ * double precision on bf16-valued inputs (bf16 -> double is exact), with no
+ * tiling, fusion or reordering beyond the definitions below.
+ *
+ * Sources (page title, section):
+ *  - "手搓 vLLM 推理引擎" (LLM-101-CN nano-vllm walkthrough), Step 4
+ *    "Triton Kernel：写入 KV Cache": a token whose slot is -1 is skipped,
+ *    otherwise its num_kv_heads*head_dim K and V values are copied to
+ *    cache row `slot`.
+ *  - same page, Step 5 "prepare_prefill()" / "prepare_decode()": the new
+ *    tokens of a sequence are positions [num_cached, len); their slots are
+ *    block_table[pos / block_size] * block_size + pos % block_size (the
+ *    decode form, block_table[-1]*bs + last_block_num_tokens - 1, is the same
+ *    formula at pos = len - 1).
+ *  - "mini-infer系统实战-03-向量化 KV Gather", sections 2.2-2.3: the physical
+ *    block of logical position pos is block_table[pos // block_size] and the
+ *    row inside it is pos % block_size; the gathered rows form dense K/V.
+ *  - "推理系统" (CS 与 LLM 学习知识库), the KV-cache toy: new tokens sit at
+ *    the end, new token i (of T) sees the first S - T + i + 1 keys (a lower
+ *    triangular mask shifted by S - T), scores are q.k * scale, softmax over
+ *    the visible keys, output is the probability-weighted sum of V.
+ *  - "面试问答准备: nano-vLLM 推理引擎优化", Q1: the causal bound of a query
+ *    at absolute position p is context_len = p + 1.
+ *  - Grouped-query attention: query head h reads KV head h / (Hq / Hkv)
+ *    (contiguous groups; the pages do not state the mapping, this is the
+ *    plainest reading and reduces to multi-head attention when Hq == Hkv).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Slot of every new token (prepare_prefill / prepare_decode).
+ * Sequence b has seq_lens[b] tokens of which the last query_lens[b] are new;
+ * its physical blocks are blk_ids[blk_off[b] .. blk_off[b+1]).
+ * Writes sum(query_lens) slots in sequence order.  Returns the count, or -1
+ * if a position falls outside the sequence's block list.
+ */
+int64_t oracle_slot_mapping(int num_seqs, const int32_t *seq_lens, const int32_t *query_lens,
+                            const int32_t *blk_off, const int32_t *blk_ids, int block_size,
+                            int32_t *slots)
+{
+    int64_t t = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        int first = seq_lens[b] - query_lens[b];
+        for (int pos = first; pos < seq_lens[b]; ++pos) {
+            int logical = pos / block_size;
+            if (logical >= blk_off[b + 1] - blk_off[b])
+                return -1;
+            int phys = blk_ids[blk_off[b] + logical];
+            slots[t++] = phys * block_size + pos % block_size;
+        }
+    }
+    return t;
+}
+
+/*
+ * KV scatter: cache row `slot` (row = num_kv_heads*head_dim bf16 values)
+ * receives the token's K and V rows, bit for bit.  slot == -1 is skipped.
+ */
+void oracle_store_kvcache(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k, const uint16_t *v,
+                          const int32_t *slots, int64_t num_tokens, int64_t row_elems)
+{
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int32_t s = slots[t];
+        if (s == -1)
+            continue;
+        memcpy(k_cache + (int64_t)s * row_elems, k + t * row_elems, (size_t)row_elems * 2);
+        memcpy(v_cache + (int64_t)s * row_elems, v + t * row_elems, (size_t)row_elems * 2);
+    }
+}
+
+/*
+ * Dense rebuild of one sequence's keys (or values) through its block list:
+ * dense[j][g][d] = cache[blk[j / bs]][j % bs][g][d], for j < len.
+ */
+void oracle_gather_dense(const uint16_t *cache, int len, const int32_t *blocks, int num_kv_heads,
+                         int head_dim, int block_size, double *dense)
+{
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int j = 0; j < len; ++j) {
+        int64_t phys = blocks[j / block_size];
+        int64_t slot = phys * block_size + j % block_size;
+        const uint16_t *src = cache + slot * row;
+        for (int64_t e = 0; e < row; ++e)
+            dense[(int64_t)j * row + e] = bf16_to_double(src[e]);
+    }
+}
+
+/*
+ * Causal attention for every query row of every sequence.
+ *   q:   [sum(query_lens), Hq, D] bf16 bits, rows in sequence order
+ *   out: [sum(query_lens), Hq, D] double
+ * Query row i of sequence b (0 <= i < query_lens[b]) is at absolute position
+ * seq_lens[b] - query_lens[b] + i and sees keys 0..that position.
+ * row_select (nullable): when given, only packed query rows t with
+ * row_select[t] != 0 are computed (all heads); other output rows are left
+ * untouched.  Returns the number of (query row, head, key) scores computed,
+ * or -1 on malformed input.
+ */
+int64_t oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                               int num_seqs, const int32_t *seq_lens, const int32_t *query_lens,
+                               const int32_t *blk_off, const int32_t *blk_ids, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size, double scale,
+                               const uint8_t *row_select, double *out, int num_threads)
+{
+#ifdef _OPENMP
+    if (num_threads > 0)
+        omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+    if (num_heads % num_kv_heads != 0)
+        return -1;
+    const int group = num_heads / num_kv_heads;
+    const int64_t kv_row = (int64_t)num_kv_heads * head_dim;
+    int64_t pairs = 0;
+    int64_t q_begin = 0;
+
+    for (int b = 0; b < num_seqs; ++b) {
+        const int lk = seq_lens[b], lq = query_lens[b];
+        if (lq < 0 || lk < lq || (lq > 0 && lk < 1))
+            return -1;
+        if ((int64_t)(lk + block_size - 1) / block_size > blk_off[b + 1] - blk_off[b])
+            return -1;
+        int any = 0;
+        for (int i = 0; i < lq; ++i)
+            if (!row_select || row_select[q_begin + i])
+                any = 1;
+        if (!any) {
+            q_begin += lq;
+            continue;
+        }
+        /* step 1: dense K and V of this sequence through its block table */
+        double *kd = (double *)malloc(sizeof(double) * (size_t)lk * (size_t)kv_row);
+        double *vd = (double *)malloc(sizeof(double) * (size_t)lk * (size_t)kv_row);
+        if (!kd || !vd) {
+            free(kd);
+            free(vd);
+            return -1;
+        }
+        oracle_gather_dense(k_cache, lk, blk_ids + blk_off[b], num_kv_heads, head_dim, block_size, kd);
+        oracle_gather_dense(v_cache, lk, blk_ids + blk_off[b], num_kv_heads, head_dim, block_size, vd);
+
+        /* step 2: causal softmax(q K^T * scale) V for each (row, head) */
+        int64_t work = (int64_t)lq * num_heads;
+        int64_t seq_pairs = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(+ : seq_pairs)
+        for (int64_t w = 0; w < work; ++w) {
+            int i = (int)(w / num_heads), h = (int)(w % num_heads);
+            int64_t t = q_begin + i;
+            if (row_select && !row_select[t])
+                continue;
+            int g = h / group;
+            int visible = lk - lq + i + 1; /* keys 0 .. position */
+            const uint16_t *qrow = q + (t * num_heads + h) * head_dim;
+            double *qd = (double *)malloc(sizeof(double) * (size_t)head_dim);
+            double *s = (double *)malloc(sizeof(double) * (size_t)visible);
+            for (int d = 0; d < head_dim; ++d)
+                qd[d] = bf16_to_double(qrow[d]);
+            double m = -INFINITY;
+            for (int j = 0; j < visible; ++j) {
+                const double *kr = kd + (int64_t)j * kv_row + (int64_t)g * head_dim;
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d)
+                    dot += qd[d] * kr[d];
+                s[j] = dot * scale;
+                if (s[j] > m)
+                    m = s[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j < visible; ++j) {
+                s[j] = exp(s[j] - m);
+                l += s[j];
+            }
+            double *o = out + (t * num_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                o[d] = 0.0;
+            for (int j = 0; j < visible; ++j) {
+                const double *vr = vd + (int64_t)j * kv_row + (int64_t)g * head_dim;
+                double p = s[j] / l;
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] += p * vr[d];
+            }
+            seq_pairs += visible;
+            free(qd);
+            free(s);
+        }
+        pairs += seq_pairs;
+        free(kd);
+        free(vd);
+        q_begin += lq;
+    }
+    return pairs;
+}

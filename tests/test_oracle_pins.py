@@ -1,0 +1,277 @@
+"""Pins for the CPU oracle: facts fixed by the pages and by mathematics.
+
+Each test checks the oracle against something other than itself: hand-worked
+fixtures, a pure-Python brute force, closed forms, invariants and a library
+routine (torch's fp64 attention on the CPU).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import brute
+from paged_kv_cache_kvcache_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def _identity_case(seed, num_seqs, hq, hkv, d, bs, max_len, cached=True):
+    """Blocks of sequence b are consecutive (identity layout), so the dense
+    keys of b are a plain slice of the pool: no slot arithmetic needed."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(1, max_len + 1, (num_seqs,), generator=g).numpy().astype(np.int32)
+    if cached:
+        qlens = np.array([int(torch.randint(1, int(l) + 1, (1,), generator=g)) for l in lens], np.int32)
+    else:
+        qlens = lens.copy()
+    nblk = [-(-int(l) // bs) for l in lens]
+    starts = np.concatenate([[0], np.cumsum(nblk)]).astype(np.int32)
+    blocks = [np.arange(starts[b], starts[b + 1], dtype=np.int32) for b in range(num_seqs)]
+    nb = int(starts[-1]) + 2
+    pool_k = torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16)
+    pool_v = torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16)
+    t = int(qlens.sum())
+    q = torch.randn(t, hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(t, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(t, hkv, d, generator=g).to(torch.bfloat16)
+    return dict(lens=lens, qlens=qlens, blocks=blocks, starts=starts, pool_k=pool_k, pool_v=pool_v,
+                q=q, k=k, v=v, bs=bs, scale=1.0 / np.sqrt(d))
+
+
+def _contiguous_kv(c, b):
+    """Dense K/V of sequence b for the identity layout: cached prefix is a
+    slice of the pool, the new tokens follow."""
+    bs = c["bs"]
+    lk, lq = int(c["lens"][b]), int(c["qlens"][b])
+    t0 = int(c["qlens"][:b].sum())
+    hkv, d = c["pool_k"].shape[2], c["pool_k"].shape[3]
+    flat_k = c["pool_k"].reshape(-1, hkv, d)
+    flat_v = c["pool_v"].reshape(-1, hkv, d)
+    s0 = int(c["starts"][b]) * bs
+    kk = torch.cat([flat_k[s0:s0 + lk - lq], c["k"][t0:t0 + lq]])
+    vv = torch.cat([flat_v[s0:s0 + lk - lq], c["v"][t0:t0 + lq]])
+    return kk, vv
+
+
+def _oracle_case(c):
+    pk, pv = _bits(c["pool_k"]), _bits(c["pool_v"])
+    slots = oracle.slot_mapping(c["lens"], c["qlens"], c["blocks"], c["bs"])
+    oracle.store_kvcache(pk, pv, c["k"], c["v"], slots)
+    out, pairs = oracle.paged_attention(c["q"], pk, pv, c["lens"], c["qlens"], c["blocks"], c["bs"], c["scale"])
+    return out, pairs, pk, pv
+
+
+# ---------------------------------------------------------------- fixtures
+
+
+def test_gather_golden():
+    fx = json.load(open(os.path.join(GOLDEN, "gather_toy.json")))
+    pool = torch.tensor(fx["pool"], dtype=torch.float32).to(torch.bfloat16)
+    for s in fx["sequences"]:
+        dense = oracle.gather_dense(pool, s["len"], s["blocks"], fx["block_size"])
+        assert dense.tolist() == [[[float(x) for x in h] for h in row] for row in s["expected"]]
+
+
+def test_slot_mapping_golden():
+    fx = json.load(open(os.path.join(GOLDEN, "slot_mapping_toy.json")))
+    seqs = fx["sequences"]
+    lens = [s["len"] for s in seqs]
+    qlens = [s["len"] - s["num_cached"] for s in seqs]
+    blocks = [s["blocks"] for s in seqs]
+    got = oracle.slot_mapping(lens, qlens, blocks, fx["block_size"])
+    want = sum((s["expected_slots"] for s in seqs), [])
+    assert got.tolist() == want
+
+
+def test_slot_mapping_rejects_short_block_list():
+    with pytest.raises(ValueError):
+        oracle.slot_mapping([17], [17], [[0]], 16)
+
+
+# ---------------------------------------------------------------- scatter
+
+
+def test_scatter_matches_fancy_index_and_keeps_canary():
+    g = torch.Generator().manual_seed(11)
+    nb, bs, hkv, d, t = 9, 4, 3, 8, 13
+    kc = _bits(torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16))
+    vc = _bits(torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16))
+    k = torch.randn(t, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(t, hkv, d, generator=g).to(torch.bfloat16)
+    slots = torch.randperm(nb * bs, generator=g)[:t].numpy().astype(np.int32)
+    slots[[2, 7]] = -1  # padded tokens
+    want_k, want_v = kc.copy(), vc.copy()
+    ok = slots >= 0
+    want_k.reshape(nb * bs, -1)[slots[ok]] = _bits(k).reshape(t, -1)[ok]
+    want_v.reshape(nb * bs, -1)[slots[ok]] = _bits(v).reshape(t, -1)[ok]
+    before = kc.copy()
+    oracle.store_kvcache(kc, vc, k, v, slots)
+    assert np.array_equal(kc, want_k) and np.array_equal(vc, want_v)
+    untouched = np.setdiff1d(np.arange(nb * bs), slots[ok])
+    assert np.array_equal(kc.reshape(nb * bs, -1)[untouched], before.reshape(nb * bs, -1)[untouched])
+
+
+# ---------------------------------------------------------------- attention vs brute force
+
+
+@pytest.mark.parametrize("seed,hq,hkv,bs,cached", [(1, 4, 2, 4, True), (2, 3, 1, 5, False), (3, 2, 2, 8, True)])
+def test_oracle_matches_brute_force(seed, hq, hkv, bs, cached):
+    c = _identity_case(seed, num_seqs=3, hq=hq, hkv=hkv, d=16, bs=bs, max_len=24, cached=cached)
+    out, _, _, _ = _oracle_case(c)
+    t0 = 0
+    for b in range(3):
+        kk, vv = _contiguous_kv(c, b)
+        lq = int(c["qlens"][b])
+        qb = _f64(c["q"][t0:t0 + lq]).tolist()
+        ref = np.array(brute.attention(qb, _f64(kk).tolist(), _f64(vv).tolist(), c["scale"]))
+        np.testing.assert_allclose(out[t0:t0 + lq], ref, rtol=0, atol=1e-12)
+        t0 += lq
+
+
+def test_tiny_workload_matches_brute_force_on_numpy_gather():
+    """Seeded tiny case (permuted pool): dense K/V rebuilt independently by
+    numpy advanced indexing, pool[blocks[pos // bs], pos % bs]."""
+    w = workloads.tiny()
+    bs = w.pool.block_size
+    pk, pv = _bits(w.pool.k_cache), _bits(w.pool.v_cache)
+    for batch in w.batches:
+        out, _ = oracle.run_batch(pk, pv, batch, bs)
+        t0 = 0
+        for b in range(batch.num_seqs):
+            lk, lq = int(batch.seq_lens[b]), int(batch.query_lens[b])
+            pos = np.arange(lk)
+            blk = batch.block_lists[b][pos // bs]
+            kk = torch.from_numpy(pk.view(np.int16)[blk, pos % bs].copy()).view(torch.bfloat16)
+            vv = torch.from_numpy(pv.view(np.int16)[blk, pos % bs].copy()).view(torch.bfloat16)
+            qb = _f64(batch.q[t0:t0 + lq]).tolist()
+            ref = np.array(brute.attention(qb, _f64(kk).tolist(), _f64(vv).tolist(), batch.scale))
+            np.testing.assert_allclose(out[t0:t0 + lq], ref, rtol=0, atol=1e-12)
+            t0 += lq
+
+
+def test_oracle_matches_torch_sdpa_fp64():
+    """Library routine: torch CPU fp64 attention with a causal mask, Lq == Lk."""
+    c = _identity_case(21, num_seqs=2, hq=6, hkv=2, d=32, bs=16, max_len=70, cached=False)
+    out, _, _, _ = _oracle_case(c)
+    t0 = 0
+    for b in range(2):
+        kk, vv = _contiguous_kv(c, b)
+        lq = int(c["qlens"][b])
+        q = c["q"][t0:t0 + lq].to(torch.float64).transpose(0, 1)
+        k = kk.to(torch.float64).transpose(0, 1).repeat_interleave(3, dim=0)
+        v = vv.to(torch.float64).transpose(0, 1).repeat_interleave(3, dim=0)
+        ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, scale=c["scale"])
+        np.testing.assert_allclose(out[t0:t0 + lq], ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12)
+        t0 += lq
+
+
+# ---------------------------------------------------------------- invariants
+
+
+def test_permutation_invariance_bit_exact():
+    c = _identity_case(5, num_seqs=4, hq=4, hkv=2, d=16, bs=4, max_len=30, cached=True)
+    out_a, _, _, _ = _oracle_case(c)
+    nb = c["pool_k"].shape[0]
+    sigma = torch.randperm(nb, generator=torch.Generator().manual_seed(99))
+    inv = torch.empty_like(sigma)
+    inv[sigma] = torch.arange(nb)
+    c2 = dict(c)
+    c2["pool_k"] = c["pool_k"][inv]  # new_pool[sigma[p]] = pool[p]
+    c2["pool_v"] = c["pool_v"][inv]
+    c2["blocks"] = [sigma.numpy()[b].astype(np.int32) for b in c["blocks"]]
+    out_b, _, _, _ = _oracle_case(c2)
+    assert np.array_equal(out_a, out_b)
+
+
+def test_pair_count_closed_form():
+    c = _identity_case(6, num_seqs=5, hq=3, hkv=1, d=8, bs=4, max_len=40, cached=True)
+    _, pairs, _, _ = _oracle_case(c)
+    lk, lq = c["lens"].astype(np.int64), c["qlens"].astype(np.int64)
+    assert pairs == 3 * int(np.sum(lq * (lk - lq) + lq * (lq + 1) // 2))
+    # full prefill of N tokens: N(N+1)/2 pairs per head
+    n = 37
+    c = _fixed_len_case(n, n, hq=1, hkv=1, d=8, bs=8, seed=7)
+    _, pairs, _, _ = _oracle_case(c)
+    assert pairs == n * (n + 1) // 2
+
+
+def _fixed_len_case(lk, lq, hq, hkv, d, bs, seed, scale=None):
+    g = torch.Generator().manual_seed(seed)
+    nblk = -(-lk // bs)
+    pool_k = torch.randn(nblk + 1, bs, hkv, d, generator=g).to(torch.bfloat16)
+    pool_v = torch.randn(nblk + 1, bs, hkv, d, generator=g).to(torch.bfloat16)
+    perm = torch.randperm(nblk + 1, generator=g).numpy().astype(np.int32)
+    return dict(lens=np.array([lk], np.int32), qlens=np.array([lq], np.int32), blocks=[perm[:nblk]],
+                starts=None, pool_k=pool_k, pool_v=pool_v,
+                q=torch.randn(lq, hq, d, generator=g).to(torch.bfloat16),
+                k=torch.randn(lq, hkv, d, generator=g).to(torch.bfloat16),
+                v=torch.randn(lq, hkv, d, generator=g).to(torch.bfloat16),
+                bs=bs, scale=scale if scale is not None else 1.0 / np.sqrt(d))
+
+
+def test_prefix_suffix_equals_full_prefill_rows():
+    """300-token sequence: querying only the last 44 (first 256 cached) gives
+    exactly rows 256..299 of the full prefill."""
+    full = _fixed_len_case(300, 300, hq=4, hkv=2, d=64, bs=256, seed=8)
+    out_full, _, pk, pv = _oracle_case(full)
+    out_sfx, _ = oracle.paged_attention(full["q"][256:], pk, pv, [300], [44], full["blocks"], 256, full["scale"])
+    assert np.array_equal(out_sfx, out_full[256:])
+
+
+def test_decode_equals_last_prefill_row():
+    n = 65
+    full = _fixed_len_case(n, n, hq=2, hkv=1, d=64, bs=16, seed=9)
+    out_full, _, pk, pv = _oracle_case(full)
+    out_dec, _ = oracle.paged_attention(full["q"][n - 1:], pk, pv, [n], [1], full["blocks"], 16, full["scale"])
+    assert np.array_equal(out_dec[0], out_full[n - 1])
+
+
+# ---------------------------------------------------------------- closed forms
+
+
+def test_single_key_returns_its_value_exactly():
+    c = _fixed_len_case(1, 1, hq=3, hkv=3, d=32, bs=16, seed=10)
+    out, _, _, _ = _oracle_case(c)
+    np.testing.assert_array_equal(out[0], _f64(c["v"][0]))
+
+
+def test_zero_scale_gives_mean_of_visible_values():
+    c = _fixed_len_case(20, 20, hq=2, hkv=1, d=16, bs=4, seed=12, scale=0.0)
+    out, _, _, _ = _oracle_case(c)
+    vv = _f64(c["v"])  # full prefill: the dense values are the new tokens' values
+    for i in range(20):
+        np.testing.assert_allclose(out[i, 0], vv[:i + 1, 0].mean(axis=0), rtol=0, atol=1e-13)
+
+
+def test_equal_keys_give_mean_of_values():
+    c = _fixed_len_case(12, 12, hq=1, hkv=1, d=8, bs=4, seed=13)
+    c["k"] = c["k"][:1].expand(12, 1, 8).contiguous()
+    out, _, _, _ = _oracle_case(c)
+    vv = _f64(c["v"])
+    for i in range(12):
+        np.testing.assert_allclose(out[i, 0], vv[:i + 1, 0].mean(axis=0), rtol=0, atol=1e-13)
+
+
+def test_dominant_logit_selects_that_value():
+    n, d, star = 10, 16, 6
+    c = _fixed_len_case(n, n, hq=1, hkv=1, d=d, bs=4, seed=14, scale=1.0)
+    k = torch.zeros(n, 1, d)
+    for j in range(n):
+        k[j, 0, j] = 1.0  # orthonormal keys
+    c["k"] = k.to(torch.bfloat16)
+    q = torch.zeros(n, 1, d)
+    q[n - 1, 0, star] = 40.0
+    c["q"] = q.to(torch.bfloat16)
+    out, _, _, _ = _oracle_case(c)
+    np.testing.assert_allclose(out[n - 1, 0], _f64(c["v"][star, 0]), rtol=0, atol=1e-12)
