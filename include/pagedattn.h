@@ -1,0 +1,217 @@
+/*
+ * libpagedattn — attention over a paged (block-table) bf16 KV cache, GB300 (sm_103a).
+ *
+ * The cache of one layer is two tensors (K and V), each laid out
+ *     [num_blocks][block_size][num_kv_heads][head_dim]   bf16, row-major,
+ * the per-layer view of the cache described in "手搓 vLLM 推理引擎"
+ * (LLM-101-CN nano-vllm walkthrough), Step 5, "KV Cache 的内存布局".  A token's
+ * slot is block_id * block_size + offset_in_block; row `slot` of the cache holds
+ * its num_kv_heads*head_dim values.
+ *
+ * Three device operations, always in this order within one attention layer
+ * (same page, Step 4, Attention.forward): store the new tokens' K/V, then run
+ * prefill or decode attention.  All of them only enqueue work on `stream`: no
+ * host synchronisation, no allocation, no device-to-host reads.  Every buffer
+ * is owned by the caller.
+ *
+ * Host-side metadata (cu_seqlens, block tables, slot mapping, work lists) is
+ * packed on the CPU into ONE caller-provided buffer by pa_pack_prefill /
+ * pa_pack_decode and uploaded with one asynchronous copy (pa_upload or the
+ * caller's own cudaMemcpyAsync); the library never reads device metadata on
+ * the host ("面试问答准备: nano-vLLM 推理引擎优化", Q1, item 2: scheduling
+ * metadata is computed on the CPU so that no .item() sync is needed).
+ *
+ * Error behaviour: every entry point validates its arguments on the host
+ * before any launch and returns a PA_ERR_* code with no device side effect on
+ * failure.  PA_ERR_CUDA means a CUDA call failed; pa_last_error_string()
+ * gives the text (thread-local).
+ *
+ * Supported: head_dim 64 or 128; num_heads % num_kv_heads == 0 with group
+ * size num_heads/num_kv_heads <= 16; block_size a power of two in [16, 1024];
+ * bf16 data.  Device pointers must be 16-byte aligned.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *pa_stream_t;
+
+enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* malformed sizes, pointers or metadata */
+    PA_ERR_UNSUPPORTED = 2, /* head_dim, group size or block_size outside the supported set */
+    PA_ERR_WORKSPACE = 3,   /* caller buffer (metadata image or decode workspace) too small */
+    PA_ERR_CUDA = 4         /* a CUDA runtime/driver call failed; see pa_last_error_string() */
+};
+
+/* Shapes of one layer's cache and attention heads.  Passed by pointer to every call. */
+typedef struct pa_dims {
+    int32_t num_blocks;   /* physical blocks in the pool */
+    int32_t block_size;   /* tokens per block */
+    int32_t num_heads;    /* query heads Hq */
+    int32_t num_kv_heads; /* KV heads Hkv; query head h reads KV head h / (Hq/Hkv) */
+    int32_t head_dim;     /* D */
+} pa_dims;
+
+/*
+ * Packed prefill metadata: host scalars plus byte offsets of each int32 array
+ * inside the metadata image written by pa_pack_prefill.  After the image is
+ * copied to device memory at `dev`, array X lives at dev + off_X.
+ */
+typedef struct pa_prefill_meta {
+    int32_t num_seqs;
+    int32_t total_q;            /* sum of query lengths = rows of q/out */
+    int32_t max_seqlen_q;
+    int32_t max_seqlen_k;
+    int32_t max_blocks_per_seq; /* row pitch of block_tables */
+    int32_t num_tiles;          /* CTAs of the prefill launch */
+    int32_t rows_per_tile;      /* query positions per tile (128 / group, floored) */
+    int32_t reserved;
+    uint64_t off_cu_seqlens_q;  /* int32 [num_seqs+1] */
+    uint64_t off_cu_seqlens_k;  /* int32 [num_seqs+1] */
+    uint64_t off_block_tables;  /* int32 [num_seqs][max_blocks_per_seq], -1 padded */
+    uint64_t off_slot_mapping;  /* int32 [total_q] */
+    uint64_t off_tiles;         /* int32 [num_tiles][4] work list, longest first */
+    uint64_t total_bytes;       /* size of the image */
+} pa_prefill_meta;
+
+/* Packed decode metadata (one query token per sequence). */
+typedef struct pa_decode_meta {
+    int32_t num_seqs;
+    int32_t max_blocks_per_seq;
+    int32_t num_items;          /* (sequence, key split) work items */
+    int32_t split_tokens;       /* keys per split (multiple of 64) */
+    int32_t max_splits;         /* largest split count of any sequence */
+    int32_t num_partials;       /* partial results in the workspace (sequences with > 1 split) */
+    uint64_t off_context_lens;  /* int32 [num_seqs] */
+    uint64_t off_block_tables;  /* int32 [num_seqs][max_blocks_per_seq], -1 padded */
+    uint64_t off_slot_mapping;  /* int32 [num_seqs] */
+    uint64_t off_items;         /* int32 [num_items][4] work list, longest first */
+    uint64_t off_seq_items;     /* int32 [num_seqs+1] first work item of each sequence */
+    uint64_t total_bytes;
+    uint64_t workspace_bytes;   /* device workspace pa_decode needs */
+} pa_decode_meta;
+
+/* ------------------------------------------------------------------ host packing */
+
+/*
+ * pa_pack_prefill — build the metadata of a prefill batch on the CPU.
+ * Source: "手搓 vLLM 推理引擎", Step 5, prepare_prefill(): sequence b has
+ * seq_lens[b] tokens of which the first seq_lens[b]-query_lens[b] are already
+ * cached (prefix-cache hit); cu_seqlens_q/k are prefix sums of the query and
+ * key lengths; the new tokens are positions [cached, len) and their slots are
+ * block_table[pos / block_size]*block_size + pos % block_size.
+ *   seq_lens, query_lens: host int32 [num_seqs], 0 <= query_lens[b] <= seq_lens[b]
+ *   block_offsets:        host int32 [num_seqs+1]; sequence b's physical blocks
+ *                         are block_ids[block_offsets[b] .. block_offsets[b+1])
+ *                         and must number at least ceil(seq_lens[b]/block_size)
+ *   host_buf:             caller memory (pinned for an asynchronous upload) of
+ *                         host_buf_bytes; NULL to only compute meta->total_bytes
+ * Returns PA_ERR_WORKSPACE (with meta->total_bytes set) when the buffer is too small.
+ */
+int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int32_t *seq_lens,
+                    const int32_t *query_lens, const int32_t *block_offsets,
+                    const int32_t *block_ids, void *host_buf, size_t host_buf_bytes,
+                    pa_prefill_meta *meta);
+
+/*
+ * pa_pack_decode — build the metadata of a decode batch (one new token per
+ * sequence) on the CPU.  Source: same page, Step 5, prepare_decode():
+ * context_lens[b] = len(seq) includes the token being decoded; its slot is
+ * block_table[-1]*block_size + last_block_num_tokens - 1.
+ * The context of each sequence is cut into splits of `split_tokens` keys
+ * (a multiple of 64; 0 = choose from the current device's SM count) whose
+ * partial results are merged by log-sum-exp ("面试问答准备", the Split-K entry:
+ * each segment yields a local max, normaliser and fp32 accumulator, a second
+ * kernel merges them).
+ */
+int pa_pack_decode(const pa_dims *dims, int32_t num_seqs, const int32_t *context_lens,
+                   const int32_t *block_offsets, const int32_t *block_ids, int32_t split_tokens,
+                   void *host_buf, size_t host_buf_bytes, pa_decode_meta *meta);
+
+/* One asynchronous host-to-device copy of a packed metadata image. */
+int pa_upload(void *dev_dst, const void *host_src, size_t bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------ device operations */
+
+/*
+ * pa_store_kvcache — KV scatter.  Source: "手搓 vLLM 推理引擎", Step 4,
+ * "Triton Kernel：写入 KV Cache": token t with slot s = slot_mapping[t] copies
+ * its K and V rows (num_kv_heads*head_dim bf16 each) to cache row s; s == -1
+ * (padding) is skipped.  Bit-exact copy.
+ *   k, v:          device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   k_cache/v_cache: device bf16 [num_blocks][block_size][num_kv_heads][head_dim]
+ *   slot_mapping:  device int32 [num_tokens], each -1 or in [0, num_blocks*block_size)
+ * Slots must be unique (duplicates race).  num_tokens == 0 launches nothing.
+ */
+int pa_store_kvcache(const pa_dims *dims, const void *k, const void *v, void *k_cache,
+                     void *v_cache, const int32_t *slot_mapping, int32_t num_tokens,
+                     pa_stream_t stream);
+
+/*
+ * pa_prefill_varlen — causal variable-length prefill over the paged cache.
+ * Source: "手搓 vLLM 推理引擎", Step 4 (flash_attn_varlen_func with
+ * cu_seqlens_q/k and block_table; prefix-cache hits have cu_seqlens_k >
+ * cu_seqlens_q) and "推理系统" (KV-cache toy: new token i of T sees the first
+ * S-T+i+1 keys).  For sequence b, query row i (0 <= i < Lq) at absolute
+ * position Lk-Lq+i, head h:
+ *   out = softmax(scale * q . K^T over keys j <= Lk-Lq+i) V,  K/V of key j at
+ *   slot block_tables[b][j/block_size]*block_size + j%block_size, KV head h/G.
+ * The K/V of every key (including the new tokens) must already be stored.
+ *   q, out:  device bf16 [meta->total_q][num_heads][head_dim]
+ *   cu_seqlens_q, cu_seqlens_k, block_tables, tiles: device copies of the
+ *            arrays pa_pack_prefill wrote (dev + meta->off_*)
+ * bf16 in, fp32 accumulation and softmax, bf16 out (round to nearest even).
+ */
+int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache,
+                      const void *v_cache, const int32_t *cu_seqlens_q,
+                      const int32_t *cu_seqlens_k, const int32_t *block_tables, float scale,
+                      void *out, const pa_prefill_meta *meta, const int32_t *tiles,
+                      pa_stream_t stream);
+
+/*
+ * pa_decode — batched single-token GQA decode over the paged cache.
+ * Source: "手搓 vLLM 推理引擎", Step 4 (flash_attn_with_kvcache with
+ * cache_seqlens and block_table) and "推理系统" (decode reads the whole cache
+ * and is bandwidth bound).  For sequence b and query head h, the single query
+ * sees all context_lens[b] keys:
+ *   out[b][h] = softmax(scale * q[b][h] . K^T) V.
+ * Long contexts are split per the packed plan; partial (max, sum, fp32
+ * accumulator) triples go to `workspace` and a combine kernel merges them by
+ * log-sum-exp.
+ *   q, out:     device bf16 [num_seqs][num_heads][head_dim]
+ *   workspace:  device memory of at least meta->workspace_bytes (may be NULL
+ *               when that is 0), 256-byte aligned
+ */
+int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *context_lens, const int32_t *block_tables, float scale, void *out,
+              const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items,
+              void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* ------------------------------------------------------------------ diagnostics */
+
+/* Text of the last error on this thread ("" if none). */
+const char *pa_last_error_string(void);
+
+/*
+ * Reads and clears the device-side error word (bounded waits that timed out
+ * inside a kernel set it; 0 = none).  Synchronises `stream`: for tests and
+ * debugging, never on the hot path.
+ */
+int pa_read_device_error(uint32_t *code, pa_stream_t stream);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,199 @@
+// C ABI of libpagedattn: argument validation on the host, then kernel launches.
+// No entry point allocates, synchronises or reads device memory on the host
+// (except pa_read_device_error, a debugging aid).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace pa {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+}
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int check_dims(const pa_dims *dims)
+{
+    if (!dims)
+        return fail(PA_ERR_INVALID_ARG, "dims is NULL");
+    const pa_dims &d = *dims;
+    if (d.num_blocks < 0 || d.block_size <= 0 || d.num_heads <= 0 || d.num_kv_heads <= 0 || d.head_dim <= 0)
+        return fail(PA_ERR_INVALID_ARG, "dims must be positive (num_blocks may be 0)");
+    if (d.num_heads % d.num_kv_heads != 0)
+        return fail(PA_ERR_UNSUPPORTED, "num_heads (%d) is not a multiple of num_kv_heads (%d)", d.num_heads,
+                    d.num_kv_heads);
+    if (d.num_heads / d.num_kv_heads > kMaxGroup)
+        return fail(PA_ERR_UNSUPPORTED, "group size %d > %d", d.num_heads / d.num_kv_heads, kMaxGroup);
+    if (d.head_dim != 64 && d.head_dim != 128)
+        return fail(PA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", d.head_dim);
+    if (d.block_size < 16 || d.block_size > 1024 || (d.block_size & (d.block_size - 1)))
+        return fail(PA_ERR_UNSUPPORTED, "block_size %d is not a power of two in [16, 1024]", d.block_size);
+    if ((int64_t)d.num_blocks * d.block_size > INT32_MAX)
+        return fail(PA_ERR_UNSUPPORTED, "num_blocks*block_size exceeds int32");
+    return PA_OK;
+}
+
+static bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+} // namespace pa
+
+using namespace pa;
+
+extern "C" const char *pa_last_error_string(void) { return g_err; }
+
+extern "C" int pa_version(void) { return 0x000100; }
+
+extern "C" int pa_upload(void *dev_dst, const void *host_src, size_t bytes, pa_stream_t stream)
+{
+    if (bytes == 0)
+        return PA_OK;
+    if (!dev_dst || !host_src)
+        return fail(PA_ERR_INVALID_ARG, "pa_upload: NULL pointer");
+    cudaError_t e = cudaMemcpyAsync(dev_dst, host_src, bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "cudaMemcpyAsync: %s", cudaGetErrorString(e));
+    return PA_OK;
+}
+
+extern "C" int pa_store_kvcache(const pa_dims *dims, const void *k, const void *v, void *k_cache, void *v_cache,
+                                const int32_t *slot_mapping, int32_t num_tokens, pa_stream_t stream)
+{
+    int rc = check_dims(dims);
+    if (rc != PA_OK)
+        return rc;
+    if (num_tokens < 0)
+        return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "pa_store_kvcache: NULL pointer");
+    if (misaligned(k) || misaligned(v) || misaligned(k_cache) || misaligned(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "pa_store_kvcache: tensors must be 16-byte aligned");
+    return launch_store_kvcache(*dims, k, v, k_cache, v_cache, slot_mapping, num_tokens, stream);
+}
+
+extern "C" int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                 const int32_t *block_tables, float scale, void *out, const pa_prefill_meta *meta,
+                                 const int32_t *tiles, pa_stream_t stream)
+{
+    int rc = check_dims(dims);
+    if (rc != PA_OK)
+        return rc;
+    if (!meta)
+        return fail(PA_ERR_INVALID_ARG, "meta is NULL");
+    if (meta->num_tiles < 0 || meta->total_q < 0 || meta->num_seqs < 0 || meta->max_blocks_per_seq < 1)
+        return fail(PA_ERR_INVALID_ARG, "malformed prefill meta");
+    const int group = dims->num_heads / dims->num_kv_heads;
+    if (meta->rows_per_tile != (kPrefillRows / group > 0 ? kPrefillRows / group : 1))
+        return fail(PA_ERR_INVALID_ARG, "prefill meta was packed for other dims");
+    if (meta->num_tiles == 0 || meta->total_q == 0)
+        return PA_OK;
+    if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables || !out || !tiles)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen: NULL pointer");
+    if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen: tensors must be 16-byte aligned");
+    if (dims->num_blocks == 0)
+        return fail(PA_ERR_INVALID_ARG, "empty KV pool");
+    PrefillArgs a{};
+    a.dims = *dims;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.cu_seqlens_k = cu_seqlens_k;
+    a.block_tables = block_tables;
+    a.tiles = tiles;
+    a.out = out;
+    a.scale = scale;
+    a.num_tiles = meta->num_tiles;
+    a.total_q = meta->total_q;
+    a.max_blocks_per_seq = meta->max_blocks_per_seq;
+    a.rows_per_tile = meta->rows_per_tile;
+    return launch_prefill(a, stream);
+}
+
+extern "C" int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *context_lens, const int32_t *block_tables, float scale, void *out,
+                         const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items, void *workspace,
+                         size_t workspace_bytes, pa_stream_t stream)
+{
+    int rc = check_dims(dims);
+    if (rc != PA_OK)
+        return rc;
+    if (!meta)
+        return fail(PA_ERR_INVALID_ARG, "meta is NULL");
+    if (meta->num_items < 0 || meta->num_seqs < 0 || meta->max_blocks_per_seq < 1 || meta->max_splits < 1)
+        return fail(PA_ERR_INVALID_ARG, "malformed decode meta");
+    if (meta->num_items == 0)
+        return PA_OK;
+    if (!q || !k_cache || !v_cache || !context_lens || !block_tables || !out || !items || !seq_items)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode: NULL pointer");
+    if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode: tensors must be 16-byte aligned");
+    if (workspace_bytes < meta->workspace_bytes)
+        return fail(PA_ERR_WORKSPACE, "decode workspace has %zu bytes, needs %llu", workspace_bytes,
+                    (unsigned long long)meta->workspace_bytes);
+    if (meta->workspace_bytes > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return fail(PA_ERR_INVALID_ARG, "decode workspace must be non-NULL and 256-byte aligned");
+    DecodeArgs a{};
+    a.dims = *dims;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.context_lens = context_lens;
+    a.block_tables = block_tables;
+    a.items = items;
+    a.seq_items = seq_items;
+    a.out = out;
+    if (meta->num_partials < 0)
+        return fail(PA_ERR_INVALID_ARG, "malformed decode meta");
+    if (meta->num_partials > 0) {
+        size_t per = (size_t)dims->num_heads * dims->head_dim * 4;
+        size_t need = align_up((size_t)meta->num_partials * per, 256) +
+                      align_up((size_t)meta->num_partials * dims->num_heads * 4, 256);
+        if (need > meta->workspace_bytes)
+            return fail(PA_ERR_INVALID_ARG, "decode meta workspace size inconsistent with its partial count");
+        a.part_o = static_cast<float *>(workspace);
+        a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align_up((size_t)meta->num_partials * per, 256));
+    }
+    a.scale = scale;
+    a.num_seqs = meta->num_seqs;
+    a.num_items = meta->num_items;
+    a.max_blocks_per_seq = meta->max_blocks_per_seq;
+    a.max_splits = meta->max_splits;
+    return launch_decode(a, stream);
+}
+
+extern "C" int pa_read_device_error(uint32_t *code, pa_stream_t stream)
+{
+    if (!code)
+        return fail(PA_ERR_INVALID_ARG, "code is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    *code = 0;
+    int rc = read_store_error(code);
+    if (rc == PA_OK)
+        rc = read_prefill_error(code);
+    return rc;
+}

@@ -1,0 +1,398 @@
+// Batched single-token GQA decode over the paged KV cache, split-KV + LSE combine.
+//
+// Sources (page title, section):
+//  - "手搓 vLLM 推理引擎" (LLM-101-CN nano-vllm walkthrough), Step 4: decode
+//    attends one new query per sequence to all context_lens[b] cached keys,
+//    found through the sequence's block table.
+//  - "推理系统" (CS 与 LLM 学习知识库), "瓶颈不是算力，是带宽": decode
+//    attention does ~1 flop per byte of K/V read, so its time is the bytes
+//    read divided by the memory bandwidth.
+//  - "面试问答准备: nano-vLLM 推理引擎优化", Q3 follow-ups / summary table:
+//    Paged Attention v2 reuses each KV head for its whole query-head group and
+//    uses tensor cores; Split-K cuts a long context into segments that each
+//    emit a local max, normaliser and fp32 accumulator, merged by a second
+//    kernel with log-sum-exp.
+//
+// GB300 design.  One CTA per (work item = sequence x key range, KV head); its
+// 4 warps stream disjoint 16-token chunks of K and V for that head through a
+// 3-stage cp.async (16-byte, L2-only) pipeline into XOR-swizzled shared
+// memory.  The G query heads of the group share every K/V byte read:
+//   S^T[16 tok x 8 heads] = K[16 x D] . Q^T      (mma.sync m16n8k16, bf16)
+//   O^T[D x 8 heads]    += V^T[D x 16] . P^T      (P^T via movmatrix.trans)
+// so the per-byte arithmetic (G flops/byte at G = 7) runs on the tensor pipe
+// instead of the FP32 lanes, and the kernel stays bound by HBM.  Online
+// softmax state lives in the accumulator fragments' own threads (no shuffles
+// except one 3-step max per chunk).  The 4 warps merge through shared memory;
+// a single-split sequence writes bf16 directly, otherwise (o/l, log2-sum-exp)
+// partials go to the workspace and a combine kernel merges them.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct DecLayout {
+    static constexpr int kRowBytes = D * 2;             // one head row of one token
+    static constexpr int kChunkBytes = 16 * kRowBytes;  // 16 tokens of K (or V)
+    static constexpr int kStageBytes = 2 * kChunkBytes; // K + V
+    static constexpr int kWarpBytes = kStages * kStageBytes;
+    static constexpr int kSmemBytes = kWarps * kWarpBytes;
+    static constexpr int kVecPerRow = D / 8;            // 16-byte vectors per row
+};
+
+struct DecParams {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_cache;
+    const __nv_bfloat16 *v_cache;
+    const int32_t *block_tables;
+    const int4 *items;
+    __nv_bfloat16 *out;
+    float *part_o;
+    float *part_lse;
+    float scale_log2;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t group;
+    int32_t block_size;
+    int32_t max_blocks;
+};
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const DecParams p)
+{
+    using L = DecLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int4 item = p.items[blockIdx.x];
+    const int b = item.x, k0 = item.y, k1 = item.z, pslot = item.w;
+    const int g = blockIdx.y;
+    const int G = p.group;
+    const int Hq = p.num_heads;
+
+    // Q^T fragments: B operand (k = d, n = head) of the score MMA.
+    uint32_t qf[NT][D / 16][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hl = nt * 8 + (lane >> 2);
+        const bool valid = hl < G;
+        const uint32_t *qrow =
+            reinterpret_cast<const uint32_t *>(p.q + ((size_t)b * Hq + (size_t)g * G + (valid ? hl : 0)) * D);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qf[nt][kk][0] = valid ? __ldg(qrow + kk * 8 + (lane & 3)) : 0u;
+            qf[nt][kk][1] = valid ? __ldg(qrow + kk * 8 + 4 + (lane & 3)) : 0u;
+        }
+    }
+
+    const int nchunks = (k1 - k0 + 15) >> 4;
+    const int my_n = nchunks > warp ? (nchunks - warp + kWarps - 1) / kWarps : 0;
+    const uint32_t wbase = ptx::smem_u32(smem) + warp * L::kWarpBytes;
+    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks;
+    const int bs = p.block_size;
+    const int Hkv = p.num_kv_heads;
+    int blk_cache = 0;
+
+    auto issue = [&](int i) {
+        if ((i & 31) == 0) { // refresh the block ids of local chunks i .. i+31, one per lane
+            const int key = k0 + 16 * (warp + kWarps * (i + lane));
+            blk_cache = key < k1 ? __ldg(bt_row + key / bs) : 0;
+        }
+        const int phys = __shfl_sync(0xffffffffu, blk_cache, i & 31);
+        const int key0 = k0 + 16 * (warp + kWarps * i);
+        const int64_t row0 = (int64_t)phys * bs + (key0 & (bs - 1));
+        const uint32_t sbase = wbase + (i % kStages) * L::kStageBytes;
+#pragma unroll
+        for (int r = 0; r < L::kVecPerRow / 2; ++r) {
+            const int e = r * 32 + lane;
+            const int t = e / L::kVecPerRow;
+            const int c = e % L::kVecPerRow;
+            const bool valid = key0 + t < k1;
+            const size_t off = ((size_t)(row0 + t) * Hkv + g) * D + c * 8;
+            const uint32_t dst = sbase + t * L::kRowBytes + ((c ^ (t & 7)) << 4);
+            ptx::cp_async_16(dst, valid ? (const void *)(p.k_cache + off) : (const void *)p.k_cache, valid ? 16u : 0u);
+            ptx::cp_async_16(dst + L::kChunkBytes, valid ? (const void *)(p.v_cache + off) : (const void *)p.v_cache,
+                             valid ? 16u : 0u);
+        }
+    };
+
+    float acc[NT][D / 16][4];
+    float m_r[NT][2], l_r[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_r[nt][0] = m_r[nt][1] = -INFINITY;
+        l_r[nt][0] = l_r[nt][1] = 0.f;
+#pragma unroll
+        for (int mi = 0; mi < D / 16; ++mi)
+            acc[nt][mi][0] = acc[nt][mi][1] = acc[nt][mi][2] = acc[nt][mi][3] = 0.f;
+    }
+
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < my_n)
+            issue(s);
+        ptx::cp_async_commit();
+    }
+
+    // ldmatrix row addressing (per lane) inside a 16-token chunk
+    const int a_tok = (lane & 7) + ((lane >> 3) & 1) * 8; // K: A = K[tok][d]
+    const int a_hi = lane >> 4;
+    const int v_tok = (lane & 7) + (lane >> 4) * 8;       // V: A = V^T via .trans
+    const int v_hi = (lane >> 3) & 1;
+
+    for (int i = 0; i < my_n; ++i) {
+        __syncwarp();
+        if (i + kStages - 1 < my_n)
+            issue(i + kStages - 1);
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<kStages - 1>();
+        __syncwarp();
+
+        const uint32_t kb = wbase + (i % kStages) * L::kStageBytes;
+        const uint32_t vb = kb + L::kChunkBytes;
+        const int key0 = k0 + 16 * (warp + kWarps * i);
+
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            const int c = 2 * kk + a_hi;
+            ptx::ldmatrix_x4(kb + a_tok * L::kRowBytes + ((c ^ (a_tok & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                ptx::mma_16816(sc[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+        }
+
+        const bool v0 = key0 + (lane >> 2) < k1;
+        const bool v1 = key0 + (lane >> 2) + 8 < k1;
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float s0 = v0 ? sc[nt][0] * p.scale_log2 : -INFINITY;
+            const float s1 = v0 ? sc[nt][1] * p.scale_log2 : -INFINITY;
+            const float s2 = v1 ? sc[nt][2] * p.scale_log2 : -INFINITY;
+            const float s3 = v1 ? sc[nt][3] * p.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m_r[nt][0], mx0), mn1 = fmaxf(m_r[nt][1], mx1);
+            const float al0 = ptx::ex2(m_r[nt][0] - mn0), al1 = ptx::ex2(m_r[nt][1] - mn1);
+            m_r[nt][0] = mn0;
+            m_r[nt][1] = mn1;
+            const float p0 = ptx::ex2(s0 - mn0), p1 = ptx::ex2(s1 - mn1);
+            const float p2 = ptx::ex2(s2 - mn0), p3 = ptx::ex2(s3 - mn1);
+            l_r[nt][0] = l_r[nt][0] * al0 + p0 + p2;
+            l_r[nt][1] = l_r[nt][1] * al1 + p1 + p3;
+#pragma unroll
+            for (int mi = 0; mi < D / 16; ++mi) {
+                acc[nt][mi][0] *= al0;
+                acc[nt][mi][1] *= al1;
+                acc[nt][mi][2] *= al0;
+                acc[nt][mi][3] *= al1;
+            }
+            pb[nt][0] = ptx::movmatrix_trans(ptx::pack_bf16(p0, p1));
+            pb[nt][1] = ptx::movmatrix_trans(ptx::pack_bf16(p2, p3));
+        }
+
+#pragma unroll
+        for (int mi = 0; mi < D / 16; ++mi) {
+            uint32_t a0, a1, a2, a3;
+            const int c = 2 * mi + v_hi;
+            ptx::ldmatrix_x4_trans(vb + v_tok * L::kRowBytes + ((c ^ (v_tok & 7)) << 4), a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                ptx::mma_16816(acc[nt][mi], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+    }
+    ptx::cp_async_wait<0>();
+
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1)
+                l_r[nt][j] += __shfl_xor_sync(0xffffffffu, l_r[nt][j], o);
+
+    // merge the 4 warps through shared memory (pipeline buffers are free now)
+    __syncthreads();
+    constexpr int H8 = 8 * NT;
+    float *mrg_m = reinterpret_cast<float *>(smem);
+    float *mrg_l = mrg_m + kWarps * H8;
+    float *mrg_o = mrg_l + kWarps * H8; // [warp][head][D]
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int h0 = nt * 8 + (lane & 3) * 2;
+        if (lane < 4) {
+            mrg_m[warp * H8 + h0] = m_r[nt][0];
+            mrg_m[warp * H8 + h0 + 1] = m_r[nt][1];
+            mrg_l[warp * H8 + h0] = l_r[nt][0];
+            mrg_l[warp * H8 + h0 + 1] = l_r[nt][1];
+        }
+#pragma unroll
+        for (int mi = 0; mi < D / 16; ++mi) {
+            const int d = mi * 16 + (lane >> 2);
+            float *o0 = mrg_o + ((size_t)warp * H8 + h0) * D;
+            float *o1 = o0 + D;
+            o0[d] = acc[nt][mi][0];
+            o1[d] = acc[nt][mi][1];
+            o0[d + 8] = acc[nt][mi][2];
+            o1[d + 8] = acc[nt][mi][3];
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int hl = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            M = fmaxf(M, mrg_m[w * H8 + hl]);
+        float Lsum = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = ptx::ex2(mrg_m[w * H8 + hl] - M);
+                Lsum += f * mrg_l[w * H8 + hl];
+                O += f * mrg_o[((size_t)w * H8 + hl) * D + d];
+            }
+        }
+        const float o = Lsum > 0.f ? O / Lsum : 0.f;
+        const size_t h = (size_t)g * G + hl;
+        if (pslot < 0) {
+            p.out[((size_t)b * Hq + h) * D + d] = __float2bfloat16_rn(o);
+        } else {
+            p.part_o[((size_t)pslot * Hq + h) * D + d] = o;
+            if (d == 0)
+                p.part_lse[(size_t)pslot * Hq + h] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
+        }
+    }
+}
+
+// out[b][h] = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M), over the splits of sequence b.
+template <int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const float *__restrict__ part_o,
+                                                             const float *__restrict__ part_lse,
+                                                             const int32_t *__restrict__ seq_items,
+                                                             __nv_bfloat16 *__restrict__ out, int num_heads)
+{
+    const int b = blockIdx.x;
+    const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int s0 = seq_items[b], n = seq_items[b + 1] - s0;
+    if (n <= 1 || h >= num_heads)
+        return;
+    float M = -INFINITY;
+    for (int s = 0; s < n; ++s)
+        M = fmaxf(M, part_lse[(size_t)(s0 + s) * num_heads + h]);
+    constexpr int E = D / 32;
+    float accv[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        accv[e] = 0.f;
+    float W = 0.f;
+    for (int s = 0; s < n; ++s) {
+        const float lse = part_lse[(size_t)(s0 + s) * num_heads + h];
+        const float w = lse == -INFINITY ? 0.f : ptx::ex2(lse - M);
+        W += w;
+        const float *src = part_o + ((size_t)(s0 + s) * num_heads + h) * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            accv[e] += w * src[e];
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    __nv_bfloat16 *dst = out + ((size_t)b * num_heads + h) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        dst[e] = __float2bfloat16_rn(accv[e] * inv);
+}
+
+template <int D, int NT>
+int launch_split(const DecodeArgs &a, const DecParams &p, cudaStream_t stream)
+{
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DecLayout<D>::kSmemBytes);
+        if (e != cudaSuccess)
+            return fail(PA_ERR_CUDA, "decode smem attribute: %s", cudaGetErrorString(e));
+        configured = true;
+    }
+    dim3 grid((unsigned)a.num_items, (unsigned)a.dims.num_kv_heads);
+    decode_split_kernel<D, NT><<<grid, kWarps * 32, DecLayout<D>::kSmemBytes, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    if (a.part_o) {
+        dim3 cg((unsigned)a.num_seqs, (unsigned)((a.dims.num_heads + 3) / 4));
+        decode_combine_kernel<D><<<cg, 128, 0, stream>>>(a.part_o, a.part_lse, a.seq_items,
+                                                         static_cast<__nv_bfloat16 *>(a.out), a.dims.num_heads);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return fail(PA_ERR_CUDA, "decode combine launch: %s", cudaGetErrorString(e));
+    }
+    return PA_OK;
+}
+
+template <int D, int NT>
+int occupancy()
+{
+    int n = 0;
+    cudaFuncSetAttribute(decode_split_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         DecLayout<D>::kSmemBytes);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, NT>, kWarps * 32,
+                                                      DecLayout<D>::kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return 2;
+    }
+    return n;
+}
+
+} // namespace
+
+int launch_decode(const DecodeArgs &a, void *stream)
+{
+    DecParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.k_cache = static_cast<const __nv_bfloat16 *>(a.k_cache);
+    p.v_cache = static_cast<const __nv_bfloat16 *>(a.v_cache);
+    p.block_tables = a.block_tables;
+    p.items = reinterpret_cast<const int4 *>(a.items);
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.part_o = a.part_o;
+    p.part_lse = a.part_lse;
+    p.scale_log2 = a.scale * kLog2e;
+    p.num_heads = a.dims.num_heads;
+    p.num_kv_heads = a.dims.num_kv_heads;
+    p.group = a.dims.num_heads / a.dims.num_kv_heads;
+    p.block_size = a.dims.block_size;
+    p.max_blocks = a.max_blocks_per_seq;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool two = p.group > 8;
+    if (a.dims.head_dim == 128)
+        return two ? launch_split<128, 2>(a, p, s) : launch_split<128, 1>(a, p, s);
+    return two ? launch_split<64, 2>(a, p, s) : launch_split<64, 1>(a, p, s);
+}
+
+int decode_ctas_per_sm(int head_dim, int group)
+{
+    const bool two = group > 8;
+    if (head_dim == 128)
+        return two ? occupancy<128, 2>() : occupancy<128, 1>();
+    return two ? occupancy<64, 2>() : occupancy<64, 1>();
+}
+
+} // namespace pa

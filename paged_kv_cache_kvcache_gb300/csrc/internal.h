@@ -1,0 +1,77 @@
+// Internal declarations shared by the host-side translation units of libpagedattn.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// Key tile of the prefill kernel and query rows of one tile (tcgen05 M).
+constexpr int kPrefillKeyTile = 128;
+constexpr int kPrefillRows = 128;
+// Keys per warp step of the decode kernel and per CTA step (4 warps).
+constexpr int kDecodeChunk = 16;
+constexpr int kDecodeStep = 64;
+constexpr int kMaxGroup = 16;
+
+// Thread-local error text.
+void set_error(const char *fmt, ...);
+int fail(int code, const char *fmt, ...);
+
+// Shape checks shared by every entry point; returns PA_OK or an error code.
+int check_dims(const pa_dims *dims);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Launchers (defined in the .cu files).  Each returns PA_OK or PA_ERR_CUDA.
+int launch_store_kvcache(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,
+                         const int32_t *slot_mapping, int32_t num_tokens, void *stream);
+
+struct PrefillArgs {
+    pa_dims dims;
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *cu_seqlens_q;
+    const int32_t *cu_seqlens_k;
+    const int32_t *block_tables;
+    const int32_t *tiles;
+    void *out;
+    float scale;
+    int32_t num_tiles;
+    int32_t total_q;
+    int32_t max_blocks_per_seq;
+    int32_t rows_per_tile;
+};
+int launch_prefill(const PrefillArgs &a, void *stream);
+
+struct DecodeArgs {
+    pa_dims dims;
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *context_lens;
+    const int32_t *block_tables;
+    const int32_t *items;
+    const int32_t *seq_items;
+    void *out;
+    float *part_o;   // [num_partials][Hq][D]
+    float *part_lse; // [num_partials][Hq]
+    float scale;
+    int32_t num_seqs;
+    int32_t num_items;
+    int32_t max_blocks_per_seq;
+    int32_t max_splits;
+};
+int launch_decode(const DecodeArgs &a, void *stream);
+
+// Concurrent decode CTAs one SM holds (occupancy of the decode kernel).
+int decode_ctas_per_sm(int head_dim, int group);
+
+// Read and clear the device error words (store: bit 0, prefill waits: bit 1).
+int read_store_error(uint32_t *code);
+int read_prefill_error(uint32_t *code);
+
+} // namespace pa

@@ -1,0 +1,238 @@
+"""Thin ctypes binding of libpagedattn (include/pagedattn.h), same entry-point names.
+
+Argument marshalling only: every step of the path (metadata packing, KV
+scatter, prefill, decode) runs in the native library; torch provides device
+memory, pinned host memory and streams.  There is no fallback: if the CUDA
+library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _build
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, 1, 2, 3, 4
+
+EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
+           "pa_decode", "pa_last_error_string", "pa_read_device_error", "pa_version")
+
+
+class pa_dims(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class pa_prefill_meta(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
+                ("max_seqlen_k", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_tiles", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("off_cu_seqlens_q", ctypes.c_uint64), ("off_cu_seqlens_k", ctypes.c_uint64),
+                ("off_block_tables", ctypes.c_uint64), ("off_slot_mapping", ctypes.c_uint64),
+                ("off_tiles", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
+
+
+class pa_decode_meta(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("num_items", ctypes.c_int32), ("split_tokens", ctypes.c_int32), ("max_splits", ctypes.c_int32),
+                ("num_partials", ctypes.c_int32), ("off_context_lens", ctypes.c_uint64),
+                ("off_block_tables", ctypes.c_uint64), ("off_slot_mapping", ctypes.c_uint64),
+                ("off_items", ctypes.c_uint64), ("off_seq_items", ctypes.c_uint64),
+                ("total_bytes", ctypes.c_uint64), ("workspace_bytes", ctypes.c_uint64)]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, code: int, fn: str, msg: str):
+        super().__init__(f"{fn} failed with code {code}: {msg}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpagedattn (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            L.pa_pack_prefill.argtypes = [P, I32, P, P, P, P, P, SZ, P]
+            L.pa_pack_decode.argtypes = [P, I32, P, P, P, I32, P, SZ, P]
+            L.pa_upload.argtypes = [P, P, SZ, P]
+            L.pa_store_kvcache.argtypes = [P, P, P, P, P, P, I32, P]
+            L.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
+            L.pa_decode.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
+            L.pa_last_error_string.argtypes = []
+            L.pa_last_error_string.restype = ctypes.c_char_p
+            L.pa_read_device_error.argtypes = [P, P]
+            L.pa_version.argtypes = []
+            for name in EXPORTS:
+                if name not in ("pa_last_error_string",):
+                    getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, fn: str):
+    if rc != PA_OK:
+        raise PagedAttnError(rc, fn, pa_last_error_string())
+
+
+def pa_last_error_string() -> str:
+    return lib().pa_last_error_string().decode(errors="replace")
+
+
+def pa_version() -> int:
+    return int(lib().pa_version())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr() if t.numel() > 0 else None
+    return int(t)
+
+
+def make_dims(num_blocks: int, block_size: int, num_heads: int, num_kv_heads: int, head_dim: int) -> pa_dims:
+    return pa_dims(num_blocks, block_size, num_heads, num_kv_heads, head_dim)
+
+
+def _i32(x) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _np_ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p) if a.size else None
+
+
+def _flatten(block_lists: Sequence) -> tuple:
+    off = np.zeros(len(block_lists) + 1, dtype=np.int32)
+    for i, b in enumerate(block_lists):
+        off[i + 1] = off[i] + len(b)
+    ids = (np.concatenate([np.asarray(b, np.int32) for b in block_lists]) if len(block_lists)
+           else np.zeros(0, np.int32))
+    return off, _i32(ids)
+
+
+@dataclass
+class _Plan:
+    meta: ctypes.Structure
+    host: torch.Tensor                 # pinned uint8 image
+    dev: Optional[torch.Tensor] = None  # device copy
+
+    def upload(self, device="cuda", stream=None) -> "_Plan":
+        """One asynchronous host-to-device copy of the packed image (pa_upload)."""
+        n = int(self.meta.total_bytes)
+        if self.dev is None or self.dev.numel() < n:
+            self.dev = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        _check(lib().pa_upload(_ptr(self.dev), _ptr(self.host), n, _stream(stream)), "pa_upload")
+        return self
+
+    def dptr(self, off: int) -> int:
+        assert self.dev is not None, "upload the plan first"
+        return self.dev.data_ptr() + int(off)
+
+    def host_array(self, off: int, count: int) -> np.ndarray:
+        """Read back a packed int32 array from the host image (tests/debugging)."""
+        buf = self.host.numpy()
+        return np.frombuffer(buf, dtype=np.int32, count=count, offset=int(off)).copy()
+
+
+class PrefillPlan(_Plan):
+    @property
+    def slot_mapping(self) -> int:
+        return self.dptr(self.meta.off_slot_mapping)
+
+
+class DecodePlan(_Plan):
+    @property
+    def slot_mapping(self) -> int:
+        return self.dptr(self.meta.off_slot_mapping)
+
+
+def pa_pack_prefill(dims: pa_dims, seq_lens, query_lens, block_lists, pin: bool = True) -> PrefillPlan:
+    """Pack cu_seqlens, block tables, slot mapping and the tile list on the CPU."""
+    L = lib()
+    seq_lens, query_lens = _i32(seq_lens), _i32(query_lens)
+    off, ids = _flatten(block_lists)
+    meta = pa_prefill_meta()
+    args = (ctypes.byref(dims), len(seq_lens), _np_ptr(seq_lens), _np_ptr(query_lens), _np_ptr(off), _np_ptr(ids))
+    _check(L.pa_pack_prefill(*args, None, 0, ctypes.byref(meta)), "pa_pack_prefill")
+    host = torch.empty(max(int(meta.total_bytes), 256), dtype=torch.uint8, pin_memory=pin)
+    _check(L.pa_pack_prefill(*args, _ptr(host), host.numel(), ctypes.byref(meta)), "pa_pack_prefill")
+    return PrefillPlan(meta, host)
+
+
+def pa_pack_decode(dims: pa_dims, context_lens, block_lists, split_tokens: int = 0, pin: bool = True) -> DecodePlan:
+    """Pack context lens, block tables, slot mapping and the split plan on the CPU."""
+    L = lib()
+    ctx = _i32(context_lens)
+    off, ids = _flatten(block_lists)
+    meta = pa_decode_meta()
+    args = (ctypes.byref(dims), len(ctx), _np_ptr(ctx), _np_ptr(off), _np_ptr(ids), int(split_tokens))
+    _check(L.pa_pack_decode(*args, None, 0, ctypes.byref(meta)), "pa_pack_decode")
+    host = torch.empty(max(int(meta.total_bytes), 256), dtype=torch.uint8, pin_memory=pin)
+    _check(L.pa_pack_decode(*args, _ptr(host), host.numel(), ctypes.byref(meta)), "pa_pack_decode")
+    return DecodePlan(meta, host)
+
+
+def pa_upload(dev_dst, host_src, nbytes: int, stream=None):
+    _check(lib().pa_upload(_ptr(dev_dst), _ptr(host_src), int(nbytes), _stream(stream)), "pa_upload")
+
+
+def pa_store_kvcache(dims: pa_dims, k, v, k_cache, v_cache, slot_mapping, num_tokens: Optional[int] = None,
+                     stream=None):
+    n = int(k.shape[0]) if num_tokens is None else int(num_tokens)
+    _check(lib().pa_store_kvcache(ctypes.byref(dims), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(slot_mapping), n, _stream(stream)), "pa_store_kvcache")
+
+
+def pa_prefill_varlen(dims: pa_dims, q, k_cache, v_cache, plan: PrefillPlan, scale: float, out, stream=None):
+    m = plan.meta
+    _check(lib().pa_prefill_varlen(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                   plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
+                                   plan.dptr(m.off_block_tables), float(scale), _ptr(out), ctypes.byref(m),
+                                   plan.dptr(m.off_tiles), _stream(stream)), "pa_prefill_varlen")
+
+
+def decode_workspace(plan: DecodePlan, device="cuda") -> Optional[torch.Tensor]:
+    n = int(plan.meta.workspace_bytes)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def pa_decode(dims: pa_dims, q, k_cache, v_cache, plan: DecodePlan, scale: float, out, workspace=None,
+              stream=None):
+    m = plan.meta
+    ws_bytes = int(workspace.numel()) if isinstance(workspace, torch.Tensor) else 0
+    _check(lib().pa_decode(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                           plan.dptr(m.off_context_lens), plan.dptr(m.off_block_tables), float(scale), _ptr(out),
+                           ctypes.byref(m), plan.dptr(m.off_items), plan.dptr(m.off_seq_items), _ptr(workspace),
+                           ws_bytes, _stream(stream)), "pa_decode")
+
+
+def pa_read_device_error(stream=None) -> int:
+    code = ctypes.c_uint32(0)
+    _check(lib().pa_read_device_error(ctypes.byref(code), _stream(stream)), "pa_read_device_error")
+    return int(code.value)

@@ -1,0 +1,174 @@
+"""CPU tests of the C ABI: the library loads, exports every declared entry point,
+rejects bad arguments on the host, and packs metadata exactly as the oracle's
+own definition does (integer work: bit-exact)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_cache_kvcache_gb300 import pagedattn as pa
+from paged_kv_cache_kvcache_gb300 import workloads
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pagedattn.h")
+
+
+def test_library_exports_every_declared_symbol():
+    text = open(HEADER).read()
+    declared = set(re.findall(r"^(?:int|const char \*)\s*(pa_\w+)\s*\(", text, flags=re.M))
+    assert {"pa_store_kvcache", "pa_prefill_varlen", "pa_decode"} <= declared
+    lib = pa.lib()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(pa.EXPORTS) == declared
+    assert pa.pa_version() == 0x000100
+
+
+def test_struct_sizes_match_header_layout():
+    assert ctypes.sizeof(pa.pa_dims) == 20
+    assert ctypes.sizeof(pa.pa_prefill_meta) == 8 * 4 + 6 * 8
+    assert ctypes.sizeof(pa.pa_decode_meta) == 6 * 4 + 7 * 8
+
+
+@pytest.mark.parametrize("d,code", [((4, 16, 8, 3, 128), pa.PA_ERR_UNSUPPORTED),   # Hq % Hkv
+                                    ((4, 16, 8, 2, 96), pa.PA_ERR_UNSUPPORTED),    # head_dim
+                                    ((4, 24, 8, 2, 128), pa.PA_ERR_UNSUPPORTED),   # block_size not 2^k
+                                    ((4, 8, 8, 2, 128), pa.PA_ERR_UNSUPPORTED),    # block_size < 16
+                                    ((4, 16, 34, 2, 128), pa.PA_ERR_UNSUPPORTED),  # group 17 > 16
+                                    ((4, 16, 0, 1, 128), pa.PA_ERR_INVALID_ARG)])
+def test_dims_validation(d, code):
+    dims = pa.make_dims(*d)
+    meta = pa.pa_prefill_meta()
+    rc = pa.lib().pa_pack_prefill(ctypes.byref(dims), 0, None, None, None, None, None, 0, ctypes.byref(meta))
+    assert rc == code
+    rc = pa.lib().pa_store_kvcache(ctypes.byref(dims), None, None, None, None, None, 1, None)
+    assert rc == code
+
+
+def test_device_calls_reject_bad_args_without_touching_the_gpu():
+    dims = pa.make_dims(4, 16, 4, 2, 64)
+    L = pa.lib()
+    assert L.pa_store_kvcache(ctypes.byref(dims), None, None, None, None, None, 3, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_store_kvcache(ctypes.byref(dims), None, None, None, None, None, -1, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_store_kvcache(ctypes.byref(dims), None, None, None, None, None, 0, None) == pa.PA_OK
+    assert L.pa_store_kvcache(ctypes.byref(dims), 8, 16, 32, 48, 64, 1, None) == pa.PA_ERR_INVALID_ARG  # misaligned
+    meta = pa.pa_prefill_meta()
+    meta.num_tiles, meta.total_q, meta.num_seqs, meta.max_blocks_per_seq, meta.rows_per_tile = 1, 1, 1, 1, 64
+    assert L.pa_prefill_varlen(ctypes.byref(dims), None, None, None, None, None, None, ctypes.c_float(0.1),
+                               None, ctypes.byref(meta), None, None) == pa.PA_ERR_INVALID_ARG
+    meta.rows_per_tile = 7  # packed for other dims
+    assert L.pa_prefill_varlen(ctypes.byref(dims), 16, 16, 16, 16, 16, 16, ctypes.c_float(0.1), 16,
+                               ctypes.byref(meta), 16, None) == pa.PA_ERR_INVALID_ARG
+    dm = pa.pa_decode_meta()
+    dm.num_items, dm.num_seqs, dm.max_blocks_per_seq, dm.max_splits = 1, 1, 1, 1
+    dm.workspace_bytes = 1024
+    assert L.pa_decode(ctypes.byref(dims), 16, 16, 16, 16, 16, ctypes.c_float(0.1), 16, ctypes.byref(dm), 16, 16,
+                       None, 0, None) == pa.PA_ERR_WORKSPACE
+    assert "workspace" in pa.pa_last_error_string()
+
+
+def test_pack_rejects_malformed_sequences():
+    dims = pa.make_dims(8, 16, 4, 2, 64)
+    with pytest.raises(pa.PagedAttnError) as e:  # query longer than the sequence
+        pa.pa_pack_prefill(dims, [10], [11], [[0]], pin=False)
+    assert e.value.code == pa.PA_ERR_INVALID_ARG
+    with pytest.raises(pa.PagedAttnError):  # too few blocks
+        pa.pa_pack_prefill(dims, [33], [33], [[0, 1]], pin=False)
+    with pytest.raises(pa.PagedAttnError):  # block id outside the pool
+        pa.pa_pack_prefill(dims, [5], [5], [[8]], pin=False)
+    with pytest.raises(pa.PagedAttnError):
+        pa.pa_pack_decode(dims, [-1], [[0]], pin=False)
+    with pytest.raises(pa.PagedAttnError):  # split not a multiple of 64
+        pa.pa_pack_decode(dims, [5], [[0]], split_tokens=100, pin=False)
+
+
+def _prefill_arrays(plan, b):
+    m = plan.meta
+    return (plan.host_array(m.off_cu_seqlens_q, b + 1), plan.host_array(m.off_cu_seqlens_k, b + 1),
+            plan.host_array(m.off_block_tables, b * m.max_blocks_per_seq).reshape(b, m.max_blocks_per_seq),
+            plan.host_array(m.off_slot_mapping, m.total_q), plan.host_array(m.off_tiles, 4 * m.num_tiles).reshape(-1, 4))
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_prefix", "qwen3_chunked", "qwen3_prefill_128"])
+def test_pack_prefill_matches_definitions(name):
+    w = workloads.make(name)
+    p = w.pool
+    for batch in w.batches:
+        if batch.kind != "prefill":
+            continue
+        dims = pa.make_dims(p.num_blocks, p.block_size, batch.num_heads, p.num_kv_heads, p.head_dim)
+        plan = pa.pa_pack_prefill(dims, batch.seq_lens, batch.query_lens, batch.block_lists, pin=False)
+        B = batch.num_seqs
+        cu_q, cu_k, bt, slots, tiles = _prefill_arrays(plan, B)
+        assert cu_q.tolist() == [0] + np.cumsum(batch.query_lens).tolist()
+        assert cu_k.tolist() == [0] + np.cumsum(batch.seq_lens).tolist()
+        # slots: bit-exact against the oracle's own slot mapping
+        want = oracle.slot_mapping(batch.seq_lens, batch.query_lens, batch.block_lists, p.block_size)
+        assert np.array_equal(slots, want)
+        for b in range(B):
+            n = -(-int(batch.seq_lens[b]) // p.block_size)
+            assert bt[b, :n].tolist() == batch.block_lists[b][:n].tolist()
+            assert (bt[b, n:] == -1).all()
+        # tiles: each (seq, query row, kv head) exactly once, longest first
+        G = batch.num_heads // p.num_kv_heads
+        P = plan.meta.rows_per_tile
+        assert P == 128 // G
+        cover = {}
+        for s, q0, g, nkt in tiles.tolist():
+            lq, lk = int(batch.query_lens[s]), int(batch.seq_lens[s])
+            last = min(q0 + P, lq) - 1
+            assert nkt == -(-(lk - lq + last + 1) // 128)
+            for i in range(q0, last + 1):
+                cover[(s, i, g)] = cover.get((s, i, g), 0) + 1
+        assert len(cover) == int(batch.query_lens.sum()) * p.num_kv_heads
+        assert set(cover.values()) == {1}
+        assert (np.diff(tiles[:, 3]) <= 0).all()
+
+
+@pytest.mark.parametrize("split", [0, 64, 256, 1024])
+def test_pack_decode_split_plan(split):
+    w = workloads.qwen3_decode(num_seqs=32)
+    p, batch = w.pool, w.batches[0]
+    dims = pa.make_dims(p.num_blocks, p.block_size, batch.num_heads, p.num_kv_heads, p.head_dim)
+    plan = pa.pa_pack_decode(dims, batch.seq_lens, batch.block_lists, split_tokens=split, pin=False)
+    m = plan.meta
+    B = batch.num_seqs
+    slots = plan.host_array(m.off_slot_mapping, B)
+    want = oracle.slot_mapping(batch.seq_lens, batch.query_lens, batch.block_lists, p.block_size)
+    assert np.array_equal(slots, want)
+    assert np.array_equal(plan.host_array(m.off_context_lens, B), batch.seq_lens)
+    items = plan.host_array(m.off_items, 4 * m.num_items).reshape(-1, 4)
+    seq_items = plan.host_array(m.off_seq_items, B + 1)
+    ranges = {}
+    for s, k0, k1, slot in items.tolist():
+        assert k0 % 64 == 0 and k1 > k0
+        ranges.setdefault(s, []).append((k0, k1, slot))
+    used = []
+    for b in range(B):
+        r = sorted(ranges[b])
+        assert r[0][0] == 0 and r[-1][1] == batch.seq_lens[b]
+        assert all(r[i][1] == r[i + 1][0] for i in range(len(r) - 1))
+        n = seq_items[b + 1] - seq_items[b]
+        if len(r) == 1:
+            assert n == 0 and r[0][2] == -1
+        else:
+            assert n == len(r)
+            assert sorted(x[2] for x in r) == list(range(seq_items[b], seq_items[b + 1]))
+            used += [x[2] for x in r]
+    assert m.num_partials == seq_items[-1] == len(used)
+    assert m.workspace_bytes >= m.num_partials * batch.num_heads * (p.head_dim + 1) * 4
+    lens = items[:, 2] - items[:, 1]
+    assert (np.diff(lens) <= 0).all()
+    if split:
+        assert m.split_tokens == split
+        assert lens.max() <= split
+
+
+def test_pack_decode_zero_context_is_an_empty_item():
+    dims = pa.make_dims(8, 16, 4, 2, 64)
+    plan = pa.pa_pack_decode(dims, [0, 20], [[], [3, 4]], split_tokens=64, pin=False)
+    items = plan.host_array(plan.meta.off_items, 4 * plan.meta.num_items).reshape(-1, 4).tolist()
+    assert [0, 0, 0, -1] in items
+    assert plan.host_array(plan.meta.off_slot_mapping, 2).tolist() == [-1, 4 * 16 + 3]
