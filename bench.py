@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache attention hot path on one GB300.
+
+One step = the whole path over one batch of seeded synthetic input:
+  1. host metadata packing (pa_pack_prefill / pa_pack_decode) + one upload each,
+  2. KV scatter of the 4 x 4096 prompt tokens + causal varlen prefill,
+  3. KV scatter of the 64 decode tokens + split-KV decode + LSE combine,
+on the long-context Qwen2.5-7B attention shapes (28 q / 4 KV heads, head_dim
+128, block 16): prefill 4 x 4096, decode 64 sequences at context 32768 through
+fully permuted block tables.  Inputs are resident in HBM when timing starts;
+the decode phase streams 4.3 GB of K/V per step, more than the 129 MB L2, so
+every step starts with a cold L2.
+
+Prints ONE JSON line.  value = prefill attention TFLOP/s (causal FLOPs
+4*D*Hq*pairs over the prefill phase's device time); the decode KV-read GB/s
+sits beside it under "decode".  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOP/s & decode KV-read GB/s (% of GB300 roofline), 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["qwen25", "qwen3"], default="qwen25")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--phase", choices=["both", "prefill", "decode"], default="both",
+                    help="run only one phase (small profiling cases); the JSON line needs both")
+    ap.add_argument("--decode-seqs", type=int, default=64, help="decode batch (64 = the full workload)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- workload
+
+
+def make_workload(name, device, decode_seqs=64):
+    from paged_kv_cache_kvcache_gb300 import workloads
+    if name == "qwen25":
+        return workloads.make("qwen25_prefill", device), workloads.qwen25_decode(device, num_seqs=decode_seqs), \
+            f"qwen25_long: prefill 4x4096 + decode {decode_seqs}x32768, Hq 28 / Hkv 4, D 128, block 16, permuted pools"
+    return workloads.make("qwen3_prefill_256", device), workloads.make("qwen3_decode", device), \
+        "qwen3: prefill 8x256 + decode 256 x ctx(in+out, in/out~U{100..1024}), Hq 16 / Hkv 8, D 128, block 256"
+
+
+def prefill_flops(batch) -> float:
+    lk = batch.seq_lens.astype(np.int64)
+    lq = batch.query_lens.astype(np.int64)
+    pairs = int(np.sum(lq * (lk - lq) + lq * (lq + 1) // 2))
+    return 4.0 * batch.q.shape[2] * batch.num_heads * pairs
+
+
+def decode_bytes(batch, pool) -> float:
+    ctx = batch.seq_lens.astype(np.int64)
+    kv = float(np.sum(ctx)) * pool.num_kv_heads * pool.head_dim * 2 * 2
+    qo = 2.0 * batch.q.numel() * 2
+    tables = float(np.sum(-(-ctx // pool.block_size))) * 4 + ctx.size * 4
+    return kv + qo + tables
+
+
+def store_bytes(batch) -> float:
+    return 2.0 * 2 * batch.k.numel() * 2  # K and V, read + write
+
+
+class Step:
+    """Device-resident state of one replica and the calls of one step."""
+
+    def __init__(self, wp, wd, stream):
+        from paged_kv_cache_kvcache_gb300 import pagedattn as pa
+        self.pa = pa
+        self.s = stream
+        self.wp, self.wd = wp, wd
+        self.bp, self.bd = wp.batches[0], wd.batches[0]
+        pp, pd = wp.pool, wd.pool
+        self.dims_p = pa.make_dims(pp.num_blocks, pp.block_size, self.bp.num_heads, pp.num_kv_heads, pp.head_dim)
+        self.dims_d = pa.make_dims(pd.num_blocks, pd.block_size, self.bd.num_heads, pd.num_kv_heads, pd.head_dim)
+        self.kc_p, self.vc_p = pp.k_cache, pp.v_cache
+        self.kc_d, self.vc_d = pd.k_cache, pd.v_cache
+        self.blocks_p = pa._flatten(self.bp.block_lists)
+        self.blocks_d = pa._flatten(self.bd.block_lists)
+        self.out_p = torch.empty_like(self.bp.q)
+        self.out_d = torch.empty_like(self.bd.q)
+        # double-buffered pinned metadata images (no write-after-read hazard with in-flight copies)
+        self.plans_p = [pa.pa_pack_prefill(self.dims_p, self.bp.seq_lens, self.bp.query_lens, self.blocks_p)
+                        .upload(stream=stream) for _ in range(2)]
+        self.plans_d = [pa.pa_pack_decode(self.dims_d, self.bd.seq_lens, self.blocks_d).upload(stream=stream)
+                        for _ in range(2)]
+        self.up_ev = [torch.cuda.Event(), torch.cuda.Event()]
+        for e in self.up_ev:
+            e.record(stream)
+        self.ws = pa.decode_workspace(self.plans_d[0])
+        self.i = 0
+        self.launches_per_step = 4 + (1 if self.plans_d[0].meta.num_partials > 0 else 0)
+
+    def run(self, ev=None, host=None, phase="both"):
+        """Enqueue one step; ev = dict of event pairs for per-phase timing; host = e2e buffers."""
+        pa, s = self.pa, self.s
+        k = self.i & 1
+        self.i += 1
+        self.up_ev[k].synchronize()
+        rec = (lambda name: ev[name].record(s)) if ev is not None else (lambda name: None)
+        # ---- prefill phase
+        rec("p0")
+        if phase == "decode":
+            for n in ("pk0", "pk1", "p1"):
+                rec(n)
+            return self._decode(ev, host, k, rec)
+        if host is not None:
+            self.bp.q.copy_(host["pq"], non_blocking=True)
+            self.bp.k.copy_(host["pk"], non_blocking=True)
+            self.bp.v.copy_(host["pv"], non_blocking=True)
+        plan_p = pa.pa_pack_prefill(self.dims_p, self.bp.seq_lens, self.bp.query_lens, self.blocks_p,
+                                    into=self.plans_p[k]).upload(stream=s)
+        pa.pa_store_kvcache(self.dims_p, self.bp.k, self.bp.v, self.kc_p, self.vc_p, plan_p.slot_mapping,
+                            self.bp.num_tokens, stream=s)
+        rec("pk0")
+        pa.pa_prefill_varlen(self.dims_p, self.bp.q, self.kc_p, self.vc_p, plan_p, self.bp.scale, self.out_p,
+                             stream=s)
+        rec("pk1")
+        if host is not None:
+            host["po"].copy_(self.out_p, non_blocking=True)
+        rec("p1")
+        if phase == "prefill":
+            for n in ("dk0", "dk1", "d1"):
+                rec(n)
+            return
+        self._decode(ev, host, k, rec)
+
+    def _decode(self, ev, host, k, rec):
+        pa, s = self.pa, self.s
+        # ---- decode phase
+        if host is not None:
+            self.bd.q.copy_(host["dq"], non_blocking=True)
+            self.bd.k.copy_(host["dk"], non_blocking=True)
+            self.bd.v.copy_(host["dv"], non_blocking=True)
+        plan_d = pa.pa_pack_decode(self.dims_d, self.bd.seq_lens, self.blocks_d, into=self.plans_d[k]).upload(stream=s)
+        self.up_ev[k].record(s)
+        pa.pa_store_kvcache(self.dims_d, self.bd.k, self.bd.v, self.kc_d, self.vc_d, plan_d.slot_mapping,
+                            self.bd.num_tokens, stream=s)
+        rec("dk0")
+        pa.pa_decode(self.dims_d, self.bd.q, self.kc_d, self.vc_d, plan_d, self.bd.scale, self.out_d, self.ws,
+                     stream=s)
+        rec("dk1")
+        if host is not None:
+            host["do"].copy_(self.out_d, non_blocking=True)
+        rec("d1")
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, enabled=True):
+        self.proc = None
+        self.index = index
+        if not enabled:
+            return
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0=None, t1=None):
+        """Summarise samples taken in the wall-clock window [t0, t1] (widened to 0.5 s if it holds none)."""
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.flush()
+        rows = [l.split(",") for l in open(self.f.name).read().strip().splitlines() if l.strip()]
+        os.unlink(self.f.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        parsed = []
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + r[0].split(".")[1]) if "." in r[0] else 0.0
+                parsed.append((ts, float(r[2]), float(r[3]), r[6:10]))
+            except (ValueError, IndexError):
+                continue
+        if not parsed:
+            return None
+        window = "timed region"
+        sel = [x for x in parsed if t0 is None or (t0 <= x[0] <= t1)]
+        if not sel:
+            window = "timed region +/- 0.5 s"
+            sel = [x for x in parsed if t0 - 0.5 <= x[0] <= t1 + 0.5] or parsed
+        reasons = set()
+        for x in sel:
+            for n, v in zip(names, x[3]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm = [x[1] for x in sel]
+        mx = sel[-1][2]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "window": window}
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+
+def oracle_prefill_sample(wp, row_stride, threads=0):
+    """Oracle on every row_stride-th query row of the prefill batch; returns (seconds, flops)."""
+    import oracle
+    b = wp.batches[0]
+    sel = np.zeros(b.num_tokens, dtype=bool)
+    sel[::row_stride] = True
+    kb = wp.pool.k_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    vb = wp.pool.v_cache.cpu().contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    t0 = time.perf_counter()
+    _, pairs = oracle.run_batch(kb, vb, b, wp.pool.block_size, row_select=sel, num_threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, 4.0 * b.q.shape[2] * pairs
+
+
+def oracle_decode_sample(wd, nseq, threads=0):
+    """Oracle decode on the first nseq sequences; returns (seconds, KV bytes read by the method)."""
+    import oracle
+    from paged_kv_cache_kvcache_gb300 import workloads
+    b = wd.batches[0]
+    seqs = list(range(nseq))
+    used = np.unique(np.concatenate([b.block_lists[i] for i in seqs]))
+    remap = {int(p): i for i, p in enumerate(used)}
+    idx = torch.from_numpy(used.astype(np.int64)).to(wd.pool.k_cache.device)
+    kb = wd.pool.k_cache.index_select(0, idx).cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    vb = wd.pool.v_cache.index_select(0, idx).cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    sub = workloads.Batch("decode", b.seq_lens[seqs], b.query_lens[seqs],
+                          [np.array([remap[int(p)] for p in b.block_lists[i]], np.int32) for i in seqs],
+                          b.q[seqs].cpu(), b.k[seqs].cpu(), b.v[seqs].cpu(), b.num_heads, b.scale)
+    t0 = time.perf_counter()
+    oracle.run_batch(kb, vb, sub, wd.pool.block_size, num_threads=threads)
+    dt = time.perf_counter() - t0
+    kv = float(np.sum(sub.seq_lens.astype(np.int64))) * wd.pool.num_kv_heads * wd.pool.head_dim * 4
+    return dt, kv
+
+
+# ---------------------------------------------------------------- main
+
+
+def main():
+    args = parse()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    peaks, peak_src = load_peaks()
+    wp, wd, wl_desc = make_workload(args.workload, f"cuda:{local}", args.decode_seqs)
+    stream = torch.cuda.Stream()
+    clocks = Clocks(local, enabled=not args.no_clocks)
+    with torch.cuda.stream(stream):
+        step = Step(wp, wd, stream)
+        names = ["p0", "pk0", "pk1", "p1", "dk0", "dk1", "d1"]
+        for _ in range(args.warmup):
+            step.run(phase=args.phase)
+        stream.synchronize()
+        evs = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(args.steps)]
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        w0 = time.time()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step.run(evs[i], phase=args.phase)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        w1 = time.time()
+        if world > 1:
+            torch.distributed.barrier()
+        clk = clocks.stop(w0, w1)
+        total_ms = t_start.elapsed_time(t_end)
+        if world > 1:
+            t = torch.tensor([total_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            total_ms = float(t.item())
+        ph = lambda a, b: [e[a].elapsed_time(e[b]) for e in evs]
+        t_prefill_phase = statistics.mean(ph("p0", "p1"))
+        t_prefill_kernel = statistics.mean(ph("pk0", "pk1"))
+        t_decode_phase = statistics.mean(ph("p1", "d1"))
+        t_decode_kernel = statistics.mean(ph("dk0", "dk1"))
+
+        # e2e: the same step through the public API with host (pinned) inputs/outputs
+        e2e = None
+        if not args.no_e2e and args.phase == "both":
+            host = {"pq": step.bp.q.cpu().pin_memory(), "pk": step.bp.k.cpu().pin_memory(),
+                    "pv": step.bp.v.cpu().pin_memory(), "dq": step.bd.q.cpu().pin_memory(),
+                    "dk": step.bd.k.cpu().pin_memory(), "dv": step.bd.v.cpu().pin_memory(),
+                    "po": torch.empty_like(step.out_p, device="cpu").pin_memory(),
+                    "do": torch.empty_like(step.out_d, device="cpu").pin_memory()}
+            for _ in range(args.warmup):
+                step.run(host=host)
+            stream.synchronize()
+            evs2 = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(args.steps)]
+            for i in range(args.steps):
+                step.run(evs2[i], host=host)
+            torch.cuda.synchronize()
+            e2e_p = statistics.mean([e["p0"].elapsed_time(e["p1"]) for e in evs2])
+            e2e_d = statistics.mean([e["p1"].elapsed_time(e["d1"]) for e in evs2])
+            meta_bytes = int(step.plans_p[0].meta.total_bytes + step.plans_d[0].meta.total_bytes)
+            h2d = sum(int(host[k].numel() * host[k].element_size()) for k in ("pq", "pk", "pv", "dq", "dk", "dv"))
+            d2h = sum(int(host[k].numel() * host[k].element_size()) for k in ("po", "do"))
+            e2e = {"value": round(prefill_flops(step.bp) / (e2e_p * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": h2d + meta_bytes, "d2h_bytes_per_step": d2h,
+                   "decode": {"value": round(decode_bytes(step.bd, wd.pool) / (e2e_d * 1e-3) / 1e9 * world, 1),
+                              "unit": "GB/s"},
+                   "ms_per_step": round(e2e_p + e2e_d, 4)}
+
+    flops = prefill_flops(step.bp)
+    dbytes = decode_bytes(step.bd, wd.pool)
+    eps = 1e-9  # a phase left out with --phase times as ~0
+    value = flops / (max(t_prefill_phase, eps) * 1e-3) / 1e12 * world
+    decode_gbs = dbytes / (max(t_decode_phase, eps) * 1e-3) / 1e9 * world
+    pk_tflops = flops / (max(t_prefill_kernel, eps) * 1e-3) / 1e12
+    dk_gbs = dbytes / (max(t_decode_kernel, eps) * 1e-3) / 1e9
+    t_decode_phase = max(t_decode_phase, eps)
+    t_prefill_phase = max(t_prefill_phase, eps)
+    bf16_peak = float(peaks["bf16_tflops"])
+    hbm_peak = float(peaks["hbm_gbs"])
+    roof_p = {"kernel": "pa_prefill_varlen (prefill_kernel<128>)", "bound": "tensor", "achieved": round(pk_tflops, 2),
+              "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(pk_tflops / bf16_peak, 4),
+              "peak_source": f"{peak_src} bf16_tflops (burst)", "traffic": None,
+              "work_per_launch": flops, "ms_per_launch": round(t_prefill_kernel, 5)}
+    roof_d = {"kernel": "pa_decode (decode_split_kernel<128,1> + decode_combine_kernel<128>)", "bound": "hbm",
+              "achieved": round(dk_gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(dk_gbs / hbm_peak, 4),
+              "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
+              "work_per_launch": dbytes, "ms_per_launch": round(t_decode_kernel, 5)}
+    dominant = roof_p if t_prefill_kernel >= t_decode_kernel else roof_d
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1 and args.phase == "both":
+        import oracle
+        dt_p, fl = oracle_prefill_sample(wp, row_stride=1)
+        dt_d, kvb = oracle_decode_sample(wd, nseq=16)
+        cpu = {"value": round(fl / dt_p / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"prefill: the whole 4x4096 batch ({fl / 1e9:.1f} GFLOP, {dt_p:.1f} s); "
+                         f"decode: 16 of 64 sequences ({kvb / 1e9:.2f} GB K/V, {dt_d:.1f} s)",
+               "decode": {"value": round(kvb / dt_d / 1e9, 3), "unit": "GB/s"}}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl_desc, "l2": "inputs larger than L2: the decode phase streams "
+                   f"{dbytes / 1e9:.2f} GB per step", "prefill_gflop": round(flops / 1e9, 2),
+                   "decode_kv_gb": round(dbytes / 1e9, 3), "parallelism": f"replicas x{world}"},
+        "decode": {"value": round(decode_gbs, 1), "unit": "GB/s", "frac_of_hbm": round(decode_gbs / hbm_peak, 4),
+                   "seqs_per_s": round(step.bd.num_seqs / (t_decode_phase * 1e-3) * world, 1)},
+        "prefill": {"tokens_per_s": round(step.bp.num_tokens / (t_prefill_phase * 1e-3) * world, 1),
+                    "frac_of_bf16": round(value / world / bf16_peak, 4)},
+        "phase_ms": {"prefill_phase": round(t_prefill_phase, 5), "prefill_kernel": round(t_prefill_kernel, 5),
+                     "decode_phase": round(t_decode_phase, 5), "decode_kernels": round(t_decode_kernel, 5)},
+        "roofline": dominant, "rooflines": [roof_p, roof_d],
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clk, "peaks": peak_src,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def reference_arm(args, rank, world):
+    """The CPU oracle, as it stands, timed on the host cores on bounded samples of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    wp, wd, wl_desc = make_workload(args.workload, device, args.decode_seqs)
+    # size each step's sample so that the whole --warmup + --steps run takes about 90 s
+    budget = max(0.05, 90.0 / (args.warmup + args.steps))
+    t_cal, _ = oracle_prefill_sample(wp, row_stride=1024)
+    stride = int(min(16384, max(16, 1024 * t_cal / (0.7 * budget))))
+    t_dec, _ = oracle_decode_sample(wd, nseq=1)
+    dec_every = max(1, int(round(t_dec / (0.3 * budget))))
+    sp, sd = [], []
+    for i in range(args.warmup + args.steps):
+        dt_p, fl = oracle_prefill_sample(wp, row_stride=stride)
+        dt_d, kvb = oracle_decode_sample(wd, nseq=1) if i % dec_every == 0 else (0.0, 0.0)
+        if i >= args.warmup:
+            sp.append((dt_p, fl))
+            if kvb:
+                sd.append((dt_d, kvb))
+    if not sd:
+        sd.append(oracle_decode_sample(wd, nseq=1))
+    tp = sum(x[0] for x in sp)
+    value = sum(x[1] for x in sp) / tp / 1e12
+    td = sum(x[0] for x in sd)
+    dec = sum(x[1] for x in sd) / td / 1e9
+    cores = oracle.max_threads()
+    sample = (f"per step: every {stride}th query row of the 4x4096 prefill batch; 1 of the 64 decode sequences "
+              f"every {dec_every} step(s) ({wl_desc})")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round((tp + td) / len(sp) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl_desc, "parallelism": "cpu oracle"},
+            "decode": {"value": round(dec, 3), "unit": "GB/s"},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

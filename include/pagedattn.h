@@ -169,6 +169,7 @@ int pa_store_kvcache(const pa_dims *dims, const void *k, const void *v, void *k_
  *   cu_seqlens_q, cu_seqlens_k, block_tables, tiles: device copies of the
  *            arrays pa_pack_prefill wrote (dev + meta->off_*)
  * bf16 in, fp32 accumulation and softmax, bf16 out (round to nearest even).
+ * scale must be finite and > 0 (PA_ERR_INVALID_ARG otherwise).
  */
 int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache,
                       const void *v_cache, const int32_t *cu_seqlens_q,
@@ -189,6 +190,7 @@ int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache,
  *   q, out:     device bf16 [num_seqs][num_heads][head_dim]
  *   workspace:  device memory of at least meta->workspace_bytes (may be NULL
  *               when that is 0), 256-byte aligned
+ * scale must be finite and > 0 (PA_ERR_INVALID_ARG otherwise).
  */
 int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
               const int32_t *context_lens, const int32_t *block_tables, float scale, void *out,

@@ -1,6 +1,7 @@
 // C ABI of libpagedattn: argument validation on the host, then kernel launches.
 // No entry point allocates, synchronises or reads device memory on the host
 // (except pa_read_device_error, a debugging aid).
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -102,6 +103,8 @@ extern "C" int pa_prefill_varlen(const pa_dims *dims, const void *q, const void 
         return fail(PA_ERR_INVALID_ARG, "meta is NULL");
     if (meta->num_tiles < 0 || meta->total_q < 0 || meta->num_seqs < 0 || meta->max_blocks_per_seq < 1)
         return fail(PA_ERR_INVALID_ARG, "malformed prefill meta");
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(PA_ERR_INVALID_ARG, "scale must be finite and > 0");
     const int group = dims->num_heads / dims->num_kv_heads;
     if (meta->rows_per_tile != (kPrefillRows / group > 0 ? kPrefillRows / group : 1))
         return fail(PA_ERR_INVALID_ARG, "prefill meta was packed for other dims");
@@ -143,6 +146,8 @@ extern "C" int pa_decode(const pa_dims *dims, const void *q, const void *k_cache
         return fail(PA_ERR_INVALID_ARG, "meta is NULL");
     if (meta->num_items < 0 || meta->num_seqs < 0 || meta->max_blocks_per_seq < 1 || meta->max_splits < 1)
         return fail(PA_ERR_INVALID_ARG, "malformed decode meta");
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(PA_ERR_INVALID_ARG, "scale must be finite and > 0");
     if (meta->num_items == 0)
         return PA_OK;
     if (!q || !k_cache || !v_cache || !context_lens || !block_tables || !out || !items || !seq_items)

@@ -127,7 +127,10 @@ def _np_ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p) if a.size else None
 
 
-def _flatten(block_lists: Sequence) -> tuple:
+def _flatten(block_lists) -> tuple:
+    """Per-sequence block lists -> (offsets [B+1], flat ids); an (offsets, ids) pair passes through."""
+    if isinstance(block_lists, tuple) and len(block_lists) == 2 and isinstance(block_lists[0], np.ndarray):
+        return block_lists
     off = np.zeros(len(block_lists) + 1, dtype=np.int32)
     for i, b in enumerate(block_lists):
         off[i + 1] = off[i] + len(b)
@@ -172,30 +175,43 @@ class DecodePlan(_Plan):
         return self.dptr(self.meta.off_slot_mapping)
 
 
-def pa_pack_prefill(dims: pa_dims, seq_lens, query_lens, block_lists, pin: bool = True) -> PrefillPlan:
-    """Pack cu_seqlens, block tables, slot mapping and the tile list on the CPU."""
-    L = lib()
+def _pack(fn_name, meta, args, into, pin, cls):
+    fn = getattr(lib(), fn_name)
+    host = into.host if into is not None else None
+    if host is None:
+        _check(fn(*args, None, 0, ctypes.byref(meta)), fn_name)
+        host = torch.empty(max(int(meta.total_bytes), 256), dtype=torch.uint8, pin_memory=pin)
+    rc = fn(*args, _ptr(host), host.numel(), ctypes.byref(meta))
+    if rc == PA_ERR_WORKSPACE:  # reused buffer too small: grow it
+        host = torch.empty(int(meta.total_bytes), dtype=torch.uint8, pin_memory=pin)
+        rc = fn(*args, _ptr(host), host.numel(), ctypes.byref(meta))
+    _check(rc, fn_name)
+    if into is not None:
+        into.meta, into.host = meta, host
+        return into
+    return cls(meta, host)
+
+
+def pa_pack_prefill(dims: pa_dims, seq_lens, query_lens, block_lists, pin: bool = True,
+                    into: Optional["PrefillPlan"] = None) -> "PrefillPlan":
+    """Pack cu_seqlens, block tables, slot mapping and the tile list on the CPU.
+
+    ``into`` reuses an earlier plan's pinned buffer (the caller must make sure
+    no copy from it is still in flight).
+    """
     seq_lens, query_lens = _i32(seq_lens), _i32(query_lens)
     off, ids = _flatten(block_lists)
-    meta = pa_prefill_meta()
     args = (ctypes.byref(dims), len(seq_lens), _np_ptr(seq_lens), _np_ptr(query_lens), _np_ptr(off), _np_ptr(ids))
-    _check(L.pa_pack_prefill(*args, None, 0, ctypes.byref(meta)), "pa_pack_prefill")
-    host = torch.empty(max(int(meta.total_bytes), 256), dtype=torch.uint8, pin_memory=pin)
-    _check(L.pa_pack_prefill(*args, _ptr(host), host.numel(), ctypes.byref(meta)), "pa_pack_prefill")
-    return PrefillPlan(meta, host)
+    return _pack("pa_pack_prefill", pa_prefill_meta(), args, into, pin, PrefillPlan)
 
 
-def pa_pack_decode(dims: pa_dims, context_lens, block_lists, split_tokens: int = 0, pin: bool = True) -> DecodePlan:
+def pa_pack_decode(dims: pa_dims, context_lens, block_lists, split_tokens: int = 0, pin: bool = True,
+                   into: Optional["DecodePlan"] = None) -> "DecodePlan":
     """Pack context lens, block tables, slot mapping and the split plan on the CPU."""
-    L = lib()
     ctx = _i32(context_lens)
     off, ids = _flatten(block_lists)
-    meta = pa_decode_meta()
     args = (ctypes.byref(dims), len(ctx), _np_ptr(ctx), _np_ptr(off), _np_ptr(ids), int(split_tokens))
-    _check(L.pa_pack_decode(*args, None, 0, ctypes.byref(meta)), "pa_pack_decode")
-    host = torch.empty(max(int(meta.total_bytes), 256), dtype=torch.uint8, pin_memory=pin)
-    _check(L.pa_pack_decode(*args, _ptr(host), host.numel(), ctypes.byref(meta)), "pa_pack_decode")
-    return DecodePlan(meta, host)
+    return _pack("pa_pack_decode", pa_decode_meta(), args, into, pin, DecodePlan)
 
 
 def pa_upload(dev_dst, host_src, nbytes: int, stream=None):

@@ -58,6 +58,9 @@ def test_device_calls_reject_bad_args_without_touching_the_gpu():
     meta.num_tiles, meta.total_q, meta.num_seqs, meta.max_blocks_per_seq, meta.rows_per_tile = 1, 1, 1, 1, 64
     assert L.pa_prefill_varlen(ctypes.byref(dims), None, None, None, None, None, None, ctypes.c_float(0.1),
                                None, ctypes.byref(meta), None, None) == pa.PA_ERR_INVALID_ARG
+    for bad in (0.0, -0.5, float("inf"), float("nan")):
+        assert L.pa_prefill_varlen(ctypes.byref(dims), 16, 16, 16, 16, 16, 16, ctypes.c_float(bad), 16,
+                                   ctypes.byref(meta), 16, None) == pa.PA_ERR_INVALID_ARG
     meta.rows_per_tile = 7  # packed for other dims
     assert L.pa_prefill_varlen(ctypes.byref(dims), 16, 16, 16, 16, 16, 16, ctypes.c_float(0.1), 16,
                                ctypes.byref(meta), 16, None) == pa.PA_ERR_INVALID_ARG
