@@ -197,6 +197,37 @@ int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const voi
               const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items,
               void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
+/*
+ * pa_decode_static — pa_decode for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that have no way to obtain a decode workspace, e.g. code that runs while a
+ * stream is being captured into a CUDA graph (cudaMalloc is not allowed
+ * during capture in the default mode) or runtimes that only hand out fixed,
+ * pre-planned buffers.  It computes exactly what pa_decode computes, with the
+ * same arguments minus the workspace.
+ *
+ * Scratch: instead of a caller workspace it uses one array inside the library,
+ * PA_DECODE_STATIC_SCRATCH_BYTES (16 MiB) of device memory that every GPU
+ * which loads the library keeps until the process exits.  It calls no
+ * cudaMalloc/cudaFree and no allocating library routine.
+ *  - Limit: a plan whose meta->workspace_bytes exceeds the array is rejected
+ *    with PA_ERR_WORKSPACE before any launch (use pa_decode, or a larger
+ *    split_tokens when packing, for such batches).
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress, with that device current); make that first
+ *    call before any stream capture.  Later calls do no set-up.
+ *  - Sharing: every call on a device uses the same array and it keeps the
+ *    last call's contents.  Nothing in it needs to start at zero: each call
+ *    writes every partial it reads.  Calls whose work overlaps on the GPU
+ *    (different streams, not ordered) race on the array; order them.
+ * The call works on the current device.
+ */
+#define PA_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+int pa_decode_static(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *context_lens, const int32_t *block_tables, float scale, void *out,
+                     const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items,
+                     pa_stream_t stream);
+
 /* ------------------------------------------------------------------ diagnostics */
 
 /* Text of the last error on this thread ("" if none). */

@@ -189,6 +189,28 @@ extern "C" int pa_decode(const pa_dims *dims, const void *q, const void *k_cache
     return launch_decode(a, stream);
 }
 
+// pa_decode for callers that cannot allocate: the workspace is the library's
+// own scratch array (see the header for its limit, set-up and sharing rules).
+extern "C" int pa_decode_static(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *context_lens, const int32_t *block_tables, float scale, void *out,
+                                const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items,
+                                pa_stream_t stream)
+{
+    if (!meta)
+        return fail(PA_ERR_INVALID_ARG, "meta is NULL");
+    if (meta->workspace_bytes > PA_DECODE_STATIC_SCRATCH_BYTES)
+        return fail(PA_ERR_WORKSPACE,
+                    "pa_decode_static: plan needs %llu bytes of scratch, the library array holds %u; "
+                    "use pa_decode with a workspace or pack with larger splits",
+                    (unsigned long long)meta->workspace_bytes, PA_DECODE_STATIC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    int rc = decode_static_scratch(&scratch);
+    if (rc != PA_OK)
+        return rc;
+    return pa_decode(dims, q, k_cache, v_cache, context_lens, block_tables, scale, out, meta, items, seq_items,
+                     scratch, PA_DECODE_STATIC_SCRATCH_BYTES, stream);
+}
+
 extern "C" int pa_read_device_error(uint32_t *code, pa_stream_t stream)
 {
     if (!code)

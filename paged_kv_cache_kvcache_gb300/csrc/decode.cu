@@ -25,6 +25,8 @@
 // except one 3-step max per chunk).  The 4 warps merge through shared memory;
 // a single-split sequence writes bf16 directly, otherwise (o/l, log2-sum-exp)
 // partials go to the workspace and a combine kernel merges them.
+#include <mutex>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -385,6 +387,34 @@ int launch_decode(const DecodeArgs &a, void *stream)
     if (a.dims.head_dim == 128)
         return two ? launch_split<128, 2>(a, p, s) : launch_split<128, 1>(a, p, s);
     return two ? launch_split<64, 2>(a, p, s) : launch_split<64, 1>(a, p, s);
+}
+
+// Library-owned decode scratch for pa_decode_static (callers that cannot
+// allocate).  Held by every device that loads the library until exit.
+static __device__ __align__(256) unsigned char g_decode_scratch[PA_DECODE_STATIC_SCRATCH_BYTES];
+
+int decode_static_scratch(void **ptr)
+{
+    // one lookup per device, made with that device current
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(PA_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess)
+            return fail(PA_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return PA_OK;
 }
 
 int decode_ctas_per_sm(int head_dim, int group)

@@ -67,6 +67,10 @@ struct DecodeArgs {
 };
 int launch_decode(const DecodeArgs &a, void *stream);
 
+// Device address of the library-owned decode scratch on the current device
+// (looked up once per device).  Used only by pa_decode_static.
+int decode_static_scratch(void **ptr);
+
 // Concurrent decode CTAs one SM holds (occupancy of the decode kernel).
 int decode_ctas_per_sm(int head_dim, int group);
 

@@ -21,7 +21,9 @@ from . import _build
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, 1, 2, 3, 4
 
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
-           "pa_decode", "pa_last_error_string", "pa_read_device_error", "pa_version")
+           "pa_decode", "pa_decode_static", "pa_last_error_string", "pa_read_device_error", "pa_version")
+
+PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class pa_dims(ctypes.Structure):
@@ -75,6 +77,7 @@ def lib() -> ctypes.CDLL:
             L.pa_store_kvcache.argtypes = [P, P, P, P, P, P, I32, P]
             L.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
             L.pa_decode.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
+            L.pa_decode_static.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P]
             L.pa_last_error_string.argtypes = []
             L.pa_last_error_string.restype = ctypes.c_char_p
             L.pa_read_device_error.argtypes = [P, P]
@@ -246,6 +249,21 @@ def pa_decode(dims: pa_dims, q, k_cache, v_cache, plan: DecodePlan, scale: float
                            plan.dptr(m.off_context_lens), plan.dptr(m.off_block_tables), float(scale), _ptr(out),
                            ctypes.byref(m), plan.dptr(m.off_items), plan.dptr(m.off_seq_items), _ptr(workspace),
                            ws_bytes, _stream(stream)), "pa_decode")
+
+
+def pa_decode_static(dims: pa_dims, q, k_cache, v_cache, plan: DecodePlan, scale: float, out, stream=None):
+    """pa_decode without a workspace, for callers that cannot allocate device memory.
+
+    The library's own 16 MiB scratch array stands in for the workspace; every
+    call on a device shares it, so calls must not overlap on the GPU.  The
+    first call on a device does a one-time address lookup: make it before any
+    stream capture.
+    """
+    m = plan.meta
+    _check(lib().pa_decode_static(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                  plan.dptr(m.off_context_lens), plan.dptr(m.off_block_tables), float(scale),
+                                  _ptr(out), ctypes.byref(m), plan.dptr(m.off_items), plan.dptr(m.off_seq_items),
+                                  _stream(stream)), "pa_decode_static")
 
 
 def pa_read_device_error(stream=None) -> int:
