@@ -71,8 +71,9 @@ typedef struct pa_prefill_meta {
     int32_t max_seqlen_q;
     int32_t max_seqlen_k;
     int32_t max_blocks_per_seq; /* row pitch of block_tables */
-    int32_t num_tiles;          /* CTAs of the prefill launch */
-    int32_t rows_per_tile;      /* query positions per tile (128 / group, floored) */
+    int32_t num_tiles;          /* work items = CTAs of the prefill launch */
+    int32_t rows_per_tile;      /* query positions per query tile (128 / group, floored);
+                                   a work item covers two query tiles */
     int32_t reserved;
     uint64_t off_cu_seqlens_q;  /* int32 [num_seqs+1] */
     uint64_t off_cu_seqlens_k;  /* int32 [num_seqs+1] */

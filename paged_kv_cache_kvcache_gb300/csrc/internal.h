@@ -11,6 +11,7 @@ namespace pa {
 // Key tile of the prefill kernel and query rows of one tile (tcgen05 M).
 constexpr int kPrefillKeyTile = 128;
 constexpr int kPrefillRows = 128;
+constexpr int kPrefillTilesPerItem = 2; // query tiles per prefill CTA
 // Keys per warp step of the decode kernel and per CTA step (4 warps).
 constexpr int kDecodeChunk = 16;
 constexpr int kDecodeStep = 64;

@@ -114,16 +114,18 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
     if (num_seqs > 0 && (rc = check_seq_blocks(d, num_seqs, seq_lens, block_offsets, block_ids, &mb)) != PA_OK)
         return rc;
 
-    // tile work list: (sequence, first query row, KV head, key tiles), longest first
+    // work list: (sequence, first query row, KV head, key tiles), longest first.
+    // One item = two query tiles of `rows` positions each (the kernel ping-pongs them).
     const int32_t rows = std::max(1, kPrefillRows / group);
+    const int32_t span = kPrefillTilesPerItem * rows;
     struct Tile {
         int32_t seq, q0, kvh, nkt;
     };
     std::vector<Tile> tiles;
     for (int32_t b = 0; b < num_seqs; ++b) {
         const int32_t lq = query_lens[b], lk = seq_lens[b];
-        for (int32_t q0 = 0; q0 < lq; q0 += rows) {
-            int32_t last = std::min(q0 + rows, lq) - 1;       // last query row of the tile
+        for (int32_t q0 = 0; q0 < lq; q0 += span) {
+            int32_t last = std::min(q0 + span, lq) - 1;       // last query row of the item
             int32_t visible = lk - lq + last + 1;             // keys that row sees
             int32_t nkt = (visible + kPrefillKeyTile - 1) / kPrefillKeyTile;
             for (int32_t g = 0; g < d.num_kv_heads; ++g)

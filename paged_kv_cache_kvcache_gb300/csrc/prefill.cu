@@ -15,27 +15,34 @@
 //    kernel loses to tiled attention once prompts get long; the fix named
 //    there is query tiling with an in-tile causal mask.
 //
-// GB300 design (one CTA per work-list tile, 6 warps, 1 CTA per SM):
-//  * Query tile = 128 rows of one KV-head group: rows r = pos * G + h packs the
-//    G query heads that share a KV head next to each other, so one K/V stream
-//    feeds all of them (GQA reuse).  A 3-D TMA box {64 d, G heads, P positions}
-//    loads it straight into the 128B-swizzled K-major layout tcgen05 reads.
-//  * Keys in tiles of 128.  Each K/V tile is gathered through the block table
-//    with one TMA box per physical block (or one per tile when a block holds
-//    >= 128 tokens) into a 2-stage ring; boxes past the end of the pool read
-//    as zeros.
-//  * warp 0: TMA producer.  warp 1: TMEM allocation + single-thread tcgen05.mma
-//    issue: S = Q K^T (M=128, N=128, K=D) into one of two TMEM score buffers,
-//    then O += P V (M=128, N=D, K=128) into a TMEM accumulator, with V read
-//    MN-major straight from its TMA layout.  warps 2-5: one query row per
-//    thread — tcgen05.ld of the score row, causal mask on boundary tiles
-//    only, fp32 online softmax in base 2 (scale * log2 e folded into one FMA),
-//    lazy rescaling of O (only when the running max grows by more than 2^8),
-//    P rounded to bf16 into swizzled shared memory, then the epilogue (O / l,
-//    bf16, coalesced row stores).
-//  * S double buffering lets the tensor core compute S_{j+1} while the softmax
-//    warps work on S_j; mbarriers order every hand-off; every wait is bounded
-//    and reports a timeout through a device error word instead of hanging.
+// GB300 design (one CTA per work item, 12 warps, 1 CTA per SM):
+//  * A work item is (sequence, 2 query tiles, KV head).  Query tile rows
+//    r = pos * G + h pack the G query heads that share a KV head next to each
+//    other, so one K/V stream feeds all of them (GQA reuse); a 3-D TMA box
+//    {64 d, G heads, P positions} loads each tile straight into the
+//    128B-swizzled K-major layout tcgen05 reads.  The two tiles cover
+//    consecutive positions and share every K/V tile the CTA loads.
+//  * Keys in tiles of 128, gathered through the block table with one TMA box
+//    per physical block (or one per tile when a block holds >= 128 tokens)
+//    into a K/V ring; boxes past the end of the pool read as zeros and the V
+//    rows past the sequence end are zeroed before use.
+//  * warp 0: TMA producer.  warp 1: TMEM allocation + single-thread
+//    tcgen05.mma issue.  Each query tile t owns 256 TMEM columns: S_t (128
+//    fp32 columns, reused for P_t as packed bf16) and O_t.  The issue order
+//    PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core busy on one
+//    tile while the other tile's softmax runs (ping-pong).  Because the MMAs of
+//    one thread execute in order, S_t(j+1) being complete means PV_t(j) is
+//    too: O_t is stable and P_t consumed when the softmax sees S_t(j+1).
+//  * warps 4-7 and 8-11: one softmax warpgroup per query tile, one query row
+//    per thread: tcgen05.ld of the score row in two passes (row max, then
+//    exponentials), causal mask only on tiles that cross the diagonal, fp32
+//    online softmax in base 2 (scale * log2 e folded into one packed FMA),
+//    lazy O rescale (only when the running max grows by more than 2^8), P
+//    written back over S with tcgen05.st and consumed by the PV MMA straight
+//    from tensor memory; epilogue O / l -> bf16 -> shared staging ->
+//    coalesced row stores.
+//  * mbarriers order every hand-off; every wait is bounded and reports a
+//    timeout through a device error word instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -50,10 +57,12 @@ __device__ uint32_t g_prefill_error; // bit 0: a bounded wait timed out
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kSoftmaxWarp0 = 2;
+// warps 0-7: softmax (two warpgroups), 8: K/Q TMA producer, 9: MMA issuer,
+// 10: V TMA producer, 11: idle (registers are granted per 4 warps, so the CTA
+// is sized at 12 warps, <= 168 registers each)
+constexpr int kThreads = 384;
+constexpr int kKProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
 
@@ -62,16 +71,18 @@ struct PfLayout {
     static constexpr int kPanels = D / 64;          // 64-element (128-byte) panels along head_dim
     static constexpr int kPanelBytes = 128 * 128;   // 128 rows x 128 bytes
     static constexpr int kTileBytes = kPanels * kPanelBytes;
-    static constexpr int kStages = D == 128 ? 2 : 3;
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kTileBytes;
-    static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kP = kV + kStages * kTileBytes;
-    static constexpr int kPBytes = 2 * kPanelBytes; // 128 rows x 128 keys bf16; reused as O staging
-    static constexpr int kBar = kP + kPBytes;
+    // K is released as soon as the two score MMAs have read it, V only after
+    // both PV MMAs: K gets the deeper ring so its loads start earliest.
+    static constexpr int kKStages = D == 128 ? 3 : 4;
+    static constexpr int kVStages = D == 128 ? 2 : 4;
+    static constexpr int kQ = 0;                    // two query tiles (also the output staging)
+    static constexpr int kK = kQ + 2 * kTileBytes;
+    static constexpr int kV = kK + kKStages * kTileBytes;
+    static constexpr int kBar = kV + kVStages * kTileBytes;
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kBar + kBarBytes + 1024; // + alignment slack
-    static_assert(128 * D * 2 <= kPBytes, "O staging must fit in the P buffer");
+    static_assert(128 * D * 2 <= kTileBytes, "O staging must fit in a query tile");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct PfParams {
@@ -83,7 +94,7 @@ struct PfParams {
     float scale_log2;
     int32_t num_heads;
     int32_t group;
-    int32_t rows_per_tile; // query positions per tile
+    int32_t rows_per_tile; // query positions per query tile
     int32_t block_size;
     int32_t max_blocks;
     int32_t num_slots;     // num_blocks * block_size: first out-of-range row (reads as zeros)
@@ -92,17 +103,18 @@ struct PfParams {
 // barrier slots (uint64 each) inside the barrier area
 struct Bars {
     uint32_t base;
-    __device__ uint32_t q_full() const { return base; }
-    __device__ uint32_t k_full(int s) const { return base + 8 * (1 + s); }
-    __device__ uint32_t v_full(int s) const { return base + 8 * (4 + s); }
-    __device__ uint32_t kv_empty(int s) const { return base + 8 * (7 + s); }
-    __device__ uint32_t s_full(int b) const { return base + 8 * (10 + b); }
-    __device__ uint32_t s_free(int b) const { return base + 8 * (12 + b); }
-    __device__ uint32_t p_full() const { return base + 8 * 14; }
-    __device__ uint32_t pv_done() const { return base + 8 * 15; }
-    __device__ uint32_t tmem_slot() const { return base + 8 * 16; }
-    __device__ uint32_t abort_slot() const { return base + 8 * 17; }
+    __device__ uint32_t q_full(int t) const { return base + 8 * t; }
+    __device__ uint32_t k_full(int s) const { return base + 8 * (2 + s); }
+    __device__ uint32_t k_empty(int s) const { return base + 8 * (6 + s); }
+    __device__ uint32_t v_full(int s) const { return base + 8 * (10 + s); }
+    __device__ uint32_t v_empty(int s) const { return base + 8 * (14 + s); }
+    __device__ uint32_t s_full(int t) const { return base + 8 * (18 + t); }
+    __device__ uint32_t p_full(int t) const { return base + 8 * (20 + t); }
+    __device__ uint32_t v_tail() const { return base + 8 * 22; }
+    __device__ uint32_t tmem_slot() const { return base + 8 * 23; }
 };
+constexpr int kTmemSlotOffset = 8 * 23;
+constexpr int kAbortOffset = 8 * 24;
 
 struct Waiter {
     volatile uint32_t *abort;
@@ -132,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const Bars bars{sbase + L::kBar};
-    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + 8 * 17);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kAbortOffset);
     const Waiter wait{abort_flag};
 
     const int4 tile = p.tiles[blockIdx.x];
@@ -142,49 +154,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lk = p.cu_seqlens_k[b + 1] - p.cu_seqlens_k[b];
     const int G = p.group;
     const int P = p.rows_per_tile;
-    const int npos = min(P, lq - q0);     // valid query positions in this tile
-    const int off = lk - lq;              // absolute position of query row 0
-    const int nkt = (off + q0 + npos + 127) >> 7;
+    const int off = lk - lq; // absolute position of query row 0
+    // valid positions and key tiles of each query tile (tile 1 may be empty)
+    const int npos0 = min(P, lq - q0);
+    const int npos1 = max(0, min(P, lq - q0 - P));
+    const int nkt0 = (off + q0 + npos0 + 127) >> 7;
+    const int nkt1 = npos1 > 0 ? (off + q0 + P + npos1 + 127) >> 7 : 0;
+    const int nkt = max(nkt0, nkt1);
+    const bool tail = nkt * 128 > lk; // last key tile runs past the sequence end
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bars.q_full(), 1);
-        for (int s = 0; s < L::kStages; ++s) {
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bars.q_full(t), 1);
+            ptx::mbar_init(bars.s_full(t), 1);
+            ptx::mbar_init(bars.p_full(t), 128);
+        }
+        for (int s = 0; s < L::kKStages; ++s) {
             ptx::mbar_init(bars.k_full(s), 1);
+            ptx::mbar_init(bars.k_empty(s), 1);
+        }
+        for (int s = 0; s < L::kVStages; ++s) {
             ptx::mbar_init(bars.v_full(s), 1);
-            ptx::mbar_init(bars.kv_empty(s), 1);
+            ptx::mbar_init(bars.v_empty(s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(bars.s_full(s), 1);
-            ptx::mbar_init(bars.s_free(s), 128);
-        }
-        ptx::mbar_init(bars.p_full(), 128);
-        ptx::mbar_init(bars.pv_done(), 1);
+        ptx::mbar_init(bars.v_tail(), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         ptx::tmem_alloc(bars.tmem_slot(), kTmemCols);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + 8 * 16);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kTmemSlotOffset);
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
+    if (warp == kKProducerWarp || warp == kVProducerWarp) {
+        // ---------------------------------------------------------------- TMA producers (K + Q, V)
+        const bool is_k = warp == kKProducerWarp;
         const int bs = p.block_size;
         const int box_rows = bs < 128 ? bs : 128;
         const int nsub = 128 / box_rows;
         const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
+        const int nstages = is_k ? L::kKStages : L::kVStages;
+        const uint32_t ring = sbase + (is_k ? L::kK : L::kV);
+        const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
         if (lane == 0) {
-            ptx::prefetch_tmap(&tm_q);
-            ptx::prefetch_tmap(&tm_k);
-            ptx::prefetch_tmap(&tm_v);
-            ptx::mbar_arrive_expect_tx(bars.q_full(), (uint32_t)(L::kPanels * 128 * G * P));
-            for (int pp = 0; pp < L::kPanels; ++pp)
-                ptx::tma_load_3d(sbase + L::kQ + pp * L::kPanelBytes, &tm_q, bars.q_full(), pp * 64, g * G,
-                                 cq0 + q0);
+            ptx::prefetch_tmap(tm);
+            if (is_k) {
+                ptx::prefetch_tmap(&tm_q);
+                for (int t = 0; t < 2; ++t) {
+                    if ((t == 0 ? npos0 : npos1) <= 0)
+                        continue;
+                    ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, &tm_q,
+                                         bars.q_full(t), pp * 64, g * G, cq0 + q0 + t * P);
+                }
+            }
         }
         // row coordinate of sub-box `lane` of key tile j (all lanes compute their own)
         auto sub_row = [&](int j) -> int {
@@ -195,203 +223,231 @@ __global__ void __launch_bounds__(kThreads, 1)
             return phys * bs + (key & (bs - 1));
         };
         int next = sub_row(0);
+        bool ok = true;
         for (int j = 0; j < nkt; ++j) {
             const int cur = next;
             if (j + 1 < nkt)
                 next = sub_row(j + 1);
-            const int st = j % L::kStages;
-            if (j >= L::kStages && !__all_sync(0xffffffffu, wait(bars.kv_empty(st), ((j / L::kStages) - 1) & 1)))
+            const int st = j % nstages;
+            const uint32_t empty = is_k ? bars.k_empty(st) : bars.v_empty(st);
+            const uint32_t full = is_k ? bars.k_full(st) : bars.v_full(st);
+            if (j >= nstages && !__all_sync(0xffffffffu, wait(empty, ((j / nstages) - 1) & 1))) {
+                ok = false;
                 break;
-            const uint32_t kdst = sbase + L::kK + st * L::kTileBytes;
-            const uint32_t vdst = sbase + L::kV + st * L::kTileBytes;
-            if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bars.k_full(st), (uint32_t)L::kTileBytes);
-                ptx::mbar_arrive_expect_tx(bars.v_full(st), (uint32_t)L::kTileBytes);
             }
+            const uint32_t dst = ring + st * L::kTileBytes;
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(full, (uint32_t)L::kTileBytes);
             for (int i = 0; i < nsub; ++i) {
                 const int row = __shfl_sync(0xffffffffu, cur, i);
-                if (lane == 0) {
-                    for (int pp = 0; pp < L::kPanels; ++pp) {
-                        const uint32_t o = pp * L::kPanelBytes + i * box_rows * 128;
-                        ptx::tma_load_3d(kdst + o, &tm_k, bars.k_full(st), pp * 64, g, row);
-                        ptx::tma_load_3d(vdst + o, &tm_v, bars.v_full(st), pp * 64, g, row);
-                    }
-                }
+                if (lane == 0)
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        ptx::tma_load_3d(dst + pp * L::kPanelBytes + i * box_rows * 128, tm, full, pp * 64, g, row);
             }
             __syncwarp();
         }
-    } else if (warp == 1) {
+        if (!is_k && ok && tail) {
+            // V rows of keys past the sequence end may hold anything (even NaN bit
+            // patterns); zero them so that P = 0 cannot turn them into NaN in O.
+            const int j = nkt - 1, st = j % L::kVStages;
+            if (__all_sync(0xffffffffu, wait(bars.v_full(st), (j / L::kVStages) & 1))) {
+                const int first = lk - j * 128;
+                uint8_t *vt = sgen + L::kV + st * L::kTileBytes;
+                const int chunks = (128 - first) * 8;
+                for (int pp = 0; pp < L::kPanels; ++pp)
+                    for (int c = lane; c < chunks; c += 32)
+                        *reinterpret_cast<uint4 *>(vt + pp * L::kPanelBytes + (first + (c >> 3)) * 128 +
+                                                   (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bars.v_tail());
+            }
+        }
+    } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 1);
-            bool ok = wait(bars.q_full(), 0);
-            for (int j = 0; ok && j <= nkt; ++j) {
-                if (j < nkt) {
-                    const int st = j % L::kStages;
-                    if (!wait(bars.k_full(st), (j / L::kStages) & 1))
-                        break;
-                    if (j >= 2 && !wait(bars.s_free(j & 1), ((j - 2) >> 1) & 1))
-                        break;
-                    ptx::tc_fence_after();
-                    const uint32_t d_s = tmem + ((j & 1) ? kColS1 : kColS0);
-                    const uint32_t qa = sbase + L::kQ, kb = sbase + L::kK + st * L::kTileBytes;
+            const int nk[2] = {nkt0, nkt1};
+            auto issue_s = [&](int t, int ks) {
+                const uint32_t qa = sbase + L::kQ + t * L::kTileBytes, kb = sbase + L::kK + ks * L::kTileBytes;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t o = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                        ptx::mma_bf16_ss(d_s, ptx::smem_desc(qa + o, 16, 1024, ptx::kSwizzle128B),
-                                         ptx::smem_desc(kb + o, 16, 1024, ptx::kSwizzle128B), idesc_s, kk > 0);
-                    }
-                    ptx::mma_commit(bars.s_full(j & 1));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t o = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                    ptx::mma_bf16_ss(tmem + t * 256, ptx::smem_desc(qa + o, 16, 1024, ptx::kSwizzle128B),
+                                     ptx::smem_desc(kb + o, 16, 1024, ptx::kSwizzle128B), idesc_s, kk > 0);
                 }
-                if (j >= 1) {
-                    const int jj = j - 1, st = jj % L::kStages;
-                    if (!wait(bars.p_full(), jj & 1))
-                        break;
-                    if (!wait(bars.v_full(st), (jj / L::kStages) & 1))
-                        break;
-                    ptx::tc_fence_after();
-                    const uint32_t pa_ = sbase + L::kP, vb = sbase + L::kV + st * L::kTileBytes;
+            };
+            auto issue_pv = [&](int t, int vs, bool first) {
+                const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t oa = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                        ptx::mma_bf16_ss(tmem + kColO, ptx::smem_desc(pa_ + oa, 16, 1024, ptx::kSwizzle128B),
-                                         ptx::smem_desc(vb + kk * 2048, L::kPanelBytes, 1024, ptx::kSwizzle128B),
-                                         idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8,
+                                     ptx::smem_desc(vb + kk * 2048, L::kPanelBytes, 1024, ptx::kSwizzle128B), idesc_o,
+                                     (!first || kk > 0) ? 1u : 0u);
+            };
+            bool ok = true;
+            for (int t = 0; t < 2 && ok; ++t)
+                if (nk[t] > 0)
+                    ok = wait(bars.q_full(t), 0);
+            ok = ok && wait(bars.k_full(0), 0);
+            if (ok) {
+                ptx::tc_fence_after();
+                for (int t = 0; t < 2; ++t)
+                    if (nk[t] > 0) {
+                        issue_s(t, 0);
+                        ptx::mma_commit(bars.s_full(t));
                     }
-                    ptx::mma_commit(bars.pv_done());
-                    ptx::mma_commit(bars.kv_empty(st));
+                ptx::mma_commit(bars.k_empty(0)); // K tile 0 read by both score MMAs
+            }
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int vs = j % L::kVStages, ksn = (j + 1) % L::kKStages;
+                bool v_ready = false, k_next = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= nk[t])
+                        continue;
+                    if (!(ok = wait(bars.p_full(t), j & 1)))
+                        break;
+                    if (!v_ready) {
+                        if (!(ok = wait(bars.v_full(vs), (j / L::kVStages) & 1)))
+                            break;
+                        if (tail && j == nkt - 1 && !(ok = wait(bars.v_tail(), 0)))
+                            break;
+                        v_ready = true;
+                    }
+                    ptx::tc_fence_after();
+                    issue_pv(t, vs, j == 0);
+                    if (j + 1 < nk[t]) {
+                        if (!k_next) {
+                            if (!(ok = wait(bars.k_full(ksn), ((j + 1) / L::kKStages) & 1)))
+                                break;
+                            ptx::tc_fence_after();
+                            k_next = true;
+                        }
+                        issue_s(t, ksn);
+                    }
+                    ptx::mma_commit(bars.s_full(t)); // next scores ready, or the final O
+                }
+                if (ok) {
+                    ptx::mma_commit(bars.v_empty(vs));
+                    if (k_next)
+                        ptx::mma_commit(bars.k_empty(ksn));
                 }
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < 8) {
         // ---------------------------------------------------------------- softmax + epilogue
+        const int t = warp >> 2;                   // query tile of this warpgroup (warps 0-3, 4-7)
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;         // query row of the tile
-        const int tid = (warp - kSoftmaxWarp0) * 32 + lane;
+        const int tid = (warp & 3) * 32 + lane;    // thread index inside the warpgroup
+        const int npos = t == 0 ? npos0 : npos1;
+        const int ntile = t == 0 ? nkt0 : nkt1;
         const bool row_valid = r < G * npos;
-        const int limit = off + q0 + r / G + 1;    // keys visible to this row
+        const int limit = row_valid ? off + q0 + t * P + r / G + 1 : 0; // keys visible to this row
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_col = tmem + lane_addr + t * 256;
+        const uint32_t o_col = s_col + 128;
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY, l_sum = 0.f;
-        uint8_t *prow = sgen + L::kP;
         bool ok = true;
-        // all lanes poll the same barrier; agree on the outcome so .sync.aligned ops never diverge
-        auto wwait = [&](uint32_t bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, wait(bar, parity));
-        };
+        auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
 
-        for (int j = 0; j < nkt; ++j) {
-            if (!(ok = wwait(bars.s_full(j & 1), (j >> 1) & 1)))
+        for (int j = 0; j < ntile; ++j) {
+            if (!(ok = wwait(bars.s_full(t), j & 1)))
                 break;
             ptx::tc_fence_after();
-            uint32_t s[128];
-            const uint32_t sa = tmem + lane_addr + ((j & 1) ? kColS1 : kColS0);
-            ptx::tmem_ld32(sa + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            ptx::tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-            ptx::tmem_ld32(sa + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-            ptx::tmem_ld32(sa + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+            const int lim = limit - j * 128; // columns this row sees in this tile
+            // the whole score row in registers: one TMEM round trip per tile
+            uint32_t sr[128];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                ptx::tmem_ld32(s_col + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
             ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bars.s_free(j & 1));
-
-            const int kbase = j * 128;
-            const int lim = limit - kbase;
-            uint32_t pk[64];
+            if (lim < 128) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    sr[c] = c < lim ? sr[c] : __float_as_uint(-INFINITY);
+            }
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                m8[i] = ptx::max3(__uint_as_float(sr[16 * i]), __uint_as_float(sr[16 * i + 1]),
+                                  __uint_as_float(sr[16 * i + 2]));
+#pragma unroll
+            for (int c = 3; c < 16; c += 2)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    m8[i] = c + 1 < 16 ? ptx::max3(m8[i], __uint_as_float(sr[16 * i + c]), __uint_as_float(sr[16 * i + c + 1]))
+                                       : fmaxf(m8[i], __uint_as_float(sr[16 * i + c]));
+            const float mx = fmaxf(fmaxf(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5])),
+                                   fmaxf(m8[6], m8[7]));
+            const float mt = mx * sl2;
             float alpha = 1.f;
             bool rescale = false;
-            if (row_valid) {
-                float mx = -INFINITY;
-                if (lim >= 128) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        mx = fmaxf(mx, __uint_as_float(s[c]));
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const float v = c < lim ? __uint_as_float(s[c]) : -INFINITY;
-                        s[c] = __float_as_uint(v);
-                        mx = fmaxf(mx, v);
-                    }
-                }
-                const float mt = mx * sl2;
-                if (mt > m_ref + kRescaleThreshold || m_ref == -INFINITY) {
-                    const float m_new = fmaxf(m_ref, mt);
-                    alpha = ptx::ex2(m_ref - m_new); // 0 on the first tile
-                    rescale = j > 0;
-                    l_sum *= alpha;
-                    m_ref = m_new;
-                }
-                float rs = 0.f;
-#pragma unroll
-                for (int c = 0; c < 128; c += 2) {
-                    const float e0 = ptx::ex2(fmaf(__uint_as_float(s[c]), sl2, -m_ref));
-                    const float e1 = ptx::ex2(fmaf(__uint_as_float(s[c + 1]), sl2, -m_ref));
-                    rs += e0 + e1;
-                    pk[c >> 1] = ptx::pack_bf16(e0, e1);
-                }
-                l_sum += rs;
-            } else {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    pk[c] = 0u;
+            if (mt > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt != -INFINITY)) {
+                const float m_new = fmaxf(m_ref, mt);
+                alpha = ptx::ex2(m_ref - m_new); // 0 on the first tile
+                rescale = j > 0;
+                l_sum *= alpha;
+                m_ref = m_new;
             }
-
-            if (j > 0 && !(ok = wwait(bars.pv_done(), (j - 1) & 1)))
-                break;
-            ptx::tc_fence_after();
+            // P = 2^(s * scale * log2 e - m) as bf16 pairs written over S; row sum
+            const uint64_t sl2x2 = ptx::f2(sl2, sl2);
+            const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
+            const uint64_t negm2 = ptx::f2(negm, negm);
+            uint64_t sum2[4] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) { // two halves: P columns 32h..32h+31 hold keys 64h..64h+63
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 64 * h; c < 64 * h + 64; c += 2) {
+                    float x0, x1;
+                    ptx::f2_split(
+                        ptx::f2_fma(ptx::f2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2), x0, x1);
+                    const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1); // masked columns: 2^-inf = 0
+                    sum2[(c >> 1) & 3] = ptx::f2_add(sum2[(c >> 1) & 3], ptx::f2(e0, e1));
+                    pk[(c >> 1) & 31] = ptx::pack_bf16(e0, e1);
+                }
+                ptx::tmem_st32(s_col + 32 * h, pk);
+            }
+            float s0, s1, s2, s3, s4, s5, s6, s7;
+            ptx::f2_split(sum2[0], s0, s1);
+            ptx::f2_split(sum2[1], s2, s3);
+            ptx::f2_split(sum2[2], s4, s5);
+            ptx::f2_split(sum2[3], s6, s7);
+            l_sum += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+            // O is stable here: PV(j-1) completed before S(j) did (in-order MMAs), and
+            // PV(j) waits for this thread's p_full arrival below
             if (__any_sync(0xffffffffu, rescale)) {
-                const uint32_t oa = tmem + lane_addr + kColO;
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    ptx::tmem_ld32(oa + cc * 32, o);
+                    ptx::tmem_ld32(o_col + cc * 32, o);
                     ptx::tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    ptx::tmem_st32(oa + cc * 32, o);
-                }
-                ptx::tmem_wait_st();
-            }
-            if (j == nkt - 1 && kbase + 128 > lk) {
-                // keys past the sequence end: zero their V rows so 0 * garbage cannot poison O
-                const int st = j % L::kStages;
-                if (!(ok = wwait(bars.v_full(st), (j / L::kStages) & 1)))
-                    break;
-                if (r >= lk - kbase) {
-                    uint8_t *vrow = sgen + L::kV + st * L::kTileBytes + r * 128;
-#pragma unroll
-                    for (int pp = 0; pp < L::kPanels; ++pp)
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4 *>(vrow + pp * L::kPanelBytes + c * 16) = make_uint4(0, 0, 0, 0);
+                    ptx::tmem_st32(o_col + cc * 32, o);
                 }
             }
-            // P row r: keys 0-63 in panel 0, 64-127 in panel 1, 16-byte chunks XOR-swizzled by row
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const int panel = c >> 3, chunk = c & 7;
-                uint8_t *dst = prow + panel * L::kPanelBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            }
-            ptx::fence_proxy_async_smem();
+            ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bars.p_full());
+            ptx::mbar_arrive(bars.p_full(t));
         }
 
-        const bool good = ok && wwait(bars.pv_done(), (nkt - 1) & 1);
-        // epilogue: O / l -> bf16 -> staging (row pitch 2*D bytes, chunk-swizzled) -> global
-        uint8_t *stg = sgen + L::kP;
+        const bool good = ntile > 0 && ok && wwait(bars.s_full(t), ntile & 1);
+        // epilogue: O / l -> bf16 -> staging (this tile's Q buffer, row pitch 2*D, chunk-swizzled) -> global
+        uint8_t *stg = sgen + L::kQ + t * L::kTileBytes;
         if (good) {
             ptx::tc_fence_after();
             const float inv = (row_valid && l_sum > 0.f) ? 1.f / l_sum : 0.f;
-            const uint32_t oa = tmem + lane_addr + kColO;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
-                ptx::tmem_ld32(oa + cc * 32, o);
+                ptx::tmem_ld32(o_col + cc * 32, o);
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -405,13 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory"); // every softmax thread arrives exactly once
-        if (!*abort_flag) {
+        // every thread of the warpgroup arrives exactly once (named barrier 1 + t)
+        asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
+        if (good && !*abort_flag) {
             constexpr int CPR = D / 8; // 16-byte chunks per row
             const int nrows = G * npos;
             for (int idx = tid; idx < nrows * CPR; idx += 128) {
                 const int rr = idx / CPR, c = idx % CPR;
-                const int pos = q0 + rr / G, hl = rr % G;
+                const int pos = q0 + t * P + rr / G, hl = rr % G;
                 const size_t token = (size_t)cq0 + pos;
                 uint4 v = *reinterpret_cast<const uint4 *>(stg + rr * (2 * D) + ((c ^ (rr & 7)) << 4));
                 *reinterpret_cast<uint4 *>(p.out + (token * p.num_heads + (size_t)g * G + hl) * D + c * 8) = v;
@@ -421,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }

@@ -114,14 +114,16 @@ def test_pack_prefill_matches_definitions(name):
             n = -(-int(batch.seq_lens[b]) // p.block_size)
             assert bt[b, :n].tolist() == batch.block_lists[b][:n].tolist()
             assert (bt[b, n:] == -1).all()
-        # tiles: each (seq, query row, kv head) exactly once, longest first
+        # work items: each (seq, query row, kv head) exactly once, longest first;
+        # one item = two query tiles of P positions
         G = batch.num_heads // p.num_kv_heads
         P = plan.meta.rows_per_tile
         assert P == 128 // G
         cover = {}
         for s, q0, g, nkt in tiles.tolist():
             lq, lk = int(batch.query_lens[s]), int(batch.seq_lens[s])
-            last = min(q0 + P, lq) - 1
+            assert q0 % (2 * P) == 0
+            last = min(q0 + 2 * P, lq) - 1
             assert nkt == -(-(lk - lq + last + 1) // 128)
             for i in range(q0, last + 1):
                 cover[(s, i, g)] = cover.get((s, i, g), 0) + 1
