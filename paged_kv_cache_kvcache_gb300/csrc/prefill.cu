@@ -57,14 +57,20 @@ __device__ uint32_t g_prefill_error; // bit 0: a bounded wait timed out
 
 namespace {
 
-// warps 0-7: softmax (two warpgroups), 8: K/Q TMA producer, 9: MMA issuer,
-// 10: V TMA producer, 11: idle (registers are granted per 4 warps, so the CTA
-// is sized at 12 warps, <= 168 registers each)
+// warps 0-7: softmax (two warpgroups), 8: K/Q TMA producer, 9: MMA issuer (and
+// TMEM owner), 10: V TMA producer, 11: idle (registers are granted per 4 warps,
+// so the CTA is sized at 12 warps, <= 168 registers each).  One thread issues
+// the MMAs of both query tiles: its in-order stream keeps the two tiles half a
+// key tile apart, so one tile's softmax always runs under the other's MMAs.
 constexpr int kThreads = 384;
 constexpr int kKProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
+// Ring of release-event barriers.  A producer waits for event e while the MMA
+// thread cannot yet have passed event e + 3 (it needs the tile being loaded), so
+// 4 barriers keep every parity wait unambiguous.
+constexpr int kIterRing = 4;
 
 template <int D>
 struct PfLayout {
@@ -105,21 +111,25 @@ struct Bars {
     uint32_t base;
     __device__ uint32_t q_full(int t) const { return base + 8 * t; }
     __device__ uint32_t k_full(int s) const { return base + 8 * (2 + s); }
-    __device__ uint32_t k_empty(int s) const { return base + 8 * (6 + s); }
-    __device__ uint32_t v_full(int s) const { return base + 8 * (10 + s); }
-    __device__ uint32_t v_empty(int s) const { return base + 8 * (14 + s); }
+    __device__ uint32_t v_full(int s) const { return base + 8 * (6 + s); }
+    // release event e: the MMAs reading K tile e and V tile e - 1 are complete
+    // (event 0 = the prologue's score MMAs, event j + 1 = MMA iteration j)
+    __device__ uint32_t released(int e) const { return base + 8 * (10 + (e & (kIterRing - 1))); }
     __device__ uint32_t s_full(int t) const { return base + 8 * (18 + t); }
     __device__ uint32_t p_full(int t) const { return base + 8 * (20 + t); }
     __device__ uint32_t v_tail() const { return base + 8 * 22; }
     __device__ uint32_t tmem_slot() const { return base + 8 * 23; }
 };
 constexpr int kTmemSlotOffset = 8 * 23;
+static_assert(kIterRing == 4, "barrier slots 10..13");
 constexpr int kAbortOffset = 8 * 24;
 
 struct Waiter {
     volatile uint32_t *abort;
     __device__ bool operator()(uint32_t bar, uint32_t parity) const
     {
+        if (ptx::mbar_try_wait(bar, parity)) // fast path: phase already complete
+            return true;
         if (*abort)
             return false;
         if (ptx::mbar_wait(bar, parity))
@@ -167,16 +177,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bars.q_full(t), 1);
             ptx::mbar_init(bars.s_full(t), 1);
-            ptx::mbar_init(bars.p_full(t), 128);
+            ptx::mbar_init(bars.p_full(t), 4); // one arrival per softmax warp
         }
-        for (int s = 0; s < L::kKStages; ++s) {
+        for (int s = 0; s < L::kKStages; ++s)
             ptx::mbar_init(bars.k_full(s), 1);
-            ptx::mbar_init(bars.k_empty(s), 1);
-        }
-        for (int s = 0; s < L::kVStages; ++s) {
+        for (int s = 0; s < L::kVStages; ++s)
             ptx::mbar_init(bars.v_full(s), 1);
-            ptx::mbar_init(bars.v_empty(s), 1);
-        }
+        for (int s = 0; s < kIterRing; ++s)
+            ptx::mbar_init(bars.released(s), 1);
         ptx::mbar_init(bars.v_tail(), 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -200,6 +208,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nstages = is_k ? L::kKStages : L::kVStages;
         const uint32_t ring = sbase + (is_k ? L::kK : L::kV);
         const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
+        if (is_k && G * P < 128) {
+            // rows G*P..127 of each query tile receive no TMA data: zero them once so
+            // their (discarded) scores stay finite and cost the same as real rows
+            const int first = G * P, chunks = (128 - first) * 8;
+            for (int t = 0; t < 2; ++t)
+                for (int pp = 0; pp < L::kPanels; ++pp)
+                    for (int c = lane; c < chunks; c += 32)
+                        *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
+                                                   (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+        }
         if (lane == 0) {
             ptx::prefetch_tmap(tm);
             if (is_k) {
@@ -229,9 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j + 1 < nkt)
                 next = sub_row(j + 1);
             const int st = j % nstages;
-            const uint32_t empty = is_k ? bars.k_empty(st) : bars.v_empty(st);
             const uint32_t full = is_k ? bars.k_full(st) : bars.v_full(st);
-            if (j >= nstages && !__all_sync(0xffffffffu, wait(empty, ((j / nstages) - 1) & 1))) {
+            // slot reuse: tile j replaces tile j - S, free after release event
+            // j - S (K) or j - S + 1 (V)
+            bool free_ok = true;
+            if (j >= nstages) {
+                const int e = is_k ? j - nstages : j - nstages + 1;
+                free_ok = wait(bars.released(e), (e / kIterRing) & 1);
+            }
+            if (!__all_sync(0xffffffffu, free_ok)) {
                 ok = false;
                 break;
             }
@@ -269,7 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 1);
-            const int nk[2] = {nkt0, nkt1};
             auto issue_s = [&](int t, int ks) {
                 const uint32_t qa = sbase + L::kQ + t * L::kTileBytes, kb = sbase + L::kK + ks * L::kTileBytes;
 #pragma unroll
@@ -287,52 +312,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      ptx::smem_desc(vb + kk * 2048, L::kPanelBytes, 1024, ptx::kSwizzle128B), idesc_o,
                                      (!first || kk > 0) ? 1u : 0u);
             };
-            bool ok = true;
-            for (int t = 0; t < 2 && ok; ++t)
-                if (nk[t] > 0)
-                    ok = wait(bars.q_full(t), 0);
+            bool ok = wait(bars.q_full(0), 0);
+            if (ok && nkt1 > 0)
+                ok = wait(bars.q_full(1), 0);
             ok = ok && wait(bars.k_full(0), 0);
             if (ok) {
                 ptx::tc_fence_after();
-                for (int t = 0; t < 2; ++t)
-                    if (nk[t] > 0) {
-                        issue_s(t, 0);
-                        ptx::mma_commit(bars.s_full(t));
-                    }
-                ptx::mma_commit(bars.k_empty(0)); // K tile 0 read by both score MMAs
+                issue_s(0, 0);
+                ptx::mma_commit(bars.s_full(0));
+                if (nkt1 > 0) {
+                    issue_s(1, 0);
+                    ptx::mma_commit(bars.s_full(1));
+                }
+                ptx::mma_commit(bars.released(0)); // K tile 0 read by both score MMAs
             }
+            // ring positions kept as counters (no division in the issue loop)
+            int vs = 0, vph = 0, ksn = 1 % L::kKStages, kph = ksn == 0 ? 1 : 0;
             for (int j = 0; ok && j < nkt; ++j) {
-                const int vs = j % L::kVStages, ksn = (j + 1) % L::kKStages;
                 bool v_ready = false, k_next = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= nk[t])
-                        continue;
+                // one query tile: PV(t, j), then S(t, j + 1) into the same TMEM columns
+                auto step = [&](const int t, const int ntk) {
                     if (!(ok = wait(bars.p_full(t), j & 1)))
-                        break;
+                        return;
                     if (!v_ready) {
-                        if (!(ok = wait(bars.v_full(vs), (j / L::kVStages) & 1)))
-                            break;
+                        if (!(ok = wait(bars.v_full(vs), vph)))
+                            return;
                         if (tail && j == nkt - 1 && !(ok = wait(bars.v_tail(), 0)))
-                            break;
+                            return;
                         v_ready = true;
                     }
                     ptx::tc_fence_after();
                     issue_pv(t, vs, j == 0);
-                    if (j + 1 < nk[t]) {
+                    if (j + 1 < ntk) {
                         if (!k_next) {
-                            if (!(ok = wait(bars.k_full(ksn), ((j + 1) / L::kKStages) & 1)))
-                                break;
+                            if (!(ok = wait(bars.k_full(ksn), kph)))
+                                return;
                             ptx::tc_fence_after();
                             k_next = true;
                         }
                         issue_s(t, ksn);
                     }
                     ptx::mma_commit(bars.s_full(t)); // next scores ready, or the final O
+                };
+                if (j < nkt0)
+                    step(0, nkt0);
+                if (ok && j < nkt1)
+                    step(1, nkt1);
+                if (ok)
+                    ptx::mma_commit(bars.released(j + 1)); // V tile j and K tile j + 1 read
+                if (++vs == L::kVStages) {
+                    vs = 0;
+                    vph ^= 1;
                 }
-                if (ok) {
-                    ptx::mma_commit(bars.v_empty(vs));
-                    if (k_next)
-                        ptx::mma_commit(bars.k_empty(ksn));
+                if (++ksn == L::kKStages) {
+                    ksn = 0;
+                    kph ^= 1;
                 }
             }
         }
@@ -346,7 +380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int npos = t == 0 ? npos0 : npos1;
         const int ntile = t == 0 ? nkt0 : nkt1;
         const bool row_valid = r < G * npos;
-        const int limit = row_valid ? off + q0 + t * P + r / G + 1 : 0; // keys visible to this row
+        // keys visible to this row; rows that hold no query are never masked (their
+        // output is discarded) so that a warp's rows all take the same path
+        const int limit = row_valid ? off + q0 + t * P + r / G + 1 : 0x3fffffff;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const uint32_t s_col = tmem + lane_addr + t * 256;
         const uint32_t o_col = s_col + 128;
@@ -387,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mt = mx * sl2;
             float alpha = 1.f;
             bool rescale = false;
-            if (mt > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt != -INFINITY)) {
+            if (row_valid && (mt > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt != -INFINITY))) {
                 const float m_new = fmaxf(m_ref, mt);
                 alpha = ptx::ex2(m_ref - m_new); // 0 on the first tile
                 rescale = j > 0;
@@ -435,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bars.p_full(t));
+            __syncwarp(); // 128 arrivals on one word serialise: one per warp instead
+            if (lane == 0)
+                ptx::mbar_arrive(bars.p_full(t));
         }
 
         const bool good = ntile > 0 && ok && wwait(bars.s_full(t), ntile & 1);
