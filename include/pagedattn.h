@@ -79,7 +79,9 @@ typedef struct pa_prefill_meta {
     uint64_t off_cu_seqlens_k;  /* int32 [num_seqs+1] */
     uint64_t off_block_tables;  /* int32 [num_seqs][max_blocks_per_seq], -1 padded */
     uint64_t off_slot_mapping;  /* int32 [total_q] */
-    uint64_t off_tiles;         /* int32 [num_tiles][4] work list, longest first */
+    uint64_t off_tiles;         /* int32 [num_tiles][8] work list, longest first: sequence,
+                                   first query row, KV head, key tiles, first packed
+                                   query row of the sequence, query length, key length, 0 */
     uint64_t total_bytes;       /* size of the image */
 } pa_prefill_meta;
 

@@ -11,7 +11,10 @@ namespace pa {
 // Key tile of the prefill kernel and query rows of one tile (tcgen05 M).
 constexpr int kPrefillKeyTile = 128;
 constexpr int kPrefillRows = 128;
-constexpr int kPrefillTilesPerItem = 2; // query tiles per prefill CTA
+constexpr int kPrefillTilesPerItem = 2; // query tiles per prefill work item
+// work-list entry: sequence, first query row, KV head, key tiles, first packed
+// query row of the sequence, query length, key length, 0
+constexpr int kPrefillItemInts = 8;
 // Keys per warp step of the decode kernel and per CTA step (4 warps).
 constexpr int kDecodeChunk = 16;
 constexpr int kDecodeStep = 64;

@@ -133,7 +133,7 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
         }
     }
     std::stable_sort(tiles.begin(), tiles.end(), [](const Tile &x, const Tile &y) { return x.nkt > y.nkt; });
-    if (tiles.size() > (size_t)INT32_MAX / 4)
+    if (tiles.size() > (size_t)INT32_MAX / kPrefillItemInts)
         return fail(PA_ERR_INVALID_ARG, "too many tiles");
 
     Layout L;
@@ -149,7 +149,7 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
     meta->off_cu_seqlens_k = L.take(sizeof(int32_t) * (num_seqs + 1));
     meta->off_block_tables = L.take(sizeof(int32_t) * (size_t)num_seqs * mb);
     meta->off_slot_mapping = L.take(sizeof(int32_t) * (size_t)total_q);
-    meta->off_tiles = L.take(sizeof(int32_t) * 4 * tiles.size());
+    meta->off_tiles = L.take(sizeof(int32_t) * kPrefillItemInts * tiles.size());
     meta->total_bytes = L.off;
     if (!host_buf)
         return PA_OK;
@@ -177,10 +177,16 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
             slots[t++] = blk[pos / d.block_size] * d.block_size + pos % d.block_size;
     }
     for (size_t i = 0; i < tiles.size(); ++i) {
-        tl[4 * i + 0] = tiles[i].seq;
-        tl[4 * i + 1] = tiles[i].q0;
-        tl[4 * i + 2] = tiles[i].kvh;
-        tl[4 * i + 3] = tiles[i].nkt;
+        int32_t *e = tl + kPrefillItemInts * i;
+        const int32_t b = tiles[i].seq;
+        e[0] = b;
+        e[1] = tiles[i].q0;
+        e[2] = tiles[i].kvh;
+        e[3] = tiles[i].nkt;
+        e[4] = cu_q[b];       // first packed query row of the sequence
+        e[5] = query_lens[b];
+        e[6] = seq_lens[b];
+        e[7] = 0;
     }
     return PA_OK;
 }

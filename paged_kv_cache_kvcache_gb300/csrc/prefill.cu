@@ -157,11 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kAbortOffset);
     const Waiter wait{abort_flag};
 
-    const int4 tile = p.tiles[blockIdx.x];
-    const int b = tile.x, q0 = tile.y, g = tile.z;
-    const int cq0 = p.cu_seqlens_q[b];
-    const int lq = p.cu_seqlens_q[b + 1] - cq0;
-    const int lk = p.cu_seqlens_k[b + 1] - p.cu_seqlens_k[b];
+    // work-list entry: two independent 16-byte loads, no dependent metadata reads
+    const int4 e0 = __ldg(p.tiles + 2 * blockIdx.x), e1 = __ldg(p.tiles + 2 * blockIdx.x + 1);
+    const int b = e0.x, q0 = e0.y, g = e0.z;
+    const int cq0 = e1.x, lq = e1.y, lk = e1.z;
     const int G = p.group;
     const int P = p.rows_per_tile;
     const int off = lk - lq; // absolute position of query row 0

@@ -91,7 +91,7 @@ def _prefill_arrays(plan, b):
     m = plan.meta
     return (plan.host_array(m.off_cu_seqlens_q, b + 1), plan.host_array(m.off_cu_seqlens_k, b + 1),
             plan.host_array(m.off_block_tables, b * m.max_blocks_per_seq).reshape(b, m.max_blocks_per_seq),
-            plan.host_array(m.off_slot_mapping, m.total_q), plan.host_array(m.off_tiles, 4 * m.num_tiles).reshape(-1, 4))
+            plan.host_array(m.off_slot_mapping, m.total_q), plan.host_array(m.off_tiles, 8 * m.num_tiles).reshape(-1, 8))
 
 
 @pytest.mark.parametrize("name", ["tiny", "qwen3_prefix", "qwen3_chunked", "qwen3_prefill_128"])
@@ -120,8 +120,9 @@ def test_pack_prefill_matches_definitions(name):
         P = plan.meta.rows_per_tile
         assert P == 128 // G
         cover = {}
-        for s, q0, g, nkt in tiles.tolist():
+        for s, q0, g, nkt, cq, lq_, lk_, zero in tiles.tolist():
             lq, lk = int(batch.query_lens[s]), int(batch.seq_lens[s])
+            assert (cq, lq_, lk_, zero) == (int(cu_q[s]), lq, lk, 0)
             assert q0 % (2 * P) == 0
             last = min(q0 + 2 * P, lq) - 1
             assert nkt == -(-(lk - lq + last + 1) // 128)
