@@ -35,6 +35,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "prefill attn TFLOP/s & decode KV-read GB/s (% of GB300 roofline), 1 GPU"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM read + write bytes per launch from ncu captures of the current kernels on
+# this workload: the prefill launch exactly as benched; the decode kernel on 16
+# of the 64 sequences, scaled by 4 (traffic grows with the sequences).  Must be
+# re-captured (or set to None) whenever one of these kernels changes.
+NCU_TRAFFIC = {"qwen25": {"prefill": 232.9e6, "decode": 4.298e9}}
 
 
 def parse():
@@ -43,7 +48,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=600)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["qwen25", "qwen3"], default="qwen25")
+    ap.add_argument("--workload", choices=["qwen25", "qwen3", "qwen3_prefill_32", "qwen3_prefill_128",
+                                           "qwen3_prefix", "qwen3_chunked"], default="qwen25",
+                    help="qwen25: the long-context case (default); the others pair a Qwen3-0.6B prefill "
+                         "batch with the 256-sequence Qwen3 decode batch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -71,8 +79,12 @@ def make_workload(name, device, decode_seqs=64):
     if name == "qwen25":
         return workloads.make("qwen25_prefill", device), workloads.qwen25_decode(device, num_seqs=decode_seqs), \
             f"qwen25_long: prefill 4x4096 + decode {decode_seqs}x32768, Hq 28 / Hkv 4, D 128, block 16, permuted pools"
-    return workloads.make("qwen3_prefill_256", device), workloads.make("qwen3_decode", device), \
-        "qwen3: prefill 8x256 + decode 256 x ctx(in+out, in/out~U{100..1024}), Hq 16 / Hkv 8, D 128, block 256"
+    pre = {"qwen3": "qwen3_prefill_256"}.get(name, name)
+    desc = {"qwen3_prefill_256": "prefill 8x256", "qwen3_prefill_32": "prefill 8x32",
+            "qwen3_prefill_128": "prefill 8x128", "qwen3_prefix": "prefix-cache prefill 8x(44 of 300, block 0 shared)",
+            "qwen3_chunked": "chunked prefill 16x(prefix U{0..1024} + chunk U{1..512})"}[pre]
+    return workloads.make(pre, device), workloads.make("qwen3_decode", device), \
+        f"{name}: {desc} + decode 256 x ctx(in+out, in/out~U{{100..1024}}), Hq 16 / Hkv 8, D 128, block 256"
 
 
 def prefill_flops(batch) -> float:
@@ -369,11 +381,13 @@ def main():
     hbm_peak = float(peaks["hbm_gbs"])
     roof_p = {"kernel": "pa_prefill_varlen (prefill_kernel<128>)", "bound": "tensor", "achieved": round(pk_tflops, 2),
               "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(pk_tflops / bf16_peak, 4),
-              "peak_source": f"{peak_src} bf16_tflops (burst)", "traffic": None,
+              "peak_source": f"{peak_src} bf16_tflops (burst)",
+              "traffic": NCU_TRAFFIC.get(args.workload, {}).get("prefill"),
               "work_per_launch": flops, "ms_per_launch": round(t_prefill_kernel, 5)}
     roof_d = {"kernel": "pa_decode (decode_split_kernel<128,1> + decode_combine_kernel<128>)", "bound": "hbm",
               "achieved": round(dk_gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(dk_gbs / hbm_peak, 4),
-              "peak_source": f"{peak_src} hbm_gbs", "traffic": None,
+              "peak_source": f"{peak_src} hbm_gbs",
+              "traffic": NCU_TRAFFIC.get(args.workload, {}).get("decode") if args.decode_seqs == 64 else None,
               "work_per_launch": dbytes, "ms_per_launch": round(t_decode_kernel, 5)}
     dominant = roof_p if t_prefill_kernel >= t_decode_kernel else roof_d
 
