@@ -71,6 +71,20 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# ---------------------------------------------------------------- ranks
+
+
+def max_over_ranks(value: float) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- workload
 
 
@@ -331,11 +345,7 @@ def main():
         if world > 1:
             torch.distributed.barrier()
         clk = clocks.stop(w0, w1)
-        total_ms = t_start.elapsed_time(t_end)
-        if world > 1:
-            t = torch.tensor([total_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            total_ms = float(t.item())
+        total_ms = max_over_ranks(t_start.elapsed_time(t_end))
         ph = lambda a, b: [e[a].elapsed_time(e[b]) for e in evs]
         t_prefill_phase = statistics.mean(ph("p0", "p1"))
         t_prefill_kernel = statistics.mean(ph("pk0", "pk1"))
