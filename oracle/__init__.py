@@ -8,6 +8,7 @@ Every function here follows a definition on the pages (see ``ref.c`` for the
 per-step citations):
   * ``slot_mapping``   - slot of each new token (nano-vllm walkthrough, Step 5)
   * ``store_kvcache``  - bit copy of K/V rows into their slots, -1 skipped (Step 4)
+  * ``copy_blocks``    - copy-on-write fork of a shared block's valid rows (vLLM/SGLang labs §4)
   * ``gather_dense``   - block_table[pos // bs], pos % bs resolution (mini-infer §2.2-2.3)
   * ``paged_attention``- causal softmax(q K^T * scale) V, bottom-right aligned,
                          in double precision (KV-cache toy of the inference notes)
@@ -50,6 +51,8 @@ def _load():
             lib.oracle_slot_mapping.argtypes = [ctypes.c_int, P, P, P, P, ctypes.c_int, P]
             lib.oracle_store_kvcache.restype = None
             lib.oracle_store_kvcache.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_int64]
+            lib.oracle_copy_blocks.restype = None
+            lib.oracle_copy_blocks.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int64]
             lib.oracle_gather_dense.restype = None
             lib.oracle_gather_dense.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
             lib.oracle_paged_attention.restype = ctypes.c_int64
@@ -112,6 +115,14 @@ def store_kvcache(k_cache: np.ndarray, v_cache: np.ndarray, k, v, slots) -> None
     row = int(np.prod(k_cache.shape[2:]))
     assert kb.size == slots.size * row
     lib.oracle_store_kvcache(_ptr(k_cache), _ptr(v_cache), _ptr(kb), _ptr(vb), _ptr(slots), slots.size, row)
+
+
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, triples, block_size: int) -> None:
+    """In place on uint16 caches [num_blocks, bs, Hkv, D]: (src, dst, n) row copies."""
+    lib = _load()
+    tr = np.ascontiguousarray(np.asarray(triples, dtype=np.int32).reshape(-1, 3))
+    row = int(np.prod(k_cache.shape[2:]))
+    lib.oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(tr), tr.shape[0], block_size, row)
 
 
 def gather_dense(cache, length: int, blocks, block_size: int) -> np.ndarray:

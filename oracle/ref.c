@@ -29,6 +29,9 @@
  *    the visible keys, output is the probability-weighted sum of V.
  *  - "面试问答准备: nano-vLLM 推理引擎优化", Q1: the causal bound of a query
  *    at absolute position p is context_len = p + 1.
+ *  - "vLLM / SGLang 面试源码深挖", section 4 (KV block fork): a child that
+ *    appends into a shared, mutable block gets a new block holding a copy of
+ *    the shared block's valid KV.
  *  - Grouped-query attention: query head h reads KV head h / (Hq / Hkv)
  *    (contiguous groups; the pages do not state the mapping, this is the
  *    plainest reading and reduces to multi-head attention when Hq == Hkv).
@@ -96,6 +99,24 @@ void oracle_store_kvcache(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *
             continue;
         memcpy(k_cache + (int64_t)s * row_elems, k + t * row_elems, (size_t)row_elems * 2);
         memcpy(v_cache + (int64_t)s * row_elems, v + t * row_elems, (size_t)row_elems * 2);
+    }
+}
+
+/*
+ * Block copy (copy-on-write fork): for each (src, dst, n) triple, cache rows
+ * src*bs + i are copied to dst*bs + i for i < n, in K and in V, in order.
+ */
+void oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *triples, int64_t num_triples,
+                        int block_size, int64_t row_elems)
+{
+    for (int64_t t = 0; t < num_triples; ++t) {
+        const int64_t src = triples[3 * t], dst = triples[3 * t + 1], n = triples[3 * t + 2];
+        for (int64_t i = 0; i < n; ++i) {
+            memcpy(k_cache + (dst * block_size + i) * row_elems, k_cache + (src * block_size + i) * row_elems,
+                   (size_t)row_elems * 2);
+            memcpy(v_cache + (dst * block_size + i) * row_elems, v_cache + (src * block_size + i) * row_elems,
+                   (size_t)row_elems * 2);
+        }
     }
 }
 

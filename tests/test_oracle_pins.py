@@ -275,3 +275,30 @@ def test_dominant_logit_selects_that_value():
     c["q"] = q.to(torch.bfloat16)
     out, _, _, _ = _oracle_case(c)
     np.testing.assert_allclose(out[n - 1, 0], _f64(c["v"][star, 0]), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- block copy (copy-on-write fork)
+
+
+def test_copy_blocks_golden():
+    fx = json.load(open(os.path.join(GOLDEN, "copy_blocks_toy.json")))
+    k = _bits(torch.tensor(fx["k_pool"], dtype=torch.float32).to(torch.bfloat16))
+    v = _bits(torch.tensor(fx["v_pool"], dtype=torch.float32).to(torch.bfloat16))
+    oracle.copy_blocks(k, v, fx["triples"], fx["block_size"])
+    want_k = _bits(torch.tensor(fx["expected_k"], dtype=torch.float32).to(torch.bfloat16))
+    want_v = _bits(torch.tensor(fx["expected_v"], dtype=torch.float32).to(torch.bfloat16))
+    assert np.array_equal(k, want_k) and np.array_equal(v, want_v)
+
+
+def test_copy_blocks_matches_fancy_index():
+    g = torch.Generator().manual_seed(31)
+    nb, bs, hkv, d = 12, 16, 2, 8
+    k = _bits(torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16))
+    v = _bits(torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16))
+    triples = np.array([[0, 5, 16], [3, 7, 9], [4, 11, 0], [1, 6, 1]], np.int32)
+    want_k, want_v = k.copy(), v.copy()
+    for s, t, n in triples:
+        want_k[t, :n] = want_k[s, :n]
+        want_v[t, :n] = want_v[s, :n]
+    oracle.copy_blocks(k, v, triples, bs)
+    assert np.array_equal(k, want_k) and np.array_equal(v, want_v)
