@@ -201,6 +201,23 @@ int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const voi
               void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_copy_blocks — copy-on-write of shared cache blocks.  Source: "vLLM /
+ * SGLang 面试源码深挖", section 4 (KV block fork): when an append would land in
+ * a shared, still-mutable block, the child gets a new block and the valid KV
+ * is copied into it; "推理系统", PagedAttention paragraph (copy on write).
+ *   triples: device int32 [num_triples][3] = (src block, dst block, n valid
+ *            tokens); rows src*bs + i are copied to dst*bs + i for i < n, in
+ *            both K and V, bit for bit.
+ * dst blocks must be distinct and must not be the src of another triple
+ * (otherwise the result depends on order).  A triple with a block id outside
+ * [0, num_blocks) or n outside [0, block_size] is skipped and flagged in the
+ * device error word (pa_read_device_error bit 2).  num_triples == 0 launches
+ * nothing.
+ */
+int pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache, const int32_t *triples,
+                   int32_t num_triples, pa_stream_t stream);
+
+/*
  * pa_decode_static — pa_decode for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point: it exists for callers
  * that have no way to obtain a decode workspace, e.g. code that runs while a

@@ -189,6 +189,23 @@ extern "C" int pa_decode(const pa_dims *dims, const void *q, const void *k_cache
     return launch_decode(a, stream);
 }
 
+extern "C" int pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache, const int32_t *triples,
+                              int32_t num_triples, pa_stream_t stream)
+{
+    int rc = check_dims(dims);
+    if (rc != PA_OK)
+        return rc;
+    if (num_triples < 0)
+        return fail(PA_ERR_INVALID_ARG, "num_triples < 0");
+    if (num_triples == 0)
+        return PA_OK;
+    if (!k_cache || !v_cache || !triples)
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: NULL pointer");
+    if (misaligned(k_cache) || misaligned(v_cache) || (reinterpret_cast<uintptr_t>(triples) & 3u))
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: misaligned pointer");
+    return launch_copy_blocks(*dims, k_cache, v_cache, triples, num_triples, stream);
+}
+
 // pa_decode for callers that cannot allocate: the workspace is the library's
 // own scratch array (see the header for its limit, set-up and sharing rules).
 extern "C" int pa_decode_static(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
@@ -222,5 +239,7 @@ extern "C" int pa_read_device_error(uint32_t *code, pa_stream_t stream)
     int rc = read_store_error(code);
     if (rc == PA_OK)
         rc = read_prefill_error(code);
+    if (rc == PA_OK)
+        rc = read_copy_error(code);
     return rc;
 }

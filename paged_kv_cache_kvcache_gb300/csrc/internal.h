@@ -78,8 +78,13 @@ int decode_static_scratch(void **ptr);
 // Concurrent decode CTAs one SM holds (occupancy of the decode kernel).
 int decode_ctas_per_sm(int head_dim, int group);
 
-// Read and clear the device error words (store: bit 0, prefill waits: bit 1).
+int launch_copy_blocks(const pa_dims &d, void *k_cache, void *v_cache, const int32_t *triples, int32_t n,
+                       void *stream);
+
+// Read and clear the device error words (store: bit 0, prefill waits: bit 1,
+// block copy: bit 2).
 int read_store_error(uint32_t *code);
 int read_prefill_error(uint32_t *code);
+int read_copy_error(uint32_t *code);
 
 } // namespace pa

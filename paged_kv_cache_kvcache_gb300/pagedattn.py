@@ -21,7 +21,8 @@ from . import _build
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, 1, 2, 3, 4
 
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
-           "pa_decode", "pa_decode_static", "pa_last_error_string", "pa_read_device_error", "pa_version")
+           "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_last_error_string", "pa_read_device_error",
+           "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
             L.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
             L.pa_decode.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_decode_static.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P]
+            L.pa_copy_blocks.argtypes = [P, P, P, P, I32, P]
             L.pa_last_error_string.argtypes = []
             L.pa_last_error_string.restype = ctypes.c_char_p
             L.pa_read_device_error.argtypes = [P, P]
@@ -264,6 +266,13 @@ def pa_decode_static(dims: pa_dims, q, k_cache, v_cache, plan: DecodePlan, scale
                                   plan.dptr(m.off_context_lens), plan.dptr(m.off_block_tables), float(scale),
                                   _ptr(out), ctypes.byref(m), plan.dptr(m.off_items), plan.dptr(m.off_seq_items),
                                   _stream(stream)), "pa_decode_static")
+
+
+def pa_copy_blocks(dims: pa_dims, k_cache, v_cache, triples, num_triples: Optional[int] = None, stream=None):
+    """Copy the first n rows of block src to block dst (K and V) for each (src, dst, n) triple."""
+    n = int(triples.shape[0]) if num_triples is None else int(num_triples)
+    _check(lib().pa_copy_blocks(ctypes.byref(dims), _ptr(k_cache), _ptr(v_cache), _ptr(triples), n,
+                                _stream(stream)), "pa_copy_blocks")
 
 
 def pa_read_device_error(stream=None) -> int:

@@ -58,6 +58,7 @@ def compare(out_gpu: torch.Tensor, ref: np.ndarray, rows=None):
 def assert_close(out_gpu, ref, rows=None, what=""):
     assert np.isfinite(out_gpu.detach().float().cpu().numpy()).all(), f"{what}: non-finite output"
     max_abs, rrms = compare(out_gpu, ref, rows)
+    print(f"[parity] {what}: max|err|={max_abs:.3e} (bound {MAX_ABS}) rel-rms={rrms:.3e} (bound {MAX_RRMS})")
     assert max_abs <= MAX_ABS and rrms <= MAX_RRMS, f"{what}: max|err|={max_abs:.3e} rel-rms={rrms:.3e}"
     return max_abs, rrms
 
