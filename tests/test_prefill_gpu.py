@@ -143,3 +143,26 @@ def test_prefill_qwen25_full_size_sampled_rows():
     assert_close(out, ref, rows=sel, what="qwen25 prefill")
     # rows the oracle did not compute must still be finite
     assert torch.isfinite(out.float()).all()
+
+
+def test_mixed_prefill_and_decode_rows_in_one_launch():
+    """Decode rows are prefill rows with one query token: one varlen launch serves a mixed batch
+    (long-context single-token rows next to full prompts and cached-prefix suffixes)."""
+    hq, hkv, d, bs = 28, 4, 128, 16
+    lens = np.array([3000, 1, 700, 2048, 129, 999, 4096], np.int32)
+    qlens = np.array([1, 1, 700, 1, 60, 1, 300], np.int32)
+    nb = int(sum(-(-l // bs) for l in lens)) + 5
+    perm = np.random.default_rng(17).permutation(nb).astype(np.int32)
+    blocks, o = [], 0
+    for l in lens:
+        n = -(-int(l) // bs)
+        blocks.append(perm[o:o + n])
+        o += n
+    g = torch.Generator(device="cuda").manual_seed(18)
+    mk = lambda *s: torch.randn(*s, device="cuda", generator=g).to(torch.bfloat16)
+    pool = workloads.Pool(nb, bs, hkv, d, mk(nb, bs, hkv, d), mk(nb, bs, hkv, d))
+    t = int(qlens.sum())
+    batch = workloads.Batch("prefill", lens, qlens, blocks, mk(t, hq, d), mk(t, hkv, d), mk(t, hkv, d), hq, d ** -0.5)
+    w = workloads.Workload("mixed", pool, [batch])
+    batch, out, ref = _run_both(w, 0)
+    assert_close(out, ref, what="mixed prefill+decode")
