@@ -12,6 +12,9 @@ per-step citations):
   * ``gather_dense``   - block_table[pos // bs], pos % bs resolution (mini-infer §2.2-2.3)
   * ``paged_attention``- causal softmax(q K^T * scale) V, bottom-right aligned,
                          in double precision (KV-cache toy of the inference notes)
+  * ``quantize_rows`` / ``store_kvcache_int8`` / ``paged_attention_int8`` - INT8 KV
+                         cache: per-(token, KV head) symmetric codes and fp16
+                         scales, attention on the dequantised cache (nano-vLLM Q&A, Q3)
 """
 from __future__ import annotations
 
@@ -36,7 +39,8 @@ def build(force: bool = False) -> str:
         return _SO
     os.makedirs(_BUILD, exist_ok=True)
     tmp = _SO + f".{os.getpid()}.tmp"
-    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", src, "-o", tmp, "-lm"])
+    subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", src,
+                           "-o", tmp, "-lm"])
     os.replace(tmp, _SO)
     return _SO
 
@@ -58,6 +62,18 @@ def _load():
             lib.oracle_paged_attention.restype = ctypes.c_int64
             lib.oracle_paged_attention.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_double, P, P, ctypes.c_int]
+            lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+            lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+            lib.oracle_f16_to_f32.restype = ctypes.c_float
+            lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_quantize_rows.restype = None
+            lib.oracle_quantize_rows.argtypes = [P, ctypes.c_int64, ctypes.c_int, P, P]
+            lib.oracle_store_kvcache_int8.restype = None
+            lib.oracle_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+            lib.oracle_paged_attention_int8.restype = ctypes.c_int64
+            lib.oracle_paged_attention_int8.argtypes = [P, P, P, P, P, ctypes.c_int, P, P, P, P, ctypes.c_int,
+                                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, P,
+                                                        P, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -175,3 +191,65 @@ def run_batch(pool_k: np.ndarray, pool_v: np.ndarray, batch, block_size: int, ro
     store_kvcache(pool_k, pool_v, batch.k, batch.v, slots)
     return paged_attention(batch.q, pool_k, pool_v, batch.seq_lens, batch.query_lens, batch.block_lists,
                            block_size, batch.scale, row_select=row_select, num_threads=num_threads)
+
+
+# ---------------------------------------------------------------- INT8 KV cache
+
+
+def f32_to_f16(x: float) -> int:
+    return int(_load().oracle_f32_to_f16(float(x)))
+
+
+def f16_to_f32(h: int) -> float:
+    return float(_load().oracle_f16_to_f32(int(h)))
+
+
+def quantize_rows(x):
+    """bf16 [..., D] -> (int8 codes [..., D], uint16 fp16-scale bits [...])."""
+    lib = _load()
+    xb = _bits(x)
+    d = xb.shape[-1]
+    rows = xb.size // d
+    codes = np.empty(xb.shape, dtype=np.int8)
+    scales = np.empty(xb.shape[:-1], dtype=np.uint16)
+    lib.oracle_quantize_rows(_ptr(xb), rows, d, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def store_kvcache_int8(k_cache: np.ndarray, v_cache: np.ndarray, k_scale: np.ndarray, v_scale: np.ndarray,
+                       k, v, slots) -> None:
+    """In place: int8 caches [num_blocks, bs, Hkv, D], uint16 scale arrays [num_blocks, bs, Hkv]."""
+    lib = _load()
+    kb, vb, slots = _bits(k), _bits(v), _i32(slots)
+    hkv, d = k_cache.shape[2], k_cache.shape[3]
+    lib.oracle_store_kvcache_int8(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(kb),
+                                  _ptr(vb), _ptr(slots), slots.size, hkv, d)
+
+
+def paged_attention_int8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, query_lens, block_lists,
+                         block_size: int, scale: float, row_select=None, num_threads: int = 0):
+    lib = _load()
+    qb = _bits(q)
+    seq_lens, query_lens = _i32(seq_lens), _i32(query_lens)
+    off, ids = flatten_blocks(block_lists)
+    t, hq, d = qb.shape
+    hkv = k_cache.shape[2]
+    out = np.full((t, hq, d), np.nan, dtype=np.float64)
+    sel = None
+    if row_select is not None:
+        sel = np.ascontiguousarray(np.asarray(row_select, dtype=np.uint8))
+    pairs = lib.oracle_paged_attention_int8(_ptr(qb), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                            len(seq_lens), _ptr(seq_lens), _ptr(query_lens), _ptr(off), _ptr(ids),
+                                            hq, hkv, d, block_size, float(scale),
+                                            _ptr(sel) if sel is not None else None, _ptr(out), int(num_threads))
+    if pairs < 0:
+        raise ValueError("malformed paged-attention input")
+    return out, int(pairs)
+
+
+def run_batch_int8(k_cache, v_cache, k_scale, v_scale, batch, block_size: int, row_select=None):
+    """Quantising store of the batch's new K/V, then attention on the INT8 cache (mutates the caches)."""
+    slots = slot_mapping(batch.seq_lens, batch.query_lens, batch.block_lists, block_size)
+    store_kvcache_int8(k_cache, v_cache, k_scale, v_scale, batch.k, batch.v, slots)
+    return paged_attention_int8(batch.q, k_cache, v_cache, k_scale, v_scale, batch.seq_lens, batch.query_lens,
+                                batch.block_lists, block_size, batch.scale, row_select=row_select)

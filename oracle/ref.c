@@ -32,6 +32,12 @@
  *  - "vLLM / SGLang 面试源码深挖", section 4 (KV block fork): a child that
  *    appends into a shared, mutable block gets a new block holding a copy of
  *    the shared block's valid KV.
+ *  - "面试问答准备: nano-vLLM 推理引擎优化", Q3 (INT8 KV): per (token, KV
+ *    head) symmetric quantisation of the head_dim values: scale =
+ *    max(max|x| / 127, 1e-8), code = x / scale rounded half away from zero
+ *    (add +-0.5, truncate toward zero), scale kept as fp16; dequantised value
+ *    = code * scale.  Computed in fp32 as the page's kernel does, so the codes
+ *    (an integer decision) are taken in the same precision as on the GPU.
  *  - Grouped-query attention: query head h reads KV head h / (Hq / Hkv)
  *    (contiguous groups; the pages do not state the mapping, this is the
  *    plainest reading and reduces to multi-head attention when Hq == Hkv).
@@ -50,6 +56,104 @@ static double bf16_to_double(uint16_t b)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/*
+ * fp32 -> IEEE binary16, round to nearest, ties to even, written from the
+ * format's definition (1 sign, 5 exponent bits biased by 15, 10 fraction bits;
+ * subnormals below 2^-14, infinities above 65504).
+ */
+uint16_t oracle_f32_to_f16(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    const uint32_t sign = (x >> 16) & 0x8000u;
+    const int32_t exp = (int32_t)((x >> 23) & 0xffu);
+    uint32_t man = x & 0x7fffffu;
+    if (exp == 0xff)
+        return (uint16_t)(sign | 0x7c00u | (man ? 0x200u : 0u));
+    const int32_t e = exp - 127 + 15; /* biased binary16 exponent */
+    if (e >= 31)
+        return (uint16_t)(sign | 0x7c00u);
+    if (e <= 0) { /* binary16 subnormal (or zero) */
+        if (e < -10)
+            return (uint16_t)sign; /* below half the smallest subnormal */
+        man |= 0x800000u;          /* explicit leading one */
+        const uint32_t shift = (uint32_t)(14 - e);
+        uint32_t h = man >> shift;
+        const uint32_t rem = man & ((1u << shift) - 1u), half = 1u << (shift - 1u);
+        if (rem > half || (rem == half && (h & 1u)))
+            ++h; /* may carry into the exponent field: still correct */
+        return (uint16_t)(sign | h);
+    }
+    uint32_t h = sign | ((uint32_t)e << 10) | (man >> 13);
+    const uint32_t rem = man & 0x1fffu;
+    if (rem > 0x1000u || (rem == 0x1000u && (h & 1u)))
+        ++h; /* carries into the exponent (or to infinity) as rounding requires */
+    return (uint16_t)h;
+}
+
+float oracle_f16_to_f32(uint16_t h)
+{
+    const uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    const int32_t exp = (h >> 10) & 0x1f;
+    const uint32_t man = h & 0x3ffu;
+    float v;
+    if (exp == 0)
+        v = ldexpf((float)man, -24); /* subnormal: man * 2^-24 (exact in fp32) */
+    else if (exp == 31)
+        v = man ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(man | 0x400u), exp - 25);
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    u |= sign;
+    memcpy(&v, &u, sizeof v);
+    return v;
+}
+
+/*
+ * INT8 quantisation of `rows` head vectors of D bf16 values each (fp32
+ * arithmetic, IEEE division): codes [rows][D] int8, scales [rows] fp16 bits.
+ */
+void oracle_quantize_rows(const uint16_t *x, int64_t rows, int d_len, int8_t *codes, uint16_t *scales)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * d_len;
+        float amax = 0.0f;
+        for (int d = 0; d < d_len; ++d) {
+            const float v = (float)bf16_to_double(xr[d]);
+            const float a = fabsf(v);
+            if (a > amax)
+                amax = a;
+        }
+        float scale = amax / 127.0f;
+        if (scale < 1e-8f)
+            scale = 1e-8f;
+        for (int d = 0; d < d_len; ++d) {
+            const float q = (float)bf16_to_double(xr[d]) / scale;
+            const float t = q >= 0.0f ? q + 0.5f : q - 0.5f;
+            codes[r * d_len + d] = (int8_t)truncf(t);
+        }
+        scales[r] = oracle_f32_to_f16(scale);
+    }
+}
+
+/* INT8 scatter: quantise each new token's K and V head vectors into slot `slot`. */
+void oracle_store_kvcache_int8(int8_t *k_cache, int8_t *v_cache, uint16_t *k_scale, uint16_t *v_scale,
+                               const uint16_t *k, const uint16_t *v, const int32_t *slots, int64_t num_tokens,
+                               int num_kv_heads, int head_dim)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        const int32_t s = slots[t];
+        if (s == -1)
+            continue;
+        oracle_quantize_rows(k + t * row, num_kv_heads, head_dim, k_cache + (int64_t)s * row,
+                             k_scale + (int64_t)s * num_kv_heads);
+        oracle_quantize_rows(v + t * row, num_kv_heads, head_dim, v_cache + (int64_t)s * row,
+                             v_scale + (int64_t)s * num_kv_heads);
+    }
 }
 
 int oracle_max_threads(void)
@@ -137,6 +241,23 @@ void oracle_gather_dense(const uint16_t *cache, int len, const int32_t *blocks, 
     }
 }
 
+/* Same rebuild from an INT8 cache: dense value = code * fp16 scale of its (slot, head). */
+void oracle_gather_dense_int8(const int8_t *cache, const uint16_t *scales, int len, const int32_t *blocks,
+                              int num_kv_heads, int head_dim, int block_size, double *dense)
+{
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int j = 0; j < len; ++j) {
+        int64_t phys = blocks[j / block_size];
+        int64_t slot = phys * block_size + j % block_size;
+        for (int g = 0; g < num_kv_heads; ++g) {
+            const double sc = (double)oracle_f16_to_f32(scales[slot * num_kv_heads + g]);
+            for (int d = 0; d < head_dim; ++d)
+                dense[(int64_t)j * row + (int64_t)g * head_dim + d] =
+                    (double)cache[slot * row + (int64_t)g * head_dim + d] * sc;
+        }
+    }
+}
+
 /*
  * Causal attention for every query row of every sequence.
  *   q:   [sum(query_lens), Hq, D] bf16 bits, rows in sequence order
@@ -148,11 +269,11 @@ void oracle_gather_dense(const uint16_t *cache, int len, const int32_t *blocks, 
  * untouched.  Returns the number of (query row, head, key) scores computed,
  * or -1 on malformed input.
  */
-int64_t oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                               int num_seqs, const int32_t *seq_lens, const int32_t *query_lens,
-                               const int32_t *blk_off, const int32_t *blk_ids, int num_heads,
-                               int num_kv_heads, int head_dim, int block_size, double scale,
-                               const uint8_t *row_select, double *out, int num_threads)
+static int64_t attention_impl(const uint16_t *q, const void *k_cache, const void *v_cache, const uint16_t *k_scale,
+                              const uint16_t *v_scale, int is_int8, int num_seqs, const int32_t *seq_lens,
+                              const int32_t *query_lens, const int32_t *blk_off, const int32_t *blk_ids,
+                              int num_heads, int num_kv_heads, int head_dim, int block_size, double scale,
+                              const uint8_t *row_select, double *out, int num_threads)
 {
 #ifdef _OPENMP
     if (num_threads > 0)
@@ -189,8 +310,17 @@ int64_t oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const
             free(vd);
             return -1;
         }
-        oracle_gather_dense(k_cache, lk, blk_ids + blk_off[b], num_kv_heads, head_dim, block_size, kd);
-        oracle_gather_dense(v_cache, lk, blk_ids + blk_off[b], num_kv_heads, head_dim, block_size, vd);
+        if (is_int8) {
+            oracle_gather_dense_int8((const int8_t *)k_cache, k_scale, lk, blk_ids + blk_off[b], num_kv_heads,
+                                     head_dim, block_size, kd);
+            oracle_gather_dense_int8((const int8_t *)v_cache, v_scale, lk, blk_ids + blk_off[b], num_kv_heads,
+                                     head_dim, block_size, vd);
+        } else {
+            oracle_gather_dense((const uint16_t *)k_cache, lk, blk_ids + blk_off[b], num_kv_heads, head_dim,
+                                block_size, kd);
+            oracle_gather_dense((const uint16_t *)v_cache, lk, blk_ids + blk_off[b], num_kv_heads, head_dim,
+                                block_size, vd);
+        }
 
         /* step 2: causal softmax(q K^T * scale) V for each (row, head) */
         int64_t work = (int64_t)lq * num_heads;
@@ -242,4 +372,27 @@ int64_t oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const
         q_begin += lq;
     }
     return pairs;
+}
+
+int64_t oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                               int num_seqs, const int32_t *seq_lens, const int32_t *query_lens,
+                               const int32_t *blk_off, const int32_t *blk_ids, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size, double scale,
+                               const uint8_t *row_select, double *out, int num_threads)
+{
+    return attention_impl(q, k_cache, v_cache, NULL, NULL, 0, num_seqs, seq_lens, query_lens, blk_off, blk_ids,
+                          num_heads, num_kv_heads, head_dim, block_size, scale, row_select, out, num_threads);
+}
+
+/* Causal attention over an INT8 cache: the same definition on the dequantised K/V. */
+int64_t oracle_paged_attention_int8(const uint16_t *q, const int8_t *k_cache, const int8_t *v_cache,
+                                    const uint16_t *k_scale, const uint16_t *v_scale, int num_seqs,
+                                    const int32_t *seq_lens, const int32_t *query_lens, const int32_t *blk_off,
+                                    const int32_t *blk_ids, int num_heads, int num_kv_heads, int head_dim,
+                                    int block_size, double scale, const uint8_t *row_select, double *out,
+                                    int num_threads)
+{
+    return attention_impl(q, k_cache, v_cache, k_scale, v_scale, 1, num_seqs, seq_lens, query_lens, blk_off,
+                          blk_ids, num_heads, num_kv_heads, head_dim, block_size, scale, row_select, out,
+                          num_threads);
 }

@@ -302,3 +302,71 @@ def test_copy_blocks_matches_fancy_index():
         want_v[t, :n] = want_v[s, :n]
     oracle.copy_blocks(k, v, triples, bs)
     assert np.array_equal(k, want_k) and np.array_equal(v, want_v)
+
+
+# ---------------------------------------------------------------- INT8 KV cache
+
+
+def test_f16_conversion_matches_numpy():
+    rng = np.random.default_rng(41)
+    vals = np.concatenate([
+        rng.standard_normal(4000).astype(np.float32) * np.float32(3.0),
+        (rng.standard_normal(2000) * 1e-5).astype(np.float32),          # fp16 subnormals
+        (rng.standard_normal(500) * 1e-8).astype(np.float32),           # rounds to +-0 or the smallest subnormal
+        np.array([65504, 65519, 65520, 1e6, -1e6, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 1e-8, 0.0, -0.0,
+                  1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, 1.0 / 127.0], dtype=np.float32),
+    ])
+    want = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f32_to_f16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want)
+    back = np.array([oracle.f16_to_f32(int(h)) for h in want], dtype=np.float32)
+    assert np.array_equal(back, want.view(np.float16).astype(np.float32))
+
+
+def test_int8_quantize_golden():
+    fx = json.load(open(os.path.join(GOLDEN, "int8_quant_toy.json")))
+    for row in fx["rows"]:
+        x = torch.tensor([row["x"]], dtype=torch.float32).to(torch.bfloat16)
+        codes, scales = oracle.quantize_rows(x)
+        assert codes[0].tolist() == row["codes"], row["note"]
+        assert int(scales[0]) == row["scale_f16_bits"], row["note"]
+
+
+def test_int8_quantize_invariants():
+    g = torch.Generator().manual_seed(42)
+    x = (torch.randn(500, 128, generator=g) * torch.rand(500, 1, generator=g) * 10).to(torch.bfloat16)
+    codes, scales = oracle.quantize_rows(x)
+    xf = x.float().numpy()
+    amax = np.abs(xf).max(axis=1)
+    # the largest element always maps to +-127 and nothing overflows
+    assert np.abs(codes).max() <= 127
+    assert (np.abs(codes).max(axis=1) == 127).all()
+    # dequantised with the fp32 scale, every value is within half a step (plus the fp32
+    # rounding of x / scale, which can move an exact ratio of k + 0.4999... onto k + 0.5)
+    s32 = np.maximum(amax / np.float32(127.0), np.float32(1e-8)).astype(np.float32)
+    err = np.abs(codes.astype(np.float64) * s32[:, None] - xf.astype(np.float64)) / s32[:, None]
+    assert err.max() <= 0.5 + 1e-4
+    # the stored scale is the fp16 rounding of that scale
+    assert np.array_equal(scales, s32.astype(np.float16).view(np.uint16))
+
+
+def test_int8_attention_matches_brute_force_on_dequantised_cache():
+    c = _identity_case(43, num_seqs=3, hq=4, hkv=2, d=16, bs=4, max_len=20, cached=True)
+    nb, bs, hkv, d = c["pool_k"].shape
+    kc8, ks = oracle.quantize_rows(c["pool_k"])
+    vc8, vs = oracle.quantize_rows(c["pool_v"])
+    kc8, vc8, ks, vs = kc8.copy(), vc8.copy(), ks.copy(), vs.copy()
+    slots = oracle.slot_mapping(c["lens"], c["qlens"], c["blocks"], bs)
+    oracle.store_kvcache_int8(kc8, vc8, ks, vs, c["k"], c["v"], slots)
+    out, _ = oracle.paged_attention_int8(c["q"], kc8, vc8, ks, vs, c["lens"], c["qlens"], c["blocks"], bs, c["scale"])
+    # independent dequantisation: numpy's fp16 -> fp32, identity block layout (plain slices)
+    kd = (kc8.astype(np.float64) * ks.view(np.float16).astype(np.float64)[..., None]).reshape(-1, hkv, d)
+    vd = (vc8.astype(np.float64) * vs.view(np.float16).astype(np.float64)[..., None]).reshape(-1, hkv, d)
+    t0 = 0
+    for b in range(3):
+        lk, lq = int(c["lens"][b]), int(c["qlens"][b])
+        s0 = int(c["starts"][b]) * bs
+        qb = _f64(c["q"][t0:t0 + lq]).tolist()
+        ref = np.array(brute.attention(qb, kd[s0:s0 + lk].tolist(), vd[s0:s0 + lk].tolist(), c["scale"]))
+        np.testing.assert_allclose(out[t0:t0 + lq], ref, rtol=0, atol=1e-12)
+        t0 += lq
