@@ -69,7 +69,8 @@ def _load():
             lib.oracle_quantize_rows.restype = None
             lib.oracle_quantize_rows.argtypes = [P, ctypes.c_int64, ctypes.c_int, P, P]
             lib.oracle_store_kvcache_int8.restype = None
-            lib.oracle_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+            lib.oracle_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                      ctypes.c_int]
             lib.oracle_paged_attention_int8.restype = ctypes.c_int64
             lib.oracle_paged_attention_int8.argtypes = [P, P, P, P, P, ctypes.c_int, P, P, P, P, ctypes.c_int,
                                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, P,
@@ -218,12 +219,13 @@ def quantize_rows(x):
 
 def store_kvcache_int8(k_cache: np.ndarray, v_cache: np.ndarray, k_scale: np.ndarray, v_scale: np.ndarray,
                        k, v, slots) -> None:
-    """In place: int8 caches [num_blocks, bs, Hkv, D], uint16 scale arrays [num_blocks, bs, Hkv]."""
+    """In place: int8 caches [num_blocks, bs, Hkv, D], uint16 (fp16 bits) scales [num_blocks, Hkv, bs]."""
     lib = _load()
     kb, vb, slots = _bits(k), _bits(v), _i32(slots)
-    hkv, d = k_cache.shape[2], k_cache.shape[3]
+    bs, hkv, d = k_cache.shape[1], k_cache.shape[2], k_cache.shape[3]
+    assert k_scale.shape == (k_cache.shape[0], hkv, bs)
     lib.oracle_store_kvcache_int8(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(kb),
-                                  _ptr(vb), _ptr(slots), slots.size, hkv, d)
+                                  _ptr(vb), _ptr(slots), slots.size, hkv, d, bs)
 
 
 def paged_attention_int8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, query_lens, block_lists,

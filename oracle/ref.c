@@ -139,20 +139,30 @@ void oracle_quantize_rows(const uint16_t *x, int64_t rows, int d_len, int8_t *co
     }
 }
 
-/* INT8 scatter: quantise each new token's K and V head vectors into slot `slot`. */
+/*
+ * INT8 scatter: quantise each new token's K and V head vectors into its slot.
+ * Codes use the data layout [num_blocks][block_size][num_kv_heads][head_dim];
+ * scales are stored head-major inside a block, [num_blocks][num_kv_heads]
+ * [block_size] (the pages fix no layout for them; per-head token runs are
+ * then contiguous).
+ */
 void oracle_store_kvcache_int8(int8_t *k_cache, int8_t *v_cache, uint16_t *k_scale, uint16_t *v_scale,
                                const uint16_t *k, const uint16_t *v, const int32_t *slots, int64_t num_tokens,
-                               int num_kv_heads, int head_dim)
+                               int num_kv_heads, int head_dim, int block_size)
 {
     const int64_t row = (int64_t)num_kv_heads * head_dim;
     for (int64_t t = 0; t < num_tokens; ++t) {
         const int32_t s = slots[t];
         if (s == -1)
             continue;
-        oracle_quantize_rows(k + t * row, num_kv_heads, head_dim, k_cache + (int64_t)s * row,
-                             k_scale + (int64_t)s * num_kv_heads);
-        oracle_quantize_rows(v + t * row, num_kv_heads, head_dim, v_cache + (int64_t)s * row,
-                             v_scale + (int64_t)s * num_kv_heads);
+        const int64_t blk = s / block_size, off = s % block_size;
+        for (int g = 0; g < num_kv_heads; ++g) {
+            const int64_t si = (blk * num_kv_heads + g) * block_size + off;
+            oracle_quantize_rows(k + t * row + (int64_t)g * head_dim, 1, head_dim,
+                                 k_cache + (int64_t)s * row + (int64_t)g * head_dim, k_scale + si);
+            oracle_quantize_rows(v + t * row + (int64_t)g * head_dim, 1, head_dim,
+                                 v_cache + (int64_t)s * row + (int64_t)g * head_dim, v_scale + si);
+        }
     }
 }
 
@@ -250,7 +260,7 @@ void oracle_gather_dense_int8(const int8_t *cache, const uint16_t *scales, int l
         int64_t phys = blocks[j / block_size];
         int64_t slot = phys * block_size + j % block_size;
         for (int g = 0; g < num_kv_heads; ++g) {
-            const double sc = (double)oracle_f16_to_f32(scales[slot * num_kv_heads + g]);
+            const double sc = (double)oracle_f16_to_f32(scales[(phys * num_kv_heads + g) * block_size + j % block_size]);
             for (int d = 0; d < head_dim; ++d)
                 dense[(int64_t)j * row + (int64_t)g * head_dim + d] =
                     (double)cache[slot * row + (int64_t)g * head_dim + d] * sc;

@@ -350,18 +350,38 @@ def test_int8_quantize_invariants():
     assert np.array_equal(scales, s32.astype(np.float16).view(np.uint16))
 
 
+def test_int8_store_scale_layout_head_major():
+    """A token's scale for head g sits at [block][g][offset]; its codes at [block][offset][g]."""
+    nb, bs, hkv, d = 3, 4, 2, 8
+    kc = np.zeros((nb, bs, hkv, d), np.int8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((nb, hkv, bs), np.uint16)
+    vs = np.zeros_like(ks)
+    k = torch.zeros(1, hkv, d)
+    k[0, 0, 0], k[0, 1, 0] = 127.0, 254.0  # scales 1.0 and 2.0
+    k = k.to(torch.bfloat16)
+    oracle.store_kvcache_int8(kc, vc, ks, vs, k, k, [2 * bs + 3])  # block 2, offset 3
+    assert ks[2, 0, 3] == 0x3C00 and ks[2, 1, 3] == 0x4000
+    assert kc[2, 3, 0, 0] == 127 and kc[2, 3, 1, 0] == 127
+    assert np.count_nonzero(ks) == 2 and np.count_nonzero(kc) == 2
+
+
 def test_int8_attention_matches_brute_force_on_dequantised_cache():
     c = _identity_case(43, num_seqs=3, hq=4, hkv=2, d=16, bs=4, max_len=20, cached=True)
     nb, bs, hkv, d = c["pool_k"].shape
-    kc8, ks = oracle.quantize_rows(c["pool_k"])
+    kc8, ks = oracle.quantize_rows(c["pool_k"])  # scales [nb, bs, hkv]
     vc8, vs = oracle.quantize_rows(c["pool_v"])
-    kc8, vc8, ks, vs = kc8.copy(), vc8.copy(), ks.copy(), vs.copy()
+    # cache scales are head-major inside a block: [nb, hkv, bs]
+    kc8, vc8 = kc8.copy(), vc8.copy()
+    ks, vs = np.ascontiguousarray(ks.transpose(0, 2, 1)), np.ascontiguousarray(vs.transpose(0, 2, 1))
     slots = oracle.slot_mapping(c["lens"], c["qlens"], c["blocks"], bs)
     oracle.store_kvcache_int8(kc8, vc8, ks, vs, c["k"], c["v"], slots)
     out, _ = oracle.paged_attention_int8(c["q"], kc8, vc8, ks, vs, c["lens"], c["qlens"], c["blocks"], bs, c["scale"])
     # independent dequantisation: numpy's fp16 -> fp32, identity block layout (plain slices)
-    kd = (kc8.astype(np.float64) * ks.view(np.float16).astype(np.float64)[..., None]).reshape(-1, hkv, d)
-    vd = (vc8.astype(np.float64) * vs.view(np.float16).astype(np.float64)[..., None]).reshape(-1, hkv, d)
+    ksd = ks.transpose(0, 2, 1).view(np.float16).astype(np.float64)
+    vsd = vs.transpose(0, 2, 1).view(np.float16).astype(np.float64)
+    kd = (kc8.astype(np.float64) * ksd[..., None]).reshape(-1, hkv, d)
+    vd = (vc8.astype(np.float64) * vsd[..., None]).reshape(-1, hkv, d)
     t0 = 0
     for b in range(3):
         lk, lq = int(c["lens"][b]), int(c["qlens"][b])
