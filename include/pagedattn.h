@@ -217,6 +217,54 @@ int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const voi
 int pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache, const int32_t *triples,
                    int32_t num_triples, pa_stream_t stream);
 
+/* ------------------------------------------------------------------ INT8 KV cache */
+
+/*
+ * INT8 cache variant.  Source: "面试问答准备: nano-vLLM 推理引擎优化", Q3
+ * (KV cache quantisation): each token's K (and V) vector of one KV head is
+ * stored as int8 codes with one scale, scale = max|x| / 127, code =
+ * round(x / scale); the attention kernel dequantises (code * scale) as it
+ * loads, so decode reads half the bytes of the bf16 cache.  The pages fix no
+ * rounding rule or scale type; this library reads them as: fp32 arithmetic
+ * with IEEE division, scale floored at 1e-8 (an all-zero vector), rounding
+ * half away from zero, scale stored as fp16 (round to nearest even) and the
+ * dequantised value being code * (fp16 scale).
+ *
+ * Layout (per layer; both owned by the caller):
+ *   k_cache, v_cache: int8  [num_blocks][block_size][num_kv_heads][head_dim]
+ *                     (the bf16 layout with 1-byte elements)
+ *   k_scale, v_scale: fp16  [num_blocks][num_kv_heads][block_size]
+ *                     (head-major inside a block: one head's scales for a
+ *                     run of tokens are contiguous)
+ * All four pointers must be 16-byte aligned.
+ */
+
+/*
+ * pa_store_kvcache_int8 — quantising scatter: for each token t with
+ * slot_mapping[t] != -1, quantise k[t][g][:] and v[t][g][:] (bf16) for every
+ * KV head g into the codes of row slot and the scales at
+ * [slot / block_size][g][slot % block_size].  Codes and scales are
+ * deterministic (bit-identical on every run).  Slots outside [-1, num_slots)
+ * are skipped and flagged (pa_read_device_error bit 0).
+ */
+int pa_store_kvcache_int8(const pa_dims *dims, const void *k, const void *v, void *k_cache, void *v_cache,
+                          void *k_scale, void *v_scale, const int32_t *slot_mapping, int32_t num_tokens,
+                          pa_stream_t stream);
+
+/*
+ * pa_decode_int8 — pa_decode over an INT8 cache: the same plan
+ * (pa_pack_decode), arguments, workspace and result, with the cached K and V
+ * read as code * scale.  Internally the codes (exact in fp16) and q (rounded
+ * to fp16; exact for bf16 magnitudes in [2^-14, 65504], clamped to +-65504)
+ * feed fp16 tensor-core products with fp32 accumulation; the V scale is
+ * applied to the softmax weights before the P.V product.
+ */
+int pa_decode_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                   const void *k_scale, const void *v_scale, const int32_t *context_lens,
+                   const int32_t *block_tables, float scale, void *out, const pa_decode_meta *meta,
+                   const int32_t *items, const int32_t *seq_items, void *workspace, size_t workspace_bytes,
+                   pa_stream_t stream);
+
 /*
  * pa_decode_static — pa_decode for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point: it exists for callers

@@ -134,11 +134,14 @@ extern "C" int pa_prefill_varlen(const pa_dims *dims, const void *q, const void 
     return launch_prefill(a, stream);
 }
 
-extern "C" int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
-                         const int32_t *context_lens, const int32_t *block_tables, float scale, void *out,
-                         const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items, void *workspace,
-                         size_t workspace_bytes, pa_stream_t stream)
+// Host-side checks shared by pa_decode and pa_decode_int8; fills `a`.  Sets
+// *nothing when the plan has no work (then no launch happens).
+static int prepare_decode(const char *fn, const pa_dims *dims, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *context_lens, const int32_t *block_tables, float scale,
+                          void *out, const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items,
+                          void *workspace, size_t workspace_bytes, DecodeArgs *a, bool *nothing)
 {
+    *nothing = false;
     int rc = check_dims(dims);
     if (rc != PA_OK)
         return rc;
@@ -148,27 +151,29 @@ extern "C" int pa_decode(const pa_dims *dims, const void *q, const void *k_cache
         return fail(PA_ERR_INVALID_ARG, "malformed decode meta");
     if (!(scale > 0.f) || !std::isfinite(scale))
         return fail(PA_ERR_INVALID_ARG, "scale must be finite and > 0");
-    if (meta->num_items == 0)
+    if (meta->num_items == 0) {
+        *nothing = true;
         return PA_OK;
+    }
     if (!q || !k_cache || !v_cache || !context_lens || !block_tables || !out || !items || !seq_items)
-        return fail(PA_ERR_INVALID_ARG, "pa_decode: NULL pointer");
+        return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", fn);
     if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
-        return fail(PA_ERR_INVALID_ARG, "pa_decode: tensors must be 16-byte aligned");
+        return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
     if (workspace_bytes < meta->workspace_bytes)
         return fail(PA_ERR_WORKSPACE, "decode workspace has %zu bytes, needs %llu", workspace_bytes,
                     (unsigned long long)meta->workspace_bytes);
     if (meta->workspace_bytes > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return fail(PA_ERR_INVALID_ARG, "decode workspace must be non-NULL and 256-byte aligned");
-    DecodeArgs a{};
-    a.dims = *dims;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.context_lens = context_lens;
-    a.block_tables = block_tables;
-    a.items = items;
-    a.seq_items = seq_items;
-    a.out = out;
+    *a = DecodeArgs{};
+    a->dims = *dims;
+    a->q = q;
+    a->k_cache = k_cache;
+    a->v_cache = v_cache;
+    a->context_lens = context_lens;
+    a->block_tables = block_tables;
+    a->items = items;
+    a->seq_items = seq_items;
+    a->out = out;
     if (meta->num_partials < 0)
         return fail(PA_ERR_INVALID_ARG, "malformed decode meta");
     if (meta->num_partials > 0) {
@@ -177,16 +182,71 @@ extern "C" int pa_decode(const pa_dims *dims, const void *q, const void *k_cache
                       align_up((size_t)meta->num_partials * dims->num_heads * 4, 256);
         if (need > meta->workspace_bytes)
             return fail(PA_ERR_INVALID_ARG, "decode meta workspace size inconsistent with its partial count");
-        a.part_o = static_cast<float *>(workspace);
-        a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               align_up((size_t)meta->num_partials * per, 256));
+        a->part_o = static_cast<float *>(workspace);
+        a->part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                                align_up((size_t)meta->num_partials * per, 256));
     }
-    a.scale = scale;
-    a.num_seqs = meta->num_seqs;
-    a.num_items = meta->num_items;
-    a.max_blocks_per_seq = meta->max_blocks_per_seq;
-    a.max_splits = meta->max_splits;
+    a->scale = scale;
+    a->num_seqs = meta->num_seqs;
+    a->num_items = meta->num_items;
+    a->max_blocks_per_seq = meta->max_blocks_per_seq;
+    a->max_splits = meta->max_splits;
+    return PA_OK;
+}
+
+extern "C" int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *context_lens, const int32_t *block_tables, float scale, void *out,
+                         const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items, void *workspace,
+                         size_t workspace_bytes, pa_stream_t stream)
+{
+    DecodeArgs a;
+    bool nothing = false;
+    int rc = prepare_decode("pa_decode", dims, q, k_cache, v_cache, context_lens, block_tables, scale, out, meta,
+                            items, seq_items, workspace, workspace_bytes, &a, &nothing);
+    if (rc != PA_OK || nothing)
+        return rc;
     return launch_decode(a, stream);
+}
+
+extern "C" int pa_store_kvcache_int8(const pa_dims *dims, const void *k, const void *v, void *k_cache,
+                                     void *v_cache, void *k_scale, void *v_scale, const int32_t *slot_mapping,
+                                     int32_t num_tokens, pa_stream_t stream)
+{
+    int rc = check_dims(dims);
+    if (rc != PA_OK)
+        return rc;
+    if (num_tokens < 0)
+        return fail(PA_ERR_INVALID_ARG, "num_tokens < 0");
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !k_scale || !v_scale || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "pa_store_kvcache_int8: NULL pointer");
+    if (misaligned(k) || misaligned(v) || misaligned(k_cache) || misaligned(v_cache) || misaligned(k_scale) ||
+        misaligned(v_scale))
+        return fail(PA_ERR_INVALID_ARG, "pa_store_kvcache_int8: tensors must be 16-byte aligned");
+    return launch_store_kvcache_int8(*dims, k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping, num_tokens,
+                                     stream);
+}
+
+extern "C" int pa_decode_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                              const void *k_scale, const void *v_scale, const int32_t *context_lens,
+                              const int32_t *block_tables, float scale, void *out, const pa_decode_meta *meta,
+                              const int32_t *items, const int32_t *seq_items, void *workspace,
+                              size_t workspace_bytes, pa_stream_t stream)
+{
+    DecodeArgs a;
+    bool nothing = false;
+    int rc = prepare_decode("pa_decode_int8", dims, q, k_cache, v_cache, context_lens, block_tables, scale, out,
+                            meta, items, seq_items, workspace, workspace_bytes, &a, &nothing);
+    if (rc != PA_OK || nothing)
+        return rc;
+    if (!k_scale || !v_scale)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_int8: NULL scale pointer");
+    if (misaligned(k_scale) || misaligned(v_scale))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_int8: scales must be 16-byte aligned");
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return launch_decode_int8(a, stream);
 }
 
 extern "C" int pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache, const int32_t *triples,

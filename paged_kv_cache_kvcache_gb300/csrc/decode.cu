@@ -338,15 +338,7 @@ int launch_split(const DecodeArgs &a, const DecParams &p, cudaStream_t stream)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
-    if (a.part_o) {
-        dim3 cg((unsigned)a.num_seqs, (unsigned)((a.dims.num_heads + 3) / 4));
-        decode_combine_kernel<D><<<cg, 128, 0, stream>>>(a.part_o, a.part_lse, a.seq_items,
-                                                         static_cast<__nv_bfloat16 *>(a.out), a.dims.num_heads);
-        e = cudaGetLastError();
-        if (e != cudaSuccess)
-            return fail(PA_ERR_CUDA, "decode combine launch: %s", cudaGetErrorString(e));
-    }
-    return PA_OK;
+    return launch_decode_combine(a, stream);
 }
 
 template <int D, int NT>
@@ -364,6 +356,20 @@ int occupancy()
 }
 
 } // namespace
+
+int launch_decode_combine(const DecodeArgs &a, void *stream)
+{
+    if (!a.part_o)
+        return PA_OK;
+    dim3 cg((unsigned)a.num_seqs, (unsigned)((a.dims.num_heads + 3) / 4));
+    auto kern = a.dims.head_dim == 128 ? decode_combine_kernel<128> : decode_combine_kernel<64>;
+    kern<<<cg, 128, 0, static_cast<cudaStream_t>(stream)>>>(a.part_o, a.part_lse, a.seq_items,
+                                                            static_cast<__nv_bfloat16 *>(a.out), a.dims.num_heads);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "decode combine launch: %s", cudaGetErrorString(e));
+    return PA_OK;
+}
 
 int launch_decode(const DecodeArgs &a, void *stream)
 {

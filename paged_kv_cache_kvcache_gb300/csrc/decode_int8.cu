@@ -1,0 +1,419 @@
+// Batched single-token GQA decode over an INT8 paged KV cache, dequantisation
+// fused into the attention loads; split-KV + LSE combine as in the bf16 decode.
+//
+// Sources (page title, section):
+//  - "面试问答准备: nano-vLLM 推理引擎优化", Q3 (KV cache quantisation): K and
+//    V are kept as int8 codes with one scale per token and KV head; the
+//    attention kernel dequantises as it reads, so decode moves half the bytes
+//    of the bf16 cache.  The cached value is code * scale.
+//  - the same page's Q3 follow-ups (Split-K with a log-sum-exp merge), and
+//    "推理系统", "瓶颈不是算力，是带宽" (decode time = bytes read / bandwidth).
+//
+// GB300 design.  Work items, CTA/warp decomposition, cp.async pipeline,
+// online softmax, warp merge and partial format are those of the bf16 decode;
+// what changes is the operand path:
+//  * 16-token chunks of int8 codes (D bytes per token row) plus the chunk's 16
+//    K and 16 V fp16 scales are staged with 16-byte cp.async; a tail chunk's
+//    missing tokens (codes and scales) are zero-filled by the copy itself.
+//  * A code x converts to fp16 exactly: the bit pattern 0x6400 | (x + 128) is
+//    1024 + x + 128, minus 1152 gives x (one prmt + one f16x2 subtract per
+//    pair).  Both MMAs therefore run as f16 m16n8k16 with fp32 accumulation:
+//        S^T[16 tok x 8 heads] = K_codes . Q^T,  then s *= k_scale[tok]
+//        O^T[D x 8 heads]     += V_codes^T . (P * v_scale[tok])^T
+//    The softmax normaliser sums the unscaled P.  P * v_scale never exceeds
+//    the fp16 scale itself (P <= 1), so it stays in fp16 range.
+//  * Q is rounded to fp16 once per CTA (exact for bf16 values of magnitude in
+//    [2^-14, 65504], clamped beyond).
+//  * Operand order: the MMA contraction and the O^T rows may be permuted at
+//    will (undone when O is written), so each lane's K codes for all k-steps
+//    are one contiguous run of its token row (two 16-byte loads), and its V
+//    codes for all d-tiles are one contiguous run of each of its four token
+//    rows.  Byte interleaving for V's token pairs is one prmt per word.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct DecLayout8 {
+    static constexpr int kChunkBytes = 16 * D;        // 16 tokens of int8 codes
+    static constexpr int kScaleOff = 2 * kChunkBytes; // K codes, V codes, 16 K scales, 16 V scales
+    static constexpr int kStageBytes = 2 * kChunkBytes + 64;
+    static constexpr int kWarpBytes = kStages * kStageBytes;
+    static constexpr int kSmemBytes = kWarps * kWarpBytes;
+    static constexpr int kVecPerRow = D / 16; // 16-byte vectors per token row
+};
+
+// Byte offset of 16-byte vector v of token t inside a staged chunk.  XOR
+// swizzles make every fragment load below conflict-free: D = 128 keeps one
+// token per 128-byte line, D = 64 two tokens per line.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int t, int v)
+{
+    if constexpr (D == 128)
+        return (uint32_t)(t * 128 + ((v ^ (t & 7)) << 4));
+    else
+        return (uint32_t)((t >> 1) * 128 + (((((t & 1) << 2) | v) ^ (((t >> 1) & 3) << 1)) << 4));
+}
+
+constexpr uint32_t kFlip = 0x80808080u;  // int8 -> offset binary (x + 128), per byte
+constexpr uint32_t kLoPair = 0x4140u;    // prmt: bytes 0, 1 under 0x64 high bytes
+constexpr uint32_t kHiPair = 0x4342u;    // prmt: bytes 2, 3 under 0x64 high bytes
+constexpr uint32_t kMagic = 0x64806480u; // f16x2 (1152, 1152)
+
+// Two offset-binary codes of u (chosen by sel) -> f16x2 of the signed codes, exact.
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u, uint32_t sel)
+{
+    return ptx::sub_f16x2(ptx::prmt(u, 0x64646464u, sel), kMagic);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+{
+    const float lo = fminf(fmaxf(__uint_as_float(w << 16), -65504.f), 65504.f);
+    const float hi = fminf(fmaxf(__uint_as_float(w & 0xffff0000u), -65504.f), 65504.f);
+    return ptx::pack_f16(lo, hi);
+}
+
+__device__ __forceinline__ float lds_half(uint32_t addr) { return __half2float(__ushort_as_half(ptx::lds_u16(addr))); }
+
+struct DecParams8 {
+    const __nv_bfloat16 *q;
+    const int8_t *k_cache;
+    const int8_t *v_cache;
+    const __half *k_scale;
+    const __half *v_scale;
+    const int32_t *block_tables;
+    const int4 *items;
+    __nv_bfloat16 *out;
+    float *part_o;
+    float *part_lse;
+    float scale_log2;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t group;
+    int32_t block_size;
+    int32_t max_blocks;
+};
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecParams8 p)
+{
+    using L = DecLayout8<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r = lane >> 2, c = lane & 3;
+    const int4 item = p.items[blockIdx.x];
+    const int b = item.x, k0 = item.y, k1 = item.z, pslot = item.w;
+    const int g = blockIdx.y;
+    const int G = p.group;
+    const int Hq = p.num_heads;
+
+    // Q^T fragments (f16), B operand of the score MMA.  k-step kk of lane c
+    // covers d = c*D/4 + 4kk + {0,1} (logical k 2c, 2c+1) and + {2,3} (2c+8, 2c+9).
+    uint32_t qf[NT][D / 16][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hl = nt * 8 + r;
+        const bool valid = hl < G;
+        const uint2 *qrow = reinterpret_cast<const uint2 *>(
+            p.q + ((size_t)b * Hq + (size_t)g * G + (valid ? hl : 0)) * D + c * (D / 4));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint2 w = valid ? __ldg(qrow + kk) : make_uint2(0u, 0u);
+            qf[nt][kk][0] = bf16x2_to_f16x2(w.x);
+            qf[nt][kk][1] = bf16x2_to_f16x2(w.y);
+        }
+    }
+
+    const int nchunks = (k1 - k0 + 15) >> 4;
+    const int my_n = nchunks > warp ? (nchunks - warp + kWarps - 1) / kWarps : 0;
+    const uint32_t wbase = ptx::smem_u32(smem) + warp * L::kWarpBytes;
+    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks;
+    const int bs = p.block_size;
+    const int Hkv = p.num_kv_heads;
+    int blk_cache = 0;
+
+    auto issue = [&](int i) {
+        if ((i & 31) == 0) { // refresh the block ids of local chunks i .. i+31, one per lane
+            const int key = k0 + 16 * (warp + kWarps * (i + lane));
+            blk_cache = key < k1 ? __ldg(bt_row + key / bs) : 0;
+        }
+        const int phys = __shfl_sync(0xffffffffu, blk_cache, i & 31);
+        const int key0 = k0 + 16 * (warp + kWarps * i);
+        const int off0 = key0 & (bs - 1); // a chunk never crosses a block (bs >= 16, key0 % 16 == 0)
+        const int64_t row0 = (int64_t)phys * bs + off0;
+        const uint32_t sbase = wbase + (i % kStages) * L::kStageBytes;
+#pragma unroll
+        for (int e = lane; e < 16 * L::kVecPerRow; e += 32) {
+            const int t = e / L::kVecPerRow;
+            const int v = e % L::kVecPerRow;
+            const bool valid = key0 + t < k1;
+            const size_t off = ((size_t)(row0 + t) * Hkv + g) * D + v * 16;
+            const uint32_t dst = sbase + swz<D>(t, v);
+            ptx::cp_async_16(dst, valid ? (const void *)(p.k_cache + off) : (const void *)p.k_cache, valid ? 16u : 0u);
+            ptx::cp_async_16(dst + L::kChunkBytes, valid ? (const void *)(p.v_cache + off) : (const void *)p.v_cache,
+                             valid ? 16u : 0u);
+        }
+        if (lane < 4) { // scales: lanes 0/1 K tokens 0-7/8-15, lanes 2/3 the same for V; missing tokens read 0
+            const int h = lane & 1;
+            const int n = min(max(k1 - key0 - 8 * h, 0), 8);
+            const __half *base = lane < 2 ? p.k_scale : p.v_scale;
+            const size_t si = ((size_t)phys * Hkv + g) * bs + off0 + 8 * h;
+            ptx::cp_async_16(sbase + L::kScaleOff + lane * 16, n ? (const void *)(base + si) : (const void *)base,
+                             (uint32_t)(2 * n));
+        }
+    };
+
+    float acc[NT][D / 16][4];
+    float m_r[NT][2], l_r[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_r[nt][0] = m_r[nt][1] = -INFINITY;
+        l_r[nt][0] = l_r[nt][1] = 0.f;
+#pragma unroll
+        for (int mi = 0; mi < D / 16; ++mi)
+            acc[nt][mi][0] = acc[nt][mi][1] = acc[nt][mi][2] = acc[nt][mi][3] = 0.f;
+    }
+
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < my_n)
+            issue(s);
+        ptx::cp_async_commit();
+    }
+
+    for (int i = 0; i < my_n; ++i) {
+        __syncwarp();
+        if (i + kStages - 1 < my_n)
+            issue(i + kStages - 1);
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<kStages - 1>();
+        __syncwarp();
+
+        const uint32_t kb = wbase + (i % kStages) * L::kStageBytes;
+        const uint32_t vb = kb + L::kChunkBytes;
+        const uint32_t sb = kb + L::kScaleOff;
+        const int key0 = k0 + 16 * (warp + kWarps * i);
+
+        // K codes of tokens r and r + 8: bytes [c*D/4, (c+1)*D/4) of each row
+        uint32_t kw[2][D / 16];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = r + 8 * h;
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x) {
+                const uint4 u = ptx::lds_v4(kb + swz<D>(t, (D / 64) * c + x));
+                kw[h][4 * x] = u.x, kw[h][4 * x + 1] = u.y, kw[h][4 * x + 2] = u.z, kw[h][4 * x + 3] = u.w;
+            }
+        }
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t u0 = kw[0][kk] ^ kFlip, u1 = kw[1][kk] ^ kFlip;
+            const uint32_t a0 = codes_to_f16x2(u0, kLoPair), a2 = codes_to_f16x2(u0, kHiPair);
+            const uint32_t a1 = codes_to_f16x2(u1, kLoPair), a3 = codes_to_f16x2(u1, kHiPair);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                ptx::mma_16816_f16(sc[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+        }
+
+        const float ks0 = lds_half(sb + 2 * r) * p.scale_log2;
+        const float ks1 = lds_half(sb + 2 * (r + 8)) * p.scale_log2;
+        const float vs0 = lds_half(sb + 32 + 2 * r);
+        const float vs1 = lds_half(sb + 32 + 2 * (r + 8));
+        const bool v0 = key0 + r < k1;
+        const bool v1 = key0 + r + 8 < k1;
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float s0 = v0 ? sc[nt][0] * ks0 : -INFINITY;
+            const float s1 = v0 ? sc[nt][1] * ks0 : -INFINITY;
+            const float s2 = v1 ? sc[nt][2] * ks1 : -INFINITY;
+            const float s3 = v1 ? sc[nt][3] * ks1 : -INFINITY;
+            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m_r[nt][0], mx0), mn1 = fmaxf(m_r[nt][1], mx1);
+            const float al0 = ptx::ex2(m_r[nt][0] - mn0), al1 = ptx::ex2(m_r[nt][1] - mn1);
+            m_r[nt][0] = mn0;
+            m_r[nt][1] = mn1;
+            const float p0 = ptx::ex2(s0 - mn0), p1 = ptx::ex2(s1 - mn1);
+            const float p2 = ptx::ex2(s2 - mn0), p3 = ptx::ex2(s3 - mn1);
+            l_r[nt][0] = l_r[nt][0] * al0 + p0 + p2;
+            l_r[nt][1] = l_r[nt][1] * al1 + p1 + p3;
+#pragma unroll
+            for (int mi = 0; mi < D / 16; ++mi) {
+                acc[nt][mi][0] *= al0;
+                acc[nt][mi][1] *= al1;
+                acc[nt][mi][2] *= al0;
+                acc[nt][mi][3] *= al1;
+            }
+            pb[nt][0] = ptx::movmatrix_trans(ptx::pack_f16(p0 * vs0, p1 * vs0));
+            pb[nt][1] = ptx::movmatrix_trans(ptx::pack_f16(p2 * vs1, p3 * vs1));
+        }
+
+        // V codes of tokens 2c, 2c+1, 2c+8, 2c+9: bytes [r*D/8, (r+1)*D/8) of each
+        // row.  Byte 2*mi + hi of that run is d-row (mi, r + 8*hi) of O^T tile mi.
+        uint32_t vw[4][D / 32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = 2 * c + (j & 1) + 8 * (j >> 1);
+            if constexpr (D == 128) {
+                const uint4 u = ptx::lds_v4(vb + swz<D>(t, r));
+                vw[j][0] = u.x, vw[j][1] = u.y, vw[j][2] = u.z, vw[j][3] = u.w;
+            } else {
+                const uint2 u = ptx::lds_v2(vb + swz<D>(t, r >> 1) + (r & 1) * 8);
+                vw[j][0] = u.x, vw[j][1] = u.y;
+            }
+        }
+#pragma unroll
+        for (int w = 0; w < D / 32; ++w) {
+            // token pairs (2c, 2c+1) and (2c+8, 2c+9) interleaved byte by byte
+            const uint32_t x01 = ptx::prmt(vw[0][w], vw[1][w], 0x5140u) ^ kFlip; // tile 2w
+            const uint32_t y01 = ptx::prmt(vw[0][w], vw[1][w], 0x7362u) ^ kFlip; // tile 2w + 1
+            const uint32_t x89 = ptx::prmt(vw[2][w], vw[3][w], 0x5140u) ^ kFlip;
+            const uint32_t y89 = ptx::prmt(vw[2][w], vw[3][w], 0x7362u) ^ kFlip;
+            {
+                const uint32_t a0 = codes_to_f16x2(x01, kLoPair), a1 = codes_to_f16x2(x01, kHiPair);
+                const uint32_t a2 = codes_to_f16x2(x89, kLoPair), a3 = codes_to_f16x2(x89, kHiPair);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    ptx::mma_16816_f16(acc[nt][2 * w], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+            {
+                const uint32_t a0 = codes_to_f16x2(y01, kLoPair), a1 = codes_to_f16x2(y01, kHiPair);
+                const uint32_t a2 = codes_to_f16x2(y89, kLoPair), a3 = codes_to_f16x2(y89, kHiPair);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    ptx::mma_16816_f16(acc[nt][2 * w + 1], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+        }
+    }
+    ptx::cp_async_wait<0>();
+
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1)
+                l_r[nt][j] += __shfl_xor_sync(0xffffffffu, l_r[nt][j], o);
+
+    // merge the 4 warps through shared memory (pipeline buffers are free now)
+    __syncthreads();
+    constexpr int H8 = 8 * NT;
+    float *mrg_m = reinterpret_cast<float *>(smem);
+    float *mrg_l = mrg_m + kWarps * H8;
+    float *mrg_o = mrg_l + kWarps * H8; // [warp][head][D], d in natural order
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int h0 = nt * 8 + 2 * c;
+        if (lane < 4) {
+            mrg_m[warp * H8 + h0] = m_r[nt][0];
+            mrg_m[warp * H8 + h0 + 1] = m_r[nt][1];
+            mrg_l[warp * H8 + h0] = l_r[nt][0];
+            mrg_l[warp * H8 + h0 + 1] = l_r[nt][1];
+        }
+#pragma unroll
+        for (int mi = 0; mi < D / 16; ++mi) {
+            const int d = r * (D / 8) + 2 * mi; // rows (mi, r) and (mi, r + 8) of the permuted O^T
+            float *o0 = mrg_o + ((size_t)warp * H8 + h0) * D;
+            float *o1 = o0 + D;
+            o0[d] = acc[nt][mi][0];
+            o1[d] = acc[nt][mi][1];
+            o0[d + 1] = acc[nt][mi][2];
+            o1[d + 1] = acc[nt][mi][3];
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int hl = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            M = fmaxf(M, mrg_m[w * H8 + hl]);
+        float Lsum = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = ptx::ex2(mrg_m[w * H8 + hl] - M);
+                Lsum += f * mrg_l[w * H8 + hl];
+                O += f * mrg_o[((size_t)w * H8 + hl) * D + d];
+            }
+        }
+        const float o = Lsum > 0.f ? O / Lsum : 0.f;
+        const size_t h = (size_t)g * G + hl;
+        if (pslot < 0) {
+            p.out[((size_t)b * Hq + h) * D + d] = __float2bfloat16_rn(o);
+        } else {
+            p.part_o[((size_t)pslot * Hq + h) * D + d] = o;
+            if (d == 0)
+                p.part_lse[(size_t)pslot * Hq + h] = Lsum > 0.f ? M + __log2f(Lsum) : -INFINITY;
+        }
+    }
+}
+
+template <int D, int NT>
+int launch_int8(const DecodeArgs &a, const DecParams8 &p, cudaStream_t stream)
+{
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_int8_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DecLayout8<D>::kSmemBytes);
+        if (e != cudaSuccess)
+            return fail(PA_ERR_CUDA, "decode_int8 smem attribute: %s", cudaGetErrorString(e));
+        configured = true;
+    }
+    dim3 grid((unsigned)a.num_items, (unsigned)a.dims.num_kv_heads);
+    decode_int8_kernel<D, NT><<<grid, kWarps * 32, DecLayout8<D>::kSmemBytes, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "decode_int8 launch: %s", cudaGetErrorString(e));
+    return launch_decode_combine(a, stream);
+}
+
+} // namespace
+
+int launch_decode_int8(const DecodeArgs &a, void *stream)
+{
+    DecParams8 p{};
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.k_cache = static_cast<const int8_t *>(a.k_cache);
+    p.v_cache = static_cast<const int8_t *>(a.v_cache);
+    p.k_scale = static_cast<const __half *>(a.k_scale);
+    p.v_scale = static_cast<const __half *>(a.v_scale);
+    p.block_tables = a.block_tables;
+    p.items = reinterpret_cast<const int4 *>(a.items);
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.part_o = a.part_o;
+    p.part_lse = a.part_lse;
+    p.scale_log2 = a.scale * kLog2e;
+    p.num_heads = a.dims.num_heads;
+    p.num_kv_heads = a.dims.num_kv_heads;
+    p.group = a.dims.num_heads / a.dims.num_kv_heads;
+    p.block_size = a.dims.block_size;
+    p.max_blocks = a.max_blocks_per_seq;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool two = p.group > 8;
+    if (a.dims.head_dim == 128)
+        return two ? launch_int8<128, 2>(a, p, s) : launch_int8<128, 1>(a, p, s);
+    return two ? launch_int8<64, 2>(a, p, s) : launch_int8<64, 1>(a, p, s);
+}
+
+} // namespace pa

@@ -33,6 +33,10 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int launch_store_kvcache(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,
                          const int32_t *slot_mapping, int32_t num_tokens, void *stream);
 
+int launch_store_kvcache_int8(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,
+                              void *k_scale, void *v_scale, const int32_t *slot_mapping, int32_t num_tokens,
+                              void *stream);
+
 struct PrefillArgs {
     pa_dims dims;
     const void *q;
@@ -56,6 +60,8 @@ struct DecodeArgs {
     const void *q;
     const void *k_cache;
     const void *v_cache;
+    const void *k_scale; // INT8 cache only: fp16 [num_blocks][num_kv_heads][block_size]
+    const void *v_scale;
     const int32_t *context_lens;
     const int32_t *block_tables;
     const int32_t *items;
@@ -70,6 +76,9 @@ struct DecodeArgs {
     int32_t max_splits;
 };
 int launch_decode(const DecodeArgs &a, void *stream);
+int launch_decode_int8(const DecodeArgs &a, void *stream);
+// LSE merge of the split partials into out (no-op for plans without partials).
+int launch_decode_combine(const DecodeArgs &a, void *stream);
 
 // Device address of the library-owned decode scratch on the current device
 // (looked up once per device).  Used only by pa_decode_static.

@@ -21,8 +21,8 @@ from . import _build
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0, 1, 2, 3, 4
 
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
-           "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_last_error_string", "pa_read_device_error",
-           "pa_version")
+           "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
+           "pa_last_error_string", "pa_read_device_error", "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
             L.pa_decode.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_decode_static.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P]
             L.pa_copy_blocks.argtypes = [P, P, P, P, I32, P]
+            L.pa_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, P, I32, P]
+            L.pa_decode_int8.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_last_error_string.argtypes = []
             L.pa_last_error_string.restype = ctypes.c_char_p
             L.pa_read_device_error.argtypes = [P, P]
@@ -273,6 +275,39 @@ def pa_copy_blocks(dims: pa_dims, k_cache, v_cache, triples, num_triples: Option
     n = int(triples.shape[0]) if num_triples is None else int(num_triples)
     _check(lib().pa_copy_blocks(ctypes.byref(dims), _ptr(k_cache), _ptr(v_cache), _ptr(triples), n,
                                 _stream(stream)), "pa_copy_blocks")
+
+
+def int8_cache(dims: pa_dims, device="cuda"):
+    """Allocate an empty INT8 cache: (k_codes, v_codes, k_scale, v_scale).
+
+    Codes int8 [num_blocks, block_size, Hkv, D]; scales fp16 [num_blocks, Hkv, block_size].
+    """
+    shape = (dims.num_blocks, dims.block_size, dims.num_kv_heads, dims.head_dim)
+    sshape = (dims.num_blocks, dims.num_kv_heads, dims.block_size)
+    return (torch.zeros(shape, dtype=torch.int8, device=device), torch.zeros(shape, dtype=torch.int8, device=device),
+            torch.zeros(sshape, dtype=torch.float16, device=device),
+            torch.zeros(sshape, dtype=torch.float16, device=device))
+
+
+def pa_store_kvcache_int8(dims: pa_dims, k, v, k_cache, v_cache, k_scale, v_scale, slot_mapping,
+                          num_tokens: Optional[int] = None, stream=None):
+    """Quantise each new token's K/V head vectors (bf16) into int8 codes + fp16 scales at its slot."""
+    n = int(k.shape[0]) if num_tokens is None else int(num_tokens)
+    _check(lib().pa_store_kvcache_int8(ctypes.byref(dims), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), n, _stream(stream)),
+           "pa_store_kvcache_int8")
+
+
+def pa_decode_int8(dims: pa_dims, q, k_cache, v_cache, k_scale, v_scale, plan: DecodePlan, scale: float, out,
+                   workspace=None, stream=None):
+    """pa_decode over an INT8 cache (same plan and workspace as pa_decode)."""
+    m = plan.meta
+    ws_bytes = int(workspace.numel()) if isinstance(workspace, torch.Tensor) else 0
+    _check(lib().pa_decode_int8(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                _ptr(v_scale), plan.dptr(m.off_context_lens), plan.dptr(m.off_block_tables),
+                                float(scale), _ptr(out), ctypes.byref(m), plan.dptr(m.off_items),
+                                plan.dptr(m.off_seq_items), _ptr(workspace), ws_bytes, _stream(stream)),
+           "pa_decode_int8")
 
 
 def pa_read_device_error(stream=None) -> int:

@@ -90,3 +90,49 @@ def oracle_subset_pool(pool_k: torch.Tensor, pool_v: torch.Tensor, batch, seqs):
     sub_v = bits(pool_v.index_select(0, idx))
     lists = [np.array([remap[int(p)] for p in batch.block_lists[b]], np.int32) for b in seqs]
     return sub_k, sub_v, lists
+
+
+def int8_pools(w, num_heads: int):
+    """Quantise the workload's bf16 pool on both sides, independently.
+
+    GPU: pa_store_kvcache_int8 over every slot of the pool.  Oracle:
+    oracle.quantize_rows on a host copy, scales moved to the cache's
+    head-major [blocks][kv heads][block] layout.  Returns (gpu, host) tuples
+    of (k_codes, v_codes, k_scale, v_scale); host scales are fp16 bits.
+    """
+    p = w.pool
+    dev = p.k_cache.device
+    dims = pa.make_dims(p.num_blocks, p.block_size, num_heads, p.num_kv_heads, p.head_dim)
+    n = p.num_blocks * p.block_size
+    slots = torch.arange(n, dtype=torch.int32, device=dev)
+    gpu = pa.int8_cache(dims, dev)
+    pa.pa_store_kvcache_int8(dims, p.k_cache.view(n, p.num_kv_heads, p.head_dim),
+                             p.v_cache.view(n, p.num_kv_heads, p.head_dim), *gpu, slots, n)
+    kc, ks = oracle.quantize_rows(p.k_cache.cpu())
+    vc, vs = oracle.quantize_rows(p.v_cache.cpu())
+    host = (kc, vc, np.ascontiguousarray(ks.transpose(0, 2, 1)), np.ascontiguousarray(vs.transpose(0, 2, 1)))
+    return gpu, host
+
+
+def int8_equal(gpu, host, what=""):
+    """Bit-exact comparison of a GPU INT8 cache with the oracle's."""
+    names = ("k codes", "v codes", "k scales", "v scales")
+    for name, g, h in zip(names, gpu, host):
+        got = g.cpu().numpy()
+        if got.dtype == np.float16:
+            got = got.view(np.uint16)
+        bad = np.count_nonzero(got != h)
+        assert bad == 0, f"{what}: {bad} of {h.size} {name} differ"
+
+
+def run_gpu_decode_int8(w, batch, cache, split_tokens: int = 0, stream=None):
+    """Quantising store of the batch's new K/V, then INT8 decode. Returns out (bf16, device)."""
+    dims = dims_of(w, batch)
+    dev = cache[0].device
+    q, k, v = batch.q.to(dev), batch.k.to(dev), batch.v.to(dev)
+    out = torch.empty_like(q)
+    plan = pa.pa_pack_decode(dims, batch.seq_lens, batch.block_lists, split_tokens).upload(dev, stream)
+    pa.pa_store_kvcache_int8(dims, k, v, *cache, plan.slot_mapping, batch.num_tokens, stream=stream)
+    ws = pa.decode_workspace(plan, dev)
+    pa.pa_decode_int8(dims, q, *cache, plan, batch.scale, out, ws, stream=stream)
+    return out, plan
