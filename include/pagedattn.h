@@ -302,8 +302,10 @@ int pa_decode_static(const pa_dims *dims, const void *q, const void *k_cache, co
 const char *pa_last_error_string(void);
 
 /*
- * Reads and clears the device-side error word (bounded waits that timed out
- * inside a kernel set it; 0 = none).  Synchronises `stream`: for tests and
+ * Reads and clears the device-side error word (0 = none).  Bits: 0 a store
+ * met a slot outside [-1, num_slots); 1 a bounded wait in the prefill kernel
+ * timed out; 2 a block-copy triple was out of range; 3 a bounded wait in the
+ * INT8 decode kernel timed out.  Synchronises `stream`: for tests and
  * debugging, never on the hot path.
  */
 int pa_read_device_error(uint32_t *code, pa_stream_t stream);

@@ -301,5 +301,7 @@ extern "C" int pa_read_device_error(uint32_t *code, pa_stream_t stream)
         rc = read_prefill_error(code);
     if (rc == PA_OK)
         rc = read_copy_error(code);
+    if (rc == PA_OK)
+        rc = read_decode_error(code);
     return rc;
 }

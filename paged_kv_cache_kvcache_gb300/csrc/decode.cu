@@ -74,9 +74,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const DecP
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int4 item = p.items[blockIdx.x];
+    const int4 item = p.items[blockIdx.x / p.num_kv_heads];
     const int b = item.x, k0 = item.y, k1 = item.z, pslot = item.w;
-    const int g = blockIdx.y;
+    const int g = blockIdx.x % p.num_kv_heads;
     const int G = p.group;
     const int Hq = p.num_heads;
 
@@ -333,7 +333,9 @@ int launch_split(const DecodeArgs &a, const DecParams &p, cudaStream_t stream)
             return fail(PA_ERR_CUDA, "decode smem attribute: %s", cudaGetErrorString(e));
         configured = true;
     }
-    dim3 grid((unsigned)a.num_items, (unsigned)a.dims.num_kv_heads);
+    // flat grid, heads of one work item adjacent: they read neighbouring
+    // segments of the same token rows at about the same time (DRAM locality)
+    dim3 grid((unsigned)(a.num_items * a.dims.num_kv_heads));
     decode_split_kernel<D, NT><<<grid, kWarps * 32, DecLayout<D>::kSmemBytes, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)

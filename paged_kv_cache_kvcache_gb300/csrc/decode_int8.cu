@@ -12,9 +12,13 @@
 // GB300 design.  Work items, CTA/warp decomposition, cp.async pipeline,
 // online softmax, warp merge and partial format are those of the bf16 decode;
 // what changes is the operand path:
-//  * 16-token chunks of int8 codes (D bytes per token row) plus the chunk's 16
-//    K and 16 V fp16 scales are staged with 16-byte cp.async; a tail chunk's
-//    missing tokens (codes and scales) are zero-filled by the copy itself.
+//  * Each warp owns a ring of stages fed by TMA: for every 16-token chunk its
+//    lane 0 issues one 3-D tensor copy of the K codes (16 token rows of D bytes
+//    for one KV head, hardware-swizzled), one of the V codes and two 32-byte
+//    bulk copies of the chunk's fp16 K and V scales, all completing on the
+//    stage's mbarrier (waits are bounded).  A chunk never crosses a block, so a
+//    tail chunk's extra rows are in-bounds cache memory; their scores are
+//    masked and their V scales zeroed before use.
 //  * A code x converts to fp16 exactly: the bit pattern 0x6400 | (x + 128) is
 //    1024 + x + 128, minus 1152 gives x (one prmt + one f16x2 subtract per
 //    pair).  Both MMAs therefore run as f16 m16n8k16 with fp32 accumulation:
@@ -40,30 +44,35 @@ namespace pa {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct DecLayout8 {
-    static constexpr int kChunkBytes = 16 * D;        // 16 tokens of int8 codes
-    static constexpr int kScaleOff = 2 * kChunkBytes; // K codes, V codes, 16 K scales, 16 V scales
-    static constexpr int kStageBytes = 2 * kChunkBytes + 64;
+    static constexpr int kChunkBytes = 16 * D;          // 16 tokens of int8 codes
+    static constexpr int kStageBytes = 2 * kChunkBytes; // K codes, V codes
     static constexpr int kWarpBytes = kStages * kStageBytes;
-    static constexpr int kSmemBytes = kWarps * kWarpBytes;
-    static constexpr int kVecPerRow = D / 16; // 16-byte vectors per token row
+    static constexpr int kScaleOff = kWarps * kWarpBytes; // [warp][stage]: 16 K + 16 V fp16 scales
+    static constexpr int kBarOff = kScaleOff + kWarps * kStages * 64;
+    static constexpr int kUsed = kBarOff + kWarps * kStages * 8;
+    static constexpr int kSmemBytes = kUsed + 1024; // + slack to align the base to the swizzle atom
+    static constexpr uint32_t kTxBytes = 2 * kChunkBytes + 64;
 };
 
-// Byte offset of 16-byte vector v of token t inside a staged chunk.  XOR
-// swizzles make every fragment load below conflict-free: D = 128 keeps one
-// token per 128-byte line, D = 64 two tokens per line.
+// Byte offset of 16-byte vector v of token t inside a staged chunk, as the TMA
+// swizzle writes it: 128-byte rows (D = 128) under SWIZZLE_128B, 64-byte rows
+// (D = 64) under SWIZZLE_64B.  The fragment loads below are conflict-free at
+// D = 128 (two-way on V at D = 64).
 template <int D>
 __device__ __forceinline__ uint32_t swz(int t, int v)
 {
     if constexpr (D == 128)
         return (uint32_t)(t * 128 + ((v ^ (t & 7)) << 4));
     else
-        return (uint32_t)((t >> 1) * 128 + (((((t & 1) << 2) | v) ^ (((t >> 1) & 3) << 1)) << 4));
+        return (uint32_t)(t * 64 + ((v ^ ((t >> 1) & 3)) << 4));
 }
+
+__device__ uint32_t g_decode_error; // bit 0: a bounded wait timed out
 
 constexpr uint32_t kFlip = 0x80808080u;  // int8 -> offset binary (x + 128), per byte
 constexpr uint32_t kLoPair = 0x4140u;    // prmt: bytes 0, 1 under 0x64 high bytes
@@ -87,8 +96,6 @@ __device__ __forceinline__ float lds_half(uint32_t addr) { return __half2float(_
 
 struct DecParams8 {
     const __nv_bfloat16 *q;
-    const int8_t *k_cache;
-    const int8_t *v_cache;
     const __half *k_scale;
     const __half *v_scale;
     const int32_t *block_tables;
@@ -105,18 +112,70 @@ struct DecParams8 {
 };
 
 template <int D, int NT>
-__global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecParams8 p)
+__global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
+    decode_int8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const DecParams8 p)
 {
     using L = DecLayout8<D>;
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw); // generic pointer to the aligned base
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int r = lane >> 2, c = lane & 3;
-    const int4 item = p.items[blockIdx.x];
+    const int4 item = p.items[blockIdx.x / p.num_kv_heads];
     const int b = item.x, k0 = item.y, k1 = item.z, pslot = item.w;
-    const int g = blockIdx.y;
+    const int g = blockIdx.x % p.num_kv_heads;
     const int G = p.group;
     const int Hq = p.num_heads;
+
+    const int nchunks = (k1 - k0 + 15) >> 4;
+    const int my_n = nchunks > warp ? (nchunks - warp + kWarps - 1) / kWarps : 0;
+    const uint32_t wbase = sbase + warp * L::kWarpBytes;
+    const uint32_t sc_base = sbase + L::kScaleOff + warp * kStages * 64;
+    const uint32_t bar_base = sbase + L::kBarOff + warp * kStages * 8;
+    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks;
+    const int bs = p.block_size;
+    const int Hkv = p.num_kv_heads;
+    int blk_cache = 0;
+
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s)
+            ptx::mbar_init(bar_base + 8 * s, 1);
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+    }
+    __syncwarp();
+
+    // Chunk i of this warp into stage i % kStages (whole warp: the block id comes by shuffle).
+    auto issue = [&](int i) {
+        if ((i & 31) == 0) { // refresh the block ids of local chunks i .. i+31, one per lane
+            const int key = k0 + 16 * (warp + kWarps * (i + lane));
+            blk_cache = key < k1 ? __ldg(bt_row + key / bs) : 0;
+        }
+        const int phys = __shfl_sync(0xffffffffu, blk_cache, i & 31);
+        if (lane == 0) {
+            const int key0 = k0 + 16 * (warp + kWarps * i);
+            const int off0 = key0 & (bs - 1); // a chunk never crosses a block (bs >= 16, key0 % 16 == 0)
+            const int st = i % kStages;
+            const uint32_t bar = bar_base + 8 * st;
+            const uint32_t dst = wbase + st * L::kStageBytes;
+            const size_t si = ((size_t)phys * Hkv + g) * bs + off0;
+            ptx::mbar_arrive_expect_tx(bar, L::kTxBytes);
+            ptx::tma_load_3d(dst, &tm_k, bar, 0, g, phys * bs + off0);
+            ptx::tma_load_3d(dst + L::kChunkBytes, &tm_v, bar, 0, g, phys * bs + off0);
+            ptx::bulk_load(sc_base + st * 64, p.k_scale + si, 32u, bar);
+            ptx::bulk_load(sc_base + st * 64 + 32, p.v_scale + si, 32u, bar);
+        }
+    };
+
+    // first stages in flight before Q is fetched, so the two latencies overlap
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s)
+        if (s < my_n)
+            issue(s);
 
     // Q^T fragments (f16), B operand of the score MMA.  k-step kk of lane c
     // covers d = c*D/4 + 4kk + {0,1} (logical k 2c, 2c+1) and + {2,3} (2c+8, 2c+9).
@@ -135,45 +194,6 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecPa
         }
     }
 
-    const int nchunks = (k1 - k0 + 15) >> 4;
-    const int my_n = nchunks > warp ? (nchunks - warp + kWarps - 1) / kWarps : 0;
-    const uint32_t wbase = ptx::smem_u32(smem) + warp * L::kWarpBytes;
-    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks;
-    const int bs = p.block_size;
-    const int Hkv = p.num_kv_heads;
-    int blk_cache = 0;
-
-    auto issue = [&](int i) {
-        if ((i & 31) == 0) { // refresh the block ids of local chunks i .. i+31, one per lane
-            const int key = k0 + 16 * (warp + kWarps * (i + lane));
-            blk_cache = key < k1 ? __ldg(bt_row + key / bs) : 0;
-        }
-        const int phys = __shfl_sync(0xffffffffu, blk_cache, i & 31);
-        const int key0 = k0 + 16 * (warp + kWarps * i);
-        const int off0 = key0 & (bs - 1); // a chunk never crosses a block (bs >= 16, key0 % 16 == 0)
-        const int64_t row0 = (int64_t)phys * bs + off0;
-        const uint32_t sbase = wbase + (i % kStages) * L::kStageBytes;
-#pragma unroll
-        for (int e = lane; e < 16 * L::kVecPerRow; e += 32) {
-            const int t = e / L::kVecPerRow;
-            const int v = e % L::kVecPerRow;
-            const bool valid = key0 + t < k1;
-            const size_t off = ((size_t)(row0 + t) * Hkv + g) * D + v * 16;
-            const uint32_t dst = sbase + swz<D>(t, v);
-            ptx::cp_async_16(dst, valid ? (const void *)(p.k_cache + off) : (const void *)p.k_cache, valid ? 16u : 0u);
-            ptx::cp_async_16(dst + L::kChunkBytes, valid ? (const void *)(p.v_cache + off) : (const void *)p.v_cache,
-                             valid ? 16u : 0u);
-        }
-        if (lane < 4) { // scales: lanes 0/1 K tokens 0-7/8-15, lanes 2/3 the same for V; missing tokens read 0
-            const int h = lane & 1;
-            const int n = min(max(k1 - key0 - 8 * h, 0), 8);
-            const __half *base = lane < 2 ? p.k_scale : p.v_scale;
-            const size_t si = ((size_t)phys * Hkv + g) * bs + off0 + 8 * h;
-            ptx::cp_async_16(sbase + L::kScaleOff + lane * 16, n ? (const void *)(base + si) : (const void *)base,
-                             (uint32_t)(2 * n));
-        }
-    };
-
     float acc[NT][D / 16][4];
     float m_r[NT][2], l_r[NT][2];
 #pragma unroll
@@ -185,24 +205,24 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecPa
             acc[nt][mi][0] = acc[nt][mi][1] = acc[nt][mi][2] = acc[nt][mi][3] = 0.f;
     }
 
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (s < my_n)
-            issue(s);
-        ptx::cp_async_commit();
-    }
 
+    int done = 0; // chunks consumed (all issued chunks are waited for before exit)
     for (int i = 0; i < my_n; ++i) {
+        // stage (i - 1) % kStages was read by every lane in the previous iteration
         __syncwarp();
         if (i + kStages - 1 < my_n)
             issue(i + kStages - 1);
-        ptx::cp_async_commit();
-        ptx::cp_async_wait<kStages - 1>();
-        __syncwarp();
+        const int st = i % kStages;
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_base + 8 * st, (uint32_t)(i / kStages) & 1u))) {
+            if (lane == 0)
+                atomicOr(&g_decode_error, 1u);
+            break;
+        }
+        done = i + 1;
 
-        const uint32_t kb = wbase + (i % kStages) * L::kStageBytes;
+        const uint32_t kb = wbase + st * L::kStageBytes;
         const uint32_t vb = kb + L::kChunkBytes;
-        const uint32_t sb = kb + L::kScaleOff;
+        const uint32_t sb = sc_base + st * 64;
         const int key0 = k0 + 16 * (warp + kWarps * i);
 
         // K codes of tokens r and r + 8: bytes [c*D/4, (c+1)*D/4) of each row
@@ -232,10 +252,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecPa
 
         const float ks0 = lds_half(sb + 2 * r) * p.scale_log2;
         const float ks1 = lds_half(sb + 2 * (r + 8)) * p.scale_log2;
-        const float vs0 = lds_half(sb + 32 + 2 * r);
-        const float vs1 = lds_half(sb + 32 + 2 * (r + 8));
         const bool v0 = key0 + r < k1;
         const bool v1 = key0 + r + 8 < k1;
+        const float vs0 = v0 ? lds_half(sb + 32 + 2 * r) : 0.f; // rows past the context: weight 0
+        const float vs1 = v1 ? lds_half(sb + 32 + 2 * (r + 8)) : 0.f;
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -257,12 +277,14 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecPa
             const float p2 = ptx::ex2(s2 - mn0), p3 = ptx::ex2(s3 - mn1);
             l_r[nt][0] = l_r[nt][0] * al0 + p0 + p2;
             l_r[nt][1] = l_r[nt][1] * al1 + p1 + p3;
+            if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) { // skipped while no row max moves
 #pragma unroll
-            for (int mi = 0; mi < D / 16; ++mi) {
-                acc[nt][mi][0] *= al0;
-                acc[nt][mi][1] *= al1;
-                acc[nt][mi][2] *= al0;
-                acc[nt][mi][3] *= al1;
+                for (int mi = 0; mi < D / 16; ++mi) {
+                    acc[nt][mi][0] *= al0;
+                    acc[nt][mi][1] *= al1;
+                    acc[nt][mi][2] *= al0;
+                    acc[nt][mi][3] *= al1;
+                }
             }
             pb[nt][0] = ptx::movmatrix_trans(ptx::pack_f16(p0 * vs0, p1 * vs0));
             pb[nt][1] = ptx::movmatrix_trans(ptx::pack_f16(p2 * vs1, p3 * vs1));
@@ -305,7 +327,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecPa
             }
         }
     }
-    ptx::cp_async_wait<0>();
+    // after a timed-out wait: let the copies still in flight land (bounded) before the buffers are reused
+    for (int i = done; i < my_n && i < done + kStages; ++i)
+        ptx::mbar_wait(bar_base + 8 * (i % kStages), (uint32_t)(i / kStages) & 1u);
 
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -318,9 +342,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecPa
     // merge the 4 warps through shared memory (pipeline buffers are free now)
     __syncthreads();
     constexpr int H8 = 8 * NT;
+    constexpr int kRow = D + 4; // padded head row (floats): the float4 stores below conflict at most 2-way
     float *mrg_m = reinterpret_cast<float *>(smem);
     float *mrg_l = mrg_m + kWarps * H8;
-    float *mrg_o = mrg_l + kWarps * H8; // [warp][head][D], d in natural order
+    float *mrg_o = mrg_l + kWarps * H8; // [warp][head][kRow], d in natural order
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int h0 = nt * 8 + 2 * c;
@@ -330,15 +355,14 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecPa
             mrg_l[warp * H8 + h0] = l_r[nt][0];
             mrg_l[warp * H8 + h0 + 1] = l_r[nt][1];
         }
+        // O^T row (mi, r + 8*hi) is d = r*D/8 + 2*mi + hi: this lane's D/8 values per head are contiguous
 #pragma unroll
-        for (int mi = 0; mi < D / 16; ++mi) {
-            const int d = r * (D / 8) + 2 * mi; // rows (mi, r) and (mi, r + 8) of the permuted O^T
-            float *o0 = mrg_o + ((size_t)warp * H8 + h0) * D;
-            float *o1 = o0 + D;
-            o0[d] = acc[nt][mi][0];
-            o1[d] = acc[nt][mi][1];
-            o0[d + 1] = acc[nt][mi][2];
-            o1[d + 1] = acc[nt][mi][3];
+        for (int j = 0; j < 2; ++j) {
+            float4 *dst = reinterpret_cast<float4 *>(mrg_o + ((size_t)warp * H8 + h0 + j) * kRow + r * (D / 8));
+#pragma unroll
+            for (int v = 0; v < D / 32; ++v)
+                dst[v] = make_float4(acc[nt][2 * v][j], acc[nt][2 * v][j + 2], acc[nt][2 * v + 1][j],
+                                     acc[nt][2 * v + 1][j + 2]);
         }
     }
     __syncthreads();
@@ -354,7 +378,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_int8_kernel(const DecPa
             for (int w = 0; w < kWarps; ++w) {
                 const float f = ptx::ex2(mrg_m[w * H8 + hl] - M);
                 Lsum += f * mrg_l[w * H8 + hl];
-                O += f * mrg_o[((size_t)w * H8 + hl) * D + d];
+                O += f * mrg_o[((size_t)w * H8 + hl) * kRow + d];
             }
         }
         const float o = Lsum > 0.f ? O / Lsum : 0.f;
@@ -380,8 +404,22 @@ int launch_int8(const DecodeArgs &a, const DecParams8 &p, cudaStream_t stream)
             return fail(PA_ERR_CUDA, "decode_int8 smem attribute: %s", cudaGetErrorString(e));
         configured = true;
     }
-    dim3 grid((unsigned)a.num_items, (unsigned)a.dims.num_kv_heads);
-    decode_int8_kernel<D, NT><<<grid, kWarps * 32, DecLayout8<D>::kSmemBytes, stream>>>(p);
+    // codes as uint8 [num_slots][Hkv][D]: box = one head's D bytes x 16 token rows
+    const pa_dims &d = a.dims;
+    const uint64_t rows = (uint64_t)d.num_blocks * d.block_size;
+    const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap tk, tv;
+    int rc;
+    if ((rc = encode_tmap_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.k_cache, D, d.num_kv_heads, rows, D,
+                             (uint64_t)d.num_kv_heads * D, D, 1, 16, sw, "int8 k_cache")) != PA_OK)
+        return rc;
+    if ((rc = encode_tmap_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.v_cache, D, d.num_kv_heads, rows, D,
+                             (uint64_t)d.num_kv_heads * D, D, 1, 16, sw, "int8 v_cache")) != PA_OK)
+        return rc;
+    // flat grid, heads of one work item adjacent: they read neighbouring
+    // segments of the same token rows at about the same time (DRAM locality)
+    dim3 grid((unsigned)(a.num_items * a.dims.num_kv_heads));
+    decode_int8_kernel<D, NT><<<grid, kWarps * 32, DecLayout8<D>::kSmemBytes, stream>>>(tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "decode_int8 launch: %s", cudaGetErrorString(e));
@@ -394,8 +432,6 @@ int launch_decode_int8(const DecodeArgs &a, void *stream)
 {
     DecParams8 p{};
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
-    p.k_cache = static_cast<const int8_t *>(a.k_cache);
-    p.v_cache = static_cast<const int8_t *>(a.v_cache);
     p.k_scale = static_cast<const __half *>(a.k_scale);
     p.v_scale = static_cast<const __half *>(a.v_scale);
     p.block_tables = a.block_tables;
@@ -414,6 +450,18 @@ int launch_decode_int8(const DecodeArgs &a, void *stream)
     if (a.dims.head_dim == 128)
         return two ? launch_int8<128, 2>(a, p, s) : launch_int8<128, 1>(a, p, s);
     return two ? launch_int8<64, 2>(a, p, s) : launch_int8<64, 1>(a, p, s);
+}
+
+int read_decode_error(uint32_t *code)
+{
+    uint32_t v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_decode_error, sizeof v);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(g_decode_error, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "reading decode error word: %s", cudaGetErrorString(e));
+    *code |= v << 3;
+    return PA_OK;
 }
 
 } // namespace pa

@@ -4,6 +4,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
+
 #include "pagedattn.h"
 
 namespace pa {
@@ -28,6 +30,12 @@ int fail(int code, const char *fmt, ...);
 int check_dims(const pa_dims *dims);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// 3-D TMA descriptor (dims innermost first, strides of dims 1 and 2 in bytes,
+// box in elements); PA_ERR_CUDA if the driver rejects it.
+int encode_tmap_3d(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t d0, uint64_t d1,
+                   uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
+                   CUtensorMapSwizzle swizzle, const char *what);
 
 // Launchers (defined in the .cu files).  Each returns PA_OK or PA_ERR_CUDA.
 int launch_store_kvcache(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,
@@ -91,9 +99,10 @@ int launch_copy_blocks(const pa_dims &d, void *k_cache, void *v_cache, const int
                        void *stream);
 
 // Read and clear the device error words (store: bit 0, prefill waits: bit 1,
-// block copy: bit 2).
+// block copy: bit 2, INT8 decode waits: bit 3).
 int read_store_error(uint32_t *code);
 int read_prefill_error(uint32_t *code);
 int read_copy_error(uint32_t *code);
+int read_decode_error(uint32_t *code);
 
 } // namespace pa

@@ -521,37 +521,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-        cudaGetLastError();
-    }
-    return fn;
-}
-
-int encode_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1,
-              uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2,
-              const char *what)
-{
-    cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
-    cuuint32_t box[3] = {b0, b1, b2};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
-    return PA_OK;
-}
-
 template <int D>
 int launch(const PrefillArgs &a, cudaStream_t stream)
 {
@@ -564,23 +533,23 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
             return fail(PA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
         configured = true;
     }
-    auto enc = get_encoder();
-    if (!enc)
-        return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
     const pa_dims &d = a.dims;
     const int G = d.num_heads / d.num_kv_heads;
     const uint64_t rows = (uint64_t)d.num_blocks * d.block_size;
     CUtensorMap tq, tk, tv;
     int rc;
-    if ((rc = encode_3d(enc, &tq, a.q, D, d.num_heads, (uint64_t)a.total_q, (uint64_t)D * 2,
-                        (uint64_t)d.num_heads * D * 2, 64, (uint32_t)G, (uint32_t)a.rows_per_tile, "q")) != PA_OK)
+    constexpr CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    constexpr CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    if ((rc = encode_tmap_3d(&tq, bf16, a.q, D, d.num_heads, (uint64_t)a.total_q, (uint64_t)D * 2,
+                             (uint64_t)d.num_heads * D * 2, 64, (uint32_t)G, (uint32_t)a.rows_per_tile, sw, "q")) !=
+        PA_OK)
         return rc;
     const uint32_t box_rows = d.block_size < 128 ? (uint32_t)d.block_size : 128u;
-    if ((rc = encode_3d(enc, &tk, a.k_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
-                        (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, "k_cache")) != PA_OK)
+    if ((rc = encode_tmap_3d(&tk, bf16, a.k_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
+                             (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "k_cache")) != PA_OK)
         return rc;
-    if ((rc = encode_3d(enc, &tv, a.v_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
-                        (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, "v_cache")) != PA_OK)
+    if ((rc = encode_tmap_3d(&tv, bf16, a.v_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
+                             (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "v_cache")) != PA_OK)
         return rc;
     PfParams p{};
     p.cu_seqlens_q = a.cu_seqlens_q;
