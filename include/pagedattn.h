@@ -266,6 +266,22 @@ int pa_decode_int8(const pa_dims *dims, const void *q, const void *k_cache, cons
                    pa_stream_t stream);
 
 /*
+ * pa_prefill_varlen_int8 — pa_prefill_varlen over an INT8 cache: the same
+ * plan (pa_pack_prefill), arguments and result, with the cached K and V read
+ * as code * scale.  The dequantisation is fused the way the page's Q3
+ * follow-ups describe it: the key scale multiplies each score after the
+ * q.k dot product over the raw codes, and the value scale is folded into the
+ * softmax weights (the normaliser keeps the unscaled weights); no floating
+ * copy of the cache is materialised.  Internally the codes (exact in fp16),
+ * q (rounded to fp16, saturating at +-65504) and the scaled weights feed
+ * fp16 tensor-core products with fp32 accumulation.
+ */
+int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                           const void *k_scale, const void *v_scale, const int32_t *cu_seqlens_q,
+                           const int32_t *cu_seqlens_k, const int32_t *block_tables, float scale, void *out,
+                           const pa_prefill_meta *meta, const int32_t *tiles, pa_stream_t stream);
+
+/*
  * pa_decode_static — pa_decode for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point: it exists for callers
  * that have no way to obtain a decode workspace, e.g. code that runs while a

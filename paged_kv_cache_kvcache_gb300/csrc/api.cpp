@@ -91,11 +91,14 @@ extern "C" int pa_store_kvcache(const pa_dims *dims, const void *k, const void *
     return launch_store_kvcache(*dims, k, v, k_cache, v_cache, slot_mapping, num_tokens, stream);
 }
 
-extern "C" int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
-                                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
-                                 const int32_t *block_tables, float scale, void *out, const pa_prefill_meta *meta,
-                                 const int32_t *tiles, pa_stream_t stream)
+// Host-side checks shared by pa_prefill_varlen and pa_prefill_varlen_int8;
+// fills `a`.  Sets *nothing when the plan has no work (then no launch happens).
+static int prepare_prefill(const char *fn, const pa_dims *dims, const void *q, const void *k_cache,
+                           const void *v_cache, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                           const int32_t *block_tables, float scale, void *out, const pa_prefill_meta *meta,
+                           const int32_t *tiles, PrefillArgs *a, bool *nothing)
 {
+    *nothing = false;
     int rc = check_dims(dims);
     if (rc != PA_OK)
         return rc;
@@ -108,30 +111,67 @@ extern "C" int pa_prefill_varlen(const pa_dims *dims, const void *q, const void 
     const int group = dims->num_heads / dims->num_kv_heads;
     if (meta->rows_per_tile != (kPrefillRows / group > 0 ? kPrefillRows / group : 1))
         return fail(PA_ERR_INVALID_ARG, "prefill meta was packed for other dims");
-    if (meta->num_tiles == 0 || meta->total_q == 0)
+    if (meta->num_tiles == 0 || meta->total_q == 0) {
+        *nothing = true;
         return PA_OK;
+    }
     if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables || !out || !tiles)
-        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen: NULL pointer");
+        return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", fn);
     if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
-        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen: tensors must be 16-byte aligned");
+        return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
     if (dims->num_blocks == 0)
         return fail(PA_ERR_INVALID_ARG, "empty KV pool");
-    PrefillArgs a{};
-    a.dims = *dims;
-    a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
-    a.cu_seqlens_q = cu_seqlens_q;
-    a.cu_seqlens_k = cu_seqlens_k;
-    a.block_tables = block_tables;
-    a.tiles = tiles;
-    a.out = out;
-    a.scale = scale;
-    a.num_tiles = meta->num_tiles;
-    a.total_q = meta->total_q;
-    a.max_blocks_per_seq = meta->max_blocks_per_seq;
-    a.rows_per_tile = meta->rows_per_tile;
+    *a = PrefillArgs{};
+    a->dims = *dims;
+    a->q = q;
+    a->k_cache = k_cache;
+    a->v_cache = v_cache;
+    a->cu_seqlens_q = cu_seqlens_q;
+    a->cu_seqlens_k = cu_seqlens_k;
+    a->block_tables = block_tables;
+    a->tiles = tiles;
+    a->out = out;
+    a->scale = scale;
+    a->num_tiles = meta->num_tiles;
+    a->total_q = meta->total_q;
+    a->max_blocks_per_seq = meta->max_blocks_per_seq;
+    a->rows_per_tile = meta->rows_per_tile;
+    return PA_OK;
+}
+
+extern "C" int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                 const int32_t *block_tables, float scale, void *out, const pa_prefill_meta *meta,
+                                 const int32_t *tiles, pa_stream_t stream)
+{
+    PrefillArgs a;
+    bool nothing = false;
+    int rc = prepare_prefill("pa_prefill_varlen", dims, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                             block_tables, scale, out, meta, tiles, &a, &nothing);
+    if (rc != PA_OK || nothing)
+        return rc;
     return launch_prefill(a, stream);
+}
+
+extern "C" int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                                      const void *k_scale, const void *v_scale, const int32_t *cu_seqlens_q,
+                                      const int32_t *cu_seqlens_k, const int32_t *block_tables, float scale,
+                                      void *out, const pa_prefill_meta *meta, const int32_t *tiles,
+                                      pa_stream_t stream)
+{
+    PrefillArgs a;
+    bool nothing = false;
+    int rc = prepare_prefill("pa_prefill_varlen_int8", dims, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                             block_tables, scale, out, meta, tiles, &a, &nothing);
+    if (rc != PA_OK || nothing)
+        return rc;
+    if (!k_scale || !v_scale)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8: NULL scale pointer");
+    if (misaligned(k_scale) || misaligned(v_scale))
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8: scales must be 16-byte aligned");
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return launch_prefill_int8(a, stream);
 }
 
 // Host-side checks shared by pa_decode and pa_decode_int8; fills `a`.  Sets

@@ -50,6 +50,8 @@ struct PrefillArgs {
     const void *q;
     const void *k_cache;
     const void *v_cache;
+    const void *k_scale; // INT8 cache only: fp16 [num_blocks][num_kv_heads][block_size]
+    const void *v_scale;
     const int32_t *cu_seqlens_q;
     const int32_t *cu_seqlens_k;
     const int32_t *block_tables;
@@ -62,6 +64,7 @@ struct PrefillArgs {
     int32_t rows_per_tile;
 };
 int launch_prefill(const PrefillArgs &a, void *stream);
+int launch_prefill_int8(const PrefillArgs &a, void *stream);
 
 struct DecodeArgs {
     pa_dims dims;

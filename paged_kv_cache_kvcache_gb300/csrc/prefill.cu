@@ -45,6 +45,7 @@
 //    timeout through a device error word instead of hanging.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -63,7 +64,7 @@ namespace {
 // the MMAs of both query tiles: its in-order stream keeps the two tiles half a
 // key tile apart, so one tile's softmax always runs under the other's MMAs.
 constexpr int kThreads = 384;
-constexpr int kKProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10;
+constexpr int kKProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10, kLoaderWarp = 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
@@ -72,22 +73,44 @@ constexpr float kRescaleThreshold = 8.0f; // log2 units
 // 4 barriers keep every parity wait unambiguous.
 constexpr int kIterRing = 4;
 
-template <int D>
+template <int D, bool I8>
 struct PfLayout {
     static constexpr int kPanels = D / 64;          // 64-element (128-byte) panels along head_dim
     static constexpr int kPanelBytes = 128 * 128;   // 128 rows x 128 bytes
     static constexpr int kTileBytes = kPanels * kPanelBytes;
     // K is released as soon as the two score MMAs have read it, V only after
-    // both PV MMAs: K gets the deeper ring so its loads start earliest.
-    static constexpr int kKStages = D == 128 ? 3 : 4;
-    static constexpr int kVStages = D == 128 ? 2 : 4;
+    // both PV MMAs: K gets the deeper ring so its loads start earliest (the
+    // INT8 variant's extra buffers leave room for two K stages at D = 128).
+    static constexpr int kKStages = I8 ? (D == 128 ? 2 : 3) : (D == 128 ? 3 : 4);
+    static constexpr int kVStages = I8 ? (D == 128 ? 2 : 3) : (D == 128 ? 2 : 4);
     static constexpr int kQ = 0;                    // two query tiles (also the output staging)
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
-    static constexpr int kBar = kV + kVStages * kTileBytes;
-    static constexpr int kBarBytes = 256;
+    // INT8 cache: a key tile's raw codes (128 rows x D bytes) land in the upper
+    // half of the 16-bit tile they are converted into (D = 128: row t's codes
+    // occupy the slot of row t's second panel) or in a ring of their own
+    // (D = 64), and a 2-slot ring holds each key tile's per-key factors.
+    static constexpr bool kInPlace = D == 128;
+    static constexpr int kCodeBytes = 128 * D;
+    static constexpr int kStg = kV + kVStages * kTileBytes;
+    static constexpr int kStgBytes = I8 && !kInPlace ? (kKStages + kVStages) * kCodeBytes : 0;
+    static constexpr int kScl = kStg + kStgBytes;
+    static constexpr int kSclSlot = 2 * 128 * 4; // 128 fp32 K factors, then 128 fp32 V scales
+    static constexpr int kSclBytes = I8 ? 2 * kSclSlot : 0;
+    static constexpr int kBar = kScl + kSclBytes;
+    static constexpr int kBarBytes = 512;
     static constexpr int kSmemBytes = kBar + kBarBytes + 1024; // + alignment slack
+    __host__ __device__ static constexpr int k_codes(int s)
+    {
+        return kInPlace ? kK + s * kTileBytes + kTileBytes / 2 : kStg + s * kCodeBytes;
+    }
+    __host__ __device__ static constexpr int v_codes(int s)
+    {
+        return kInPlace ? kV + s * kTileBytes + kTileBytes / 2 : kStg + (kKStages + s) * kCodeBytes;
+    }
     static_assert(128 * D * 2 <= kTileBytes, "O staging must fit in a query tile");
+    static_assert(!kInPlace || kCodeBytes == kTileBytes / 2, "in-place codes fill the second panel");
+    static_assert(kKStages <= 4 && kVStages <= 4, "barrier slots");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -104,6 +127,9 @@ struct PfParams {
     int32_t block_size;
     int32_t max_blocks;
     int32_t num_slots;     // num_blocks * block_size: first out-of-range row (reads as zeros)
+    int32_t num_kv_heads;
+    const __half *k_scale; // INT8 cache only: fp16 [num_blocks][num_kv_heads][block_size]
+    const __half *v_scale;
 };
 
 // barrier slots (uint64 each) inside the barrier area
@@ -119,6 +145,11 @@ struct Bars {
     __device__ uint32_t p_full(int t) const { return base + 8 * (20 + t); }
     __device__ uint32_t v_tail() const { return base + 8 * 22; }
     __device__ uint32_t tmem_slot() const { return base + 8 * 23; }
+    // INT8 variant: raw code tiles landed, per-key factors written, Q converted
+    __device__ uint32_t k_load(int s) const { return base + 8 * (25 + s); }
+    __device__ uint32_t v_load(int s) const { return base + 8 * (29 + s); }
+    __device__ uint32_t sc_full(int i) const { return base + 8 * (33 + i); }
+    __device__ uint32_t q_ready(int t) const { return base + 8 * (35 + t); }
 };
 constexpr int kTmemSlotOffset = 8 * 23;
 static_assert(kIterRing == 4, "barrier slots 10..13");
@@ -140,12 +171,74 @@ struct Waiter {
     }
 };
 
+constexpr uint32_t kFlip = 0x80808080u;  // int8 -> offset binary (x + 128), per byte
+constexpr uint32_t kMagic = 0x64806480u; // f16x2 (1152, 1152)
+
+// Two offset-binary codes of u (bytes chosen by sel) -> f16x2 of the signed
+// codes, exactly: the f16 bit pattern 0x6400 | (x + 128) is 1152 + x.
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u, uint32_t sel)
+{
+    return ptx::sub_f16x2(ptx::prmt(u, 0x64646464u, sel), kMagic);
+}
+
+// Raw int8 code rows of a staged key tile -> f16 codes (exact, |code| <= 127)
+// in the 128B-swizzled layout the MMAs read (panels of 64 elements x 128
+// rows, the layout TMA gives the bf16 tiles).  One warp; D/16 lanes per row.
+template <int D, bool kInPlace>
+__device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int lane)
+{
+    constexpr int LPR = D / 16;   // lanes per row, 16 codes each
+    constexpr int RPP = 32 / LPR; // rows per pass
+    const int sub = lane / LPR, l = lane % LPR;
+    const int panel = l >> 2;     // 4 lanes cover one 64-element panel row
+    const int c0 = (l & 3) * 2;   // first of the lane's two 16-byte chunks
+    const int h0 = panel & 1;     // second-panel lanes store their chunks in the other order (no bank conflict)
+#pragma unroll 4
+    for (int t = sub; t < 128; t += RPP) {
+        const uint4 w = ptx::lds_v4(codes + t * D + 16 * l);
+        if constexpr (kInPlace)
+            __syncwarp(); // row t's codes are read before its second panel is written over them
+        uint32_t o[8];
+        const uint32_t u[4] = {w.x ^ kFlip, w.y ^ kFlip, w.z ^ kFlip, w.w ^ kFlip};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            o[2 * i] = codes_to_f16x2(u[i], 0x4140u);
+            o[2 * i + 1] = codes_to_f16x2(u[i], 0x4342u);
+        }
+        const uint32_t row = tile + panel * (128 * 128) + t * 128;
+        const uint32_t ca = (uint32_t)(((c0 + h0) ^ (t & 7)) << 4), cb = (uint32_t)(((c0 + (h0 ^ 1)) ^ (t & 7)) << 4);
+        if (h0) {
+            ptx::sts_v4(row + ca, o[4], o[5], o[6], o[7]);
+            ptx::sts_v4(row + cb, o[0], o[1], o[2], o[3]);
+        } else {
+            ptx::sts_v4(row + ca, o[0], o[1], o[2], o[3]);
+            ptx::sts_v4(row + cb, o[4], o[5], o[6], o[7]);
+        }
+    }
+}
+
+// A landed bf16 query tile -> f16 in place (element-wise, layout unchanged),
+// saturating at +-65504.
 template <int D>
+__device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int lane)
+{
+    for (int i = lane; i < 128 * D / 8; i += 32) {
+        uint4 *c = reinterpret_cast<uint4 *>(tile + 16 * i);
+        uint4 v = *c;
+        v.x = ptx::pack_f16_sat(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+        v.y = ptx::pack_f16_sat(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+        v.z = ptx::pack_f16_sat(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+        v.w = ptx::pack_f16_sat(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+        *c = v;
+    }
+}
+
+template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PfParams p)
 {
-    using L = PfLayout<D>;
+    using L = PfLayout<D, I8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -185,6 +278,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kIterRing; ++s)
             ptx::mbar_init(bars.released(s), 1);
         ptx::mbar_init(bars.v_tail(), 1);
+        if constexpr (I8) {
+            for (int s = 0; s < L::kKStages; ++s)
+                ptx::mbar_init(bars.k_load(s), 1);
+            for (int s = 0; s < L::kVStages; ++s)
+                ptx::mbar_init(bars.v_load(s), 1);
+            for (int i = 0; i < 2; ++i) {
+                ptx::mbar_init(bars.sc_full(i), 1);
+                ptx::mbar_init(bars.q_ready(i), 1);
+            }
+        }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -197,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kTmemSlotOffset);
 
-    if (warp == kKProducerWarp || warp == kVProducerWarp) {
+    if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
         // ---------------------------------------------------------------- TMA producers (K + Q, V)
         const bool is_k = warp == kKProducerWarp;
         const int bs = p.block_size;
@@ -289,11 +392,169 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive(bars.v_tail());
             }
         }
+    } else if (I8 && warp == kLoaderWarp) {
+        // ---------------------------------------------------------------- INT8: TMA loader (Q, K codes, V codes)
+        const int bs = p.block_size;
+        const int box_rows = bs < 128 ? bs : 128;
+        const int nsub = 128 / box_rows;
+        const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
+        if (G * P < 128) {
+            // rows G*P..127 of each query tile receive no TMA data: zero them once
+            const int first = G * P, chunks = (128 - first) * 8;
+            for (int t = 0; t < 2; ++t)
+                for (int pp = 0; pp < L::kPanels; ++pp)
+                    for (int c = lane; c < chunks; c += 32)
+                        *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
+                                                   (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+        }
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tm_k);
+            ptx::prefetch_tmap(&tm_v);
+            ptx::prefetch_tmap(&tm_q);
+            for (int t = 0; t < 2; ++t) {
+                if ((t == 0 ? npos0 : npos1) <= 0)
+                    continue;
+                ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
+                for (int pp = 0; pp < L::kPanels; ++pp)
+                    ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, &tm_q, bars.q_full(t),
+                                     pp * 64, g * G, cq0 + q0 + t * P);
+            }
+        }
+        auto sub_row = [&](int j) -> int {
+            const int key = j * 128 + lane * box_rows;
+            if (lane >= nsub || key >= lk)
+                return p.num_slots; // fully out of range: TMA fills zeros
+            const int phys = __ldg(bt + key / bs);
+            return phys * bs + (key & (bs - 1));
+        };
+        // raw codes of key tile j (one box of D bytes x box_rows per block) into the staging slot
+        auto load = [&](bool is_k, int j, int cur) {
+            const int st = j % (is_k ? L::kKStages : L::kVStages);
+            const uint32_t bar = is_k ? bars.k_load(st) : bars.v_load(st);
+            const uint32_t dst = sbase + (is_k ? L::k_codes(st) : L::v_codes(st));
+            if (lane == 0)
+                ptx::mbar_arrive_expect_tx(bar, (uint32_t)L::kCodeBytes);
+            for (int i = 0; i < nsub; ++i) {
+                const int row = __shfl_sync(0xffffffffu, cur, i);
+                if (lane == 0)
+                    ptx::tma_load_3d(dst + i * box_rows * D, is_k ? &tm_k : &tm_v, bar, 0, g, row);
+            }
+            __syncwarp();
+        };
+        int next = sub_row(0);
+        for (int j = 0; j < nkt; ++j) {
+            const int cur = next;
+            if (j + 1 < nkt)
+                next = sub_row(j + 1);
+            // K tile j replaces tile j - S_K: free after release event j - S_K
+            if (j >= L::kKStages) {
+                const int e = j - L::kKStages;
+                if (!__all_sync(0xffffffffu, wait(bars.released(e), (e / kIterRing) & 1)))
+                    break;
+            }
+            load(true, j, cur);
+            // V tile j replaces tile j - S_V: free after release event j - S_V + 1
+            if (j >= L::kVStages) {
+                const int e = j - L::kVStages + 1;
+                if (!__all_sync(0xffffffffu, wait(bars.released(e), (e / kIterRing) & 1)))
+                    break;
+            }
+            load(false, j, cur);
+        }
+    } else if (I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
+        // ---------------------------------------------------------------- INT8: converters
+        // warp 8: query tile 0 and every K tile; warp 10: query tile 1, every V
+        // tile and the per-key factors.  Codes become exact f16 values; the scales
+        // are applied after the products (softmax), not to the tiles.
+        const bool is_k = warp == kKProducerWarp;
+        const int tq = is_k ? 0 : 1;
+        bool ok = true;
+        if ((tq == 0 ? npos0 : npos1) > 0) {
+            ok = __all_sync(0xffffffffu, wait(bars.q_full(tq), 0));
+            if (ok) {
+                q_tile_to_f16<D>(sgen + L::kQ + tq * L::kTileBytes, lane);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bars.q_ready(tq));
+            }
+        }
+        if (is_k) {
+            for (int j = 0; ok && j < nkt; ++j) {
+                const int st = j % L::kKStages;
+                if (!(ok = __all_sync(0xffffffffu, wait(bars.k_load(st), (j / L::kKStages) & 1))))
+                    break;
+                convert_codes<D, L::kInPlace>(sbase + L::k_codes(st), sbase + L::kK + st * L::kTileBytes, lane);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bars.k_full(st));
+            }
+        } else {
+            // factors of key tile j, keys 4*lane .. 4*lane+3 (one block: bs >= 16)
+            const int bs = p.block_size, Hkv = p.num_kv_heads;
+            const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
+            const float sl2 = p.scale_log2;
+            auto fetch = [&](int j, uint2 &kr, uint2 &vr) {
+                const int key = j * 128 + 4 * lane;
+                kr = vr = make_uint2(0u, 0u);
+                if (key < lk) {
+                    const int phys = __ldg(bt + key / bs);
+                    const size_t si = ((size_t)phys * Hkv + g) * bs + (key & (bs - 1));
+                    kr = __ldg(reinterpret_cast<const uint2 *>(p.k_scale + si));
+                    vr = __ldg(reinterpret_cast<const uint2 *>(p.v_scale + si));
+                }
+            };
+            uint2 kr, vr;
+            fetch(0, kr, vr);
+            for (int j = 0; ok && j < nkt; ++j) {
+                // slot j & 1 held tile j - 2's factors, read until release event j - 1
+                if (j >= 2 && !(ok = __all_sync(0xffffffffu,
+                                                 wait(bars.released(j - 1), ((j - 1) / kIterRing) & 1))))
+                    break;
+                {
+                    const int key = j * 128 + 4 * lane;
+                    const uint32_t kw[2] = {kr.x, kr.y}, vw[2] = {vr.x, vr.y};
+                    float kf[4], vf[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        // keys past the sequence: factor 0 (their scores are masked, their weights 0)
+                        const bool valid = key + i < lk;
+                        const float ks = __half2float(__ushort_as_half((unsigned short)(kw[i >> 1] >> (16 * (i & 1)))));
+                        const float vs = __half2float(__ushort_as_half((unsigned short)(vw[i >> 1] >> (16 * (i & 1)))));
+                        kf[i] = valid ? ks * sl2 : 0.f;
+                        vf[i] = valid ? vs : 0.f;
+                    }
+                    float *slot = reinterpret_cast<float *>(sgen + L::kScl + (j & 1) * L::kSclSlot);
+                    *reinterpret_cast<float4 *>(slot + 4 * lane) = make_float4(kf[0], kf[1], kf[2], kf[3]);
+                    *reinterpret_cast<float4 *>(slot + 128 + 4 * lane) = make_float4(vf[0], vf[1], vf[2], vf[3]);
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(bars.sc_full(j & 1));
+                }
+                if (j + 1 < nkt)
+                    fetch(j + 1, kr, vr);
+                const int st = j % L::kVStages;
+                if (!(ok = __all_sync(0xffffffffu, wait(bars.v_load(st), (j / L::kVStages) & 1))))
+                    break;
+                convert_codes<D, L::kInPlace>(sbase + L::v_codes(st), sbase + L::kV + st * L::kTileBytes, lane);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::mbar_arrive(bars.v_full(st));
+                    if (tail && j == nkt - 1)
+                        ptx::mbar_arrive(bars.v_tail()); // codes are finite and weights past the end 0: nothing to zero
+                }
+            }
+        }
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0);
-            constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 1);
+            // INT8 cache: f16 operands (exact codes, f16 Q and P)
+            constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
+            constexpr uint32_t idesc_o = I8 ? ptx::idesc_f16(128, D, 1) : ptx::idesc_bf16(128, D, 1);
             auto issue_s = [&](int t, int ks) {
                 const uint32_t qa = sbase + L::kQ + t * L::kTileBytes, kb = sbase + L::kK + ks * L::kTileBytes;
 #pragma unroll
@@ -311,9 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      ptx::smem_desc(vb + kk * 2048, L::kPanelBytes, 1024, ptx::kSwizzle128B), idesc_o,
                                      (!first || kk > 0) ? 1u : 0u);
             };
-            bool ok = wait(bars.q_full(0), 0);
+            bool ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), 0);
             if (ok && nkt1 > 0)
-                ok = wait(bars.q_full(1), 0);
+                ok = wait(I8 ? bars.q_ready(1) : bars.q_full(1), 0);
             ok = ok && wait(bars.k_full(0), 0);
             if (ok) {
                 ptx::tc_fence_after();
@@ -393,6 +654,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < ntile; ++j) {
             if (!(ok = wwait(bars.s_full(t), j & 1)))
                 break;
+            if constexpr (I8) {
+                if (!(ok = wwait(bars.sc_full(j & 1), (j >> 1) & 1)))
+                    break;
+            }
             ptx::tc_fence_after();
             const int lim = limit - j * 128; // columns this row sees in this tile
             // the whole score row in registers: one TMEM round trip per tile
@@ -401,6 +666,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 4; ++q)
                 ptx::tmem_ld32(s_col + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
             ptx::tmem_wait_ld();
+            const float *fac = reinterpret_cast<const float *>(sgen + L::kScl + (j & 1) * L::kSclSlot);
+            if constexpr (I8) {
+                // K scale after the dot product: column c times k_scale[c] * scale * log2 e
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const float4 f = reinterpret_cast<const float4 *>(fac)[q];
+                    float a0, a1, a2, a3;
+                    ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(sr[4 * q]), __uint_as_float(sr[4 * q + 1])),
+                                              ptx::f2(f.x, f.y)),
+                                  a0, a1);
+                    ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3])),
+                                              ptx::f2(f.z, f.w)),
+                                  a2, a3);
+                    sr[4 * q] = __float_as_uint(a0);
+                    sr[4 * q + 1] = __float_as_uint(a1);
+                    sr[4 * q + 2] = __float_as_uint(a2);
+                    sr[4 * q + 3] = __float_as_uint(a3);
+                }
+            }
             if (lim < 128) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
@@ -419,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        : fmaxf(m8[i], __uint_as_float(sr[16 * i + c]));
             const float mx = fmaxf(fmaxf(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5])),
                                    fmaxf(m8[6], m8[7]));
-            const float mt = mx * sl2;
+            const float mt = I8 ? mx : mx * sl2; // INT8: the factors already hold scale * log2 e
             float alpha = 1.f;
             bool rescale = false;
             if (row_valid && (mt > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt != -INFINITY))) {
@@ -430,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = m_new;
             }
             // P = 2^(s * scale * log2 e - m) as bf16 pairs written over S; row sum
-            const uint64_t sl2x2 = ptx::f2(sl2, sl2);
+            const uint64_t sl2x2 = I8 ? ptx::f2(1.f, 1.f) : ptx::f2(sl2, sl2);
             const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
             const uint64_t negm2 = ptx::f2(negm, negm);
             uint64_t sum2[4] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
@@ -444,7 +728,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::f2_fma(ptx::f2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2), x0, x1);
                     const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1); // masked columns: 2^-inf = 0
                     sum2[(c >> 1) & 3] = ptx::f2_add(sum2[(c >> 1) & 3], ptx::f2(e0, e1));
-                    pk[(c >> 1) & 31] = ptx::pack_bf16(e0, e1);
+                    if constexpr (I8) { // V scale folded into P; the row sum keeps the unscaled P
+                        const float2 vsc = *reinterpret_cast<const float2 *>(fac + 128 + c);
+                        pk[(c >> 1) & 31] = ptx::pack_f16(e0 * vsc.x, e1 * vsc.y);
+                    } else {
+                        pk[(c >> 1) & 31] = ptx::pack_bf16(e0, e1);
+                    }
                 }
                 ptx::tmem_st32(s_col + 32 * h, pk);
             }
@@ -521,14 +810,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool I8>
 int launch(const PrefillArgs &a, cudaStream_t stream)
 {
-    using L = PfLayout<D>;
+    using L = PfLayout<D, I8>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e =
-            cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+            cudaFuncSetAttribute(prefill_kernel<D, I8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
         if (e != cudaSuccess)
             return fail(PA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
         configured = true;
@@ -545,12 +834,23 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
         PA_OK)
         return rc;
     const uint32_t box_rows = d.block_size < 128 ? (uint32_t)d.block_size : 128u;
-    if ((rc = encode_tmap_3d(&tk, bf16, a.k_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
-                             (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "k_cache")) != PA_OK)
-        return rc;
-    if ((rc = encode_tmap_3d(&tv, bf16, a.v_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
-                             (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "v_cache")) != PA_OK)
-        return rc;
+    if constexpr (I8) { // raw codes: one head's D bytes x box_rows rows, unswizzled
+        constexpr CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+        constexpr CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
+        if ((rc = encode_tmap_3d(&tk, u8, a.k_cache, D, d.num_kv_heads, rows, (uint64_t)D, (uint64_t)d.num_kv_heads * D,
+                                 D, 1, box_rows, none, "int8 k_cache")) != PA_OK)
+            return rc;
+        if ((rc = encode_tmap_3d(&tv, u8, a.v_cache, D, d.num_kv_heads, rows, (uint64_t)D, (uint64_t)d.num_kv_heads * D,
+                                 D, 1, box_rows, none, "int8 v_cache")) != PA_OK)
+            return rc;
+    } else {
+        if ((rc = encode_tmap_3d(&tk, bf16, a.k_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
+                                 (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "k_cache")) != PA_OK)
+            return rc;
+        if ((rc = encode_tmap_3d(&tv, bf16, a.v_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
+                                 (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "v_cache")) != PA_OK)
+            return rc;
+    }
     PfParams p{};
     p.cu_seqlens_q = a.cu_seqlens_q;
     p.cu_seqlens_k = a.cu_seqlens_k;
@@ -564,7 +864,10 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     p.block_size = d.block_size;
     p.max_blocks = a.max_blocks_per_seq;
     p.num_slots = (int32_t)rows;
-    prefill_kernel<D><<<(unsigned)a.num_tiles, kThreads, L::kSmemBytes, stream>>>(tq, tk, tv, p);
+    p.num_kv_heads = d.num_kv_heads;
+    p.k_scale = static_cast<const __half *>(a.k_scale);
+    p.v_scale = static_cast<const __half *>(a.v_scale);
+    prefill_kernel<D, I8><<<(unsigned)a.num_tiles, kThreads, L::kSmemBytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
@@ -576,7 +879,13 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
 int launch_prefill(const PrefillArgs &a, void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return a.dims.head_dim == 128 ? launch<128>(a, s) : launch<64>(a, s);
+    return a.dims.head_dim == 128 ? launch<128, false>(a, s) : launch<64, false>(a, s);
+}
+
+int launch_prefill_int8(const PrefillArgs &a, void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return a.dims.head_dim == 128 ? launch<128, true>(a, s) : launch<64, true>(a, s);
 }
 
 int read_prefill_error(uint32_t *code)

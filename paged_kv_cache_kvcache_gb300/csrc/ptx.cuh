@@ -202,6 +202,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int b_mn_major)
            ((uint32_t)(m >> 4) << 24);
 }
 
+// Same with f16 A and B.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, int b_mn_major)
+{
+    return (1u << 4) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
 // ------------------------------------------------------------------ warp-level MMA (decode)
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
@@ -340,6 +346,19 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Round to f16, saturating at +-65504 instead of overflowing to infinity.
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)

@@ -22,6 +22,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0
 
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
            "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
+           "pa_prefill_varlen_int8",
            "pa_last_error_string", "pa_read_device_error", "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
@@ -82,6 +83,7 @@ def lib() -> ctypes.CDLL:
             L.pa_copy_blocks.argtypes = [P, P, P, P, I32, P]
             L.pa_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, P, I32, P]
             L.pa_decode_int8.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
+            L.pa_prefill_varlen_int8.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
             L.pa_last_error_string.argtypes = []
             L.pa_last_error_string.restype = ctypes.c_char_p
             L.pa_read_device_error.argtypes = [P, P]
@@ -296,6 +298,16 @@ def pa_store_kvcache_int8(dims: pa_dims, k, v, k_cache, v_cache, k_scale, v_scal
     _check(lib().pa_store_kvcache_int8(ctypes.byref(dims), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                                        _ptr(k_scale), _ptr(v_scale), _ptr(slot_mapping), n, _stream(stream)),
            "pa_store_kvcache_int8")
+
+
+def pa_prefill_varlen_int8(dims: pa_dims, q, k_cache, v_cache, k_scale, v_scale, plan: PrefillPlan, scale: float,
+                           out, stream=None):
+    """pa_prefill_varlen over an INT8 cache (same plan as pa_prefill_varlen)."""
+    m = plan.meta
+    _check(lib().pa_prefill_varlen_int8(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                        _ptr(v_scale), plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
+                                        plan.dptr(m.off_block_tables), float(scale), _ptr(out), ctypes.byref(m),
+                                        plan.dptr(m.off_tiles), _stream(stream)), "pa_prefill_varlen_int8")
 
 
 def pa_decode_int8(dims: pa_dims, q, k_cache, v_cache, k_scale, v_scale, plan: DecodePlan, scale: float, out,

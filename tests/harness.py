@@ -125,6 +125,20 @@ def int8_equal(gpu, host, what=""):
         assert bad == 0, f"{what}: {bad} of {h.size} {name} differ"
 
 
+def run_gpu_batch_int8(w, batch, cache, split_tokens: int = 0, stream=None):
+    """Quantising store of the batch's new K/V, then INT8 prefill or decode. Returns (out, plan)."""
+    if batch.kind == "decode":
+        return run_gpu_decode_int8(w, batch, cache, split_tokens, stream)
+    dims = dims_of(w, batch)
+    dev = cache[0].device
+    q, k, v = batch.q.to(dev), batch.k.to(dev), batch.v.to(dev)
+    out = torch.empty_like(q)
+    plan = pa.pa_pack_prefill(dims, batch.seq_lens, batch.query_lens, batch.block_lists).upload(dev, stream)
+    pa.pa_store_kvcache_int8(dims, k, v, *cache, plan.slot_mapping, batch.num_tokens, stream=stream)
+    pa.pa_prefill_varlen_int8(dims, q, *cache, plan, batch.scale, out, stream=stream)
+    return out, plan
+
+
 def run_gpu_decode_int8(w, batch, cache, split_tokens: int = 0, stream=None):
     """Quantising store of the batch's new K/V, then INT8 decode. Returns out (bf16, device)."""
     dims = dims_of(w, batch)

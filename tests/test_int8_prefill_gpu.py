@@ -1,0 +1,105 @@
+"""INT8 prefill on the GPU against the oracle's attention over the dequantised cache.
+
+Method: "面试问答准备: nano-vLLM 推理引擎优化", Q3 — per-(token, KV head) INT8
+codes with fp16 scales; the prefill reads the codes directly (key scale after
+the dot product, value scale folded into the softmax weights).  Tolerances
+as for the bf16 path: max |err| <= 2e-2, relative RMS <= 1e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_kvcache_gb300 import pagedattn as pa
+from paged_kv_cache_kvcache_gb300 import workloads
+from tests.harness import assert_close, int8_equal, int8_pools, run_gpu_batch_int8, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_both(w, row_select=None):
+    """Every batch in order on both sides (store, then attention); the caches must stay bit-identical."""
+    gpu, host = int8_pools(w, w.batches[0].num_heads)
+    res = []
+    for batch in w.batches:
+        out, _ = run_gpu_batch_int8(w, batch, gpu)
+        sel = row_select(batch) if callable(row_select) else row_select
+        ref, _ = oracle.run_batch_int8(*host, batch, w.pool.block_size, row_select=sel)
+        res.append((batch, out, ref, sel))
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    int8_equal(gpu, host, what=w.name)
+    return res
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_prefill_32", "qwen3_prefill_128", "qwen3_prefill_256",
+                                  "qwen3_prefix", "qwen3_chunked"])
+def test_int8_prefill_configs(name):
+    """Prefill (and, for the tiny case, the decode step after it) on the INT8 cache."""
+    for batch, out, ref, _ in _run_both(workloads.make(name, device="cuda")):
+        assert_close(out, ref, what=f"int8 {name} {batch.kind}")
+
+
+CASES = [  # seed, num_seqs, hq, hkv, d, bs, max_len, cached
+    (501, 3, 2, 1, 64, 16, 300, None),
+    (502, 4, 4, 2, 64, 256, 700, "random"),
+    (503, 5, 7, 1, 128, 16, 400, "random"),
+    (504, 3, 14, 2, 128, 256, 520, None),
+    (505, 6, 8, 8, 128, 16, 260, "random"),
+    (506, 2, 16, 1, 64, 32, 390, "random"),
+    (507, 4, 28, 4, 128, 16, 333, "random"),
+    (508, 3, 16, 8, 128, 1024, 1100, "random"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c[0]) for c in CASES])
+def test_int8_prefill_random(case):
+    seed, B, hq, hkv, d, bs, max_len, cached = case
+    w = workloads.random_case(seed, num_seqs=B, hq=hq, hkv=hkv, d=d, bs=bs, max_len=max_len, device="cuda",
+                              cached=cached)
+    (batch, out, ref, _), = _run_both(w)
+    assert_close(out, ref, what=f"int8 case {seed}")
+
+
+def test_int8_prefill_edge_lengths():
+    """Sequences with no new tokens, single-token sequences and exact-tile lengths in one batch."""
+    hq, hkv, d, bs = 4, 2, 128, 16
+    lens = np.array([1, 17, 40, 129, 5, 128, 256], np.int32)
+    qlens = np.array([1, 0, 1, 129, 0, 128, 100], np.int32)
+    nb = int(sum(-(-l // bs) for l in lens)) + 2
+    perm = np.random.default_rng(9).permutation(nb).astype(np.int32)
+    blocks, o = [], 0
+    for l in lens:
+        n = -(-int(l) // bs)
+        blocks.append(perm[o:o + n])
+        o += n
+    g = torch.Generator(device="cuda").manual_seed(10)
+    mk = lambda *s: torch.randn(*s, device="cuda", generator=g).to(torch.bfloat16)
+    pool = workloads.Pool(nb, bs, hkv, d, mk(nb, bs, hkv, d), mk(nb, bs, hkv, d))
+    t = int(qlens.sum())
+    batch = workloads.Batch("prefill", lens, qlens, blocks, mk(t, hq, d), mk(t, hkv, d), mk(t, hkv, d), hq, d ** -0.5)
+    (batch, out, ref, _), = _run_both(workloads.Workload("int8_edges", pool, [batch]))
+    assert_close(out, ref, what="int8 edges")
+
+
+def test_int8_prefill_qwen25_sampled():
+    """Qwen2.5-7B attention shape, 4 x 4096 causal prefill (the measured workload), sampled rows."""
+    w = workloads.make("qwen25_prefill", device="cuda")
+    (batch, out, ref, sel), = _run_both(w, row_select=lambda b: sample_rows(b, 24, seed=5))
+    assert_close(out, ref, rows=sel, what="int8 qwen25 prefill (sampled rows)")
+
+
+def test_int8_prefill_matches_int8_decode():
+    """Decode at context n equals row n-1 of an INT8 prefill over the same n tokens (same cache)."""
+    n, hq, hkv, d, bs = 777, 14, 2, 128, 16
+    w = workloads.random_case(13, num_seqs=1, hq=hq, hkv=hkv, d=d, bs=bs, min_len=n, max_len=n, device="cuda",
+                              cached=None)
+    batch = w.batches[0]
+    gpu, _ = int8_pools(w, hq)
+    out_p, _ = run_gpu_batch_int8(w, batch, gpu)
+    dec = workloads.Batch("decode", batch.seq_lens, np.ones(1, np.int32), batch.block_lists, batch.q[-1:],
+                          batch.k[-1:], batch.v[-1:], hq, batch.scale)
+    out_d, _ = run_gpu_batch_int8(w, dec, gpu, split_tokens=128)
+    torch.cuda.synchronize()
+    a, b = out_p[-1].float(), out_d[0].float()
+    assert (a - b).abs().max().item() < 1e-2
