@@ -79,9 +79,8 @@ struct PfLayout {
     static constexpr int kPanelBytes = 128 * 128;   // 128 rows x 128 bytes
     static constexpr int kTileBytes = kPanels * kPanelBytes;
     // K is released as soon as the two score MMAs have read it, V only after
-    // both PV MMAs: K gets the deeper ring so its loads start earliest (the
-    // INT8 variant's extra buffers leave room for two K stages at D = 128).
-    static constexpr int kKStages = I8 ? (D == 128 ? 2 : 3) : (D == 128 ? 3 : 4);
+    // both PV MMAs: K gets the deeper ring so its loads start earliest.
+    static constexpr int kKStages = I8 ? 3 : (D == 128 ? 3 : 4);
     static constexpr int kVStages = I8 ? (D == 128 ? 2 : 3) : (D == 128 ? 2 : 4);
     static constexpr int kQ = 0;                    // two query tiles (also the output staging)
     static constexpr int kK = kQ + 2 * kTileBytes;
@@ -95,7 +94,7 @@ struct PfLayout {
     static constexpr int kStg = kV + kVStages * kTileBytes;
     static constexpr int kStgBytes = I8 && !kInPlace ? (kKStages + kVStages) * kCodeBytes : 0;
     static constexpr int kScl = kStg + kStgBytes;
-    static constexpr int kSclSlot = 2 * 128 * 4; // 128 fp32 K factors, then 128 fp32 V scales
+    static constexpr int kSclSlot = 128 * 4 + 128 * 2; // 128 fp32 K factors, then 128 fp16 V scales
     static constexpr int kSclBytes = I8 ? 2 * kSclSlot : 0;
     static constexpr int kBar = kScl + kSclBytes;
     static constexpr int kBarBytes = 512;
@@ -193,7 +192,7 @@ __device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int
     const int panel = l >> 2;     // 4 lanes cover one 64-element panel row
     const int c0 = (l & 3) * 2;   // first of the lane's two 16-byte chunks
     const int h0 = panel & 1;     // second-panel lanes store their chunks in the other order (no bank conflict)
-#pragma unroll 4
+#pragma unroll 2
     for (int t = sub; t < 128; t += RPP) {
         const uint4 w = ptx::lds_v4(codes + t * D + 16 * l);
         if constexpr (kInPlace)
@@ -516,20 +515,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 {
                     const int key = j * 128 + 4 * lane;
-                    const uint32_t kw[2] = {kr.x, kr.y}, vw[2] = {vr.x, vr.y};
-                    float kf[4], vf[4];
+                    const uint32_t kw[2] = {kr.x, kr.y};
+                    uint32_t vw[2] = {vr.x, vr.y};
+                    float kf[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         // keys past the sequence: factor 0 (their scores are masked, their weights 0)
                         const bool valid = key + i < lk;
                         const float ks = __half2float(__ushort_as_half((unsigned short)(kw[i >> 1] >> (16 * (i & 1)))));
-                        const float vs = __half2float(__ushort_as_half((unsigned short)(vw[i >> 1] >> (16 * (i & 1)))));
                         kf[i] = valid ? ks * sl2 : 0.f;
-                        vf[i] = valid ? vs : 0.f;
+                        if (!valid)
+                            vw[i >> 1] &= (i & 1) ? 0x0000ffffu : 0xffff0000u;
                     }
-                    float *slot = reinterpret_cast<float *>(sgen + L::kScl + (j & 1) * L::kSclSlot);
-                    *reinterpret_cast<float4 *>(slot + 4 * lane) = make_float4(kf[0], kf[1], kf[2], kf[3]);
-                    *reinterpret_cast<float4 *>(slot + 128 + 4 * lane) = make_float4(vf[0], vf[1], vf[2], vf[3]);
+                    uint8_t *slot = sgen + L::kScl + (j & 1) * L::kSclSlot;
+                    *reinterpret_cast<float4 *>(slot + 16 * lane) = make_float4(kf[0], kf[1], kf[2], kf[3]);
+                    *reinterpret_cast<uint2 *>(slot + 512 + 8 * lane) = make_uint2(vw[0], vw[1]); // fp16 V scales
                     __syncwarp();
                     if (lane == 0)
                         ptx::mbar_arrive(bars.sc_full(j & 1));
@@ -718,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
             const uint64_t negm2 = ptx::f2(negm, negm);
             uint64_t sum2[4] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
+            uint4 vs8 = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
             for (int h = 0; h < 2; ++h) { // two halves: P columns 32h..32h+31 hold keys 64h..64h+63
                 uint32_t pk[32];
@@ -729,8 +730,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1); // masked columns: 2^-inf = 0
                     sum2[(c >> 1) & 3] = ptx::f2_add(sum2[(c >> 1) & 3], ptx::f2(e0, e1));
                     if constexpr (I8) { // V scale folded into P; the row sum keeps the unscaled P
-                        const float2 vsc = *reinterpret_cast<const float2 *>(fac + 128 + c);
-                        pk[(c >> 1) & 31] = ptx::pack_f16(e0 * vsc.x, e1 * vsc.y);
+                        if ((c & 7) == 0) // 8 fp16 V scales
+                            vs8 = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(fac) + 512 + 2 * c);
+                        const uint32_t vsw = (c & 7) == 0 ? vs8.x : (c & 7) == 2 ? vs8.y : (c & 7) == 4 ? vs8.z : vs8.w;
+                        pk[(c >> 1) & 31] = ptx::mul_f16x2(ptx::pack_f16(e0, e1), vsw);
                     } else {
                         pk[(c >> 1) & 31] = ptx::pack_bf16(e0, e1);
                     }

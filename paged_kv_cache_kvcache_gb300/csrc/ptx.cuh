@@ -268,6 +268,13 @@ __device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b)
     return d;
 }
 
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr)
 {
     uint4 v;
