@@ -201,6 +201,46 @@ int pa_decode(const pa_dims *dims, const void *q, const void *k_cache, const voi
               void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_pack_decode_fixed — a decode plan whose shapes do not depend on the
+ * contexts, for replaying captured launches (CUDA graphs) across steps.
+ * Source: "手搓 vLLM 推理引擎", Step 5 (ModelRunner): decode runs as a
+ * CUDA graph captured once per batch-size bucket, and at replay the rows a
+ * batch does not use get slot -1 (the store skips it) and context length 0.
+ * Every sequence gets
+ * ceil(max_context / split) key ranges of split_tokens keys (0: one range of
+ * max_context keys), empty ones included, and the block-table rows are
+ * ceil(max_context / block_size) wide; so meta's sizes, offsets, item count
+ * and workspace_bytes depend only on (dims, num_seqs, max_context,
+ * split_tokens).  Re-packing new contexts into the same host buffer,
+ * uploading it to the same device buffer and replaying launches captured
+ * with that meta is valid.  Padding entries: context_lens[b] = 0 (slot -1,
+ * output rows of zeros).  Requires num_seqs >= 1, 1 <= max_context, every
+ * context in [0, max_context], split_tokens 0 or a positive multiple of 64.
+ * Same buffer and error rules as pa_pack_decode.
+ */
+int pa_pack_decode_fixed(const pa_dims *dims, int32_t num_seqs, const int32_t *context_lens,
+                         const int32_t *block_offsets, const int32_t *block_ids, int32_t max_context,
+                         int32_t split_tokens, void *host_buf, size_t host_buf_bytes, pa_decode_meta *meta);
+
+/*
+ * pa_decode_fused — store + decode in one launch: writes k[b], v[b] (bf16
+ * [num_seqs][num_kv_heads][head_dim], the new token of each sequence) into
+ * cache row slot_mapping[b] and returns what pa_store_kvcache followed by
+ * pa_decode returns.  Source: "手搓 vLLM 推理引擎", Step 4 (Attention.forward
+ * stores the new K/V, then attends over the cache including them); fusing
+ * the two removes one launch and the ordering between them.  The work item
+ * that ends at the last key takes that key from k/v and writes the row; the
+ * other items read the cache.  slot_mapping is the plan's (meta
+ * off_slot_mapping); slot -1 writes nothing, other out-of-range slots are
+ * skipped and flagged (pa_read_device_error bit 0).  Same plan, workspace and
+ * error rules as pa_decode.
+ */
+int pa_decode_fused(const pa_dims *dims, const void *q, const void *k, const void *v, void *k_cache, void *v_cache,
+                    const int32_t *slot_mapping, const int32_t *context_lens, const int32_t *block_tables,
+                    float scale, void *out, const pa_decode_meta *meta, const int32_t *items,
+                    const int32_t *seq_items, void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_copy_blocks — copy-on-write of shared cache blocks.  Source: "vLLM /
  * SGLang 面试源码深挖", section 4 (KV block fork): when an append would land in
  * a shared, still-mutable block, the child gets a new block and the valid KV

@@ -65,9 +65,23 @@ struct DecParams {
     int32_t group;
     int32_t block_size;
     int32_t max_blocks;
+    // fused store (FUSED kernels only): the new token's K/V rows, its slot, the context lengths
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    __nv_bfloat16 *k_store;
+    __nv_bfloat16 *v_store;
+    const int32_t *slot_mapping;
+    const int32_t *context_lens;
+    int64_t num_slots;
 };
 
-template <int D, int NT>
+__device__ uint32_t g_fused_error; // bit 0: a fused-store slot outside [-1, num_slots) was skipped
+
+// FUSED: the CTA whose work item ends at the sequence's last key (the token
+// being decoded) writes that token's K/V rows into the cache slot and takes
+// its key from the input instead of the cache, so store and attention need
+// no ordering between launches.
+template <int D, int NT, bool FUSED>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const DecParams p)
 {
     using L = DecLayout<D>;
@@ -75,10 +89,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const DecP
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int4 item = p.items[blockIdx.x / p.num_kv_heads];
-    const int b = item.x, k0 = item.y, k1 = item.z, pslot = item.w;
+    const int b = item.x, k0 = item.y, pslot = item.w;
     const int g = blockIdx.x % p.num_kv_heads;
     const int G = p.group;
     const int Hq = p.num_heads;
+    // FUSED: does this item hold the new token (the last key)?  Then the cache supplies keys k0 .. ctx-2.
+    const bool has_new = FUSED && item.z > 0 && item.z == __ldg(p.context_lens + b);
+    const int k1 = has_new ? item.z - 1 : item.z;
 
     // Q^T fragments: B operand (k = d, n = head) of the score MMA.
     uint32_t qf[NT][D / 16][2];
@@ -236,6 +253,38 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const DecP
     float *mrg_m = reinterpret_cast<float *>(smem);
     float *mrg_l = mrg_m + kWarps * H8;
     float *mrg_o = mrg_l + kWarps * H8; // [warp][head][D]
+    float *s_new = mrg_o + (size_t)kWarps * H8 * D; // FUSED: the new key's score per head (log2 units)
+    if constexpr (FUSED) {
+        if (has_new) {
+            const size_t row = ((size_t)b * p.num_kv_heads + g) * D;
+            // the new key's score for each head of the group: one warp per head, D/32 values per lane
+            for (int hl = warp; hl < G; hl += kWarps) {
+                const __nv_bfloat16 *qr = p.q + ((size_t)b * Hq + (size_t)g * G + hl) * D;
+                float acc_s = 0.f;
+#pragma unroll
+                for (int e = 0; e < D / 32; ++e)
+                    acc_s += __bfloat162float(qr[lane + 32 * e]) * __bfloat162float(p.k_new[row + lane + 32 * e]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    acc_s += __shfl_xor_sync(0xffffffffu, acc_s, o);
+                if (lane == 0)
+                    s_new[hl] = acc_s * p.scale_log2;
+            }
+            // the store: this head's K and V rows of the new token into its slot
+            const int32_t slot = __ldg(p.slot_mapping + b);
+            if (slot >= 0 && slot < p.num_slots) {
+                const size_t dst = ((size_t)slot * p.num_kv_heads + g) * D;
+                for (int i = threadIdx.x; i < 2 * (D / 8); i += blockDim.x) {
+                    const bool isv = i >= D / 8;
+                    const int c = isv ? i - D / 8 : i;
+                    const uint4 v = *reinterpret_cast<const uint4 *>((isv ? p.v_new : p.k_new) + row + 8 * c);
+                    *reinterpret_cast<uint4 *>((isv ? p.v_store : p.k_store) + dst + 8 * c) = v;
+                }
+            } else if (slot != -1 && threadIdx.x == 0) {
+                atomicOr(&g_fused_error, 1u);
+            }
+        }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int h0 = nt * 8 + (lane & 3) * 2;
@@ -264,12 +313,19 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const DecP
         for (int w = 0; w < kWarps; ++w)
             M = fmaxf(M, mrg_m[w * H8 + hl]);
         float Lsum = 0.f, O = 0.f;
+        if (FUSED && has_new)
+            M = fmaxf(M, s_new[hl]);
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
                 const float f = ptx::ex2(mrg_m[w * H8 + hl] - M);
                 Lsum += f * mrg_l[w * H8 + hl];
                 O += f * mrg_o[((size_t)w * H8 + hl) * D + d];
+            }
+            if (FUSED && has_new) { // the new token: weight 2^(s - M), value from the input row
+                const float f = ptx::ex2(s_new[hl] - M);
+                Lsum += f;
+                O += f * __bfloat162float(p.v_new[((size_t)b * p.num_kv_heads + g) * D + d]);
             }
         }
         const float o = Lsum > 0.f ? O / Lsum : 0.f;
@@ -322,13 +378,13 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const float *__rest
         dst[e] = __float2bfloat16_rn(accv[e] * inv);
 }
 
-template <int D, int NT>
+template <int D, int NT, bool FUSED>
 int launch_split(const DecodeArgs &a, const DecParams &p, cudaStream_t stream)
 {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             DecLayout<D>::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, NT, FUSED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout<D>::kSmemBytes);
         if (e != cudaSuccess)
             return fail(PA_ERR_CUDA, "decode smem attribute: %s", cudaGetErrorString(e));
         configured = true;
@@ -336,7 +392,7 @@ int launch_split(const DecodeArgs &a, const DecParams &p, cudaStream_t stream)
     // flat grid, heads of one work item adjacent: they read neighbouring
     // segments of the same token rows at about the same time (DRAM locality)
     dim3 grid((unsigned)(a.num_items * a.dims.num_kv_heads));
-    decode_split_kernel<D, NT><<<grid, kWarps * 32, DecLayout<D>::kSmemBytes, stream>>>(p);
+    decode_split_kernel<D, NT, FUSED><<<grid, kWarps * 32, DecLayout<D>::kSmemBytes, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
@@ -347,9 +403,9 @@ template <int D, int NT>
 int occupancy()
 {
     int n = 0;
-    cudaFuncSetAttribute(decode_split_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(decode_split_kernel<D, NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          DecLayout<D>::kSmemBytes);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, NT>, kWarps * 32,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, NT, false>, kWarps * 32,
                                                       DecLayout<D>::kSmemBytes) != cudaSuccess) {
         cudaGetLastError();
         return 2;
@@ -392,9 +448,33 @@ int launch_decode(const DecodeArgs &a, void *stream)
     p.max_blocks = a.max_blocks_per_seq;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool two = p.group > 8;
+    if (a.k_new) { // fused store + decode
+        p.k_new = static_cast<const __nv_bfloat16 *>(a.k_new);
+        p.v_new = static_cast<const __nv_bfloat16 *>(a.v_new);
+        p.k_store = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.k_cache));
+        p.v_store = static_cast<__nv_bfloat16 *>(const_cast<void *>(a.v_cache));
+        p.slot_mapping = a.slot_mapping;
+        p.context_lens = a.context_lens;
+        p.num_slots = (int64_t)a.dims.num_blocks * a.dims.block_size;
+        if (a.dims.head_dim == 128)
+            return two ? launch_split<128, 2, true>(a, p, s) : launch_split<128, 1, true>(a, p, s);
+        return two ? launch_split<64, 2, true>(a, p, s) : launch_split<64, 1, true>(a, p, s);
+    }
     if (a.dims.head_dim == 128)
-        return two ? launch_split<128, 2>(a, p, s) : launch_split<128, 1>(a, p, s);
-    return two ? launch_split<64, 2>(a, p, s) : launch_split<64, 1>(a, p, s);
+        return two ? launch_split<128, 2, false>(a, p, s) : launch_split<128, 1, false>(a, p, s);
+    return two ? launch_split<64, 2, false>(a, p, s) : launch_split<64, 1, false>(a, p, s);
+}
+
+int read_fused_error(uint32_t *code)
+{
+    uint32_t v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_fused_error, sizeof v);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(g_fused_error, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "reading fused-store error word: %s", cudaGetErrorString(e));
+    *code |= v; // same meaning as the store kernel's bit 0
+    return PA_OK;
 }
 
 // Library-owned decode scratch for pa_decode_static (callers that cannot

@@ -85,6 +85,10 @@ struct DecodeArgs {
     int32_t num_items;
     int32_t max_blocks_per_seq;
     int32_t max_splits;
+    // fused store + decode only (else NULL): new K/V rows [num_seqs][Hkv][D] and their slots
+    const void *k_new;
+    const void *v_new;
+    const int32_t *slot_mapping;
 };
 int launch_decode(const DecodeArgs &a, void *stream);
 int launch_decode_int8(const DecodeArgs &a, void *stream);
@@ -107,5 +111,6 @@ int read_store_error(uint32_t *code);
 int read_prefill_error(uint32_t *code);
 int read_copy_error(uint32_t *code);
 int read_decode_error(uint32_t *code);
+int read_fused_error(uint32_t *code);
 
 } // namespace pa

@@ -307,3 +307,87 @@ extern "C" int pa_pack_decode(const pa_dims *dims, int32_t num_seqs, const int32
     std::memcpy(si, seq_items.data(), sizeof(int32_t) * (num_seqs + 1));
     return PA_OK;
 }
+
+extern "C" int pa_pack_decode_fixed(const pa_dims *dims, int32_t num_seqs, const int32_t *context_lens,
+                                    const int32_t *block_offsets, const int32_t *block_ids, int32_t max_context,
+                                    int32_t split_tokens, void *host_buf, size_t host_buf_bytes,
+                                    pa_decode_meta *meta)
+{
+    int rc = check_dims(dims);
+    if (rc != PA_OK)
+        return rc;
+    if (!meta)
+        return fail(PA_ERR_INVALID_ARG, "meta is NULL");
+    if (num_seqs < 1)
+        return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 1 for a fixed-shape plan");
+    if (!context_lens)
+        return fail(PA_ERR_INVALID_ARG, "context_lens is NULL");
+    if (max_context < 1)
+        return fail(PA_ERR_INVALID_ARG, "max_context must be >= 1");
+    if (split_tokens < 0 || split_tokens % kDecodeStep != 0)
+        return fail(PA_ERR_INVALID_ARG, "split_tokens (%d) must be 0 or a positive multiple of %d", split_tokens,
+                    kDecodeStep);
+    const pa_dims &d = *dims;
+    for (int32_t b = 0; b < num_seqs; ++b)
+        if (context_lens[b] < 0 || context_lens[b] > max_context)
+            return fail(PA_ERR_INVALID_ARG, "context_lens[%d] = %d outside [0, max_context = %d]", b, context_lens[b],
+                        max_context);
+    int32_t mb_used = 1;
+    if ((rc = check_seq_blocks(d, num_seqs, context_lens, block_offsets, block_ids, &mb_used)) != PA_OK)
+        return rc;
+    // every shape below depends on (dims, num_seqs, max_context, split_tokens) only
+    const int32_t split = split_tokens == 0 ? (int32_t)align_up((size_t)max_context, kDecodeStep) : split_tokens;
+    const int32_t S = (max_context + split - 1) / split;
+    const int32_t mb = (int32_t)(((int64_t)max_context + d.block_size - 1) / d.block_size);
+    const int64_t num_items = (int64_t)num_seqs * S;
+    if (num_items > INT32_MAX / 4)
+        return fail(PA_ERR_INVALID_ARG, "too many work items");
+    const int64_t partials = S > 1 ? num_items : 0;
+
+    Layout L;
+    meta->num_seqs = num_seqs;
+    meta->max_blocks_per_seq = mb;
+    meta->num_items = (int32_t)num_items;
+    meta->split_tokens = split;
+    meta->max_splits = S;
+    meta->num_partials = (int32_t)partials;
+    meta->off_context_lens = L.take(sizeof(int32_t) * num_seqs);
+    meta->off_block_tables = L.take(sizeof(int32_t) * (size_t)num_seqs * mb);
+    meta->off_slot_mapping = L.take(sizeof(int32_t) * num_seqs);
+    meta->off_items = L.take(sizeof(int32_t) * 4 * (size_t)num_items);
+    meta->off_seq_items = L.take(sizeof(int32_t) * (num_seqs + 1));
+    meta->total_bytes = L.off;
+    meta->workspace_bytes = partials > 0 ? align_up((size_t)partials * d.num_heads * d.head_dim * 4, 256) +
+                                               align_up((size_t)partials * d.num_heads * 4, 256)
+                                         : 0;
+    if (!host_buf)
+        return PA_OK;
+    if (host_buf_bytes < meta->total_bytes)
+        return fail(PA_ERR_WORKSPACE, "metadata buffer has %zu bytes, needs %llu", host_buf_bytes,
+                    (unsigned long long)meta->total_bytes);
+
+    char *base = static_cast<char *>(host_buf);
+    int32_t *cl = reinterpret_cast<int32_t *>(base + meta->off_context_lens);
+    int32_t *bt = reinterpret_cast<int32_t *>(base + meta->off_block_tables);
+    int32_t *slots = reinterpret_cast<int32_t *>(base + meta->off_slot_mapping);
+    int32_t *it = reinterpret_cast<int32_t *>(base + meta->off_items);
+    int32_t *si = reinterpret_cast<int32_t *>(base + meta->off_seq_items);
+    std::memcpy(cl, context_lens, sizeof(int32_t) * num_seqs);
+    write_block_tables(d, num_seqs, context_lens, block_offsets, block_ids, mb, bt);
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int32_t pos = context_lens[b] - 1; // the token being decoded; -1 (padding entry) writes nothing
+        slots[b] = pos < 0 ? -1 : block_ids[block_offsets[b] + pos / d.block_size] * d.block_size + pos % d.block_size;
+        si[b] = S > 1 ? b * S : 0;
+        for (int32_t s = 0; s < S; ++s) {
+            const int32_t k0 = s * split;
+            const bool empty = k0 >= context_lens[b];
+            int32_t *e = it + 4 * ((size_t)b * S + s);
+            e[0] = b;
+            e[1] = empty ? 0 : k0; // empty ranges are (0, 0): only one item ends at the last key
+            e[2] = empty ? 0 : std::min(context_lens[b], k0 + split);
+            e[3] = S > 1 ? b * S + s : -1;
+        }
+    }
+    si[num_seqs] = S > 1 ? num_seqs * S : 0;
+    return PA_OK;
+}

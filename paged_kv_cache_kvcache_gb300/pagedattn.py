@@ -22,7 +22,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0
 
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
            "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
-           "pa_prefill_varlen_int8",
+           "pa_prefill_varlen_int8", "pa_pack_decode_fixed", "pa_decode_fused",
            "pa_last_error_string", "pa_read_device_error", "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
             L.pa_pack_prefill.argtypes = [P, I32, P, P, P, P, P, SZ, P]
             L.pa_pack_decode.argtypes = [P, I32, P, P, P, I32, P, SZ, P]
+            L.pa_pack_decode_fixed.argtypes = [P, I32, P, P, P, I32, I32, P, SZ, P]
+            L.pa_decode_fused.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_upload.argtypes = [P, P, SZ, P]
             L.pa_store_kvcache.argtypes = [P, P, P, P, P, P, I32, P]
             L.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
@@ -223,6 +225,21 @@ def pa_pack_decode(dims: pa_dims, context_lens, block_lists, split_tokens: int =
     return _pack("pa_pack_decode", pa_decode_meta(), args, into, pin, DecodePlan)
 
 
+def pa_pack_decode_fixed(dims: pa_dims, context_lens, block_lists, max_context: int, split_tokens: int = 0,
+                         pin: bool = True, into: Optional["DecodePlan"] = None) -> "DecodePlan":
+    """Decode plan whose shapes depend only on (dims, len(context_lens), max_context, split_tokens).
+
+    Padding entries have context 0 and an empty block list.  With ``into`` the
+    previous plan's pinned buffer (and, after ``upload``, its device buffer)
+    is reused, so launches captured in a CUDA graph stay valid.
+    """
+    ctx = _i32(context_lens)
+    off, ids = _flatten(block_lists)
+    args = (ctypes.byref(dims), len(ctx), _np_ptr(ctx), _np_ptr(off), _np_ptr(ids), int(max_context),
+            int(split_tokens))
+    return _pack("pa_pack_decode_fixed", pa_decode_meta(), args, into, pin, DecodePlan)
+
+
 def pa_upload(dev_dst, host_src, nbytes: int, stream=None):
     _check(lib().pa_upload(_ptr(dev_dst), _ptr(host_src), int(nbytes), _stream(stream)), "pa_upload")
 
@@ -255,6 +272,18 @@ def pa_decode(dims: pa_dims, q, k_cache, v_cache, plan: DecodePlan, scale: float
                            plan.dptr(m.off_context_lens), plan.dptr(m.off_block_tables), float(scale), _ptr(out),
                            ctypes.byref(m), plan.dptr(m.off_items), plan.dptr(m.off_seq_items), _ptr(workspace),
                            ws_bytes, _stream(stream)), "pa_decode")
+
+
+def pa_decode_fused(dims: pa_dims, q, k, v, k_cache, v_cache, plan: DecodePlan, scale: float, out, workspace=None,
+                    stream=None):
+    """Store each sequence's new K/V row and decode, in one launch (pa_store_kvcache + pa_decode)."""
+    m = plan.meta
+    ws_bytes = int(workspace.numel()) if isinstance(workspace, torch.Tensor) else 0
+    _check(lib().pa_decode_fused(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                 plan.dptr(m.off_slot_mapping), plan.dptr(m.off_context_lens),
+                                 plan.dptr(m.off_block_tables), float(scale), _ptr(out), ctypes.byref(m),
+                                 plan.dptr(m.off_items), plan.dptr(m.off_seq_items), _ptr(workspace), ws_bytes,
+                                 _stream(stream)), "pa_decode_fused")
 
 
 def pa_decode_static(dims: pa_dims, q, k_cache, v_cache, plan: DecodePlan, scale: float, out, stream=None):

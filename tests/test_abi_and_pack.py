@@ -178,3 +178,61 @@ def test_pack_decode_zero_context_is_an_empty_item():
     items = plan.host_array(plan.meta.off_items, 4 * plan.meta.num_items).reshape(-1, 4).tolist()
     assert [0, 0, 0, -1] in items
     assert plan.host_array(plan.meta.off_slot_mapping, 2).tolist() == [-1, 4 * 16 + 3]
+
+
+def _fixed_plan(ctx, max_ctx, split, bs=16, seed=0):
+    rng = np.random.default_rng(seed)
+    nb = sum(-(-int(c) // bs) for c in ctx) + 3
+    perm = rng.permutation(nb).astype(np.int32)
+    blocks, o = [], 0
+    for c in ctx:
+        n = -(-int(c) // bs)
+        blocks.append(perm[o:o + n])
+        o += n
+    dims = pa.make_dims(nb, bs, 8, 2, 128)
+    return pa.pa_pack_decode_fixed(dims, ctx, blocks, max_ctx, split, pin=False), blocks, bs
+
+
+META_SHAPE = ("num_seqs", "max_blocks_per_seq", "num_items", "split_tokens", "max_splits", "num_partials",
+              "off_context_lens", "off_block_tables", "off_slot_mapping", "off_items", "off_seq_items",
+              "total_bytes", "workspace_bytes")
+
+
+@pytest.mark.parametrize("split", [0, 64, 256])
+def test_pack_decode_fixed_shapes_do_not_depend_on_contexts(split):
+    """Graph replay needs the same sizes and offsets for any contexts in the bucket."""
+    metas = []
+    for ctx in ([1000, 17, 0, 512], [1, 1024, 1024, 0], [0, 0, 0, 5], [64, 128, 192, 256]):
+        plan, _, _ = _fixed_plan(np.array(ctx, np.int32), 1024, split)
+        metas.append(tuple(getattr(plan.meta, f) for f in META_SHAPE))
+    assert len(set(metas)) == 1
+    S = -(-1024 // (split or 1024))
+    assert metas[0][2] == 4 * S and metas[0][1] == 64
+
+
+@pytest.mark.parametrize("split", [0, 64, 320])
+def test_pack_decode_fixed_items(split):
+    """Ranges tile [0, ctx) in order, empty ranges are (0, 0), exactly one range ends at ctx."""
+    ctx = np.array([700, 1, 0, 640, 333, 1000], np.int32)
+    plan, blocks, bs = _fixed_plan(ctx, 1000, split, seed=3)
+    m = plan.meta
+    items = plan.host_array(m.off_items, 4 * m.num_items).reshape(-1, 4)
+    S = m.max_splits
+    for b, c in enumerate(ctx):
+        mine = items[b * S:(b + 1) * S]
+        assert (mine[:, 0] == b).all()
+        covered = [k for _, k0, k1, _ in mine for k in range(k0, k1)]
+        assert covered == list(range(int(c)))
+        assert sum(1 for _, k0, k1, _ in mine if k1 == c and k1 > k0) == (1 if c > 0 else 0)
+        assert all((k0, k1) == (0, 0) for _, k0, k1, _ in mine if k1 <= k0)
+        assert list(mine[:, 3]) == (list(range(b * S, (b + 1) * S)) if S > 1 else [-1] * S)
+    slots = plan.host_array(m.off_slot_mapping, len(ctx))
+    for b, c in enumerate(ctx):
+        want = -1 if c == 0 else int(blocks[b][(c - 1) // bs]) * bs + (c - 1) % bs
+        assert slots[b] == want
+
+
+def test_pack_decode_fixed_rejects_contexts_over_the_bucket():
+    ctx = np.array([10, 2000], np.int32)
+    with pytest.raises(pa.PagedAttnError):
+        _fixed_plan(ctx, 1024, 64)
