@@ -39,7 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # this workload: the prefill launch exactly as benched; the decode kernel on 16
 # of the 64 sequences, scaled by 4 (traffic grows with the sequences).  Must be
 # re-captured (or set to None) whenever one of these kernels changes.
-NCU_TRAFFIC = {"qwen25": {"prefill": 232.9e6, "decode": 4.298e9}}
+NCU_TRAFFIC = {"qwen25": {"prefill": 232.2e6, "decode": 4.334e9}}
+NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": None, "decode": 2.214e9}}
 
 
 def parse():
@@ -58,6 +59,11 @@ def parse():
     ap.add_argument("--phase", choices=["both", "prefill", "decode"], default="both",
                     help="run only one phase (small profiling cases); the JSON line needs both")
     ap.add_argument("--decode-seqs", type=int, default=64, help="decode batch (64 = the full workload)")
+    ap.add_argument("--kv", choices=["bf16", "int8"], default="bf16",
+                    help="cache format: bf16, or int8 codes + fp16 scales (quantising store, fused-dequant "
+                         "prefill and decode)")
+    ap.add_argument("--decode-path", choices=["store+decode", "fused"], default="store+decode",
+                    help="fused: pa_decode_fused (bf16 cache only)")
     return ap.parse_args()
 
 
@@ -108,9 +114,11 @@ def prefill_flops(batch) -> float:
     return 4.0 * batch.q.shape[2] * batch.num_heads * pairs
 
 
-def decode_bytes(batch, pool) -> float:
+def decode_bytes(batch, pool, kv_fmt="bf16") -> float:
     ctx = batch.seq_lens.astype(np.int64)
-    kv = float(np.sum(ctx)) * pool.num_kv_heads * pool.head_dim * 2 * 2
+    # K and V per key and KV head: D bf16 values, or D int8 codes + one fp16 scale
+    per = pool.head_dim * 2 if kv_fmt == "bf16" else pool.head_dim + 2
+    kv = float(np.sum(ctx)) * pool.num_kv_heads * per * 2
     qo = 2.0 * batch.q.numel() * 2
     tables = float(np.sum(-(-ctx // pool.block_size))) * 4 + ctx.size * 4
     return kv + qo + tables
@@ -123,10 +131,11 @@ def store_bytes(batch) -> float:
 class Step:
     """Device-resident state of one replica and the calls of one step."""
 
-    def __init__(self, wp, wd, stream):
+    def __init__(self, wp, wd, stream, kv="bf16", fused=False):
         from paged_kv_cache_kvcache_gb300 import pagedattn as pa
         self.pa = pa
         self.s = stream
+        self.int8, self.fused = kv == "int8", fused
         self.wp, self.wd = wp, wd
         self.bp, self.bd = wp.batches[0], wd.batches[0]
         pp, pd = wp.pool, wd.pool
@@ -148,7 +157,21 @@ class Step:
             e.record(stream)
         self.ws = pa.decode_workspace(self.plans_d[0])
         self.i = 0
-        self.launches_per_step = 4 + (1 if self.plans_d[0].meta.num_partials > 0 else 0)
+        self.launches_per_step = 4 + (1 if self.plans_d[0].meta.num_partials > 0 else 0) - (1 if fused else 0)
+        if self.int8:  # INT8 caches: the bf16 pools quantised once, every slot, by the library's store
+            self.c8_p = self._quantised(self.dims_p, pp)
+            self.c8_d = self._quantised(self.dims_d, pd)
+            torch.cuda.current_stream().synchronize()
+
+    def _quantised(self, dims, pool):
+        pa = self.pa
+        n = pool.num_blocks * pool.block_size
+        cache = pa.int8_cache(dims, pool.k_cache.device)
+        slots = torch.arange(n, dtype=torch.int32, device=pool.k_cache.device)
+        pa.pa_store_kvcache_int8(dims, pool.k_cache.view(n, pool.num_kv_heads, pool.head_dim),
+                                 pool.v_cache.view(n, pool.num_kv_heads, pool.head_dim), *cache, slots, n,
+                                 stream=self.s)
+        return cache
 
     def run(self, ev=None, host=None, phase="both"):
         """Enqueue one step; ev = dict of event pairs for per-phase timing; host = e2e buffers."""
@@ -169,11 +192,18 @@ class Step:
             self.bp.v.copy_(host["pv"], non_blocking=True)
         plan_p = pa.pa_pack_prefill(self.dims_p, self.bp.seq_lens, self.bp.query_lens, self.blocks_p,
                                     into=self.plans_p[k]).upload(stream=s)
-        pa.pa_store_kvcache(self.dims_p, self.bp.k, self.bp.v, self.kc_p, self.vc_p, plan_p.slot_mapping,
-                            self.bp.num_tokens, stream=s)
-        rec("pk0")
-        pa.pa_prefill_varlen(self.dims_p, self.bp.q, self.kc_p, self.vc_p, plan_p, self.bp.scale, self.out_p,
-                             stream=s)
+        if self.int8:
+            pa.pa_store_kvcache_int8(self.dims_p, self.bp.k, self.bp.v, *self.c8_p, plan_p.slot_mapping,
+                                     self.bp.num_tokens, stream=s)
+            rec("pk0")
+            pa.pa_prefill_varlen_int8(self.dims_p, self.bp.q, *self.c8_p, plan_p, self.bp.scale, self.out_p,
+                                      stream=s)
+        else:
+            pa.pa_store_kvcache(self.dims_p, self.bp.k, self.bp.v, self.kc_p, self.vc_p, plan_p.slot_mapping,
+                                self.bp.num_tokens, stream=s)
+            rec("pk0")
+            pa.pa_prefill_varlen(self.dims_p, self.bp.q, self.kc_p, self.vc_p, plan_p, self.bp.scale, self.out_p,
+                                 stream=s)
         rec("pk1")
         if host is not None:
             host["po"].copy_(self.out_p, non_blocking=True)
@@ -193,11 +223,21 @@ class Step:
             self.bd.v.copy_(host["dv"], non_blocking=True)
         plan_d = pa.pa_pack_decode(self.dims_d, self.bd.seq_lens, self.blocks_d, into=self.plans_d[k]).upload(stream=s)
         self.up_ev[k].record(s)
-        pa.pa_store_kvcache(self.dims_d, self.bd.k, self.bd.v, self.kc_d, self.vc_d, plan_d.slot_mapping,
-                            self.bd.num_tokens, stream=s)
-        rec("dk0")
-        pa.pa_decode(self.dims_d, self.bd.q, self.kc_d, self.vc_d, plan_d, self.bd.scale, self.out_d, self.ws,
-                     stream=s)
+        if self.int8:
+            pa.pa_store_kvcache_int8(self.dims_d, self.bd.k, self.bd.v, *self.c8_d, plan_d.slot_mapping,
+                                     self.bd.num_tokens, stream=s)
+            rec("dk0")
+            pa.pa_decode_int8(self.dims_d, self.bd.q, *self.c8_d, plan_d, self.bd.scale, self.out_d, self.ws, stream=s)
+        elif self.fused:  # store + decode in one launch: the phase's kernel time includes the store
+            rec("dk0")
+            pa.pa_decode_fused(self.dims_d, self.bd.q, self.bd.k, self.bd.v, self.kc_d, self.vc_d, plan_d,
+                               self.bd.scale, self.out_d, self.ws, stream=s)
+        else:
+            pa.pa_store_kvcache(self.dims_d, self.bd.k, self.bd.v, self.kc_d, self.vc_d, plan_d.slot_mapping,
+                                self.bd.num_tokens, stream=s)
+            rec("dk0")
+            pa.pa_decode(self.dims_d, self.bd.q, self.kc_d, self.vc_d, plan_d, self.bd.scale, self.out_d, self.ws,
+                         stream=s)
         rec("dk1")
         if host is not None:
             host["do"].copy_(self.out_d, non_blocking=True)
@@ -324,8 +364,9 @@ def main():
     wp, wd, wl_desc = make_workload(args.workload, f"cuda:{local}", args.decode_seqs)
     stream = torch.cuda.Stream()
     clocks = Clocks(local, enabled=not args.no_clocks)
+    assert not (args.kv == "int8" and args.decode_path == "fused"), "the fused decode reads a bf16 cache"
     with torch.cuda.stream(stream):
-        step = Step(wp, wd, stream)
+        step = Step(wp, wd, stream, kv=args.kv, fused=args.decode_path == "fused")
         names = ["p0", "pk0", "pk1", "p1", "dk0", "dk1", "d1"]
         for _ in range(args.warmup):
             step.run(phase=args.phase)
@@ -374,12 +415,13 @@ def main():
             d2h = sum(int(host[k].numel() * host[k].element_size()) for k in ("po", "do"))
             e2e = {"value": round(prefill_flops(step.bp) / (e2e_p * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
                    "h2d_bytes_per_step": h2d + meta_bytes, "d2h_bytes_per_step": d2h,
-                   "decode": {"value": round(decode_bytes(step.bd, wd.pool) / (e2e_d * 1e-3) / 1e9 * world, 1),
+                   "decode": {"value": round(decode_bytes(step.bd, wd.pool, args.kv) / (e2e_d * 1e-3) / 1e9 * world,
+                                             1),
                               "unit": "GB/s"},
                    "ms_per_step": round(e2e_p + e2e_d, 4)}
 
     flops = prefill_flops(step.bp)
-    dbytes = decode_bytes(step.bd, wd.pool)
+    dbytes = decode_bytes(step.bd, wd.pool, args.kv)
     eps = 1e-9  # a phase left out with --phase times as ~0
     value = flops / (max(t_prefill_phase, eps) * 1e-3) / 1e12 * world
     decode_gbs = dbytes / (max(t_decode_phase, eps) * 1e-3) / 1e9 * world
@@ -389,20 +431,30 @@ def main():
     t_prefill_phase = max(t_prefill_phase, eps)
     bf16_peak = float(peaks["bf16_tflops"])
     hbm_peak = float(peaks["hbm_gbs"])
-    roof_p = {"kernel": "pa_prefill_varlen (prefill_kernel<128>)", "bound": "tensor", "achieved": round(pk_tflops, 2),
+    int8 = args.kv == "int8"
+    traffic = {} if args.decode_path == "fused" else (NCU_TRAFFIC_INT8 if int8 else NCU_TRAFFIC).get(args.workload, {})
+    roof_p = {"kernel": ("pa_prefill_varlen_int8 (prefill_kernel<128,true>, f16 MMAs)" if int8 else
+                         "pa_prefill_varlen (prefill_kernel<128,false>)"),
+              "bound": "tensor", "achieved": round(pk_tflops, 2),
               "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(pk_tflops / bf16_peak, 4),
-              "peak_source": f"{peak_src} bf16_tflops (burst)",
-              "traffic": NCU_TRAFFIC.get(args.workload, {}).get("prefill"),
+              "peak_source": f"{peak_src} bf16_tflops (burst; f16 has the same nominal rate)",
+              "traffic": traffic.get("prefill"),
               "work_per_launch": flops, "ms_per_launch": round(t_prefill_kernel, 5)}
-    roof_d = {"kernel": "pa_decode (decode_split_kernel<128,1> + decode_combine_kernel<128>)", "bound": "hbm",
+    dk_name = {"bf16": "pa_decode (decode_split_kernel<128,1,false> + decode_combine_kernel<128>)",
+               "int8": "pa_decode_int8 (decode_int8_kernel<128,1> + decode_combine_kernel<128>)"}[args.kv]
+    if args.decode_path == "fused":
+        dk_name = "pa_decode_fused (decode_split_kernel<128,1,true> + decode_combine_kernel<128>)"
+    roof_d = {"kernel": dk_name, "bound": "hbm",
               "achieved": round(dk_gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(dk_gbs / hbm_peak, 4),
               "peak_source": f"{peak_src} hbm_gbs",
-              "traffic": NCU_TRAFFIC.get(args.workload, {}).get("decode") if args.decode_seqs == 64 else None,
+              "traffic": traffic.get("decode") if args.decode_seqs == 64 else None,
               "work_per_launch": dbytes, "ms_per_launch": round(t_decode_kernel, 5)}
     dominant = roof_p if t_prefill_kernel >= t_decode_kernel else roof_d
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and world == 1 and args.phase == "both":
+    # the CPU leg times the bf16 oracle on the default path only
+    if (rank == 0 and not args.no_cpu_baseline and world == 1 and args.phase == "both" and args.kv == "bf16"
+            and args.decode_path == "store+decode"):
         import oracle
         dt_p, fl = oracle_prefill_sample(wp, row_stride=1)
         dt_d, kvb = oracle_decode_sample(wd, nseq=16)
@@ -415,10 +467,11 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 KV, f16 MMA" if int8 else "bf16", "data": "synthetic",
         "config": {"workload": wl_desc, "l2": "inputs larger than L2: the decode phase streams "
                    f"{dbytes / 1e9:.2f} GB per step", "prefill_gflop": round(flops / 1e9, 2),
-                   "decode_kv_gb": round(dbytes / 1e9, 3), "parallelism": f"replicas x{world}"},
+                   "decode_kv_gb": round(dbytes / 1e9, 3), "parallelism": f"replicas x{world}", "kv": args.kv,
+                   "decode_path": args.decode_path},
         "decode": {"value": round(decode_gbs, 1), "unit": "GB/s", "frac_of_hbm": round(decode_gbs / hbm_peak, 4),
                    "seqs_per_s": round(step.bd.num_seqs / (t_decode_phase * 1e-3) * world, 1)},
         "prefill": {"tokens_per_s": round(step.bp.num_tokens / (t_prefill_phase * 1e-3) * world, 1),

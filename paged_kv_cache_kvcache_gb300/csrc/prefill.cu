@@ -26,21 +26,28 @@
 //    per physical block (or one per tile when a block holds >= 128 tokens)
 //    into a K/V ring; boxes past the end of the pool read as zeros and the V
 //    rows past the sequence end are zeroed before use.
-//  * warp 0: TMA producer.  warp 1: TMEM allocation + single-thread
-//    tcgen05.mma issue.  Each query tile t owns 256 TMEM columns: S_t (128
-//    fp32 columns, reused for P_t as packed bf16) and O_t.  The issue order
-//    PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core busy on one
-//    tile while the other tile's softmax runs (ping-pong).  Because the MMAs of
-//    one thread execute in order, S_t(j+1) being complete means PV_t(j) is
-//    too: O_t is stable and P_t consumed when the softmax sees S_t(j+1).
-//  * warps 4-7 and 8-11: one softmax warpgroup per query tile, one query row
-//    per thread: tcgen05.ld of the score row in two passes (row max, then
-//    exponentials), causal mask only on tiles that cross the diagonal, fp32
-//    online softmax in base 2 (scale * log2 e folded into one packed FMA),
-//    lazy O rescale (only when the running max grows by more than 2^8), P
-//    written back over S with tcgen05.st and consumed by the PV MMA straight
-//    from tensor memory; epilogue O / l -> bf16 -> shared staging ->
-//    coalesced row stores.
+//  * warp 8: K + Q TMA producer; warp 10: V producer; warp 9: TMEM owner and
+//    the single thread issuing every tcgen05.mma.  Each query tile t owns 256
+//    TMEM columns: S_t (128 fp32 columns, reused for P_t) and O_t.  The issue
+//    order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core busy on
+//    one tile while the other tile's softmax runs (ping-pong).  Because the
+//    MMAs of one thread execute in order, S_t(j+1) being complete means
+//    PV_t(j) is too: O_t is stable and P_t consumed when the softmax sees
+//    S_t(j+1).
+//  * warps 0-3 and 4-7: one softmax warpgroup per query tile, one query row
+//    per thread: one tcgen05.ld round trip of the score row, causal mask only
+//    on tiles that cross the diagonal, fp32 online softmax in base 2
+//    (scale * log2 e folded into one packed FMA), lazy O rescale (only when
+//    the running max grows by more than 2^8), P written back over S with
+//    tcgen05.st and consumed by the PV MMA straight from tensor memory;
+//    epilogue O / l -> bf16 -> shared staging -> coalesced row stores.
+//  * INT8 cache (prefill_kernel<D, true>; "面试问答准备: nano-vLLM 推理引擎优化",
+//    Q3 and its follow-up on where the scales go): warp 11 issues every TMA
+//    load, raw code tiles land next to (D = 128: inside) the tiles they are
+//    converted into, warps 8 and 10 turn codes into exact f16 values and Q
+//    into f16, the MMAs run kind::f16, and the softmax applies the key scale
+//    to each score column after the dot product and folds the value scale
+//    into P, keeping the unscaled P for the row sum.
 //  * mbarriers order every hand-off; every wait is bounded and reports a
 //    timeout through a device error word instead of hanging.
 #include <cuda.h>
