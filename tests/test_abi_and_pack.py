@@ -236,3 +236,50 @@ def test_pack_decode_fixed_rejects_contexts_over_the_bucket():
     ctx = np.array([10, 2000], np.int32)
     with pytest.raises(pa.PagedAttnError):
         _fixed_plan(ctx, 1024, 64)
+
+
+def test_int8_fused_and_copy_calls_reject_bad_args_without_touching_the_gpu():
+    """Host-side checks of the INT8, fused-decode and block-copy entry points (no launch on failure)."""
+    dims = pa.make_dims(4, 16, 4, 2, 64)
+    L = pa.lib()
+    f = ctypes.c_float
+    # quantising store: NULL scales, misaligned scales, zero tokens is a no-op
+    assert L.pa_store_kvcache_int8(ctypes.byref(dims), 16, 16, 16, 16, None, 16, 16, 1, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_store_kvcache_int8(ctypes.byref(dims), 16, 16, 16, 16, 24, 16, 16, 1, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_store_kvcache_int8(ctypes.byref(dims), None, None, None, None, None, None, None, 0, None) == pa.PA_OK
+    assert L.pa_store_kvcache_int8(ctypes.byref(dims), 16, 16, 16, 16, 16, 16, 16, -2, None) == pa.PA_ERR_INVALID_ARG
+    # INT8 decode: NULL / misaligned scales, bad scale value, short workspace
+    dm = pa.pa_decode_meta()
+    dm.num_items, dm.num_seqs, dm.max_blocks_per_seq, dm.max_splits = 1, 1, 1, 1
+    args = (ctypes.byref(dims), 16, 16, 16)
+    assert L.pa_decode_int8(*args, None, 16, 16, 16, f(0.1), 16, ctypes.byref(dm), 16, 16, None, 0,
+                            None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_decode_int8(*args, 16, 40, 16, 16, f(0.1), 16, ctypes.byref(dm), 16, 16, None, 0,
+                            None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_decode_int8(*args, 16, 16, 16, 16, f(float("nan")), 16, ctypes.byref(dm), 16, 16, None, 0,
+                            None) == pa.PA_ERR_INVALID_ARG
+    dm.workspace_bytes = 512
+    assert L.pa_decode_int8(*args, 16, 16, 16, 16, f(0.1), 16, ctypes.byref(dm), 16, 16, None, 0,
+                            None) == pa.PA_ERR_WORKSPACE
+    dm.workspace_bytes = 0
+    # INT8 prefill: unsupported dims are rejected before anything else
+    bad = pa.make_dims(4, 16, 4, 2, 96)
+    pm = pa.pa_prefill_meta()
+    pm.num_tiles, pm.total_q, pm.num_seqs, pm.max_blocks_per_seq, pm.rows_per_tile = 1, 1, 1, 1, 64
+    assert L.pa_prefill_varlen_int8(ctypes.byref(bad), 16, 16, 16, 16, 16, 16, 16, 16, f(0.1), 16, ctypes.byref(pm),
+                                    16, None) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_prefill_varlen_int8(ctypes.byref(dims), 16, 16, 16, None, 16, 16, 16, 16, f(0.1), 16,
+                                    ctypes.byref(pm), 16, None) == pa.PA_ERR_INVALID_ARG
+    # fused decode: NULL new-token rows or slot mapping
+    assert L.pa_decode_fused(ctypes.byref(dims), 16, None, 16, 16, 16, 16, 16, 16, f(0.1), 16, ctypes.byref(dm), 16,
+                             16, None, 0, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_decode_fused(ctypes.byref(dims), 16, 16, 16, 16, 16, None, 16, 16, f(0.1), 16, ctypes.byref(dm), 16,
+                             16, None, 0, None) == pa.PA_ERR_INVALID_ARG
+    # block copy: negative count, NULL triples, zero triples is a no-op
+    assert L.pa_copy_blocks(ctypes.byref(dims), 16, 16, 16, -1, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_copy_blocks(ctypes.byref(dims), 16, 16, None, 2, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_copy_blocks(ctypes.byref(dims), None, None, None, 0, None) == pa.PA_OK
+    # static-scratch decode: a plan larger than the library array is refused
+    dm.workspace_bytes = pa.PA_DECODE_STATIC_SCRATCH_BYTES + 256
+    assert L.pa_decode_static(ctypes.byref(dims), 16, 16, 16, 16, 16, f(0.1), 16, ctypes.byref(dm), 16, 16,
+                              None) == pa.PA_ERR_WORKSPACE
