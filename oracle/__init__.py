@@ -9,6 +9,7 @@ per-step citations):
   * ``slot_mapping``   - slot of each new token (nano-vllm walkthrough, Step 5)
   * ``store_kvcache``  - bit copy of K/V rows into their slots, -1 skipped (Step 4)
   * ``copy_blocks``    - copy-on-write fork of a shared block's valid rows (vLLM/SGLang labs §4)
+  * ``copy_blocks_int8`` - the same fork on an INT8 cache (codes and per-head scale runs)
   * ``gather_dense``   - block_table[pos // bs], pos % bs resolution (mini-infer §2.2-2.3)
   * ``paged_attention``- causal softmax(q K^T * scale) V, bottom-right aligned,
                          in double precision (KV-cache toy of the inference notes)
@@ -57,6 +58,9 @@ def _load():
             lib.oracle_store_kvcache.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_int64]
             lib.oracle_copy_blocks.restype = None
             lib.oracle_copy_blocks.argtypes = [P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int64]
+            lib.oracle_copy_blocks_int8.restype = None
+            lib.oracle_copy_blocks_int8.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int]
             lib.oracle_gather_dense.restype = None
             lib.oracle_gather_dense.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
             lib.oracle_paged_attention.restype = ctypes.c_int64
@@ -140,6 +144,17 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, triples, block_size: i
     tr = np.ascontiguousarray(np.asarray(triples, dtype=np.int32).reshape(-1, 3))
     row = int(np.prod(k_cache.shape[2:]))
     lib.oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(tr), tr.shape[0], block_size, row)
+
+
+def copy_blocks_int8(k_cache: np.ndarray, v_cache: np.ndarray, k_scale: np.ndarray, v_scale: np.ndarray,
+                     triples) -> None:
+    """In place on an INT8 cache: codes [nb, bs, Hkv, D] int8, scales [nb, Hkv, bs] fp16 bits."""
+    lib = _load()
+    tr = np.ascontiguousarray(np.asarray(triples, dtype=np.int32).reshape(-1, 3))
+    nb, bs, hkv, d = k_cache.shape
+    assert k_scale.shape == (nb, hkv, bs)
+    lib.oracle_copy_blocks_int8(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(tr), tr.shape[0],
+                                bs, hkv, d)
 
 
 def gather_dense(cache, length: int, blocks, block_size: int) -> np.ndarray:

@@ -235,6 +235,29 @@ void oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *tri
 }
 
 /*
+ * Block copy of an INT8 cache: the same (src, dst, n) triples move the codes
+ * of rows src*bs + i to dst*bs + i (i < n) and, for every KV head g, the
+ * scales [src][g][i] to [dst][g][i] (scale layout [blocks][Hkv][bs]).
+ */
+void oracle_copy_blocks_int8(int8_t *k_cache, int8_t *v_cache, uint16_t *k_scale, uint16_t *v_scale,
+                             const int32_t *triples, int64_t num_triples, int block_size, int num_kv_heads,
+                             int head_dim)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    for (int64_t t = 0; t < num_triples; ++t) {
+        const int64_t src = triples[3 * t], dst = triples[3 * t + 1], n = triples[3 * t + 2];
+        for (int64_t i = 0; i < n; ++i) {
+            memcpy(k_cache + (dst * block_size + i) * row, k_cache + (src * block_size + i) * row, (size_t)row);
+            memcpy(v_cache + (dst * block_size + i) * row, v_cache + (src * block_size + i) * row, (size_t)row);
+            for (int g = 0; g < num_kv_heads; ++g) {
+                k_scale[(dst * num_kv_heads + g) * block_size + i] = k_scale[(src * num_kv_heads + g) * block_size + i];
+                v_scale[(dst * num_kv_heads + g) * block_size + i] = v_scale[(src * num_kv_heads + g) * block_size + i];
+            }
+        }
+    }
+}
+
+/*
  * Dense rebuild of one sequence's keys (or values) through its block list:
  * dense[j][g][d] = cache[blk[j / bs]][j % bs][g][d], for j < len.
  */

@@ -304,6 +304,36 @@ def test_copy_blocks_matches_fancy_index():
     assert np.array_equal(k, want_k) and np.array_equal(v, want_v)
 
 
+def test_copy_blocks_int8_commutes_with_quantisation():
+    """Forking a quantised cache equals quantising the forked bf16 cache: quantisation is per
+    (token, KV head) and the fork moves whole tokens (a wrong scale index breaks this)."""
+    g = torch.Generator().manual_seed(33)
+    nb, bs, hkv, d = 10, 16, 3, 8
+    pool_k = torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16)
+    pool_v = torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16)
+    triples = np.array([[0, 5, 16], [3, 7, 9], [4, 9, 0], [1, 6, 1], [2, 8, 15]], np.int32)
+
+    def quantised(kb, vb):
+        kc, ks = oracle.quantize_rows(kb)
+        vc, vs = oracle.quantize_rows(vb)
+        return (kc.copy(), vc.copy(), np.ascontiguousarray(ks.transpose(0, 2, 1)),
+                np.ascontiguousarray(vs.transpose(0, 2, 1)))
+
+    a = quantised(pool_k, pool_v)
+    oracle.copy_blocks_int8(*a, triples)
+    kb, vb = _bits(pool_k), _bits(pool_v)
+    oracle.copy_blocks(kb, vb, triples, bs)
+    b = quantised(torch.from_numpy(kb.view(np.int16)).view(torch.bfloat16),
+                  torch.from_numpy(vb.view(np.int16)).view(torch.bfloat16))
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    # and blocks outside every dst are untouched
+    c = quantised(pool_k, pool_v)
+    for x, y in zip(a, c):
+        untouched = [blk for blk in range(nb) if blk not in triples[:, 1]]
+        assert np.array_equal(x[untouched], y[untouched])
+
+
 # ---------------------------------------------------------------- INT8 KV cache
 
 
