@@ -322,6 +322,17 @@ int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cac
                            const pa_prefill_meta *meta, const int32_t *tiles, pa_stream_t stream);
 
 /*
+ * pa_copy_blocks_int8 — pa_copy_blocks on an INT8 cache: for each (src, dst, n)
+ * triple the codes of rows src*bs + i go to dst*bs + i and, for every KV head
+ * g, the scales [src][g][i] to [dst][g][i], i < n, bit for bit (the
+ * copy-on-write fork of "vLLM / SGLang 面试源码深挖", section 4, on the cache
+ * of "面试问答准备: nano-vLLM 推理引擎优化", Q3).  Same triple rules and error
+ * flag (bit 2) as pa_copy_blocks.
+ */
+int pa_copy_blocks_int8(const pa_dims *dims, void *k_cache, void *v_cache, void *k_scale, void *v_scale,
+                        const int32_t *triples, int32_t num_triples, pa_stream_t stream);
+
+/*
  * pa_decode_static — pa_decode for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point: it exists for callers
  * that have no way to obtain a decode workspace, e.g. code that runs while a

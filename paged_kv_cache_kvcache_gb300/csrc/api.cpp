@@ -328,6 +328,24 @@ extern "C" int pa_copy_blocks(const pa_dims *dims, void *k_cache, void *v_cache,
     return launch_copy_blocks(*dims, k_cache, v_cache, triples, num_triples, stream);
 }
 
+extern "C" int pa_copy_blocks_int8(const pa_dims *dims, void *k_cache, void *v_cache, void *k_scale, void *v_scale,
+                                   const int32_t *triples, int32_t num_triples, pa_stream_t stream)
+{
+    int rc = check_dims(dims);
+    if (rc != PA_OK)
+        return rc;
+    if (num_triples < 0)
+        return fail(PA_ERR_INVALID_ARG, "num_triples < 0");
+    if (num_triples == 0)
+        return PA_OK;
+    if (!k_cache || !v_cache || !k_scale || !v_scale || !triples)
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks_int8: NULL pointer");
+    if (misaligned(k_cache) || misaligned(v_cache) || misaligned(k_scale) || misaligned(v_scale) ||
+        (reinterpret_cast<uintptr_t>(triples) & 3u))
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks_int8: misaligned pointer");
+    return launch_copy_blocks(*dims, k_cache, v_cache, triples, num_triples, stream, k_scale, v_scale);
+}
+
 // pa_decode for callers that cannot allocate: the workspace is the library's
 // own scratch array (see the header for its limit, set-up and sharing rules).
 extern "C" int pa_decode_static(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,

@@ -8,7 +8,8 @@
 // (PagedAttention paragraph): shared blocks are copied on write, as in fork.
 //
 // Each (src, dst, n) triple copies cache rows src*bs + i -> dst*bs + i for
-// i < n, in K and in V.  Grid: (triple, 16-row chunk); 16-byte vectors.
+// i < n, in K and in V (and, for an INT8 cache, the rows' scales).  Grid:
+// (triple, 16-row chunk); 16-byte vectors.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -17,9 +18,14 @@ namespace pa {
 
 __device__ uint32_t g_copy_error; // 1 = a triple outside the pool was skipped
 
+// INT8 caches (k_scale != NULL): codes move like bf16 rows (row_vecs counts
+// their 16-byte vectors) and the first chunk's CTA also moves each KV head's
+// run of n fp16 scales, [src][g][0..n) -> [dst][g][0..n).
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                                                           const int3 *__restrict__ triples, int32_t row_vecs,
-                                                          int32_t block_size, int32_t num_blocks)
+                                                          int32_t block_size, int32_t num_blocks,
+                                                          uint16_t *__restrict__ k_scale,
+                                                          uint16_t *__restrict__ v_scale, int32_t num_kv_heads)
 {
     const int3 tr = triples[blockIdx.x];
     const int src = tr.x, dst = tr.y, n = tr.z;
@@ -27,6 +33,16 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_
         if (threadIdx.x == 0)
             atomicOr(&g_copy_error, 1u);
         return;
+    }
+    if (k_scale && blockIdx.y == 0) {
+        for (int i = threadIdx.x; i < num_kv_heads * n; i += blockDim.x) {
+            const int h = i / n, r = i % n;
+            const size_t from = ((size_t)src * num_kv_heads + h) * block_size + r;
+            const size_t to = ((size_t)dst * num_kv_heads + h) * block_size + r;
+            const uint16_t a = k_scale[from], b = v_scale[from];
+            k_scale[to] = a;
+            v_scale[to] = b;
+        }
     }
     const int r0 = blockIdx.y * 16;
     const int rows = min(16, n - r0);
@@ -44,13 +60,15 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_
 }
 
 int launch_copy_blocks(const pa_dims &dm, void *k_cache, void *v_cache, const int32_t *triples, int32_t n,
-                       void *stream)
+                       void *stream, void *k_scale, void *v_scale)
 {
-    const int32_t row_vecs = dm.num_kv_heads * dm.head_dim * 2 / 16;
+    const int elem = k_scale ? 1 : 2; // INT8 codes or bf16 values
+    const int32_t row_vecs = dm.num_kv_heads * dm.head_dim * elem / 16;
     dim3 grid((unsigned)n, (unsigned)((dm.block_size + 15) / 16));
     copy_blocks_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), reinterpret_cast<const int3 *>(triples),
-        row_vecs, dm.block_size, dm.num_blocks);
+        row_vecs, dm.block_size, dm.num_blocks, static_cast<uint16_t *>(k_scale), static_cast<uint16_t *>(v_scale),
+        dm.num_kv_heads);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "copy_blocks launch: %s", cudaGetErrorString(e));

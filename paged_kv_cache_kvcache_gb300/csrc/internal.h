@@ -102,8 +102,9 @@ int decode_static_scratch(void **ptr);
 // Concurrent decode CTAs one SM holds (occupancy of the decode kernel).
 int decode_ctas_per_sm(int head_dim, int group);
 
+// k_scale / v_scale NULL: bf16 cache; else INT8 codes plus fp16 scales [blocks][Hkv][bs].
 int launch_copy_blocks(const pa_dims &d, void *k_cache, void *v_cache, const int32_t *triples, int32_t n,
-                       void *stream);
+                       void *stream, void *k_scale = nullptr, void *v_scale = nullptr);
 
 // Read and clear the device error words (store: bit 0, prefill waits: bit 1,
 // block copy: bit 2, INT8 decode waits: bit 3).

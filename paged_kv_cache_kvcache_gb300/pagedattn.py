@@ -22,7 +22,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0
 
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
            "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
-           "pa_prefill_varlen_int8", "pa_pack_decode_fixed", "pa_decode_fused",
+           "pa_prefill_varlen_int8", "pa_pack_decode_fixed", "pa_decode_fused", "pa_copy_blocks_int8",
            "pa_last_error_string", "pa_read_device_error", "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
             L.pa_decode.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_decode_static.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P]
             L.pa_copy_blocks.argtypes = [P, P, P, P, I32, P]
+            L.pa_copy_blocks_int8.argtypes = [P, P, P, P, P, P, I32, P]
             L.pa_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, P, I32, P]
             L.pa_decode_int8.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_prefill_varlen_int8.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
@@ -349,6 +350,14 @@ def pa_decode_int8(dims: pa_dims, q, k_cache, v_cache, k_scale, v_scale, plan: D
                                 float(scale), _ptr(out), ctypes.byref(m), plan.dptr(m.off_items),
                                 plan.dptr(m.off_seq_items), _ptr(workspace), ws_bytes, _stream(stream)),
            "pa_decode_int8")
+
+
+def pa_copy_blocks_int8(dims: pa_dims, k_cache, v_cache, k_scale, v_scale, triples,
+                        num_triples: Optional[int] = None, stream=None):
+    """pa_copy_blocks on an INT8 cache: codes and each KV head's scale run."""
+    n = int(triples.shape[0]) if num_triples is None else int(num_triples)
+    _check(lib().pa_copy_blocks_int8(ctypes.byref(dims), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(triples), n, _stream(stream)), "pa_copy_blocks_int8")
 
 
 def pa_read_device_error(stream=None) -> int:

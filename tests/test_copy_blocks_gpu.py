@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from paged_kv_cache_kvcache_gb300 import pagedattn as pa
-from tests.harness import bits
+from tests.harness import bits, int8_equal
 
 pytestmark = pytest.mark.gpu
 
@@ -41,3 +41,30 @@ def test_copy_blocks_rejects_out_of_range_triples():
     pa.pa_copy_blocks(dims, kc, vc, bad)
     assert pa.pa_read_device_error() & 4
     assert np.array_equal(bits(kc), before)
+
+
+@pytest.mark.parametrize("bs,hkv,d", [(16, 4, 128), (256, 8, 128), (32, 1, 64)])
+def test_copy_blocks_int8_bit_exact(bs, hkv, d):
+    """INT8 cache fork: codes and every head's scale run byte-identical to the oracle's copy."""
+    g = torch.Generator(device="cuda").manual_seed(bs + hkv + 1)
+    nb = 40
+    dims = pa.make_dims(nb, bs, hkv * 2, hkv, d)
+    n = nb * bs
+    cache = pa.int8_cache(dims, "cuda")
+    k = torch.randn(n, hkv, d, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(n, hkv, d, device="cuda", generator=g).to(torch.bfloat16)
+    pa.pa_store_kvcache_int8(dims, k, v, *cache, torch.arange(n, dtype=torch.int32, device="cuda"), n)
+    torch.cuda.synchronize()
+    host = [c.cpu().numpy() for c in cache]
+    host = [h.view(np.uint16) if h.dtype == np.float16 else h.copy() for h in host]
+    rng = np.random.default_rng(bs + 1)
+    blocks = rng.permutation(nb)
+    srcs, dsts = blocks[:10], blocks[10:20]
+    ns = rng.integers(0, bs + 1, size=10)
+    ns[0], ns[1] = bs, 1
+    triples = np.stack([srcs, dsts, ns], 1).astype(np.int32)
+    oracle.copy_blocks_int8(*host, triples)
+    pa.pa_copy_blocks_int8(dims, *cache, torch.from_numpy(triples).cuda())
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    int8_equal(cache, host, what=f"int8 copy bs={bs}")
