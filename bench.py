@@ -63,7 +63,7 @@ def parse():
                     help="cache format: bf16, or int8 codes + fp16 scales (quantising store, fused-dequant "
                          "prefill and decode)")
     ap.add_argument("--decode-path", choices=["store+decode", "fused"], default="store+decode",
-                    help="fused: pa_decode_fused (bf16 cache only)")
+                    help="fused: store and decode in one launch (pa_decode_fused / pa_decode_int8_fused)")
     return ap.parse_args()
 
 
@@ -223,7 +223,11 @@ class Step:
             self.bd.v.copy_(host["dv"], non_blocking=True)
         plan_d = pa.pa_pack_decode(self.dims_d, self.bd.seq_lens, self.blocks_d, into=self.plans_d[k]).upload(stream=s)
         self.up_ev[k].record(s)
-        if self.int8:
+        if self.int8 and self.fused:  # quantising store + INT8 decode in one launch
+            rec("dk0")
+            pa.pa_decode_int8_fused(self.dims_d, self.bd.q, self.bd.k, self.bd.v, *self.c8_d, plan_d, self.bd.scale,
+                                    self.out_d, self.ws, stream=s)
+        elif self.int8:
             pa.pa_store_kvcache_int8(self.dims_d, self.bd.k, self.bd.v, *self.c8_d, plan_d.slot_mapping,
                                      self.bd.num_tokens, stream=s)
             rec("dk0")
@@ -364,7 +368,6 @@ def main():
     wp, wd, wl_desc = make_workload(args.workload, f"cuda:{local}", args.decode_seqs)
     stream = torch.cuda.Stream()
     clocks = Clocks(local, enabled=not args.no_clocks)
-    assert not (args.kv == "int8" and args.decode_path == "fused"), "the fused decode reads a bf16 cache"
     with torch.cuda.stream(stream):
         step = Step(wp, wd, stream, kv=args.kv, fused=args.decode_path == "fused")
         names = ["p0", "pk0", "pk1", "p1", "dk0", "dk1", "d1"]
@@ -443,7 +446,8 @@ def main():
     dk_name = {"bf16": "pa_decode (decode_split_kernel<128,1,false> + decode_combine_kernel<128>)",
                "int8": "pa_decode_int8 (decode_int8_kernel<128,1> + decode_combine_kernel<128>)"}[args.kv]
     if args.decode_path == "fused":
-        dk_name = "pa_decode_fused (decode_split_kernel<128,1,true> + decode_combine_kernel<128>)"
+        dk_name = ("pa_decode_int8_fused (decode_int8_kernel<128,1,true> + decode_combine_kernel<128>)" if int8 else
+                   "pa_decode_fused (decode_split_kernel<128,1,true> + decode_combine_kernel<128>)")
     roof_d = {"kernel": dk_name, "bound": "hbm",
               "achieved": round(dk_gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(dk_gbs / hbm_peak, 4),
               "peak_source": f"{peak_src} hbm_gbs",

@@ -322,6 +322,22 @@ int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cac
                            const pa_prefill_meta *meta, const int32_t *tiles, pa_stream_t stream);
 
 /*
+ * pa_decode_int8_fused — pa_store_kvcache_int8 followed by pa_decode_int8 in
+ * one launch: quantises k[b], v[b] (bf16 [num_seqs][num_kv_heads][head_dim],
+ * the new token of each sequence) into cache row slot_mapping[b] (codes and
+ * scales, bit-identical to pa_store_kvcache_int8) and decodes over the cache
+ * including it.  The work item that ends at the last key does the store and
+ * takes that key's dequantised values from its registers.  Same plan,
+ * workspace and error rules as pa_decode_int8; slot -1 writes nothing, other
+ * out-of-range slots are skipped and flagged (bit 0).
+ */
+int pa_decode_int8_fused(const pa_dims *dims, const void *q, const void *k, const void *v, void *k_cache,
+                         void *v_cache, void *k_scale, void *v_scale, const int32_t *slot_mapping,
+                         const int32_t *context_lens, const int32_t *block_tables, float scale, void *out,
+                         const pa_decode_meta *meta, const int32_t *items, const int32_t *seq_items,
+                         void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_copy_blocks_int8 — pa_copy_blocks on an INT8 cache: for each (src, dst, n)
  * triple the codes of rows src*bs + i go to dst*bs + i and, for every KV head
  * g, the scales [src][g][i] to [dst][g][i], i < n, bit for bit (the

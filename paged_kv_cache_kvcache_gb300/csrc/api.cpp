@@ -270,6 +270,31 @@ extern "C" int pa_decode_fused(const pa_dims *dims, const void *q, const void *k
     return launch_decode(a, stream);
 }
 
+extern "C" int pa_decode_int8_fused(const pa_dims *dims, const void *q, const void *k, const void *v,
+                                    void *k_cache, void *v_cache, void *k_scale, void *v_scale,
+                                    const int32_t *slot_mapping, const int32_t *context_lens,
+                                    const int32_t *block_tables, float scale, void *out, const pa_decode_meta *meta,
+                                    const int32_t *items, const int32_t *seq_items, void *workspace,
+                                    size_t workspace_bytes, pa_stream_t stream)
+{
+    DecodeArgs a;
+    bool nothing = false;
+    int rc = prepare_decode("pa_decode_int8_fused", dims, q, k_cache, v_cache, context_lens, block_tables, scale,
+                            out, meta, items, seq_items, workspace, workspace_bytes, &a, &nothing);
+    if (rc != PA_OK || nothing)
+        return rc;
+    if (!k || !v || !slot_mapping || !k_scale || !v_scale)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_int8_fused: NULL pointer");
+    if (misaligned(k) || misaligned(v) || misaligned(k_scale) || misaligned(v_scale))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_int8_fused: tensors must be 16-byte aligned");
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.k_new = k;
+    a.v_new = v;
+    a.slot_mapping = slot_mapping;
+    return launch_decode_int8(a, stream);
+}
+
 extern "C" int pa_store_kvcache_int8(const pa_dims *dims, const void *k, const void *v, void *k_cache,
                                      void *v_cache, void *k_scale, void *v_scale, const int32_t *slot_mapping,
                                      int32_t num_tokens, pa_stream_t stream)
@@ -385,5 +410,7 @@ extern "C" int pa_read_device_error(uint32_t *code, pa_stream_t stream)
         rc = read_decode_error(code);
     if (rc == PA_OK)
         rc = read_fused_error(code);
+    if (rc == PA_OK)
+        rc = read_fused8_error(code);
     return rc;
 }

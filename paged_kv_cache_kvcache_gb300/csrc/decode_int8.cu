@@ -109,9 +109,50 @@ struct DecParams8 {
     int32_t group;
     int32_t block_size;
     int32_t max_blocks;
+    // fused store (FUSED kernels only): the new token's bf16 K/V rows, where they go, the context lengths
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    int8_t *k_codes_out;
+    int8_t *v_codes_out;
+    __half *k_scale_out;
+    __half *v_scale_out;
+    const int32_t *slot_mapping;
+    const int32_t *context_lens;
+    int64_t num_slots;
 };
 
-template <int D, int NT>
+__device__ uint32_t g_fused8_error; // bit 0: a fused-store slot outside [-1, num_slots) was skipped
+
+// The INT8 quantiser of pa_store_kvcache_int8 on one (token, KV head) row held
+// by a warp (D/32 values per lane): returns the codes packed in one word and
+// the fp32 scale; arithmetic identical to the store kernel, bit for bit.
+template <int D>
+__device__ __forceinline__ uint32_t quantise_row(const float (&x)[D / 32], float &scale)
+{
+    constexpr int E = D / 32;
+    float a = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        a = fmaxf(a, fabsf(x[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    scale = fmaxf(__fdiv_rn(a, 127.0f), 1e-8f);
+    uint32_t codes = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float q = __fdiv_rn(x[e], scale);
+        const int i = __float2int_rz(q >= 0.f ? __fadd_rn(q, 0.5f) : __fsub_rn(q, 0.5f));
+        codes |= (uint32_t)(i & 0xff) << (8 * e);
+    }
+    return codes;
+}
+
+// FUSED: the CTA whose work item ends at the sequence's last key (the token
+// being decoded) quantises that token's K/V rows of its head, writes codes and
+// scales into the cache slot and takes the key from its own registers (the
+// dequantised values the cache now holds) instead of from the cache.
+template <int D, int NT, bool FUSED>
 __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
     decode_int8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const DecParams8 p)
@@ -125,7 +166,10 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
     const int lane = threadIdx.x & 31;
     const int r = lane >> 2, c = lane & 3;
     const int4 item = p.items[blockIdx.x / p.num_kv_heads];
-    const int b = item.x, k0 = item.y, k1 = item.z, pslot = item.w;
+    const int b = item.x, k0 = item.y, pslot = item.w;
+    // FUSED: does this item hold the new token?  Then the cache supplies keys k0 .. ctx-2.
+    const bool has_new = FUSED && item.z > 0 && item.z == __ldg(p.context_lens + b);
+    const int k1 = has_new ? item.z - 1 : item.z;
     const int g = blockIdx.x % p.num_kv_heads;
     const int G = p.group;
     const int Hq = p.num_heads;
@@ -346,6 +390,62 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
     float *mrg_m = reinterpret_cast<float *>(smem);
     float *mrg_l = mrg_m + kWarps * H8;
     float *mrg_o = mrg_l + kWarps * H8; // [warp][head][kRow], d in natural order
+    float *s_new = mrg_o + (size_t)kWarps * H8 * kRow; // FUSED: the new key's score per head (log2 units)
+    float *v_new = s_new + H8;                         // FUSED: the new value, dequantised
+    if constexpr (FUSED) {
+        if (has_new && warp < 2) {
+            // warp 0 quantises K, warp 1 V: codes and fp16 scale into the slot, dequantised values kept
+            constexpr int E = D / 32;
+            const size_t row = ((size_t)b * p.num_kv_heads + g) * D + lane * E;
+            const __nv_bfloat16 *src = (warp == 0 ? p.k_new : p.v_new) + row;
+            float x[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                x[e] = __bfloat162float(src[e]);
+            float sc;
+            const uint32_t codes = quantise_row<D>(x, sc);
+            const __half sc16 = __float2half_rn(sc);
+            const float deq = __half2float(sc16);
+            float xd[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                xd[e] = (float)(int8_t)(codes >> (8 * e)) * deq;
+            const int32_t slot = __ldg(p.slot_mapping + b);
+            if (slot >= 0 && slot < p.num_slots) {
+                const size_t dst = ((size_t)slot * p.num_kv_heads + g) * D + lane * E;
+                int8_t *cd = (warp == 0 ? p.k_codes_out : p.v_codes_out) + dst;
+                if constexpr (E == 4)
+                    *reinterpret_cast<uint32_t *>(cd) = codes;
+                else
+                    *reinterpret_cast<uint16_t *>(cd) = (uint16_t)codes;
+                if (lane == 0) {
+                    const int bs = p.block_size;
+                    (warp == 0 ? p.k_scale_out : p.v_scale_out)[((size_t)(slot / bs) * p.num_kv_heads + g) * bs +
+                                                                slot % bs] = sc16;
+                }
+            } else if (slot != -1 && lane == 0) {
+                atomicOr(&g_fused8_error, 1u);
+            }
+            if (warp == 0) { // the new key's score for every head of the group
+                for (int hl = 0; hl < G; ++hl) {
+                    const __nv_bfloat16 *qr = p.q + ((size_t)b * Hq + (size_t)g * G + hl) * D + lane * E;
+                    float acc_s = 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e)
+                        acc_s += __bfloat162float(qr[e]) * xd[e];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        acc_s += __shfl_xor_sync(0xffffffffu, acc_s, o);
+                    if (lane == 0)
+                        s_new[hl] = acc_s * p.scale_log2;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    v_new[lane * E + e] = xd[e];
+            }
+        }
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int h0 = nt * 8 + 2 * c;
@@ -373,12 +473,19 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
         for (int w = 0; w < kWarps; ++w)
             M = fmaxf(M, mrg_m[w * H8 + hl]);
         float Lsum = 0.f, O = 0.f;
+        if (FUSED && has_new)
+            M = fmaxf(M, s_new[hl]);
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
                 const float f = ptx::ex2(mrg_m[w * H8 + hl] - M);
                 Lsum += f * mrg_l[w * H8 + hl];
                 O += f * mrg_o[((size_t)w * H8 + hl) * kRow + d];
+            }
+            if (FUSED && has_new) { // the new token: weight 2^(s - M), its dequantised value
+                const float f = ptx::ex2(s_new[hl] - M);
+                Lsum += f;
+                O += f * v_new[d];
             }
         }
         const float o = Lsum > 0.f ? O / Lsum : 0.f;
@@ -393,12 +500,12 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
     }
 }
 
-template <int D, int NT>
+template <int D, int NT, bool FUSED>
 int launch_int8(const DecodeArgs &a, const DecParams8 &p, cudaStream_t stream)
 {
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_int8_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(decode_int8_kernel<D, NT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              DecLayout8<D>::kSmemBytes);
         if (e != cudaSuccess)
             return fail(PA_ERR_CUDA, "decode_int8 smem attribute: %s", cudaGetErrorString(e));
@@ -419,7 +526,7 @@ int launch_int8(const DecodeArgs &a, const DecParams8 &p, cudaStream_t stream)
     // flat grid, heads of one work item adjacent: they read neighbouring
     // segments of the same token rows at about the same time (DRAM locality)
     dim3 grid((unsigned)(a.num_items * a.dims.num_kv_heads));
-    decode_int8_kernel<D, NT><<<grid, kWarps * 32, DecLayout8<D>::kSmemBytes, stream>>>(tk, tv, p);
+    decode_int8_kernel<D, NT, FUSED><<<grid, kWarps * 32, DecLayout8<D>::kSmemBytes, stream>>>(tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "decode_int8 launch: %s", cudaGetErrorString(e));
@@ -447,9 +554,35 @@ int launch_decode_int8(const DecodeArgs &a, void *stream)
     p.max_blocks = a.max_blocks_per_seq;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool two = p.group > 8;
+    if (a.k_new) { // fused quantising store + decode
+        p.k_new = static_cast<const __nv_bfloat16 *>(a.k_new);
+        p.v_new = static_cast<const __nv_bfloat16 *>(a.v_new);
+        p.k_codes_out = static_cast<int8_t *>(const_cast<void *>(a.k_cache));
+        p.v_codes_out = static_cast<int8_t *>(const_cast<void *>(a.v_cache));
+        p.k_scale_out = static_cast<__half *>(const_cast<void *>(a.k_scale));
+        p.v_scale_out = static_cast<__half *>(const_cast<void *>(a.v_scale));
+        p.slot_mapping = a.slot_mapping;
+        p.context_lens = a.context_lens;
+        p.num_slots = (int64_t)a.dims.num_blocks * a.dims.block_size;
+        if (a.dims.head_dim == 128)
+            return two ? launch_int8<128, 2, true>(a, p, s) : launch_int8<128, 1, true>(a, p, s);
+        return two ? launch_int8<64, 2, true>(a, p, s) : launch_int8<64, 1, true>(a, p, s);
+    }
     if (a.dims.head_dim == 128)
-        return two ? launch_int8<128, 2>(a, p, s) : launch_int8<128, 1>(a, p, s);
-    return two ? launch_int8<64, 2>(a, p, s) : launch_int8<64, 1>(a, p, s);
+        return two ? launch_int8<128, 2, false>(a, p, s) : launch_int8<128, 1, false>(a, p, s);
+    return two ? launch_int8<64, 2, false>(a, p, s) : launch_int8<64, 1, false>(a, p, s);
+}
+
+int read_fused8_error(uint32_t *code)
+{
+    uint32_t v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_fused8_error, sizeof v);
+    if (e == cudaSuccess)
+        e = cudaMemcpyToSymbol(g_fused8_error, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "reading fused-store error word: %s", cudaGetErrorString(e));
+    *code |= v; // same meaning as the store kernels' bit 0
+    return PA_OK;
 }
 
 int read_decode_error(uint32_t *code)

@@ -113,5 +113,6 @@ int read_prefill_error(uint32_t *code);
 int read_copy_error(uint32_t *code);
 int read_decode_error(uint32_t *code);
 int read_fused_error(uint32_t *code);
+int read_fused8_error(uint32_t *code);
 
 } // namespace pa

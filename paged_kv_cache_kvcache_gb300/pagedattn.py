@@ -23,6 +23,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
            "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
            "pa_prefill_varlen_int8", "pa_pack_decode_fixed", "pa_decode_fused", "pa_copy_blocks_int8",
+           "pa_decode_int8_fused",
            "pa_last_error_string", "pa_read_device_error", "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.pa_decode_static.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P]
             L.pa_copy_blocks.argtypes = [P, P, P, P, I32, P]
             L.pa_copy_blocks_int8.argtypes = [P, P, P, P, P, P, I32, P]
+            L.pa_decode_int8_fused.argtypes = [P, P, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ,
+                                               P]
             L.pa_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, P, I32, P]
             L.pa_decode_int8.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_prefill_varlen_int8.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
@@ -338,6 +341,18 @@ def pa_prefill_varlen_int8(dims: pa_dims, q, k_cache, v_cache, k_scale, v_scale,
                                         _ptr(v_scale), plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
                                         plan.dptr(m.off_block_tables), float(scale), _ptr(out), ctypes.byref(m),
                                         plan.dptr(m.off_tiles), _stream(stream)), "pa_prefill_varlen_int8")
+
+
+def pa_decode_int8_fused(dims: pa_dims, q, k, v, k_cache, v_cache, k_scale, v_scale, plan: DecodePlan,
+                         scale: float, out, workspace=None, stream=None):
+    """Quantising store of each sequence's new K/V row + INT8 decode, in one launch."""
+    m = plan.meta
+    ws_bytes = int(workspace.numel()) if isinstance(workspace, torch.Tensor) else 0
+    _check(lib().pa_decode_int8_fused(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(k_scale), _ptr(v_scale), plan.dptr(m.off_slot_mapping),
+                                      plan.dptr(m.off_context_lens), plan.dptr(m.off_block_tables), float(scale),
+                                      _ptr(out), ctypes.byref(m), plan.dptr(m.off_items), plan.dptr(m.off_seq_items),
+                                      _ptr(workspace), ws_bytes, _stream(stream)), "pa_decode_int8_fused")
 
 
 def pa_decode_int8(dims: pa_dims, q, k_cache, v_cache, k_scale, v_scale, plan: DecodePlan, scale: float, out,

@@ -79,9 +79,10 @@ def _bucket_step(rng, B, real, max_ctx, nb, bs, hq, hkv, d, gen):
     return ctx, blocks, mk(B, hq, d), mk(B, hkv, d), mk(B, hkv, d)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("d,hq,hkv,split", [(128, 16, 2, 256), (64, 12, 1, 64), (128, 28, 4, 0)])
-def test_decode_graph_replay_fixed_bucket(fused, d, hq, hkv, split):
+def test_decode_graph_replay_fixed_bucket(kv, fused, d, hq, hkv, split):
     """Capture once, replay on three steps with new contexts, blocks and padding."""
     B, max_ctx, bs = 8, 1024, 16
     nb = B * (max_ctx // bs) + 4
@@ -98,12 +99,29 @@ def test_decode_graph_replay_fixed_bucket(fused, d, hq, hkv, split):
     out = torch.zeros(B, hq, d, dtype=torch.bfloat16, device="cuda")
     shape = tuple(getattr(plan.meta, f) for f in ("num_items", "total_bytes", "workspace_bytes", "off_items"))
 
+    if kv == "int8":  # the pool quantised slot by slot; the caches below are what the graph reads and writes
+        c8 = pa.int8_cache(dims, "cuda")
+        n_slots = nb * bs
+        pa.pa_store_kvcache_int8(dims, kc.view(n_slots, hkv, d), vc.view(n_slots, hkv, d), *c8,
+                                 torch.arange(n_slots, dtype=torch.int32, device="cuda"), n_slots)
+
     def step():
-        if fused:
+        if kv == "int8" and fused:
+            pa.pa_decode_int8_fused(dims, q_in, k_in, v_in, *c8, plan, scale, out, ws)
+        elif kv == "int8":
+            pa.pa_store_kvcache_int8(dims, k_in, v_in, *c8, plan.slot_mapping, B)
+            pa.pa_decode_int8(dims, q_in, *c8, plan, scale, out, ws)
+        elif fused:
             pa.pa_decode_fused(dims, q_in, k_in, v_in, kc, vc, plan, scale, out, ws)
         else:
             pa.pa_store_kvcache(dims, k_in, v_in, kc, vc, plan.slot_mapping, B)
             pa.pa_decode(dims, q_in, kc, vc, plan, scale, out, ws)
+
+    def host_cache():
+        if kv == "int8":
+            h = [c.cpu().numpy() for c in c8]
+            return [x.view(np.uint16) if x.dtype == np.float16 else x.copy() for x in h]
+        return [bits(kc), bits(vc)]
 
     step()  # first call outside capture: one-time set-up (function attributes)
     torch.cuda.synchronize()
@@ -119,14 +137,18 @@ def test_decode_graph_replay_fixed_bucket(fused, d, hq, hkv, split):
             plan.upload("cuda")  # same device buffer the graph reads
             q_in.copy_(q), k_in.copy_(k), v_in.copy_(v)
         torch.cuda.synchronize()
-        ok_, ov_ = bits(kc), bits(vc)
+        before = host_cache()
         out.fill_(1.0)
         graph.replay()
         torch.cuda.synchronize()
         assert pa.pa_read_device_error() == 0
         live = workloads.Batch("decode", ctx[:real], np.ones(real, np.int32), blocks[:real], q[:real].cpu(),
                                k[:real].cpu(), v[:real].cpu(), hq, scale)
-        ref, _ = oracle.run_batch(ok_, ov_, live, bs)
-        assert_close(out[:real], ref, what=f"graph step {it} fused={fused} d={d} real={real}")
+        if kv == "int8":
+            ref, _ = oracle.run_batch_int8(*before, live, bs)
+        else:
+            ref, _ = oracle.run_batch(*before, live, bs)
+        assert_close(out[:real], ref, what=f"graph step {it} kv={kv} fused={fused} d={d} real={real}")
         assert not out[real:].float().abs().any(), "padding rows must be zero"
-        assert np.array_equal(bits(kc), ok_) and np.array_equal(bits(vc), ov_), "cache after the step"
+        for got, want in zip(host_cache(), before):
+            assert np.array_equal(got, want), "cache after the step"

@@ -133,3 +133,31 @@ def test_decode_int8_deterministic():
     b, _ = run_gpu_decode_int8(w, batch, gpu, split_tokens=256)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("case", [(421, 7, 8, 2, 128, 16, 900), (422, 5, 12, 1, 64, 32, 700),
+                                  (423, 6, 16, 1, 128, 256, 1500)], ids=["421", "422", "423"])
+@pytest.mark.parametrize("split", [0, 64])
+def test_decode_int8_fused(case, split):
+    """Quantising store + INT8 decode in one launch: cache bit-exact, output as the oracle's."""
+    seed, B, hq, hkv, d, bs, max_len = case
+    w = workloads.random_case(seed, num_seqs=B, hq=hq, hkv=hkv, d=d, bs=bs, max_len=max_len, kind="decode",
+                              device="cuda")
+    batch = w.batches[0]
+    gpu, host = int8_pools(w, batch.num_heads)
+    dims = pa.make_dims(w.pool.num_blocks, w.pool.block_size, batch.num_heads, w.pool.num_kv_heads,
+                        w.pool.head_dim)
+    plan = pa.pa_pack_decode(dims, batch.seq_lens, batch.block_lists, split).upload("cuda")
+    ws = pa.decode_workspace(plan)
+    out = torch.empty_like(batch.q)
+    pa.pa_decode_int8_fused(dims, batch.q, batch.k, batch.v, *gpu, plan, batch.scale, out, ws)
+    ref, _ = oracle.run_batch_int8(*host, batch, w.pool.block_size)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    int8_equal(gpu, host, what="cache after the fused store")
+    assert_close(out, ref, what=f"int8 fused case {seed} split {split}")
+    # and the unfused pair on the same (now stored) cache agrees up to rounding order
+    out2 = torch.empty_like(batch.q)
+    pa.pa_decode_int8(dims, batch.q, *gpu, plan, batch.scale, out2, ws)
+    torch.cuda.synchronize()
+    assert (out.float() - out2.float()).abs().max().item() < 1e-2
