@@ -381,14 +381,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const float *__rest
 template <int D, int NT, bool FUSED>
 int launch_split(const DecodeArgs &a, const DecParams &p, cudaStream_t stream)
 {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, NT, FUSED>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, DecLayout<D>::kSmemBytes);
-        if (e != cudaSuccess)
-            return fail(PA_ERR_CUDA, "decode smem attribute: %s", cudaGetErrorString(e));
-        configured = true;
-    }
+    if (int rc = ensure_smem<decode_split_kernel<D, NT, FUSED>>(DecLayout<D>::kSmemBytes, "decode"))
+        return rc;
     // flat grid, heads of one work item adjacent: they read neighbouring
     // segments of the same token rows at about the same time (DRAM locality)
     dim3 grid((unsigned)(a.num_items * a.dims.num_kv_heads));

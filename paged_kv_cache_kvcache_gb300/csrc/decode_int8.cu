@@ -503,14 +503,8 @@ __global__ void __launch_bounds__(kWarps * 32, NT == 1 ? 4 : 3)
 template <int D, int NT, bool FUSED>
 int launch_int8(const DecodeArgs &a, const DecParams8 &p, cudaStream_t stream)
 {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_int8_kernel<D, NT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             DecLayout8<D>::kSmemBytes);
-        if (e != cudaSuccess)
-            return fail(PA_ERR_CUDA, "decode_int8 smem attribute: %s", cudaGetErrorString(e));
-        configured = true;
-    }
+    if (int rc = ensure_smem<decode_int8_kernel<D, NT, FUSED>>(DecLayout8<D>::kSmemBytes, "decode_int8"))
+        return rc;
     // codes as uint8 [num_slots][Hkv][D]: box = one head's D bytes x 16 token rows
     const pa_dims &d = a.dims;
     const uint64_t rows = (uint64_t)d.num_blocks * d.block_size;

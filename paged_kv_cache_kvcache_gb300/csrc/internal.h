@@ -1,10 +1,12 @@
 // Internal declarations shared by the host-side translation units of libpagedattn.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 #include "pagedattn.h"
 
@@ -30,6 +32,26 @@ int fail(int code, const char *fmt, ...);
 int check_dims(const pa_dims *dims);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Raise a kernel's dynamic shared-memory limit once per device (the attribute is
+// per device; a process may drive several GPUs).  One flag word per kernel.
+template <auto Kernel>
+int ensure_smem(int bytes, const char *what)
+{
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t)1 << dev : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit))
+        return PA_OK;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "%s shared-memory attribute: %s", what, cudaGetErrorString(e));
+    done.fetch_or(bit, std::memory_order_release);
+    return PA_OK;
+}
 
 // 3-D TMA descriptor (dims innermost first, strides of dims 1 and 2 in bytes,
 // box in elements); PA_ERR_CUDA if the driver rejects it.

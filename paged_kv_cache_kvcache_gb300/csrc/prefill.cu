@@ -271,6 +271,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkt = max(nkt0, nkt1);
     const bool tail = nkt * 128 > lk; // last key tile runs past the sequence end
 
+    // Block ids of key tile 0 (one TMA box per lane), read before the set-up below so
+    // that their latency overlaps it: the producers' first loads depend on them.
+    const int box_rows0 = p.block_size < 128 ? p.block_size : 128;
+    int row0 = p.num_slots;
+    if ((warp == kKProducerWarp || warp == kVProducerWarp || (I8 && warp == kLoaderWarp)) &&
+        lane < 128 / box_rows0 && lane * box_rows0 < lk) {
+        const int key = lane * box_rows0;
+        row0 = __ldg(p.block_tables + (size_t)b * p.max_blocks + key / p.block_size) * p.block_size +
+               (key & (p.block_size - 1));
+    }
+
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bars.q_full(t), 1);
@@ -350,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int phys = __ldg(bt + key / bs);
             return phys * bs + (key & (bs - 1));
         };
-        int next = sub_row(0);
+        int next = row0; // sub_row(0), read at kernel entry
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
             const int cur = next;
@@ -449,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         };
-        int next = sub_row(0);
+        int next = row0; // sub_row(0), read at kernel entry
         for (int j = 0; j < nkt; ++j) {
             const int cur = next;
             if (j + 1 < nkt)
@@ -824,14 +835,8 @@ template <int D, bool I8>
 int launch(const PrefillArgs &a, cudaStream_t stream)
 {
     using L = PfLayout<D, I8>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(prefill_kernel<D, I8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-        if (e != cudaSuccess)
-            return fail(PA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
-        configured = true;
-    }
+    if (int rc = ensure_smem<prefill_kernel<D, I8>>(L::kSmemBytes, "prefill"))
+        return rc;
     const pa_dims &d = a.dims;
     const int G = d.num_heads / d.num_kv_heads;
     const uint64_t rows = (uint64_t)d.num_blocks * d.block_size;
