@@ -383,12 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = ring + st * L::kTileBytes;
             if (lane == 0)
                 ptx::mbar_arrive_expect_tx(full, (uint32_t)L::kTileBytes);
-            for (int i = 0; i < nsub; ++i) {
-                const int row = __shfl_sync(0xffffffffu, cur, i);
-                if (lane == 0)
-                    for (int pp = 0; pp < L::kPanels; ++pp)
-                        ptx::tma_load_3d(dst + pp * L::kPanelBytes + i * box_rows * 128, tm, full, pp * 64, g, row);
-            }
+            // lane i issues the boxes of sub-box i (its own row coordinate)
+            if (lane < nsub)
+                for (int pp = 0; pp < L::kPanels; ++pp)
+                    ptx::tma_load_3d(dst + pp * L::kPanelBytes + lane * box_rows * 128, tm, full, pp * 64, g, cur);
             __syncwarp();
         }
         if (!is_k && ok && tail) {
@@ -453,11 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = sbase + (is_k ? L::k_codes(st) : L::v_codes(st));
             if (lane == 0)
                 ptx::mbar_arrive_expect_tx(bar, (uint32_t)L::kCodeBytes);
-            for (int i = 0; i < nsub; ++i) {
-                const int row = __shfl_sync(0xffffffffu, cur, i);
-                if (lane == 0)
-                    ptx::tma_load_3d(dst + i * box_rows * D, is_k ? &tm_k : &tm_v, bar, 0, g, row);
-            }
+            if (lane < nsub)
+                ptx::tma_load_3d(dst + lane * box_rows * D, is_k ? &tm_k : &tm_v, bar, 0, g, cur);
             __syncwarp();
         };
         int next = row0; // sub_row(0), read at kernel entry
