@@ -67,7 +67,8 @@ namespace {
 
 // warps 0-7: softmax (two warpgroups), 8: K/Q TMA producer, 9: MMA issuer (and
 // TMEM owner), 10: V TMA producer, 11: idle (registers are granted per 4 warps,
-// so the CTA is sized at 12 warps, <= 168 registers each).  One thread issues
+// so the CTA is sized at 12 warps, 168 registers each at launch; the bf16
+// variant moves them to the softmax warpgroups: 224 there, 56 in warps 8-11).  One thread issues
 // the MMAs of both query tiles: its in-order stream keeps the two tiles half a
 // key tile apart, so one tile's softmax always runs under the other's MMAs.
 constexpr int kThreads = 384;
@@ -317,335 +318,344 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kTmemSlotOffset);
 
-    if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
-        // ---------------------------------------------------------------- TMA producers (K + Q, V)
-        const bool is_k = warp == kKProducerWarp;
-        const int bs = p.block_size;
-        const int box_rows = bs < 128 ? bs : 128;
-        const int nsub = 128 / box_rows;
-        const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
-        const int nstages = is_k ? L::kKStages : L::kVStages;
-        const uint32_t ring = sbase + (is_k ? L::kK : L::kV);
-        const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
-        if (is_k && G * P < 128) {
-            // rows G*P..127 of each query tile receive no TMA data: zero them once so
-            // their (discarded) scores stay finite and cost the same as real rows
-            const int first = G * P, chunks = (128 - first) * 8;
-            for (int t = 0; t < 2; ++t)
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    for (int c = lane; c < chunks; c += 32)
-                        *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
-                                                   (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-        }
-        if (lane == 0) {
-            ptx::prefetch_tmap(tm);
-            if (is_k) {
+    if (warp >= 8) {
+        // warps 8-11 (copies, conversion, MMA issue) need few registers: the
+        // bf16 variant hands 112 of each thread's 168 to the softmax warpgroups
+        // (128 x (56 + 224 + 224) = 384 x 168, the registers of the launch)
+        if constexpr (!I8)
+            ptx::reg_dealloc<56>();
+        if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
+            // ---------------------------------------------------------------- TMA producers (K + Q, V)
+            const bool is_k = warp == kKProducerWarp;
+            const int bs = p.block_size;
+            const int box_rows = bs < 128 ? bs : 128;
+            const int nsub = 128 / box_rows;
+            const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
+            const int nstages = is_k ? L::kKStages : L::kVStages;
+            const uint32_t ring = sbase + (is_k ? L::kK : L::kV);
+            const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
+            if (is_k && G * P < 128) {
+                // rows G*P..127 of each query tile receive no TMA data: zero them once so
+                // their (discarded) scores stay finite and cost the same as real rows
+                const int first = G * P, chunks = (128 - first) * 8;
+                for (int t = 0; t < 2; ++t)
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        for (int c = lane; c < chunks; c += 32)
+                            *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
+                                                       (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                ptx::prefetch_tmap(tm);
+                if (is_k) {
+                    ptx::prefetch_tmap(&tm_q);
+                    for (int t = 0; t < 2; ++t) {
+                        if ((t == 0 ? npos0 : npos1) <= 0)
+                            continue;
+                        ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
+                        for (int pp = 0; pp < L::kPanels; ++pp)
+                            ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, &tm_q,
+                                             bars.q_full(t), pp * 64, g * G, cq0 + q0 + t * P);
+                    }
+                }
+            }
+            // row coordinate of sub-box `lane` of key tile j (all lanes compute their own)
+            auto sub_row = [&](int j) -> int {
+                const int key = j * 128 + lane * box_rows;
+                if (lane >= nsub || key >= lk)
+                    return p.num_slots; // fully out of range: TMA fills zeros
+                const int phys = __ldg(bt + key / bs);
+                return phys * bs + (key & (bs - 1));
+            };
+            int next = row0; // sub_row(0), read at kernel entry
+            bool ok = true;
+            for (int j = 0; j < nkt; ++j) {
+                const int cur = next;
+                if (j + 1 < nkt)
+                    next = sub_row(j + 1);
+                const int st = j % nstages;
+                const uint32_t full = is_k ? bars.k_full(st) : bars.v_full(st);
+                // slot reuse: tile j replaces tile j - S, free after release event
+                // j - S (K) or j - S + 1 (V)
+                bool free_ok = true;
+                if (j >= nstages) {
+                    const int e = is_k ? j - nstages : j - nstages + 1;
+                    free_ok = wait(bars.released(e), (e / kIterRing) & 1);
+                }
+                if (!__all_sync(0xffffffffu, free_ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = ring + st * L::kTileBytes;
+                if (lane == 0)
+                    ptx::mbar_arrive_expect_tx(full, (uint32_t)L::kTileBytes);
+                // lane i issues the boxes of sub-box i (its own row coordinate)
+                if (lane < nsub)
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        ptx::tma_load_3d(dst + pp * L::kPanelBytes + lane * box_rows * 128, tm, full, pp * 64, g, cur);
+                __syncwarp();
+            }
+            if (!is_k && ok && tail) {
+                // V rows of keys past the sequence end may hold anything (even NaN bit
+                // patterns); zero them so that P = 0 cannot turn them into NaN in O.
+                const int j = nkt - 1, st = j % L::kVStages;
+                if (__all_sync(0xffffffffu, wait(bars.v_full(st), (j / L::kVStages) & 1))) {
+                    const int first = lk - j * 128;
+                    uint8_t *vt = sgen + L::kV + st * L::kTileBytes;
+                    const int chunks = (128 - first) * 8;
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        for (int c = lane; c < chunks; c += 32)
+                            *reinterpret_cast<uint4 *>(vt + pp * L::kPanelBytes + (first + (c >> 3)) * 128 +
+                                                       (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(bars.v_tail());
+                }
+            }
+        } else if (I8 && warp == kLoaderWarp) {
+            // ---------------------------------------------------------------- INT8: TMA loader (Q, K codes, V codes)
+            const int bs = p.block_size;
+            const int box_rows = bs < 128 ? bs : 128;
+            const int nsub = 128 / box_rows;
+            const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
+            if (G * P < 128) {
+                // rows G*P..127 of each query tile receive no TMA data: zero them once
+                const int first = G * P, chunks = (128 - first) * 8;
+                for (int t = 0; t < 2; ++t)
+                    for (int pp = 0; pp < L::kPanels; ++pp)
+                        for (int c = lane; c < chunks; c += 32)
+                            *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
+                                                       (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                ptx::prefetch_tmap(&tm_k);
+                ptx::prefetch_tmap(&tm_v);
                 ptx::prefetch_tmap(&tm_q);
                 for (int t = 0; t < 2; ++t) {
                     if ((t == 0 ? npos0 : npos1) <= 0)
                         continue;
                     ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
                     for (int pp = 0; pp < L::kPanels; ++pp)
-                        ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, &tm_q,
-                                         bars.q_full(t), pp * 64, g * G, cq0 + q0 + t * P);
+                        ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, &tm_q, bars.q_full(t),
+                                         pp * 64, g * G, cq0 + q0 + t * P);
                 }
             }
-        }
-        // row coordinate of sub-box `lane` of key tile j (all lanes compute their own)
-        auto sub_row = [&](int j) -> int {
-            const int key = j * 128 + lane * box_rows;
-            if (lane >= nsub || key >= lk)
-                return p.num_slots; // fully out of range: TMA fills zeros
-            const int phys = __ldg(bt + key / bs);
-            return phys * bs + (key & (bs - 1));
-        };
-        int next = row0; // sub_row(0), read at kernel entry
-        bool ok = true;
-        for (int j = 0; j < nkt; ++j) {
-            const int cur = next;
-            if (j + 1 < nkt)
-                next = sub_row(j + 1);
-            const int st = j % nstages;
-            const uint32_t full = is_k ? bars.k_full(st) : bars.v_full(st);
-            // slot reuse: tile j replaces tile j - S, free after release event
-            // j - S (K) or j - S + 1 (V)
-            bool free_ok = true;
-            if (j >= nstages) {
-                const int e = is_k ? j - nstages : j - nstages + 1;
-                free_ok = wait(bars.released(e), (e / kIterRing) & 1);
-            }
-            if (!__all_sync(0xffffffffu, free_ok)) {
-                ok = false;
-                break;
-            }
-            const uint32_t dst = ring + st * L::kTileBytes;
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(full, (uint32_t)L::kTileBytes);
-            // lane i issues the boxes of sub-box i (its own row coordinate)
-            if (lane < nsub)
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    ptx::tma_load_3d(dst + pp * L::kPanelBytes + lane * box_rows * 128, tm, full, pp * 64, g, cur);
-            __syncwarp();
-        }
-        if (!is_k && ok && tail) {
-            // V rows of keys past the sequence end may hold anything (even NaN bit
-            // patterns); zero them so that P = 0 cannot turn them into NaN in O.
-            const int j = nkt - 1, st = j % L::kVStages;
-            if (__all_sync(0xffffffffu, wait(bars.v_full(st), (j / L::kVStages) & 1))) {
-                const int first = lk - j * 128;
-                uint8_t *vt = sgen + L::kV + st * L::kTileBytes;
-                const int chunks = (128 - first) * 8;
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    for (int c = lane; c < chunks; c += 32)
-                        *reinterpret_cast<uint4 *>(vt + pp * L::kPanelBytes + (first + (c >> 3)) * 128 +
-                                                   (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(bars.v_tail());
-            }
-        }
-    } else if (I8 && warp == kLoaderWarp) {
-        // ---------------------------------------------------------------- INT8: TMA loader (Q, K codes, V codes)
-        const int bs = p.block_size;
-        const int box_rows = bs < 128 ? bs : 128;
-        const int nsub = 128 / box_rows;
-        const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
-        if (G * P < 128) {
-            // rows G*P..127 of each query tile receive no TMA data: zero them once
-            const int first = G * P, chunks = (128 - first) * 8;
-            for (int t = 0; t < 2; ++t)
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    for (int c = lane; c < chunks; c += 32)
-                        *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
-                                                   (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-        }
-        if (lane == 0) {
-            ptx::prefetch_tmap(&tm_k);
-            ptx::prefetch_tmap(&tm_v);
-            ptx::prefetch_tmap(&tm_q);
-            for (int t = 0; t < 2; ++t) {
-                if ((t == 0 ? npos0 : npos1) <= 0)
-                    continue;
-                ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
-                for (int pp = 0; pp < L::kPanels; ++pp)
-                    ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, &tm_q, bars.q_full(t),
-                                     pp * 64, g * G, cq0 + q0 + t * P);
-            }
-        }
-        auto sub_row = [&](int j) -> int {
-            const int key = j * 128 + lane * box_rows;
-            if (lane >= nsub || key >= lk)
-                return p.num_slots; // fully out of range: TMA fills zeros
-            const int phys = __ldg(bt + key / bs);
-            return phys * bs + (key & (bs - 1));
-        };
-        // raw codes of key tile j (one box of D bytes x box_rows per block) into the staging slot
-        auto load = [&](bool is_k, int j, int cur) {
-            const int st = j % (is_k ? L::kKStages : L::kVStages);
-            const uint32_t bar = is_k ? bars.k_load(st) : bars.v_load(st);
-            const uint32_t dst = sbase + (is_k ? L::k_codes(st) : L::v_codes(st));
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(bar, (uint32_t)L::kCodeBytes);
-            if (lane < nsub)
-                ptx::tma_load_3d(dst + lane * box_rows * D, is_k ? &tm_k : &tm_v, bar, 0, g, cur);
-            __syncwarp();
-        };
-        int next = row0; // sub_row(0), read at kernel entry
-        for (int j = 0; j < nkt; ++j) {
-            const int cur = next;
-            if (j + 1 < nkt)
-                next = sub_row(j + 1);
-            // K tile j replaces tile j - S_K: free after release event j - S_K
-            if (j >= L::kKStages) {
-                const int e = j - L::kKStages;
-                if (!__all_sync(0xffffffffu, wait(bars.released(e), (e / kIterRing) & 1)))
-                    break;
-            }
-            load(true, j, cur);
-            // V tile j replaces tile j - S_V: free after release event j - S_V + 1
-            if (j >= L::kVStages) {
-                const int e = j - L::kVStages + 1;
-                if (!__all_sync(0xffffffffu, wait(bars.released(e), (e / kIterRing) & 1)))
-                    break;
-            }
-            load(false, j, cur);
-        }
-    } else if (I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
-        // ---------------------------------------------------------------- INT8: converters
-        // warp 8: query tile 0 and every K tile; warp 10: query tile 1, every V
-        // tile and the per-key factors.  Codes become exact f16 values; the scales
-        // are applied after the products (softmax), not to the tiles.
-        const bool is_k = warp == kKProducerWarp;
-        const int tq = is_k ? 0 : 1;
-        bool ok = true;
-        if ((tq == 0 ? npos0 : npos1) > 0) {
-            ok = __all_sync(0xffffffffu, wait(bars.q_full(tq), 0));
-            if (ok) {
-                q_tile_to_f16<D>(sgen + L::kQ + tq * L::kTileBytes, lane);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(bars.q_ready(tq));
-            }
-        }
-        if (is_k) {
-            for (int j = 0; ok && j < nkt; ++j) {
-                const int st = j % L::kKStages;
-                if (!(ok = __all_sync(0xffffffffu, wait(bars.k_load(st), (j / L::kKStages) & 1))))
-                    break;
-                convert_codes<D, L::kInPlace>(sbase + L::k_codes(st), sbase + L::kK + st * L::kTileBytes, lane);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(bars.k_full(st));
-            }
-        } else {
-            // factors of key tile j, keys 4*lane .. 4*lane+3 (one block: bs >= 16)
-            const int bs = p.block_size, Hkv = p.num_kv_heads;
-            const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
-            const float sl2 = p.scale_log2;
-            auto fetch = [&](int j, uint2 &kr, uint2 &vr) {
-                const int key = j * 128 + 4 * lane;
-                kr = vr = make_uint2(0u, 0u);
-                if (key < lk) {
-                    const int phys = __ldg(bt + key / bs);
-                    const size_t si = ((size_t)phys * Hkv + g) * bs + (key & (bs - 1));
-                    kr = __ldg(reinterpret_cast<const uint2 *>(p.k_scale + si));
-                    vr = __ldg(reinterpret_cast<const uint2 *>(p.v_scale + si));
-                }
+            auto sub_row = [&](int j) -> int {
+                const int key = j * 128 + lane * box_rows;
+                if (lane >= nsub || key >= lk)
+                    return p.num_slots; // fully out of range: TMA fills zeros
+                const int phys = __ldg(bt + key / bs);
+                return phys * bs + (key & (bs - 1));
             };
-            uint2 kr, vr;
-            fetch(0, kr, vr);
-            for (int j = 0; ok && j < nkt; ++j) {
-                // slot j & 1 held tile j - 2's factors, read until release event j - 1
-                if (j >= 2 && !(ok = __all_sync(0xffffffffu,
-                                                 wait(bars.released(j - 1), ((j - 1) / kIterRing) & 1))))
-                    break;
-                {
-                    const int key = j * 128 + 4 * lane;
-                    const uint32_t kw[2] = {kr.x, kr.y};
-                    uint32_t vw[2] = {vr.x, vr.y};
-                    float kf[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        // keys past the sequence: factor 0 (their scores are masked, their weights 0)
-                        const bool valid = key + i < lk;
-                        const float ks = __half2float(__ushort_as_half((unsigned short)(kw[i >> 1] >> (16 * (i & 1)))));
-                        kf[i] = valid ? ks * sl2 : 0.f;
-                        if (!valid)
-                            vw[i >> 1] &= (i & 1) ? 0x0000ffffu : 0xffff0000u;
-                    }
-                    uint8_t *slot = sgen + L::kScl + (j & 1) * L::kSclSlot;
-                    *reinterpret_cast<float4 *>(slot + 16 * lane) = make_float4(kf[0], kf[1], kf[2], kf[3]);
-                    *reinterpret_cast<uint2 *>(slot + 512 + 8 * lane) = make_uint2(vw[0], vw[1]); // fp16 V scales
+            // raw codes of key tile j (one box of D bytes x box_rows per block) into the staging slot
+            auto load = [&](bool is_k, int j, int cur) {
+                const int st = j % (is_k ? L::kKStages : L::kVStages);
+                const uint32_t bar = is_k ? bars.k_load(st) : bars.v_load(st);
+                const uint32_t dst = sbase + (is_k ? L::k_codes(st) : L::v_codes(st));
+                if (lane == 0)
+                    ptx::mbar_arrive_expect_tx(bar, (uint32_t)L::kCodeBytes);
+                if (lane < nsub)
+                    ptx::tma_load_3d(dst + lane * box_rows * D, is_k ? &tm_k : &tm_v, bar, 0, g, cur);
+                __syncwarp();
+            };
+            int next = row0; // sub_row(0), read at kernel entry
+            for (int j = 0; j < nkt; ++j) {
+                const int cur = next;
+                if (j + 1 < nkt)
+                    next = sub_row(j + 1);
+                // K tile j replaces tile j - S_K: free after release event j - S_K
+                if (j >= L::kKStages) {
+                    const int e = j - L::kKStages;
+                    if (!__all_sync(0xffffffffu, wait(bars.released(e), (e / kIterRing) & 1)))
+                        break;
+                }
+                load(true, j, cur);
+                // V tile j replaces tile j - S_V: free after release event j - S_V + 1
+                if (j >= L::kVStages) {
+                    const int e = j - L::kVStages + 1;
+                    if (!__all_sync(0xffffffffu, wait(bars.released(e), (e / kIterRing) & 1)))
+                        break;
+                }
+                load(false, j, cur);
+            }
+        } else if (I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
+            // ---------------------------------------------------------------- INT8: converters
+            // warp 8: query tile 0 and every K tile; warp 10: query tile 1, every V
+            // tile and the per-key factors.  Codes become exact f16 values; the scales
+            // are applied after the products (softmax), not to the tiles.
+            const bool is_k = warp == kKProducerWarp;
+            const int tq = is_k ? 0 : 1;
+            bool ok = true;
+            if ((tq == 0 ? npos0 : npos1) > 0) {
+                ok = __all_sync(0xffffffffu, wait(bars.q_full(tq), 0));
+                if (ok) {
+                    q_tile_to_f16<D>(sgen + L::kQ + tq * L::kTileBytes, lane);
+                    ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0)
-                        ptx::mbar_arrive(bars.sc_full(j & 1));
-                }
-                if (j + 1 < nkt)
-                    fetch(j + 1, kr, vr);
-                const int st = j % L::kVStages;
-                if (!(ok = __all_sync(0xffffffffu, wait(bars.v_load(st), (j / L::kVStages) & 1))))
-                    break;
-                convert_codes<D, L::kInPlace>(sbase + L::v_codes(st), sbase + L::kV + st * L::kTileBytes, lane);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::mbar_arrive(bars.v_full(st));
-                    if (tail && j == nkt - 1)
-                        ptx::mbar_arrive(bars.v_tail()); // codes are finite and weights past the end 0: nothing to zero
+                        ptx::mbar_arrive(bars.q_ready(tq));
                 }
             }
-        }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            // INT8 cache: f16 operands (exact codes, f16 Q and P)
-            constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
-            constexpr uint32_t idesc_o = I8 ? ptx::idesc_f16(128, D, 1) : ptx::idesc_bf16(128, D, 1);
-            auto issue_s = [&](int t, int ks) {
-                const uint32_t qa = sbase + L::kQ + t * L::kTileBytes, kb = sbase + L::kK + ks * L::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                    ptx::mma_bf16_ss(tmem + t * 256, ptx::smem_desc(qa + o, 16, 1024, ptx::kSwizzle128B),
-                                     ptx::smem_desc(kb + o, 16, 1024, ptx::kSwizzle128B), idesc_s, kk > 0);
+            if (is_k) {
+                for (int j = 0; ok && j < nkt; ++j) {
+                    const int st = j % L::kKStages;
+                    if (!(ok = __all_sync(0xffffffffu, wait(bars.k_load(st), (j / L::kKStages) & 1))))
+                        break;
+                    convert_codes<D, L::kInPlace>(sbase + L::k_codes(st), sbase + L::kK + st * L::kTileBytes, lane);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(bars.k_full(st));
                 }
-            };
-            auto issue_pv = [&](int t, int vs, bool first) {
-                const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8,
-                                     ptx::smem_desc(vb + kk * 2048, L::kPanelBytes, 1024, ptx::kSwizzle128B), idesc_o,
-                                     (!first || kk > 0) ? 1u : 0u);
-            };
-            bool ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), 0);
-            if (ok && nkt1 > 0)
-                ok = wait(I8 ? bars.q_ready(1) : bars.q_full(1), 0);
-            ok = ok && wait(bars.k_full(0), 0);
-            if (ok) {
-                ptx::tc_fence_after();
-                issue_s(0, 0);
-                ptx::mma_commit(bars.s_full(0));
-                if (nkt1 > 0) {
-                    issue_s(1, 0);
-                    ptx::mma_commit(bars.s_full(1));
-                }
-                ptx::mma_commit(bars.released(0)); // K tile 0 read by both score MMAs
-            }
-            // ring positions kept as counters (no division in the issue loop)
-            int vs = 0, vph = 0, ksn = 1 % L::kKStages, kph = ksn == 0 ? 1 : 0;
-            for (int j = 0; ok && j < nkt; ++j) {
-                bool v_ready = false, k_next = false;
-                // one query tile: PV(t, j), then S(t, j + 1) into the same TMEM columns
-                auto step = [&](const int t, const int ntk) {
-                    if (!(ok = wait(bars.p_full(t), j & 1)))
-                        return;
-                    if (!v_ready) {
-                        if (!(ok = wait(bars.v_full(vs), vph)))
-                            return;
-                        if (tail && j == nkt - 1 && !(ok = wait(bars.v_tail(), 0)))
-                            return;
-                        v_ready = true;
+            } else {
+                // factors of key tile j, keys 4*lane .. 4*lane+3 (one block: bs >= 16)
+                const int bs = p.block_size, Hkv = p.num_kv_heads;
+                const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
+                const float sl2 = p.scale_log2;
+                auto fetch = [&](int j, uint2 &kr, uint2 &vr) {
+                    const int key = j * 128 + 4 * lane;
+                    kr = vr = make_uint2(0u, 0u);
+                    if (key < lk) {
+                        const int phys = __ldg(bt + key / bs);
+                        const size_t si = ((size_t)phys * Hkv + g) * bs + (key & (bs - 1));
+                        kr = __ldg(reinterpret_cast<const uint2 *>(p.k_scale + si));
+                        vr = __ldg(reinterpret_cast<const uint2 *>(p.v_scale + si));
                     }
-                    ptx::tc_fence_after();
-                    issue_pv(t, vs, j == 0);
-                    if (j + 1 < ntk) {
-                        if (!k_next) {
-                            if (!(ok = wait(bars.k_full(ksn), kph)))
-                                return;
-                            ptx::tc_fence_after();
-                            k_next = true;
-                        }
-                        issue_s(t, ksn);
-                    }
-                    ptx::mma_commit(bars.s_full(t)); // next scores ready, or the final O
                 };
-                if (j < nkt0)
-                    step(0, nkt0);
-                if (ok && j < nkt1)
-                    step(1, nkt1);
-                if (ok)
-                    ptx::mma_commit(bars.released(j + 1)); // V tile j and K tile j + 1 read
-                if (++vs == L::kVStages) {
-                    vs = 0;
-                    vph ^= 1;
-                }
-                if (++ksn == L::kKStages) {
-                    ksn = 0;
-                    kph ^= 1;
+                uint2 kr, vr;
+                fetch(0, kr, vr);
+                for (int j = 0; ok && j < nkt; ++j) {
+                    // slot j & 1 held tile j - 2's factors, read until release event j - 1
+                    if (j >= 2 && !(ok = __all_sync(0xffffffffu,
+                                                     wait(bars.released(j - 1), ((j - 1) / kIterRing) & 1))))
+                        break;
+                    {
+                        const int key = j * 128 + 4 * lane;
+                        const uint32_t kw[2] = {kr.x, kr.y};
+                        uint32_t vw[2] = {vr.x, vr.y};
+                        float kf[4];
+    #pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            // keys past the sequence: factor 0 (their scores are masked, their weights 0)
+                            const bool valid = key + i < lk;
+                            const float ks = __half2float(__ushort_as_half((unsigned short)(kw[i >> 1] >> (16 * (i & 1)))));
+                            kf[i] = valid ? ks * sl2 : 0.f;
+                            if (!valid)
+                                vw[i >> 1] &= (i & 1) ? 0x0000ffffu : 0xffff0000u;
+                        }
+                        uint8_t *slot = sgen + L::kScl + (j & 1) * L::kSclSlot;
+                        *reinterpret_cast<float4 *>(slot + 16 * lane) = make_float4(kf[0], kf[1], kf[2], kf[3]);
+                        *reinterpret_cast<uint2 *>(slot + 512 + 8 * lane) = make_uint2(vw[0], vw[1]); // fp16 V scales
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::mbar_arrive(bars.sc_full(j & 1));
+                    }
+                    if (j + 1 < nkt)
+                        fetch(j + 1, kr, vr);
+                    const int st = j % L::kVStages;
+                    if (!(ok = __all_sync(0xffffffffu, wait(bars.v_load(st), (j / L::kVStages) & 1))))
+                        break;
+                    convert_codes<D, L::kInPlace>(sbase + L::v_codes(st), sbase + L::kV + st * L::kTileBytes, lane);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::mbar_arrive(bars.v_full(st));
+                        if (tail && j == nkt - 1)
+                            ptx::mbar_arrive(bars.v_tail()); // codes are finite and weights past the end 0: nothing to zero
+                    }
                 }
             }
+        } else if (warp == kMmaWarp) {
+            // ---------------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                // INT8 cache: f16 operands (exact codes, f16 Q and P)
+                constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
+                constexpr uint32_t idesc_o = I8 ? ptx::idesc_f16(128, D, 1) : ptx::idesc_bf16(128, D, 1);
+                auto issue_s = [&](int t, int ks) {
+                    const uint32_t qa = sbase + L::kQ + t * L::kTileBytes, kb = sbase + L::kK + ks * L::kTileBytes;
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t o = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+                        ptx::mma_bf16_ss(tmem + t * 256, ptx::smem_desc(qa + o, 16, 1024, ptx::kSwizzle128B),
+                                         ptx::smem_desc(kb + o, 16, 1024, ptx::kSwizzle128B), idesc_s, kk > 0);
+                    }
+                };
+                auto issue_pv = [&](int t, int vs, bool first) {
+                    const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
+    #pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8,
+                                         ptx::smem_desc(vb + kk * 2048, L::kPanelBytes, 1024, ptx::kSwizzle128B), idesc_o,
+                                         (!first || kk > 0) ? 1u : 0u);
+                };
+                bool ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), 0);
+                if (ok && nkt1 > 0)
+                    ok = wait(I8 ? bars.q_ready(1) : bars.q_full(1), 0);
+                ok = ok && wait(bars.k_full(0), 0);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s(0, 0);
+                    ptx::mma_commit(bars.s_full(0));
+                    if (nkt1 > 0) {
+                        issue_s(1, 0);
+                        ptx::mma_commit(bars.s_full(1));
+                    }
+                    ptx::mma_commit(bars.released(0)); // K tile 0 read by both score MMAs
+                }
+                // ring positions kept as counters (no division in the issue loop)
+                int vs = 0, vph = 0, ksn = 1 % L::kKStages, kph = ksn == 0 ? 1 : 0;
+                for (int j = 0; ok && j < nkt; ++j) {
+                    bool v_ready = false, k_next = false;
+                    // one query tile: PV(t, j), then S(t, j + 1) into the same TMEM columns
+                    auto step = [&](const int t, const int ntk) {
+                        if (!(ok = wait(bars.p_full(t), j & 1)))
+                            return;
+                        if (!v_ready) {
+                            if (!(ok = wait(bars.v_full(vs), vph)))
+                                return;
+                            if (tail && j == nkt - 1 && !(ok = wait(bars.v_tail(), 0)))
+                                return;
+                            v_ready = true;
+                        }
+                        ptx::tc_fence_after();
+                        issue_pv(t, vs, j == 0);
+                        if (j + 1 < ntk) {
+                            if (!k_next) {
+                                if (!(ok = wait(bars.k_full(ksn), kph)))
+                                    return;
+                                ptx::tc_fence_after();
+                                k_next = true;
+                            }
+                            issue_s(t, ksn);
+                        }
+                        ptx::mma_commit(bars.s_full(t)); // next scores ready, or the final O
+                    };
+                    if (j < nkt0)
+                        step(0, nkt0);
+                    if (ok && j < nkt1)
+                        step(1, nkt1);
+                    if (ok)
+                        ptx::mma_commit(bars.released(j + 1)); // V tile j and K tile j + 1 read
+                    if (++vs == L::kVStages) {
+                        vs = 0;
+                        vph ^= 1;
+                    }
+                    if (++ksn == L::kKStages) {
+                        ksn = 0;
+                        kph ^= 1;
+                    }
+                }
+            }
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (warp < 8) {
+    } else {
         // ---------------------------------------------------------------- softmax + epilogue
+        if constexpr (!I8)
+            ptx::reg_alloc<224>();
         const int t = warp >> 2;                   // query tile of this warpgroup (warps 0-3, 4-7)
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;         // query row of the tile
