@@ -172,7 +172,9 @@ int pa_store_kvcache(const pa_dims *dims, const void *k, const void *v, void *k_
  *   cu_seqlens_q, cu_seqlens_k, block_tables, tiles: device copies of the
  *            arrays pa_pack_prefill wrote (dev + meta->off_*)
  * bf16 in, fp32 accumulation and softmax, bf16 out (round to nearest even).
- * scale must be finite and > 0 (PA_ERR_INVALID_ARG otherwise).
+ * scale must be finite and > 0 (PA_ERR_INVALID_ARG otherwise).  PA_ERR_UNSUPPORTED,
+ * before any launch, if the library's prefill kernel was compiled with other
+ * than 168 registers per thread (its warps re-divide exactly that many).
  */
 int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache,
                       const void *v_cache, const int32_t *cu_seqlens_q,

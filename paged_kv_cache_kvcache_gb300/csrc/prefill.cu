@@ -68,10 +68,12 @@ namespace {
 // warps 0-7: softmax (two warpgroups), 8: K/Q TMA producer, 9: MMA issuer (and
 // TMEM owner), 10: V TMA producer, 11: idle (registers are granted per 4 warps,
 // so the CTA is sized at 12 warps, 168 registers each at launch; the bf16
-// variant moves them to the softmax warpgroups: 224 there, 56 in warps 8-11).  One thread issues
+// variant then moves part of warps 8-11's share to the softmax warpgroups:
+// 224 there, 56 in warps 8-11).  One thread issues
 // the MMAs of both query tiles: its in-order stream keeps the two tiles half a
 // key tile apart, so one tile's softmax always runs under the other's MMAs.
 constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168; // 65536 / 384, rounded down to the allocation unit of 8
 constexpr int kKProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10, kLoaderWarp = 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -246,6 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const PfParams p)
 {
     using L = PfLayout<D, I8>;
+    // per-thread register budgets after the hand-over (bf16 variant)
+    constexpr int kSoftmaxRegs = 224, kOtherRegs = 56;
+    static_assert(128 * (2 * kSoftmaxRegs + kOtherRegs) == kThreads * kLaunchRegs, "register hand-over");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -319,11 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kTmemSlotOffset);
 
     if (warp >= 8) {
-        // warps 8-11 (copies, conversion, MMA issue) need few registers: the
-        // bf16 variant hands 112 of each thread's 168 to the softmax warpgroups
-        // (128 x (56 + 224 + 224) = 384 x 168, the registers of the launch)
+        // bf16: warps 8-11 (copies, MMA issue) need few registers and hand part
+        // of their 168 to the softmax warpgroups (128 x (2 kSoftmaxRegs +
+        // kOtherRegs) = 384 x 168, the launch's registers).  The INT8 converters
+        // run faster keeping theirs.
         if constexpr (!I8)
-            ptx::reg_dealloc<56>();
+            ptx::reg_dealloc<kOtherRegs>();
         if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
             // ---------------------------------------------------------------- TMA producers (K + Q, V)
             const bool is_k = warp == kKProducerWarp;
@@ -655,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
         if constexpr (!I8)
-            ptx::reg_alloc<224>();
+            ptx::reg_alloc<kSoftmaxRegs>();
         const int t = warp >> 2;                   // query tile of this warpgroup (warps 0-3, 4-7)
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;         // query row of the tile
@@ -842,6 +848,20 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     using L = PfLayout<D, I8>;
     if (int rc = ensure_smem<prefill_kernel<D, I8>>(L::kSmemBytes, "prefill"))
         return rc;
+    // The register hand-over inside the kernel assumes kLaunchRegs per thread at
+    // launch; with fewer the softmax warpgroups' request could never be granted.
+    static std::atomic<int> launch_regs{0};
+    int nreg = launch_regs.load(std::memory_order_acquire);
+    if (nreg == 0) {
+        cudaFuncAttributes fa{};
+        const cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, I8>);
+        if (e != cudaSuccess)
+            return fail(PA_ERR_CUDA, "prefill kernel attributes: %s", cudaGetErrorString(e));
+        launch_regs.store(nreg = fa.numRegs, std::memory_order_release);
+    }
+    if (nreg != kLaunchRegs)
+        return fail(PA_ERR_UNSUPPORTED, "prefill kernel built with %d registers per thread, needs %d", nreg,
+                    kLaunchRegs);
     const pa_dims &d = a.dims;
     const int G = d.num_heads / d.num_kv_heads;
     const uint64_t rows = (uint64_t)d.num_blocks * d.block_size;
