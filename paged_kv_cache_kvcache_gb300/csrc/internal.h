@@ -53,6 +53,25 @@ int ensure_smem(int bytes, const char *what)
     return PA_OK;
 }
 
+// Number of SMs of the current device (looked up once per device).
+inline int sm_count(int *n)
+{
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    const bool slot = dev >= 0 && dev < 64;
+    if (slot && (*n = cached[dev].load(std::memory_order_relaxed)) > 0)
+        return PA_OK;
+    e = cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || *n < 1)
+        return fail(PA_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+    if (slot)
+        cached[dev].store(*n, std::memory_order_relaxed);
+    return PA_OK;
+}
+
 // 3-D TMA descriptor (dims innermost first, strides of dims 1 and 2 in bytes,
 // box in elements); PA_ERR_CUDA if the driver rejects it.
 int encode_tmap_3d(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t d0, uint64_t d1,

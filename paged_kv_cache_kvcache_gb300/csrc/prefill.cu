@@ -15,7 +15,8 @@
 //    kernel loses to tiled attention once prompts get long; the fix named
 //    there is query tiling with an in-tile causal mask.
 //
-// GB300 design (one CTA per work item, 12 warps, 1 CTA per SM):
+// GB300 design (persistent: one CTA per SM, 12 warps, each CTA walking its
+// share of the work items; every ring and barrier phase runs on across items):
 //  * A work item is (sequence, 2 query tiles, KV head).  Query tile rows
 //    r = pos * G + h pack the G query heads that share a KV head next to each
 //    other, so one K/V stream feeds all of them (GQA reuse); a 3-D TMA box
@@ -26,21 +27,26 @@
 //    per physical block (or one per tile when a block holds >= 128 tokens)
 //    into a K/V ring; boxes past the end of the pool read as zeros and the V
 //    rows past the sequence end are zeroed before use.
-//  * warp 8: K + Q TMA producer; warp 10: V producer; warp 9: TMEM owner and
-//    the single thread issuing every tcgen05.mma.  Each query tile t owns 256
+//  * warp 8: K TMA producer; warp 10: V producer; warp 11: Q producer (it
+//    refills a query tile as soon as the item's last score MMA of that tile
+//    has read it); warp 9: TMEM owner and the single thread issuing every
+//    tcgen05.mma.  Each query tile t owns 256
 //    TMEM columns: S_t (128 fp32 columns, reused for P_t) and O_t.  The issue
 //    order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core busy on
 //    one tile while the other tile's softmax runs (ping-pong).  Because the
 //    MMAs of one thread execute in order, S_t(j+1) being complete means
 //    PV_t(j) is too: O_t is stable and P_t consumed when the softmax sees
-//    S_t(j+1).
+//    S_t(j+1).  Across items the stream simply continues: the next item's first
+//    score MMAs follow the last PVs, so they run while the softmax warps write
+//    the previous item's output.
 //  * warps 0-3 and 4-7: one softmax warpgroup per query tile, one query row
 //    per thread: one tcgen05.ld round trip of the score row, causal mask only
 //    on tiles that cross the diagonal, fp32 online softmax in base 2
 //    (scale * log2 e folded into one packed FMA), lazy O rescale (only when
 //    the running max grows by more than 2^8), P written back over S with
 //    tcgen05.st and consumed by the PV MMA straight from tensor memory;
-//    epilogue O / l -> bf16 -> shared staging -> coalesced row stores.
+//    epilogue (once the item's last PV is complete) O / l -> bf16 -> each
+//    thread's own output row, straight from registers.
 //  * INT8 cache (prefill_kernel<D, true>; "面试问答准备: nano-vLLM 推理引擎优化",
 //    Q3 and its follow-up on where the scales go): warp 11 issues every TMA
 //    load, raw code tiles land next to (D = 128: inside) the tiles they are
@@ -65,23 +71,29 @@ __device__ uint32_t g_prefill_error; // bit 0: a bounded wait timed out
 
 namespace {
 
-// warps 0-7: softmax (two warpgroups), 8: K/Q TMA producer, 9: MMA issuer (and
-// TMEM owner), 10: V TMA producer, 11: idle (registers are granted per 4 warps,
-// so the CTA is sized at 12 warps, 168 registers each at launch; the bf16
-// variant then moves part of warps 8-11's share to the softmax warpgroups:
-// 224 there, 56 in warps 8-11).  One thread issues
-// the MMAs of both query tiles: its in-order stream keeps the two tiles half a
-// key tile apart, so one tile's softmax always runs under the other's MMAs.
+// warps 0-7: softmax (two warpgroups), 8: K TMA producer, 9: MMA issuer (and
+// TMEM owner), 10: V TMA producer, 11: Q TMA producer (INT8: 8 and 10 convert,
+// 11 loads everything).  Registers are granted per 4 warps, so the CTA is sized
+// at 12 warps, 168 registers each at launch; the bf16 variant then moves part
+// of warps 8-11's share to the softmax warpgroups: 216 there, 72 in warps 8-11.
+// One thread issues the MMAs of both query tiles: its in-order stream keeps the
+// two tiles half a key tile apart, so one tile's softmax always runs under the
+// other's MMAs.
 constexpr int kThreads = 384;
 constexpr int kLaunchRegs = 168; // 65536 / 384, rounded down to the allocation unit of 8
 constexpr int kKProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10, kLoaderWarp = 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f; // log2 units
-// Ring of release-event barriers.  A producer waits for event e while the MMA
-// thread cannot yet have passed event e + 3 (it needs the tile being loaded), so
-// 4 barriers keep every parity wait unambiguous.
-constexpr int kIterRing = 4;
+// Release events, numbered per CTA across its work items: an item with nkt key
+// tiles owns nkt + 1 consecutive events, the first for its opening score MMAs
+// (K tile 0 read), event first + j + 1 for MMA iteration j (V tile j and K tile
+// j + 1 read).  A producer refilling a ring of S slots waits for the event that
+// released the tile S places back; the MMA thread cannot pass the event that
+// needs the tile being loaded, and between the two lie at most 2S - 1 events
+// (one extra per item boundary), so 8 barriers keep every parity wait
+// unambiguous for rings of up to 4 slots.
+constexpr int kIterRing = 8;
 
 template <int D, bool I8>
 struct PfLayout {
@@ -124,6 +136,7 @@ struct PfLayout {
 };
 
 struct PfParams {
+    int32_t num_items;     // entries of `tiles` (the CTAs walk them persistently)
     const int32_t *cu_seqlens_q;
     const int32_t *cu_seqlens_k;
     const int32_t *block_tables;
@@ -145,24 +158,102 @@ struct PfParams {
 struct Bars {
     uint32_t base;
     __device__ uint32_t q_full(int t) const { return base + 8 * t; }
-    __device__ uint32_t k_full(int s) const { return base + 8 * (2 + s); }
-    __device__ uint32_t v_full(int s) const { return base + 8 * (6 + s); }
-    // release event e: the MMAs reading K tile e and V tile e - 1 are complete
-    // (event 0 = the prologue's score MMAs, event j + 1 = MMA iteration j)
-    __device__ uint32_t released(int e) const { return base + 8 * (10 + (e & (kIterRing - 1))); }
-    __device__ uint32_t s_full(int t) const { return base + 8 * (18 + t); }
-    __device__ uint32_t p_full(int t) const { return base + 8 * (20 + t); }
-    __device__ uint32_t v_tail() const { return base + 8 * 22; }
-    __device__ uint32_t tmem_slot() const { return base + 8 * 23; }
+    // the item's last score MMA of query tile t is complete: its Q buffer may be refilled
+    __device__ uint32_t q_free(int t) const { return base + 8 * (2 + t); }
+    __device__ uint32_t k_full(int s) const { return base + 8 * (4 + s); }
+    __device__ uint32_t v_full(int s) const { return base + 8 * (8 + s); }
+    __device__ uint32_t released(int e) const { return base + 8 * (12 + (e & (kIterRing - 1))); }
+    __device__ uint32_t s_full(int t) const { return base + 8 * (20 + t); }
+    __device__ uint32_t p_full(int t) const { return base + 8 * (22 + t); }
+    // the item's last PV MMA of query tile t is complete: O_t is final
+    __device__ uint32_t o_full(int t) const { return base + 8 * (24 + t); }
+    // V slot s holds an item's last key tile with its rows past the sequence end zeroed
+    __device__ uint32_t v_tail(int s) const { return base + 8 * (26 + s); }
+    __device__ uint32_t tmem_slot() const { return base + 8 * 30; }
     // INT8 variant: raw code tiles landed, per-key factors written, Q converted
-    __device__ uint32_t k_load(int s) const { return base + 8 * (25 + s); }
-    __device__ uint32_t v_load(int s) const { return base + 8 * (29 + s); }
-    __device__ uint32_t sc_full(int i) const { return base + 8 * (33 + i); }
-    __device__ uint32_t q_ready(int t) const { return base + 8 * (35 + t); }
+    __device__ uint32_t k_load(int s) const { return base + 8 * (32 + s); }
+    __device__ uint32_t v_load(int s) const { return base + 8 * (36 + s); }
+    __device__ uint32_t sc_full(int i) const { return base + 8 * (40 + i); }
+    __device__ uint32_t q_ready(int t) const { return base + 8 * (42 + t); }
 };
-constexpr int kTmemSlotOffset = 8 * 23;
-static_assert(kIterRing == 4, "barrier slots 10..13");
-constexpr int kAbortOffset = 8 * 24;
+static_assert(kIterRing == 8, "barrier slots 12..19");
+constexpr int kTmemSlotOffset = 8 * 30;
+constexpr int kAbortOffset = 8 * 31;
+
+// One work item: (sequence, two query tiles of P positions, KV head) and the
+// key tiles each query tile sees.
+struct Item {
+    int ord;                // position in this CTA's sequence of items
+    int b, q0, g, cq0, lq, lk;
+    int npos0, npos1;       // valid positions of query tiles 0 and 1 (tile 1 may be empty)
+    int nkt0, nkt1, nkt;    // key tiles of each query tile; nkt = max
+    bool tail;              // the last key tile runs past the sequence end
+};
+
+// The items of this CTA: rounds of gridDim.x consecutive entries of the list
+// (sorted longest first), odd rounds walked backwards so that the CTAs' totals
+// stay even.  The next item's entry is fetched while the current one runs
+// (from its start, or where the caller asks, to keep it out of a register-heavy loop).
+struct ItemIter {
+    const int4 *tiles;
+    int n, P, ord, idx;
+    int4 a0, a1;
+    __device__ static int index(int ord)
+    {
+        const int c = (int)gridDim.x;
+        return ord * c + ((ord & 1) ? c - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    }
+    __device__ ItemIter(const int4 *t, int n_, int P_) : tiles(t), n(n_), P(P_), ord(0), idx(index(0))
+    {
+        if (idx < n) {
+            a0 = __ldg(tiles + 2 * idx);
+            a1 = __ldg(tiles + 2 * idx + 1);
+        }
+    }
+    __device__ bool more() const { return idx < n; }
+    __device__ Item decode(int o) const
+    {
+        Item w;
+        w.ord = o;
+        w.b = a0.x, w.q0 = a0.y, w.g = a0.z;
+        w.cq0 = a1.x, w.lq = a1.y, w.lk = a1.z;
+        const int off = w.lk - w.lq; // absolute position of query row 0
+        w.npos0 = min(P, w.lq - w.q0);
+        w.npos1 = max(0, min(P, w.lq - w.q0 - P));
+        w.nkt0 = (off + w.q0 + w.npos0 + 127) >> 7;
+        w.nkt1 = w.npos1 > 0 ? (off + w.q0 + P + w.npos1 + 127) >> 7 : 0;
+        w.nkt = max(w.nkt0, w.nkt1);
+        w.tail = w.nkt * 128 > w.lk;
+        return w;
+    }
+    // the current item; advances to the next and (unless told not to) starts fetching its entry
+    __device__ Item next(bool fetch_now = true)
+    {
+        const Item w = decode(ord);
+        idx = index(++ord);
+        if (fetch_now)
+            fetch();
+        return w;
+    }
+    __device__ void fetch()
+    {
+        if (idx < n) {
+            a0 = __ldg(tiles + 2 * idx);
+            a1 = __ldg(tiles + 2 * idx + 1);
+        }
+    }
+    // the item next() returns next (valid while more())
+    __device__ Item peek() const { return decode(ord); }
+};
+
+// Release event of the key tile `back` places before global tile X (X >= back),
+// given the current item's ordinal and the item-start bits of the last tiles
+// (bit i: tile X - i opens its item).  K tile j of item i is released by event
+// (its global index) + i, V tile j one event later.
+__device__ __forceinline__ int release_event(int X, int back, int ord, uint32_t starts, int v)
+{
+    return X - back + ord - __popc(starts & ((1u << back) - 1u)) + v;
+}
 
 struct Waiter {
     volatile uint32_t *abort;
@@ -242,6 +333,37 @@ __device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int lane)
     }
 }
 
+// Rows G*P..127 of each query tile receive no TMA data: zero them once so their
+// (discarded) scores stay finite and cost the same as real rows.
+template <int D, bool I8>
+__device__ __forceinline__ void zero_query_padding(uint8_t *sgen, int first, int lane)
+{
+    using L = PfLayout<D, I8>;
+    if (first >= 128)
+        return;
+    const int chunks = (128 - first) * 8;
+    for (int t = 0; t < 2; ++t)
+        for (int pp = 0; pp < L::kPanels; ++pp)
+            for (int c = lane; c < chunks; c += 32)
+                *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
+                                           (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+}
+
+// Query tile t of item w: one 3-D box {64 d, G heads, P positions} per panel.
+// Always issued, also for an empty tile 1 (its rows are never used).
+template <int D, bool I8>
+__device__ __forceinline__ void load_query_tile(const CUtensorMap *tm_q, const Bars &bars, uint32_t sbase,
+                                                const Item &w, int t, int G, int P)
+{
+    using L = PfLayout<D, I8>;
+    ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
+    for (int pp = 0; pp < L::kPanels; ++pp)
+        ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, tm_q, bars.q_full(t), pp * 64,
+                         w.g * G, w.cq0 + w.q0 + t * P);
+}
+
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -249,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using L = PfLayout<D, I8>;
     // per-thread register budgets after the hand-over (bf16 variant)
-    constexpr int kSoftmaxRegs = 224, kOtherRegs = 56;
+    constexpr int kSoftmaxRegs = 216, kOtherRegs = 72;
     static_assert(128 * (2 * kSoftmaxRegs + kOtherRegs) == kThreads * kLaunchRegs, "register hand-over");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -261,46 +383,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Bars bars{sbase + L::kBar};
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kAbortOffset);
     const Waiter wait{abort_flag};
-
-    // work-list entry: two independent 16-byte loads, no dependent metadata reads
-    const int4 e0 = __ldg(p.tiles + 2 * blockIdx.x), e1 = __ldg(p.tiles + 2 * blockIdx.x + 1);
-    const int b = e0.x, q0 = e0.y, g = e0.z;
-    const int cq0 = e1.x, lq = e1.y, lk = e1.z;
     const int G = p.group;
     const int P = p.rows_per_tile;
-    const int off = lk - lq; // absolute position of query row 0
-    // valid positions and key tiles of each query tile (tile 1 may be empty)
-    const int npos0 = min(P, lq - q0);
-    const int npos1 = max(0, min(P, lq - q0 - P));
-    const int nkt0 = (off + q0 + npos0 + 127) >> 7;
-    const int nkt1 = npos1 > 0 ? (off + q0 + P + npos1 + 127) >> 7 : 0;
-    const int nkt = max(nkt0, nkt1);
-    const bool tail = nkt * 128 > lk; // last key tile runs past the sequence end
-
-    // Block ids of key tile 0 (one TMA box per lane), read before the set-up below so
-    // that their latency overlaps it: the producers' first loads depend on them.
-    const int box_rows0 = p.block_size < 128 ? p.block_size : 128;
-    int row0 = p.num_slots;
-    if ((warp == kKProducerWarp || warp == kVProducerWarp || (I8 && warp == kLoaderWarp)) &&
-        lane < 128 / box_rows0 && lane * box_rows0 < lk) {
-        const int key = lane * box_rows0;
-        row0 = __ldg(p.block_tables + (size_t)b * p.max_blocks + key / p.block_size) * p.block_size +
-               (key & (p.block_size - 1));
-    }
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bars.q_full(t), 1);
+            ptx::mbar_init(bars.q_free(t), 1);
             ptx::mbar_init(bars.s_full(t), 1);
             ptx::mbar_init(bars.p_full(t), 4); // one arrival per softmax warp
+            ptx::mbar_init(bars.o_full(t), 1);
         }
         for (int s = 0; s < L::kKStages; ++s)
             ptx::mbar_init(bars.k_full(s), 1);
-        for (int s = 0; s < L::kVStages; ++s)
+        for (int s = 0; s < L::kVStages; ++s) {
             ptx::mbar_init(bars.v_full(s), 1);
+            ptx::mbar_init(bars.v_tail(s), 1);
+        }
         for (int s = 0; s < kIterRing; ++s)
             ptx::mbar_init(bars.released(s), 1);
-        ptx::mbar_init(bars.v_tail(), 1);
         if constexpr (I8) {
             for (int s = 0; s < L::kKStages; ++s)
                 ptx::mbar_init(bars.k_load(s), 1);
@@ -322,514 +423,552 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kTmemSlotOffset);
+    auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
 
     if (warp >= 8) {
-        // bf16: warps 8-11 (copies, MMA issue) need few registers and hand part
+        // bf16: warps 8-11 (copies, MMA issue) need fewer registers and hand part
         // of their 168 to the softmax warpgroups (128 x (2 kSoftmaxRegs +
         // kOtherRegs) = 384 x 168, the launch's registers).  The INT8 converters
         // run faster keeping theirs.
         if constexpr (!I8)
             ptx::reg_dealloc<kOtherRegs>();
-        if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
-            // ---------------------------------------------------------------- TMA producers (K + Q, V)
+        const int bs = p.block_size;
+        const int box_rows = bs < 128 ? bs : 128;
+        const int nsub = 128 / box_rows;
+        // row coordinate of sub-box `lane` of key tile j of item w (one TMA box per lane)
+        auto sub_row = [&](const Item &w, const int32_t *bt, int j) -> int {
+            const int key = j * 128 + lane * box_rows;
+            if (lane >= nsub || key >= w.lk)
+                return p.num_slots; // fully out of range: TMA fills zeros
+            const int phys = __ldg(bt + key / bs);
+            return phys * bs + (key & (bs - 1));
+        };
+        if (!I8 && warp == kLoaderWarp) {
+            // ------------------------------------------------------------ bf16: Q producer
+            ItemIter items(p.tiles, p.num_items, P);
+            zero_query_padding<D, I8>(sgen, G * P, lane);
+            if (lane == 0)
+                ptx::prefetch_tmap(&tm_q);
+            bool ok = true;
+            while (ok && items.more()) {
+                const Item w = items.next();
+                for (int t = 0; t < 2; ++t) {
+                    // refill after the previous item's last score MMA of this tile
+                    if (w.ord > 0 && !(ok = wwait(bars.q_free(t), (w.ord - 1) & 1)))
+                        break;
+                    if (lane == 0)
+                        load_query_tile<D, I8>(&tm_q, bars, sbase, w, t, G, P);
+                    __syncwarp();
+                }
+            }
+        } else if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
+            // ------------------------------------------------------------ bf16: K and V producers
+            ItemIter items(p.tiles, p.num_items, P);
             const bool is_k = warp == kKProducerWarp;
-            const int bs = p.block_size;
-            const int box_rows = bs < 128 ? bs : 128;
-            const int nsub = 128 / box_rows;
-            const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
             const int nstages = is_k ? L::kKStages : L::kVStages;
             const uint32_t ring = sbase + (is_k ? L::kK : L::kV);
             const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
-            if (is_k && G * P < 128) {
-                // rows G*P..127 of each query tile receive no TMA data: zero them once so
-                // their (discarded) scores stay finite and cost the same as real rows
-                const int first = G * P, chunks = (128 - first) * 8;
-                for (int t = 0; t < 2; ++t)
-                    for (int pp = 0; pp < L::kPanels; ++pp)
-                        for (int c = lane; c < chunks; c += 32)
-                            *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
-                                                       (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (lane == 0) {
+            if (lane == 0)
                 ptx::prefetch_tmap(tm);
-                if (is_k) {
-                    ptx::prefetch_tmap(&tm_q);
-                    for (int t = 0; t < 2; ++t) {
-                        if ((t == 0 ? npos0 : npos1) <= 0)
-                            continue;
-                        ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
+            uint32_t starts = 0; // bit i: global key tile X - i opens its item
+            int X = 0;           // global key tile (this CTA, all items)
+            bool ok = true;
+            while (ok && items.more()) {
+                const Item w = items.next();
+                const int32_t *bt = p.block_tables + (size_t)w.b * p.max_blocks;
+                int next = sub_row(w, bt, 0);
+                for (int j = 0; j < w.nkt; ++j, ++X) {
+                    const int cur = next;
+                    if (j + 1 < w.nkt)
+                        next = sub_row(w, bt, j + 1);
+                    starts = (starts << 1) | (j == 0 ? 1u : 0u);
+                    const int st = X % nstages;
+                    // slot reuse: free once the tile nstages back is released
+                    if (X >= nstages) {
+                        const int e = release_event(X, nstages, w.ord, starts, is_k ? 0 : 1);
+                        if (!(ok = wwait(bars.released(e), (e / kIterRing) & 1)))
+                            break;
+                    }
+                    const uint32_t full = is_k ? bars.k_full(st) : bars.v_full(st);
+                    const uint32_t dst = ring + st * L::kTileBytes;
+                    if (lane == 0)
+                        ptx::mbar_arrive_expect_tx(full, (uint32_t)L::kTileBytes);
+                    // lane i issues the boxes of sub-box i (its own row coordinate)
+                    if (lane < nsub)
                         for (int pp = 0; pp < L::kPanels; ++pp)
-                            ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, &tm_q,
-                                             bars.q_full(t), pp * 64, g * G, cq0 + q0 + t * P);
+                            ptx::tma_load_3d(dst + pp * L::kPanelBytes + lane * box_rows * 128, tm, full, pp * 64,
+                                             w.g, cur);
+                    __syncwarp();
+                    if (!is_k && w.tail && j == w.nkt - 1) {
+                        // V rows of keys past the sequence end may hold anything (even NaN
+                        // bit patterns); zero them so that P = 0 cannot turn them into NaN in O.
+                        if (!(ok = wwait(full, (X / nstages) & 1)))
+                            break;
+                        const int first = w.lk - j * 128;
+                        uint8_t *vt = sgen + L::kV + st * L::kTileBytes;
+                        const int chunks = (128 - first) * 8;
+                        for (int pp = 0; pp < L::kPanels; ++pp)
+                            for (int c = lane; c < chunks; c += 32)
+                                *reinterpret_cast<uint4 *>(vt + pp * L::kPanelBytes + (first + (c >> 3)) * 128 +
+                                                           (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::mbar_arrive(bars.v_tail(st));
                     }
                 }
             }
-            // row coordinate of sub-box `lane` of key tile j (all lanes compute their own)
-            auto sub_row = [&](int j) -> int {
-                const int key = j * 128 + lane * box_rows;
-                if (lane >= nsub || key >= lk)
-                    return p.num_slots; // fully out of range: TMA fills zeros
-                const int phys = __ldg(bt + key / bs);
-                return phys * bs + (key & (bs - 1));
-            };
-            int next = row0; // sub_row(0), read at kernel entry
-            bool ok = true;
-            for (int j = 0; j < nkt; ++j) {
-                const int cur = next;
-                if (j + 1 < nkt)
-                    next = sub_row(j + 1);
-                const int st = j % nstages;
-                const uint32_t full = is_k ? bars.k_full(st) : bars.v_full(st);
-                // slot reuse: tile j replaces tile j - S, free after release event
-                // j - S (K) or j - S + 1 (V)
-                bool free_ok = true;
-                if (j >= nstages) {
-                    const int e = is_k ? j - nstages : j - nstages + 1;
-                    free_ok = wait(bars.released(e), (e / kIterRing) & 1);
-                }
-                if (!__all_sync(0xffffffffu, free_ok)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t dst = ring + st * L::kTileBytes;
-                if (lane == 0)
-                    ptx::mbar_arrive_expect_tx(full, (uint32_t)L::kTileBytes);
-                // lane i issues the boxes of sub-box i (its own row coordinate)
-                if (lane < nsub)
-                    for (int pp = 0; pp < L::kPanels; ++pp)
-                        ptx::tma_load_3d(dst + pp * L::kPanelBytes + lane * box_rows * 128, tm, full, pp * 64, g, cur);
-                __syncwarp();
-            }
-            if (!is_k && ok && tail) {
-                // V rows of keys past the sequence end may hold anything (even NaN bit
-                // patterns); zero them so that P = 0 cannot turn them into NaN in O.
-                const int j = nkt - 1, st = j % L::kVStages;
-                if (__all_sync(0xffffffffu, wait(bars.v_full(st), (j / L::kVStages) & 1))) {
-                    const int first = lk - j * 128;
-                    uint8_t *vt = sgen + L::kV + st * L::kTileBytes;
-                    const int chunks = (128 - first) * 8;
-                    for (int pp = 0; pp < L::kPanels; ++pp)
-                        for (int c = lane; c < chunks; c += 32)
-                            *reinterpret_cast<uint4 *>(vt + pp * L::kPanelBytes + (first + (c >> 3)) * 128 +
-                                                       (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(bars.v_tail());
-                }
-            }
         } else if (I8 && warp == kLoaderWarp) {
-            // ---------------------------------------------------------------- INT8: TMA loader (Q, K codes, V codes)
-            const int bs = p.block_size;
-            const int box_rows = bs < 128 ? bs : 128;
-            const int nsub = 128 / box_rows;
-            const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
-            if (G * P < 128) {
-                // rows G*P..127 of each query tile receive no TMA data: zero them once
-                const int first = G * P, chunks = (128 - first) * 8;
-                for (int t = 0; t < 2; ++t)
-                    for (int pp = 0; pp < L::kPanels; ++pp)
-                        for (int c = lane; c < chunks; c += 32)
-                            *reinterpret_cast<uint4 *>(sgen + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes +
-                                                       (first + (c >> 3)) * 128 + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-            }
+            // ------------------------------------------------------------ INT8: TMA loader (Q, K codes, V codes)
+            ItemIter items(p.tiles, p.num_items, P);
+            zero_query_padding<D, I8>(sgen, G * P, lane);
             if (lane == 0) {
                 ptx::prefetch_tmap(&tm_k);
                 ptx::prefetch_tmap(&tm_v);
                 ptx::prefetch_tmap(&tm_q);
-                for (int t = 0; t < 2; ++t) {
-                    if ((t == 0 ? npos0 : npos1) <= 0)
-                        continue;
-                    ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
-                    for (int pp = 0; pp < L::kPanels; ++pp)
-                        ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, &tm_q, bars.q_full(t),
-                                         pp * 64, g * G, cq0 + q0 + t * P);
-                }
             }
-            auto sub_row = [&](int j) -> int {
-                const int key = j * 128 + lane * box_rows;
-                if (lane >= nsub || key >= lk)
-                    return p.num_slots; // fully out of range: TMA fills zeros
-                const int phys = __ldg(bt + key / bs);
-                return phys * bs + (key & (bs - 1));
-            };
-            // raw codes of key tile j (one box of D bytes x box_rows per block) into the staging slot
-            auto load = [&](bool is_k, int j, int cur) {
-                const int st = j % (is_k ? L::kKStages : L::kVStages);
+            // raw codes of global key tile X (one box of D bytes x box_rows per block) into its staging slot
+            auto load = [&](bool is_k, int X, int cur, const Item &w) {
+                const int st = X % (is_k ? L::kKStages : L::kVStages);
                 const uint32_t bar = is_k ? bars.k_load(st) : bars.v_load(st);
                 const uint32_t dst = sbase + (is_k ? L::k_codes(st) : L::v_codes(st));
                 if (lane == 0)
                     ptx::mbar_arrive_expect_tx(bar, (uint32_t)L::kCodeBytes);
                 if (lane < nsub)
-                    ptx::tma_load_3d(dst + lane * box_rows * D, is_k ? &tm_k : &tm_v, bar, 0, g, cur);
+                    ptx::tma_load_3d(dst + lane * box_rows * D, is_k ? &tm_k : &tm_v, bar, 0, w.g, cur);
                 __syncwarp();
             };
-            int next = row0; // sub_row(0), read at kernel entry
-            for (int j = 0; j < nkt; ++j) {
-                const int cur = next;
-                if (j + 1 < nkt)
-                    next = sub_row(j + 1);
-                // K tile j replaces tile j - S_K: free after release event j - S_K
-                if (j >= L::kKStages) {
-                    const int e = j - L::kKStages;
-                    if (!__all_sync(0xffffffffu, wait(bars.released(e), (e / kIterRing) & 1)))
+            uint32_t starts = 0;
+            int X = 0;
+            bool ok = true;
+            while (ok && items.more()) {
+                const Item w = items.next();
+                for (int t = 0; t < 2; ++t) {
+                    if (w.ord > 0 && !(ok = wwait(bars.q_free(t), (w.ord - 1) & 1)))
                         break;
+                    if (lane == 0)
+                        load_query_tile<D, I8>(&tm_q, bars, sbase, w, t, G, P);
+                    __syncwarp();
                 }
-                load(true, j, cur);
-                // V tile j replaces tile j - S_V: free after release event j - S_V + 1
-                if (j >= L::kVStages) {
-                    const int e = j - L::kVStages + 1;
-                    if (!__all_sync(0xffffffffu, wait(bars.released(e), (e / kIterRing) & 1)))
-                        break;
+                const int32_t *bt = p.block_tables + (size_t)w.b * p.max_blocks;
+                int next = sub_row(w, bt, 0);
+                for (int j = 0; ok && j < w.nkt; ++j, ++X) {
+                    const int cur = next;
+                    if (j + 1 < w.nkt)
+                        next = sub_row(w, bt, j + 1);
+                    starts = (starts << 1) | (j == 0 ? 1u : 0u);
+                    if (X >= L::kKStages) {
+                        const int e = release_event(X, L::kKStages, w.ord, starts, 0);
+                        if (!(ok = wwait(bars.released(e), (e / kIterRing) & 1)))
+                            break;
+                    }
+                    load(true, X, cur, w);
+                    if (X >= L::kVStages) {
+                        const int e = release_event(X, L::kVStages, w.ord, starts, 1);
+                        if (!(ok = wwait(bars.released(e), (e / kIterRing) & 1)))
+                            break;
+                    }
+                    load(false, X, cur, w);
                 }
-                load(false, j, cur);
             }
         } else if (I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
-            // ---------------------------------------------------------------- INT8: converters
+            // ------------------------------------------------------------ INT8: converters
+            ItemIter items(p.tiles, p.num_items, P);
             // warp 8: query tile 0 and every K tile; warp 10: query tile 1, every V
             // tile and the per-key factors.  Codes become exact f16 values; the scales
             // are applied after the products (softmax), not to the tiles.
             const bool is_k = warp == kKProducerWarp;
             const int tq = is_k ? 0 : 1;
+            auto convert_q = [&](const Item &w) -> bool {
+                if (!wwait(bars.q_full(tq), w.ord & 1))
+                    return false;
+                q_tile_to_f16<D>(sgen + L::kQ + tq * L::kTileBytes, lane);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bars.q_ready(tq));
+                return true;
+            };
             bool ok = true;
-            if ((tq == 0 ? npos0 : npos1) > 0) {
-                ok = __all_sync(0xffffffffu, wait(bars.q_full(tq), 0));
-                if (ok) {
-                    q_tile_to_f16<D>(sgen + L::kQ + tq * L::kTileBytes, lane);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(bars.q_ready(tq));
-                }
-            }
+            int X = 0;
             if (is_k) {
-                for (int j = 0; ok && j < nkt; ++j) {
-                    const int st = j % L::kKStages;
-                    if (!(ok = __all_sync(0xffffffffu, wait(bars.k_load(st), (j / L::kKStages) & 1))))
+                while (ok && items.more()) {
+                    const Item w = items.next();
+                    if (!(ok = convert_q(w)))
                         break;
-                    convert_codes<D, L::kInPlace>(sbase + L::k_codes(st), sbase + L::kK + st * L::kTileBytes, lane);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(bars.k_full(st));
+                    for (int j = 0; j < w.nkt; ++j, ++X) {
+                        const int st = X % L::kKStages;
+                        if (!(ok = wwait(bars.k_load(st), (X / L::kKStages) & 1)))
+                            break;
+                        convert_codes<D, L::kInPlace>(sbase + L::k_codes(st), sbase + L::kK + st * L::kTileBytes,
+                                                      lane);
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0)
+                            ptx::mbar_arrive(bars.k_full(st));
+                    }
                 }
-            } else {
+            } else if (items.more()) {
                 // factors of key tile j, keys 4*lane .. 4*lane+3 (one block: bs >= 16)
-                const int bs = p.block_size, Hkv = p.num_kv_heads;
-                const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks;
+                const int Hkv = p.num_kv_heads;
                 const float sl2 = p.scale_log2;
-                auto fetch = [&](int j, uint2 &kr, uint2 &vr) {
+                auto fetch = [&](const Item &w, int j, uint2 &kr, uint2 &vr) {
                     const int key = j * 128 + 4 * lane;
                     kr = vr = make_uint2(0u, 0u);
-                    if (key < lk) {
-                        const int phys = __ldg(bt + key / bs);
-                        const size_t si = ((size_t)phys * Hkv + g) * bs + (key & (bs - 1));
+                    if (key < w.lk) {
+                        const int phys = __ldg(p.block_tables + (size_t)w.b * p.max_blocks + key / bs);
+                        const size_t si = ((size_t)phys * Hkv + w.g) * bs + (key & (bs - 1));
                         kr = __ldg(reinterpret_cast<const uint2 *>(p.k_scale + si));
                         vr = __ldg(reinterpret_cast<const uint2 *>(p.v_scale + si));
                     }
                 };
+                Item w = items.next();
                 uint2 kr, vr;
-                fetch(0, kr, vr);
-                for (int j = 0; ok && j < nkt; ++j) {
-                    // slot j & 1 held tile j - 2's factors, read until release event j - 1
-                    if (j >= 2 && !(ok = __all_sync(0xffffffffu,
-                                                     wait(bars.released(j - 1), ((j - 1) / kIterRing) & 1))))
+                fetch(w, 0, kr, vr);
+                uint32_t starts = 0;
+                for (int j = 0;; ++X) {
+                    if (j == 0 && !(ok = convert_q(w)))
                         break;
+                    starts = (starts << 1) | (j == 0 ? 1u : 0u);
+                    // slot X & 1 held tile X - 2's factors, read until V tile X - 2's release
+                    if (X >= 2) {
+                        const int e = release_event(X, 2, w.ord, starts, 1);
+                        if (!(ok = wwait(bars.released(e), (e / kIterRing) & 1)))
+                            break;
+                    }
                     {
                         const int key = j * 128 + 4 * lane;
                         const uint32_t kw[2] = {kr.x, kr.y};
                         uint32_t vw[2] = {vr.x, vr.y};
                         float kf[4];
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             // keys past the sequence: factor 0 (their scores are masked, their weights 0)
-                            const bool valid = key + i < lk;
+                            const bool valid = key + i < w.lk;
                             const float ks = __half2float(__ushort_as_half((unsigned short)(kw[i >> 1] >> (16 * (i & 1)))));
                             kf[i] = valid ? ks * sl2 : 0.f;
                             if (!valid)
                                 vw[i >> 1] &= (i & 1) ? 0x0000ffffu : 0xffff0000u;
                         }
-                        uint8_t *slot = sgen + L::kScl + (j & 1) * L::kSclSlot;
+                        uint8_t *slot = sgen + L::kScl + (X & 1) * L::kSclSlot;
                         *reinterpret_cast<float4 *>(slot + 16 * lane) = make_float4(kf[0], kf[1], kf[2], kf[3]);
                         *reinterpret_cast<uint2 *>(slot + 512 + 8 * lane) = make_uint2(vw[0], vw[1]); // fp16 V scales
                         __syncwarp();
                         if (lane == 0)
-                            ptx::mbar_arrive(bars.sc_full(j & 1));
+                            ptx::mbar_arrive(bars.sc_full(X & 1));
                     }
-                    if (j + 1 < nkt)
-                        fetch(j + 1, kr, vr);
-                    const int st = j % L::kVStages;
-                    if (!(ok = __all_sync(0xffffffffu, wait(bars.v_load(st), (j / L::kVStages) & 1))))
+                    // the next tile's factors (perhaps the next item's first) while V converts
+                    const bool last = j + 1 == w.nkt;
+                    if (!last)
+                        fetch(w, j + 1, kr, vr);
+                    else if (items.more())
+                        fetch(items.peek(), 0, kr, vr);
+                    const int st = X % L::kVStages;
+                    if (!(ok = wwait(bars.v_load(st), (X / L::kVStages) & 1)))
                         break;
                     convert_codes<D, L::kInPlace>(sbase + L::v_codes(st), sbase + L::kV + st * L::kTileBytes, lane);
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) {
-                        ptx::mbar_arrive(bars.v_full(st));
-                        if (tail && j == nkt - 1)
-                            ptx::mbar_arrive(bars.v_tail()); // codes are finite and weights past the end 0: nothing to zero
+                    if (lane == 0)
+                        ptx::mbar_arrive(bars.v_full(st)); // codes are finite and weights past the end 0: nothing to zero
+                    if (!last) {
+                        ++j;
+                    } else {
+                        if (!items.more())
+                            break;
+                        w = items.next();
+                        j = 0;
                     }
                 }
             }
-        } else if (warp == kMmaWarp) {
-            // ---------------------------------------------------------------- MMA issuer
-            if (lane == 0) {
-                // INT8 cache: f16 operands (exact codes, f16 Q and P)
-                constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
-                constexpr uint32_t idesc_o = I8 ? ptx::idesc_f16(128, D, 1) : ptx::idesc_bf16(128, D, 1);
-                auto issue_s = [&](int t, int ks) {
-                    const uint32_t qa = sbase + L::kQ + t * L::kTileBytes, kb = sbase + L::kK + ks * L::kTileBytes;
-    #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t o = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-                        ptx::mma_bf16_ss(tmem + t * 256, ptx::smem_desc(qa + o, 16, 1024, ptx::kSwizzle128B),
-                                         ptx::smem_desc(kb + o, 16, 1024, ptx::kSwizzle128B), idesc_s, kk > 0);
-                    }
-                };
-                auto issue_pv = [&](int t, int vs, bool first) {
-                    const uint32_t vb = sbase + L::kV + vs * L::kTileBytes;
-    #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8,
-                                         ptx::smem_desc(vb + kk * 2048, L::kPanelBytes, 1024, ptx::kSwizzle128B), idesc_o,
-                                         (!first || kk > 0) ? 1u : 0u);
-                };
-                bool ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), 0);
-                if (ok && nkt1 > 0)
-                    ok = wait(I8 ? bars.q_ready(1) : bars.q_full(1), 0);
-                ok = ok && wait(bars.k_full(0), 0);
-                if (ok) {
-                    ptx::tc_fence_after();
-                    issue_s(0, 0);
-                    ptx::mma_commit(bars.s_full(0));
-                    if (nkt1 > 0) {
-                        issue_s(1, 0);
-                        ptx::mma_commit(bars.s_full(1));
-                    }
-                    ptx::mma_commit(bars.released(0)); // K tile 0 read by both score MMAs
+        } else if (warp == kMmaWarp && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            ItemIter items(p.tiles, p.num_items, P);
+            // INT8 cache: f16 operands (exact codes, f16 Q and P)
+            constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
+            constexpr uint32_t idesc_o = I8 ? ptx::idesc_f16(128, D, 1) : ptx::idesc_bf16(128, D, 1);
+            // Shared-memory descriptors: a constant upper word and a lower word of base
+            // address + the k step's offset.  The base passes through an empty asm so that
+            // it is rebuilt at each use instead of hoisting all 16 k-step descriptors into
+            // registers (this warpgroup runs on few).
+            const uint32_t hi_k = (uint32_t)(ptx::smem_desc(0, 16, 1024, ptx::kSwizzle128B) >> 32);
+            const uint32_t hi_v = (uint32_t)(ptx::smem_desc(0, L::kPanelBytes, 1024, ptx::kSwizzle128B) >> 32);
+            auto desc = [](uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; };
+            auto issue_s = [&](int t, int ks) {
+                uint32_t qa = (uint32_t)ptx::smem_desc(sbase + L::kQ + t * L::kTileBytes, 16, 1024, ptx::kSwizzle128B);
+                uint32_t kb = (uint32_t)ptx::smem_desc(sbase + L::kK + ks * L::kTileBytes, 16, 1024, ptx::kSwizzle128B);
+                asm volatile("" : "+r"(qa), "+r"(kb));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t o = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
+                    ptx::mma_bf16_ss(tmem + t * 256, desc(qa + o, hi_k), desc(kb + o, hi_k), idesc_s, kk > 0);
                 }
-                // ring positions kept as counters (no division in the issue loop)
-                int vs = 0, vph = 0, ksn = 1 % L::kKStages, kph = ksn == 0 ? 1 : 0;
-                for (int j = 0; ok && j < nkt; ++j) {
+            };
+            auto issue_pv = [&](int t, int vs, bool first) {
+                uint32_t vb = (uint32_t)ptx::smem_desc(sbase + L::kV + vs * L::kTileBytes, L::kPanelBytes, 1024,
+                                                       ptx::kSwizzle128B);
+                asm volatile("" : "+r"(vb));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc(vb + kk * (2048 >> 4), hi_v),
+                                     idesc_o, (!first || kk > 0) ? 1u : 0u);
+            };
+            // ring positions kept as counters (no division in the issue loop)
+            int ks = 0, kph = 0, vs = 0, vph = 0;
+            uint32_t np = 0;       // bit t: parity of the P tiles of query tile t consumed so far
+            uint32_t tailpar = 0;  // bit s: parity of the tail tiles V slot s has held
+            int E = 0;             // first release event of the current item
+            bool ok = true;
+            while (ok && items.more()) {
+                const Item w = items.next();
+                const uint32_t qpar = w.ord & 1;
+                ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) &&
+                     wait(I8 ? bars.q_ready(1) : bars.q_full(1), qpar) && wait(bars.k_full(ks), kph);
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+                issue_s(0, ks);
+                ptx::mma_commit(bars.s_full(0));
+                if (w.nkt1 > 0) {
+                    issue_s(1, ks);
+                    ptx::mma_commit(bars.s_full(1));
+                }
+                ptx::mma_commit(bars.released(E)); // K tile 0 read by both score MMAs
+                if (w.nkt0 == 1)
+                    ptx::mma_commit(bars.q_free(0));
+                if (w.nkt1 <= 1)
+                    ptx::mma_commit(bars.q_free(1));
+                if (++ks == L::kKStages) {
+                    ks = 0;
+                    kph ^= 1;
+                }
+                for (int j = 0; ok && j < w.nkt; ++j) {
                     bool v_ready = false, k_next = false;
                     // one query tile: PV(t, j), then S(t, j + 1) into the same TMEM columns
                     auto step = [&](const int t, const int ntk) {
-                        if (!(ok = wait(bars.p_full(t), j & 1)))
+                        if (!(ok = wait(bars.p_full(t), (np >> t) & 1u)))
                             return;
+                        np ^= 1u << t;
                         if (!v_ready) {
                             if (!(ok = wait(bars.v_full(vs), vph)))
                                 return;
-                            if (tail && j == nkt - 1 && !(ok = wait(bars.v_tail(), 0)))
-                                return;
+                            if (!I8 && w.tail && j == w.nkt - 1) {
+                                if (!(ok = wait(bars.v_tail(vs), (tailpar >> vs) & 1u)))
+                                    return;
+                                tailpar ^= 1u << vs;
+                            }
                             v_ready = true;
                         }
                         ptx::tc_fence_after();
                         issue_pv(t, vs, j == 0);
+                        if (j + 1 == ntk)
+                            ptx::mma_commit(bars.o_full(t)); // O_t final
                         if (j + 1 < ntk) {
                             if (!k_next) {
-                                if (!(ok = wait(bars.k_full(ksn), kph)))
+                                if (!(ok = wait(bars.k_full(ks), kph)))
                                     return;
                                 ptx::tc_fence_after();
                                 k_next = true;
                             }
-                            issue_s(t, ksn);
+                            issue_s(t, ks);
+                            ptx::mma_commit(bars.s_full(t));
+                            if (j + 2 == ntk)
+                                ptx::mma_commit(bars.q_free(t)); // that was the last read of Q_t
                         }
-                        ptx::mma_commit(bars.s_full(t)); // next scores ready, or the final O
                     };
-                    if (j < nkt0)
-                        step(0, nkt0);
-                    if (ok && j < nkt1)
-                        step(1, nkt1);
-                    if (ok)
-                        ptx::mma_commit(bars.released(j + 1)); // V tile j and K tile j + 1 read
+                    if (j < w.nkt0)
+                        step(0, w.nkt0);
+                    if (ok && j < w.nkt1)
+                        step(1, w.nkt1);
+                    if (!ok)
+                        break;
+                    ptx::mma_commit(bars.released(E + j + 1)); // V tile j and K tile j + 1 read
                     if (++vs == L::kVStages) {
                         vs = 0;
                         vph ^= 1;
                     }
-                    if (++ksn == L::kKStages) {
-                        ksn = 0;
+                    if (k_next && ++ks == L::kKStages) {
+                        ks = 0;
                         kph ^= 1;
                     }
                 }
+                E += w.nkt + 1;
             }
-            __syncwarp();
         }
+        __syncwarp();
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
+        ItemIter items(p.tiles, p.num_items, P);
         if constexpr (!I8)
             ptx::reg_alloc<kSoftmaxRegs>();
         const int t = warp >> 2;                   // query tile of this warpgroup (warps 0-3, 4-7)
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;         // query row of the tile
-        const int tid = (warp & 3) * 32 + lane;    // thread index inside the warpgroup
-        const int npos = t == 0 ? npos0 : npos1;
-        const int ntile = t == 0 ? nkt0 : nkt1;
-        const bool row_valid = r < G * npos;
-        // keys visible to this row; rows that hold no query are never masked (their
-        // output is discarded) so that a warp's rows all take the same path
-        const int limit = row_valid ? off + q0 + t * P + r / G + 1 : 0x3fffffff;
+        const int rpos = r / G, rhead = r % G;     // its position in the tile and head in the group
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const uint32_t s_col = tmem + lane_addr + t * 256;
         const uint32_t o_col = s_col + 128;
         const float sl2 = p.scale_log2;
-        float m_ref = -INFINITY, l_sum = 0.f;
+        uint32_t ns = 0, no = 0; // S tiles and items of this query tile so far (parities)
+        int X0 = 0;              // global index of the current item's key tile 0
         bool ok = true;
-        auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
 
-        for (int j = 0; j < ntile; ++j) {
-            if (!(ok = wwait(bars.s_full(t), j & 1)))
-                break;
-            if constexpr (I8) {
-                if (!(ok = wwait(bars.sc_full(j & 1), (j >> 1) & 1)))
+        while (ok && items.more()) {
+            const Item w = items.next(false);
+            const int ntile = t == 0 ? w.nkt0 : w.nkt1;
+            const int npos = t == 0 ? w.npos0 : w.npos1;
+            const bool row_valid = r < G * npos;
+            // keys visible to this row; rows that hold no query are never masked (their
+            // output is discarded) so that a warp's rows all take the same path
+            const int limit = row_valid ? w.lk - w.lq + w.q0 + t * P + rpos + 1 : 0x3fffffff;
+            float m_ref = -INFINITY, l_sum = 0.f;
+            for (int j = 0; j < ntile; ++j) {
+                if (!(ok = wwait(bars.s_full(t), ns & 1)))
                     break;
-            }
-            ptx::tc_fence_after();
-            const int lim = limit - j * 128; // columns this row sees in this tile
-            // the whole score row in registers: one TMEM round trip per tile
-            uint32_t sr[128];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                ptx::tmem_ld32(s_col + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
-            ptx::tmem_wait_ld();
-            const float *fac = reinterpret_cast<const float *>(sgen + L::kScl + (j & 1) * L::kSclSlot);
-            if constexpr (I8) {
-                // K scale after the dot product: column c times k_scale[c] * scale * log2 e
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const float4 f = reinterpret_cast<const float4 *>(fac)[q];
-                    float a0, a1, a2, a3;
-                    ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(sr[4 * q]), __uint_as_float(sr[4 * q + 1])),
-                                              ptx::f2(f.x, f.y)),
-                                  a0, a1);
-                    ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3])),
-                                              ptx::f2(f.z, f.w)),
-                                  a2, a3);
-                    sr[4 * q] = __float_as_uint(a0);
-                    sr[4 * q + 1] = __float_as_uint(a1);
-                    sr[4 * q + 2] = __float_as_uint(a2);
-                    sr[4 * q + 3] = __float_as_uint(a3);
+                ns ^= 1;
+                const int Xj = X0 + j;
+                if constexpr (I8) {
+                    if (!(ok = wwait(bars.sc_full(Xj & 1), (Xj >> 1) & 1)))
+                        break;
                 }
-            }
-            if (lim < 128) {
+                ptx::tc_fence_after();
+                const int lim = limit - j * 128; // columns this row sees in this tile
+                // the whole score row in registers: one TMEM round trip per tile
+                uint32_t sr[128];
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    sr[c] = c < lim ? sr[c] : __float_as_uint(-INFINITY);
-            }
-            float m8[8];
+                for (int q = 0; q < 4; ++q)
+                    ptx::tmem_ld32(s_col + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
+                ptx::tmem_wait_ld();
+                const float *fac = reinterpret_cast<const float *>(sgen + L::kScl + (Xj & 1) * L::kSclSlot);
+                if constexpr (I8) {
+                    // K scale after the dot product: column c times k_scale[c] * scale * log2 e
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                m8[i] = ptx::max3(__uint_as_float(sr[16 * i]), __uint_as_float(sr[16 * i + 1]),
-                                  __uint_as_float(sr[16 * i + 2]));
-#pragma unroll
-            for (int c = 3; c < 16; c += 2)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    m8[i] = c + 1 < 16 ? ptx::max3(m8[i], __uint_as_float(sr[16 * i + c]), __uint_as_float(sr[16 * i + c + 1]))
-                                       : fmaxf(m8[i], __uint_as_float(sr[16 * i + c]));
-            const float mx = fmaxf(fmaxf(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5])),
-                                   fmaxf(m8[6], m8[7]));
-            const float mt = I8 ? mx : mx * sl2; // INT8: the factors already hold scale * log2 e
-            float alpha = 1.f;
-            bool rescale = false;
-            if (row_valid && (mt > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt != -INFINITY))) {
-                const float m_new = fmaxf(m_ref, mt);
-                alpha = ptx::ex2(m_ref - m_new); // 0 on the first tile
-                rescale = j > 0;
-                l_sum *= alpha;
-                m_ref = m_new;
-            }
-            // P = 2^(s * scale * log2 e - m) as bf16 pairs written over S; row sum
-            const uint64_t sl2x2 = I8 ? ptx::f2(1.f, 1.f) : ptx::f2(sl2, sl2);
-            const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
-            const uint64_t negm2 = ptx::f2(negm, negm);
-            uint64_t sum2[4] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
-            uint4 vs8 = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) { // two halves: P columns 32h..32h+31 hold keys 64h..64h+63
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 64 * h; c < 64 * h + 64; c += 2) {
-                    float x0, x1;
-                    ptx::f2_split(
-                        ptx::f2_fma(ptx::f2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2), x0, x1);
-                    const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1); // masked columns: 2^-inf = 0
-                    sum2[(c >> 1) & 3] = ptx::f2_add(sum2[(c >> 1) & 3], ptx::f2(e0, e1));
-                    if constexpr (I8) { // V scale folded into P; the row sum keeps the unscaled P
-                        if ((c & 7) == 0) // 8 fp16 V scales
-                            vs8 = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(fac) + 512 + 2 * c);
-                        const uint32_t vsw = (c & 7) == 0 ? vs8.x : (c & 7) == 2 ? vs8.y : (c & 7) == 4 ? vs8.z : vs8.w;
-                        pk[(c >> 1) & 31] = ptx::mul_f16x2(ptx::pack_f16(e0, e1), vsw);
-                    } else {
-                        pk[(c >> 1) & 31] = ptx::pack_bf16(e0, e1);
+                    for (int q = 0; q < 32; ++q) {
+                        const float4 f = reinterpret_cast<const float4 *>(fac)[q];
+                        float a0, a1, a2, a3;
+                        ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(sr[4 * q]), __uint_as_float(sr[4 * q + 1])),
+                                                  ptx::f2(f.x, f.y)),
+                                      a0, a1);
+                        ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3])),
+                                                  ptx::f2(f.z, f.w)),
+                                      a2, a3);
+                        sr[4 * q] = __float_as_uint(a0);
+                        sr[4 * q + 1] = __float_as_uint(a1);
+                        sr[4 * q + 2] = __float_as_uint(a2);
+                        sr[4 * q + 3] = __float_as_uint(a3);
                     }
                 }
-                ptx::tmem_st32(s_col + 32 * h, pk);
-            }
-            float s0, s1, s2, s3, s4, s5, s6, s7;
-            ptx::f2_split(sum2[0], s0, s1);
-            ptx::f2_split(sum2[1], s2, s3);
-            ptx::f2_split(sum2[2], s4, s5);
-            ptx::f2_split(sum2[3], s6, s7);
-            l_sum += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
-            // O is stable here: PV(j-1) completed before S(j) did (in-order MMAs), and
-            // PV(j) waits for this thread's p_full arrival below
-            if (__any_sync(0xffffffffu, rescale)) {
+                if (lim < 128) {
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(o_col + cc * 32, o);
-                    ptx::tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    ptx::tmem_st32(o_col + cc * 32, o);
+                    for (int c = 0; c < 128; ++c)
+                        sr[c] = c < lim ? sr[c] : __float_as_uint(-INFINITY);
                 }
+                float m8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    m8[i] = ptx::max3(__uint_as_float(sr[16 * i]), __uint_as_float(sr[16 * i + 1]),
+                                      __uint_as_float(sr[16 * i + 2]));
+#pragma unroll
+                for (int c = 3; c < 16; c += 2)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        m8[i] = c + 1 < 16 ? ptx::max3(m8[i], __uint_as_float(sr[16 * i + c]), __uint_as_float(sr[16 * i + c + 1]))
+                                           : fmaxf(m8[i], __uint_as_float(sr[16 * i + c]));
+                const float mx = fmaxf(fmaxf(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5])),
+                                       fmaxf(m8[6], m8[7]));
+                const float mt = I8 ? mx : mx * sl2; // INT8: the factors already hold scale * log2 e
+                float alpha = 1.f;
+                bool rescale = false;
+                if (row_valid && (mt > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt != -INFINITY))) {
+                    const float m_new = fmaxf(m_ref, mt);
+                    alpha = ptx::ex2(m_ref - m_new); // 0 on the first tile
+                    rescale = j > 0;
+                    l_sum *= alpha;
+                    m_ref = m_new;
+                }
+                // P = 2^(s * scale * log2 e - m) as bf16 pairs written over S; row sum
+                const uint64_t sl2x2 = I8 ? ptx::f2(1.f, 1.f) : ptx::f2(sl2, sl2);
+                const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
+                const uint64_t negm2 = ptx::f2(negm, negm);
+                uint64_t sum2[4] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
+                uint4 vs8 = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) { // two halves: P columns 32h..32h+31 hold keys 64h..64h+63
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 64 * h; c < 64 * h + 64; c += 2) {
+                        float x0, x1;
+                        ptx::f2_split(
+                            ptx::f2_fma(ptx::f2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2), x0, x1);
+                        const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1); // masked columns: 2^-inf = 0
+                        sum2[(c >> 1) & 3] = ptx::f2_add(sum2[(c >> 1) & 3], ptx::f2(e0, e1));
+                        if constexpr (I8) { // V scale folded into P; the row sum keeps the unscaled P
+                            if ((c & 7) == 0) // 8 fp16 V scales
+                                vs8 = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(fac) + 512 + 2 * c);
+                            const uint32_t vsw = (c & 7) == 0 ? vs8.x : (c & 7) == 2 ? vs8.y : (c & 7) == 4 ? vs8.z : vs8.w;
+                            pk[(c >> 1) & 31] = ptx::mul_f16x2(ptx::pack_f16(e0, e1), vsw);
+                        } else {
+                            pk[(c >> 1) & 31] = ptx::pack_bf16(e0, e1);
+                        }
+                    }
+                    ptx::tmem_st32(s_col + 32 * h, pk);
+                }
+                float s0, s1, s2, s3, s4, s5, s6, s7;
+                ptx::f2_split(sum2[0], s0, s1);
+                ptx::f2_split(sum2[1], s2, s3);
+                ptx::f2_split(sum2[2], s4, s5);
+                ptx::f2_split(sum2[3], s6, s7);
+                l_sum += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+                // O is stable here: PV(j-1) completed before S(j) did (in-order MMAs), and
+                // PV(j) waits for this thread's p_full arrival below
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(o_col + cc * 32, o);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        ptx::tmem_st32(o_col + cc * 32, o);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp(); // 128 arrivals on one word serialise: one per warp instead
+                if (lane == 0)
+                    ptx::mbar_arrive(bars.p_full(t));
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            __syncwarp(); // 128 arrivals on one word serialise: one per warp instead
-            if (lane == 0)
-                ptx::mbar_arrive(bars.p_full(t));
-        }
-
-        const bool good = ntile > 0 && ok && wwait(bars.s_full(t), ntile & 1);
-        // epilogue: O / l -> bf16 -> staging (this tile's Q buffer, row pitch 2*D, chunk-swizzled) -> global
-        uint8_t *stg = sgen + L::kQ + t * L::kTileBytes;
-        if (good) {
+            X0 += w.nkt;
+            items.fetch();
+            if (!ok || ntile == 0)
+                continue;
+            // epilogue: O / l -> bf16 -> this row's output, straight from registers.  The
+            // MMAs meanwhile run the next item's score tiles; the next item's first PV
+            // (which overwrites O_t) waits for this warpgroup's next P, issued after these reads.
+            if (!(ok = wwait(bars.o_full(t), no & 1)))
+                break;
+            no ^= 1;
             ptx::tc_fence_after();
             const float inv = (row_valid && l_sum > 0.f) ? 1.f / l_sum : 0.f;
+            __nv_bfloat16 *orow =
+                p.out + ((size_t)(w.cq0 + w.q0 + t * P + rpos) * p.num_heads + (size_t)w.g * G + rhead) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
                 ptx::tmem_ld32(o_col + cc * 32, o);
                 ptx::tmem_wait_ld();
+                if (row_valid && !*abort_flag) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = cc * 4 + c;
-                    uint4 v;
-                    v.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-                    v.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-                    v.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-                    v.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-                    *reinterpret_cast<uint4 *>(stg + r * (2 * D) + ((chunk ^ (r & 7)) << 4)) = v;
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 v;
+                        v.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                        v.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                        v.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                        v.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(orow + cc * 32 + c * 8) = v;
+                    }
                 }
-            }
-        }
-        // every thread of the warpgroup arrives exactly once (named barrier 1 + t)
-        asm volatile("bar.sync %0, 128;" ::"r"(1 + t) : "memory");
-        if (good && !*abort_flag) {
-            constexpr int CPR = D / 8; // 16-byte chunks per row
-            const int nrows = G * npos;
-            for (int idx = tid; idx < nrows * CPR; idx += 128) {
-                const int rr = idx / CPR, c = idx % CPR;
-                const int pos = q0 + t * P + rr / G, hl = rr % G;
-                const size_t token = (size_t)cq0 + pos;
-                uint4 v = *reinterpret_cast<const uint4 *>(stg + rr * (2 * D) + ((c ^ (rr & 7)) << 4));
-                *reinterpret_cast<uint4 *>(p.out + (token * p.num_heads + (size_t)g * G + hl) * D + c * 8) = v;
             }
         }
     }
@@ -907,7 +1046,13 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     p.num_kv_heads = d.num_kv_heads;
     p.k_scale = static_cast<const __half *>(a.k_scale);
     p.v_scale = static_cast<const __half *>(a.v_scale);
-    prefill_kernel<D, I8><<<(unsigned)a.num_tiles, kThreads, L::kSmemBytes, stream>>>(tq, tk, tv, p);
+    p.num_items = a.num_tiles;
+    // persistent: one CTA per SM (shared memory and TMEM admit one), each walking its items
+    int sms = 0;
+    if (int rc2 = sm_count(&sms))
+        return rc2;
+    const int grid = a.num_tiles < sms ? a.num_tiles : sms;
+    prefill_kernel<D, I8><<<(unsigned)grid, kThreads, L::kSmemBytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
