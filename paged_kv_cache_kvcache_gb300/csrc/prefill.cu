@@ -364,6 +364,17 @@ __device__ __forceinline__ void load_query_tile(const CUtensorMap *tm_q, const B
                          w.g * G, w.cq0 + w.q0 + t * P);
 }
 
+// The next item's query tiles into L2, so that their loads (which must wait for
+// the current item's last score MMAs) arrive sooner.
+template <int D, bool I8>
+__device__ __forceinline__ void prefetch_query_tiles(const CUtensorMap *tm_q, const Item &w, int G, int P)
+{
+    using L = PfLayout<D, I8>;
+    for (int t = 0; t < 2; ++t)
+        for (int pp = 0; pp < L::kPanels; ++pp)
+            ptx::tma_prefetch_3d(tm_q, pp * 64, w.g * G, w.cq0 + w.q0 + t * P);
+}
+
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -460,6 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         load_query_tile<D, I8>(&tm_q, bars, sbase, w, t, G, P);
                     __syncwarp();
                 }
+                if (ok && lane == 0 && items.more())
+                    prefetch_query_tiles<D, I8>(&tm_q, items.peek(), G, P);
             }
         } else if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
             // ------------------------------------------------------------ bf16: K and V producers
@@ -722,14 +735,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ok && items.more()) {
                 const Item w = items.next();
                 const uint32_t qpar = w.ord & 1;
-                ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) &&
-                     wait(I8 ? bars.q_ready(1) : bars.q_full(1), qpar) && wait(bars.k_full(ks), kph);
+                ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) && wait(bars.k_full(ks), kph);
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
                 issue_s(0, ks);
                 ptx::mma_commit(bars.s_full(0));
+                // query tile 1 is waited for only now (also when empty: its buffer is
+                // released below, and every load of it must be consumed first)
+                if (!(ok = wait(I8 ? bars.q_ready(1) : bars.q_full(1), qpar)))
+                    break;
                 if (w.nkt1 > 0) {
+                    ptx::tc_fence_after();
                     issue_s(1, ks);
                     ptx::mma_commit(bars.s_full(1));
                 }
@@ -953,21 +970,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = (row_valid && l_sum > 0.f) ? 1.f / l_sum : 0.f;
             __nv_bfloat16 *orow =
                 p.out + ((size_t)(w.cq0 + w.q0 + t * P + rpos) * p.num_heads + (size_t)w.g * G + rhead) * D;
+            // TMEM loads in batches of kBatch 32-column chunks, one wait per batch
+            // (bf16: the whole row at once; the register budget allows it)
+            constexpr int kBatch = I8 ? 1 : D / 32;
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                ptx::tmem_ld32(o_col + cc * 32, o);
+            for (int c0 = 0; c0 < D / 32; c0 += kBatch) {
+                uint32_t o[kBatch][32];
+#pragma unroll
+                for (int cc = 0; cc < kBatch; ++cc)
+                    ptx::tmem_ld32(o_col + (c0 + cc) * 32, o[cc]);
                 ptx::tmem_wait_ld();
                 if (row_valid && !*abort_flag) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 v;
-                        v.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-                        v.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-                        v.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-                        v.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + cc * 32 + c * 8) = v;
-                    }
+                    for (int cc = 0; cc < kBatch; ++cc)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t *x = o[cc] + 8 * c;
+                            uint4 v;
+                            v.x = ptx::pack_bf16(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv);
+                            v.y = ptx::pack_bf16(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
+                            v.z = ptx::pack_bf16(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv);
+                            v.w = ptx::pack_bf16(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv);
+                            *reinterpret_cast<uint4 *>(orow + (c0 + cc) * 32 + c * 8) = v;
+                        }
                 }
             }
         }

@@ -87,6 +87,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
                  : "memory");
 }
 
+// Pull a 3-D box into L2 ahead of its load (innermost coordinate x element size a multiple of 16 bytes).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0), "r"(c1),
+                 "r"(c2)
+                 : "memory");
+}
+
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes % 16 == 0), completing on an mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {

@@ -12,7 +12,7 @@ import torch
 import oracle
 from paged_kv_cache_kvcache_gb300 import pagedattn as pa
 from paged_kv_cache_kvcache_gb300 import workloads
-from tests.harness import assert_close, int8_equal, int8_pools, run_gpu_batch_int8, sample_rows
+from tests.harness import assert_close, dims_of, int8_equal, int8_pools, run_gpu_batch_int8, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +59,28 @@ def test_int8_prefill_random(case):
                               cached=cached)
     (batch, out, ref, _), = _run_both(w)
     assert_close(out, ref, what=f"int8 case {seed}")
+
+
+# Many more work items than SMs: every CTA of the persistent kernel runs several
+# items back to back (code and factor rings, query refills and conversions
+# carried across items).
+MULTI = [  # seed, num_seqs, hq, hkv, d, bs, max_len, cached
+    (521, 160, 4, 4, 128, 16, 512, "random"),
+    (522, 96, 16, 4, 64, 32, 300, "random"),
+    (523, 48, 28, 4, 128, 16, 200, None),
+]
+
+
+@pytest.mark.parametrize("case", MULTI, ids=[str(c[0]) for c in MULTI])
+def test_int8_prefill_many_items_per_cta(case):
+    seed, B, hq, hkv, d, bs, max_len, cached = case
+    w = workloads.random_case(seed, num_seqs=B, hq=hq, hkv=hkv, d=d, bs=bs, max_len=max_len, device="cuda",
+                              cached=cached)
+    b = w.batches[0]
+    items = pa.pa_pack_prefill(dims_of(w, b), b.seq_lens, b.query_lens, b.block_lists, pin=False).meta.num_tiles
+    assert items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    (batch, out, ref, _), = _run_both(w)
+    assert_close(out, ref, what=f"int8 case {seed}, {items} items")
 
 
 def test_int8_prefill_edge_lengths():

@@ -56,6 +56,28 @@ def test_prefill_random(case):
     assert_close(out, ref, what=f"case {seed}")
 
 
+# Many more work items than SMs: every CTA of the persistent kernel runs several
+# items back to back (rings, barrier phases, tail zeroing and query refills
+# carried across items; empty second query tiles; prefix and no-prefix items).
+MULTI = [  # seed, num_seqs, hq, hkv, d, bs, max_len, cached
+    (121, 160, 4, 4, 128, 16, 512, "random"),
+    (122, 96, 16, 4, 64, 32, 300, "random"),
+    (123, 48, 28, 4, 128, 16, 200, None),
+]
+
+
+@pytest.mark.parametrize("case", MULTI, ids=[str(c[0]) for c in MULTI])
+def test_prefill_many_items_per_cta(case):
+    seed, B, hq, hkv, d, bs, max_len, cached = case
+    w = workloads.random_case(seed, num_seqs=B, hq=hq, hkv=hkv, d=d, bs=bs, max_len=max_len, device="cuda",
+                              cached=cached)
+    b = w.batches[0]
+    items = pa.pa_pack_prefill(dims_of(w, b), b.seq_lens, b.query_lens, b.block_lists, pin=False).meta.num_tiles
+    assert items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    batch, out, ref = _run_both(w, 0)
+    assert_close(out, ref, what=f"case {seed}, {items} items")
+
+
 def test_prefill_edge_lengths():
     """Sequences with no new tokens, single-token sequences and a 1-of-N suffix in one batch."""
     hq, hkv, d, bs = 4, 2, 64, 16
