@@ -62,8 +62,10 @@ def parse():
     ap.add_argument("--kv", choices=["bf16", "int8"], default="bf16",
                     help="cache format: bf16, or int8 codes + fp16 scales (quantising store, fused-dequant "
                          "prefill and decode)")
-    ap.add_argument("--decode-path", choices=["store+decode", "fused"], default="store+decode",
-                    help="fused: store and decode in one launch (pa_decode_fused / pa_decode_int8_fused)")
+    ap.add_argument("--decode-path", choices=["store+decode", "fused", "mixed"], default="store+decode",
+                    help="fused: store and decode in one launch (pa_decode_fused / pa_decode_int8_fused); "
+                         "mixed (bf16): the decode rows join the prefill rows as Lq = 1 varlen rows of one "
+                         "pa_prefill_varlen launch over one pool, timed against the separate launches")
     return ap.parse_args()
 
 
@@ -128,14 +130,31 @@ def store_bytes(batch) -> float:
     return 2.0 * 2 * batch.k.numel() * 2  # K and V, read + write
 
 
+def mixed_batch(wp, wd):
+    """One pool (prefill blocks, then decode blocks) and one varlen batch: the prefill
+    sequences followed by the decode sequences as query-length-1 rows."""
+    from paged_kv_cache_kvcache_gb300 import workloads
+    bp, bd, pp, pd = wp.batches[0], wd.batches[0], wp.pool, wd.pool
+    assert (pp.block_size, pp.num_kv_heads, pp.head_dim, bp.num_heads) == \
+        (pd.block_size, pd.num_kv_heads, pd.head_dim, bd.num_heads), "mixed: the two phases need one cache shape"
+    kc = torch.cat([pp.k_cache, pd.k_cache])
+    vc = torch.cat([pp.v_cache, pd.v_cache])
+    lists = list(bp.block_lists) + [np.asarray(b, np.int32) + pp.num_blocks for b in bd.block_lists]
+    b = workloads.Batch("prefill", np.concatenate([bp.seq_lens, bd.seq_lens]).astype(np.int32),
+                        np.concatenate([bp.query_lens, np.ones(len(bd.seq_lens), np.int32)]).astype(np.int32),
+                        lists, torch.cat([bp.q, bd.q]), torch.cat([bp.k, bd.k]), torch.cat([bp.v, bd.v]),
+                        bp.num_heads, bp.scale)
+    return kc, vc, b
+
+
 class Step:
     """Device-resident state of one replica and the calls of one step."""
 
-    def __init__(self, wp, wd, stream, kv="bf16", fused=False):
+    def __init__(self, wp, wd, stream, kv="bf16", fused=False, mixed=False):
         from paged_kv_cache_kvcache_gb300 import pagedattn as pa
         self.pa = pa
         self.s = stream
-        self.int8, self.fused = kv == "int8", fused
+        self.int8, self.fused, self.mixed = kv == "int8", fused, mixed
         self.wp, self.wd = wp, wd
         self.bp, self.bd = wp.batches[0], wd.batches[0]
         pp, pd = wp.pool, wd.pool
@@ -158,6 +177,15 @@ class Step:
         self.ws = pa.decode_workspace(self.plans_d[0])
         self.i = 0
         self.launches_per_step = 4 + (1 if self.plans_d[0].meta.num_partials > 0 else 0) - (1 if fused else 0)
+        if mixed:  # one launch for both phases' rows, over one pool
+            self.kc_m, self.vc_m, self.bm = mixed_batch(wp, wd)
+            self.dims_m = pa.make_dims(self.kc_m.shape[0], pp.block_size, self.bm.num_heads, pp.num_kv_heads,
+                                       pp.head_dim)
+            self.blocks_m = pa._flatten(self.bm.block_lists)
+            self.out_m = torch.empty_like(self.bm.q)
+            self.plans_m = [pa.pa_pack_prefill(self.dims_m, self.bm.seq_lens, self.bm.query_lens, self.blocks_m)
+                            .upload(stream=stream) for _ in range(2)]
+            self.launches_per_step = 2
         if self.int8:  # INT8 caches: the bf16 pools quantised once, every slot, by the library's store
             self.c8_p = self._quantised(self.dims_p, pp)
             self.c8_d = self._quantised(self.dims_d, pd)
@@ -182,6 +210,18 @@ class Step:
         rec = (lambda name: ev[name].record(s)) if ev is not None else (lambda name: None)
         # ---- prefill phase
         rec("p0")
+        if self.mixed:  # both phases' rows: one store, one prefill launch; the decode phase stays empty
+            plan_m = pa.pa_pack_prefill(self.dims_m, self.bm.seq_lens, self.bm.query_lens, self.blocks_m,
+                                        into=self.plans_m[k]).upload(stream=s)
+            self.up_ev[k].record(s)
+            pa.pa_store_kvcache(self.dims_m, self.bm.k, self.bm.v, self.kc_m, self.vc_m, plan_m.slot_mapping,
+                                self.bm.num_tokens, stream=s)
+            rec("pk0")
+            pa.pa_prefill_varlen(self.dims_m, self.bm.q, self.kc_m, self.vc_m, plan_m, self.bm.scale, self.out_m,
+                                 stream=s)
+            for n in ("pk1", "p1", "dk0", "dk1", "d1"):
+                rec(n)
+            return
         if phase == "decode":
             for n in ("pk0", "pk1", "p1"):
                 rec(n)
@@ -354,6 +394,8 @@ def oracle_decode_sample(wd, nseq, threads=0):
 def main():
     args = parse()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+    assert args.decode_path != "mixed" or (args.kv == "bf16" and args.phase == "both"), \
+        "--decode-path mixed runs the bf16 cache, both phases"
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -369,7 +411,8 @@ def main():
     stream = torch.cuda.Stream()
     clocks = Clocks(local, enabled=not args.no_clocks)
     with torch.cuda.stream(stream):
-        step = Step(wp, wd, stream, kv=args.kv, fused=args.decode_path == "fused")
+        step = Step(wp, wd, stream, kv=args.kv, fused=args.decode_path == "fused",
+                    mixed=args.decode_path == "mixed")
         names = ["p0", "pk0", "pk1", "p1", "dk0", "dk1", "d1"]
         for _ in range(args.warmup):
             step.run(phase=args.phase)
@@ -397,8 +440,22 @@ def main():
         t_decode_kernel = statistics.mean(ph("dk0", "dk1"))
 
         # e2e: the same step through the public API with host (pinned) inputs/outputs
+        # mixed: the same rows as separate prefill and decode launches, timed the same way
+        separate = None
+        if args.decode_path == "mixed":
+            ref_step = Step(wp, wd, stream)
+            for _ in range(args.warmup):
+                ref_step.run()
+            evs3 = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(args.steps)]
+            for i in range(args.steps):
+                ref_step.run(evs3[i])
+            torch.cuda.synchronize()
+            ph3 = lambda a, b: statistics.mean([e[a].elapsed_time(e[b]) for e in evs3])
+            separate = {"prefill_kernel_ms": round(ph3("pk0", "pk1"), 5), "decode_kernels_ms": round(ph3("dk0", "dk1"), 5),
+                        "step_ms": round(ph3("p0", "d1"), 5)}
+
         e2e = None
-        if not args.no_e2e and args.phase == "both":
+        if not args.no_e2e and args.phase == "both" and args.decode_path != "mixed":
             host = {"pq": step.bp.q.cpu().pin_memory(), "pk": step.bp.k.cpu().pin_memory(),
                     "pv": step.bp.v.cpu().pin_memory(), "dq": step.bd.q.cpu().pin_memory(),
                     "dk": step.bd.k.cpu().pin_memory(), "dv": step.bd.v.cpu().pin_memory(),
@@ -428,6 +485,10 @@ def main():
     eps = 1e-9  # a phase left out with --phase times as ~0
     value = flops / (max(t_prefill_phase, eps) * 1e-3) / 1e12 * world
     decode_gbs = dbytes / (max(t_decode_phase, eps) * 1e-3) / 1e9 * world
+    if args.decode_path == "mixed":  # one phase holds both: rates over that phase
+        flops = prefill_flops(step.bm)
+        value = flops / (t_prefill_phase * 1e-3) / 1e12 * world
+        decode_gbs = dbytes / (t_prefill_phase * 1e-3) / 1e9 * world
     pk_tflops = flops / (max(t_prefill_kernel, eps) * 1e-3) / 1e12
     dk_gbs = dbytes / (max(t_decode_kernel, eps) * 1e-3) / 1e9
     t_decode_phase = max(t_decode_phase, eps)
@@ -435,7 +496,8 @@ def main():
     bf16_peak = float(peaks["bf16_tflops"])
     hbm_peak = float(peaks["hbm_gbs"])
     int8 = args.kv == "int8"
-    traffic = {} if args.decode_path == "fused" else (NCU_TRAFFIC_INT8 if int8 else NCU_TRAFFIC).get(args.workload, {})
+    traffic = {} if args.decode_path in ("fused", "mixed") else \
+        (NCU_TRAFFIC_INT8 if int8 else NCU_TRAFFIC).get(args.workload, {})
     roof_p = {"kernel": ("pa_prefill_varlen_int8 (prefill_kernel<128,true>, f16 MMAs)" if int8 else
                          "pa_prefill_varlen (prefill_kernel<128,false>)"),
               "bound": "tensor", "achieved": round(pk_tflops, 2),
@@ -454,6 +516,24 @@ def main():
               "traffic": traffic.get("decode") if args.decode_seqs == 64 else None,
               "work_per_launch": dbytes, "ms_per_launch": round(t_decode_kernel, 5)}
     dominant = roof_p if t_prefill_kernel >= t_decode_kernel else roof_d
+    rooflines = [roof_p, roof_d]
+    mixed = None
+    if args.decode_path == "mixed":
+        # One launch holds compute-bound prefill rows and bandwidth-bound decode rows: its
+        # lower bound is the prefill rows' FLOPs at the tensor peak plus the decode rows'
+        # K/V bytes at the copy peak.  The roofline entry counts the decode bytes (the larger part).
+        pf = prefill_flops(step.bp)
+        t_low = (pf / (bf16_peak * 1e12) + dbytes / (hbm_peak * 1e9)) * 1e3
+        gbs = dbytes / (t_prefill_kernel * 1e-3) / 1e9
+        roof_p = {"kernel": "pa_prefill_varlen (prefill_kernel<128,false>), prefill + decode rows", "bound": "hbm",
+                  "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
+                  "peak_source": f"{peak_src} hbm_gbs", "traffic": None, "work_per_launch": dbytes,
+                  "ms_per_launch": round(t_prefill_kernel, 5)}
+        dominant, rooflines = roof_p, [roof_p]
+        mixed = {"kernel_ms": round(t_prefill_kernel, 5), "phase_ms": round(t_prefill_phase, 5),
+                 "rows": {"prefill_tokens": int(step.bp.num_tokens), "decode_rows": int(step.bd.num_seqs)},
+                 "lower_bound_ms": round(t_low, 5), "frac_of_lower_bound": round(t_low / t_prefill_kernel, 4),
+                 "separate": separate}
 
     cpu = None
     # the CPU leg times the bf16 oracle on the default path only
@@ -467,6 +547,13 @@ def main():
                "sample": f"prefill: the whole 4x4096 batch ({fl / 1e9:.1f} GFLOP, {dt_p:.1f} s); "
                          f"decode: 16 of 64 sequences ({kvb / 1e9:.2f} GB K/V, {dt_d:.1f} s)",
                "decode": {"value": round(kvb / dt_d / 1e9, 3), "unit": "GB/s"}}
+        # one host thread, on smaller samples (every 64th prefill row, 2 decode sequences)
+        dt_p1, fl1 = oracle_prefill_sample(wp, row_stride=64, threads=1)
+        dt_d1, kvb1 = oracle_decode_sample(wd, nseq=2, threads=1)
+        cpu["single_thread"] = {"value": round(fl1 / dt_p1 / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+                                "sample": f"prefill: every 64th query row ({fl1 / 1e9:.1f} GFLOP, {dt_p1:.1f} s); "
+                                          f"decode: 2 sequences ({kvb1 / 1e9:.2f} GB K/V, {dt_d1:.1f} s)",
+                                "decode": {"value": round(kvb1 / dt_d1 / 1e9, 3), "unit": "GB/s"}}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -482,10 +569,12 @@ def main():
                     "frac_of_bf16": round(value / world / bf16_peak, 4)},
         "phase_ms": {"prefill_phase": round(t_prefill_phase, 5), "prefill_kernel": round(t_prefill_kernel, 5),
                      "decode_phase": round(t_decode_phase, 5), "decode_kernels": round(t_decode_kernel, 5)},
-        "roofline": dominant, "rooflines": [roof_p, roof_d],
+        "roofline": dominant, "rooflines": rooflines,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": step.launches_per_step * args.steps,
         "clocks": clk, "peaks": peak_src,
     }
+    if mixed is not None:
+        line["mixed"] = mixed
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

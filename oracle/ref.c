@@ -309,8 +309,8 @@ static int64_t attention_impl(const uint16_t *q, const void *k_cache, const void
                               const uint8_t *row_select, double *out, int num_threads)
 {
 #ifdef _OPENMP
-    if (num_threads > 0)
-        omp_set_num_threads(num_threads);
+    /* thread count of this call only (0: the OpenMP default) */
+    const int nthreads = num_threads > 0 ? num_threads : omp_get_max_threads();
 #else
     (void)num_threads;
 #endif
@@ -358,7 +358,7 @@ static int64_t attention_impl(const uint16_t *q, const void *k_cache, const void
         /* step 2: causal softmax(q K^T * scale) V for each (row, head) */
         int64_t work = (int64_t)lq * num_heads;
         int64_t seq_pairs = 0;
-#pragma omp parallel for schedule(dynamic, 4) reduction(+ : seq_pairs)
+#pragma omp parallel for schedule(dynamic, 4) reduction(+ : seq_pairs) num_threads(nthreads)
         for (int64_t w = 0; w < work; ++w) {
             int i = (int)(w / num_heads), h = (int)(w % num_heads);
             int64_t t = q_begin + i;
