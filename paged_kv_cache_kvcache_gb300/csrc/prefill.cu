@@ -137,6 +137,7 @@ struct PfLayout {
 
 struct PfParams {
     int32_t num_items;     // entries of `tiles` (the CTAs walk them persistently)
+    int32_t out_v8;        // out is 32-byte aligned: the epilogue stores 32 bytes per instruction
     const int32_t *cu_seqlens_q;
     const int32_t *cu_seqlens_k;
     const int32_t *block_tables;
@@ -235,11 +236,12 @@ struct ItemIter {
             fetch();
         return w;
     }
+    // issued where it stands, so that its latency hides behind the current item
     __device__ void fetch()
     {
         if (idx < n) {
-            a0 = __ldg(tiles + 2 * idx);
-            a1 = __ldg(tiles + 2 * idx + 1);
+            a0 = ptx::ld_nc_v4_now(tiles + 2 * idx);
+            a1 = ptx::ld_nc_v4_now(tiles + 2 * idx + 1);
         }
     }
     // the item next() returns next (valid while more())
@@ -984,14 +986,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int cc = 0; cc < kBatch; ++cc)
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t *x = o[cc] + 8 * c;
-                            uint4 v;
-                            v.x = ptx::pack_bf16(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv);
-                            v.y = ptx::pack_bf16(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv);
-                            v.z = ptx::pack_bf16(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv);
-                            v.w = ptx::pack_bf16(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv);
-                            *reinterpret_cast<uint4 *>(orow + (c0 + cc) * 32 + c * 8) = v;
+                        for (int c = 0; c < 2; ++c) {
+                            const uint32_t *x = o[cc] + 16 * c;
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                w[i] = ptx::pack_bf16(__uint_as_float(x[2 * i]) * inv, __uint_as_float(x[2 * i + 1]) * inv);
+                            __nv_bfloat16 *dst = orow + (c0 + cc) * 32 + c * 16;
+                            // 32-byte stores when out allows (rows are 128 or 256 bytes, so each
+                            // row keeps the base's alignment): each thread writes whole sectors,
+                            // half the store instructions in the memory pipeline the MMA
+                            // thread's barrier polls share
+                            if (p.out_v8) {
+                                ptx::st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                            } else {
+                                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                                reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                            }
                         }
                 }
             }
@@ -1072,6 +1083,7 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     p.k_scale = static_cast<const __half *>(a.k_scale);
     p.v_scale = static_cast<const __half *>(a.v_scale);
     p.num_items = a.num_tiles;
+    p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
     // persistent: one CTA per SM (shared memory and TMEM admit one), each walking its items
     int sms = 0;
     if (int rc2 = sm_count(&sms))

@@ -87,6 +87,27 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
                  : "memory");
 }
 
+// 16-byte read-only global load issued exactly here (an asm volatile the
+// compiler neither sinks towards its first use nor merges): for prefetching a
+// value needed much later.
+__device__ __forceinline__ int4 ld_nc_v4_now(const int4 *p)
+{
+    int4 v;
+    asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 32-byte global store (address 32-byte aligned): one whole sector per thread.
+__device__ __forceinline__ void st_global_v8(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                             uint32_t f, uint32_t g, uint32_t h)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+                 "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
+}
+
 // Pull a 3-D box into L2 ahead of its load (innermost coordinate x element size a multiple of 16 bytes).
 __device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2)
 {

@@ -78,6 +78,27 @@ def test_prefill_many_items_per_cta(case):
     assert_close(out, ref, what=f"case {seed}, {items} items")
 
 
+def test_prefill_output_alignment_16_and_32_bytes():
+    """An output 16 but not 32 bytes aligned (allowed) gives the same bits as an aligned one."""
+    w = workloads.random_case(131, num_seqs=40, hq=8, hkv=2, d=128, bs=16, max_len=400, device="cuda")
+    b = w.batches[0]
+    dims = dims_of(w, b)
+    kc, vc = w.pool.k_cache.clone(), w.pool.v_cache.clone()
+    plan = pa.pa_pack_prefill(dims, b.seq_lens, b.query_lens, b.block_lists).upload("cuda")
+    q, k, v = b.q.cuda(), b.k.cuda(), b.v.cuda()
+    pa.pa_store_kvcache(dims, k, v, kc, vc, plan.slot_mapping, b.num_tokens)
+    out32 = torch.empty_like(q)
+    assert out32.data_ptr() % 32 == 0
+    buf = torch.empty(q.numel() + 8, dtype=q.dtype, device="cuda")
+    out16 = buf[8:].view(q.shape)  # 16 bytes past a 32-byte boundary
+    assert out16.data_ptr() % 32 == 16
+    pa.pa_prefill_varlen(dims, q, kc, vc, plan, b.scale, out32)
+    pa.pa_prefill_varlen(dims, q, kc, vc, plan, b.scale, out16)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    assert np.array_equal(bits(out32), bits(out16))
+
+
 def test_prefill_edge_lengths():
     """Sequences with no new tokens, single-token sequences and a 1-of-N suffix in one batch."""
     hq, hkv, d, bs = 4, 2, 64, 16
