@@ -79,8 +79,14 @@ namespace {
 // One thread issues the MMAs of both query tiles: its in-order stream keeps the
 // two tiles half a key tile apart, so one tile's softmax always runs under the
 // other's MMAs.
-constexpr int kThreads = 384;
-constexpr int kLaunchRegs = 168; // 65536 / 384, rounded down to the allocation unit of 8
+// threads per CTA and registers per thread the launch grants (65536 / threads,
+// rounded down to the allocation unit of 8): 12 warps (bf16) or 16 (INT8: warps
+// 12-15 convert the code tiles, one warp per SM sub-partition)
+template <bool I8>
+constexpr int kThreadsOf = I8 ? 512 : 384;
+template <bool I8>
+constexpr int kLaunchRegsOf = I8 ? 128 : 168;
+constexpr int kConvWarp0 = 12;
 constexpr int kKProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10, kLoaderWarp = 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -283,11 +289,12 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u, uint32_t sel)
     return ptx::sub_f16x2(ptx::prmt(u, 0x64646464u, sel), kMagic);
 }
 
-// Raw int8 code rows of a staged key tile -> f16 codes (exact, |code| <= 127)
-// in the 128B-swizzled layout the MMAs read (panels of 64 elements x 128
-// rows, the layout TMA gives the bf16 tiles).  One warp; D/16 lanes per row.
+// Raw int8 code rows r0 .. r0+31 of a staged key tile -> f16 codes (exact,
+// |code| <= 127) in the 128B-swizzled layout the MMAs read (panels of 64
+// elements x 128 rows, the layout TMA gives the bf16 tiles).  One warp; D/16
+// lanes per row.
 template <int D, bool kInPlace>
-__device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int lane)
+__device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int lane, int r0)
 {
     constexpr int LPR = D / 16;   // lanes per row, 16 codes each
     constexpr int RPP = 32 / LPR; // rows per pass
@@ -296,7 +303,7 @@ __device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int
     const int c0 = (l & 3) * 2;   // first of the lane's two 16-byte chunks
     const int h0 = panel & 1;     // second-panel lanes store their chunks in the other order (no bank conflict)
 #pragma unroll 2
-    for (int t = sub; t < 128; t += RPP) {
+    for (int t = r0 + sub; t < r0 + 32; t += RPP) {
         const uint4 w = ptx::lds_v4(codes + t * D + 16 * l);
         if constexpr (kInPlace)
             __syncwarp(); // row t's codes are read before its second panel is written over them
@@ -378,14 +385,17 @@ __device__ __forceinline__ void prefetch_query_tiles(const CUtensorMap *tm_q, co
 }
 
 template <int D, bool I8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsOf<I8>, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PfParams p)
 {
     using L = PfLayout<D, I8>;
     // per-thread register budgets after the hand-over (bf16 variant)
-    constexpr int kSoftmaxRegs = 216, kOtherRegs = 72;
-    static_assert(128 * (2 * kSoftmaxRegs + kOtherRegs) == kThreads * kLaunchRegs, "register hand-over");
+    // (INT8: the converter warpgroup keeps kConvRegs)
+    constexpr int kSoftmaxRegs = I8 ? 176 : 216, kOtherRegs = 72, kConvRegs = 88;
+    static_assert(128 * (2 * kSoftmaxRegs + kOtherRegs + (I8 ? kConvRegs : 0)) ==
+                      kThreadsOf<I8> * kLaunchRegsOf<I8>,
+                  "register hand-over");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -408,9 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bars.o_full(t), 1);
         }
         for (int s = 0; s < L::kKStages; ++s)
-            ptx::mbar_init(bars.k_full(s), 1);
+            ptx::mbar_init(bars.k_full(s), I8 ? 4 : 1); // INT8: one arrival per converter warp
         for (int s = 0; s < L::kVStages; ++s) {
-            ptx::mbar_init(bars.v_full(s), 1);
+            ptx::mbar_init(bars.v_full(s), I8 ? 4 : 1);
             ptx::mbar_init(bars.v_tail(s), 1);
         }
         for (int s = 0; s < kIterRing; ++s)
@@ -438,13 +448,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kTmemSlotOffset);
     auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
 
-    if (warp >= 8) {
-        // bf16: warps 8-11 (copies, MMA issue) need fewer registers and hand part
-        // of their 168 to the softmax warpgroups (128 x (2 kSoftmaxRegs +
-        // kOtherRegs) = 384 x 168, the launch's registers).  The INT8 converters
-        // run faster keeping theirs.
-        if constexpr (!I8)
-            ptx::reg_dealloc<kOtherRegs>();
+    if (I8 && warp >= kConvWarp0) {
+        // ---------------------------------------------------------------- INT8: code converters
+        // warp 12 + i turns rows 32i .. 32i+31 of every K and V code tile into exact
+        // f16 codes: the conversion is spread over all four SM sub-partitions, so it
+        // slows each softmax warp alike.  The scales are applied after the products
+        // (softmax), not to the tiles.
+        ptx::reg_dealloc<kConvRegs>();
+        ItemIter items(p.tiles, p.num_items, P);
+        const int r0 = 32 * (warp - kConvWarp0);
+        int X = 0;
+        bool ok = true;
+        while (ok && items.more()) {
+            const Item w = items.next();
+            for (int j = 0; j < w.nkt; ++j, ++X) {
+                const int sk = X % L::kKStages;
+                if (!(ok = wwait(bars.k_load(sk), (X / L::kKStages) & 1)))
+                    break;
+                convert_codes<D, L::kInPlace>(sbase + L::k_codes(sk), sbase + L::kK + sk * L::kTileBytes, lane, r0);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bars.k_full(sk));
+                const int sv = X % L::kVStages;
+                if (!(ok = wwait(bars.v_load(sv), (X / L::kVStages) & 1)))
+                    break;
+                convert_codes<D, L::kInPlace>(sbase + L::v_codes(sv), sbase + L::kV + sv * L::kTileBytes, lane, r0);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bars.v_full(sv)); // codes are finite and weights past the end 0: nothing to zero
+            }
+        }
+    } else if (warp >= 8) {
+        // warps 8-11 (copies, MMA issue; INT8 also Q conversion and factors) need
+        // fewer registers and hand part of theirs to the softmax warpgroups (128 x
+        // (2 kSoftmaxRegs + kOtherRegs [+ kConvRegs]) = the launch's registers)
+        ptx::reg_dealloc<kOtherRegs>();
         const int bs = p.block_size;
         const int box_rows = bs < 128 ? bs : 128;
         const int nsub = 128 / box_rows;
@@ -587,11 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
-            // ------------------------------------------------------------ INT8: converters
+            // ------------------------------------------------------------ INT8: Q conversion, factors
             ItemIter items(p.tiles, p.num_items, P);
-            // warp 8: query tile 0 and every K tile; warp 10: query tile 1, every V
-            // tile and the per-key factors.  Codes become exact f16 values; the scales
-            // are applied after the products (softmax), not to the tiles.
+            // warp 8: query tile 0; warp 10: query tile 1 and the per-key factors
             const bool is_k = warp == kKProducerWarp;
             const int tq = is_k ? 0 : 1;
             auto convert_q = [&](const Item &w) -> bool {
@@ -607,22 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int X = 0;
             if (is_k) {
-                while (ok && items.more()) {
-                    const Item w = items.next();
-                    if (!(ok = convert_q(w)))
-                        break;
-                    for (int j = 0; j < w.nkt; ++j, ++X) {
-                        const int st = X % L::kKStages;
-                        if (!(ok = wwait(bars.k_load(st), (X / L::kKStages) & 1)))
-                            break;
-                        convert_codes<D, L::kInPlace>(sbase + L::k_codes(st), sbase + L::kK + st * L::kTileBytes,
-                                                      lane);
-                        ptx::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0)
-                            ptx::mbar_arrive(bars.k_full(st));
-                    }
-                }
+                while (ok && items.more())
+                    ok = convert_q(items.next());
             } else if (items.more()) {
                 // factors of key tile j, keys 4*lane .. 4*lane+3 (one block: bs >= 16)
                 const int Hkv = p.num_kv_heads;
@@ -672,20 +696,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0)
                             ptx::mbar_arrive(bars.sc_full(X & 1));
                     }
-                    // the next tile's factors (perhaps the next item's first) while V converts
+                    // the next tile's factors (perhaps the next item's first)
                     const bool last = j + 1 == w.nkt;
                     if (!last)
                         fetch(w, j + 1, kr, vr);
                     else if (items.more())
                         fetch(items.peek(), 0, kr, vr);
-                    const int st = X % L::kVStages;
-                    if (!(ok = wwait(bars.v_load(st), (X / L::kVStages) & 1)))
-                        break;
-                    convert_codes<D, L::kInPlace>(sbase + L::v_codes(st), sbase + L::kV + st * L::kTileBytes, lane);
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(bars.v_full(st)); // codes are finite and weights past the end 0: nothing to zero
                     if (!last) {
                         ++j;
                     } else {
@@ -818,8 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------------------------------------------------------- softmax + epilogue
         ItemIter items(p.tiles, p.num_items, P);
-        if constexpr (!I8)
-            ptx::reg_alloc<kSoftmaxRegs>();
+        ptx::reg_alloc<kSoftmaxRegs>();
         const int t = warp >> 2;                   // query tile of this warpgroup (warps 0-3, 4-7)
         const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
         const int r = quarter * 32 + lane;         // query row of the tile
@@ -1023,8 +1038,8 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     using L = PfLayout<D, I8>;
     if (int rc = ensure_smem<prefill_kernel<D, I8>>(L::kSmemBytes, "prefill"))
         return rc;
-    // The register hand-over inside the kernel assumes kLaunchRegs per thread at
-    // launch; with fewer the softmax warpgroups' request could never be granted.
+    // The register hand-over inside the kernel assumes kLaunchRegsOf<I8> per thread
+    // at launch; with fewer the softmax warpgroups' request could never be granted.
     static std::atomic<int> launch_regs{0};
     int nreg = launch_regs.load(std::memory_order_acquire);
     if (nreg == 0) {
@@ -1034,9 +1049,9 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
             return fail(PA_ERR_CUDA, "prefill kernel attributes: %s", cudaGetErrorString(e));
         launch_regs.store(nreg = fa.numRegs, std::memory_order_release);
     }
-    if (nreg != kLaunchRegs)
+    if (nreg != kLaunchRegsOf<I8>)
         return fail(PA_ERR_UNSUPPORTED, "prefill kernel built with %d registers per thread, needs %d", nreg,
-                    kLaunchRegs);
+                    kLaunchRegsOf<I8>);
     const pa_dims &d = a.dims;
     const int G = d.num_heads / d.num_kv_heads;
     const uint64_t rows = (uint64_t)d.num_blocks * d.block_size;
@@ -1089,7 +1104,7 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     if (int rc2 = sm_count(&sms))
         return rc2;
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-    prefill_kernel<D, I8><<<(unsigned)grid, kThreads, L::kSmemBytes, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D, I8><<<(unsigned)grid, kThreadsOf<I8>, L::kSmemBytes, stream>>>(tq, tk, tv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
