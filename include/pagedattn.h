@@ -316,7 +316,9 @@ int pa_decode_int8(const pa_dims *dims, const void *q, const void *k_cache, cons
  * softmax weights (the normaliser keeps the unscaled weights); no floating
  * copy of the cache is materialised.  Internally the codes (exact in fp16),
  * q (rounded to fp16, saturating at +-65504) and the scaled weights feed
- * fp16 tensor-core products with fp32 accumulation.
+ * fp16 tensor-core products with fp32 accumulation.  PA_ERR_UNSUPPORTED, before
+ * any launch, if the library's INT8 prefill kernel was compiled with other
+ * than 128 registers per thread (its 16 warps re-divide exactly that many).
  */
 int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
                            const void *k_scale, const void *v_scale, const int32_t *cu_seqlens_q,

@@ -48,10 +48,12 @@
 //    epilogue (once the item's last PV is complete) O / l -> bf16 -> each
 //    thread's own output row, straight from registers.
 //  * INT8 cache (prefill_kernel<D, true>; "面试问答准备: nano-vLLM 推理引擎优化",
-//    Q3 and its follow-up on where the scales go): warp 11 issues every TMA
-//    load, raw code tiles land next to (D = 128: inside) the tiles they are
-//    converted into, warps 8 and 10 turn codes into exact f16 values and Q
-//    into f16, the MMAs run kind::f16, and the softmax applies the key scale
+//    Q3 and its follow-up on where the scales go): 16 warps; warp 11 issues
+//    every TMA load, raw code tiles land next to (D = 128: inside) the tiles
+//    they are converted into, warps 12-15 (one per SM sub-partition) turn a
+//    quarter of the rows of every code tile each into exact f16 values, warps
+//    8 and 10 turn Q into f16 and stage the per-key factors, the MMAs run
+//    kind::f16, and the softmax applies the key scale
 //    to each score column after the dot product and folds the value scale
 //    into P, keeping the unscaled P for the row sum.
 //  * mbarriers order every hand-off; every wait is bounded and reports a
@@ -72,10 +74,12 @@ __device__ uint32_t g_prefill_error; // bit 0: a bounded wait timed out
 namespace {
 
 // warps 0-7: softmax (two warpgroups), 8: K TMA producer, 9: MMA issuer (and
-// TMEM owner), 10: V TMA producer, 11: Q TMA producer (INT8: 8 and 10 convert,
-// 11 loads everything).  Registers are granted per 4 warps, so the CTA is sized
-// at 12 warps, 168 registers each at launch; the bf16 variant then moves part
-// of warps 8-11's share to the softmax warpgroups: 216 there, 72 in warps 8-11.
+// TMEM owner), 10: V TMA producer, 11: Q TMA producer (INT8: 11 loads
+// everything, 8 and 10 convert Q and stage factors, 12-15 convert the code
+// tiles).  Registers are granted per 4 warps: 168 per thread at launch for the
+// 12-warp bf16 CTA, 128 for the 16-warp INT8 one; setmaxnreg then moves part of
+// the other warpgroups' share to the softmax warpgroups (bf16: 216 softmax, 72
+// in warps 8-11; INT8: 192 softmax, 64 in warps 8-11 and 64 in 12-15).
 // One thread issues the MMAs of both query tiles: its in-order stream keeps the
 // two tiles half a key tile apart, so one tile's softmax always runs under the
 // other's MMAs.
@@ -302,7 +306,7 @@ __device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int
     const int panel = l >> 2;     // 4 lanes cover one 64-element panel row
     const int c0 = (l & 3) * 2;   // first of the lane's two 16-byte chunks
     const int h0 = panel & 1;     // second-panel lanes store their chunks in the other order (no bank conflict)
-#pragma unroll 2
+#pragma unroll
     for (int t = r0 + sub; t < r0 + 32; t += RPP) {
         const uint4 w = ptx::lds_v4(codes + t * D + 16 * l);
         if constexpr (kInPlace)
@@ -392,7 +396,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
     using L = PfLayout<D, I8>;
     // per-thread register budgets after the hand-over (bf16 variant)
     // (INT8: the converter warpgroup keeps kConvRegs)
-    constexpr int kSoftmaxRegs = I8 ? 176 : 216, kOtherRegs = 72, kConvRegs = 88;
+    constexpr int kSoftmaxRegs = I8 ? 192 : 216, kOtherRegs = I8 ? 64 : 72, kConvRegs = 64;
     static_assert(128 * (2 * kSoftmaxRegs + kOtherRegs + (I8 ? kConvRegs : 0)) ==
                       kThreadsOf<I8> * kLaunchRegsOf<I8>,
                   "register hand-over");
