@@ -320,13 +320,12 @@ __device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int
         }
         const uint32_t row = tile + panel * (128 * 128) + t * 128;
         const uint32_t ca = (uint32_t)(((c0 + h0) ^ (t & 7)) << 4), cb = (uint32_t)(((c0 + (h0 ^ 1)) ^ (t & 7)) << 4);
-        if (h0) {
-            ptx::sts_v4(row + ca, o[4], o[5], o[6], o[7]);
-            ptx::sts_v4(row + cb, o[0], o[1], o[2], o[3]);
-        } else {
-            ptx::sts_v4(row + ca, o[0], o[1], o[2], o[3]);
-            ptx::sts_v4(row + cb, o[4], o[5], o[6], o[7]);
-        }
+        // selects, not a branch: a divergent branch here turns each store into two
+        // half-warp stores
+        const uint32_t x0 = h0 ? o[4] : o[0], x1 = h0 ? o[5] : o[1], x2 = h0 ? o[6] : o[2], x3 = h0 ? o[7] : o[3];
+        const uint32_t y0 = h0 ? o[0] : o[4], y1 = h0 ? o[1] : o[5], y2 = h0 ? o[2] : o[6], y3 = h0 ? o[3] : o[7];
+        ptx::sts_v4(row + ca, x0, x1, x2, x3);
+        ptx::sts_v4(row + cb, y0, y1, y2, y3);
     }
 }
 
