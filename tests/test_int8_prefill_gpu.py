@@ -68,6 +68,7 @@ MULTI = [  # seed, num_seqs, hq, hkv, d, bs, max_len, cached
     (521, 160, 4, 4, 128, 16, 512, "random"),
     (522, 96, 16, 4, 64, 32, 300, "random"),
     (523, 48, 28, 4, 128, 16, 200, None),
+    (524, 200, 16, 8, 128, 256, 300, "random"),
 ]
 
 
