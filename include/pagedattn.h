@@ -392,10 +392,22 @@ const char *pa_last_error_string(void);
  * Reads and clears the device-side error word (0 = none).  Bits: 0 a store
  * met a slot outside [-1, num_slots); 1 a bounded wait in the prefill kernel
  * timed out; 2 a block-copy triple was out of range; 3 a bounded wait in the
- * INT8 decode kernel timed out.  Synchronises `stream`: for tests and
- * debugging, never on the hot path.
+ * INT8 decode kernel timed out; 4 the wait of pa_selftest_bounded_wait timed
+ * out.  Synchronises `stream`: for tests and debugging, never on the hot path.
  */
 int pa_read_device_error(uint32_t *code, pa_stream_t stream);
+
+/*
+ * pa_selftest_bounded_wait — diagnostic of the library's failure path.  Every
+ * kernel hand-off waits on an mbarrier with a time limit; on expiry the kernel
+ * records the fact in the device error word and returns instead of hanging.
+ * This launches one warp that runs that same bounded wait on a barrier
+ * nothing completes (arrive_first == 0: bit 4 is set after about timeout_us
+ * microseconds) or one it completes itself first (arrive_first != 0: no
+ * error).  timeout_us in [1, 10^7], else PA_ERR_INVALID_ARG.  The GPU context
+ * stays usable either way.
+ */
+int pa_selftest_bounded_wait(uint32_t timeout_us, int arrive_first, pa_stream_t stream);
 
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int pa_version(void);

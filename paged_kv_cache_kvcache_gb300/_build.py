@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpagedattn.so")
 
-SOURCES = ["api.cpp", "pack.cpp", "store_kv.cu", "decode.cu", "decode_int8.cu", "prefill.cu", "copy_blocks.cu", "tmap.cpp"]
+SOURCES = ["api.cpp", "pack.cpp", "store_kv.cu", "decode.cu", "decode_int8.cu", "prefill.cu", "copy_blocks.cu", "tmap.cpp",
+           "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -412,5 +412,14 @@ extern "C" int pa_read_device_error(uint32_t *code, pa_stream_t stream)
         rc = read_fused_error(code);
     if (rc == PA_OK)
         rc = read_fused8_error(code);
+    if (rc == PA_OK)
+        rc = read_selftest_error(code);
     return rc;
+}
+
+extern "C" int pa_selftest_bounded_wait(uint32_t timeout_us, int arrive_first, pa_stream_t stream)
+{
+    if (timeout_us < 1 || timeout_us > 10000000u)
+        return fail(PA_ERR_INVALID_ARG, "timeout_us (%u) must be in [1, 10000000]", timeout_us);
+    return launch_selftest_wait(timeout_us, arrive_first ? 1 : 0, stream);
 }

@@ -155,5 +155,7 @@ int read_copy_error(uint32_t *code);
 int read_decode_error(uint32_t *code);
 int read_fused_error(uint32_t *code);
 int read_fused8_error(uint32_t *code);
+int launch_selftest_wait(uint32_t timeout_us, int arrive_first, void *stream);
+int read_selftest_error(uint32_t *code);
 
 } // namespace pa

@@ -24,7 +24,7 @@ EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache",
            "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
            "pa_prefill_varlen_int8", "pa_pack_decode_fixed", "pa_decode_fused", "pa_copy_blocks_int8",
            "pa_decode_int8_fused",
-           "pa_last_error_string", "pa_read_device_error", "pa_version")
+           "pa_last_error_string", "pa_read_device_error", "pa_selftest_bounded_wait", "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             L.pa_last_error_string.argtypes = []
             L.pa_last_error_string.restype = ctypes.c_char_p
             L.pa_read_device_error.argtypes = [P, P]
+            L.pa_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_int, P]
             L.pa_version.argtypes = []
             for name in EXPORTS:
                 if name not in ("pa_last_error_string",):
@@ -373,6 +374,13 @@ def pa_copy_blocks_int8(dims: pa_dims, k_cache, v_cache, k_scale, v_scale, tripl
     n = int(triples.shape[0]) if num_triples is None else int(num_triples)
     _check(lib().pa_copy_blocks_int8(ctypes.byref(dims), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                      _ptr(v_scale), _ptr(triples), n, _stream(stream)), "pa_copy_blocks_int8")
+
+
+def pa_selftest_bounded_wait(timeout_us: int, arrive_first: bool = False, stream=None):
+    """Run the library's bounded mbarrier wait on a barrier nothing completes (or, with
+    arrive_first, one it completes itself); a timeout shows as bit 4 of pa_read_device_error."""
+    _check(lib().pa_selftest_bounded_wait(ctypes.c_uint32(int(timeout_us)), 1 if arrive_first else 0, _stream(stream)),
+           "pa_selftest_bounded_wait")
 
 
 def pa_read_device_error(stream=None) -> int:

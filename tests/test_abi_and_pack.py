@@ -70,6 +70,8 @@ def test_device_calls_reject_bad_args_without_touching_the_gpu():
     assert L.pa_decode(ctypes.byref(dims), 16, 16, 16, 16, 16, ctypes.c_float(0.1), 16, ctypes.byref(dm), 16, 16,
                        None, 0, None) == pa.PA_ERR_WORKSPACE
     assert "workspace" in pa.pa_last_error_string()
+    for bad in (0, 10000001):
+        assert L.pa_selftest_bounded_wait(bad, 0, None) == pa.PA_ERR_INVALID_ARG
 
 
 def test_pack_rejects_malformed_sequences():
