@@ -114,7 +114,7 @@ struct PfLayout {
     // both PV MMAs: K gets the deeper ring so its loads start earliest.
     static constexpr int kKStages = I8 ? 3 : (D == 128 ? 3 : 4);
     static constexpr int kVStages = I8 ? (D == 128 ? 2 : 3) : (D == 128 ? 2 : 4);
-    static constexpr int kQ = 0;                    // two query tiles (also the output staging)
+    static constexpr int kQ = 0;                    // two query tiles
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
     // INT8 cache: a key tile's raw codes (128 rows x D bytes) land in the upper
@@ -139,7 +139,6 @@ struct PfLayout {
     {
         return kInPlace ? kV + s * kTileBytes + kTileBytes / 2 : kStg + (kKStages + s) * kCodeBytes;
     }
-    static_assert(128 * D * 2 <= kTileBytes, "O staging must fit in a query tile");
     static_assert(!kInPlace || kCodeBytes == kTileBytes / 2, "in-place codes fill the second panel");
     static_assert(kKStages <= 4 && kVStages <= 4, "barrier slots");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
