@@ -175,6 +175,10 @@ class Step:
         for e in self.up_ev:
             e.record(stream)
         self.ws = pa.decode_workspace(self.plans_d[0])
+        self.pipe_ev = {"p": [torch.cuda.Event(), torch.cuda.Event()], "d": [torch.cuda.Event(), torch.cuda.Event()]}
+        for evs_ in self.pipe_ev.values():
+            for e in evs_:
+                e.record(stream)
         self.i = 0
         self.launches_per_step = 4 + (1 if self.plans_d[0].meta.num_partials > 0 else 0) - (1 if fused else 0)
         if mixed:  # one launch for both phases' rows, over one pool
@@ -201,8 +205,43 @@ class Step:
                                  stream=self.s)
         return cache
 
-    def run(self, ev=None, host=None, phase="both"):
-        """Enqueue one step; ev = dict of event pairs for per-phase timing; host = e2e buffers."""
+    # ---- pipelined end-to-end steps: one phase's compute on explicit device buffers
+    def prefill_on(self, q, k, v, out, slot):
+        """Pack + upload + store + prefill of the prompt batch, reading q/k/v and writing out."""
+        pa, s = self.pa, self.s
+        self.pipe_ev["p"][slot].synchronize()  # the pinned plan image of this slot is free again
+        plan = pa.pa_pack_prefill(self.dims_p, self.bp.seq_lens, self.bp.query_lens, self.blocks_p,
+                                  into=self.plans_p[slot]).upload(stream=s)
+        self.pipe_ev["p"][slot].record(s)
+        if self.int8:
+            pa.pa_store_kvcache_int8(self.dims_p, k, v, *self.c8_p, plan.slot_mapping, self.bp.num_tokens, stream=s)
+            pa.pa_prefill_varlen_int8(self.dims_p, q, *self.c8_p, plan, self.bp.scale, out, stream=s)
+        else:
+            pa.pa_store_kvcache(self.dims_p, k, v, self.kc_p, self.vc_p, plan.slot_mapping, self.bp.num_tokens,
+                                stream=s)
+            pa.pa_prefill_varlen(self.dims_p, q, self.kc_p, self.vc_p, plan, self.bp.scale, out, stream=s)
+
+    def decode_on(self, q, k, v, out, slot):
+        """Pack + upload + store + decode of the decode batch, reading q/k/v and writing out."""
+        pa, s = self.pa, self.s
+        self.pipe_ev["d"][slot].synchronize()
+        plan = pa.pa_pack_decode(self.dims_d, self.bd.seq_lens, self.blocks_d, into=self.plans_d[slot]).upload(stream=s)
+        self.pipe_ev["d"][slot].record(s)
+        if self.int8 and self.fused:
+            pa.pa_decode_int8_fused(self.dims_d, q, k, v, *self.c8_d, plan, self.bd.scale, out, self.ws, stream=s)
+        elif self.int8:
+            pa.pa_store_kvcache_int8(self.dims_d, k, v, *self.c8_d, plan.slot_mapping, self.bd.num_tokens, stream=s)
+            pa.pa_decode_int8(self.dims_d, q, *self.c8_d, plan, self.bd.scale, out, self.ws, stream=s)
+        elif self.fused:
+            pa.pa_decode_fused(self.dims_d, q, k, v, self.kc_d, self.vc_d, plan, self.bd.scale, out, self.ws,
+                               stream=s)
+        else:
+            pa.pa_store_kvcache(self.dims_d, k, v, self.kc_d, self.vc_d, plan.slot_mapping, self.bd.num_tokens,
+                                stream=s)
+            pa.pa_decode(self.dims_d, q, self.kc_d, self.vc_d, plan, self.bd.scale, out, self.ws, stream=s)
+
+    def run(self, ev=None, phase="both"):
+        """Enqueue one step; ev = dict of event pairs for per-phase timing."""
         pa, s = self.pa, self.s
         k = self.i & 1
         self.i += 1
@@ -225,11 +264,7 @@ class Step:
         if phase == "decode":
             for n in ("pk0", "pk1", "p1"):
                 rec(n)
-            return self._decode(ev, host, k, rec)
-        if host is not None:
-            self.bp.q.copy_(host["pq"], non_blocking=True)
-            self.bp.k.copy_(host["pk"], non_blocking=True)
-            self.bp.v.copy_(host["pv"], non_blocking=True)
+            return self._decode(ev, k, rec)
         plan_p = pa.pa_pack_prefill(self.dims_p, self.bp.seq_lens, self.bp.query_lens, self.blocks_p,
                                     into=self.plans_p[k]).upload(stream=s)
         if self.int8:
@@ -245,22 +280,16 @@ class Step:
             pa.pa_prefill_varlen(self.dims_p, self.bp.q, self.kc_p, self.vc_p, plan_p, self.bp.scale, self.out_p,
                                  stream=s)
         rec("pk1")
-        if host is not None:
-            host["po"].copy_(self.out_p, non_blocking=True)
         rec("p1")
         if phase == "prefill":
             for n in ("dk0", "dk1", "d1"):
                 rec(n)
             return
-        self._decode(ev, host, k, rec)
+        self._decode(ev, k, rec)
 
-    def _decode(self, ev, host, k, rec):
+    def _decode(self, ev, k, rec):
         pa, s = self.pa, self.s
         # ---- decode phase
-        if host is not None:
-            self.bd.q.copy_(host["dq"], non_blocking=True)
-            self.bd.k.copy_(host["dk"], non_blocking=True)
-            self.bd.v.copy_(host["dv"], non_blocking=True)
         plan_d = pa.pa_pack_decode(self.dims_d, self.bd.seq_lens, self.blocks_d, into=self.plans_d[k]).upload(stream=s)
         self.up_ev[k].record(s)
         if self.int8 and self.fused:  # quantising store + INT8 decode in one launch
@@ -283,9 +312,63 @@ class Step:
             pa.pa_decode(self.dims_d, self.bd.q, self.kc_d, self.vc_d, plan_d, self.bd.scale, self.out_d, self.ws,
                          stream=s)
         rec("dk1")
-        if host is not None:
-            host["do"].copy_(self.out_d, non_blocking=True)
         rec("d1")
+
+
+def pipelined_e2e(step, phase, steps, warmup):
+    """One phase end to end through the public API, copies overlapped across steps: while
+    step i computes on the compute stream, step i+1's inputs are copied in from pinned host
+    memory and step i-1's output is copied back out (one copy stream per direction, two
+    device slots; events keep every copy off the buffers a step still uses).  Every timed
+    step still moves all of its inputs in and its whole output out.
+    Returns (ms per step, H2D bytes per step, D2H bytes per step)."""
+    s = step.s
+    b = step.bp if phase == "p" else step.bd
+    run = step.prefill_on if phase == "p" else step.decode_on
+    out0 = step.out_p if phase == "p" else step.out_d
+    host_in = [t.cpu().pin_memory() for t in (b.q, b.k, b.v)]
+    host_out = [torch.empty_like(out0, device="cpu").pin_memory() for _ in range(2)]
+    dev = [[b.q, b.k, b.v, out0], [torch.empty_like(b.q), torch.empty_like(b.k), torch.empty_like(b.v),
+                                   torch.empty_like(out0)]]
+    ci, co = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    out_read = [torch.cuda.Event(), torch.cuda.Event()]
+    used = [False, False]
+
+    def one(i):
+        k = i & 1
+        q, kk, vv, out = dev[k]
+        with torch.cuda.stream(ci):
+            if used[k]:
+                ci.wait_event(done[k])  # step i-2 has finished reading this slot's inputs
+            q.copy_(host_in[0], non_blocking=True)
+            kk.copy_(host_in[1], non_blocking=True)
+            vv.copy_(host_in[2], non_blocking=True)
+            in_ready[k].record(ci)
+        s.wait_event(in_ready[k])
+        if used[k]:
+            s.wait_event(out_read[k])  # step i-2's output has left this slot
+        run(q, kk, vv, out, k)
+        done[k].record(s)
+        with torch.cuda.stream(co):
+            co.wait_event(done[k])
+            host_out[k].copy_(out, non_blocking=True)
+            out_read[k].record(co)
+        used[k] = True
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(ci)
+    for i in range(warmup, warmup + steps):
+        one(i)
+    t1.record(co)  # after the last output copy, which follows every earlier copy and step
+    torch.cuda.synchronize()
+    h2d = sum(int(t.numel() * t.element_size()) for t in host_in)
+    d2h = int(host_out[0].numel() * host_out[0].element_size())
+    return t0.elapsed_time(t1) / steps, h2d, d2h
 
 
 class Clocks:
@@ -456,29 +539,17 @@ def main():
 
         e2e = None
         if not args.no_e2e and args.phase == "both" and args.decode_path != "mixed":
-            host = {"pq": step.bp.q.cpu().pin_memory(), "pk": step.bp.k.cpu().pin_memory(),
-                    "pv": step.bp.v.cpu().pin_memory(), "dq": step.bd.q.cpu().pin_memory(),
-                    "dk": step.bd.k.cpu().pin_memory(), "dv": step.bd.v.cpu().pin_memory(),
-                    "po": torch.empty_like(step.out_p, device="cpu").pin_memory(),
-                    "do": torch.empty_like(step.out_d, device="cpu").pin_memory()}
-            for _ in range(args.warmup):
-                step.run(host=host)
-            stream.synchronize()
-            evs2 = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(args.steps)]
-            for i in range(args.steps):
-                step.run(evs2[i], host=host)
-            torch.cuda.synchronize()
-            e2e_p = statistics.mean([e["p0"].elapsed_time(e["p1"]) for e in evs2])
-            e2e_d = statistics.mean([e["p1"].elapsed_time(e["d1"]) for e in evs2])
+            e2e_p, h2d_p, d2h_p = pipelined_e2e(step, "p", args.steps, args.warmup)
+            e2e_d, h2d_d, d2h_d = pipelined_e2e(step, "d", args.steps, args.warmup)
             meta_bytes = int(step.plans_p[0].meta.total_bytes + step.plans_d[0].meta.total_bytes)
-            h2d = sum(int(host[k].numel() * host[k].element_size()) for k in ("pq", "pk", "pv", "dq", "dk", "dv"))
-            d2h = sum(int(host[k].numel() * host[k].element_size()) for k in ("po", "do"))
             e2e = {"value": round(prefill_flops(step.bp) / (e2e_p * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
-                   "h2d_bytes_per_step": h2d + meta_bytes, "d2h_bytes_per_step": d2h,
+                   "h2d_bytes_per_step": h2d_p + h2d_d + meta_bytes, "d2h_bytes_per_step": d2h_p + d2h_d,
                    "decode": {"value": round(decode_bytes(step.bd, wd.pool, args.kv) / (e2e_d * 1e-3) / 1e9 * world,
                                              1),
                               "unit": "GB/s"},
-                   "ms_per_step": round(e2e_p + e2e_d, 4)}
+                   "ms_per_step": round(e2e_p + e2e_d, 4),
+                   "pipelining": "per phase: step i+1's inputs copied in and step i-1's output copied out "
+                                 "(pinned host memory, one copy stream each way) while step i computes"}
 
     flops = prefill_flops(step.bp)
     dbytes = decode_bytes(step.bd, wd.pool, args.kv)
