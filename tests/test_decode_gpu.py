@@ -124,3 +124,39 @@ def test_decode_qwen25_full_size_sampled_sequences():
     ref, _ = oracle.run_batch(sub_k, sub_v, sub, w.pool.block_size)
     assert_close(out[seqs], ref, what="qwen25 decode")
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_two_split_plans_share_an_uninitialised_workspace(kv):
+    """Plans with different split counts on one workspace holding junk: both match the
+    oracle, and the same plan run again gives the same bits."""
+    from tests.harness import int8_pools
+    w = workloads.random_case(151, num_seqs=6, hq=8, hkv=2, d=128, bs=16, max_len=2000, kind="decode",
+                              device="cuda")
+    b = w.batches[0]
+    dims = dims_of(w, b)
+    plans = [pa.pa_pack_decode(dims, b.seq_lens, b.block_lists, s).upload("cuda") for s in (256, 576)]
+    assert plans[0].meta.max_splits > plans[1].meta.max_splits > 1
+    ws = torch.full((max(int(p.meta.workspace_bytes) for p in plans),), 0x5A, dtype=torch.uint8, device="cuda")
+    q, k, v = b.q.cuda(), b.k.cuda(), b.v.cuda()
+    if kv == "bf16":
+        kc, vc = w.pool.k_cache.clone(), w.pool.v_cache.clone()
+        pa.pa_store_kvcache(dims, k, v, kc, vc, plans[0].slot_mapping, b.num_tokens)
+        ref, _ = oracle.run_batch(bits(w.pool.k_cache), bits(w.pool.v_cache), b, w.pool.block_size)
+        call = lambda p, out: pa.pa_decode(dims, q, kc, vc, p, b.scale, out, ws)
+    else:
+        gpu, host = int8_pools(w, b.num_heads)
+        pa.pa_store_kvcache_int8(dims, k, v, *gpu, plans[0].slot_mapping, b.num_tokens)
+        ref, _ = oracle.run_batch_int8(*host, b, w.pool.block_size)  # stores the batch's rows, then attends
+        call = lambda p, out: pa.pa_decode_int8(dims, q, *gpu, p, b.scale, out, ws)
+    outs = []
+    for rep in range(2):
+        for p in plans:
+            out = torch.empty_like(q)
+            call(p, out)
+            outs.append(out)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    for out in outs:
+        assert_close(out, ref, what=f"{kv} shared workspace")
+    assert torch.equal(outs[0], outs[2]) and torch.equal(outs[1], outs[3])
