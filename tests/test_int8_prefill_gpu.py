@@ -112,6 +112,15 @@ def test_int8_prefill_qwen25_sampled():
     assert_close(out, ref, rows=sel, what="int8 qwen25 prefill (sampled rows)")
 
 
+def test_int8_prefill_single_32k_sequence_sampled():
+    """One 32768-token causal prompt on the INT8 cache: items of up to 256 key tiles (code,
+    factor and release rings wrapping many times); sampled rows."""
+    w = workloads.random_case(561, num_seqs=1, hq=28, hkv=4, d=128, bs=16, min_len=32768, max_len=32768,
+                              cached=None, device="cuda")
+    (batch, out, ref, sel), = _run_both(w, row_select=lambda b: sample_rows(b, 24, seed=9))
+    assert_close(out, ref, rows=sel, what="int8 single 32k prefill (sampled rows)")
+
+
 def test_int8_prefill_matches_int8_decode():
     """Decode at context n equals row n-1 of an INT8 prefill over the same n tokens (same cache)."""
     n, hq, hkv, d, bs = 777, 14, 2, 128, 16

@@ -189,6 +189,23 @@ def test_prefill_qwen25_full_size_sampled_rows():
     assert torch.isfinite(out.float()).all()
 
 
+def test_prefill_single_32k_sequence_sampled_rows():
+    """One 32768-token causal prompt (Qwen2.5 heads): items of up to 256 key tiles, so every
+    ring and the release-event ring wrap many times within an item; oracle on sampled rows."""
+    w = workloads.random_case(161, num_seqs=1, hq=28, hkv=4, d=128, bs=16, min_len=32768, max_len=32768,
+                              cached=None, device="cuda")
+    batch = w.batches[0]
+    sel = sample_rows(batch, per_seq=24, seed=7)
+    kc, vc = w.pool.k_cache.clone(), w.pool.v_cache.clone()
+    ok_, ov_ = bits(w.pool.k_cache), bits(w.pool.v_cache)
+    out, _ = run_gpu_batch(w, batch, kc, vc)
+    ref, _ = oracle.run_batch(ok_, ov_, batch, w.pool.block_size, row_select=sel)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    assert_close(out, ref, rows=sel, what="single 32k prefill")
+    assert torch.isfinite(out.float()).all()
+
+
 def test_mixed_prefill_and_decode_rows_in_one_launch():
     """Decode rows are prefill rows with one query token: one varlen launch serves a mixed batch
     (long-context single-token rows next to full prompts and cached-prefix suffixes)."""
