@@ -310,13 +310,14 @@ int pa_decode_int8(const pa_dims *dims, const void *q, const void *k_cache, cons
 /*
  * pa_prefill_varlen_int8 — pa_prefill_varlen over an INT8 cache: the same
  * plan (pa_pack_prefill), arguments and result, with the cached K and V read
- * as code * scale.  The dequantisation is fused the way the page's Q3
- * follow-ups describe it: the key scale multiplies each score after the
- * q.k dot product over the raw codes, and the value scale is folded into the
- * softmax weights (the normaliser keeps the unscaled weights); no floating
- * copy of the cache is materialised.  Internally the codes (exact in fp16),
- * q (rounded to fp16, saturating at +-65504) and the scaled weights feed
- * fp16 tensor-core products with fp32 accumulation.  PA_ERR_UNSUPPORTED, before
+ * as code * scale, dequantised inside the kernel (the page's Q3: no
+ * floating copy of the cache is materialised).  Each key tile's codes are
+ * turned in shared memory into fp16 code * token scale (one rounding; the
+ * tile serves 256 query rows, so this is one multiply per element where the
+ * page's per-query kernel saves multiplies by scaling scores and weights
+ * instead; the product is the same), q is rounded to fp16 (saturating at
+ * +-65504), and fp16 tensor-core products accumulate in fp32.  Cached values
+ * must lie within the fp16 range (|x| < 65504).  PA_ERR_UNSUPPORTED, before
  * any launch, if the library's INT8 prefill kernel was compiled with other
  * than 128 registers per thread (its 16 warps re-divide exactly that many).
  */

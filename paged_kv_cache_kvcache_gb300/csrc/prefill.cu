@@ -51,11 +51,14 @@
 //    Q3 and its follow-up on where the scales go): 16 warps; warp 11 issues
 //    every TMA load, raw code tiles land next to (D = 128: inside) the tiles
 //    they are converted into, warps 12-15 (one per SM sub-partition) turn a
-//    quarter of the rows of every code tile each into exact f16 values, warps
-//    8 and 10 turn Q into f16 and stage the per-key factors, the MMAs run
-//    kind::f16, and the softmax applies the key scale
-//    to each score column after the dot product and folds the value scale
-//    into P, keeping the unscaled P for the row sum.
+//    quarter of the rows of every code tile each into f16 code x token
+//    scale, warps 8 and 10 turn Q into f16, the MMAs run kind::f16 and the
+//    softmax is the bf16 one.  The page moves the scales out of the tile
+//    (key scale after the dot product, value scale into P) to save
+//    multiplies in a kernel that dequantises in registers per query; here
+//    the tile is converted once for 2 x 128 query rows anyway, so scaling it
+//    there is one multiply per element instead of one per score (the result
+//    is the same product, rounded once more to f16).
 //  * mbarriers order every hand-off; every wait is bounded and reports a
 //    timeout through a device error word instead of hanging.
 #include <cuda.h>
@@ -75,8 +78,7 @@ namespace {
 
 // warps 0-7: softmax (two warpgroups), 8: K TMA producer, 9: MMA issuer (and
 // TMEM owner), 10: V TMA producer, 11: Q TMA producer (INT8: 11 loads
-// everything, 8 and 10 convert Q and stage factors, 12-15 convert the code
-// tiles).  Registers are granted per 4 warps: 168 per thread at launch for the
+// everything, 8 and 10 convert Q, 12-15 convert and scale the code tiles).  Registers are granted per 4 warps: 168 per thread at launch for the
 // 12-warp bf16 CTA, 128 for the 16-warp INT8 one; setmaxnreg then moves part of
 // the other warpgroups' share to the softmax warpgroups (bf16: 216 softmax, 72
 // in warps 8-11; INT8: 192 softmax, 64 in warps 8-11 and 64 in 12-15).
@@ -120,15 +122,12 @@ struct PfLayout {
     // INT8 cache: a key tile's raw codes (128 rows x D bytes) land in the upper
     // half of the 16-bit tile they are converted into (D = 128: row t's codes
     // occupy the slot of row t's second panel) or in a ring of their own
-    // (D = 64), and a 2-slot ring holds each key tile's per-key factors.
+    // (D = 64).
     static constexpr bool kInPlace = D == 128;
     static constexpr int kCodeBytes = 128 * D;
     static constexpr int kStg = kV + kVStages * kTileBytes;
     static constexpr int kStgBytes = I8 && !kInPlace ? (kKStages + kVStages) * kCodeBytes : 0;
-    static constexpr int kScl = kStg + kStgBytes;
-    static constexpr int kSclSlot = 128 * 4 + 128 * 2; // 128 fp32 K factors, then 128 fp16 V scales
-    static constexpr int kSclBytes = I8 ? 2 * kSclSlot : 0;
-    static constexpr int kBar = kScl + kSclBytes;
+    static constexpr int kBar = kStg + kStgBytes;
     static constexpr int kBarBytes = 512;
     static constexpr int kSmemBytes = kBar + kBarBytes + 1024; // + alignment slack
     __host__ __device__ static constexpr int k_codes(int s)
@@ -180,10 +179,9 @@ struct Bars {
     // V slot s holds an item's last key tile with its rows past the sequence end zeroed
     __device__ uint32_t v_tail(int s) const { return base + 8 * (26 + s); }
     __device__ uint32_t tmem_slot() const { return base + 8 * 30; }
-    // INT8 variant: raw code tiles landed, per-key factors written, Q converted
+    // INT8 variant: raw code tiles landed, Q converted
     __device__ uint32_t k_load(int s) const { return base + 8 * (32 + s); }
     __device__ uint32_t v_load(int s) const { return base + 8 * (36 + s); }
-    __device__ uint32_t sc_full(int i) const { return base + 8 * (40 + i); }
     __device__ uint32_t q_ready(int t) const { return base + 8 * (42 + t); }
 };
 static_assert(kIterRing == 8, "barrier slots 12..19");
@@ -292,39 +290,59 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u, uint32_t sel)
     return ptx::sub_f16x2(ptx::prmt(u, 0x64646464u, sel), kMagic);
 }
 
-// Raw int8 code rows r0 .. r0+31 of a staged key tile -> f16 codes (exact,
-// |code| <= 127) in the 128B-swizzled layout the MMAs read (panels of 64
-// elements x 128 rows, the layout TMA gives the bf16 tiles).  One warp; D/16
-// lanes per row.
+// Raw int8 code rows r0 .. r0+31 of a staged key tile -> f16 code x scale of
+// the row's token (the code exact in f16, one rounding in the product) in the
+// 128B-swizzled layout the MMAs read (panels of 64 elements x 128 rows, the
+// layout TMA gives the bf16 tiles).  One warp; D/16 lanes per row, each
+// converting 16 codes (two 16-byte output chunks); lane i holds the f16x2
+// pair (scale, scale) of row r0 + i (0 for keys past the sequence).
+//
+// Bank conflicts: an 8-lane store phase covers one row (D = 128: both
+// panels) or two rows (D = 64); the lanes of panel 1 and of odd rows at
+// D = 128 handle their two chunks in the other order, so that every store
+// and every 8-byte half-row load (D = 128: rows t and t+1 in one 16-lane
+// phase) touches each bank once.
 template <int D, bool kInPlace>
-__device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int lane, int r0)
+__device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int lane, int r0, uint32_t scale2)
 {
     constexpr int LPR = D / 16;   // lanes per row, 16 codes each
     constexpr int RPP = 32 / LPR; // rows per pass
     const int sub = lane / LPR, l = lane % LPR;
     const int panel = l >> 2;     // 4 lanes cover one 64-element panel row
-    const int c0 = (l & 3) * 2;   // first of the lane's two 16-byte chunks
-    const int h0 = panel & 1;     // second-panel lanes store their chunks in the other order (no bank conflict)
+    const int c0 = (l & 3) * 2;   // the lane's two chunks: c0, c0 + 1
+    // chunk handled first (D = 64: always c0; a 4-lane row never meets itself)
+    const int h0 = D == 128 ? (panel ^ (sub & 1)) : 0;
+    const int ta = c0 + h0, tb = c0 + (h0 ^ 1);
+    // t & 7 = sub ^ (RPP * pass & 7): two swizzle phases, fixed per lane
+    const uint32_t dst = tile + panel * (128 * 128) + (uint32_t)(r0 + sub) * 128;
+    const uint32_t a0 = dst + (uint32_t)((ta ^ sub) << 4), b0 = dst + (uint32_t)((tb ^ sub) << 4);
+    const uint32_t a1 = dst + (uint32_t)((ta ^ sub ^ (RPP & 7)) << 4), b1 = dst + (uint32_t)((tb ^ sub ^ (RPP & 7)) << 4);
+    const uint32_t src = codes + (uint32_t)(r0 + sub) * D + 16 * l;
 #pragma unroll
-    for (int t = r0 + sub; t < r0 + 32; t += RPP) {
-        const uint4 w = ptx::lds_v4(codes + t * D + 16 * l);
+    for (int pass = 0; pass < 32 / RPP; ++pass) {
+        uint32_t u[4];
+        if constexpr (D == 128) {
+            const uint2 x = ptx::lds_v2(src + pass * RPP * D + 8 * h0);
+            const uint2 y = ptx::lds_v2(src + pass * RPP * D + 8 * (h0 ^ 1));
+            u[0] = x.x, u[1] = x.y, u[2] = y.x, u[3] = y.y;
+        } else {
+            const uint4 w = ptx::lds_v4(src + pass * RPP * D);
+            u[0] = w.x, u[1] = w.y, u[2] = w.z, u[3] = w.w;
+        }
         if constexpr (kInPlace)
             __syncwarp(); // row t's codes are read before its second panel is written over them
+        const uint32_t sc2 = __shfl_sync(0xffffffffu, scale2, sub + RPP * pass);
         uint32_t o[8];
-        const uint32_t u[4] = {w.x ^ kFlip, w.y ^ kFlip, w.z ^ kFlip, w.w ^ kFlip};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            o[2 * i] = codes_to_f16x2(u[i], 0x4140u);
-            o[2 * i + 1] = codes_to_f16x2(u[i], 0x4342u);
+            const uint32_t f = u[i] ^ kFlip;
+            o[2 * i] = ptx::mul_f16x2(codes_to_f16x2(f, 0x4140u), sc2);
+            o[2 * i + 1] = ptx::mul_f16x2(codes_to_f16x2(f, 0x4342u), sc2);
         }
-        const uint32_t row = tile + panel * (128 * 128) + t * 128;
-        const uint32_t ca = (uint32_t)(((c0 + h0) ^ (t & 7)) << 4), cb = (uint32_t)(((c0 + (h0 ^ 1)) ^ (t & 7)) << 4);
-        // selects, not a branch: a divergent branch here turns each store into two
-        // half-warp stores
-        const uint32_t x0 = h0 ? o[4] : o[0], x1 = h0 ? o[5] : o[1], x2 = h0 ? o[6] : o[2], x3 = h0 ? o[7] : o[3];
-        const uint32_t y0 = h0 ? o[0] : o[4], y1 = h0 ? o[1] : o[5], y2 = h0 ? o[2] : o[6], y3 = h0 ? o[3] : o[7];
-        ptx::sts_v4(row + ca, x0, x1, x2, x3);
-        ptx::sts_v4(row + cb, y0, y1, y2, y3);
+        const uint32_t off = (uint32_t)(pass * RPP * 128);
+        const bool odd = ((RPP * pass) & 7) != 0;
+        ptx::sts_v4((odd ? a1 : a0) + off, o[0], o[1], o[2], o[3]);
+        ptx::sts_v4((odd ? b1 : b0) + off, o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -432,10 +450,8 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 ptx::mbar_init(bars.k_load(s), 1);
             for (int s = 0; s < L::kVStages; ++s)
                 ptx::mbar_init(bars.v_load(s), 1);
-            for (int i = 0; i < 2; ++i) {
-                ptx::mbar_init(bars.sc_full(i), 1);
+            for (int i = 0; i < 2; ++i)
                 ptx::mbar_init(bars.q_ready(i), 1);
-            }
         }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
@@ -452,22 +468,44 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
 
     if (I8 && warp >= kConvWarp0) {
         // ---------------------------------------------------------------- INT8: code converters
-        // warp 12 + i turns rows 32i .. 32i+31 of every K and V code tile into exact
-        // f16 codes: the conversion is spread over all four SM sub-partitions, so it
-        // slows each softmax warp alike.  The scales are applied after the products
-        // (softmax), not to the tiles.
+        // warp 12 + i turns rows 32i .. 32i+31 of every K and V code tile into f16
+        // code x token scale: the conversion is spread over all four SM
+        // sub-partitions, so it slows each softmax warp alike, and with the scales
+        // applied here the softmax is the bf16 one (a tile feeds 2 x 128 query rows,
+        // so one multiply per tile element replaces one per score).
         ptx::reg_dealloc<kConvRegs>();
         ItemIter items(p.tiles, p.num_items, P);
         const int r0 = 32 * (warp - kConvWarp0);
+        const int bs = p.block_size, Hkv = p.num_kv_heads;
+        // K and V scales of key r0 + lane of key tile j of item w as f16x2 pairs (0 past the sequence)
+        auto fetch = [&](const Item &w, int j, uint32_t &ks, uint32_t &vs) {
+            const int key = j * 128 + r0 + lane;
+            ks = vs = 0u;
+            if (key < w.lk) {
+                const int phys = __ldg(p.block_tables + (size_t)w.b * p.max_blocks + key / bs);
+                const size_t si = ((size_t)phys * Hkv + w.g) * bs + (key & (bs - 1));
+                ks = __ldg(reinterpret_cast<const unsigned short *>(p.k_scale) + si) * 0x10001u;
+                vs = __ldg(reinterpret_cast<const unsigned short *>(p.v_scale) + si) * 0x10001u;
+            }
+        };
         int X = 0;
         bool ok = true;
+        uint32_t ks = 0u, vs = 0u;
+        if (items.more())
+            fetch(items.peek(), 0, ks, vs);
         while (ok && items.more()) {
             const Item w = items.next();
             for (int j = 0; j < w.nkt; ++j, ++X) {
+                const uint32_t ks_j = ks, vs_j = vs;
+                if (j + 1 < w.nkt) // the next tile's scales (perhaps the next item's first)
+                    fetch(w, j + 1, ks, vs);
+                else if (items.more())
+                    fetch(items.peek(), 0, ks, vs);
                 const int sk = X % L::kKStages;
                 if (!(ok = wwait(bars.k_load(sk), (X / L::kKStages) & 1)))
                     break;
-                convert_codes<D, L::kInPlace>(sbase + L::k_codes(sk), sbase + L::kK + sk * L::kTileBytes, lane, r0);
+                convert_codes<D, L::kInPlace>(sbase + L::k_codes(sk), sbase + L::kK + sk * L::kTileBytes, lane, r0,
+                                              ks_j);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)
@@ -475,7 +513,8 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 const int sv = X % L::kVStages;
                 if (!(ok = wwait(bars.v_load(sv), (X / L::kVStages) & 1)))
                     break;
-                convert_codes<D, L::kInPlace>(sbase + L::v_codes(sv), sbase + L::kV + sv * L::kTileBytes, lane, r0);
+                convert_codes<D, L::kInPlace>(sbase + L::v_codes(sv), sbase + L::kV + sv * L::kTileBytes, lane, r0,
+                                              vs_j);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)
@@ -483,7 +522,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             }
         }
     } else if (warp >= 8) {
-        // warps 8-11 (copies, MMA issue; INT8 also Q conversion and factors) need
+        // warps 8-11 (copies, MMA issue; INT8 also Q conversion) need
         // fewer registers and hand part of theirs to the softmax warpgroups (128 x
         // (2 kSoftmaxRegs + kOtherRegs [+ kConvRegs]) = the launch's registers)
         ptx::reg_dealloc<kOtherRegs>();
@@ -629,90 +668,20 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 }
             }
         } else if (I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
-            // ------------------------------------------------------------ INT8: Q conversion, factors
+            // ------------------------------------------------------------ INT8: Q conversion
             ItemIter items(p.tiles, p.num_items, P);
-            // warp 8: query tile 0; warp 10: query tile 1 and the per-key factors
-            const bool is_k = warp == kKProducerWarp;
-            const int tq = is_k ? 0 : 1;
-            auto convert_q = [&](const Item &w) -> bool {
-                if (!wwait(bars.q_full(tq), w.ord & 1))
-                    return false;
+            // warp 8: query tile 0; warp 10: query tile 1
+            const int tq = warp == kKProducerWarp ? 0 : 1;
+            bool ok = true;
+            while (ok && items.more()) {
+                const Item w = items.next();
+                if (!(ok = wwait(bars.q_full(tq), w.ord & 1)))
+                    break;
                 q_tile_to_f16<D>(sgen + L::kQ + tq * L::kTileBytes, lane);
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0)
                     ptx::mbar_arrive(bars.q_ready(tq));
-                return true;
-            };
-            bool ok = true;
-            int X = 0;
-            if (is_k) {
-                while (ok && items.more())
-                    ok = convert_q(items.next());
-            } else if (items.more()) {
-                // factors of key tile j, keys 4*lane .. 4*lane+3 (one block: bs >= 16)
-                const int Hkv = p.num_kv_heads;
-                const float sl2 = p.scale_log2;
-                auto fetch = [&](const Item &w, int j, uint2 &kr, uint2 &vr) {
-                    const int key = j * 128 + 4 * lane;
-                    kr = vr = make_uint2(0u, 0u);
-                    if (key < w.lk) {
-                        const int phys = __ldg(p.block_tables + (size_t)w.b * p.max_blocks + key / bs);
-                        const size_t si = ((size_t)phys * Hkv + w.g) * bs + (key & (bs - 1));
-                        kr = __ldg(reinterpret_cast<const uint2 *>(p.k_scale + si));
-                        vr = __ldg(reinterpret_cast<const uint2 *>(p.v_scale + si));
-                    }
-                };
-                Item w = items.next();
-                uint2 kr, vr;
-                fetch(w, 0, kr, vr);
-                uint32_t starts = 0;
-                for (int j = 0;; ++X) {
-                    if (j == 0 && !(ok = convert_q(w)))
-                        break;
-                    starts = (starts << 1) | (j == 0 ? 1u : 0u);
-                    // slot X & 1 held tile X - 2's factors, read until V tile X - 2's release
-                    if (X >= 2) {
-                        const int e = release_event(X, 2, w.ord, starts, 1);
-                        if (!(ok = wwait(bars.released(e), (e / kIterRing) & 1)))
-                            break;
-                    }
-                    {
-                        const int key = j * 128 + 4 * lane;
-                        const uint32_t kw[2] = {kr.x, kr.y};
-                        uint32_t vw[2] = {vr.x, vr.y};
-                        float kf[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            // keys past the sequence: factor 0 (their scores are masked, their weights 0)
-                            const bool valid = key + i < w.lk;
-                            const float ks = __half2float(__ushort_as_half((unsigned short)(kw[i >> 1] >> (16 * (i & 1)))));
-                            kf[i] = valid ? ks * sl2 : 0.f;
-                            if (!valid)
-                                vw[i >> 1] &= (i & 1) ? 0x0000ffffu : 0xffff0000u;
-                        }
-                        uint8_t *slot = sgen + L::kScl + (X & 1) * L::kSclSlot;
-                        *reinterpret_cast<float4 *>(slot + 16 * lane) = make_float4(kf[0], kf[1], kf[2], kf[3]);
-                        *reinterpret_cast<uint2 *>(slot + 512 + 8 * lane) = make_uint2(vw[0], vw[1]); // fp16 V scales
-                        __syncwarp();
-                        if (lane == 0)
-                            ptx::mbar_arrive(bars.sc_full(X & 1));
-                    }
-                    // the next tile's factors (perhaps the next item's first)
-                    const bool last = j + 1 == w.nkt;
-                    if (!last)
-                        fetch(w, j + 1, kr, vr);
-                    else if (items.more())
-                        fetch(items.peek(), 0, kr, vr);
-                    if (!last) {
-                        ++j;
-                    } else {
-                        if (!items.more())
-                            break;
-                        w = items.next();
-                        j = 0;
-                    }
-                }
             }
         } else if (warp == kMmaWarp && lane == 0) {
             // ------------------------------------------------------------ MMA issuer
@@ -846,7 +815,6 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
         const uint32_t o_col = s_col + 128;
         const float sl2 = p.scale_log2;
         uint32_t ns = 0, no = 0; // S tiles and items of this query tile so far (parities)
-        int X0 = 0;              // global index of the current item's key tile 0
         bool ok = true;
 
         while (ok && items.more()) {
@@ -862,11 +830,6 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 if (!(ok = wwait(bars.s_full(t), ns & 1)))
                     break;
                 ns ^= 1;
-                const int Xj = X0 + j;
-                if constexpr (I8) {
-                    if (!(ok = wwait(bars.sc_full(Xj & 1), (Xj >> 1) & 1)))
-                        break;
-                }
                 ptx::tc_fence_after();
                 const int lim = limit - j * 128; // columns this row sees in this tile
                 // the whole score row in registers: one TMEM round trip per tile
@@ -875,25 +838,6 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 for (int q = 0; q < 4; ++q)
                     ptx::tmem_ld32(s_col + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
                 ptx::tmem_wait_ld();
-                const float *fac = reinterpret_cast<const float *>(sgen + L::kScl + (Xj & 1) * L::kSclSlot);
-                if constexpr (I8) {
-                    // K scale after the dot product: column c times k_scale[c] * scale * log2 e
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const float4 f = reinterpret_cast<const float4 *>(fac)[q];
-                        float a0, a1, a2, a3;
-                        ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(sr[4 * q]), __uint_as_float(sr[4 * q + 1])),
-                                                  ptx::f2(f.x, f.y)),
-                                      a0, a1);
-                        ptx::f2_split(ptx::f2_mul(ptx::f2(__uint_as_float(sr[4 * q + 2]), __uint_as_float(sr[4 * q + 3])),
-                                                  ptx::f2(f.z, f.w)),
-                                      a2, a3);
-                        sr[4 * q] = __float_as_uint(a0);
-                        sr[4 * q + 1] = __float_as_uint(a1);
-                        sr[4 * q + 2] = __float_as_uint(a2);
-                        sr[4 * q + 3] = __float_as_uint(a3);
-                    }
-                }
                 if (lim < 128) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
@@ -912,7 +856,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                                            : fmaxf(m8[i], __uint_as_float(sr[16 * i + c]));
                 const float mx = fmaxf(fmaxf(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5])),
                                        fmaxf(m8[6], m8[7]));
-                const float mt = I8 ? mx : mx * sl2; // INT8: the factors already hold scale * log2 e
+                const float mt = mx * sl2;
                 float alpha = 1.f;
                 bool rescale = false;
                 if (row_valid && (mt > m_ref + kRescaleThreshold || (m_ref == -INFINITY && mt != -INFINITY))) {
@@ -923,11 +867,10 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                     m_ref = m_new;
                 }
                 // P = 2^(s * scale * log2 e - m) as bf16 pairs written over S; row sum
-                const uint64_t sl2x2 = I8 ? ptx::f2(1.f, 1.f) : ptx::f2(sl2, sl2);
+                const uint64_t sl2x2 = ptx::f2(sl2, sl2);
                 const float negm = m_ref == -INFINITY ? 0.f : -m_ref;
                 const uint64_t negm2 = ptx::f2(negm, negm);
                 uint64_t sum2[4] = {ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f), ptx::f2(0.f, 0.f)};
-                uint4 vs8 = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) { // two halves: P columns 32h..32h+31 hold keys 64h..64h+63
                     uint32_t pk[32];
@@ -938,14 +881,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                             ptx::f2_fma(ptx::f2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2), x0, x1);
                         const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1); // masked columns: 2^-inf = 0
                         sum2[(c >> 1) & 3] = ptx::f2_add(sum2[(c >> 1) & 3], ptx::f2(e0, e1));
-                        if constexpr (I8) { // V scale folded into P; the row sum keeps the unscaled P
-                            if ((c & 7) == 0) // 8 fp16 V scales
-                                vs8 = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint8_t *>(fac) + 512 + 2 * c);
-                            const uint32_t vsw = (c & 7) == 0 ? vs8.x : (c & 7) == 2 ? vs8.y : (c & 7) == 4 ? vs8.z : vs8.w;
-                            pk[(c >> 1) & 31] = ptx::mul_f16x2(ptx::pack_f16(e0, e1), vsw);
-                        } else {
-                            pk[(c >> 1) & 31] = ptx::pack_bf16(e0, e1);
-                        }
+                        pk[(c >> 1) & 31] = I8 ? ptx::pack_f16(e0, e1) : ptx::pack_bf16(e0, e1);
                     }
                     ptx::tmem_st32(s_col + 32 * h, pk);
                 }
@@ -975,7 +911,6 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 if (lane == 0)
                     ptx::mbar_arrive(bars.p_full(t));
             }
-            X0 += w.nkt;
             items.fetch();
             if (!ok || ntile == 0)
                 continue;
