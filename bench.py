@@ -40,7 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # of the 64 sequences, scaled by 4 (traffic grows with the sequences).  Must be
 # re-captured (or set to None) whenever one of these kernels changes.
 NCU_TRAFFIC = {"qwen25": {"prefill": 232.5e6, "decode": 4.334e9}}
-NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": None, "decode": 2.214e9}}
+NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": 211.4e6, "decode": 2.214e9}}
 
 
 def parse():
