@@ -1,9 +1,10 @@
 """INT8 prefill on the GPU against the oracle's attention over the dequantised cache.
 
 Method: "面试问答准备: nano-vLLM 推理引擎优化", Q3 — per-(token, KV head) INT8
-codes with fp16 scales; the prefill reads the codes directly (key scale after
-the dot product, value scale folded into the softmax weights).  Tolerances
-as for the bf16 path: max |err| <= 2e-2, relative RMS <= 1e-2.
+codes with fp16 scales, dequantised inside the kernel (each code tile turned
+once into fp16 code x token scale for the tensor cores; no floating copy of
+the cache).  Tolerances as for the bf16 path: max |err| <= 2e-2, relative
+RMS <= 1e-2.
 """
 import numpy as np
 import pytest
@@ -119,6 +120,38 @@ def test_int8_prefill_single_32k_sequence_sampled():
                               cached=None, device="cuda")
     (batch, out, ref, sel), = _run_both(w, row_select=lambda b: sample_rows(b, 24, seed=9))
     assert_close(out, ref, rows=sel, what="int8 single 32k prefill (sampled rows)")
+
+
+def test_int8_prefill_and_decode_over_mixed_token_magnitudes():
+    """Tokens whose K/V magnitudes span 1e-4 .. 3 (scales down to ~1e-6, so that fp16
+    code x scale products fall in the subnormal range) and all-zero tokens (scale 0):
+    a prefill over them, then a decode of each sequence's last token."""
+    hq, hkv, d, bs = 8, 2, 128, 16
+    lens = np.array([300, 77, 129], np.int32)
+    nb = int(sum(-(-l // bs) for l in lens)) + 3
+    perm = np.random.default_rng(31).permutation(nb).astype(np.int32)
+    blocks, o = [], 0
+    for l in lens:
+        n = -(-int(l) // bs)
+        blocks.append(perm[o:o + n])
+        o += n
+    g = torch.Generator(device="cuda").manual_seed(32)
+
+    def kv(*shape):  # rows scaled by 10^U(-4, 0.5) per (token, head); one row in 9 all zero
+        x = torch.randn(*shape, device="cuda", generator=g)
+        mag = 10.0 ** (torch.rand(*shape[:-1], 1, device="cuda", generator=g) * 4.5 - 4.0)
+        zero = torch.rand(*shape[:-1], 1, device="cuda", generator=g) < 1 / 9
+        return (x * mag).masked_fill(zero, 0.0).to(torch.bfloat16)
+
+    pool = workloads.Pool(nb, bs, hkv, d, kv(nb, bs, hkv, d), kv(nb, bs, hkv, d))
+    t = int(lens.sum())
+    q = torch.randn(t, hq, d, device="cuda", generator=g).to(torch.bfloat16)
+    pre = workloads.Batch("prefill", lens, lens.copy(), blocks, q, kv(t, hkv, d), kv(t, hkv, d), hq, d ** -0.5)
+    last = np.cumsum(lens) - 1
+    dec = workloads.Batch("decode", lens, np.ones(3, np.int32), blocks, pre.q[last], pre.k[last], pre.v[last], hq,
+                          d ** -0.5)
+    for batch, out, ref, _ in _run_both(workloads.Workload("int8_magnitudes", pool, [pre, dec])):
+        assert_close(out, ref, what=f"int8 mixed magnitudes {batch.kind}")
 
 
 def test_int8_prefill_matches_int8_decode():
