@@ -436,6 +436,39 @@ class Clocks:
 # ---------------------------------------------------------------- CPU oracle legs
 
 
+def copy_blocks_roofline(device, stream, hbm_peak, peak_src, iters=20, warmup=3):
+    """Copy-on-write block copies (row f4) against the HBM roofline.
+
+    8192 full-block copies (Qwen2.5 layout: block 16, 4 KV heads, D 128) between two
+    halves of a scratch pool of 16384 blocks, src and dst permuted: 256 MB read and
+    256 MB written per launch, so no launch is served from L2.  Work = bytes read +
+    bytes written, like the copy-bandwidth peak it is compared with.
+    """
+    from paged_kv_cache_kvcache_gb300 import pagedattn as pa
+    nb, bs, hkv, d, n = 16384, 16, 4, 128, 8192
+    dims = pa.make_dims(nb, bs, 28, hkv, d)
+    kc = torch.empty(nb, bs, hkv, d, dtype=torch.bfloat16, device=device).normal_()
+    vc = torch.empty_like(kc).normal_()
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(5)).to(torch.int32)
+    trip = torch.stack([perm[:n], perm[n:], torch.full((n,), bs, dtype=torch.int32)], 1).contiguous().to(device)
+    for _ in range(warmup):
+        pa.pa_copy_blocks(dims, kc, vc, trip, stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for a, b in evs:
+        a.record(stream)
+        pa.pa_copy_blocks(dims, kc, vc, trip, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    work = 2.0 * n * bs * hkv * d * 2 * 2  # K and V rows, read and written
+    gbs = work / (ms * 1e-3) / 1e9
+    return {"kernel": "pa_copy_blocks (copy_blocks_kernel)", "bound": "hbm", "achieved": round(gbs, 1),
+            "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "peak_source": f"{peak_src} hbm_gbs",
+            "traffic": None, "work_per_launch": work, "ms_per_launch": round(ms, 5),
+            "workload": "8192 full-block copies (block 16, 4 KV heads, D 128), 256 MB read + 256 MB written"}
+
+
 def oracle_prefill_sample(wp, row_stride, threads=0):
     """Oracle on every row_stride-th query row of the prefill batch; returns (seconds, flops)."""
     import oracle
@@ -588,6 +621,9 @@ def main():
               "work_per_launch": dbytes, "ms_per_launch": round(t_decode_kernel, 5)}
     dominant = roof_p if t_prefill_kernel >= t_decode_kernel else roof_d
     rooflines = [roof_p, roof_d]
+    if args.phase == "both" and args.decode_path == "store+decode" and args.kv == "bf16":
+        with torch.cuda.stream(stream):
+            rooflines.append(copy_blocks_roofline(f"cuda:{local}", stream, hbm_peak, peak_src))
     mixed = None
     if args.decode_path == "mixed":
         # One launch holds compute-bound prefill rows and bandwidth-bound decode rows: its
