@@ -174,6 +174,13 @@ class Step:
         self.up_ev = [torch.cuda.Event(), torch.cuda.Event()]
         for e in self.up_ev:
             e.record(stream)
+        # run(): each step's metadata is packed and uploaded on a copy stream while the
+        # previous step computes; plan_free[k] marks the last kernel that read slot k's images
+        self.cs = torch.cuda.Stream(device=stream.device)
+        self.plan_free = [torch.cuda.Event(), torch.cuda.Event()]
+        for e in self.plan_free:
+            e.record(stream)
+        self.staged = [False, False]
         self.ws = pa.decode_workspace(self.plans_d[0])
         self.pipe_ev = {"p": [torch.cuda.Event(), torch.cuda.Event()], "d": [torch.cuda.Event(), torch.cuda.Event()]}
         for evs_ in self.pipe_ev.values():
@@ -240,19 +247,45 @@ class Step:
                                 stream=s)
             pa.pa_decode(self.dims_d, q, self.kc_d, self.vc_d, plan, self.bd.scale, out, self.ws, stream=s)
 
+    def _stage(self, k, phase):
+        """Pack slot k's metadata images on the host and upload them on the copy stream."""
+        pa = self.pa
+        self.up_ev[k].synchronize()  # the pinned images of slot k are free (their last upload is done)
+        if self.mixed:
+            plans = [pa.pa_pack_prefill(self.dims_m, self.bm.seq_lens, self.bm.query_lens, self.blocks_m,
+                                        into=self.plans_m[k])]
+        else:
+            plans = []
+            if phase != "decode":
+                plans.append(pa.pa_pack_prefill(self.dims_p, self.bp.seq_lens, self.bp.query_lens, self.blocks_p,
+                                                into=self.plans_p[k]))
+            if phase != "prefill":
+                plans.append(pa.pa_pack_decode(self.dims_d, self.bd.seq_lens, self.blocks_d, into=self.plans_d[k]))
+        self.cs.wait_event(self.plan_free[k])  # no kernel still reads slot k's device images
+        for plan in plans:
+            plan.upload(stream=self.cs)
+        self.up_ev[k].record(self.cs)
+        self.staged[k] = True
+
     def run(self, ev=None, phase="both"):
-        """Enqueue one step; ev = dict of event pairs for per-phase timing."""
+        """Enqueue one step; ev = dict of event pairs for per-phase timing.
+
+        The step's metadata (pack + upload) was staged on the copy stream while the
+        previous step computed; the compute stream waits for it inside the prefill
+        phase (so an upload that is late shows in the phase's time).
+        """
         pa, s = self.pa, self.s
         k = self.i & 1
         self.i += 1
-        self.up_ev[k].synchronize()
+        if not self.staged[k]:
+            self._stage(k, phase)
+        self.staged[k] = False
         rec = (lambda name: ev[name].record(s)) if ev is not None else (lambda name: None)
         # ---- prefill phase
         rec("p0")
+        s.wait_event(self.up_ev[k])
         if self.mixed:  # both phases' rows: one store, one prefill launch; the decode phase stays empty
-            plan_m = pa.pa_pack_prefill(self.dims_m, self.bm.seq_lens, self.bm.query_lens, self.blocks_m,
-                                        into=self.plans_m[k]).upload(stream=s)
-            self.up_ev[k].record(s)
+            plan_m = self.plans_m[k]
             pa.pa_store_kvcache(self.dims_m, self.bm.k, self.bm.v, self.kc_m, self.vc_m, plan_m.slot_mapping,
                                 self.bm.num_tokens, stream=s)
             rec("pk0")
@@ -260,13 +293,17 @@ class Step:
                                  stream=s)
             for n in ("pk1", "p1", "dk0", "dk1", "d1"):
                 rec(n)
+            self.plan_free[k].record(s)
+            self._stage(1 - k, phase)
             return
         if phase == "decode":
             for n in ("pk0", "pk1", "p1"):
                 rec(n)
-            return self._decode(ev, k, rec)
-        plan_p = pa.pa_pack_prefill(self.dims_p, self.bp.seq_lens, self.bp.query_lens, self.blocks_p,
-                                    into=self.plans_p[k]).upload(stream=s)
+            self._decode(ev, k, rec)
+            self.plan_free[k].record(s)
+            self._stage(1 - k, phase)
+            return
+        plan_p = self.plans_p[k]
         if self.int8:
             pa.pa_store_kvcache_int8(self.dims_p, self.bp.k, self.bp.v, *self.c8_p, plan_p.slot_mapping,
                                      self.bp.num_tokens, stream=s)
@@ -284,14 +321,15 @@ class Step:
         if phase == "prefill":
             for n in ("dk0", "dk1", "d1"):
                 rec(n)
-            return
-        self._decode(ev, k, rec)
+        else:
+            self._decode(ev, k, rec)
+        self.plan_free[k].record(s)
+        self._stage(1 - k, phase)
 
     def _decode(self, ev, k, rec):
         pa, s = self.pa, self.s
-        # ---- decode phase
-        plan_d = pa.pa_pack_decode(self.dims_d, self.bd.seq_lens, self.blocks_d, into=self.plans_d[k]).upload(stream=s)
-        self.up_ev[k].record(s)
+        # ---- decode phase (its metadata image was uploaded with the prefill's)
+        plan_d = self.plans_d[k]
         if self.int8 and self.fused:  # quantising store + INT8 decode in one launch
             rec("dk0")
             pa.pa_decode_int8_fused(self.dims_d, self.bd.q, self.bd.k, self.bd.v, *self.c8_d, plan_d, self.bd.scale,
