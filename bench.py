@@ -41,6 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # re-captured (or set to None) whenever one of these kernels changes.
 NCU_TRAFFIC = {"qwen25": {"prefill": 232.2e6, "decode": 4.334e9}}
 NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": 211.4e6, "decode": 2.214e9}}
+NCU_TRAFFIC_FUSED_PREFILL = {"qwen25": 266.9e6}
 
 
 def parse():
@@ -62,6 +63,8 @@ def parse():
     ap.add_argument("--kv", choices=["bf16", "int8"], default="bf16",
                     help="cache format: bf16, or int8 codes + fp16 scales (quantising store, fused-dequant "
                          "prefill and decode)")
+    ap.add_argument("--prefill-path", choices=["store+prefill", "fused"], default="fused",
+                    help="bf16 prompt batch: pa_store_kvcache + pa_prefill_varlen, or pa_prefill_varlen_fused")
     ap.add_argument("--decode-path", choices=["store+decode", "fused", "mixed"], default="store+decode",
                     help="fused: store and decode in one launch (pa_decode_fused / pa_decode_int8_fused); "
                          "mixed (bf16): the decode rows join the prefill rows as Lq = 1 varlen rows of one "
@@ -150,11 +153,12 @@ def mixed_batch(wp, wd):
 class Step:
     """Device-resident state of one replica and the calls of one step."""
 
-    def __init__(self, wp, wd, stream, kv="bf16", fused=False, mixed=False):
+    def __init__(self, wp, wd, stream, kv="bf16", fused=False, mixed=False, prefill_fused=False):
         from paged_kv_cache_kvcache_gb300 import pagedattn as pa
         self.pa = pa
         self.s = stream
         self.int8, self.fused, self.mixed = kv == "int8", fused, mixed
+        self.prefill_fused = prefill_fused and not self.int8 and not mixed
         self.wp, self.wd = wp, wd
         self.bp, self.bd = wp.batches[0], wd.batches[0]
         pp, pd = wp.pool, wd.pool
@@ -188,6 +192,8 @@ class Step:
                 e.record(stream)
         self.i = 0
         self.launches_per_step = 4 + (1 if self.plans_d[0].meta.num_partials > 0 else 0) - (1 if fused else 0)
+        if self.prefill_fused and self.plans_p[0].meta.prefix_aligned:
+            self.launches_per_step -= 1
         if mixed:  # one launch for both phases' rows, over one pool
             self.kc_m, self.vc_m, self.bm = mixed_batch(wp, wd)
             self.dims_m = pa.make_dims(self.kc_m.shape[0], pp.block_size, self.bm.num_heads, pp.num_kv_heads,
@@ -223,6 +229,8 @@ class Step:
         if self.int8:
             pa.pa_store_kvcache_int8(self.dims_p, k, v, *self.c8_p, plan.slot_mapping, self.bp.num_tokens, stream=s)
             pa.pa_prefill_varlen_int8(self.dims_p, q, *self.c8_p, plan, self.bp.scale, out, stream=s)
+        elif self.prefill_fused:
+            pa.pa_prefill_varlen_fused(self.dims_p, q, k, v, self.kc_p, self.vc_p, plan, self.bp.scale, out, stream=s)
         else:
             pa.pa_store_kvcache(self.dims_p, k, v, self.kc_p, self.vc_p, plan.slot_mapping, self.bp.num_tokens,
                                 stream=s)
@@ -310,6 +318,10 @@ class Step:
             rec("pk0")
             pa.pa_prefill_varlen_int8(self.dims_p, self.bp.q, *self.c8_p, plan_p, self.bp.scale, self.out_p,
                                       stream=s)
+        elif self.prefill_fused:  # store + prefill in one launch: the kernel time includes the store
+            rec("pk0")
+            pa.pa_prefill_varlen_fused(self.dims_p, self.bp.q, self.bp.k, self.bp.v, self.kc_p, self.vc_p, plan_p,
+                                       self.bp.scale, self.out_p, stream=s)
         else:
             pa.pa_store_kvcache(self.dims_p, self.bp.k, self.bp.v, self.kc_p, self.vc_p, plan_p.slot_mapping,
                                 self.bp.num_tokens, stream=s)
@@ -566,7 +578,7 @@ def main():
     clocks = Clocks(local, enabled=not args.no_clocks)
     with torch.cuda.stream(stream):
         step = Step(wp, wd, stream, kv=args.kv, fused=args.decode_path == "fused",
-                    mixed=args.decode_path == "mixed")
+                    mixed=args.decode_path == "mixed", prefill_fused=args.prefill_path == "fused")
         names = ["p0", "pk0", "pk1", "p1", "dk0", "dk1", "d1"]
         for _ in range(args.warmup):
             step.run(phase=args.phase)
@@ -640,8 +652,11 @@ def main():
     int8 = args.kv == "int8"
     traffic = {} if args.decode_path in ("fused", "mixed") else \
         (NCU_TRAFFIC_INT8 if int8 else NCU_TRAFFIC).get(args.workload, {})
+    if step.prefill_fused:
+        traffic = {"prefill": NCU_TRAFFIC_FUSED_PREFILL.get(args.workload), "decode": traffic.get("decode")}
     roof_p = {"kernel": ("pa_prefill_varlen_int8 (prefill_kernel<128,true>, f16 MMAs)" if int8 else
-                         "pa_prefill_varlen (prefill_kernel<128,false>)"),
+                         "pa_prefill_varlen_fused (prefill_kernel<128,false>, store of the new K/V fused)"
+                         if step.prefill_fused else "pa_prefill_varlen (prefill_kernel<128,false>)"),
               "bound": "tensor", "achieved": round(pk_tflops, 2),
               "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(pk_tflops / bf16_peak, 4),
               "peak_source": f"{peak_src} bf16_tflops (burst; f16 has the same nominal rate)",
@@ -707,7 +722,7 @@ def main():
         "config": {"workload": wl_desc, "l2": "inputs larger than L2: the decode phase streams "
                    f"{dbytes / 1e9:.2f} GB per step", "prefill_gflop": round(flops / 1e9, 2),
                    "decode_kv_gb": round(dbytes / 1e9, 3), "parallelism": f"replicas x{world}", "kv": args.kv,
-                   "decode_path": args.decode_path},
+                   "decode_path": args.decode_path, "prefill_path": "fused" if step.prefill_fused else "store+prefill"},
         "decode": {"value": round(decode_gbs, 1), "unit": "GB/s", "frac_of_hbm": round(decode_gbs / hbm_peak, 4),
                    "seqs_per_s": round(step.bd.num_seqs / (t_decode_phase * 1e-3) * world, 1)},
         "prefill": {"tokens_per_s": round(step.bp.num_tokens / (t_prefill_phase * 1e-3) * world, 1),

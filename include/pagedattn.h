@@ -74,7 +74,9 @@ typedef struct pa_prefill_meta {
     int32_t num_tiles;          /* work items = CTAs of the prefill launch */
     int32_t rows_per_tile;      /* query positions per query tile (128 / group, floored);
                                    a work item covers two query tiles */
-    int32_t reserved;
+    int32_t prefix_aligned;     /* 1 if every cached prefix (seq_len - query_len) is a
+                                   multiple of min(block_size, 128): pa_prefill_varlen_fused
+                                   then runs as one launch */
     uint64_t off_cu_seqlens_q;  /* int32 [num_seqs+1] */
     uint64_t off_cu_seqlens_k;  /* int32 [num_seqs+1] */
     uint64_t off_block_tables;  /* int32 [num_seqs][max_blocks_per_seq], -1 padded */
@@ -181,6 +183,30 @@ int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache,
                       const int32_t *cu_seqlens_k, const int32_t *block_tables, float scale,
                       void *out, const pa_prefill_meta *meta, const int32_t *tiles,
                       pa_stream_t stream);
+
+/*
+ * pa_prefill_varlen_fused — pa_store_kvcache of the new tokens followed by
+ * pa_prefill_varlen, with the same result, in one launch when the plan allows
+ * (meta->prefix_aligned; otherwise the two launches run in that order).
+ * Source: "手搓 vLLM 推理引擎", Step 4 (store_kvcache, then attention over the
+ * cache).  In the fused launch the prefill reads the new tokens' keys and
+ * values from k and v themselves (the same bf16 values the store writes) and
+ * the cached prefix from the cache, while one warp of each CTA copies the rows
+ * of its work item's query positions into their slots (each (token, KV head)
+ * row by exactly one item).
+ *   k, v:          device bf16 [meta->total_q][num_kv_heads][head_dim], row t
+ *                  the key/value of packed query row t
+ *   slot_mapping:  device int32 [meta->total_q] (dev + meta->off_slot_mapping);
+ *                  -1 skips the row, a slot outside [-1, num_blocks*block_size)
+ *                  is skipped and flagged (pa_read_device_error bit 0)
+ * The new tokens' slots must not hold keys that a sequence of the call reads
+ * from the cache (true of any slot mapping a block allocator produces).
+ * Other arguments, errors and numerics as pa_prefill_varlen.
+ */
+int pa_prefill_varlen_fused(const pa_dims *dims, const void *q, const void *k, const void *v, void *k_cache,
+                            void *v_cache, const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            const int32_t *block_tables, const int32_t *slot_mapping, float scale, void *out,
+                            const pa_prefill_meta *meta, const int32_t *tiles, pa_stream_t stream);
 
 /*
  * pa_decode — batched single-token GQA decode over the paged cache.

@@ -153,6 +153,33 @@ extern "C" int pa_prefill_varlen(const pa_dims *dims, const void *q, const void 
     return launch_prefill(a, stream);
 }
 
+extern "C" int pa_prefill_varlen_fused(const pa_dims *dims, const void *q, const void *k, const void *v,
+                                       void *k_cache, void *v_cache, const int32_t *cu_seqlens_q,
+                                       const int32_t *cu_seqlens_k, const int32_t *block_tables,
+                                       const int32_t *slot_mapping, float scale, void *out,
+                                       const pa_prefill_meta *meta, const int32_t *tiles, pa_stream_t stream)
+{
+    PrefillArgs a;
+    bool nothing = false;
+    int rc = prepare_prefill("pa_prefill_varlen_fused", dims, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                             block_tables, scale, out, meta, tiles, &a, &nothing);
+    if (rc != PA_OK || nothing)
+        return rc;
+    if (!k || !v || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_fused: NULL pointer");
+    if (misaligned(k) || misaligned(v))
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_fused: tensors must be 16-byte aligned");
+    if (!meta->prefix_aligned) { // a key box would straddle a cached prefix: store, then prefill
+        if ((rc = launch_store_kvcache(*dims, k, v, k_cache, v_cache, slot_mapping, meta->total_q, stream)) != PA_OK)
+            return rc;
+        return launch_prefill(a, stream);
+    }
+    a.k_in = k;
+    a.v_in = v;
+    a.slot_mapping = slot_mapping;
+    return launch_prefill(a, stream);
+}
+
 extern "C" int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
                                       const void *k_scale, const void *v_scale, const int32_t *cu_seqlens_q,
                                       const int32_t *cu_seqlens_k, const int32_t *block_tables, float scale,

@@ -103,6 +103,10 @@ struct PrefillArgs {
     int32_t total_q;
     int32_t max_blocks_per_seq;
     int32_t rows_per_tile;
+    // fused store (bf16 only; NULL otherwise): new tokens' K/V [total_q][Hkv][D] and their slots
+    const void *k_in;
+    const void *v_in;
+    const int32_t *slot_mapping;
 };
 int launch_prefill(const PrefillArgs &a, void *stream);
 int launch_prefill_int8(const PrefillArgs &a, void *stream);

@@ -144,7 +144,14 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
     meta->max_blocks_per_seq = mb;
     meta->num_tiles = (int32_t)tiles.size();
     meta->rows_per_tile = rows;
-    meta->reserved = 0;
+    // the fused store + prefill reads the new keys from the inputs in boxes of min(block
+    // size, 128) keys: possible when no box straddles a cached prefix and the new keys
+    int32_t aligned = 1;
+    const int32_t box = std::min<int32_t>(d.block_size, kPrefillKeyTile);
+    for (int32_t b = 0; b < num_seqs; ++b)
+        if ((seq_lens[b] - query_lens[b]) % box != 0)
+            aligned = 0;
+    meta->prefix_aligned = aligned;
     meta->off_cu_seqlens_q = L.take(sizeof(int32_t) * (num_seqs + 1));
     meta->off_cu_seqlens_k = L.take(sizeof(int32_t) * (num_seqs + 1));
     meta->off_block_tables = L.take(sizeof(int32_t) * (size_t)num_seqs * mb);

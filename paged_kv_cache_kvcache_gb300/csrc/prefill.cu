@@ -72,7 +72,7 @@
 
 namespace pa {
 
-__device__ uint32_t g_prefill_error; // bit 0: a bounded wait timed out
+__device__ uint32_t g_prefill_error; // bit 0: a bounded wait timed out; bit 1: the fused store met a bad slot
 
 namespace {
 
@@ -161,6 +161,14 @@ struct PfParams {
     int32_t num_kv_heads;
     const __half *k_scale; // INT8 cache only: fp16 [num_blocks][num_kv_heads][block_size]
     const __half *v_scale;
+    // fused store (bf16): the new tokens' K/V rows are read from k_in/v_in (tensor maps
+    // tm_kin/tm_vin) instead of the cache, and written into the cache at slot_mapping
+    int32_t fused;
+    const int32_t *slot_mapping;
+    const uint4 *k_in;
+    const uint4 *v_in;
+    uint4 *k_cache;
+    uint4 *v_cache;
 };
 
 // barrier slots (uint64 each) inside the barrier area
@@ -362,6 +370,45 @@ __device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int lane)
     }
 }
 
+// Fused store: the new K/V rows of item w's query positions, KV head w.g, copied
+// from the inputs to their cache slots (one warp; each (token, KV head) row
+// belongs to exactly one item).  The kernel itself reads the new keys from the
+// inputs, so nothing here is waited for.
+template <int D>
+__device__ __forceinline__ void store_item_rows(const PfParams &p, const Item &w, int lane)
+{
+    constexpr int VPR = D / 8; // 16-byte vectors per row of one head
+    constexpr int kU = 4;      // vectors of K and of V in flight per lane
+    const int total = (w.npos0 + w.npos1) * VPR;
+    const size_t hkv = (size_t)p.num_kv_heads;
+    for (int i0 = lane; i0 < total; i0 += 32 * kU) {
+        uint4 kx[kU], vx[kU];
+        size_t to[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + 32 * u;
+            to[u] = ~(size_t)0;
+            if (i < total) {
+                const int row = w.cq0 + w.q0 + i / VPR;
+                const int slot = __ldg(p.slot_mapping + row);
+                const size_t from = ((size_t)row * hkv + w.g) * VPR + i % VPR;
+                kx[u] = __ldg(p.k_in + from);
+                vx[u] = __ldg(p.v_in + from);
+                if (slot >= 0 && slot < p.num_slots)
+                    to[u] = ((size_t)slot * hkv + w.g) * VPR + i % VPR;
+                else if (slot != -1)
+                    atomicOr(&g_prefill_error, 2u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (to[u] != ~(size_t)0) {
+                p.k_cache[to[u]] = kx[u];
+                p.v_cache[to[u]] = vx[u];
+            }
+    }
+}
+
 // Rows G*P..127 of each query tile receive no TMA data: zero them once so their
 // (discarded) scores stay finite and cost the same as real rows.
 template <int D, bool I8>
@@ -407,7 +454,8 @@ __device__ __forceinline__ void prefetch_query_tiles(const CUtensorMap *tm_q, co
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PfParams p)
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kin,
+                   const __grid_constant__ CUtensorMap tm_vin, const PfParams p)
 {
     using L = PfLayout<D, I8>;
     // per-thread register budgets after the hand-over (bf16 variant)
@@ -529,11 +577,16 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
         const int bs = p.block_size;
         const int box_rows = bs < 128 ? bs : 128;
         const int nsub = 128 / box_rows;
-        // row coordinate of sub-box `lane` of key tile j of item w (one TMA box per lane)
+        // row coordinate of sub-box `lane` of key tile j of item w (one TMA box per lane):
+        // a cache row, or -(r + 1) for row r of the new keys' input (fused store; a box
+        // never straddles the cached prefix and the new keys, the host checks)
         auto sub_row = [&](const Item &w, const int32_t *bt, int j) -> int {
             const int key = j * 128 + lane * box_rows;
             if (lane >= nsub || key >= w.lk)
                 return p.num_slots; // fully out of range: TMA fills zeros
+            const int off = w.lk - w.lq; // cached prefix
+            if (p.fused && key >= off)
+                return -(w.cq0 + key - off + 1);
             const int phys = __ldg(bt + key / bs);
             return phys * bs + (key & (bs - 1));
         };
@@ -556,6 +609,8 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 }
                 if (ok && lane == 0 && items.more())
                     prefetch_query_tiles<D, I8>(&tm_q, items.peek(), G, P);
+                if (ok && p.fused)
+                    store_item_rows<D>(p, w, lane);
             }
         } else if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
             // ------------------------------------------------------------ bf16: K and V producers
@@ -564,8 +619,12 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             const int nstages = is_k ? L::kKStages : L::kVStages;
             const uint32_t ring = sbase + (is_k ? L::kK : L::kV);
             const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
-            if (lane == 0)
+            const CUtensorMap *tm_in = is_k ? &tm_kin : &tm_vin;
+            if (lane == 0) {
                 ptx::prefetch_tmap(tm);
+                if (p.fused)
+                    ptx::prefetch_tmap(tm_in);
+            }
             uint32_t starts = 0; // bit i: global key tile X - i opens its item
             int X = 0;           // global key tile (this CTA, all items)
             bool ok = true;
@@ -589,11 +648,14 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                     const uint32_t dst = ring + st * L::kTileBytes;
                     if (lane == 0)
                         ptx::mbar_arrive_expect_tx(full, (uint32_t)L::kTileBytes);
-                    // lane i issues the boxes of sub-box i (its own row coordinate)
-                    if (lane < nsub)
+                    // lane i issues the boxes of sub-box i (its own row coordinate and source)
+                    if (lane < nsub) {
+                        const CUtensorMap *src = cur < 0 ? tm_in : tm;
+                        const int row = cur < 0 ? -cur - 1 : cur;
                         for (int pp = 0; pp < L::kPanels; ++pp)
-                            ptx::tma_load_3d(dst + pp * L::kPanelBytes + lane * box_rows * 128, tm, full, pp * 64,
-                                             w.g, cur);
+                            ptx::tma_load_3d(dst + pp * L::kPanelBytes + lane * box_rows * 128, src, full, pp * 64,
+                                             w.g, row);
+                    }
                     __syncwarp();
                     if (!is_k && w.tail && j == w.nkt - 1) {
                         // V rows of keys past the sequence end may hold anything (even NaN
@@ -1018,6 +1080,15 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
                                  (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "v_cache")) != PA_OK)
             return rc;
     }
+    CUtensorMap tkin = tk, tvin = tv; // fused store: the new keys' inputs, same box as the cache's
+    if (!I8 && a.k_in) {
+        if ((rc = encode_tmap_3d(&tkin, bf16, a.k_in, D, d.num_kv_heads, (uint64_t)a.total_q, (uint64_t)D * 2,
+                                 (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "k")) != PA_OK)
+            return rc;
+        if ((rc = encode_tmap_3d(&tvin, bf16, a.v_in, D, d.num_kv_heads, (uint64_t)a.total_q, (uint64_t)D * 2,
+                                 (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "v")) != PA_OK)
+            return rc;
+    }
     PfParams p{};
     p.cu_seqlens_q = a.cu_seqlens_q;
     p.cu_seqlens_k = a.cu_seqlens_k;
@@ -1036,12 +1107,18 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     p.v_scale = static_cast<const __half *>(a.v_scale);
     p.num_items = a.num_tiles;
     p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
+    p.fused = !I8 && a.k_in ? 1 : 0;
+    p.slot_mapping = a.slot_mapping;
+    p.k_in = static_cast<const uint4 *>(a.k_in);
+    p.v_in = static_cast<const uint4 *>(a.v_in);
+    p.k_cache = static_cast<uint4 *>(const_cast<void *>(a.k_cache));
+    p.v_cache = static_cast<uint4 *>(const_cast<void *>(a.v_cache));
     // persistent: one CTA per SM (shared memory and TMEM admit one), each walking its items
     int sms = 0;
     if (int rc2 = sm_count(&sms))
         return rc2;
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-    prefill_kernel<D, I8><<<(unsigned)grid, kThreadsOf<I8>, L::kSmemBytes, stream>>>(tq, tk, tv, p);
+    prefill_kernel<D, I8><<<(unsigned)grid, kThreadsOf<I8>, L::kSmemBytes, stream>>>(tq, tk, tv, tkin, tvin, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
@@ -1070,7 +1147,8 @@ int read_prefill_error(uint32_t *code)
         e = cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof zero);
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "reading prefill error word: %s", cudaGetErrorString(e));
-    *code |= v << 1;
+    *code |= (v & 1u) << 1; // a bounded wait timed out
+    *code |= (v & 2u) >> 1; // the fused store met a slot outside [-1, num_slots): the store's bit
     return PA_OK;
 }
 

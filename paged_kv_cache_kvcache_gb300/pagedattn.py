@@ -23,7 +23,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
            "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
            "pa_prefill_varlen_int8", "pa_pack_decode_fixed", "pa_decode_fused", "pa_copy_blocks_int8",
-           "pa_decode_int8_fused",
+           "pa_decode_int8_fused", "pa_prefill_varlen_fused",
            "pa_last_error_string", "pa_read_device_error", "pa_selftest_bounded_wait", "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
@@ -37,7 +37,7 @@ class pa_dims(ctypes.Structure):
 class pa_prefill_meta(ctypes.Structure):
     _fields_ = [("num_seqs", ctypes.c_int32), ("total_q", ctypes.c_int32), ("max_seqlen_q", ctypes.c_int32),
                 ("max_seqlen_k", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
-                ("num_tiles", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("num_tiles", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32), ("prefix_aligned", ctypes.c_int32),
                 ("off_cu_seqlens_q", ctypes.c_uint64), ("off_cu_seqlens_k", ctypes.c_uint64),
                 ("off_block_tables", ctypes.c_uint64), ("off_slot_mapping", ctypes.c_uint64),
                 ("off_tiles", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
             L.pa_upload.argtypes = [P, P, SZ, P]
             L.pa_store_kvcache.argtypes = [P, P, P, P, P, P, I32, P]
             L.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
+            L.pa_prefill_varlen_fused.argtypes = [P, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
             L.pa_decode.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_decode_static.argtypes = [P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P]
             L.pa_copy_blocks.argtypes = [P, P, P, P, I32, P]
@@ -262,6 +263,18 @@ def pa_prefill_varlen(dims: pa_dims, q, k_cache, v_cache, plan: PrefillPlan, sca
                                    plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
                                    plan.dptr(m.off_block_tables), float(scale), _ptr(out), ctypes.byref(m),
                                    plan.dptr(m.off_tiles), _stream(stream)), "pa_prefill_varlen")
+
+
+def pa_prefill_varlen_fused(dims: pa_dims, q, k, v, k_cache, v_cache, plan: PrefillPlan, scale: float, out,
+                            stream=None):
+    """pa_store_kvcache of the new tokens' k/v at the plan's slots + pa_prefill_varlen (one launch
+    when plan.meta.prefix_aligned)."""
+    m = plan.meta
+    _check(lib().pa_prefill_varlen_fused(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+                                         plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
+                                         plan.dptr(m.off_block_tables), plan.dptr(m.off_slot_mapping), float(scale),
+                                         _ptr(out), ctypes.byref(m), plan.dptr(m.off_tiles), _stream(stream)),
+           "pa_prefill_varlen_fused")
 
 
 def decode_workspace(plan: DecodePlan, device="cuda") -> Optional[torch.Tensor]:

@@ -223,8 +223,9 @@ def random_case(seed: int, *, num_seqs: int, hq: int, hkv: int, d: int, bs: int,
     """Small random varlen case for parity sweeps.
 
     Lengths ~ U{min_len..max_len}; for prefill, the cached prefix is either 0
-    (``cached=None``) or ~ U{0..len-1}; for decode, every sequence queries its
-    last token.  Blocks are a random permutation of a pool with a few spare
+    (``cached=None``), ~ U{0..len-1} (``"random"``) or that rounded down to a
+    multiple of min(bs, 128) (``"aligned"``, whole cached blocks); for decode,
+    every sequence queries its last token.  Blocks are a random permutation of a pool with a few spare
     blocks that stay untouched (canary).
     """
     meta, vals, dev = _gens(seed, device)
@@ -235,6 +236,8 @@ def random_case(seed: int, *, num_seqs: int, hq: int, hkv: int, d: int, bs: int,
         qlens = lens.copy()
     else:
         pre = np.array([int(torch.randint(0, int(l), (1,), generator=meta)) for l in lens], np.int32)
+        if cached == "aligned":
+            pre -= pre % min(bs, 128)
         qlens = (lens - pre).astype(np.int32)
     need = [_ceil_div(int(c), bs) for c in lens]
     nb = int(sum(need)) + extra_blocks

@@ -285,3 +285,37 @@ def test_int8_fused_and_copy_calls_reject_bad_args_without_touching_the_gpu():
     dm.workspace_bytes = pa.PA_DECODE_STATIC_SCRATCH_BYTES + 256
     assert L.pa_decode_static(ctypes.byref(dims), 16, 16, 16, 16, 16, f(0.1), 16, ctypes.byref(dm), 16, 16,
                               None) == pa.PA_ERR_WORKSPACE
+
+
+def test_pack_prefill_prefix_aligned_flag():
+    """meta.prefix_aligned: every cached prefix a multiple of min(block_size, 128)."""
+    for bs, lens, qlens, expect in ((16, [40, 17], [8, 17], 1),       # prefixes 32, 0
+                                    (16, [40, 17], [9, 17], 0),       # prefix 31
+                                    (256, [300, 700], [44, 444], 1),  # prefixes 256, 256: boxes of 128
+                                    (256, [300], [172], 1),           # prefix 128: half a block, 128-aligned
+                                    (256, [300], [100], 0),           # prefix 200
+                                    (32, [64], [64], 1)):             # no prefix
+        dims = pa.make_dims(64, bs, 4, 2, 64)
+        blocks = [list(range(i * 8, i * 8 + -(-n // bs))) for i, n in enumerate(lens)]
+        plan = pa.pa_pack_prefill(dims, lens, qlens, blocks, pin=False)
+        assert plan.meta.prefix_aligned == expect, (bs, lens, qlens)
+
+
+def test_prefill_fused_rejects_bad_args_without_touching_the_gpu():
+    dims = pa.make_dims(4, 16, 4, 2, 64)
+    L = pa.lib()
+    pm = pa.pa_prefill_meta()
+    pm.num_tiles, pm.total_q, pm.num_seqs, pm.max_blocks_per_seq, pm.rows_per_tile = 1, 1, 1, 1, 64
+    f = ctypes.c_float
+    # NULL new-token rows, NULL slot mapping, misaligned rows, bad scale
+    assert L.pa_prefill_varlen_fused(ctypes.byref(dims), 16, None, 16, 16, 16, 16, 16, 16, 16, f(0.1), 16,
+                                     ctypes.byref(pm), 16, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_prefill_varlen_fused(ctypes.byref(dims), 16, 16, 16, 16, 16, 16, 16, 16, None, f(0.1), 16,
+                                     ctypes.byref(pm), 16, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_prefill_varlen_fused(ctypes.byref(dims), 16, 24, 16, 16, 16, 16, 16, 16, 16, f(0.1), 16,
+                                     ctypes.byref(pm), 16, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_prefill_varlen_fused(ctypes.byref(dims), 16, 16, 16, 16, 16, 16, 16, 16, 16, f(-1.0), 16,
+                                     ctypes.byref(pm), 16, None) == pa.PA_ERR_INVALID_ARG
+    pm.num_tiles = 0  # nothing to do: no launch, no error
+    assert L.pa_prefill_varlen_fused(ctypes.byref(dims), None, None, None, None, None, None, None, None, None, f(0.1),
+                                     None, ctypes.byref(pm), None, None) == pa.PA_OK
