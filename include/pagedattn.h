@@ -74,9 +74,10 @@ typedef struct pa_prefill_meta {
     int32_t num_tiles;          /* work items = CTAs of the prefill launch */
     int32_t rows_per_tile;      /* query positions per query tile (128 / group, floored);
                                    a work item covers two query tiles */
-    int32_t prefix_aligned;     /* 1 if every cached prefix (seq_len - query_len) is a
-                                   multiple of min(block_size, 128): pa_prefill_varlen_fused
-                                   then runs as one launch */
+    int32_t prefix_aligned;     /* 1 if the cached prefix (seq_len - query_len) of every
+                                   sequence with new tokens is a multiple of
+                                   min(block_size, 128): pa_prefill_varlen_fused then
+                                   runs as one launch */
     uint64_t off_cu_seqlens_q;  /* int32 [num_seqs+1] */
     uint64_t off_cu_seqlens_k;  /* int32 [num_seqs+1] */
     uint64_t off_block_tables;  /* int32 [num_seqs][max_blocks_per_seq], -1 padded */

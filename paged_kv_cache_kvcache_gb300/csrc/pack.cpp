@@ -148,8 +148,8 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
     // size, 128) keys: possible when no box straddles a cached prefix and the new keys
     int32_t aligned = 1;
     const int32_t box = std::min<int32_t>(d.block_size, kPrefillKeyTile);
-    for (int32_t b = 0; b < num_seqs; ++b)
-        if ((seq_lens[b] - query_lens[b]) % box != 0)
+    for (int32_t b = 0; b < num_seqs; ++b) // sequences without new tokens have no work items
+        if (query_lens[b] > 0 && (seq_lens[b] - query_lens[b]) % box != 0)
             aligned = 0;
     meta->prefix_aligned = aligned;
     meta->off_cu_seqlens_q = L.take(sizeof(int32_t) * (num_seqs + 1));

@@ -294,7 +294,8 @@ def test_pack_prefill_prefix_aligned_flag():
                                     (256, [300, 700], [44, 444], 1),  # prefixes 256, 256: boxes of 128
                                     (256, [300], [172], 1),           # prefix 128: half a block, 128-aligned
                                     (256, [300], [100], 0),           # prefix 200
-                                    (32, [64], [64], 1)):             # no prefix
+                                    (32, [64], [64], 1),              # no prefix
+                                    (16, [40, 17], [8, 0], 1)):       # prefix 17 but no new tokens
         dims = pa.make_dims(64, bs, 4, 2, 64)
         blocks = [list(range(i * 8, i * 8 + -(-n // bs))) for i, n in enumerate(lens)]
         plan = pa.pa_pack_prefill(dims, lens, qlens, blocks, pin=False)

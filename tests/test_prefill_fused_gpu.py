@@ -118,6 +118,29 @@ def test_fused_prefill_decode_rows():
     assert torch.equal(out, sep)
 
 
+def test_fused_prefill_edge_lengths():
+    """Sequences without new tokens, single tokens, exact tiles and block-aligned prefixes in one batch."""
+    hq, hkv, d, bs = 4, 2, 128, 16
+    lens = np.array([16, 17, 48, 129, 5, 128, 256], np.int32)
+    qlens = np.array([0, 1, 16, 129, 0, 128, 96], np.int32)  # prefixes 16, 16, 32, 0, -, 0, 160
+    nb = int(sum(-(-int(l) // bs) for l in lens)) + 2
+    perm = np.random.default_rng(19).permutation(nb).astype(np.int32)
+    blocks, o = [], 0
+    for l in lens:
+        n = -(-int(l) // bs)
+        blocks.append(perm[o:o + n])
+        o += n
+    g = torch.Generator(device="cuda").manual_seed(20)
+    mk = lambda *sh: torch.randn(*sh, device="cuda", generator=g).to(torch.bfloat16)
+    pool = workloads.Pool(nb, bs, hkv, d, mk(nb, bs, hkv, d), mk(nb, bs, hkv, d))
+    t = int(qlens.sum())
+    batch = workloads.Batch("prefill", lens, qlens, blocks, mk(t, hq, d), mk(t, hkv, d), mk(t, hkv, d), hq, d ** -0.5)
+    (batch, out, sep, ref, plan, _), = _run(workloads.Workload("fused_edges", pool, [batch]))
+    assert plan.meta.prefix_aligned == 1
+    assert_close(out, ref, what="fused edges")
+    assert torch.equal(out, sep)
+
+
 def test_fused_prefill_bad_slot_flagged():
     """A slot outside [-1, num_slots) is skipped and flagged (bit 0); -1 skips silently; the other
     rows are stored and the attention reads the new keys from the inputs either way."""
