@@ -59,6 +59,10 @@
 //    the tile is converted once for 2 x 128 query rows anyway, so scaling it
 //    there is one multiply per element instead of one per score (the result
 //    is the same product, rounded once more to f16).
+//  * Fused store (pa_prefill_varlen_fused, bf16): the K/V producers take the
+//    new keys' boxes from the k/v inputs instead of the cache (so nothing
+//    the launch writes is read by it), and warp 11, between its query loads,
+//    copies the K/V rows of its item's query positions into their slots.
 //  * mbarriers order every hand-off; every wait is bounded and reports a
 //    timeout through a device error word instead of hanging.
 #include <cuda.h>
