@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # this workload: the prefill launch exactly as benched; the decode kernel on 16
 # of the 64 sequences, scaled by 4 (traffic grows with the sequences).  Must be
 # re-captured (or set to None) whenever one of these kernels changes.
-NCU_TRAFFIC = {"qwen25": {"prefill": 232.2e6, "decode": 4.334e9}}
-NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": 211.4e6, "decode": 2.214e9}}
+NCU_TRAFFIC = {"qwen25": {"prefill": 232.1e6, "decode": 4.334e9}}
+NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": 210.6e6, "decode": 2.214e9}}
 NCU_TRAFFIC_FUSED_PREFILL = {"qwen25": 266.9e6}
 
 
