@@ -1,6 +1,6 @@
 """The device entry points only enqueue work: no host synchronisation inside the library.
 
-Right after pa_prefill_varlen / pa_decode return on the full-size Qwen2.5
+Right after pa_prefill_varlen (fused or not) / pa_decode return on the full-size Qwen2.5
 workloads (hundreds of microseconds of GPU work), the stream must still have
 work pending; a call that synchronised internally would return with the
 stream idle.  (The packing and upload steps never read device memory either.)
@@ -40,6 +40,13 @@ def test_prefill_and_decode_calls_do_not_synchronise():
     call()
     pending, dt = _pending_after(call)
     assert pending, f"prefill calls returned with the stream idle ({dt * 1e3:.2f} ms)"
+
+    kc, vc = wp.pool.k_cache.clone(), wp.pool.v_cache.clone()
+    call = lambda: [pa.pa_prefill_varlen_fused(dims, bp.q, bp.k, bp.v, kc, vc, plan, bp.scale, out)
+                    for _ in range(3)]
+    call()
+    pending, dt = _pending_after(call)
+    assert pending, f"fused store + prefill calls returned with the stream idle ({dt * 1e3:.2f} ms)"
 
     wd = workloads.make("qwen25_decode", device="cuda")
     bd = wd.batches[0]

@@ -176,3 +176,45 @@ def test_fused_prefill_bad_slot_flagged():
     torch.cuda.synchronize()
     assert pa.pa_read_device_error() == 0
     assert torch.equal(out, out2)
+
+
+def test_fused_prefill_replayed_from_a_cuda_graph():
+    """Captured once, replayed on new inputs copied into the captured buffers: the same output and
+    cache as eager calls (no host synchronisation or allocation inside the call)."""
+    w = workloads.random_case(721, num_seqs=3, hq=8, hkv=2, d=128, bs=16, max_len=600, cached="aligned",
+                              device="cuda")
+    batch = w.batches[0]
+    dims = dims_of(w, batch)
+    plan = pa.pa_pack_prefill(dims, batch.seq_lens, batch.query_lens, batch.block_lists).upload("cuda")
+    assert plan.meta.prefix_aligned == 1
+    q, k, v = batch.q.clone(), batch.k.clone(), batch.v.clone()
+    kc, vc = w.pool.k_cache.clone(), w.pool.v_cache.clone()
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pa.pa_prefill_varlen_fused(dims, q, k, v, kc, vc, plan, batch.scale, out, stream=s)  # set-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pa.pa_prefill_varlen_fused(dims, q, k, v, kc, vc, plan, batch.scale, out,
+                                   stream=torch.cuda.current_stream())
+    g = torch.Generator(device="cuda").manual_seed(722)
+    for _ in range(2):
+        nq = torch.randn(q.shape, device="cuda", generator=g).to(torch.bfloat16)
+        nk = torch.randn(k.shape, device="cuda", generator=g).to(torch.bfloat16)
+        nv = torch.randn(v.shape, device="cuda", generator=g).to(torch.bfloat16)
+        q.copy_(nq), k.copy_(nk), v.copy_(nv)
+        graph.replay()
+        kc2, vc2 = w.pool.k_cache.clone(), w.pool.v_cache.clone()
+        ref = torch.empty_like(q)
+        pa.pa_prefill_varlen_fused(dims, nq, nk, nv, kc2, vc2, plan, batch.scale, ref)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+        sm = plan.host_array(plan.meta.off_slot_mapping, batch.num_tokens)
+        n = w.pool.num_blocks * w.pool.block_size
+        assert torch.equal(kc.view(n, -1)[torch.as_tensor(sm, device="cuda").long()], nk.view(batch.num_tokens, -1))
+        assert torch.equal(kc.view(n, -1)[torch.as_tensor(sm, device="cuda").long()],
+                           kc2.view(n, -1)[torch.as_tensor(sm, device="cuda").long()])
+    assert pa.pa_read_device_error() == 0
