@@ -42,6 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {"qwen25": {"prefill": 232.1e6, "decode": 4.334e9}}
 NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": 210.6e6, "decode": 2.214e9}}
 NCU_TRAFFIC_FUSED_PREFILL = {"qwen25": 266.9e6}
+NCU_TRAFFIC_COPY_BLOCKS = 488.3e6  # 268.5 MB read + 219.7 MB written (part of the writes still in L2 at exit)
 
 
 def parse():
@@ -515,7 +516,7 @@ def copy_blocks_roofline(device, stream, hbm_peak, peak_src, iters=20, warmup=3)
     gbs = work / (ms * 1e-3) / 1e9
     return {"kernel": "pa_copy_blocks (copy_blocks_kernel)", "bound": "hbm", "achieved": round(gbs, 1),
             "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4), "peak_source": f"{peak_src} hbm_gbs",
-            "traffic": None, "work_per_launch": work, "ms_per_launch": round(ms, 5),
+            "traffic": NCU_TRAFFIC_COPY_BLOCKS, "work_per_launch": work, "ms_per_launch": round(ms, 5),
             "workload": "8192 full-block copies (block 16, 4 KV heads, D 128), 256 MB read + 256 MB written"}
 
 
