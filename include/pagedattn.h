@@ -437,7 +437,8 @@ int pa_read_device_error(uint32_t *code, pa_stream_t stream);
  */
 int pa_selftest_bounded_wait(uint32_t timeout_us, int arrive_first, pa_stream_t stream);
 
-/* Library version, e.g. 0x000100 for 0.1.0. */
+/* Library version, e.g. 0x000200 for 0.2.0.  0.2.0 added pa_prefill_varlen_fused
+ * and gave pa_prefill_meta's spare field its meaning (prefix_aligned). */
 int pa_version(void);
 
 #ifdef __cplusplus

@@ -60,7 +60,7 @@ using namespace pa;
 
 extern "C" const char *pa_last_error_string(void) { return g_err; }
 
-extern "C" int pa_version(void) { return 0x000100; }
+extern "C" int pa_version(void) { return 0x000200; }
 
 extern "C" int pa_upload(void *dev_dst, const void *host_src, size_t bytes, pa_stream_t stream)
 {
