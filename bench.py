@@ -3,7 +3,9 @@
 
 One step = the whole path over one batch of seeded synthetic input:
   1. host metadata packing (pa_pack_prefill / pa_pack_decode) + one upload each,
-  2. KV scatter of the 4 x 4096 prompt tokens + causal varlen prefill,
+     on a copy stream while the previous step computes (double-buffered images),
+  2. KV scatter of the 4 x 4096 prompt tokens + causal varlen prefill, by default
+     as one pa_prefill_varlen_fused launch (--prefill-path store+prefill: two),
   3. KV scatter of the 64 decode tokens + split-KV decode + LSE combine,
 on the long-context Qwen2.5-7B attention shapes (28 q / 4 KV heads, head_dim
 128, block 16): prefill 4 x 4096, decode 64 sequences at context 32768 through
