@@ -29,8 +29,11 @@
 //    rows past the sequence end are zeroed before use.
 //  * warp 8: K TMA producer; warp 10: V producer; warp 11: Q producer (it
 //    refills a query tile as soon as the item's last score MMA of that tile
-//    has read it); warp 9: TMEM owner and the single thread issuing every
-//    tcgen05.mma.  Each query tile t owns 256
+//    has read it); warp 9: TMEM owner and the MMA issuer.  The whole warp runs
+//    the issue loop, converged, and an elected lane issues each tcgen05.mma and
+//    commit: a 128 x 128 x 16 product runs 64 cycles, and a lone lane in a
+//    divergent branch spends nearly as long issuing it, which left no slack
+//    for the waits and commits between products.  Each query tile t owns 256
 //    TMEM columns: S_t (128 fp32 columns, reused for P_t) and O_t.  The issue
 //    order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core busy on
 //    one tile while the other tile's softmax runs (ping-pong).  Because the
@@ -40,8 +43,10 @@
 //    score MMAs follow the last PVs, so they run while the softmax warps write
 //    the previous item's output.
 //  * warps 0-3 and 4-7: one softmax warpgroup per query tile, one query row
-//    per thread: one tcgen05.ld round trip of the score row, causal mask only
-//    on tiles that cross the diagonal, fp32 online softmax in base 2
+//    per thread: one tcgen05.ld round trip of the score row, which on tiles
+//    that do not cross the causal diagonal also returns the row max
+//    (tcgen05.ld.red, sm_103a); diagonal tiles are masked and reduced in
+//    registers; fp32 online softmax in base 2
 //    (scale * log2 e folded into one packed FMA), lazy O rescale (only when
 //    the running max grows by more than 2^8), P written back over S with
 //    tcgen05.st and consumed by the PV MMA straight from tensor memory;
@@ -749,8 +754,9 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 if (lane == 0)
                     ptx::mbar_arrive(bars.q_ready(tq));
             }
-        } else if (warp == kMmaWarp && lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer (the whole warp;
+            // one elected lane issues each MMA and commit)
             ItemIter items(p.tiles, p.num_items, P);
             // INT8 cache: f16 operands (exact codes, f16 Q and P)
             constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
@@ -769,7 +775,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t o = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
-                    ptx::mma_bf16_ss(tmem + t * 256, desc(qa + o, hi_k), desc(kb + o, hi_k), idesc_s, kk > 0);
+                    ptx::mma_bf16_ss_warp(tmem + t * 256, desc(qa + o, hi_k), desc(kb + o, hi_k), idesc_s, kk > 0);
                 }
             };
             auto issue_pv = [&](int t, int vs, bool first) {
@@ -778,7 +784,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 asm volatile("" : "+r"(vb));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc(vb + kk * (2048 >> 4), hi_v),
+                    ptx::mma_bf16_ts_warp(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc(vb + kk * (2048 >> 4), hi_v),
                                      idesc_o, (!first || kk > 0) ? 1u : 0u);
             };
             // ring positions kept as counters (no division in the issue loop)
@@ -790,26 +796,26 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             while (ok && items.more()) {
                 const Item w = items.next();
                 const uint32_t qpar = w.ord & 1;
-                ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) && wait(bars.k_full(ks), kph);
+                ok = wwait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) && wwait(bars.k_full(ks), kph);
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
                 issue_s(0, ks);
-                ptx::mma_commit(bars.s_full(0));
+                ptx::mma_commit_warp(bars.s_full(0));
                 // query tile 1 is waited for only now (also when empty: its buffer is
                 // released below, and every load of it must be consumed first)
-                if (!(ok = wait(I8 ? bars.q_ready(1) : bars.q_full(1), qpar)))
+                if (!(ok = wwait(I8 ? bars.q_ready(1) : bars.q_full(1), qpar)))
                     break;
                 if (w.nkt1 > 0) {
                     ptx::tc_fence_after();
                     issue_s(1, ks);
-                    ptx::mma_commit(bars.s_full(1));
+                    ptx::mma_commit_warp(bars.s_full(1));
                 }
-                ptx::mma_commit(bars.released(E)); // K tile 0 read by both score MMAs
+                ptx::mma_commit_warp(bars.released(E)); // K tile 0 read by both score MMAs
                 if (w.nkt0 == 1)
-                    ptx::mma_commit(bars.q_free(0));
+                    ptx::mma_commit_warp(bars.q_free(0));
                 if (w.nkt1 <= 1)
-                    ptx::mma_commit(bars.q_free(1));
+                    ptx::mma_commit_warp(bars.q_free(1));
                 if (++ks == L::kKStages) {
                     ks = 0;
                     kph ^= 1;
@@ -818,14 +824,14 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                     bool v_ready = false, k_next = false;
                     // one query tile: PV(t, j), then S(t, j + 1) into the same TMEM columns
                     auto step = [&](const int t, const int ntk) {
-                        if (!(ok = wait(bars.p_full(t), (np >> t) & 1u)))
+                        if (!(ok = wwait(bars.p_full(t), (np >> t) & 1u)))
                             return;
                         np ^= 1u << t;
                         if (!v_ready) {
-                            if (!(ok = wait(bars.v_full(vs), vph)))
+                            if (!(ok = wwait(bars.v_full(vs), vph)))
                                 return;
                             if (!I8 && w.tail && j == w.nkt - 1) {
-                                if (!(ok = wait(bars.v_tail(vs), (tailpar >> vs) & 1u)))
+                                if (!(ok = wwait(bars.v_tail(vs), (tailpar >> vs) & 1u)))
                                     return;
                                 tailpar ^= 1u << vs;
                             }
@@ -834,18 +840,18 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                         ptx::tc_fence_after();
                         issue_pv(t, vs, j == 0);
                         if (j + 1 == ntk)
-                            ptx::mma_commit(bars.o_full(t)); // O_t final
+                            ptx::mma_commit_warp(bars.o_full(t)); // O_t final
                         if (j + 1 < ntk) {
                             if (!k_next) {
-                                if (!(ok = wait(bars.k_full(ks), kph)))
+                                if (!(ok = wwait(bars.k_full(ks), kph)))
                                     return;
                                 ptx::tc_fence_after();
                                 k_next = true;
                             }
                             issue_s(t, ks);
-                            ptx::mma_commit(bars.s_full(t));
+                            ptx::mma_commit_warp(bars.s_full(t));
                             if (j + 2 == ntk)
-                                ptx::mma_commit(bars.q_free(t)); // that was the last read of Q_t
+                                ptx::mma_commit_warp(bars.q_free(t)); // that was the last read of Q_t
                         }
                     };
                     if (j < w.nkt0)
@@ -854,7 +860,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                         step(1, w.nkt1);
                     if (!ok)
                         break;
-                    ptx::mma_commit(bars.released(E + j + 1)); // V tile j and K tile j + 1 read
+                    ptx::mma_commit_warp(bars.released(E + j + 1)); // V tile j and K tile j + 1 read
                     if (++vs == L::kVStages) {
                         vs = 0;
                         vph ^= 1;
@@ -898,30 +904,41 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 ns ^= 1;
                 ptx::tc_fence_after();
                 const int lim = limit - j * 128; // columns this row sees in this tile
-                // the whole score row in registers: one TMEM round trip per tile
+                // the whole score row in registers: one TMEM round trip per tile.  Tiles no row
+                // of the warp sees only in part take the row max from the loads themselves
+                // (tcgen05.ld.red); tiles crossing the causal diagonal mask first, then reduce.
                 uint32_t sr[128];
+                float mx;
+                if (__any_sync(0xffffffffu, lim < 128)) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    ptx::tmem_ld32(s_col + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
-                ptx::tmem_wait_ld();
-                if (lim < 128) {
+                    for (int q = 0; q < 4; ++q)
+                        ptx::tmem_ld32(s_col + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
+                    ptx::tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
                         sr[c] = c < lim ? sr[c] : __float_as_uint(-INFINITY);
-                }
-                float m8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    m8[i] = ptx::max3(__uint_as_float(sr[16 * i]), __uint_as_float(sr[16 * i + 1]),
-                                      __uint_as_float(sr[16 * i + 2]));
-#pragma unroll
-                for (int c = 3; c < 16; c += 2)
+                    float m8[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        m8[i] = c + 1 < 16 ? ptx::max3(m8[i], __uint_as_float(sr[16 * i + c]), __uint_as_float(sr[16 * i + c + 1]))
-                                           : fmaxf(m8[i], __uint_as_float(sr[16 * i + c]));
-                const float mx = fmaxf(fmaxf(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5])),
-                                       fmaxf(m8[6], m8[7]));
+                        m8[i] = ptx::max3(__uint_as_float(sr[16 * i]), __uint_as_float(sr[16 * i + 1]),
+                                          __uint_as_float(sr[16 * i + 2]));
+#pragma unroll
+                    for (int c = 3; c < 16; c += 2)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            m8[i] = c + 1 < 16 ? ptx::max3(m8[i], __uint_as_float(sr[16 * i + c]),
+                                                           __uint_as_float(sr[16 * i + c + 1]))
+                                               : fmaxf(m8[i], __uint_as_float(sr[16 * i + c]));
+                    mx = fmaxf(fmaxf(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5])),
+                               fmaxf(m8[6], m8[7]));
+                } else {
+                    float m4[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        m4[q] = ptx::tmem_ld32_max(s_col + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * q]));
+                    ptx::tmem_wait_ld();
+                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                }
                 const float mt = mx * sl2;
                 float alpha = 1.f;
                 bool rescale = false;
