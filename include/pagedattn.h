@@ -437,6 +437,20 @@ int pa_read_device_error(uint32_t *code, pa_stream_t stream);
  */
 int pa_selftest_bounded_wait(uint32_t timeout_us, int arrive_first, pa_stream_t stream);
 
+/*
+ * pa_stream_read — measurement helper, not part of the attention path.  Reads
+ * every 16-byte vector of the device buffer src[0 .. bytes) once with
+ * streaming (non-caching) loads and XOR-folds the words into *sink (device,
+ * 4 bytes, caller-owned; its value is meaningless, it only keeps the loads
+ * live).  It is the read-only memory bandwidth that bounds the decode kernels
+ * (they read the whole cache and write little), so timing it beside them gives
+ * the ceiling they are measured against; the pages' "decode time = bytes /
+ * bandwidth" ("推理系统", 瓶颈不是算力，是带宽) states the bound.  src and sink
+ * 16- and 4-byte aligned, bytes a multiple of 16, else PA_ERR_INVALID_ARG;
+ * bytes == 0 launches nothing.  Asynchronous on `stream`.
+ */
+int pa_stream_read(const void *src, size_t bytes, uint32_t *sink, pa_stream_t stream);
+
 /* Library version, e.g. 0x000200 for 0.2.0.  0.2.0 added pa_prefill_varlen_fused
  * and gave pa_prefill_meta's spare field its meaning (prefix_aligned). */
 int pa_version(void);

@@ -444,6 +444,17 @@ extern "C" int pa_read_device_error(uint32_t *code, pa_stream_t stream)
     return rc;
 }
 
+extern "C" int pa_stream_read(const void *src, size_t bytes, uint32_t *sink, pa_stream_t stream)
+{
+    if (bytes && !src)
+        return fail(PA_ERR_INVALID_ARG, "pa_stream_read: src is NULL");
+    if (!sink)
+        return fail(PA_ERR_INVALID_ARG, "pa_stream_read: sink is NULL");
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) || (bytes & 15u) || (reinterpret_cast<uintptr_t>(sink) & 3u))
+        return fail(PA_ERR_INVALID_ARG, "pa_stream_read: src and bytes must be 16-byte aligned, sink 4-byte aligned");
+    return launch_stream_read(src, bytes, sink, stream);
+}
+
 extern "C" int pa_selftest_bounded_wait(uint32_t timeout_us, int arrive_first, pa_stream_t stream)
 {
     if (timeout_us < 1 || timeout_us > 10000000u)

@@ -161,5 +161,6 @@ int read_fused_error(uint32_t *code);
 int read_fused8_error(uint32_t *code);
 int launch_selftest_wait(uint32_t timeout_us, int arrive_first, void *stream);
 int read_selftest_error(uint32_t *code);
+int launch_stream_read(const void *src, size_t bytes, uint32_t *sink, void *stream);
 
 } // namespace pa

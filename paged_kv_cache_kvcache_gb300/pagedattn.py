@@ -24,7 +24,8 @@ EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache",
            "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
            "pa_prefill_varlen_int8", "pa_pack_decode_fixed", "pa_decode_fused", "pa_copy_blocks_int8",
            "pa_decode_int8_fused", "pa_prefill_varlen_fused",
-           "pa_last_error_string", "pa_read_device_error", "pa_selftest_bounded_wait", "pa_version")
+           "pa_last_error_string", "pa_read_device_error", "pa_selftest_bounded_wait", "pa_stream_read",
+           "pa_version")
 
 PA_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -95,6 +96,7 @@ def lib() -> ctypes.CDLL:
             L.pa_last_error_string.restype = ctypes.c_char_p
             L.pa_read_device_error.argtypes = [P, P]
             L.pa_selftest_bounded_wait.argtypes = [ctypes.c_uint32, ctypes.c_int, P]
+            L.pa_stream_read.argtypes = [P, SZ, P, P]
             L.pa_version.argtypes = []
             for name in EXPORTS:
                 if name not in ("pa_last_error_string",):
@@ -394,6 +396,13 @@ def pa_selftest_bounded_wait(timeout_us: int, arrive_first: bool = False, stream
     arrive_first, one it completes itself); a timeout shows as bit 4 of pa_read_device_error."""
     _check(lib().pa_selftest_bounded_wait(ctypes.c_uint32(int(timeout_us)), 1 if arrive_first else 0, _stream(stream)),
            "pa_selftest_bounded_wait")
+
+
+def pa_stream_read(src: torch.Tensor, sink: torch.Tensor, stream=None):
+    """Read every byte of the device tensor `src` once (streaming loads): the read-only
+    bandwidth that bounds the decode kernels.  `sink` is a 4-byte device tensor."""
+    _check(lib().pa_stream_read(_ptr(src), src.numel() * src.element_size(), _ptr(sink), _stream(stream)),
+           "pa_stream_read")
 
 
 def pa_read_device_error(stream=None) -> int:

@@ -72,6 +72,11 @@ def test_device_calls_reject_bad_args_without_touching_the_gpu():
     assert "workspace" in pa.pa_last_error_string()
     for bad in (0, 10000001):
         assert L.pa_selftest_bounded_wait(bad, 0, None) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_stream_read(16, 64, None, None) == pa.PA_ERR_INVALID_ARG     # no sink
+    assert L.pa_stream_read(8, 64, 16, None) == pa.PA_ERR_INVALID_ARG       # src misaligned
+    assert L.pa_stream_read(16, 40, 16, None) == pa.PA_ERR_INVALID_ARG      # bytes not a multiple of 16
+    assert L.pa_stream_read(None, 16, 16, None) == pa.PA_ERR_INVALID_ARG    # no src
+    assert L.pa_stream_read(None, 0, 16, None) == pa.PA_OK                  # nothing to read: no launch
 
 
 def test_pack_rejects_malformed_sequences():
