@@ -619,6 +619,11 @@ def main():
         t_end.record(stream)
         torch.cuda.synchronize()
         w1 = time.time()
+        # every kernel hand-off waits with a time limit; a wait that ran out leaves its
+        # outputs undefined and is recorded in the device error word: such a run is invalid
+        derr = step.pa.pa_read_device_error(stream)
+        if derr:
+            raise RuntimeError(f"device error word {derr:#x} after the timed steps: outputs undefined")
         if world > 1:
             torch.distributed.barrier()
         clk = clocks.stop(w0, w1)
@@ -768,7 +773,7 @@ def main():
                      "decode_phase": round(t_decode_phase, 5), "decode_kernels": round(t_decode_kernel, 5)},
         "roofline": dominant, "rooflines": rooflines,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": step.launches_per_step * args.steps,
-        "clocks": clk, "peaks": peak_src,
+        "clocks": clk, "peaks": peak_src, "device_error": 0,
     }
     if mixed is not None:
         line["mixed"] = mixed

@@ -178,6 +178,10 @@ int pa_store_kvcache(const pa_dims *dims, const void *k, const void *v, void *k_
  * scale must be finite and > 0 (PA_ERR_INVALID_ARG otherwise).  PA_ERR_UNSUPPORTED,
  * before any launch, if the library's prefill kernel was compiled with other
  * than 168 registers per thread (its warps re-divide exactly that many).
+ * Every hand-off inside the kernel waits with a time limit (2 s); a wait that
+ * runs out sets bit 1 of the device error word and the kernel returns early,
+ * so `out` is undefined whenever pa_read_device_error reports bit 1 (the same
+ * holds for pa_prefill_varlen_fused and pa_prefill_varlen_int8).
  */
 int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache,
                       const void *v_cache, const int32_t *cu_seqlens_q,
@@ -326,7 +330,10 @@ int pa_store_kvcache_int8(const pa_dims *dims, const void *k, const void *v, voi
  * read as code * scale.  Internally the codes (exact in fp16) and q (rounded
  * to fp16; exact for bf16 magnitudes in [2^-14, 65504], clamped to +-65504)
  * feed fp16 tensor-core products with fp32 accumulation; the V scale is
- * applied to the softmax weights before the P.V product.
+ * applied to the softmax weights before the P.V product.  Its staged loads
+ * are waited for with a time limit (2 s); a wait that runs out sets bit 3 of
+ * the device error word and the kernel returns early, so `out` is undefined
+ * whenever pa_read_device_error reports bit 3 (also for pa_decode_int8_fused).
  */
 int pa_decode_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
                    const void *k_scale, const void *v_scale, const int32_t *context_lens,
@@ -398,7 +405,11 @@ int pa_copy_blocks_int8(const pa_dims *dims, void *k_cache, void *v_cache, void 
  *    split_tokens when packing, for such batches).
  *  - Set-up: the first call on each device looks up the array's device
  *    address (cudaGetSymbolAddress, with that device current); make that first
- *    call before any stream capture.  Later calls do no set-up.
+ *    call before any stream capture.  Later calls do no set-up and reuse that
+ *    address for the life of the process: after cudaDeviceReset (or anything
+ *    else that destroys the device's primary context) the library's module is
+ *    loaded again at another address, so do not call pa_decode_static on that
+ *    device again in this process.
  *  - Sharing: every call on a device uses the same array and it keeps the
  *    last call's contents.  Nothing in it needs to start at zero: each call
  *    writes every partial it reads.  Calls whose work overlaps on the GPU

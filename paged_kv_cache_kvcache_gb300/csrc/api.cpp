@@ -416,8 +416,13 @@ extern "C" int pa_decode_static(const pa_dims *dims, const void *q, const void *
     int rc = decode_static_scratch(&scratch);
     if (rc != PA_OK)
         return rc;
-    return pa_decode(dims, q, k_cache, v_cache, context_lens, block_tables, scale, out, meta, items, seq_items,
-                     scratch, PA_DECODE_STATIC_SCRATCH_BYTES, stream);
+    DecodeArgs a;
+    bool nothing = false;
+    rc = prepare_decode("pa_decode_static", dims, q, k_cache, v_cache, context_lens, block_tables, scale, out, meta,
+                        items, seq_items, scratch, PA_DECODE_STATIC_SCRATCH_BYTES, &a, &nothing);
+    if (rc != PA_OK || nothing)
+        return rc;
+    return launch_decode(a, stream);
 }
 
 extern "C" int pa_read_device_error(uint32_t *code, pa_stream_t stream)

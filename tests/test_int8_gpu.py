@@ -28,6 +28,10 @@ def _special_rows(t, hkv, d, seed):
     x[3, :, 1:] = torch.tensor([2.5, -3.5, 0.5, -0.5, 126.5, -126.5, 64.25, -1.0])[torch.arange(d - 1) % 8]
     x[4, :, 0] = -254.0                          # negative extreme sets the scale (2.0)
     x[5] = torch.where(torch.arange(d) % 2 == 0, torch.tensor(1e-3), torch.tensor(-3e38))[None]  # near bf16 max
+    # the scale stored as fp16 leaves the normal range: max|x| ~ 6e-6 (< 1e-5) gives a scale of
+    # a few fp16 subnormal steps, max|x| ~ 3e-3 one with a few bits (both sides must agree)
+    x[6] = 2e-6 * torch.randn(hkv, d, generator=g)
+    x[7] = 1e-3 * torch.randn(hkv, d, generator=g)
     return x.to(torch.bfloat16)
 
 

@@ -106,11 +106,11 @@ def test_int8_prefill_edge_lengths():
     assert_close(out, ref, what="int8 edges")
 
 
-def test_int8_prefill_qwen25_sampled():
-    """Qwen2.5-7B attention shape, 4 x 4096 causal prefill (the measured workload), sampled rows."""
+def test_int8_prefill_qwen25_every_row():
+    """Qwen2.5-7B attention shape, 4 x 4096 causal prefill (the measured workload), every row."""
     w = workloads.make("qwen25_prefill", device="cuda")
-    (batch, out, ref, sel), = _run_both(w, row_select=lambda b: sample_rows(b, 24, seed=5))
-    assert_close(out, ref, rows=sel, what="int8 qwen25 prefill (sampled rows)")
+    (batch, out, ref, _), = _run_both(w)
+    assert_close(out, ref, what="int8 qwen25 prefill (every row)")
 
 
 def test_int8_prefill_single_32k_sequence_sampled():
@@ -123,11 +123,10 @@ def test_int8_prefill_single_32k_sequence_sampled():
 
 
 def test_int8_prefill_and_decode_over_mixed_token_magnitudes():
-    """Tokens whose K/V magnitudes span 1e-4 .. 1 (scales down to ~1e-6, so that fp16
-    code x scale products fall in the subnormal range) and all-zero tokens (scale 0):
-    a prefill over them, then a decode of each sequence's last token.  (Magnitudes stay
-    at or below those of N(0, 1) data: the absolute bound is sized for outputs of order
-    one, whose bf16 rounding alone reaches 2^-8 at 2..4.)"""
+    """Tokens whose K/V magnitudes span 1e-4 .. 10^0.5 (scales down to ~1e-6, so that fp16
+    code x scale products fall in the subnormal range, and up to about 3x those of N(0, 1)
+    data) and all-zero tokens (scale 0): a prefill over them, then a decode of each
+    sequence's last token."""
     hq, hkv, d, bs = 8, 2, 128, 16
     lens = np.array([300, 77, 129], np.int32)
     nb = int(sum(-(-l // bs) for l in lens)) + 3
@@ -139,9 +138,9 @@ def test_int8_prefill_and_decode_over_mixed_token_magnitudes():
         o += n
     g = torch.Generator(device="cuda").manual_seed(32)
 
-    def kv(*shape):  # rows scaled by 10^U(-4, 0) per (token, head); one row in 9 all zero
+    def kv(*shape):  # rows scaled by 10^U(-4, 0.5) per (token, head); one row in 9 all zero
         x = torch.randn(*shape, device="cuda", generator=g)
-        mag = 10.0 ** (torch.rand(*shape[:-1], 1, device="cuda", generator=g) * 4.0 - 4.0)
+        mag = 10.0 ** (torch.rand(*shape[:-1], 1, device="cuda", generator=g) * 4.5 - 4.0)
         zero = torch.rand(*shape[:-1], 1, device="cuda", generator=g) < 1 / 9
         return (x * mag).masked_fill(zero, 0.0).to(torch.bfloat16)
 

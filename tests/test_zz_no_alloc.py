@@ -5,8 +5,9 @@ running while a stream is captured into a CUDA graph, where cudaMalloc is not
 allowed, or runtimes that only own fixed pre-planned buffers).  For them
 pa_decode_static uses the library's own fixed scratch array instead.  These
 tests call it through the C ABI and check it against pa_decode (which gets a
-caller workspace), on two calls in a row because the array is shared and keeps
-the previous call's contents.  The file is named so pytest collects it last.
+caller workspace) and against the CPU oracle, on two calls in a row because the
+array is shared and keeps the previous call's contents.  The file is named so
+pytest collects it last.
 """
 import ctypes
 
@@ -14,9 +15,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_kvcache_gb300 import pagedattn as pa
 from paged_kv_cache_kvcache_gb300 import workloads
-from tests.harness import MAX_ABS, MAX_RRMS, compare, dims_of
+from tests.harness import MAX_ABS, MAX_RRMS, assert_close, bits, compare, dims_of
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +48,18 @@ def test_static_scratch_matches_workspace_decode_twice():
         torch.cuda.synchronize()
         max_abs, rrms = compare(out, ref64)
         assert max_abs <= MAX_ABS and rrms <= MAX_RRMS, (max_abs, rrms)
+
+
+def test_static_scratch_matches_the_oracle_twice():
+    """Against the fp64 CPU oracle (its own store of the batch, then attention), two calls in a row."""
+    w, batch, dims, plan, kc, vc = _setup(305, 256)
+    assert plan.meta.num_partials > 0
+    ref, _ = oracle.run_batch(bits(w.pool.k_cache), bits(w.pool.v_cache), batch, w.pool.block_size)
+    for i in range(2):
+        out = torch.full_like(batch.q, float("nan"))
+        pa.pa_decode_static(dims, batch.q, kc, vc, plan, batch.scale, out)
+        torch.cuda.synchronize()
+        assert_close(out, ref, what=f"pa_decode_static call {i + 1}")
 
 
 def test_static_scratch_second_plan_after_first():
