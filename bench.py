@@ -196,7 +196,7 @@ class Step:
                 e.record(stream)
         self.i = 0
         self.launches_per_step = 4 + (1 if self.plans_d[0].meta.num_partials > 0 else 0) - (1 if fused else 0)
-        if self.prefill_fused and self.plans_p[0].meta.prefix_aligned:
+        if self.prefill_fused:  # store and prefill in one launch
             self.launches_per_step -= 1
         if mixed:  # one launch for both phases' rows, over one pool
             self.kc_m, self.vc_m, self.bm = mixed_batch(wp, wd)

@@ -76,8 +76,9 @@ typedef struct pa_prefill_meta {
                                    a work item covers two query tiles */
     int32_t prefix_aligned;     /* 1 if the cached prefix (seq_len - query_len) of every
                                    sequence with new tokens is a multiple of
-                                   min(block_size, 128): pa_prefill_varlen_fused then
-                                   runs as one launch */
+                                   min(block_size, 128) (then no key box of the fused
+                                   launch needs its new rows patched in); informational:
+                                   pa_prefill_varlen_fused runs as one launch either way */
     uint64_t off_cu_seqlens_q;  /* int32 [num_seqs+1] */
     uint64_t off_cu_seqlens_k;  /* int32 [num_seqs+1] */
     uint64_t off_block_tables;  /* int32 [num_seqs][max_blocks_per_seq], -1 padded */
@@ -191,14 +192,16 @@ int pa_prefill_varlen(const pa_dims *dims, const void *q, const void *k_cache,
 
 /*
  * pa_prefill_varlen_fused — pa_store_kvcache of the new tokens followed by
- * pa_prefill_varlen, with the same result, in one launch when the plan allows
- * (meta->prefix_aligned; otherwise the two launches run in that order).
- * Source: "手搓 vLLM 推理引擎", Step 4 (store_kvcache, then attention over the
- * cache).  In the fused launch the prefill reads the new tokens' keys and
- * values from k and v themselves (the same bf16 values the store writes) and
- * the cached prefix from the cache, while one warp of each CTA copies the rows
- * of its work item's query positions into their slots (each (token, KV head)
- * row by exactly one item).
+ * pa_prefill_varlen, with the same result, in one launch.  Source: "手搓 vLLM
+ * 推理引擎", Step 4 (store_kvcache, then attention over the cache); "面试问答准备:
+ * nano-vLLM 推理引擎优化", Q1 (chunked prefill resumes at any token count, so a
+ * cached prefix need not end on a block boundary).  The prefill reads the new
+ * tokens' keys and values from k and v themselves (the same bf16 values the
+ * store writes) and the cached prefix from the cache; a key box that starts in
+ * the prefix and ends among the new keys is read from the cache and its new
+ * rows are replaced from k and v before use.  Meanwhile one warp of each CTA
+ * copies the rows of its work item's query positions into their slots (each
+ * (token, KV head) row by exactly one item).
  *   k, v:          device bf16 [meta->total_q][num_kv_heads][head_dim], row t
  *                  the key/value of packed query row t
  *   slot_mapping:  device int32 [meta->total_q] (dev + meta->off_slot_mapping);
@@ -462,8 +465,10 @@ int pa_selftest_bounded_wait(uint32_t timeout_us, int arrive_first, pa_stream_t 
  */
 int pa_stream_read(const void *src, size_t bytes, uint32_t *sink, pa_stream_t stream);
 
-/* Library version, e.g. 0x000200 for 0.2.0.  0.2.0 added pa_prefill_varlen_fused
- * and gave pa_prefill_meta's spare field its meaning (prefix_aligned). */
+/* Library version, e.g. 0x000300 for 0.3.0.  0.2.0 added pa_prefill_varlen_fused
+ * and gave pa_prefill_meta's spare field its meaning (prefix_aligned); 0.3.0
+ * made pa_prefill_varlen_fused one launch for any cached prefix and added
+ * pa_stream_read. */
 int pa_version(void);
 
 #ifdef __cplusplus

@@ -60,7 +60,7 @@ using namespace pa;
 
 extern "C" const char *pa_last_error_string(void) { return g_err; }
 
-extern "C" int pa_version(void) { return 0x000200; }
+extern "C" int pa_version(void) { return 0x000300; }
 
 extern "C" int pa_upload(void *dev_dst, const void *host_src, size_t bytes, pa_stream_t stream)
 {
@@ -169,14 +169,10 @@ extern "C" int pa_prefill_varlen_fused(const pa_dims *dims, const void *q, const
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_fused: NULL pointer");
     if (misaligned(k) || misaligned(v))
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_fused: tensors must be 16-byte aligned");
-    if (!meta->prefix_aligned) { // a key box would straddle a cached prefix: store, then prefill
-        if ((rc = launch_store_kvcache(*dims, k, v, k_cache, v_cache, slot_mapping, meta->total_q, stream)) != PA_OK)
-            return rc;
-        return launch_prefill(a, stream);
-    }
     a.k_in = k;
     a.v_in = v;
     a.slot_mapping = slot_mapping;
+    a.small_boxes = !meta->prefix_aligned;
     return launch_prefill(a, stream);
 }
 

@@ -107,6 +107,9 @@ struct PrefillArgs {
     const void *k_in;
     const void *v_in;
     const int32_t *slot_mapping;
+    // fused store with a cached prefix that does not end on a box boundary: fetch keys in
+    // boxes of 16 rows, so that the box straddling the prefix end has few rows to patch
+    bool small_boxes;
 };
 int launch_prefill(const PrefillArgs &a, void *stream);
 int launch_prefill_int8(const PrefillArgs &a, void *stream);

@@ -67,7 +67,11 @@
 //  * Fused store (pa_prefill_varlen_fused, bf16): the K/V producers take the
 //    new keys' boxes from the k/v inputs instead of the cache (so nothing
 //    the launch writes is read by it), and warp 11, between its query loads,
-//    copies the K/V rows of its item's query positions into their slots.
+//    copies the K/V rows of its item's query positions into their slots.  A
+//    box that starts in the cached prefix and ends among the new keys (chunked
+//    prefill resumes at any token count) is loaded from the cache and its new
+//    keys' rows are then copied over it from the inputs by the producer before
+//    the MMAs may read it.
 //  * mbarriers order every hand-off; every wait is bounded and reports a
 //    timeout through a device error word instead of hanging.
 #include <cuda.h>
@@ -165,6 +169,7 @@ struct PfParams {
     int32_t group;
     int32_t rows_per_tile; // query positions per query tile
     int32_t block_size;
+    int32_t box_rows;      // rows per TMA box of a key tile: min(block size, 128), or 16 (see launch)
     int32_t max_blocks;
     int32_t num_slots;     // num_blocks * block_size: first out-of-range row (reads as zeros)
     int32_t num_kv_heads;
@@ -200,6 +205,9 @@ struct Bars {
     __device__ uint32_t k_load(int s) const { return base + 8 * (32 + s); }
     __device__ uint32_t v_load(int s) const { return base + 8 * (36 + s); }
     __device__ uint32_t q_ready(int t) const { return base + 8 * (42 + t); }
+    // fused store: K slot s holds the key tile whose straddling box (cached prefix, then
+    // new keys) has had its new keys' rows copied in from the inputs
+    __device__ uint32_t k_fix(int s) const { return base + 8 * (44 + s); }
 };
 static_assert(kIterRing == 8, "barrier slots 12..19");
 constexpr int kTmemSlotOffset = 8 * 30;
@@ -271,6 +279,49 @@ struct ItemIter {
     // the item next() returns next (valid while more())
     __device__ Item peek() const { return decode(ord); }
 };
+
+// Fused store: the key tile of item w holding a box that starts in the cached prefix
+// and ends among the new keys (the prefix length is not a multiple of the box), or -1.
+// That box is loaded from the cache like the rest of the prefix; the producer then
+// copies the new keys' rows over it from the k/v inputs, since the launch is writing
+// those cache rows itself.
+__device__ __forceinline__ int straddle_tile(const Item &w, int fused, int box_rows)
+{
+    const int off = w.lk - w.lq; // cached prefix
+    return fused && w.lq > 0 && (off & (box_rows - 1)) != 0 ? off >> 7 : -1;
+}
+
+// Rows [off, min(box end, lk)) of the straddling box of key tile j: the new keys, copied
+// from the inputs (16-byte vectors, one warp) into their 128B-swizzled places in the tile.
+template <int D>
+__device__ __forceinline__ void patch_new_keys(uint8_t *tile, const uint4 *in, const Item &w, int j, int box_rows,
+                                               int num_kv_heads, int lane)
+{
+    constexpr int VPR = D / 8; // 16-byte vectors per row
+    constexpr int kU = 4;      // vectors in flight per lane
+    const int off = w.lk - w.lq;
+    const int end = min(off - (off & (box_rows - 1)) + box_rows, w.lk);
+    const int total = (end - off) * VPR;
+    for (int i0 = lane; i0 < total; i0 += 32 * kU) {
+        uint4 x[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + 32 * u;
+            if (i < total)
+                x[u] = __ldg(in + ((size_t)(w.cq0 + i / VPR) * num_kv_heads + w.g) * VPR + i % VPR);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + 32 * u;
+            if (i < total) {
+                const int rr = off + i / VPR - j * 128;  // row in the tile
+                const int c16 = i % VPR;
+                const int panel = c16 >> 3, c = c16 & 7; // 64-element panel, 16-byte chunk in its row
+                *reinterpret_cast<uint4 *>(tile + panel * (128 * 128) + rr * 128 + ((c ^ (rr & 7)) << 4)) = x[u];
+            }
+        }
+    }
+}
 
 // Release event of the key tile `back` places before global tile X (X >= back),
 // given the current item's ordinal and the item-start bits of the last tiles
@@ -494,8 +545,10 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             ptx::mbar_init(bars.p_full(t), 4); // one arrival per softmax warp
             ptx::mbar_init(bars.o_full(t), 1);
         }
-        for (int s = 0; s < L::kKStages; ++s)
+        for (int s = 0; s < L::kKStages; ++s) {
             ptx::mbar_init(bars.k_full(s), I8 ? 4 : 1); // INT8: one arrival per converter warp
+            ptx::mbar_init(bars.k_fix(s), 1);
+        }
         for (int s = 0; s < L::kVStages; ++s) {
             ptx::mbar_init(bars.v_full(s), I8 ? 4 : 1);
             ptx::mbar_init(bars.v_tail(s), 1);
@@ -584,11 +637,11 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
         // (2 kSoftmaxRegs + kOtherRegs [+ kConvRegs]) = the launch's registers)
         ptx::reg_dealloc<kOtherRegs>();
         const int bs = p.block_size;
-        const int box_rows = bs < 128 ? bs : 128;
+        const int box_rows = p.box_rows;
         const int nsub = 128 / box_rows;
         // row coordinate of sub-box `lane` of key tile j of item w (one TMA box per lane):
-        // a cache row, or -(r + 1) for row r of the new keys' input (fused store; a box
-        // never straddles the cached prefix and the new keys, the host checks)
+        // a cache row, or -(r + 1) for row r of the new keys' input (fused store); a box that
+        // starts in the cached prefix comes from the cache (its new rows are patched in later)
         auto sub_row = [&](const Item &w, const int32_t *bt, int j) -> int {
             const int key = j * 128 + lane * box_rows;
             if (lane >= nsub || key >= w.lk)
@@ -639,6 +692,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             bool ok = true;
             while (ok && items.more()) {
                 const Item w = items.next();
+                const int jfix = straddle_tile(w, p.fused, box_rows);
                 const int32_t *bt = p.block_tables + (size_t)w.b * p.max_blocks;
                 int next = sub_row(w, bt, 0);
                 for (int j = 0; j < w.nkt; ++j, ++X) {
@@ -666,22 +720,27 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                                              w.g, row);
                     }
                     __syncwarp();
-                    if (!is_k && w.tail && j == w.nkt - 1) {
-                        // V rows of keys past the sequence end may hold anything (even NaN
-                        // bit patterns); zero them so that P = 0 cannot turn them into NaN in O.
+                    const bool fix = j == jfix, zero = !is_k && w.tail && j == w.nkt - 1;
+                    if (fix || zero) {
                         if (!(ok = wwait(full, (X / nstages) & 1)))
                             break;
-                        const int first = w.lk - j * 128;
-                        uint8_t *vt = sgen + L::kV + st * L::kTileBytes;
-                        const int chunks = (128 - first) * 8;
-                        for (int pp = 0; pp < L::kPanels; ++pp)
-                            for (int c = lane; c < chunks; c += 32)
-                                *reinterpret_cast<uint4 *>(vt + pp * L::kPanelBytes + (first + (c >> 3)) * 128 +
-                                                           (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                        uint8_t *tile = sgen + (is_k ? L::kK : L::kV) + st * L::kTileBytes;
+                        if (fix) // the straddling box's new keys, from the inputs
+                            patch_new_keys<D>(tile, is_k ? p.k_in : p.v_in, w, j, box_rows, p.num_kv_heads, lane);
+                        if (zero) {
+                            // V rows of keys past the sequence end may hold anything (even NaN
+                            // bit patterns); zero them so that P = 0 cannot turn them into NaN in O.
+                            const int first = w.lk - j * 128;
+                            const int chunks = (128 - first) * 8;
+                            for (int pp = 0; pp < L::kPanels; ++pp)
+                                for (int c = lane; c < chunks; c += 32)
+                                    *reinterpret_cast<uint4 *>(tile + pp * L::kPanelBytes + (first + (c >> 3)) * 128 +
+                                                               (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+                        }
                         ptx::fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0)
-                            ptx::mbar_arrive(bars.v_tail(st));
+                            ptx::mbar_arrive(is_k ? bars.k_fix(st) : bars.v_tail(st));
                     }
                 }
             }
@@ -790,13 +849,19 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             // ring positions kept as counters (no division in the issue loop)
             int ks = 0, kph = 0, vs = 0, vph = 0;
             uint32_t np = 0;       // bit t: parity of the P tiles of query tile t consumed so far
-            uint32_t tailpar = 0;  // bit s: parity of the tail tiles V slot s has held
+            uint32_t tailpar = 0;  // bit s: parity of the tail (or patched) tiles V slot s has held
+            uint32_t fixpar = 0;   // bit s: parity of the patched tiles K slot s has held
             int E = 0;             // first release event of the current item
             bool ok = true;
             while (ok && items.more()) {
                 const Item w = items.next();
                 const uint32_t qpar = w.ord & 1;
+                const int jfix = straddle_tile(w, p.fused, box_rows);
                 ok = wwait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) && wwait(bars.k_full(ks), kph);
+                if (ok && jfix == 0) { // key tile 0's straddling box patched
+                    ok = wwait(bars.k_fix(ks), (fixpar >> ks) & 1u);
+                    fixpar ^= 1u << ks;
+                }
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
@@ -830,7 +895,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                         if (!v_ready) {
                             if (!(ok = wwait(bars.v_full(vs), vph)))
                                 return;
-                            if (!I8 && w.tail && j == w.nkt - 1) {
+                            if (!I8 && ((w.tail && j == w.nkt - 1) || j == jfix)) {
                                 if (!(ok = wwait(bars.v_tail(vs), (tailpar >> vs) & 1u)))
                                     return;
                                 tailpar ^= 1u << vs;
@@ -845,6 +910,11 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                             if (!k_next) {
                                 if (!(ok = wwait(bars.k_full(ks), kph)))
                                     return;
+                                if (j + 1 == jfix) { // that key tile's straddling box patched
+                                    if (!(ok = wwait(bars.k_fix(ks), (fixpar >> ks) & 1u)))
+                                        return;
+                                    fixpar ^= 1u << ks;
+                                }
                                 ptx::tc_fence_after();
                                 k_next = true;
                             }
@@ -1083,7 +1153,10 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
                              (uint64_t)d.num_heads * D * 2, 64, (uint32_t)G, (uint32_t)a.rows_per_tile, sw, "q")) !=
         PA_OK)
         return rc;
-    const uint32_t box_rows = d.block_size < 128 ? (uint32_t)d.block_size : 128u;
+    // One box per physical block (or per 128-key tile); for a fused store whose cached
+    // prefixes end inside a box, boxes of 16 rows, so a straddling box has at most 15 new
+    // rows for the producer to patch in.
+    const uint32_t box_rows = !I8 && a.k_in && a.small_boxes ? 16u : d.block_size < 128 ? (uint32_t)d.block_size : 128u;
     if constexpr (I8) { // raw codes: one head's D bytes x box_rows rows, unswizzled
         constexpr CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
         constexpr CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -1121,6 +1194,7 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     p.group = G;
     p.rows_per_tile = a.rows_per_tile;
     p.block_size = d.block_size;
+    p.box_rows = (int32_t)box_rows;
     p.max_blocks = a.max_blocks_per_seq;
     p.num_slots = (int32_t)rows;
     p.num_kv_heads = d.num_kv_heads;

@@ -269,8 +269,7 @@ def pa_prefill_varlen(dims: pa_dims, q, k_cache, v_cache, plan: PrefillPlan, sca
 
 def pa_prefill_varlen_fused(dims: pa_dims, q, k, v, k_cache, v_cache, plan: PrefillPlan, scale: float, out,
                             stream=None):
-    """pa_store_kvcache of the new tokens' k/v at the plan's slots + pa_prefill_varlen (one launch
-    when plan.meta.prefix_aligned)."""
+    """pa_store_kvcache of the new tokens' k/v at the plan's slots + pa_prefill_varlen, in one launch."""
     m = plan.meta
     _check(lib().pa_prefill_varlen_fused(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
                                          plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),

@@ -23,7 +23,7 @@ def test_library_exports_every_declared_symbol():
     for name in declared:
         assert hasattr(lib, name), name
     assert set(pa.EXPORTS) == declared
-    assert pa.pa_version() == 0x000200
+    assert pa.pa_version() == 0x000300
 
 
 def test_struct_sizes_match_header_layout():

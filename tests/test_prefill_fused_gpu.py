@@ -56,7 +56,7 @@ def _run(w, row_select=None, compare_separate=True):
 @pytest.mark.parametrize("name", ["tiny", "qwen3_prefill_32", "qwen3_prefill_128", "qwen3_prefill_256",
                                   "qwen3_prefix", "qwen3_chunked"])
 def test_fused_prefill_configs(name):
-    """Configs with and without cached prefixes (qwen3_chunked: unaligned, the two-launch order)."""
+    """Configs with and without cached prefixes (qwen3_chunked: prefixes ending inside a block)."""
     w = workloads.make(name, device="cuda")
     for batch, out, sep, ref, plan, _ in _run(w):
         if batch.kind == "prefill":
@@ -71,6 +71,12 @@ FUSED_CASES = [  # seed, num_seqs, hq, hkv, d, bs, max_len, cached
     (704, 4, 4, 4, 64, 256, 700, "aligned"),
     (705, 6, 28, 4, 128, 16, 520, "random"),
     (706, 2, 16, 8, 128, 128, 1300, "aligned"),
+    # cached prefixes ending anywhere (the straddling key box patched from the inputs)
+    (707, 5, 28, 4, 128, 16, 700, "random"),
+    (708, 4, 16, 8, 128, 256, 1500, "random"),
+    (709, 3, 8, 2, 64, 1024, 2100, "random"),
+    (710, 6, 14, 2, 128, 64, 900, "random"),
+    (711, 7, 7, 1, 64, 32, 400, "random"),
 ]
 
 
@@ -218,3 +224,55 @@ def test_fused_prefill_replayed_from_a_cuda_graph():
         assert torch.equal(kc.view(n, -1)[torch.as_tensor(sm, device="cuda").long()],
                            kc2.view(n, -1)[torch.as_tensor(sm, device="cuda").long()])
     assert pa.pa_read_device_error() == 0
+
+
+def _launches(fn, stream):
+    """Nodes of the graph that stream capture of fn() records (each launch is one node)."""
+    import ctypes
+    import glob
+    import os
+    rt = None
+    cands = ["libcudart.so", "libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so"]
+    cands += glob.glob(os.path.join(os.path.dirname(torch.__file__), "lib", "libcudart*.so*"))
+    for c in cands:
+        try:
+            rt = ctypes.CDLL(c)
+            break
+        except OSError:
+            continue
+    if rt is None:
+        pytest.skip("no CUDA runtime library to capture with")
+    h = ctypes.c_void_p(stream.cuda_stream)
+    assert rt.cudaStreamBeginCapture(h, 2) == 0  # relaxed capture mode
+    try:
+        fn()
+    finally:
+        graph = ctypes.c_void_p()
+        rc = rt.cudaStreamEndCapture(h, ctypes.byref(graph))
+    assert rc == 0
+    n = ctypes.c_size_t(0)
+    assert rt.cudaGraphGetNodes(graph, None, ctypes.byref(n)) == 0
+    rt.cudaGraphDestroy(graph)
+    return n.value
+
+
+def test_fused_prefill_unaligned_prefixes_are_one_launch():
+    """The chunked-prefill batch (prefixes ~ U{0..1024}, block 256): the call records one launch
+    (stream capture), the cache equals the oracle's store and the output is bitwise the
+    two-launch one."""
+    w = workloads.make("qwen3_chunked", device="cuda")
+    batch = w.batches[0]
+    dims = dims_of(w, batch)
+    plan = pa.pa_pack_prefill(dims, batch.seq_lens, batch.query_lens, batch.block_lists).upload("cuda")
+    assert plan.meta.prefix_aligned == 0
+    kc, vc = w.pool.k_cache.clone(), w.pool.v_cache.clone()
+    out = torch.empty_like(batch.q)
+    pa.pa_prefill_varlen_fused(dims, batch.q, batch.k, batch.v, kc, vc, plan, batch.scale, out)  # warm-up
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    n = _launches(lambda: pa.pa_prefill_varlen_fused(dims, batch.q, batch.k, batch.v, kc, vc, plan, batch.scale, out,
+                                                     stream=s), s)
+    assert n == 1, f"{n} launches"
+    (b, out2, sep, ref, _, _), = _run(w)
+    assert torch.equal(out, out2) and torch.equal(out, sep)
+    assert_close(out, ref, what="fused qwen3 chunked (one launch)")
