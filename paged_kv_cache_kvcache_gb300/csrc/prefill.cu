@@ -29,11 +29,12 @@
 //    rows past the sequence end are zeroed before use.
 //  * warp 8: K TMA producer; warp 10: V producer; warp 11: Q producer (it
 //    refills a query tile as soon as the item's last score MMA of that tile
-//    has read it); warp 9: TMEM owner and the MMA issuer.  The whole warp runs
-//    the issue loop, converged, and an elected lane issues each tcgen05.mma and
-//    commit: a 128 x 128 x 16 product runs 64 cycles, and a lone lane in a
-//    divergent branch spends nearly as long issuing it, which left no slack
-//    for the waits and commits between products.  Each query tile t owns 256
+//    has read it); warp 9: TMEM owner and the MMA issuer.  In the bf16 kernel
+//    the whole warp runs the issue loop, converged, and an elected lane issues
+//    each tcgen05.mma and commit: a 128 x 128 x 16 product runs 64 cycles, and a
+//    lone lane in a divergent branch spends nearly as long issuing it, which
+//    left no slack for the waits and commits between products (the 16-warp INT8
+//    kernel measured faster with lane 0 alone).  Each query tile t owns 256
 //    TMEM columns: S_t (128 fp32 columns, reused for P_t) and O_t.  The issue
 //    order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core busy on
 //    one tile while the other tile's softmax runs (ping-pong).  Because the
@@ -813,9 +814,11 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 if (lane == 0)
                     ptx::mbar_arrive(bars.q_ready(tq));
             }
-        } else if (warp == kMmaWarp) {
-            // ------------------------------------------------------------ MMA issuer (the whole warp;
-            // one elected lane issues each MMA and commit)
+        } else if (!I8 && warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer (bf16: the whole
+            // warp, one elected lane issuing each MMA and commit; INT8: lane 0 alone, which measured
+            // faster with that kernel's 16 warps)
+
             ItemIter items(p.tiles, p.num_items, P);
             // INT8 cache: f16 operands (exact codes, f16 Q and P)
             constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
@@ -931,6 +934,123 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                     if (!ok)
                         break;
                     ptx::mma_commit_warp(bars.released(E + j + 1)); // V tile j and K tile j + 1 read
+                    if (++vs == L::kVStages) {
+                        vs = 0;
+                        vph ^= 1;
+                    }
+                    if (k_next && ++ks == L::kKStages) {
+                        ks = 0;
+                        kph ^= 1;
+                    }
+                }
+                E += w.nkt + 1;
+            }
+        } else if (I8 && warp == kMmaWarp && lane == 0) {
+            // ------------------------------------------------------------ INT8: MMA issuer (lane 0)
+            ItemIter items(p.tiles, p.num_items, P);
+            // INT8 cache: f16 operands (exact codes, f16 Q and P)
+            constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
+            constexpr uint32_t idesc_o = I8 ? ptx::idesc_f16(128, D, 1) : ptx::idesc_bf16(128, D, 1);
+            // Shared-memory descriptors: a constant upper word and a lower word of base
+            // address + the k step's offset.  The base passes through an empty asm so that
+            // it is rebuilt at each use instead of hoisting all 16 k-step descriptors into
+            // registers (this warpgroup runs on few).
+            const uint32_t hi_k = (uint32_t)(ptx::smem_desc(0, 16, 1024, ptx::kSwizzle128B) >> 32);
+            const uint32_t hi_v = (uint32_t)(ptx::smem_desc(0, L::kPanelBytes, 1024, ptx::kSwizzle128B) >> 32);
+            auto desc = [](uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; };
+            auto issue_s = [&](int t, int ks) {
+                uint32_t qa = (uint32_t)ptx::smem_desc(sbase + L::kQ + t * L::kTileBytes, 16, 1024, ptx::kSwizzle128B);
+                uint32_t kb = (uint32_t)ptx::smem_desc(sbase + L::kK + ks * L::kTileBytes, 16, 1024, ptx::kSwizzle128B);
+                asm volatile("" : "+r"(qa), "+r"(kb));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t o = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
+                    ptx::mma_bf16_ss(tmem + t * 256, desc(qa + o, hi_k), desc(kb + o, hi_k), idesc_s, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int t, int vs, bool first) {
+                uint32_t vb = (uint32_t)ptx::smem_desc(sbase + L::kV + vs * L::kTileBytes, L::kPanelBytes, 1024,
+                                                       ptx::kSwizzle128B);
+                asm volatile("" : "+r"(vb));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc(vb + kk * (2048 >> 4), hi_v),
+                                     idesc_o, (!first || kk > 0) ? 1u : 0u);
+            };
+            // ring positions kept as counters (no division in the issue loop)
+            int ks = 0, kph = 0, vs = 0, vph = 0;
+            uint32_t np = 0;       // bit t: parity of the P tiles of query tile t consumed so far
+            uint32_t tailpar = 0;  // bit s: parity of the tail tiles V slot s has held
+            int E = 0;             // first release event of the current item
+            bool ok = true;
+            while (ok && items.more()) {
+                const Item w = items.next();
+                const uint32_t qpar = w.ord & 1;
+                ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) && wait(bars.k_full(ks), kph);
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+                issue_s(0, ks);
+                ptx::mma_commit(bars.s_full(0));
+                // query tile 1 is waited for only now (also when empty: its buffer is
+                // released below, and every load of it must be consumed first)
+                if (!(ok = wait(I8 ? bars.q_ready(1) : bars.q_full(1), qpar)))
+                    break;
+                if (w.nkt1 > 0) {
+                    ptx::tc_fence_after();
+                    issue_s(1, ks);
+                    ptx::mma_commit(bars.s_full(1));
+                }
+                ptx::mma_commit(bars.released(E)); // K tile 0 read by both score MMAs
+                if (w.nkt0 == 1)
+                    ptx::mma_commit(bars.q_free(0));
+                if (w.nkt1 <= 1)
+                    ptx::mma_commit(bars.q_free(1));
+                if (++ks == L::kKStages) {
+                    ks = 0;
+                    kph ^= 1;
+                }
+                for (int j = 0; ok && j < w.nkt; ++j) {
+                    bool v_ready = false, k_next = false;
+                    // one query tile: PV(t, j), then S(t, j + 1) into the same TMEM columns
+                    auto step = [&](const int t, const int ntk) {
+                        if (!(ok = wait(bars.p_full(t), (np >> t) & 1u)))
+                            return;
+                        np ^= 1u << t;
+                        if (!v_ready) {
+                            if (!(ok = wait(bars.v_full(vs), vph)))
+                                return;
+                            if (!I8 && w.tail && j == w.nkt - 1) {
+                                if (!(ok = wait(bars.v_tail(vs), (tailpar >> vs) & 1u)))
+                                    return;
+                                tailpar ^= 1u << vs;
+                            }
+                            v_ready = true;
+                        }
+                        ptx::tc_fence_after();
+                        issue_pv(t, vs, j == 0);
+                        if (j + 1 == ntk)
+                            ptx::mma_commit(bars.o_full(t)); // O_t final
+                        if (j + 1 < ntk) {
+                            if (!k_next) {
+                                if (!(ok = wait(bars.k_full(ks), kph)))
+                                    return;
+                                ptx::tc_fence_after();
+                                k_next = true;
+                            }
+                            issue_s(t, ks);
+                            ptx::mma_commit(bars.s_full(t));
+                            if (j + 2 == ntk)
+                                ptx::mma_commit(bars.q_free(t)); // that was the last read of Q_t
+                        }
+                    };
+                    if (j < w.nkt0)
+                        step(0, w.nkt0);
+                    if (ok && j < w.nkt1)
+                        step(1, w.nkt1);
+                    if (!ok)
+                        break;
+                    ptx::mma_commit(bars.released(E + j + 1)); // V tile j and K tile j + 1 read
                     if (++vs == L::kVStages) {
                         vs = 0;
                         vph ^= 1;
