@@ -432,15 +432,19 @@ __device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int lane)
 }
 
 // Fused store: the new K/V rows of item w's query positions, KV head w.g, copied
-// from the inputs to their cache slots (one warp; each (token, KV head) row
-// belongs to exactly one item).  The kernel itself reads the new keys from the
-// inputs, so nothing here is waited for.
+// from the inputs to their cache slots (one warp; each (token, KV head) row belongs
+// to exactly one item): the positions first, first + step, ...  Warp 11 copies each
+// item's rows after loading its query tiles; the rows of a CTA's last item are split
+// three ways with the K and V producers, which have nothing left to load by then.
+// The kernel itself reads the new keys from the inputs, so nothing here is waited for.
 template <int D>
-__device__ __forceinline__ void store_item_rows(const PfParams &p, const Item &w, int lane)
+__device__ __forceinline__ void store_item_rows(const PfParams &p, const Item &w, int lane, int first = 0,
+                                                int step = 1)
 {
     constexpr int VPR = D / 8; // 16-byte vectors per row of one head
     constexpr int kU = 4;      // vectors of K and of V in flight per lane
-    const int total = (w.npos0 + w.npos1) * VPR;
+    const int npos = (w.npos0 + w.npos1 - first + step - 1) / step;
+    const int total = npos * VPR;
     const size_t hkv = (size_t)p.num_kv_heads;
     for (int i0 = lane; i0 < total; i0 += 32 * kU) {
         uint4 kx[kU], vx[kU];
@@ -450,7 +454,7 @@ __device__ __forceinline__ void store_item_rows(const PfParams &p, const Item &w
             const int i = i0 + 32 * u;
             to[u] = ~(size_t)0;
             if (i < total) {
-                const int row = w.cq0 + w.q0 + i / VPR;
+                const int row = w.cq0 + w.q0 + first + (i / VPR) * step;
                 const int slot = __ldg(p.slot_mapping + row);
                 const size_t from = ((size_t)row * hkv + w.g) * VPR + i % VPR;
                 kx[u] = __ldg(p.k_in + from);
@@ -672,8 +676,8 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 }
                 if (ok && lane == 0 && items.more())
                     prefetch_query_tiles<D, I8>(&tm_q, items.peek(), G, P);
-                if (ok && p.fused)
-                    store_item_rows<D>(p, w, lane);
+                if (ok && p.fused) // the CTA's last item: a third of its rows (the producers copy the rest)
+                    store_item_rows<D>(p, w, lane, 0, items.more() ? 1 : 3);
             }
         } else if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
             // ------------------------------------------------------------ bf16: K and V producers
@@ -745,6 +749,10 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                     }
                 }
             }
+            // fused store: this producer's third of the rows of the CTA's last item (its work
+            // entry is still the iterator's last one)
+            if (ok && p.fused && items.ord > 0)
+                store_item_rows<D>(p, items.decode(items.ord - 1), lane, is_k ? 1 : 2, 3);
         } else if (I8 && warp == kLoaderWarp) {
             // ------------------------------------------------------------ INT8: TMA loader (Q, K codes, V codes)
             ItemIter items(p.tiles, p.num_items, P);
