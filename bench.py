@@ -45,6 +45,7 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 NCU_TRAFFIC = {"qwen25": {"prefill": 233.6e6, "decode": 4.334e9}}
 NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": 211.2e6, "decode": 2.214e9}}
 NCU_TRAFFIC_FUSED_PREFILL = {"qwen25": 268.9e6}
+NCU_TRAFFIC_INT8_FUSED_PREFILL = {}
 NCU_TRAFFIC_COPY_BLOCKS = 488.3e6  # 268.5 MB read + 219.7 MB written (part of the writes still in L2 at exit)
 
 
@@ -68,7 +69,8 @@ def parse():
                     help="cache format: bf16, or int8 codes + fp16 scales (quantising store, fused-dequant "
                          "prefill and decode)")
     ap.add_argument("--prefill-path", choices=["store+prefill", "fused"], default="fused",
-                    help="bf16 prompt batch: pa_store_kvcache + pa_prefill_varlen, or pa_prefill_varlen_fused")
+                    help="prompt batch: store + prefill (two launches), or the fused call "
+                         "(pa_prefill_varlen_fused; INT8: pa_prefill_varlen_int8_fused)")
     ap.add_argument("--decode-path", choices=["store+decode", "fused", "mixed"], default="store+decode",
                     help="fused: store and decode in one launch (pa_decode_fused / pa_decode_int8_fused); "
                          "mixed (bf16): the decode rows join the prefill rows as Lq = 1 varlen rows of one "
@@ -162,7 +164,7 @@ class Step:
         self.pa = pa
         self.s = stream
         self.int8, self.fused, self.mixed = kv == "int8", fused, mixed
-        self.prefill_fused = prefill_fused and not self.int8 and not mixed
+        self.prefill_fused = prefill_fused and not mixed
         self.wp, self.wd = wp, wd
         self.bp, self.bd = wp.batches[0], wd.batches[0]
         pp, pd = wp.pool, wd.pool
@@ -230,7 +232,9 @@ class Step:
         plan = pa.pa_pack_prefill(self.dims_p, self.bp.seq_lens, self.bp.query_lens, self.blocks_p,
                                   into=self.plans_p[slot]).upload(stream=s)
         self.pipe_ev["p"][slot].record(s)
-        if self.int8:
+        if self.int8 and self.prefill_fused:
+            pa.pa_prefill_varlen_int8_fused(self.dims_p, q, k, v, *self.c8_p, plan, self.bp.scale, out, stream=s)
+        elif self.int8:
             pa.pa_store_kvcache_int8(self.dims_p, k, v, *self.c8_p, plan.slot_mapping, self.bp.num_tokens, stream=s)
             pa.pa_prefill_varlen_int8(self.dims_p, q, *self.c8_p, plan, self.bp.scale, out, stream=s)
         elif self.prefill_fused:
@@ -316,7 +320,11 @@ class Step:
             self._stage(1 - k, phase)
             return
         plan_p = self.plans_p[k]
-        if self.int8:
+        if self.int8 and self.prefill_fused:  # quantising store + INT8 prefill in one launch
+            rec("pk0")
+            pa.pa_prefill_varlen_int8_fused(self.dims_p, self.bp.q, self.bp.k, self.bp.v, *self.c8_p, plan_p,
+                                            self.bp.scale, self.out_p, stream=s)
+        elif self.int8:
             pa.pa_store_kvcache_int8(self.dims_p, self.bp.k, self.bp.v, *self.c8_p, plan_p.slot_mapping,
                                      self.bp.num_tokens, stream=s)
             rec("pk0")
@@ -682,10 +690,16 @@ def main():
     traffic = {} if args.decode_path in ("fused", "mixed") else \
         (NCU_TRAFFIC_INT8 if int8 else NCU_TRAFFIC).get(args.workload, {})
     if step.prefill_fused:
-        traffic = {"prefill": NCU_TRAFFIC_FUSED_PREFILL.get(args.workload), "decode": traffic.get("decode")}
-    roof_p = {"kernel": ("pa_prefill_varlen_int8 (prefill_kernel<128,true>, f16 MMAs)" if int8 else
-                         "pa_prefill_varlen_fused (prefill_kernel<128,false>, store of the new K/V fused)"
-                         if step.prefill_fused else "pa_prefill_varlen (prefill_kernel<128,false>)"),
+        traffic = {"prefill": (NCU_TRAFFIC_INT8_FUSED_PREFILL if int8 else NCU_TRAFFIC_FUSED_PREFILL).get(args.workload),
+                   "decode": traffic.get("decode")}
+    if int8:
+        pk_name = ("pa_prefill_varlen_int8_fused (prefill_kernel<128,true>: quantising store pass, grid barrier, "
+                   "INT8 prefill; f16 MMAs)" if step.prefill_fused else
+                   "pa_prefill_varlen_int8 (prefill_kernel<128,true>, f16 MMAs)")
+    else:
+        pk_name = ("pa_prefill_varlen_fused (prefill_kernel<128,false>, store of the new K/V fused)"
+                   if step.prefill_fused else "pa_prefill_varlen (prefill_kernel<128,false>)")
+    roof_p = {"kernel": pk_name,
               "bound": "tensor", "achieved": round(pk_tflops, 2),
               "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(pk_tflops / bf16_peak, 4),
               "peak_source": f"{peak_src} bf16_tflops (burst; f16 has the same nominal rate)",

@@ -87,6 +87,10 @@ typedef struct pa_prefill_meta {
                                    first query row, KV head, key tiles, first packed
                                    query row of the sequence, query length, key length, 0 */
     uint64_t total_bytes;       /* size of the image */
+    uint64_t off_grid_sync;     /* uint32 [2], 0 in the image: arrival count and
+                                   generation of the grid barrier of
+                                   pa_prefill_varlen_int8_fused (the count is back
+                                   at 0 after every launch) */
 } pa_prefill_meta;
 
 /* Packed decode metadata (one query token per sequence). */
@@ -364,6 +368,41 @@ int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cac
                            const pa_prefill_meta *meta, const int32_t *tiles, pa_stream_t stream);
 
 /*
+ * pa_prefill_varlen_int8_fused — pa_store_kvcache_int8 of the new tokens
+ * followed by pa_prefill_varlen_int8, in one launch, with the same codes,
+ * scales and output bit for bit.  Source: "面试问答准备: nano-vLLM 推理引擎优化",
+ * Q3 (the INT8 cache's prefill cost comes from work outside the attention
+ * kernel) and "手搓 vLLM 推理引擎", Step 4 (store_kvcache, then attention over
+ * the cache).  A new key row is read by every later query of its sequence, so
+ * the launch quantises each new (token, KV head) row once, before any
+ * attention: it is a cooperative launch (all CTAs resident at once, at most
+ * one per SM) whose warps first run the store's quantiser over all rows, then
+ * meet at a grid barrier and run pa_prefill_varlen_int8 over the cache.
+ *   k, v:          device bf16 [meta->total_q][num_kv_heads][head_dim], row t
+ *                  the key/value of packed query row t
+ *   slot_mapping:  device int32 [meta->total_q] (dev + meta->off_slot_mapping);
+ *                  -1 skips the row, a slot outside [-1, num_blocks*block_size)
+ *                  is skipped and flagged (pa_read_device_error bit 0)
+ *   grid_sync:     device uint32 [2] at dev + meta->off_grid_sync (0 in the
+ *                  packed image; the launch leaves the count at 0, so the
+ *                  uploaded plan may be launched again).  Two launches that
+ *                  share one plan buffer must not overlap on the GPU (order
+ *                  them on one stream).
+ * The barrier's wait is bounded (2 s, which only a CTA that never arrives
+ * could reach): if it runs out, bit 1 of the device error word is set, no
+ * attention runs and `out` is undefined.  PA_ERR_CUDA if the device cannot
+ * host the cooperative launch.  Other arguments, errors and numerics as
+ * pa_prefill_varlen_int8 and pa_store_kvcache_int8; the new tokens' slots
+ * must not hold keys that a sequence of the call reads from the cache.
+ */
+int pa_prefill_varlen_int8_fused(const pa_dims *dims, const void *q, const void *k, const void *v,
+                                 void *k_cache, void *v_cache, void *k_scale, void *v_scale,
+                                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                 const int32_t *block_tables, const int32_t *slot_mapping, float scale,
+                                 void *out, const pa_prefill_meta *meta, const int32_t *tiles,
+                                 uint32_t *grid_sync, pa_stream_t stream);
+
+/*
  * pa_decode_int8_fused — pa_store_kvcache_int8 followed by pa_decode_int8 in
  * one launch: quantises k[b], v[b] (bf16 [num_seqs][num_kv_heads][head_dim],
  * the new token of each sequence) into cache row slot_mapping[b] (codes and
@@ -465,10 +504,12 @@ int pa_selftest_bounded_wait(uint32_t timeout_us, int arrive_first, pa_stream_t 
  */
 int pa_stream_read(const void *src, size_t bytes, uint32_t *sink, pa_stream_t stream);
 
-/* Library version, e.g. 0x000300 for 0.3.0.  0.2.0 added pa_prefill_varlen_fused
+/* Library version, e.g. 0x000400 for 0.4.0.  0.2.0 added pa_prefill_varlen_fused
  * and gave pa_prefill_meta's spare field its meaning (prefix_aligned); 0.3.0
  * made pa_prefill_varlen_fused one launch for any cached prefix and added
- * pa_stream_read. */
+ * pa_stream_read; 0.4.0 added pa_prefill_varlen_int8_fused and
+ * pa_prefill_meta.off_grid_sync (a field after total_bytes: the earlier
+ * fields keep their offsets). */
 int pa_version(void);
 
 #ifdef __cplusplus

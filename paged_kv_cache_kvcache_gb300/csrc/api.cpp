@@ -60,7 +60,7 @@ using namespace pa;
 
 extern "C" const char *pa_last_error_string(void) { return g_err; }
 
-extern "C" int pa_version(void) { return 0x000300; }
+extern "C" int pa_version(void) { return 0x000400; }
 
 extern "C" int pa_upload(void *dev_dst, const void *host_src, size_t bytes, pa_stream_t stream)
 {
@@ -194,6 +194,34 @@ extern "C" int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const 
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8: scales must be 16-byte aligned");
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    return launch_prefill_int8(a, stream);
+}
+
+extern "C" int pa_prefill_varlen_int8_fused(const pa_dims *dims, const void *q, const void *k, const void *v,
+                                            void *k_cache, void *v_cache, void *k_scale, void *v_scale,
+                                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                            const int32_t *block_tables, const int32_t *slot_mapping, float scale,
+                                            void *out, const pa_prefill_meta *meta, const int32_t *tiles,
+                                            uint32_t *grid_sync, pa_stream_t stream)
+{
+    PrefillArgs a;
+    bool nothing = false;
+    int rc = prepare_prefill("pa_prefill_varlen_int8_fused", dims, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                             block_tables, scale, out, meta, tiles, &a, &nothing);
+    if (rc != PA_OK || nothing)
+        return rc;
+    if (!k || !v || !k_scale || !v_scale || !slot_mapping || !grid_sync)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8_fused: NULL pointer");
+    if (misaligned(k) || misaligned(v) || misaligned(k_scale) || misaligned(v_scale))
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8_fused: tensors and scales must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(grid_sync) % 4 != 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8_fused: grid_sync must be 4-byte aligned");
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.k_in = k;
+    a.v_in = v;
+    a.slot_mapping = slot_mapping;
+    a.grid_sync = grid_sync;
     return launch_prefill_int8(a, stream);
 }
 

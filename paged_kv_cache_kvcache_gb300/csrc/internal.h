@@ -103,13 +103,16 @@ struct PrefillArgs {
     int32_t total_q;
     int32_t max_blocks_per_seq;
     int32_t rows_per_tile;
-    // fused store (bf16 only; NULL otherwise): new tokens' K/V [total_q][Hkv][D] and their slots
+    // fused store (NULL otherwise): new tokens' K/V [total_q][Hkv][D] bf16 and their slots;
+    // INT8 cache: quantised into the codes and scales by a store pass at the start of the
+    // launch, which then meets at a grid barrier on grid_sync (2 words of the plan)
     const void *k_in;
     const void *v_in;
     const int32_t *slot_mapping;
     // fused store with a cached prefix that does not end on a box boundary: fetch keys in
     // boxes of 16 rows, so that the box straddling the prefix end has few rows to patch
     bool small_boxes;
+    uint32_t *grid_sync;
 };
 int launch_prefill(const PrefillArgs &a, void *stream);
 int launch_prefill_int8(const PrefillArgs &a, void *stream);

@@ -157,6 +157,7 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
     meta->off_block_tables = L.take(sizeof(int32_t) * (size_t)num_seqs * mb);
     meta->off_slot_mapping = L.take(sizeof(int32_t) * (size_t)total_q);
     meta->off_tiles = L.take(sizeof(int32_t) * kPrefillItemInts * tiles.size());
+    meta->off_grid_sync = L.take(2 * sizeof(uint32_t));
     meta->total_bytes = L.off;
     if (!host_buf)
         return PA_OK;
@@ -170,6 +171,7 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
     int32_t *bt = reinterpret_cast<int32_t *>(base + meta->off_block_tables);
     int32_t *slots = reinterpret_cast<int32_t *>(base + meta->off_slot_mapping);
     int32_t *tl = reinterpret_cast<int32_t *>(base + meta->off_tiles);
+    std::memset(base + meta->off_grid_sync, 0, 2 * sizeof(uint32_t));
     cu_q[0] = cu_k[0] = 0;
     for (int32_t b = 0; b < num_seqs; ++b) {
         cu_q[b + 1] = cu_q[b] + query_lens[b];

@@ -73,6 +73,17 @@
 //    prefill resumes at any token count) is loaded from the cache and its new
 //    keys' rows are then copied over it from the inputs by the producer before
 //    the MMAs may read it.
+//  * Fused store, INT8 cache (pa_prefill_varlen_int8_fused): the attention
+//    must see each new key as the cache will hold it (codes x fp16 scale), and
+//    a new key row is read by every item that follows it in its sequence, so
+//    the launch quantises each new row once, before any attention: a
+//    cooperative launch (all CTAs resident) whose warps first run the store
+//    kernel's quantiser over all new (token, head group) rows, grid-stride,
+//    then meet at a grid barrier on two words of the plan (arrival count back
+//    at 0 after every use, generation advanced by the last arrival; the wait
+//    is bounded), after which the code tiles come from the cache as in the
+//    unfused kernel.  Codes, scales and output are those of the store kernel
+//    followed by pa_prefill_varlen_int8, bit for bit.
 //  * mbarriers order every hand-off; every wait is bounded and reports a
 //    timeout through a device error word instead of hanging.
 #include <cuda.h>
@@ -83,6 +94,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace pa {
 
@@ -184,6 +196,12 @@ struct PfParams {
     const uint4 *v_in;
     uint4 *k_cache;
     uint4 *v_cache;
+    // fused store, INT8 cache: quantise rows 0 .. total_q-1 of k_in/v_in into the codes
+    // (k_cache/v_cache) and scales (k_scale/v_scale) before the attention; grid_sync: the
+    // plan's two barrier words
+    int32_t store8;
+    int32_t total_q;
+    uint32_t *grid_sync;
 };
 
 // barrier slots (uint64 each) inside the barrier area
@@ -516,6 +534,70 @@ __device__ __forceinline__ void prefetch_query_tiles(const CUtensorMap *tm_q, co
             ptx::tma_prefetch_3d(tm_q, pp * 64, w.g * G, w.cq0 + w.q0 + t * P);
 }
 
+// Grid-wide barrier of a cooperative launch on two words of global memory:
+// words[0] counts arrivals (back at 0 after every use), words[1] is the
+// generation.  Thread 0 of each CTA arrives; the last arrival resets the count
+// and advances the generation, the others wait until it moves (bounded: false
+// after about 2 s, which only a CTA that never arrives could cause).  `flag` is
+// a shared word used to hand the outcome to the CTA.
+__device__ bool grid_barrier(uint32_t *words, volatile uint32_t *flag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        bool ok = true;
+        const uint32_t gen = ptx::ld_acquire_gpu(words + 1);
+        const uint32_t old = ptx::atom_add_acq_rel_gpu(words, 1u);
+        if (old == gridDim.x - 1) {
+            ptx::st_relaxed_gpu(words, 0u);
+            ptx::atom_add_release_gpu(words + 1, 1u);
+        } else {
+            const uint64_t t0 = ptx::globaltimer();
+            while (ptx::ld_acquire_gpu(words + 1) == gen) {
+                if (ptx::globaltimer() - t0 > 2000000000ull) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(128);
+            }
+        }
+        *flag = ok ? 1u : 0u;
+    }
+    __syncthreads();
+    return *flag != 0u;
+}
+
+// INT8 fused store: every warp of the grid quantises (token, head group) units,
+// grid-stride, with the store kernel's quantiser, into the cache slots of
+// slot_mapping (-1 skipped, other out-of-range slots reported in bit 1); then the
+// writes are ordered before the TMA loads of every CTA (proxy fence + grid barrier).
+template <int D>
+__device__ bool int8_store_pass(const PfParams &p, volatile uint32_t *flag)
+{
+    const int lane = threadIdx.x & 31;
+    const int groups = (p.num_kv_heads + quant::kHeadsPerWarp - 1) / quant::kHeadsPerWarp;
+    const int64_t units = (int64_t)p.total_q * groups;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += nwarps) {
+        const int32_t t = (int32_t)(u / groups);
+        const int g0 = (int)(u % groups) * quant::kHeadsPerWarp;
+        const int32_t slot = __ldg(p.slot_mapping + t);
+        if (slot < 0 || slot >= p.num_slots) {
+            if (slot != -1 && lane == 0 && g0 == 0)
+                atomicOr(&g_prefill_error, 2u);
+            continue;
+        }
+        quant::store_token_heads<D>(reinterpret_cast<const uint16_t *>(p.k_in),
+                                    reinterpret_cast<const uint16_t *>(p.v_in), reinterpret_cast<int8_t *>(p.k_cache),
+                                    reinterpret_cast<int8_t *>(p.v_cache), const_cast<__half *>(p.k_scale),
+                                    const_cast<__half *>(p.v_scale), t, g0, slot, p.num_kv_heads, p.block_size, lane);
+    }
+    ptx::fence_proxy_async_global();
+    __threadfence();
+    const bool ok = grid_barrier(p.grid_sync, flag);
+    ptx::fence_proxy_async_global();
+    return ok;
+}
+
 template <int D, bool I8>
 __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -541,6 +623,16 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
     const Waiter wait{abort_flag};
     const int G = p.group;
     const int P = p.rows_per_tile;
+
+    if constexpr (I8) {
+        // fused store: the new rows' codes and scales first, in every CTA (the abort word
+        // carries the barrier's outcome; it is set to 0 below before anything waits on it)
+        if (p.store8 && !int8_store_pass<D>(p, abort_flag)) {
+            if (threadIdx.x == 0)
+                atomicOr(&g_prefill_error, 1u);
+            return;
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -1336,15 +1428,36 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     p.v_in = static_cast<const uint4 *>(a.v_in);
     p.k_cache = static_cast<uint4 *>(const_cast<void *>(a.k_cache));
     p.v_cache = static_cast<uint4 *>(const_cast<void *>(a.v_cache));
+    p.store8 = I8 && a.k_in ? 1 : 0;
+    p.total_q = a.total_q;
+    p.grid_sync = a.grid_sync;
     // persistent: one CTA per SM (shared memory and TMEM admit one), each walking its items
     int sms = 0;
     if (int rc2 = sm_count(&sms))
         return rc2;
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-    prefill_kernel<D, I8><<<(unsigned)grid, kThreadsOf<I8>, L::kSmemBytes, stream>>>(tq, tk, tv, tkin, tvin, p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
+    cudaError_t e;
+    if (p.store8) {
+        // the store pass ends in a grid barrier: every CTA must be resident at once
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kThreadsOf<I8>);
+        cfg.dynamicSmemBytes = L::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, prefill_kernel<D, I8>, tq, tk, tv, tkin, tvin, p);
+    } else {
+        prefill_kernel<D, I8><<<(unsigned)grid, kThreadsOf<I8>, L::kSmemBytes, stream>>>(tq, tk, tv, tkin, tvin, p);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
         return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    }
     return PA_OK;
 }
 

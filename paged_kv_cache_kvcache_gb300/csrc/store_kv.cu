@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "quant.cuh"
 
 namespace pa {
 
@@ -59,45 +60,8 @@ int launch_store_kvcache(const pa_dims &d, const void *k, const void *v, void *k
     return PA_OK;
 }
 
-// INT8 scatter.  Source: "面试问答准备: nano-vLLM 推理引擎优化", Q3 (KV cache
-// quantisation): each head vector gets scale = max|x| / 127 (floored at 1e-8)
-// and codes round(x / scale) in int8; the scale is kept in fp16.  Arithmetic
-// in fp32 with IEEE division, rounding half away from zero, so codes and
-// scales are reproducible bit for bit.  One warp per (token, group of up to
-// kHeadsPerWarp KV heads): the group's K and V loads are all issued before any
-// arithmetic (more bytes in flight per warp than one head's 2 x 2*D), then
-// per head a warp reduction gives max|x| and each lane quantises D/32 values
-// of K and of V.
-constexpr int kHeadsPerWarp = 4;
-
-template <int D>
-__device__ __forceinline__ void quantise_lane(const uint32_t (&r)[D / 64], float a, uint32_t &codes, float &scale)
-{
-    constexpr int E = D / 32; // values per lane
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    scale = fmaxf(__fdiv_rn(a, 127.0f), 1e-8f);
-    codes = 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float x = __uint_as_float(e & 1 ? r[e / 2] & 0xffff0000u : r[e / 2] << 16);
-        const float q = __fdiv_rn(x, scale);
-        const int i = __float2int_rz(q >= 0.f ? __fadd_rn(q, 0.5f) : __fsub_rn(q, 0.5f));
-        codes |= (uint32_t)(i & 0xff) << (8 * e);
-    }
-}
-
-template <int D>
-__device__ __forceinline__ float lane_absmax(const uint32_t (&r)[D / 64])
-{
-    float a = 0.f;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e)
-        a = fmaxf(a, fabsf(__uint_as_float(e & 1 ? r[e / 2] & 0xffff0000u : r[e / 2] << 16)));
-    return a;
-}
-
+// INT8 scatter: the quantiser of quant.cuh (one warp per token and group of up
+// to quant::kHeadsPerWarp KV heads), slots checked as in the bf16 scatter.
 template <int D>
 __global__ void __launch_bounds__(256) store_kvcache_int8_kernel(
     const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, int8_t *__restrict__ k_cache,
@@ -105,59 +69,21 @@ __global__ void __launch_bounds__(256) store_kvcache_int8_kernel(
     const int32_t *__restrict__ slot_mapping, int32_t num_tokens, int32_t num_kv_heads, int32_t block_size,
     int64_t num_slots)
 {
-    constexpr int E = D / 32; // values per lane
-    constexpr int W = E / 2;  // 32-bit words per lane and row
-    const int groups = (num_kv_heads + kHeadsPerWarp - 1) / kHeadsPerWarp;
+    const int groups = (num_kv_heads + quant::kHeadsPerWarp - 1) / quant::kHeadsPerWarp;
     const int64_t w = (int64_t)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= (int64_t)num_tokens * groups)
         return;
     const int32_t t = (int32_t)(w / groups);
-    const int g0 = (int)(w % groups) * kHeadsPerWarp;
+    const int g0 = (int)(w % groups) * quant::kHeadsPerWarp;
     const int32_t slot = __ldg(slot_mapping + t);
     if (slot < 0 || slot >= num_slots) {
         if (slot != -1 && lane == 0 && g0 == 0)
             atomicOr(&g_store_error, 1u);
         return;
     }
-    uint32_t rk[kHeadsPerWarp][W], rv[kHeadsPerWarp][W]; // E bf16 values per lane and head
-#pragma unroll
-    for (int h = 0; h < kHeadsPerWarp; ++h) {
-        if (g0 + h >= num_kv_heads)
-            break;
-        const size_t src = ((size_t)t * num_kv_heads + g0 + h) * D + lane * E;
-        if constexpr (E == 4) {
-            const uint2 a = __ldcs(reinterpret_cast<const uint2 *>(k + src));
-            const uint2 b = __ldcs(reinterpret_cast<const uint2 *>(v + src));
-            rk[h][0] = a.x, rk[h][1] = a.y, rv[h][0] = b.x, rv[h][1] = b.y;
-        } else {
-            rk[h][0] = __ldcs(reinterpret_cast<const unsigned int *>(k + src));
-            rv[h][0] = __ldcs(reinterpret_cast<const unsigned int *>(v + src));
-        }
-    }
-#pragma unroll
-    for (int h = 0; h < kHeadsPerWarp; ++h) {
-        const int g = g0 + h;
-        if (g >= num_kv_heads)
-            break;
-        uint32_t ck, cv;
-        float sk, sv;
-        quantise_lane<D>(rk[h], lane_absmax<D>(rk[h]), ck, sk);
-        quantise_lane<D>(rv[h], lane_absmax<D>(rv[h]), cv, sv);
-        const size_t dst = ((size_t)slot * num_kv_heads + g) * D + lane * E;
-        if constexpr (E == 4) {
-            *reinterpret_cast<uint32_t *>(k_cache + dst) = ck;
-            *reinterpret_cast<uint32_t *>(v_cache + dst) = cv;
-        } else {
-            *reinterpret_cast<uint16_t *>(k_cache + dst) = (uint16_t)ck;
-            *reinterpret_cast<uint16_t *>(v_cache + dst) = (uint16_t)cv;
-        }
-        if (lane == 0) {
-            const size_t si = ((size_t)(slot / block_size) * num_kv_heads + g) * block_size + slot % block_size;
-            k_scale[si] = __float2half_rn(sk);
-            v_scale[si] = __float2half_rn(sv);
-        }
-    }
+    quant::store_token_heads<D>(k, v, k_cache, v_cache, k_scale, v_scale, t, g0, slot, num_kv_heads, block_size,
+                                lane);
 }
 
 int launch_store_kvcache_int8(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,
@@ -165,7 +91,7 @@ int launch_store_kvcache_int8(const pa_dims &d, const void *k, const void *v, vo
                               void *stream)
 {
     const int threads = 256;
-    const int64_t groups = (d.num_kv_heads + kHeadsPerWarp - 1) / kHeadsPerWarp;
+    const int64_t groups = (d.num_kv_heads + quant::kHeadsPerWarp - 1) / quant::kHeadsPerWarp;
     const int64_t blocks = ((int64_t)num_tokens * groups * 32 + threads - 1) / threads;
     auto kern = d.head_dim == 128 ? store_kvcache_int8_kernel<128> : store_kvcache_int8_kernel<64>;
     kern<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(

@@ -23,7 +23,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = 0
 EXPORTS = ("pa_pack_prefill", "pa_pack_decode", "pa_upload", "pa_store_kvcache", "pa_prefill_varlen",
            "pa_decode", "pa_decode_static", "pa_copy_blocks", "pa_store_kvcache_int8", "pa_decode_int8",
            "pa_prefill_varlen_int8", "pa_pack_decode_fixed", "pa_decode_fused", "pa_copy_blocks_int8",
-           "pa_decode_int8_fused", "pa_prefill_varlen_fused",
+           "pa_decode_int8_fused", "pa_prefill_varlen_fused", "pa_prefill_varlen_int8_fused",
            "pa_last_error_string", "pa_read_device_error", "pa_selftest_bounded_wait", "pa_stream_read",
            "pa_version")
 
@@ -41,7 +41,7 @@ class pa_prefill_meta(ctypes.Structure):
                 ("num_tiles", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32), ("prefix_aligned", ctypes.c_int32),
                 ("off_cu_seqlens_q", ctypes.c_uint64), ("off_cu_seqlens_k", ctypes.c_uint64),
                 ("off_block_tables", ctypes.c_uint64), ("off_slot_mapping", ctypes.c_uint64),
-                ("off_tiles", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
+                ("off_tiles", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64), ("off_grid_sync", ctypes.c_uint64)]
 
 
 class pa_decode_meta(ctypes.Structure):
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
             L.pa_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, P, I32, P]
             L.pa_decode_int8.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
             L.pa_prefill_varlen_int8.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
+            L.pa_prefill_varlen_int8_fused.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P,
+                                                       P, P]
             L.pa_last_error_string.argtypes = []
             L.pa_last_error_string.restype = ctypes.c_char_p
             L.pa_read_device_error.argtypes = [P, P]
@@ -356,6 +358,19 @@ def pa_prefill_varlen_int8(dims: pa_dims, q, k_cache, v_cache, k_scale, v_scale,
                                         _ptr(v_scale), plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
                                         plan.dptr(m.off_block_tables), float(scale), _ptr(out), ctypes.byref(m),
                                         plan.dptr(m.off_tiles), _stream(stream)), "pa_prefill_varlen_int8")
+
+
+def pa_prefill_varlen_int8_fused(dims: pa_dims, q, k, v, k_cache, v_cache, k_scale, v_scale, plan: PrefillPlan,
+                                 scale: float, out, stream=None):
+    """pa_store_kvcache_int8 of the new tokens' k/v at the plan's slots + pa_prefill_varlen_int8, in one launch."""
+    m = plan.meta
+    _check(lib().pa_prefill_varlen_int8_fused(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache),
+                                              _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                              plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
+                                              plan.dptr(m.off_block_tables), plan.dptr(m.off_slot_mapping),
+                                              float(scale), _ptr(out), ctypes.byref(m), plan.dptr(m.off_tiles),
+                                              plan.dptr(m.off_grid_sync), _stream(stream)),
+           "pa_prefill_varlen_int8_fused")
 
 
 def pa_decode_int8_fused(dims: pa_dims, q, k, v, k_cache, v_cache, k_scale, v_scale, plan: DecodePlan,

@@ -23,12 +23,14 @@ def test_library_exports_every_declared_symbol():
     for name in declared:
         assert hasattr(lib, name), name
     assert set(pa.EXPORTS) == declared
-    assert pa.pa_version() == 0x000300
+    assert pa.pa_version() == 0x000400
 
 
 def test_struct_sizes_match_header_layout():
     assert ctypes.sizeof(pa.pa_dims) == 20
-    assert ctypes.sizeof(pa.pa_prefill_meta) == 8 * 4 + 6 * 8
+    assert ctypes.sizeof(pa.pa_prefill_meta) == 8 * 4 + 7 * 8
+    # fields added after total_bytes leave the earlier offsets where they were
+    assert pa.pa_prefill_meta.total_bytes.offset == 8 * 4 + 5 * 8
     assert ctypes.sizeof(pa.pa_decode_meta) == 6 * 4 + 7 * 8
 
 
@@ -325,3 +327,40 @@ def test_prefill_fused_rejects_bad_args_without_touching_the_gpu():
     pm.num_tiles = 0  # nothing to do: no launch, no error
     assert L.pa_prefill_varlen_fused(ctypes.byref(dims), None, None, None, None, None, None, None, None, None, f(0.1),
                                      None, ctypes.byref(pm), None, None) == pa.PA_OK
+
+
+def test_prefill_int8_fused_rejects_bad_args_without_touching_the_gpu():
+    dims = pa.make_dims(4, 16, 4, 2, 64)
+    L = pa.lib()
+    pm = pa.pa_prefill_meta()
+    pm.num_tiles, pm.total_q, pm.num_seqs, pm.max_blocks_per_seq, pm.rows_per_tile = 1, 1, 1, 1, 64
+    f = ctypes.c_float
+
+    def call(q=16, k=16, v=16, kc=16, vc=16, ks=16, vs=16, slots=16, scale=0.1, sync=16):
+        return L.pa_prefill_varlen_int8_fused(ctypes.byref(dims), q, k, v, kc, vc, ks, vs, 16, 16, 16, slots,
+                                              f(scale), 16, ctypes.byref(pm), 16, sync, None)
+
+    assert call(k=None) == pa.PA_ERR_INVALID_ARG       # new-token rows
+    assert call(vs=None) == pa.PA_ERR_INVALID_ARG      # scales
+    assert call(slots=None) == pa.PA_ERR_INVALID_ARG   # slot mapping
+    assert call(sync=None) == pa.PA_ERR_INVALID_ARG    # the plan's barrier words
+    assert call(sync=18) == pa.PA_ERR_INVALID_ARG      # barrier words not 4-byte aligned
+    assert call(v=24) == pa.PA_ERR_INVALID_ARG         # misaligned rows
+    assert call(ks=40) == pa.PA_ERR_INVALID_ARG        # misaligned scales
+    assert call(scale=-1.0) == pa.PA_ERR_INVALID_ARG
+    pm.num_tiles = 0  # nothing to do: no launch, no error
+    assert L.pa_prefill_varlen_int8_fused(ctypes.byref(dims), None, None, None, None, None, None, None, None, None,
+                                          None, None, f(0.1), None, ctypes.byref(pm), None, None,
+                                          None) == pa.PA_OK
+
+
+def test_pack_prefill_grid_sync_words_are_zero():
+    """The packed image carries the fused INT8 launch's two barrier words, zeroed, after the work list."""
+    dims = pa.make_dims(64, 16, 4, 2, 64)
+    lens, qlens = [40, 17], [8, 17]
+    blocks = [list(range(i * 8, i * 8 + -(-n // 16))) for i, n in enumerate(lens)]
+    plan = pa.pa_pack_prefill(dims, lens, qlens, blocks, pin=False)
+    m = plan.meta
+    assert m.off_grid_sync >= m.off_tiles + 4 * 8 * m.num_tiles
+    assert m.off_grid_sync % 4 == 0 and m.off_grid_sync + 8 <= m.total_bytes
+    assert list(plan.host_array(m.off_grid_sync, 2)) == [0, 0]
