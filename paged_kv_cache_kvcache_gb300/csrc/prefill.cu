@@ -577,19 +577,38 @@ __device__ bool int8_store_pass(const PfParams &p, volatile uint32_t *flag)
     const int groups = (p.num_kv_heads + quant::kHeadsPerWarp - 1) / quant::kHeadsPerWarp;
     const int64_t units = (int64_t)p.total_q * groups;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += nwarps) {
-        const int32_t t = (int32_t)(u / groups);
-        const int g0 = (int)(u % groups) * quant::kHeadsPerWarp;
-        const int32_t slot = __ldg(p.slot_mapping + t);
-        if (slot < 0 || slot >= p.num_slots) {
-            if (slot != -1 && lane == 0 && g0 == 0)
-                atomicOr(&g_prefill_error, 2u);
-            continue;
+    const uint16_t *k_in = reinterpret_cast<const uint16_t *>(p.k_in);
+    const uint16_t *v_in = reinterpret_cast<const uint16_t *>(p.v_in);
+    // two units per pass, both loaded before either is quantised (one load latency per pair)
+    for (int64_t u0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u0 < units; u0 += 2 * nwarps) {
+        quant::HeadRows<D> r[2];
+        int32_t slot[2];
+        int g0[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int64_t u = u0 + i * nwarps;
+            slot[i] = -1;
+            g0[i] = 0;
+            if (u < units) {
+                const int32_t t = (int32_t)(u / groups);
+                g0[i] = (int)(u % groups) * quant::kHeadsPerWarp;
+                slot[i] = __ldg(p.slot_mapping + t);
+                if (slot[i] >= 0 && slot[i] < p.num_slots)
+                    quant::load_token_heads<D>(k_in, v_in, t, g0[i], p.num_kv_heads, lane, r[i]);
+            }
         }
-        quant::store_token_heads<D>(reinterpret_cast<const uint16_t *>(p.k_in),
-                                    reinterpret_cast<const uint16_t *>(p.v_in), reinterpret_cast<int8_t *>(p.k_cache),
-                                    reinterpret_cast<int8_t *>(p.v_cache), const_cast<__half *>(p.k_scale),
-                                    const_cast<__half *>(p.v_scale), t, g0, slot, p.num_kv_heads, p.block_size, lane);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (slot[i] < 0 || slot[i] >= p.num_slots) {
+                if (slot[i] != -1 && lane == 0 && g0[i] == 0)
+                    atomicOr(&g_prefill_error, 2u);
+                continue;
+            }
+            quant::quantise_token_heads<D>(r[i], reinterpret_cast<int8_t *>(p.k_cache),
+                                           reinterpret_cast<int8_t *>(p.v_cache), const_cast<__half *>(p.k_scale),
+                                           const_cast<__half *>(p.v_scale), g0[i], slot[i], p.num_kv_heads,
+                                           p.block_size, lane);
+        }
     }
     ptx::fence_proxy_async_global();
     __threadfence();

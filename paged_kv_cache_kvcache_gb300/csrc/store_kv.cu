@@ -82,8 +82,9 @@ __global__ void __launch_bounds__(256) store_kvcache_int8_kernel(
             atomicOr(&g_store_error, 1u);
         return;
     }
-    quant::store_token_heads<D>(k, v, k_cache, v_cache, k_scale, v_scale, t, g0, slot, num_kv_heads, block_size,
-                                lane);
+    quant::HeadRows<D> r;
+    quant::load_token_heads<D>(k, v, t, g0, num_kv_heads, lane, r);
+    quant::quantise_token_heads<D>(r, k_cache, v_cache, k_scale, v_scale, g0, slot, num_kv_heads, block_size, lane);
 }
 
 int launch_store_kvcache_int8(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,

@@ -32,6 +32,14 @@ def _special_rows(t, hkv, d, seed):
     # a few fp16 subnormal steps, max|x| ~ 3e-3 one with a few bits (both sides must agree)
     x[6] = 2e-6 * torch.randn(hkv, d, generator=g)
     x[7] = 1e-3 * torch.randn(hkv, d, generator=g)
+    # max|x| = a with a/127 inexact in fp32 and x = +-a/2: x/scale lies within an ulp of 63.5, so
+    # the IEEE quotient alone decides between codes 63 and 64 (for bf16 inputs the only
+    # half-integer quotients besides those of power-of-two scales).  For these four a, x times
+    # the rounded reciprocal of the scale lands on the other side of 63.5 (9, 13: quotient
+    # 63.499996, code 63; 15, 19: quotient 63.5, code 64)
+    for row, a in zip(range(8, 12), (9.0, 13.0 * 2 ** -7, 15.0 * 2 ** 5, 19.0 * 2 ** -20)):
+        x[row] = torch.where(torch.arange(d) % 2 == 0, torch.tensor(a / 2), torch.tensor(-a / 2))[None]
+        x[row, :, 0] = a
     return x.to(torch.bfloat16)
 
 
