@@ -566,49 +566,44 @@ __device__ bool grid_barrier(uint32_t *words, volatile uint32_t *flag)
     return *flag != 0u;
 }
 
-// INT8 fused store: every warp of the grid quantises (token, head group) units,
-// grid-stride, with the store kernel's quantiser, into the cache slots of
+// INT8 fused store: the threads of the grid quantise (tensor, token, KV head) rows,
+// grid-stride, with the store kernel's quantiser (quant::kThreadsPerRow<D> adjacent
+// threads per row), into the cache slots of
 // slot_mapping (-1 skipped, other out-of-range slots reported in bit 1); then the
 // writes are ordered before the TMA loads of every CTA (proxy fence + grid barrier).
 template <int D>
 __device__ bool int8_store_pass(const PfParams &p, volatile uint32_t *flag)
 {
-    const int lane = threadIdx.x & 31;
-    const int groups = (p.num_kv_heads + quant::kHeadsPerWarp - 1) / quant::kHeadsPerWarp;
-    const int64_t units = (int64_t)p.total_q * groups;
-    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    constexpr int TPR = quant::kThreadsPerRow<D>;
+    const int Hkv = p.num_kv_heads;
+    const int64_t rows = (int64_t)p.total_q * Hkv; // per tensor
+    const int64_t nparts = (int64_t)gridDim.x * blockDim.x / TPR;
+    const int h = (int)(threadIdx.x % TPR);
     const uint16_t *k_in = reinterpret_cast<const uint16_t *>(p.k_in);
     const uint16_t *v_in = reinterpret_cast<const uint16_t *>(p.v_in);
-    // two units per pass, both loaded before either is quantised (one load latency per pair)
-    for (int64_t u0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u0 < units; u0 += 2 * nwarps) {
-        quant::HeadRows<D> r[2];
-        int32_t slot[2];
-        int g0[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int64_t u = u0 + i * nwarps;
-            slot[i] = -1;
-            g0[i] = 0;
-            if (u < units) {
-                const int32_t t = (int32_t)(u / groups);
-                g0[i] = (int)(u % groups) * quant::kHeadsPerWarp;
-                slot[i] = __ldg(p.slot_mapping + t);
-                if (slot[i] >= 0 && slot[i] < p.num_slots)
-                    quant::load_token_heads<D>(k_in, v_in, t, g0[i], p.num_kv_heads, lane, r[i]);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            if (slot[i] < 0 || slot[i] >= p.num_slots) {
-                if (slot[i] != -1 && lane == 0 && g0[i] == 0)
-                    atomicOr(&g_prefill_error, 2u);
-                continue;
-            }
-            quant::quantise_token_heads<D>(r[i], reinterpret_cast<int8_t *>(p.k_cache),
-                                           reinterpret_cast<int8_t *>(p.v_cache), const_cast<__half *>(p.k_scale),
-                                           const_cast<__half *>(p.v_scale), g0[i], slot[i], p.num_kv_heads,
-                                           p.block_size, lane);
-        }
+    // row i's values and slot; the next row's are loaded before this one is quantised
+    auto fetch = [&](int64_t i, quant::RowPart &part) {
+        const bool is_v = i >= rows;
+        const int64_t r = is_v ? i - rows : i;
+        quant::load_row_part((is_v ? v_in : k_in) + r * D, h, part);
+        return __ldg(p.slot_mapping + r / Hkv);
+    };
+    int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / TPR;
+    quant::RowPart cur, nxt;
+    int32_t slot = i < 2 * rows ? fetch(i, cur) : -1;
+    for (; i < 2 * rows; i += nparts) {
+        const int32_t next_slot = i + nparts < 2 * rows ? fetch(i + nparts, nxt) : -1;
+        const bool is_v = i >= rows;
+        const int64_t r = is_v ? i - rows : i;
+        const int g = (int)(r % Hkv);
+        if (slot >= 0 && slot < p.num_slots)
+            quant::store_row_part<D>(cur, reinterpret_cast<int8_t *>(is_v ? p.v_cache : p.k_cache),
+                                     const_cast<__half *>(is_v ? p.v_scale : p.k_scale), g, slot, Hkv, p.block_size,
+                                     h);
+        else if (slot != -1 && !is_v && g == 0 && h == 0)
+            atomicOr(&g_prefill_error, 2u);
+        cur = nxt;
+        slot = next_slot;
     }
     ptx::fence_proxy_async_global();
     __threadfence();

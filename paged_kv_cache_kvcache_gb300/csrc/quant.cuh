@@ -6,10 +6,14 @@
 // codes round(x / scale) in int8; the scale is kept in fp16.  Arithmetic in fp32
 // with IEEE division, rounding half away from zero.
 //
-// Work unit: one warp per (token, group of up to kHeadsPerWarp KV heads).  The
-// group's K and V loads are all issued before any arithmetic (more bytes in
-// flight per warp than one head's 2 x 2*D), then per head a warp reduction gives
-// max|x| and each lane quantises D/32 values of K and of V.
+// Work unit: kThreadsPerRow<D> adjacent threads per (token, KV head) row (two at
+// D = 64, four at D = 128: 32 values per thread): each loads its values (four
+// 16-byte loads, all in flight at once), the group combines max|x| with one or
+// two shuffles, and each computes the scale and its codes and stores them with
+// two 16-byte stores.  A warp quantises 8 or 16 rows side by side, so the
+// per-row steps (the max, the scale's division and reciprocal) cost a few
+// instructions per row instead of one per lane and row as when a warp shares a
+// row, and a thread needs few registers.
 #pragma once
 
 #include <cstdint>
@@ -19,19 +23,6 @@
 
 namespace pa {
 namespace quant {
-
-constexpr int kHeadsPerWarp = 4;
-
-// max|x| over the lane's D/32 bf16 values (packed two per word)
-template <int D>
-__device__ __forceinline__ float lane_absmax(const uint32_t (&r)[D / 64])
-{
-    float a = 0.f;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e)
-        a = fmaxf(a, fabsf(__uint_as_float(e & 1 ? r[e / 2] & 0xffff0000u : r[e / 2] << 16)));
-    return a;
-}
 
 // code = trunc(q + 0.5 * sign(q)) with q = x / scale rounded to nearest (IEEE
 // division).  The division is only carried out where it can matter: q' = x *
@@ -52,85 +43,82 @@ __device__ __forceinline__ int code_of(float x, float scale, float rcp)
     return __float2int_rz(q >= 0.f ? __fadd_rn(q, 0.5f) : __fsub_rn(q, 0.5f));
 }
 
-// Warp-wide max of `a`, the fp32 scale, and the lane's D/32 codes packed in one word.
 template <int D>
-__device__ __forceinline__ void quantise_lane(const uint32_t (&r)[D / 64], float a, uint32_t &codes, float &scale)
-{
-    constexpr int E = D / 32; // values per lane
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    scale = fmaxf(__fdiv_rn(a, 127.0f), 1e-8f);
-    const float rcp = __frcp_rn(scale);
-    codes = 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float x = __uint_as_float(e & 1 ? r[e / 2] & 0xffff0000u : r[e / 2] << 16);
-        codes |= (uint32_t)(code_of(x, scale, rcp) & 0xff) << (8 * e);
-    }
-}
+constexpr int kThreadsPerRow = D / 32;
 
-// Token t's K and V rows of heads g0 .. g0 + kHeadsPerWarp - 1 into registers
-// (whole warp; D/32 bf16 values per lane and head).  k, v: bf16 bits [tokens][Hkv][D].
-template <int D>
-struct HeadRows {
-    uint32_t k[kHeadsPerWarp][D / 64], v[kHeadsPerWarp][D / 64];
+// The calling thread's 32 values (part h of kThreadsPerRow<D>) of one row of D bf16
+// values: four 16-byte loads, issued at once.
+struct RowPart {
+    uint4 v[4];
 };
 
-template <int D>
-__device__ __forceinline__ void load_token_heads(const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
-                                                 int32_t t, int g0, int num_kv_heads, int lane, HeadRows<D> &r)
+__device__ __forceinline__ void load_row_part(const uint16_t *__restrict__ row, int h, RowPart &p)
 {
-    constexpr int E = D / 32; // values per lane
 #pragma unroll
-    for (int h = 0; h < kHeadsPerWarp; ++h) {
-        if (g0 + h >= num_kv_heads)
-            break;
-        const size_t src = ((size_t)t * num_kv_heads + g0 + h) * D + lane * E;
-        if constexpr (E == 4) {
-            const uint2 a = __ldcs(reinterpret_cast<const uint2 *>(k + src));
-            const uint2 b = __ldcs(reinterpret_cast<const uint2 *>(v + src));
-            r.k[h][0] = a.x, r.k[h][1] = a.y, r.v[h][0] = b.x, r.v[h][1] = b.y;
-        } else {
-            r.k[h][0] = __ldcs(reinterpret_cast<const unsigned int *>(k + src));
-            r.v[h][0] = __ldcs(reinterpret_cast<const unsigned int *>(v + src));
-        }
-    }
+    for (int i = 0; i < 4; ++i)
+        p.v[i] = __ldcs(reinterpret_cast<const uint4 *>(row + 32 * h) + i);
 }
 
-// Quantise loaded rows into cache row `slot` (0 <= slot < num_blocks * block_size,
-// checked by the caller): codes into k_cache/v_cache [slot][Hkv][D], fp16 scales
-// into k_scale/v_scale [slot / block_size][Hkv][slot % block_size].
+// Quantises a loaded part into its 32 codes of the row (codes: the row's D int8
+// codes, 16-byte aligned); returns the row's fp32 scale (the caller stores its fp16
+// copy).  The kThreadsPerRow<D> threads of a row (adjacent lanes) call it together.
 template <int D>
-__device__ __forceinline__ void quantise_token_heads(const HeadRows<D> &r, int8_t *__restrict__ k_cache,
-                                                     int8_t *__restrict__ v_cache, __half *__restrict__ k_scale,
-                                                     __half *__restrict__ v_scale, int g0, int32_t slot,
-                                                     int num_kv_heads, int block_size, int lane)
+__device__ __forceinline__ float quantise_row_part(const RowPart &p, int8_t *__restrict__ codes, int h)
 {
-    constexpr int E = D / 32; // values per lane
+    auto word = [&](int e) { // the 32-bit word holding values 2e and 2e + 1
+        const uint4 &u = p.v[e >> 2];
+        return (e & 3) == 0 ? u.x : (e & 3) == 1 ? u.y : (e & 3) == 2 ? u.z : u.w;
+    };
+    float m[4]; // a tree of maxima: max is exact, any order gives the same value
 #pragma unroll
-    for (int h = 0; h < kHeadsPerWarp; ++h) {
-        const int g = g0 + h;
-        if (g >= num_kv_heads)
-            break;
-        uint32_t ck, cv;
-        float sk, sv;
-        quantise_lane<D>(r.k[h], lane_absmax<D>(r.k[h]), ck, sk);
-        quantise_lane<D>(r.v[h], lane_absmax<D>(r.v[h]), cv, sv);
-        const size_t dst = ((size_t)slot * num_kv_heads + g) * D + lane * E;
-        if constexpr (E == 4) {
-            *reinterpret_cast<uint32_t *>(k_cache + dst) = ck;
-            *reinterpret_cast<uint32_t *>(v_cache + dst) = cv;
-        } else {
-            *reinterpret_cast<uint16_t *>(k_cache + dst) = (uint16_t)ck;
-            *reinterpret_cast<uint16_t *>(v_cache + dst) = (uint16_t)cv;
-        }
-        if (lane == 0) {
-            const size_t si = ((size_t)(slot / block_size) * num_kv_heads + g) * block_size + slot % block_size;
-            k_scale[si] = __float2half_rn(sk);
-            v_scale[si] = __float2half_rn(sv);
+    for (int i = 0; i < 4; ++i) {
+        m[i] = 0.f;
+#pragma unroll
+        for (int e = 4 * i; e < 4 * i + 4; ++e) {
+            const uint32_t w = word(e);
+            m[i] = fmaxf(m[i], fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xffff0000u))));
         }
     }
+    float a = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+    // the row's other parts, in the adjacent lanes of the group
+    constexpr int TPR = kThreadsPerRow<D>;
+    const uint32_t group = ((1u << TPR) - 1) << (threadIdx.x & (32 - TPR));
+#pragma unroll
+    for (int o = 1; o < TPR; o <<= 1)
+        a = fmaxf(a, __shfl_xor_sync(group, a, o));
+    const float scale = fmaxf(__fdiv_rn(a, 127.0f), 1e-8f);
+    const float rcp = __frcp_rn(scale);
+#pragma unroll
+    for (int o = 0; o < 2; ++o) { // 16 codes per store
+        uint32_t c[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t w0 = word(8 * o + 2 * k), w1 = word(8 * o + 2 * k + 1);
+            const int c0 = code_of(__uint_as_float(w0 << 16), scale, rcp);
+            const int c1 = code_of(__uint_as_float(w0 & 0xffff0000u), scale, rcp);
+            const int c2 = code_of(__uint_as_float(w1 << 16), scale, rcp);
+            const int c3 = code_of(__uint_as_float(w1 & 0xffff0000u), scale, rcp);
+            c[k] = (uint32_t)(c0 & 0xff) | (uint32_t)(c1 & 0xff) << 8 | (uint32_t)(c2 & 0xff) << 16 |
+                   (uint32_t)(c3 & 0xff) << 24;
+        }
+        reinterpret_cast<uint4 *>(codes + 32 * h)[o] = make_uint4(c[0], c[1], c[2], c[3]);
+    }
+    return scale;
+}
+
+// Part h (loaded in p) of the K or V row of token t, KV head g, quantised into cache
+// row `slot` (0 <= slot < num_blocks * block_size, checked by the caller): codes
+// into codes_cache [slot][Hkv][D], the fp16 scale (written by part 0) into scales
+// [slot / block_size][Hkv][slot % block_size].
+template <int D>
+__device__ __forceinline__ void store_row_part(const RowPart &p, int8_t *__restrict__ codes_cache,
+                                               __half *__restrict__ scales, int g, int32_t slot, int num_kv_heads,
+                                               int block_size, int h)
+{
+    const float scale = quantise_row_part<D>(p, codes_cache + ((size_t)slot * num_kv_heads + g) * D, h);
+    if (h == 0)
+        scales[((size_t)(slot / block_size) * num_kv_heads + g) * block_size + slot % block_size] =
+            __float2half_rn(scale);
 }
 
 } // namespace quant

@@ -60,8 +60,8 @@ int launch_store_kvcache(const pa_dims &d, const void *k, const void *v, void *k
     return PA_OK;
 }
 
-// INT8 scatter: the quantiser of quant.cuh (one warp per token and group of up
-// to quant::kHeadsPerWarp KV heads), slots checked as in the bf16 scatter.
+// INT8 scatter: the quantiser of quant.cuh, kThreadsPerRow<D> adjacent threads
+// per (tensor, token, KV head) row, slots checked as in the bf16 scatter.
 template <int D>
 __global__ void __launch_bounds__(256) store_kvcache_int8_kernel(
     const uint16_t *__restrict__ k, const uint16_t *__restrict__ v, int8_t *__restrict__ k_cache,
@@ -69,22 +69,27 @@ __global__ void __launch_bounds__(256) store_kvcache_int8_kernel(
     const int32_t *__restrict__ slot_mapping, int32_t num_tokens, int32_t num_kv_heads, int32_t block_size,
     int64_t num_slots)
 {
-    const int groups = (num_kv_heads + quant::kHeadsPerWarp - 1) / quant::kHeadsPerWarp;
-    const int64_t w = (int64_t)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (w >= (int64_t)num_tokens * groups)
+    constexpr int TPR = quant::kThreadsPerRow<D>;
+    const int64_t rows = (int64_t)num_tokens * num_kv_heads; // per tensor
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t i = j / TPR; // the row (both threads of a row leave or stay together)
+    if (i >= 2 * rows)
         return;
-    const int32_t t = (int32_t)(w / groups);
-    const int g0 = (int)(w % groups) * quant::kHeadsPerWarp;
+    const bool is_v = i >= rows;
+    const int64_t r = is_v ? i - rows : i;
+    const int32_t t = (int32_t)(r / num_kv_heads);
+    const int g = (int)(r % num_kv_heads);
     const int32_t slot = __ldg(slot_mapping + t);
     if (slot < 0 || slot >= num_slots) {
-        if (slot != -1 && lane == 0 && g0 == 0)
+        if (slot != -1 && !is_v && g == 0)
             atomicOr(&g_store_error, 1u);
         return;
     }
-    quant::HeadRows<D> r;
-    quant::load_token_heads<D>(k, v, t, g0, num_kv_heads, lane, r);
-    quant::quantise_token_heads<D>(r, k_cache, v_cache, k_scale, v_scale, g0, slot, num_kv_heads, block_size, lane);
+    const int h = (int)(j % TPR);
+    quant::RowPart part;
+    quant::load_row_part((is_v ? v : k) + ((size_t)t * num_kv_heads + g) * D, h, part);
+    quant::store_row_part<D>(part, is_v ? v_cache : k_cache, is_v ? v_scale : k_scale, g, slot, num_kv_heads,
+                             block_size, h);
 }
 
 int launch_store_kvcache_int8(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,
@@ -92,8 +97,7 @@ int launch_store_kvcache_int8(const pa_dims &d, const void *k, const void *v, vo
                               void *stream)
 {
     const int threads = 256;
-    const int64_t groups = (d.num_kv_heads + quant::kHeadsPerWarp - 1) / quant::kHeadsPerWarp;
-    const int64_t blocks = ((int64_t)num_tokens * groups * 32 + threads - 1) / threads;
+    const int64_t blocks = (2 * (int64_t)num_tokens * d.num_kv_heads * (d.head_dim / 32) + threads - 1) / threads;
     auto kern = d.head_dim == 128 ? store_kvcache_int8_kernel<128> : store_kvcache_int8_kernel<64>;
     kern<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
         static_cast<const uint16_t *>(k), static_cast<const uint16_t *>(v), static_cast<int8_t *>(k_cache),
