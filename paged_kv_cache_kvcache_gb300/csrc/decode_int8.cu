@@ -39,6 +39,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace pa {
 namespace {
@@ -125,7 +126,8 @@ __device__ uint32_t g_fused8_error; // bit 0: a fused-store slot outside [-1, nu
 
 // The INT8 quantiser of pa_store_kvcache_int8 on one (token, KV head) row held
 // by a warp (D/32 values per lane): returns the codes packed in one word and
-// the fp32 scale; arithmetic identical to the store kernel, bit for bit.
+// the fp32 scale; the same scale and the same per-value code (quant::code_of)
+// as the store kernel, bit for bit.
 template <int D>
 __device__ __forceinline__ uint32_t quantise_row(const float (&x)[D / 32], float &scale)
 {
@@ -138,13 +140,11 @@ __device__ __forceinline__ uint32_t quantise_row(const float (&x)[D / 32], float
     for (int o = 16; o > 0; o >>= 1)
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     scale = fmaxf(__fdiv_rn(a, 127.0f), 1e-8f);
+    const float rcp = __frcp_rn(scale);
     uint32_t codes = 0;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float q = __fdiv_rn(x[e], scale);
-        const int i = __float2int_rz(q >= 0.f ? __fadd_rn(q, 0.5f) : __fsub_rn(q, 0.5f));
-        codes |= (uint32_t)(i & 0xff) << (8 * e);
-    }
+    for (int e = 0; e < E; ++e)
+        codes |= (uint32_t)(quant::code_of(x[e], scale, rcp) & 0xff) << (8 * e);
     return codes;
 }
 
