@@ -380,6 +380,36 @@ def test_int8_quantize_invariants():
     assert np.array_equal(scales, s32.astype(np.float16).view(np.uint16))
 
 
+def test_int8_quantize_matches_fp32_formula_at_half_integer_quotients():
+    """Rows whose quotient x / scale lies within an ulp of 63.5 (max|x| = a with a / 127 inexact in
+    fp32, x = +-a/2): the code is decided by the IEEE fp32 quotient alone.  The oracle equals numpy's
+    fp32 evaluation of the page's formula on them, and the product by the rounded reciprocal of the
+    scale would give other codes on some (so these rows separate the two)."""
+    rows = []
+    for o in (9, 13, 15, 19, 33, 101):
+        for j in (-20, -7, 0, 5):
+            a = o * 2.0 ** j
+            x = np.full(128, a / 2, np.float32)
+            x[1::2] *= -1
+            x[0] = a
+            rows.append(x)
+    x = torch.tensor(np.stack(rows)).to(torch.bfloat16)
+    xf = x.float().numpy()
+    assert np.array_equal(xf, np.stack(rows))  # every value exact in bf16
+    codes, scales = oracle.quantize_rows(x)
+    s = np.maximum(np.abs(xf).max(axis=1) / np.float32(127.0), np.float32(1e-8)).astype(np.float32)
+
+    def rounded(q):
+        return np.trunc(np.where(q >= 0, q + np.float32(0.5), q - np.float32(0.5)).astype(np.float32))
+
+    want = rounded((xf / s[:, None]).astype(np.float32)).astype(np.int8)
+    assert np.array_equal(codes, want)
+    assert np.array_equal(scales, s.astype(np.float16).view(np.uint16))
+    assert set(np.unique(np.abs(want[:, 1:]))) == {63, 64}  # both sides of the boundary occur
+    by_product = rounded((xf * (np.float32(1.0) / s)[:, None]).astype(np.float32)).astype(np.int8)
+    assert not np.array_equal(by_product, want)
+
+
 def test_int8_store_scale_layout_head_major():
     """A token's scale for head g sits at [block][g][offset]; its codes at [block][offset][g]."""
     nb, bs, hkv, d = 3, 4, 2, 8
