@@ -84,7 +84,7 @@ CASES = [  # seed, num_seqs, hq, hkv, d, bs, max_len, cached
     (802, 4, 4, 2, 64, 256, 700, "random"),
     (803, 5, 7, 1, 128, 16, 400, "random"),
     (804, 3, 14, 2, 128, 256, 520, None),
-    (805, 6, 8, 8, 128, 16, 260, "random"),       # 8 KV heads: two head groups per store warp
+    (805, 6, 8, 8, 128, 16, 260, "random"),       # 8 KV heads
     (806, 2, 16, 1, 64, 32, 390, "random"),
     (807, 4, 28, 4, 128, 16, 333, "random"),
     (808, 3, 16, 8, 128, 1024, 1100, "random"),
@@ -175,3 +175,30 @@ def test_int8_fused_prefill_bad_slot_flagged():
     for t in (3, 7):
         s = int(orig[t])
         assert torch.equal(codes[s], codes0[s]), f"row {t} was written"
+
+
+def test_int8_fused_prefill_two_plans_on_two_streams():
+    """Two batches with plans of their own, launched on two streams without ordering between them:
+    each plan's barrier words serve only its own launch, so both give the oracle's result."""
+    ws = [workloads.random_case(seed, num_seqs=24, hq=8, hkv=2, d=128, bs=16, max_len=600, cached="random",
+                                device="cuda") for seed in (841, 842)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    runs = []
+    for w, st in zip(ws, streams):
+        batch = w.batches[0]
+        gpu, host = int8_pools(w, batch.num_heads)
+        dims = dims_of(w, batch)
+        q, k, v = batch.q.cuda(), batch.k.cuda(), batch.v.cuda()
+        plan = pa.pa_pack_prefill(dims, batch.seq_lens, batch.query_lens, batch.block_lists).upload("cuda")
+        out = torch.full_like(q, float("nan"))
+        runs.append((w, batch, gpu, host, dims, q, k, v, plan, out, st))
+    torch.cuda.synchronize()
+    for w, batch, gpu, host, dims, q, k, v, plan, out, st in runs:
+        pa.pa_prefill_varlen_int8_fused(dims, q, k, v, *gpu, plan, batch.scale, out, stream=st)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    for w, batch, gpu, host, dims, q, k, v, plan, out, st in runs:
+        ref, _ = oracle.run_batch_int8(*host, batch, w.pool.block_size)
+        int8_equal(gpu, host, what=f"{w.name} (two streams)")
+        assert_close(out, ref, what=f"int8 fused on its own stream ({w.name})")
+        assert _sync_words(plan)[0] == 0
