@@ -26,6 +26,7 @@
 // a single-split sequence writes bf16 directly, otherwise (o/l, log2-sum-exp)
 // partials go to the workspace and a combine kernel merges them.
 #include <mutex>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -341,35 +342,54 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_split_kernel(const DecP
 }
 
 // out[b][h] = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M), over the splits of sequence b.
+// One warp per (sequence, head), D/32 values per lane.  The splits' partials are
+// loaded kBatch at a time before any is used (a split's loads would otherwise wait
+// for the previous split's), and accumulated in split order.
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const float *__restrict__ part_o,
                                                              const float *__restrict__ part_lse,
                                                              const int32_t *__restrict__ seq_items,
                                                              __nv_bfloat16 *__restrict__ out, int num_heads)
 {
+    constexpr int E = D / 32;
+    constexpr int kBatch = 8;
+    using Vec = typename std::conditional<E == 4, float4, float2>::type;
     const int b = blockIdx.x;
     const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     const int s0 = seq_items[b], n = seq_items[b + 1] - s0;
     if (n <= 1 || h >= num_heads)
         return;
+    const float *lse = part_lse + (size_t)s0 * num_heads + h;
+    const float *po = part_o + ((size_t)s0 * num_heads + h) * D + lane * E;
+    const size_t o_stride = (size_t)num_heads * D;
     float M = -INFINITY;
     for (int s = 0; s < n; ++s)
-        M = fmaxf(M, part_lse[(size_t)(s0 + s) * num_heads + h]);
-    constexpr int E = D / 32;
+        M = fmaxf(M, __ldg(lse + (size_t)s * num_heads));
     float accv[E];
 #pragma unroll
     for (int e = 0; e < E; ++e)
         accv[e] = 0.f;
     float W = 0.f;
-    for (int s = 0; s < n; ++s) {
-        const float lse = part_lse[(size_t)(s0 + s) * num_heads + h];
-        const float w = lse == -INFINITY ? 0.f : ptx::ex2(lse - M);
-        W += w;
-        const float *src = part_o + ((size_t)(s0 + s) * num_heads + h) * D + lane * E;
+    for (int s = 0; s < n; s += kBatch) {
+        float l[kBatch];
+        Vec o[kBatch];
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-            accv[e] += w * src[e];
+        for (int i = 0; i < kBatch; ++i)
+            if (s + i < n) {
+                l[i] = __ldg(lse + (size_t)(s + i) * num_heads);
+                o[i] = __ldg(reinterpret_cast<const Vec *>(po + (size_t)(s + i) * o_stride));
+            }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            if (s + i < n) {
+                const float w = l[i] == -INFINITY ? 0.f : ptx::ex2(l[i] - M);
+                W += w;
+                const float *v = reinterpret_cast<const float *>(&o[i]);
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    accv[e] += w * v[e];
+            }
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
     __nv_bfloat16 *dst = out + ((size_t)b * num_heads + h) * D + lane * E;
