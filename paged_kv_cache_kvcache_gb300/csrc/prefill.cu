@@ -452,44 +452,60 @@ __device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int lane)
 // Fused store: the new K/V rows of item w's query positions, KV head w.g, copied
 // from the inputs to their cache slots (one warp; each (token, KV head) row belongs
 // to exactly one item): the positions first, first + step, ...  Warp 11 copies each
-// item's rows after loading its query tiles; the rows of a CTA's last item are split
-// three ways with the K and V producers, which have nothing left to load by then.
-// The kernel itself reads the new keys from the inputs, so nothing here is waited for.
+// item's rows in passes while it waits to load the next item's query tiles; the rows
+// of a CTA's last item are split three ways with the K and V producers, which have
+// nothing left to load by then.  The kernel itself reads the new keys from the
+// inputs, so nothing here is waited for.
+
+template <int D>
+__device__ __forceinline__ int store_vectors(const Item &w, int first, int step)
+{
+    return (w.npos0 + w.npos1 - first + step - 1) / step * (D / 8);
+}
+
+// One pass: the warp's 32 * kU vectors from vector i0 - lane on, of `total` (16 bytes of K
+// and of V each, kU of each in flight per lane; vector i is 16-byte piece i % (D / 8) of KV
+// head g of packed token row0 + (i / (D / 8)) * step).
+template <int D, int kU>
+__device__ __forceinline__ void store_rows_pass(const PfParams &p, int row0, int g, int total, int i0, int step)
+{
+    constexpr int VPR = D / 8; // 16-byte vectors per row of one head
+    const size_t hkv = (size_t)p.num_kv_heads;
+    uint4 kx[kU], vx[kU];
+    int slot[kU]; // -1: nothing to store
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const int i = i0 + 32 * u;
+        slot[u] = -1;
+        if (i < total) {
+            const int row = row0 + (i / VPR) * step;
+            const int s = __ldg(p.slot_mapping + row);
+            const size_t from = ((size_t)row * hkv + g) * VPR + i % VPR;
+            kx[u] = __ldg(p.k_in + from);
+            vx[u] = __ldg(p.v_in + from);
+            if (s >= 0 && s < p.num_slots)
+                slot[u] = s;
+            else if (s != -1)
+                atomicOr(&g_prefill_error, 2u);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+        if (slot[u] >= 0) {
+            const size_t to = ((size_t)slot[u] * hkv + g) * VPR + (i0 + 32 * u) % VPR;
+            p.k_cache[to] = kx[u];
+            p.v_cache[to] = vx[u];
+        }
+}
+
 template <int D>
 __device__ __forceinline__ void store_item_rows(const PfParams &p, const Item &w, int lane, int first = 0,
                                                 int step = 1)
 {
-    constexpr int VPR = D / 8; // 16-byte vectors per row of one head
-    constexpr int kU = 4;      // vectors of K and of V in flight per lane
-    const int npos = (w.npos0 + w.npos1 - first + step - 1) / step;
-    const int total = npos * VPR;
-    const size_t hkv = (size_t)p.num_kv_heads;
-    for (int i0 = lane; i0 < total; i0 += 32 * kU) {
-        uint4 kx[kU], vx[kU];
-        size_t to[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int i = i0 + 32 * u;
-            to[u] = ~(size_t)0;
-            if (i < total) {
-                const int row = w.cq0 + w.q0 + first + (i / VPR) * step;
-                const int slot = __ldg(p.slot_mapping + row);
-                const size_t from = ((size_t)row * hkv + w.g) * VPR + i % VPR;
-                kx[u] = __ldg(p.k_in + from);
-                vx[u] = __ldg(p.v_in + from);
-                if (slot >= 0 && slot < p.num_slots)
-                    to[u] = ((size_t)slot * hkv + w.g) * VPR + i % VPR;
-                else if (slot != -1)
-                    atomicOr(&g_prefill_error, 2u);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-            if (to[u] != ~(size_t)0) {
-                p.k_cache[to[u]] = kx[u];
-                p.v_cache[to[u]] = vx[u];
-            }
-    }
+    constexpr int kU = 2;
+    const int total = store_vectors<D>(w, first, step);
+    for (int i0 = lane; i0 < total; i0 += 32 * kU)
+        store_rows_pass<D, kU>(p, w.cq0 + w.q0 + first, w.g, total, i0, step);
 }
 
 // Rows G*P..127 of each query tile receive no TMA data: zero them once so their
@@ -770,9 +786,12 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             if (lane == 0)
                 ptx::prefetch_tmap(&tm_q);
             bool ok = true;
+            uint32_t early = 0; // bit t: query tile t of the current item was loaded during the previous item's copy
             while (ok && items.more()) {
                 const Item w = items.next();
                 for (int t = 0; t < 2; ++t) {
+                    if (early >> t & 1u)
+                        continue;
                     // refill after the previous item's last score MMA of this tile
                     if (w.ord > 0 && !(ok = wwait(bars.q_free(t), (w.ord - 1) & 1)))
                         break;
@@ -780,10 +799,30 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                         load_query_tile<D, I8>(&tm_q, bars, sbase, w, t, G, P);
                     __syncwarp();
                 }
+                early = 0;
                 if (ok && lane == 0 && items.more())
                     prefetch_query_tiles<D, I8>(&tm_q, items.peek(), G, P);
-                if (ok && p.fused) // the CTA's last item: a third of its rows (the producers copy the rest)
-                    store_item_rows<D>(p, w, lane, 0, items.more() ? 1 : 3);
+                if (ok && p.fused) {
+                    if (items.more()) {
+                        // this item's rows, pass by pass; a query buffer that frees meanwhile is
+                        // refilled with the next item's tile at once
+                        constexpr int kU = 2;
+                        const int total = store_vectors<D>(w, 0, 1);
+                        for (int i0 = lane; __any_sync(0xffffffffu, i0 < total); i0 += 32 * kU) {
+                            store_rows_pass<D, kU>(p, w.cq0 + w.q0, w.g, total, i0, 1);
+                            for (int t = 0; t < 2; ++t)
+                                if (!(early >> t & 1u) && (t == 0 || early) &&
+                                    __shfl_sync(0xffffffffu, (int)ptx::mbar_test_wait(bars.q_free(t), w.ord & 1), 0)) {
+                                    if (lane == 0)
+                                        load_query_tile<D, I8>(&tm_q, bars, sbase, items.peek(), t, G, P);
+                                    __syncwarp();
+                                    early |= 1u << t;
+                                }
+                        }
+                    } else { // the CTA's last item: a third of its rows (the producers copy the rest)
+                        store_item_rows<D>(p, w, lane, 0, 3);
+                    }
+                }
             }
         } else if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
             // ------------------------------------------------------------ bf16: K and V producers
