@@ -15,7 +15,8 @@ per-step citations):
                          in double precision (KV-cache toy of the inference notes)
   * ``quantize_rows`` / ``store_kvcache_int8`` / ``paged_attention_int8`` - INT8 KV
                          cache: per-(token, KV head) symmetric codes and fp16
-                         scales, attention on the dequantised cache (nano-vLLM Q&A, Q3)
+                         scales, attention on the dequantised cache (nano-vLLM Q&A, Q3;
+                         decode reads code * scale exactly, prefill rounded to bf16)
 """
 from __future__ import annotations
 
@@ -61,6 +62,9 @@ def _load():
             lib.oracle_copy_blocks_int8.restype = None
             lib.oracle_copy_blocks_int8.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                     ctypes.c_int]
+            lib.oracle_gather_dense_int8.restype = None
+            lib.oracle_gather_dense_int8.argtypes = [P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, P]
             lib.oracle_gather_dense.restype = None
             lib.oracle_gather_dense.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
             lib.oracle_paged_attention.restype = ctypes.c_int64
@@ -76,7 +80,7 @@ def _load():
             lib.oracle_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                       ctypes.c_int]
             lib.oracle_paged_attention_int8.restype = ctypes.c_int64
-            lib.oracle_paged_attention_int8.argtypes = [P, P, P, P, P, ctypes.c_int, P, P, P, P, ctypes.c_int,
+            lib.oracle_paged_attention_int8.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P, ctypes.c_int,
                                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, P,
                                                         P, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
@@ -244,7 +248,12 @@ def store_kvcache_int8(k_cache: np.ndarray, v_cache: np.ndarray, k_scale: np.nda
 
 
 def paged_attention_int8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, query_lens, block_lists,
-                         block_size: int, scale: float, row_select=None, num_threads: int = 0):
+                         block_size: int, scale: float, row_select=None, num_threads: int = 0,
+                         values: str = "exact"):
+    """Causal paged attention over an INT8 cache in fp64, the cached values read as
+    code * fp16 scale: exactly (values="exact", the page's decode path) or rounded to bf16
+    (values="bf16", the page's prefill path, which casts them to the model's dtype)."""
+    assert values in ("exact", "bf16")
     lib = _load()
     qb = _bits(q)
     seq_lens, query_lens = _i32(seq_lens), _i32(query_lens)
@@ -256,7 +265,7 @@ def paged_attention_int8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, query_
     if row_select is not None:
         sel = np.ascontiguousarray(np.asarray(row_select, dtype=np.uint8))
     pairs = lib.oracle_paged_attention_int8(_ptr(qb), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                            len(seq_lens), _ptr(seq_lens), _ptr(query_lens), _ptr(off), _ptr(ids),
+                                            1 if values == "bf16" else 0, len(seq_lens), _ptr(seq_lens), _ptr(query_lens), _ptr(off), _ptr(ids),
                                             hq, hkv, d, block_size, float(scale),
                                             _ptr(sel) if sel is not None else None, _ptr(out), int(num_threads))
     if pairs < 0:
@@ -265,8 +274,25 @@ def paged_attention_int8(q, k_cache, v_cache, k_scale, v_scale, seq_lens, query_
 
 
 def run_batch_int8(k_cache, v_cache, k_scale, v_scale, batch, block_size: int, row_select=None):
-    """Quantising store of the batch's new K/V, then attention on the INT8 cache (mutates the caches)."""
+    """Quantising store of the batch's new K/V, then attention on the INT8 cache (mutates the
+    caches); a prefill batch reads the values rounded to bf16, a decode batch exactly."""
     slots = slot_mapping(batch.seq_lens, batch.query_lens, batch.block_lists, block_size)
     store_kvcache_int8(k_cache, v_cache, k_scale, v_scale, batch.k, batch.v, slots)
     return paged_attention_int8(batch.q, k_cache, v_cache, k_scale, v_scale, batch.seq_lens, batch.query_lens,
-                                batch.block_lists, block_size, batch.scale, row_select=row_select)
+                                batch.block_lists, block_size, batch.scale, row_select=row_select,
+                                values="bf16" if batch.kind == "prefill" else "exact")
+
+
+def gather_dense_int8(codes, scales, length: int, blocks, block_size: int, values: str = "exact") -> np.ndarray:
+    """Dense [length, Hkv, D] float64 values of one sequence of an INT8 cache (codes int8
+    [nb, bs, Hkv, D], scales fp16 bits [nb, Hkv, bs]), exact or rounded to bf16."""
+    assert values in ("exact", "bf16")
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.int8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint16)
+    hkv, d = c.shape[2], c.shape[3]
+    blocks = _i32(blocks)
+    out = np.empty((length, hkv, d), dtype=np.float64)
+    lib.oracle_gather_dense_int8(_ptr(c), _ptr(sc), length, _ptr(blocks), hkv, d, block_size,
+                                 1 if values == "bf16" else 0, _ptr(out))
+    return out

@@ -274,9 +274,33 @@ void oracle_gather_dense(const uint16_t *cache, int len, const int32_t *blocks, 
     }
 }
 
-/* Same rebuild from an INT8 cache: dense value = code * fp16 scale of its (slot, head). */
+/*
+ * A finite fp32 value rounded to the nearest bf16 (the upper 16 bits of an fp32
+ * pattern), ties to the even pattern: add half of the dropped 16-bit unit, less one
+ * unless the kept part is odd, then drop the low 16 bits.
+ */
+static double round_to_bf16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    u += 0x7fffu + ((u >> 16) & 1u);
+    u &= 0xffff0000u;
+    float r;
+    memcpy(&r, &u, sizeof r);
+    return (double)r;
+}
+
+/*
+ * Same rebuild from an INT8 cache: dense value = code * fp16 scale of its (slot,
+ * head) ("面试问答准备: nano-vLLM 推理引擎优化", Q3).  The page dequantises in two
+ * ways: the decode kernel multiplies each code by its token scale in fp32 and feeds
+ * the product straight into the online softmax (to_bf16 = 0: the exact product, as
+ * code * scale needs at most 8 + 11 significant bits), and the prefill path
+ * materialises the values as code * scale in fp32 cast to the model's dtype
+ * (to_bf16 = 1: that product rounded to bf16).
+ */
 void oracle_gather_dense_int8(const int8_t *cache, const uint16_t *scales, int len, const int32_t *blocks,
-                              int num_kv_heads, int head_dim, int block_size, double *dense)
+                              int num_kv_heads, int head_dim, int block_size, int to_bf16, double *dense)
 {
     int64_t row = (int64_t)num_kv_heads * head_dim;
     for (int j = 0; j < len; ++j) {
@@ -284,9 +308,11 @@ void oracle_gather_dense_int8(const int8_t *cache, const uint16_t *scales, int l
         int64_t slot = phys * block_size + j % block_size;
         for (int g = 0; g < num_kv_heads; ++g) {
             const double sc = (double)oracle_f16_to_f32(scales[(phys * num_kv_heads + g) * block_size + j % block_size]);
-            for (int d = 0; d < head_dim; ++d)
+            for (int d = 0; d < head_dim; ++d) {
+                const int8_t c = cache[slot * row + (int64_t)g * head_dim + d];
                 dense[(int64_t)j * row + (int64_t)g * head_dim + d] =
-                    (double)cache[slot * row + (int64_t)g * head_dim + d] * sc;
+                    to_bf16 ? round_to_bf16((float)c * (float)sc) : (double)c * sc;
+            }
         }
     }
 }
@@ -303,7 +329,7 @@ void oracle_gather_dense_int8(const int8_t *cache, const uint16_t *scales, int l
  * or -1 on malformed input.
  */
 static int64_t attention_impl(const uint16_t *q, const void *k_cache, const void *v_cache, const uint16_t *k_scale,
-                              const uint16_t *v_scale, int is_int8, int num_seqs, const int32_t *seq_lens,
+                              const uint16_t *v_scale, int int8_mode, int num_seqs, const int32_t *seq_lens,
                               const int32_t *query_lens, const int32_t *blk_off, const int32_t *blk_ids,
                               int num_heads, int num_kv_heads, int head_dim, int block_size, double scale,
                               const uint8_t *row_select, double *out, int num_threads)
@@ -343,11 +369,11 @@ static int64_t attention_impl(const uint16_t *q, const void *k_cache, const void
             free(vd);
             return -1;
         }
-        if (is_int8) {
+        if (int8_mode) { /* 1: exact products, 2: products rounded to bf16 */
             oracle_gather_dense_int8((const int8_t *)k_cache, k_scale, lk, blk_ids + blk_off[b], num_kv_heads,
-                                     head_dim, block_size, kd);
+                                     head_dim, block_size, int8_mode == 2, kd);
             oracle_gather_dense_int8((const int8_t *)v_cache, v_scale, lk, blk_ids + blk_off[b], num_kv_heads,
-                                     head_dim, block_size, vd);
+                                     head_dim, block_size, int8_mode == 2, vd);
         } else {
             oracle_gather_dense((const uint16_t *)k_cache, lk, blk_ids + blk_off[b], num_kv_heads, head_dim,
                                 block_size, kd);
@@ -417,15 +443,16 @@ int64_t oracle_paged_attention(const uint16_t *q, const uint16_t *k_cache, const
                           num_heads, num_kv_heads, head_dim, block_size, scale, row_select, out, num_threads);
 }
 
-/* Causal attention over an INT8 cache: the same definition on the dequantised K/V. */
+/* Causal attention over an INT8 cache: the same definition on the dequantised K/V
+ * (values_bf16: the dequantised values rounded to bf16, as the page's prefill path). */
 int64_t oracle_paged_attention_int8(const uint16_t *q, const int8_t *k_cache, const int8_t *v_cache,
-                                    const uint16_t *k_scale, const uint16_t *v_scale, int num_seqs,
+                                    const uint16_t *k_scale, const uint16_t *v_scale, int values_bf16, int num_seqs,
                                     const int32_t *seq_lens, const int32_t *query_lens, const int32_t *blk_off,
                                     const int32_t *blk_ids, int num_heads, int num_kv_heads, int head_dim,
                                     int block_size, double scale, const uint8_t *row_select, double *out,
                                     int num_threads)
 {
-    return attention_impl(q, k_cache, v_cache, k_scale, v_scale, 1, num_seqs, seq_lens, query_lens, blk_off,
+    return attention_impl(q, k_cache, v_cache, k_scale, v_scale, values_bf16 ? 2 : 1, num_seqs, seq_lens, query_lens, blk_off,
                           blk_ids, num_heads, num_kv_heads, head_dim, block_size, scale, row_select, out,
                           num_threads);
 }

@@ -5,6 +5,7 @@ fixtures, a pure-Python brute force, closed forms, invariants and a library
 routine (torch's fp64 attention on the CPU).
 """
 import json
+import math
 import os
 
 import numpy as np
@@ -450,3 +451,68 @@ def test_int8_attention_matches_brute_force_on_dequantised_cache():
         ref = np.array(brute.attention(qb, kd[s0:s0 + lk].tolist(), vd[s0:s0 + lk].tolist(), c["scale"]))
         np.testing.assert_allclose(out[t0:t0 + lq], ref, rtol=0, atol=1e-12)
         t0 += lq
+
+
+def _nearest_bf16(p: float) -> float:
+    """The bf16 value nearest to p (exact in fp32), ties to the even significand, found by
+    comparing the distances to the two bf16 neighbours that bracket it."""
+    if p == 0.0:
+        return 0.0
+    bits = int(np.array([abs(p)], np.float32).view(np.uint32)[0])
+    lo = bits & 0xFFFF0000
+    cands = [lo, lo + 0x10000]
+    vals = [float(np.array([c], np.uint32).view(np.float32)[0]) for c in cands]
+    dist = [abs(v - abs(p)) for v in vals]
+    if dist[0] < dist[1] or (dist[0] == dist[1] and (cands[0] >> 16) % 2 == 0):
+        r = vals[0]
+    else:
+        r = vals[1]
+    return math.copysign(r, p)
+
+
+def test_int8_bf16_values_are_the_nearest_bf16_of_code_times_scale():
+    """The prefill reading of an INT8 cache ("面试问答准备: nano-vLLM 推理引擎优化", Q3: values x token
+    scales in fp32, cast to the model's dtype): every code -127..127 against fp16 scales that are
+    normal, subnormal, 1 and 3 (code x 3 has up to nine significant bits, so exact ties occur),
+    each equal to the bf16 neighbour nearest the exact product; the exact reading is the product."""
+    scales16 = np.array([1.0, 3.0, 1 / 127, 0.0123, 2.0 ** -20, 5.96e-8, 0.5 + 2.0 ** -10, 1000.0], np.float16)
+    codes = np.arange(-127, 128, dtype=np.int8)
+    nb, bs, hkv, d = len(scales16), 1, 1, codes.size
+    kc = np.broadcast_to(codes, (nb, bs, hkv, d)).copy()
+    ks = scales16.view(np.uint16).reshape(nb, hkv, bs).copy()
+    got_bf16 = oracle.gather_dense_int8(kc, ks, nb, np.arange(nb), bs, values="bf16")
+    got_exact = oracle.gather_dense_int8(kc, ks, nb, np.arange(nb), bs, values="exact")
+    ties = 0
+    for j in range(nb):
+        s = float(scales16[j])
+        for i, c in enumerate(codes.tolist()):
+            p = c * s  # exact: 8 x 11 significant bits
+            assert got_exact[j, 0, i] == p
+            want = _nearest_bf16(p)
+            assert got_bf16[j, 0, i] == want, (c, s, got_bf16[j, 0, i], want)
+            f = np.array([abs(p)], np.float32).view(np.uint32)[0]
+            ties += int(p != 0 and (f & 0xFFFF) == 0x8000)
+    assert ties > 0
+
+
+def test_int8_prefill_reading_is_attention_over_bf16_rounded_values():
+    """paged_attention_int8(values="bf16") is the bf16-cache attention over code x scale rounded to
+    bf16 (torch's fp32 -> bf16 conversion), and values="exact" differs from it."""
+    c = _identity_case(47, num_seqs=3, hq=4, hkv=2, d=16, bs=4, max_len=20, cached=True)
+    nb, bs, hkv, d = c["pool_k"].shape
+    kc8, ks = oracle.quantize_rows(c["pool_k"] * 7)
+    vc8, vs = oracle.quantize_rows(c["pool_v"] * 7)
+    kc8, vc8 = kc8.copy(), vc8.copy()
+    ks, vs = np.ascontiguousarray(ks.transpose(0, 2, 1)), np.ascontiguousarray(vs.transpose(0, 2, 1))
+    args = (c["q"], kc8, vc8, ks, vs, c["lens"], c["qlens"], c["blocks"], bs, c["scale"])
+    got, _ = oracle.paged_attention_int8(*args, values="bf16")
+    exact, _ = oracle.paged_attention_int8(*args)
+
+    def rounded(codes, sc):
+        s = torch.from_numpy(sc.transpose(0, 2, 1).copy().view(np.float16)).float()
+        return (torch.from_numpy(codes).float() * s[..., None]).to(torch.bfloat16)
+
+    want, _ = oracle.paged_attention(c["q"], rounded(kc8, ks), rounded(vc8, vs), c["lens"], c["qlens"], c["blocks"],
+                                     bs, c["scale"])
+    np.testing.assert_array_equal(got, want)
+    assert not np.array_equal(got, exact)
