@@ -43,9 +43,9 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 # of the 64 sequences, scaled by 4 (traffic grows with the sequences).  Must be
 # re-captured (or set to None) whenever one of these kernels changes.
 NCU_TRAFFIC = {"qwen25": {"prefill": 232.9e6, "decode": 4.334e9}}
-NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": 210.7e6, "decode": 2.214e9}}
+NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": None, "decode": 2.214e9}}
 NCU_TRAFFIC_FUSED_PREFILL = {"qwen25": 268.8e6}
-NCU_TRAFFIC_INT8_FUSED_PREFILL = {"qwen25": 238.9e6}
+NCU_TRAFFIC_INT8_FUSED_PREFILL = {"qwen25": None}
 NCU_TRAFFIC_COPY_BLOCKS = 488.3e6  # 268.5 MB read + 219.7 MB written (part of the writes still in L2 at exit)
 
 
@@ -210,6 +210,7 @@ class Step:
                             .upload(stream=stream) for _ in range(2)]
             self.launches_per_step = 2
         if self.int8:  # INT8 caches: the bf16 pools quantised once, every slot, by the library's store
+            self.ws_p = pa.prefill_workspace(self.plans_p[0])  # the INT8 prefill's bf16 scratch cache
             self.c8_p = self._quantised(self.dims_p, pp)
             self.c8_d = self._quantised(self.dims_d, pd)
             torch.cuda.current_stream().synchronize()
@@ -233,10 +234,11 @@ class Step:
                                   into=self.plans_p[slot]).upload(stream=s)
         self.pipe_ev["p"][slot].record(s)
         if self.int8 and self.prefill_fused:
-            pa.pa_prefill_varlen_int8_fused(self.dims_p, q, k, v, *self.c8_p, plan, self.bp.scale, out, stream=s)
+            pa.pa_prefill_varlen_int8_fused(self.dims_p, q, k, v, *self.c8_p, plan, self.bp.scale, out, self.ws_p,
+                                            stream=s)
         elif self.int8:
             pa.pa_store_kvcache_int8(self.dims_p, k, v, *self.c8_p, plan.slot_mapping, self.bp.num_tokens, stream=s)
-            pa.pa_prefill_varlen_int8(self.dims_p, q, *self.c8_p, plan, self.bp.scale, out, stream=s)
+            pa.pa_prefill_varlen_int8(self.dims_p, q, *self.c8_p, plan, self.bp.scale, out, self.ws_p, stream=s)
         elif self.prefill_fused:
             pa.pa_prefill_varlen_fused(self.dims_p, q, k, v, self.kc_p, self.vc_p, plan, self.bp.scale, out, stream=s)
         else:
@@ -320,16 +322,16 @@ class Step:
             self._stage(1 - k, phase)
             return
         plan_p = self.plans_p[k]
-        if self.int8 and self.prefill_fused:  # quantising store + INT8 prefill in one launch
+        if self.int8 and self.prefill_fused:  # quantising store + gather, then the prefill
             rec("pk0")
             pa.pa_prefill_varlen_int8_fused(self.dims_p, self.bp.q, self.bp.k, self.bp.v, *self.c8_p, plan_p,
-                                            self.bp.scale, self.out_p, stream=s)
+                                            self.bp.scale, self.out_p, self.ws_p, stream=s)
         elif self.int8:
             pa.pa_store_kvcache_int8(self.dims_p, self.bp.k, self.bp.v, *self.c8_p, plan_p.slot_mapping,
                                      self.bp.num_tokens, stream=s)
             rec("pk0")
             pa.pa_prefill_varlen_int8(self.dims_p, self.bp.q, *self.c8_p, plan_p, self.bp.scale, self.out_p,
-                                      stream=s)
+                                      self.ws_p, stream=s)
         elif self.prefill_fused:  # store + prefill in one launch: the kernel time includes the store
             rec("pk0")
             pa.pa_prefill_varlen_fused(self.dims_p, self.bp.q, self.bp.k, self.bp.v, self.kc_p, self.vc_p, plan_p,
@@ -693,12 +695,13 @@ def main():
         traffic = {"prefill": (NCU_TRAFFIC_INT8_FUSED_PREFILL if int8 else NCU_TRAFFIC_FUSED_PREFILL).get(args.workload),
                    "decode": traffic.get("decode")}
     if int8:
-        pk_name = ("pa_prefill_varlen_int8_fused (prefill_kernel<128,true>: quantising store pass, grid barrier, "
-                   "INT8 prefill; f16 MMAs)" if step.prefill_fused else
-                   "pa_prefill_varlen_int8 (prefill_kernel<128,true>, f16 MMAs)")
+        pk_name = ("pa_prefill_varlen_int8_fused (int8_gather_kernel<128,true>: quantising store of the new rows "
+                   "+ bf16 dequantisation into the scratch cache; then prefill_kernel<128>)" if step.prefill_fused else
+                   "pa_prefill_varlen_int8 (int8_gather_kernel<128,false>: bf16 dequantisation into the scratch "
+                   "cache; then prefill_kernel<128>)")
     else:
-        pk_name = ("pa_prefill_varlen_fused (prefill_kernel<128,false>, store of the new K/V fused)"
-                   if step.prefill_fused else "pa_prefill_varlen (prefill_kernel<128,false>)")
+        pk_name = ("pa_prefill_varlen_fused (prefill_kernel<128>, store of the new K/V fused)"
+                   if step.prefill_fused else "pa_prefill_varlen (prefill_kernel<128>)")
     roof_p = {"kernel": pk_name,
               "bound": "tensor", "achieved": round(pk_tflops, 2),
               "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(pk_tflops / bf16_peak, 4),
@@ -740,7 +743,7 @@ def main():
         pf = prefill_flops(step.bp)
         t_low = (pf / (bf16_peak * 1e12) + dbytes / (hbm_peak * 1e9)) * 1e3
         gbs = dbytes / (t_prefill_kernel * 1e-3) / 1e9
-        roof_p = {"kernel": "pa_prefill_varlen (prefill_kernel<128,false>), prefill + decode rows", "bound": "hbm",
+        roof_p = {"kernel": "pa_prefill_varlen (prefill_kernel<128>), prefill + decode rows", "bound": "hbm",
                   "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
                   "peak_source": f"{peak_src} hbm_gbs", "traffic": None, "work_per_launch": dbytes,
                   "ms_per_launch": round(t_prefill_kernel, 5)}
@@ -774,7 +777,7 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8 KV, f16 MMA" if int8 else "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 KV (prefill: bf16 dequantised; decode: f16 MMA)" if int8 else "bf16", "data": "synthetic",
         "config": {"workload": wl_desc, "l2": "inputs larger than L2: the decode phase streams "
                    f"{dbytes / 1e9:.2f} GB per step", "prefill_gflop": round(flops / 1e9, 2),
                    "decode_kv_gb": round(dbytes / 1e9, 3), "parallelism": f"replicas x{world}", "kv": args.kv,

@@ -87,10 +87,20 @@ typedef struct pa_prefill_meta {
                                    first query row, KV head, key tiles, first packed
                                    query row of the sequence, query length, key length, 0 */
     uint64_t total_bytes;       /* size of the image */
-    uint64_t off_grid_sync;     /* uint32 [2], 0 in the image: arrival count and
-                                   generation of the grid barrier of
-                                   pa_prefill_varlen_int8_fused (the count is back
-                                   at 0 after every launch) */
+    uint64_t off_scratch_tables; /* int32 [num_seqs][scratch_pitch], -1 padded: the blocks
+                                   of sequence b in the INT8 prefill's bf16 scratch cache
+                                   (ceil(seq_len / 128) consecutive 128-token blocks for
+                                   each sequence with new tokens, none for the others) */
+    uint64_t off_scratch_items; /* int32 [scratch_blocks][8] per scratch block: sequence b, its
+                                   first key (128 x block index within b), key count
+                                   seq_len, cached prefix seq_len - query_len, packed
+                                   row of b's new keys minus the prefix
+                                   (cu_seqlens_q[b] - prefix), 0, 0, 0 */
+    uint64_t workspace_bytes;   /* device workspace pa_prefill_varlen_int8(_fused) needs:
+                                   the scratch cache, K then V, bf16
+                                   [scratch_blocks * 128][num_kv_heads][head_dim] each */
+    int32_t scratch_blocks;     /* 128-token blocks of the scratch cache */
+    int32_t scratch_pitch;      /* row pitch of the scratch tables (>= 1) */
 } pa_prefill_meta;
 
 /* Packed decode metadata (one query token per sequence). */
@@ -351,56 +361,60 @@ int pa_decode_int8(const pa_dims *dims, const void *q, const void *k_cache, cons
 /*
  * pa_prefill_varlen_int8 — pa_prefill_varlen over an INT8 cache: the same
  * plan (pa_pack_prefill), arguments and result, with the cached K and V read
- * as code * scale, dequantised inside the kernel (the page's Q3: no
- * floating copy of the cache is materialised).  Each key tile's codes are
- * turned in shared memory into fp16 code * token scale (one rounding; the
- * tile serves 256 query rows, so this is one multiply per element where the
- * page's per-query kernel saves multiplies by scaling scores and weights
- * instead; the product is the same), q is rounded to fp16 (saturating at
- * +-65504), and fp16 tensor-core products accumulate in fp32.  Cached values
- * must lie within the fp16 range (|x| < 65504).  PA_ERR_UNSUPPORTED, before
- * any launch, if the library's INT8 prefill kernel was compiled with other
- * than 128 registers per thread (its 16 warps re-divide exactly that many).
+ * as code * scale.  Source: "面试问答准备: nano-vLLM 推理引擎优化", Q3, the
+ * prefill's dequantisation path: the keys and values the block table
+ * references are read as code * token scale in fp32 and rounded to the model's
+ * dtype (bf16, round to nearest even; code * fp16 scale is exact in fp32, so
+ * this is one rounding of the exact value), then the bf16 attention runs over
+ * them.  Two launches on `stream`: a gather kernel writes every key and value
+ * of each sequence with new tokens, dequantised, into a bf16 scratch cache in
+ * `workspace` (128-token blocks, the plan's scratch tables), and the
+ * pa_prefill_varlen kernel attends over it.
+ *   scratch_tables: device int32 [num_seqs][meta->scratch_pitch]
+ *                   (dev + meta->off_scratch_tables)
+ *   scratch_items:  device int32 [meta->scratch_blocks][8] (dev + meta->off_scratch_items)
+ *   workspace:      device memory of at least meta->workspace_bytes, 16-byte
+ *                   aligned, owned by the caller; overwritten by the call
+ *                   (two calls in flight at once need separate workspaces)
+ * PA_ERR_WORKSPACE if workspace_bytes < meta->workspace_bytes; other errors as
+ * pa_prefill_varlen.
  */
 int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
                            const void *k_scale, const void *v_scale, const int32_t *cu_seqlens_q,
-                           const int32_t *cu_seqlens_k, const int32_t *block_tables, float scale, void *out,
-                           const pa_prefill_meta *meta, const int32_t *tiles, pa_stream_t stream);
+                           const int32_t *cu_seqlens_k, const int32_t *block_tables,
+                           const int32_t *scratch_tables, const int32_t *scratch_items, float scale, void *out,
+                           const pa_prefill_meta *meta, const int32_t *tiles, void *workspace,
+                           size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * pa_prefill_varlen_int8_fused — pa_store_kvcache_int8 of the new tokens
- * followed by pa_prefill_varlen_int8, in one launch, with the same codes,
- * scales and output bit for bit.  Source: "面试问答准备: nano-vLLM 推理引擎优化",
- * Q3 (the INT8 cache's prefill cost comes from work outside the attention
- * kernel) and "手搓 vLLM 推理引擎", Step 4 (store_kvcache, then attention over
- * the cache).  A new key row is read by every later query of its sequence, so
- * the launch quantises each new (token, KV head) row once, before any
- * attention: it is a cooperative launch (all CTAs resident at once, at most
- * one per SM) whose warps first run the store's quantiser over all rows, then
- * meet at a grid barrier and run pa_prefill_varlen_int8 over the cache.
+ * followed by pa_prefill_varlen_int8, with the same codes, scales and output
+ * bit for bit, in two launches instead of three.  Source: "面试问答准备:
+ * nano-vLLM 推理引擎优化", Q3 (the INT8 cache's prefill cost comes from work
+ * outside the attention kernel) and "手搓 vLLM 推理引擎", Step 4
+ * (store_kvcache, then attention over the cache).  The gather launch quantises
+ * each new (token, KV head) row into the cache (as pa_store_kvcache_int8
+ * does) and writes its scratch row from those codes and the stored fp16
+ * scale; the cached prefix is dequantised from the cache; then the bf16
+ * attention runs over the scratch cache.
  *   k, v:          device bf16 [meta->total_q][num_kv_heads][head_dim], row t
  *                  the key/value of packed query row t
  *   slot_mapping:  device int32 [meta->total_q] (dev + meta->off_slot_mapping);
- *                  -1 skips the row, a slot outside [-1, num_blocks*block_size)
- *                  is skipped and flagged (pa_read_device_error bit 0)
- *   grid_sync:     device uint32 [2] at dev + meta->off_grid_sync (0 in the
- *                  packed image; the launch leaves the count at 0, so the
- *                  uploaded plan may be launched again).  Two launches that
- *                  share one plan buffer must not overlap on the GPU (order
- *                  them on one stream).
- * The barrier's wait is bounded (2 s, which only a CTA that never arrives
- * could reach): if it runs out, bit 1 of the device error word is set, no
- * attention runs and `out` is undefined.  PA_ERR_CUDA if the device cannot
- * host the cooperative launch.  Other arguments, errors and numerics as
- * pa_prefill_varlen_int8 and pa_store_kvcache_int8; the new tokens' slots
- * must not hold keys that a sequence of the call reads from the cache.
+ *                  -1 skips the row's store, a slot outside
+ *                  [-1, num_blocks*block_size) is skipped and flagged
+ *                  (pa_read_device_error bit 0); the attention sees every new
+ *                  row as the store writes it either way
+ * Other arguments, errors and numerics as pa_prefill_varlen_int8 and
+ * pa_store_kvcache_int8; the new tokens' slots must not hold keys that a
+ * sequence of the call reads from the cache.
  */
 int pa_prefill_varlen_int8_fused(const pa_dims *dims, const void *q, const void *k, const void *v,
                                  void *k_cache, void *v_cache, void *k_scale, void *v_scale,
                                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
-                                 const int32_t *block_tables, const int32_t *slot_mapping, float scale,
+                                 const int32_t *block_tables, const int32_t *slot_mapping,
+                                 const int32_t *scratch_tables, const int32_t *scratch_items, float scale,
                                  void *out, const pa_prefill_meta *meta, const int32_t *tiles,
-                                 uint32_t *grid_sync, pa_stream_t stream);
+                                 void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * pa_decode_int8_fused — pa_store_kvcache_int8 followed by pa_decode_int8 in

@@ -60,7 +60,7 @@ using namespace pa;
 
 extern "C" const char *pa_last_error_string(void) { return g_err; }
 
-extern "C" int pa_version(void) { return 0x000400; }
+extern "C" int pa_version(void) { return 0x000500; }
 
 extern "C" int pa_upload(void *dev_dst, const void *host_src, size_t bytes, pa_stream_t stream)
 {
@@ -176,53 +176,99 @@ extern "C" int pa_prefill_varlen_fused(const pa_dims *dims, const void *q, const
     return launch_prefill(a, stream);
 }
 
-extern "C" int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
-                                      const void *k_scale, const void *v_scale, const int32_t *cu_seqlens_q,
-                                      const int32_t *cu_seqlens_k, const int32_t *block_tables, float scale,
-                                      void *out, const pa_prefill_meta *meta, const int32_t *tiles,
-                                      pa_stream_t stream)
+// INT8 prefill (plain and with the quantising store): the gather launch fills the
+// plan's bf16 scratch cache from the INT8 cache (k_in set: after quantising the new
+// rows into it), then the bf16 prefill kernel attends over the scratch cache through
+// the scratch tables (128-token blocks).
+static int prefill_int8(const char *fn, bool store, const pa_dims *dims, const void *q, const void *k, const void *v,
+                        const void *k_cache, const void *v_cache, const void *k_scale, const void *v_scale,
+                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, const int32_t *block_tables,
+                        const int32_t *slot_mapping, const int32_t *scratch_tables, const int32_t *scratch_items,
+                        float scale, void *out, const pa_prefill_meta *meta, const int32_t *tiles, void *workspace,
+                        size_t workspace_bytes, pa_stream_t stream)
 {
     PrefillArgs a;
     bool nothing = false;
-    int rc = prepare_prefill("pa_prefill_varlen_int8", dims, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
-                             block_tables, scale, out, meta, tiles, &a, &nothing);
+    int rc = prepare_prefill(fn, dims, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, scale, out,
+                             meta, tiles, &a, &nothing);
     if (rc != PA_OK || nothing)
         return rc;
-    if (!k_scale || !v_scale)
-        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8: NULL scale pointer");
-    if (misaligned(k_scale) || misaligned(v_scale))
-        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8: scales must be 16-byte aligned");
-    a.k_scale = k_scale;
-    a.v_scale = v_scale;
-    return launch_prefill_int8(a, stream);
+    const pa_dims &d = *dims;
+    if (!k_scale || !v_scale || !scratch_tables || !scratch_items || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    if (misaligned(k_scale) || misaligned(v_scale) || misaligned(workspace) || misaligned(scratch_items))
+        return fail(PA_ERR_INVALID_ARG, "%s: scales, scratch items and workspace must be 16-byte aligned", fn);
+    if (meta->scratch_blocks < 1 || meta->scratch_pitch < 1 ||
+        meta->workspace_bytes != (uint64_t)meta->scratch_blocks * kPrefillKeyTile * d.num_kv_heads * d.head_dim * 4)
+        return fail(PA_ERR_INVALID_ARG, "%s: prefill meta was packed for other dims", fn);
+    if (workspace_bytes < meta->workspace_bytes)
+        return fail(PA_ERR_WORKSPACE, "%s: workspace has %zu bytes, needs %llu", fn, workspace_bytes,
+                    (unsigned long long)meta->workspace_bytes);
+    if (store) {
+        if (!k || !v || !slot_mapping)
+            return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+        if (misaligned(k) || misaligned(v))
+            return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", fn);
+    }
+    const size_t half = (size_t)meta->scratch_blocks * kPrefillKeyTile * d.num_kv_heads * d.head_dim;
+    GatherArgs g{};
+    g.num_kv_heads = d.num_kv_heads;
+    g.head_dim = d.head_dim;
+    g.block_size = d.block_size;
+    g.max_blocks = meta->max_blocks_per_seq;
+    g.scratch_blocks = meta->scratch_blocks;
+    g.num_slots = (int64_t)d.num_blocks * d.block_size;
+    g.k_codes = static_cast<const int8_t *>(k_cache);
+    g.v_codes = static_cast<const int8_t *>(v_cache);
+    g.k_scale = static_cast<const uint16_t *>(k_scale);
+    g.v_scale = static_cast<const uint16_t *>(v_scale);
+    g.block_tables = block_tables;
+    g.scratch_items = scratch_items;
+    g.k_out = static_cast<uint16_t *>(workspace);
+    g.v_out = g.k_out + half;
+    if (store) {
+        g.k_in = static_cast<const uint16_t *>(k);
+        g.v_in = static_cast<const uint16_t *>(v);
+        g.slot_mapping = slot_mapping;
+        g.k_codes_w = static_cast<int8_t *>(const_cast<void *>(k_cache));
+        g.v_codes_w = static_cast<int8_t *>(const_cast<void *>(v_cache));
+        g.k_scale_w = static_cast<uint16_t *>(const_cast<void *>(k_scale));
+        g.v_scale_w = static_cast<uint16_t *>(const_cast<void *>(v_scale));
+    }
+    if ((rc = launch_int8_gather(g, stream)) != PA_OK)
+        return rc;
+    a.dims.num_blocks = meta->scratch_blocks;
+    a.dims.block_size = kPrefillKeyTile;
+    a.k_cache = g.k_out;
+    a.v_cache = g.v_out;
+    a.block_tables = scratch_tables;
+    a.max_blocks_per_seq = meta->scratch_pitch;
+    return launch_prefill(a, stream);
+}
+
+extern "C" int pa_prefill_varlen_int8(const pa_dims *dims, const void *q, const void *k_cache, const void *v_cache,
+                                      const void *k_scale, const void *v_scale, const int32_t *cu_seqlens_q,
+                                      const int32_t *cu_seqlens_k, const int32_t *block_tables,
+                                      const int32_t *scratch_tables, const int32_t *scratch_items, float scale,
+                                      void *out, const pa_prefill_meta *meta, const int32_t *tiles, void *workspace,
+                                      size_t workspace_bytes, pa_stream_t stream)
+{
+    return prefill_int8("pa_prefill_varlen_int8", false, dims, q, nullptr, nullptr, k_cache, v_cache, k_scale, v_scale,
+                        cu_seqlens_q, cu_seqlens_k, block_tables, nullptr, scratch_tables, scratch_items, scale, out,
+                        meta, tiles, workspace, workspace_bytes, stream);
 }
 
 extern "C" int pa_prefill_varlen_int8_fused(const pa_dims *dims, const void *q, const void *k, const void *v,
                                             void *k_cache, void *v_cache, void *k_scale, void *v_scale,
                                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
-                                            const int32_t *block_tables, const int32_t *slot_mapping, float scale,
+                                            const int32_t *block_tables, const int32_t *slot_mapping,
+                                            const int32_t *scratch_tables, const int32_t *scratch_items, float scale,
                                             void *out, const pa_prefill_meta *meta, const int32_t *tiles,
-                                            uint32_t *grid_sync, pa_stream_t stream)
+                                            void *workspace, size_t workspace_bytes, pa_stream_t stream)
 {
-    PrefillArgs a;
-    bool nothing = false;
-    int rc = prepare_prefill("pa_prefill_varlen_int8_fused", dims, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
-                             block_tables, scale, out, meta, tiles, &a, &nothing);
-    if (rc != PA_OK || nothing)
-        return rc;
-    if (!k || !v || !k_scale || !v_scale || !slot_mapping || !grid_sync)
-        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8_fused: NULL pointer");
-    if (misaligned(k) || misaligned(v) || misaligned(k_scale) || misaligned(v_scale))
-        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8_fused: tensors and scales must be 16-byte aligned");
-    if (reinterpret_cast<uintptr_t>(grid_sync) % 4 != 0)
-        return fail(PA_ERR_INVALID_ARG, "pa_prefill_varlen_int8_fused: grid_sync must be 4-byte aligned");
-    a.k_scale = k_scale;
-    a.v_scale = v_scale;
-    a.k_in = k;
-    a.v_in = v;
-    a.slot_mapping = slot_mapping;
-    a.grid_sync = grid_sync;
-    return launch_prefill_int8(a, stream);
+    return prefill_int8("pa_prefill_varlen_int8_fused", true, dims, q, k, v, k_cache, v_cache, k_scale, v_scale,
+                        cu_seqlens_q, cu_seqlens_k, block_tables, slot_mapping, scratch_tables, scratch_items, scale,
+                        out, meta, tiles, workspace, workspace_bytes, stream);
 }
 
 // Host-side checks shared by pa_decode and pa_decode_int8; fills `a`.  Sets

@@ -82,6 +82,26 @@ int encode_tmap_3d(CUtensorMap *m, CUtensorMapDataType type, const void *base, u
 int launch_store_kvcache(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,
                          const int32_t *slot_mapping, int32_t num_tokens, void *stream);
 
+// INT8 prefill front end: dequantise the keys/values a prefill batch reads into a
+// bf16 scratch cache of 128-token blocks (and, with k_in set, first quantise the new
+// tokens' rows into the INT8 cache).
+struct GatherArgs {
+    int32_t num_kv_heads, head_dim, block_size, max_blocks;
+    int32_t scratch_blocks;
+    int64_t num_slots;
+    const int8_t *k_codes, *v_codes;      // INT8 cache
+    const uint16_t *k_scale, *v_scale;    // fp16 bits
+    const int32_t *block_tables;
+    const int32_t *scratch_items; // [scratch_blocks][8], see pa_prefill_meta
+    uint16_t *k_out, *v_out;              // bf16 scratch [scratch_blocks * 128][Hkv][D]
+    // quantising store of the new tokens (NULL otherwise)
+    const uint16_t *k_in, *v_in;
+    const int32_t *slot_mapping;
+    int8_t *k_codes_w, *v_codes_w;
+    uint16_t *k_scale_w, *v_scale_w;
+};
+int launch_int8_gather(const GatherArgs &a, void *stream);
+
 int launch_store_kvcache_int8(const pa_dims &d, const void *k, const void *v, void *k_cache, void *v_cache,
                               void *k_scale, void *v_scale, const int32_t *slot_mapping, int32_t num_tokens,
                               void *stream);
@@ -91,8 +111,6 @@ struct PrefillArgs {
     const void *q;
     const void *k_cache;
     const void *v_cache;
-    const void *k_scale; // INT8 cache only: fp16 [num_blocks][num_kv_heads][block_size]
-    const void *v_scale;
     const int32_t *cu_seqlens_q;
     const int32_t *cu_seqlens_k;
     const int32_t *block_tables;
@@ -103,19 +121,15 @@ struct PrefillArgs {
     int32_t total_q;
     int32_t max_blocks_per_seq;
     int32_t rows_per_tile;
-    // fused store (NULL otherwise): new tokens' K/V [total_q][Hkv][D] bf16 and their slots;
-    // INT8 cache: quantised into the codes and scales by a store pass at the start of the
-    // launch, which then meets at a grid barrier on grid_sync (2 words of the plan)
+    // fused store (NULL otherwise): new tokens' K/V [total_q][Hkv][D] bf16 and their slots
     const void *k_in;
     const void *v_in;
     const int32_t *slot_mapping;
     // fused store with a cached prefix that does not end on a box boundary: fetch keys in
     // boxes of 16 rows, so that the box straddling the prefix end has few rows to patch
     bool small_boxes;
-    uint32_t *grid_sync;
 };
 int launch_prefill(const PrefillArgs &a, void *stream);
-int launch_prefill_int8(const PrefillArgs &a, void *stream);
 
 struct DecodeArgs {
     pa_dims dims;

@@ -152,12 +152,28 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
         if (query_lens[b] > 0 && (seq_lens[b] - query_lens[b]) % box != 0)
             aligned = 0;
     meta->prefix_aligned = aligned;
+    // INT8 prefill scratch: each sequence with new tokens gets ceil(seq_len / 128)
+    // consecutive 128-token blocks of a bf16 cache (K and V), in sequence order
+    int64_t sblocks = 0;
+    int32_t spitch = 1;
+    for (int32_t b = 0; b < num_seqs; ++b)
+        if (query_lens[b] > 0) {
+            const int32_t n = (seq_lens[b] + kPrefillKeyTile - 1) / kPrefillKeyTile;
+            sblocks += n;
+            spitch = std::max(spitch, n);
+        }
+    if (sblocks * kPrefillKeyTile > INT32_MAX)
+        return fail(PA_ERR_INVALID_ARG, "INT8 prefill scratch exceeds int32 rows");
+    meta->scratch_blocks = (int32_t)sblocks;
+    meta->scratch_pitch = spitch;
+    meta->workspace_bytes = (uint64_t)sblocks * kPrefillKeyTile * d.num_kv_heads * d.head_dim * 2 * 2;
     meta->off_cu_seqlens_q = L.take(sizeof(int32_t) * (num_seqs + 1));
     meta->off_cu_seqlens_k = L.take(sizeof(int32_t) * (num_seqs + 1));
     meta->off_block_tables = L.take(sizeof(int32_t) * (size_t)num_seqs * mb);
     meta->off_slot_mapping = L.take(sizeof(int32_t) * (size_t)total_q);
     meta->off_tiles = L.take(sizeof(int32_t) * kPrefillItemInts * tiles.size());
-    meta->off_grid_sync = L.take(2 * sizeof(uint32_t));
+    meta->off_scratch_tables = L.take(sizeof(int32_t) * (size_t)num_seqs * spitch);
+    meta->off_scratch_items = L.take(sizeof(int32_t) * 8 * (size_t)sblocks);
     meta->total_bytes = L.off;
     if (!host_buf)
         return PA_OK;
@@ -171,11 +187,28 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
     int32_t *bt = reinterpret_cast<int32_t *>(base + meta->off_block_tables);
     int32_t *slots = reinterpret_cast<int32_t *>(base + meta->off_slot_mapping);
     int32_t *tl = reinterpret_cast<int32_t *>(base + meta->off_tiles);
-    std::memset(base + meta->off_grid_sync, 0, 2 * sizeof(uint32_t));
+    int32_t *stab = reinterpret_cast<int32_t *>(base + meta->off_scratch_tables);
+    int32_t *sitem = reinterpret_cast<int32_t *>(base + meta->off_scratch_items);
     cu_q[0] = cu_k[0] = 0;
     for (int32_t b = 0; b < num_seqs; ++b) {
         cu_q[b + 1] = cu_q[b] + query_lens[b];
         cu_k[b + 1] = cu_k[b] + seq_lens[b];
+    }
+    for (int32_t b = 0, sb = 0; b < num_seqs; ++b) {
+        const int32_t n = query_lens[b] > 0 ? (seq_lens[b] + kPrefillKeyTile - 1) / kPrefillKeyTile : 0;
+        for (int32_t i = 0; i < spitch; ++i)
+            stab[(size_t)b * spitch + i] = i < n ? sb + i : -1;
+        for (int32_t i = 0; i < n; ++i) {
+            int32_t *e = sitem + 8 * (size_t)(sb + i);
+            const int32_t cached = seq_lens[b] - query_lens[b];
+            e[0] = b;
+            e[1] = i * kPrefillKeyTile;
+            e[2] = seq_lens[b];
+            e[3] = cached;
+            e[4] = cu_q[b] - cached;
+            e[5] = e[6] = e[7] = 0;
+        }
+        sb += n;
     }
     if (num_seqs > 0)
         write_block_tables(d, num_seqs, seq_lens, block_offsets, block_ids, mb, bt);

@@ -33,8 +33,7 @@
 //    the whole warp runs the issue loop, converged, and an elected lane issues
 //    each tcgen05.mma and commit: a 128 x 128 x 16 product runs 64 cycles, and a
 //    lone lane in a divergent branch spends nearly as long issuing it, which
-//    left no slack for the waits and commits between products (the 16-warp INT8
-//    kernel measured faster with lane 0 alone).  Each query tile t owns 256
+//    left no slack for the waits and commits between products.  Each query tile t owns 256
 //    TMEM columns: S_t (128 fp32 columns, reused for P_t) and O_t.  The issue
 //    order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) keeps the tensor core busy on
 //    one tile while the other tile's softmax runs (ping-pong).  Because the
@@ -53,18 +52,6 @@
 //    tcgen05.st and consumed by the PV MMA straight from tensor memory;
 //    epilogue (once the item's last PV is complete) O / l -> bf16 -> each
 //    thread's own output row, straight from registers.
-//  * INT8 cache (prefill_kernel<D, true>; "面试问答准备: nano-vLLM 推理引擎优化",
-//    Q3 and its follow-up on where the scales go): 16 warps; warp 11 issues
-//    every TMA load, raw code tiles land next to (D = 128: inside) the tiles
-//    they are converted into, warps 12-15 (one per SM sub-partition) turn a
-//    quarter of the rows of every code tile each into f16 code x token
-//    scale, warps 8 and 10 turn Q into f16, the MMAs run kind::f16 and the
-//    softmax is the bf16 one.  The page moves the scales out of the tile
-//    (key scale after the dot product, value scale into P) to save
-//    multiplies in a kernel that dequantises in registers per query; here
-//    the tile is converted once for 2 x 128 query rows anyway, so scaling it
-//    there is one multiply per element instead of one per score (the result
-//    is the same product, rounded once more to f16).
 //  * Fused store (pa_prefill_varlen_fused, bf16): the K/V producers take the
 //    new keys' boxes from the k/v inputs instead of the cache (so nothing
 //    the launch writes is read by it), and warp 11, between its query loads,
@@ -73,17 +60,6 @@
 //    prefill resumes at any token count) is loaded from the cache and its new
 //    keys' rows are then copied over it from the inputs by the producer before
 //    the MMAs may read it.
-//  * Fused store, INT8 cache (pa_prefill_varlen_int8_fused): the attention
-//    must see each new key as the cache will hold it (codes x fp16 scale), and
-//    a new key row is read by every item that follows it in its sequence, so
-//    the launch quantises each new row once, before any attention: a
-//    cooperative launch (all CTAs resident) whose warps first run the store
-//    kernel's quantiser over all new (token, head group) rows, grid-stride,
-//    then meet at a grid barrier on two words of the plan (arrival count back
-//    at 0 after every use, generation advanced by the last arrival; the wait
-//    is bounded), after which the code tiles come from the cache as in the
-//    unfused kernel.  Codes, scales and output are those of the store kernel
-//    followed by pa_prefill_varlen_int8, bit for bit.
 //  * mbarriers order every hand-off; every wait is bounded and reports a
 //    timeout through a device error word instead of hanging.
 #include <cuda.h>
@@ -94,7 +70,6 @@
 
 #include "internal.h"
 #include "ptx.cuh"
-#include "quant.cuh"
 
 namespace pa {
 
@@ -103,22 +78,15 @@ __device__ uint32_t g_prefill_error; // bit 0: a bounded wait timed out; bit 1: 
 namespace {
 
 // warps 0-7: softmax (two warpgroups), 8: K TMA producer, 9: MMA issuer (and
-// TMEM owner), 10: V TMA producer, 11: Q TMA producer (INT8: 11 loads
-// everything, 8 and 10 convert Q, 12-15 convert and scale the code tiles).  Registers are granted per 4 warps: 168 per thread at launch for the
-// 12-warp bf16 CTA, 128 for the 16-warp INT8 one; setmaxnreg then moves part of
-// the other warpgroups' share to the softmax warpgroups (bf16: 216 softmax, 72
-// in warps 8-11; INT8: 192 softmax, 64 in warps 8-11 and 64 in 12-15).
+// TMEM owner), 10: V TMA producer, 11: Q TMA producer.  Registers are granted
+// per 4 warps: 168 per thread at launch (65536 / 384 threads, rounded down to
+// the allocation unit of 8); setmaxnreg then moves part of warps 8-11's share
+// to the softmax warpgroups (216 per softmax thread, 72 in warps 8-11).
 // One thread issues the MMAs of both query tiles: its in-order stream keeps the
 // two tiles half a key tile apart, so one tile's softmax always runs under the
 // other's MMAs.
-// threads per CTA and registers per thread the launch grants (65536 / threads,
-// rounded down to the allocation unit of 8): 12 warps (bf16) or 16 (INT8: warps
-// 12-15 convert the code tiles, one warp per SM sub-partition)
-template <bool I8>
-constexpr int kThreadsOf = I8 ? 512 : 384;
-template <bool I8>
-constexpr int kLaunchRegsOf = I8 ? 128 : 168;
-constexpr int kConvWarp0 = 12;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;
 constexpr int kKProducerWarp = 8, kMmaWarp = 9, kVProducerWarp = 10, kLoaderWarp = 11;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -133,38 +101,21 @@ constexpr float kRescaleThreshold = 8.0f; // log2 units
 // unambiguous for rings of up to 4 slots.
 constexpr int kIterRing = 8;
 
-template <int D, bool I8>
+template <int D>
 struct PfLayout {
     static constexpr int kPanels = D / 64;          // 64-element (128-byte) panels along head_dim
     static constexpr int kPanelBytes = 128 * 128;   // 128 rows x 128 bytes
     static constexpr int kTileBytes = kPanels * kPanelBytes;
     // K is released as soon as the two score MMAs have read it, V only after
     // both PV MMAs: K gets the deeper ring so its loads start earliest.
-    static constexpr int kKStages = I8 ? 3 : (D == 128 ? 3 : 4);
-    static constexpr int kVStages = I8 ? (D == 128 ? 2 : 3) : (D == 128 ? 2 : 4);
+    static constexpr int kKStages = D == 128 ? 3 : 4;
+    static constexpr int kVStages = D == 128 ? 2 : 4;
     static constexpr int kQ = 0;                    // two query tiles
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kKStages * kTileBytes;
-    // INT8 cache: a key tile's raw codes (128 rows x D bytes) land in the upper
-    // half of the 16-bit tile they are converted into (D = 128: row t's codes
-    // occupy the slot of row t's second panel) or in a ring of their own
-    // (D = 64).
-    static constexpr bool kInPlace = D == 128;
-    static constexpr int kCodeBytes = 128 * D;
-    static constexpr int kStg = kV + kVStages * kTileBytes;
-    static constexpr int kStgBytes = I8 && !kInPlace ? (kKStages + kVStages) * kCodeBytes : 0;
-    static constexpr int kBar = kStg + kStgBytes;
+    static constexpr int kBar = kV + kVStages * kTileBytes;
     static constexpr int kBarBytes = 512;
     static constexpr int kSmemBytes = kBar + kBarBytes + 1024; // + alignment slack
-    __host__ __device__ static constexpr int k_codes(int s)
-    {
-        return kInPlace ? kK + s * kTileBytes + kTileBytes / 2 : kStg + s * kCodeBytes;
-    }
-    __host__ __device__ static constexpr int v_codes(int s)
-    {
-        return kInPlace ? kV + s * kTileBytes + kTileBytes / 2 : kStg + (kKStages + s) * kCodeBytes;
-    }
-    static_assert(!kInPlace || kCodeBytes == kTileBytes / 2, "in-place codes fill the second panel");
     static_assert(kKStages <= 4 && kVStages <= 4, "barrier slots");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
@@ -186,22 +137,16 @@ struct PfParams {
     int32_t max_blocks;
     int32_t num_slots;     // num_blocks * block_size: first out-of-range row (reads as zeros)
     int32_t num_kv_heads;
-    const __half *k_scale; // INT8 cache only: fp16 [num_blocks][num_kv_heads][block_size]
-    const __half *v_scale;
-    // fused store (bf16): the new tokens' K/V rows are read from k_in/v_in (tensor maps
+    // fused store: the new tokens' K/V rows are read from k_in/v_in (tensor maps
     // tm_kin/tm_vin) instead of the cache, and written into the cache at slot_mapping
+    // (field order: the register allocation of the kernel is sensitive to it; this one
+    // spills least)
+    uint4 *k_cache;
+    uint4 *v_cache;
     int32_t fused;
     const int32_t *slot_mapping;
     const uint4 *k_in;
     const uint4 *v_in;
-    uint4 *k_cache;
-    uint4 *v_cache;
-    // fused store, INT8 cache: quantise rows 0 .. total_q-1 of k_in/v_in into the codes
-    // (k_cache/v_cache) and scales (k_scale/v_scale) before the attention; grid_sync: the
-    // plan's two barrier words
-    int32_t store8;
-    int32_t total_q;
-    uint32_t *grid_sync;
 };
 
 // barrier slots (uint64 each) inside the barrier area
@@ -220,10 +165,6 @@ struct Bars {
     // V slot s holds an item's last key tile with its rows past the sequence end zeroed
     __device__ uint32_t v_tail(int s) const { return base + 8 * (26 + s); }
     __device__ uint32_t tmem_slot() const { return base + 8 * 30; }
-    // INT8 variant: raw code tiles landed, Q converted
-    __device__ uint32_t k_load(int s) const { return base + 8 * (32 + s); }
-    __device__ uint32_t v_load(int s) const { return base + 8 * (36 + s); }
-    __device__ uint32_t q_ready(int t) const { return base + 8 * (42 + t); }
     // fused store: K slot s holds the key tile whose straddling box (cached prefix, then
     // new keys) has had its new keys' rows copied in from the inputs
     __device__ uint32_t k_fix(int s) const { return base + 8 * (44 + s); }
@@ -367,88 +308,6 @@ struct Waiter {
     }
 };
 
-constexpr uint32_t kFlip = 0x80808080u;  // int8 -> offset binary (x + 128), per byte
-constexpr uint32_t kMagic = 0x64806480u; // f16x2 (1152, 1152)
-
-// Two offset-binary codes of u (bytes chosen by sel) -> f16x2 of the signed
-// codes, exactly: the f16 bit pattern 0x6400 | (x + 128) is 1152 + x.
-__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u, uint32_t sel)
-{
-    return ptx::sub_f16x2(ptx::prmt(u, 0x64646464u, sel), kMagic);
-}
-
-// Raw int8 code rows r0 .. r0+31 of a staged key tile -> f16 code x scale of
-// the row's token (the code exact in f16, one rounding in the product) in the
-// 128B-swizzled layout the MMAs read (panels of 64 elements x 128 rows, the
-// layout TMA gives the bf16 tiles).  One warp; D/16 lanes per row, each
-// converting 16 codes (two 16-byte output chunks); lane i holds the f16x2
-// pair (scale, scale) of row r0 + i (0 for keys past the sequence).
-//
-// Bank conflicts: an 8-lane store phase covers one row (D = 128: both
-// panels) or two rows (D = 64); the lanes of panel 1 and of odd rows at
-// D = 128 handle their two chunks in the other order, so that every store
-// and every 8-byte half-row load (D = 128: rows t and t+1 in one 16-lane
-// phase) touches each bank once.
-template <int D, bool kInPlace>
-__device__ __forceinline__ void convert_codes(uint32_t codes, uint32_t tile, int lane, int r0, uint32_t scale2)
-{
-    constexpr int LPR = D / 16;   // lanes per row, 16 codes each
-    constexpr int RPP = 32 / LPR; // rows per pass
-    const int sub = lane / LPR, l = lane % LPR;
-    const int panel = l >> 2;     // 4 lanes cover one 64-element panel row
-    const int c0 = (l & 3) * 2;   // the lane's two chunks: c0, c0 + 1
-    // chunk handled first (D = 64: always c0; a 4-lane row never meets itself)
-    const int h0 = D == 128 ? (panel ^ (sub & 1)) : 0;
-    const int ta = c0 + h0, tb = c0 + (h0 ^ 1);
-    // t & 7 = sub ^ (RPP * pass & 7): two swizzle phases, fixed per lane
-    const uint32_t dst = tile + panel * (128 * 128) + (uint32_t)(r0 + sub) * 128;
-    const uint32_t a0 = dst + (uint32_t)((ta ^ sub) << 4), b0 = dst + (uint32_t)((tb ^ sub) << 4);
-    const uint32_t a1 = dst + (uint32_t)((ta ^ sub ^ (RPP & 7)) << 4), b1 = dst + (uint32_t)((tb ^ sub ^ (RPP & 7)) << 4);
-    const uint32_t src = codes + (uint32_t)(r0 + sub) * D + 16 * l;
-#pragma unroll
-    for (int pass = 0; pass < 32 / RPP; ++pass) {
-        uint32_t u[4];
-        if constexpr (D == 128) {
-            const uint2 x = ptx::lds_v2(src + pass * RPP * D + 8 * h0);
-            const uint2 y = ptx::lds_v2(src + pass * RPP * D + 8 * (h0 ^ 1));
-            u[0] = x.x, u[1] = x.y, u[2] = y.x, u[3] = y.y;
-        } else {
-            const uint4 w = ptx::lds_v4(src + pass * RPP * D);
-            u[0] = w.x, u[1] = w.y, u[2] = w.z, u[3] = w.w;
-        }
-        if constexpr (kInPlace)
-            __syncwarp(); // row t's codes are read before its second panel is written over them
-        const uint32_t sc2 = __shfl_sync(0xffffffffu, scale2, sub + RPP * pass);
-        uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t f = u[i] ^ kFlip;
-            o[2 * i] = ptx::mul_f16x2(codes_to_f16x2(f, 0x4140u), sc2);
-            o[2 * i + 1] = ptx::mul_f16x2(codes_to_f16x2(f, 0x4342u), sc2);
-        }
-        const uint32_t off = (uint32_t)(pass * RPP * 128);
-        const bool odd = ((RPP * pass) & 7) != 0;
-        ptx::sts_v4((odd ? a1 : a0) + off, o[0], o[1], o[2], o[3]);
-        ptx::sts_v4((odd ? b1 : b0) + off, o[4], o[5], o[6], o[7]);
-    }
-}
-
-// A landed bf16 query tile -> f16 in place (element-wise, layout unchanged),
-// saturating at +-65504.
-template <int D>
-__device__ __forceinline__ void q_tile_to_f16(uint8_t *tile, int lane)
-{
-    for (int i = lane; i < 128 * D / 8; i += 32) {
-        uint4 *c = reinterpret_cast<uint4 *>(tile + 16 * i);
-        uint4 v = *c;
-        v.x = ptx::pack_f16_sat(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
-        v.y = ptx::pack_f16_sat(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-        v.z = ptx::pack_f16_sat(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
-        v.w = ptx::pack_f16_sat(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
-        *c = v;
-    }
-}
-
 // Fused store: the new K/V rows of item w's query positions, KV head w.g, copied
 // from the inputs to their cache slots (one warp; each (token, KV head) row belongs
 // to exactly one item): the positions first, first + step, ...  Warp 11 copies each
@@ -510,10 +369,10 @@ __device__ __forceinline__ void store_item_rows(const PfParams &p, const Item &w
 
 // Rows G*P..127 of each query tile receive no TMA data: zero them once so their
 // (discarded) scores stay finite and cost the same as real rows.
-template <int D, bool I8>
+template <int D>
 __device__ __forceinline__ void zero_query_padding(uint8_t *sgen, int first, int lane)
 {
-    using L = PfLayout<D, I8>;
+    using L = PfLayout<D>;
     if (first >= 128)
         return;
     const int chunks = (128 - first) * 8;
@@ -528,11 +387,11 @@ __device__ __forceinline__ void zero_query_padding(uint8_t *sgen, int first, int
 
 // Query tile t of item w: one 3-D box {64 d, G heads, P positions} per panel.
 // Always issued, also for an empty tile 1 (its rows are never used).
-template <int D, bool I8>
+template <int D>
 __device__ __forceinline__ void load_query_tile(const CUtensorMap *tm_q, const Bars &bars, uint32_t sbase,
                                                 const Item &w, int t, int G, int P)
 {
-    using L = PfLayout<D, I8>;
+    using L = PfLayout<D>;
     ptx::mbar_arrive_expect_tx(bars.q_full(t), (uint32_t)(L::kPanels * 128 * G * P));
     for (int pp = 0; pp < L::kPanels; ++pp)
         ptx::tma_load_3d(sbase + L::kQ + t * L::kTileBytes + pp * L::kPanelBytes, tm_q, bars.q_full(t), pp * 64,
@@ -541,106 +400,25 @@ __device__ __forceinline__ void load_query_tile(const CUtensorMap *tm_q, const B
 
 // The next item's query tiles into L2, so that their loads (which must wait for
 // the current item's last score MMAs) arrive sooner.
-template <int D, bool I8>
+template <int D>
 __device__ __forceinline__ void prefetch_query_tiles(const CUtensorMap *tm_q, const Item &w, int G, int P)
 {
-    using L = PfLayout<D, I8>;
+    using L = PfLayout<D>;
     for (int t = 0; t < 2; ++t)
         for (int pp = 0; pp < L::kPanels; ++pp)
             ptx::tma_prefetch_3d(tm_q, pp * 64, w.g * G, w.cq0 + w.q0 + t * P);
 }
 
-// Grid-wide barrier of a cooperative launch on two words of global memory:
-// words[0] counts arrivals (back at 0 after every use), words[1] is the
-// generation.  Thread 0 of each CTA arrives; the last arrival resets the count
-// and advances the generation, the others wait until it moves (bounded: false
-// after about 2 s, which only a CTA that never arrives could cause).  `flag` is
-// a shared word used to hand the outcome to the CTA.
-__device__ bool grid_barrier(uint32_t *words, volatile uint32_t *flag)
-{
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        bool ok = true;
-        const uint32_t gen = ptx::ld_acquire_gpu(words + 1);
-        const uint32_t old = ptx::atom_add_acq_rel_gpu(words, 1u);
-        if (old == gridDim.x - 1) {
-            ptx::st_relaxed_gpu(words, 0u);
-            ptx::atom_add_release_gpu(words + 1, 1u);
-        } else {
-            const uint64_t t0 = ptx::globaltimer();
-            while (ptx::ld_acquire_gpu(words + 1) == gen) {
-                if (ptx::globaltimer() - t0 > 2000000000ull) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(128);
-            }
-        }
-        *flag = ok ? 1u : 0u;
-    }
-    __syncthreads();
-    return *flag != 0u;
-}
-
-// INT8 fused store: the threads of the grid quantise (tensor, token, KV head) rows,
-// grid-stride, with the store kernel's quantiser (quant::kThreadsPerRow<D> adjacent
-// threads per row), into the cache slots of
-// slot_mapping (-1 skipped, other out-of-range slots reported in bit 1); then the
-// writes are ordered before the TMA loads of every CTA (proxy fence + grid barrier).
 template <int D>
-__device__ bool int8_store_pass(const PfParams &p, volatile uint32_t *flag)
-{
-    constexpr int TPR = quant::kThreadsPerRow<D>;
-    const int Hkv = p.num_kv_heads;
-    const int64_t rows = (int64_t)p.total_q * Hkv; // per tensor
-    const int64_t nparts = (int64_t)gridDim.x * blockDim.x / TPR;
-    const int h = (int)(threadIdx.x % TPR);
-    const uint16_t *k_in = reinterpret_cast<const uint16_t *>(p.k_in);
-    const uint16_t *v_in = reinterpret_cast<const uint16_t *>(p.v_in);
-    // row i's values and slot; the next row's are loaded before this one is quantised
-    auto fetch = [&](int64_t i, quant::RowPart &part) {
-        const bool is_v = i >= rows;
-        const int64_t r = is_v ? i - rows : i;
-        quant::load_row_part((is_v ? v_in : k_in) + r * D, h, part);
-        return __ldg(p.slot_mapping + r / Hkv);
-    };
-    int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / TPR;
-    quant::RowPart cur, nxt;
-    int32_t slot = i < 2 * rows ? fetch(i, cur) : -1;
-    for (; i < 2 * rows; i += nparts) {
-        const int32_t next_slot = i + nparts < 2 * rows ? fetch(i + nparts, nxt) : -1;
-        const bool is_v = i >= rows;
-        const int64_t r = is_v ? i - rows : i;
-        const int g = (int)(r % Hkv);
-        if (slot >= 0 && slot < p.num_slots)
-            quant::store_row_part<D>(cur, reinterpret_cast<int8_t *>(is_v ? p.v_cache : p.k_cache),
-                                     const_cast<__half *>(is_v ? p.v_scale : p.k_scale), g, slot, Hkv, p.block_size,
-                                     h);
-        else if (slot != -1 && !is_v && g == 0 && h == 0)
-            atomicOr(&g_prefill_error, 2u);
-        cur = nxt;
-        slot = next_slot;
-    }
-    ptx::fence_proxy_async_global();
-    __threadfence();
-    const bool ok = grid_barrier(p.grid_sync, flag);
-    ptx::fence_proxy_async_global();
-    return ok;
-}
-
-template <int D, bool I8>
-__global__ void __launch_bounds__(kThreadsOf<I8>, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kin,
                    const __grid_constant__ CUtensorMap tm_vin, const PfParams p)
 {
-    using L = PfLayout<D, I8>;
-    // per-thread register budgets after the hand-over (bf16 variant)
-    // (INT8: the converter warpgroup keeps kConvRegs)
-    constexpr int kSoftmaxRegs = I8 ? 192 : 216, kOtherRegs = I8 ? 64 : 72, kConvRegs = 64;
-    static_assert(128 * (2 * kSoftmaxRegs + kOtherRegs + (I8 ? kConvRegs : 0)) ==
-                      kThreadsOf<I8> * kLaunchRegsOf<I8>,
-                  "register hand-over");
+    using L = PfLayout<D>;
+    // per-thread register budgets after the hand-over
+    constexpr int kSoftmaxRegs = 216, kOtherRegs = 72;
+    static_assert(128 * (2 * kSoftmaxRegs + kOtherRegs) == kThreads * kLaunchRegs, "register hand-over");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -654,16 +432,6 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
     const int G = p.group;
     const int P = p.rows_per_tile;
 
-    if constexpr (I8) {
-        // fused store: the new rows' codes and scales first, in every CTA (the abort word
-        // carries the barrier's outcome; it is set to 0 below before anything waits on it)
-        if (p.store8 && !int8_store_pass<D>(p, abort_flag)) {
-            if (threadIdx.x == 0)
-                atomicOr(&g_prefill_error, 1u);
-            return;
-        }
-    }
-
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bars.q_full(t), 1);
@@ -673,23 +441,15 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             ptx::mbar_init(bars.o_full(t), 1);
         }
         for (int s = 0; s < L::kKStages; ++s) {
-            ptx::mbar_init(bars.k_full(s), I8 ? 4 : 1); // INT8: one arrival per converter warp
+            ptx::mbar_init(bars.k_full(s), 1);
             ptx::mbar_init(bars.k_fix(s), 1);
         }
         for (int s = 0; s < L::kVStages; ++s) {
-            ptx::mbar_init(bars.v_full(s), I8 ? 4 : 1);
+            ptx::mbar_init(bars.v_full(s), 1);
             ptx::mbar_init(bars.v_tail(s), 1);
         }
         for (int s = 0; s < kIterRing; ++s)
             ptx::mbar_init(bars.released(s), 1);
-        if constexpr (I8) {
-            for (int s = 0; s < L::kKStages; ++s)
-                ptx::mbar_init(bars.k_load(s), 1);
-            for (int s = 0; s < L::kVStages; ++s)
-                ptx::mbar_init(bars.v_load(s), 1);
-            for (int i = 0; i < 2; ++i)
-                ptx::mbar_init(bars.q_ready(i), 1);
-        }
         *abort_flag = 0u;
         ptx::fence_mbar_init();
     }
@@ -703,65 +463,10 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + L::kBar + kTmemSlotOffset);
     auto wwait = [&](uint32_t bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
 
-    if (I8 && warp >= kConvWarp0) {
-        // ---------------------------------------------------------------- INT8: code converters
-        // warp 12 + i turns rows 32i .. 32i+31 of every K and V code tile into f16
-        // code x token scale: the conversion is spread over all four SM
-        // sub-partitions, so it slows each softmax warp alike, and with the scales
-        // applied here the softmax is the bf16 one (a tile feeds 2 x 128 query rows,
-        // so one multiply per tile element replaces one per score).
-        ptx::reg_dealloc<kConvRegs>();
-        ItemIter items(p.tiles, p.num_items, P);
-        const int r0 = 32 * (warp - kConvWarp0);
-        const int bs = p.block_size, Hkv = p.num_kv_heads;
-        // K and V scales of key r0 + lane of key tile j of item w as f16x2 pairs (0 past the sequence)
-        auto fetch = [&](const Item &w, int j, uint32_t &ks, uint32_t &vs) {
-            const int key = j * 128 + r0 + lane;
-            ks = vs = 0u;
-            if (key < w.lk) {
-                const int phys = __ldg(p.block_tables + (size_t)w.b * p.max_blocks + key / bs);
-                const size_t si = ((size_t)phys * Hkv + w.g) * bs + (key & (bs - 1));
-                ks = __ldg(reinterpret_cast<const unsigned short *>(p.k_scale) + si) * 0x10001u;
-                vs = __ldg(reinterpret_cast<const unsigned short *>(p.v_scale) + si) * 0x10001u;
-            }
-        };
-        int X = 0;
-        bool ok = true;
-        uint32_t ks = 0u, vs = 0u;
-        if (items.more())
-            fetch(items.peek(), 0, ks, vs);
-        while (ok && items.more()) {
-            const Item w = items.next();
-            for (int j = 0; j < w.nkt; ++j, ++X) {
-                const uint32_t ks_j = ks, vs_j = vs;
-                if (j + 1 < w.nkt) // the next tile's scales (perhaps the next item's first)
-                    fetch(w, j + 1, ks, vs);
-                else if (items.more())
-                    fetch(items.peek(), 0, ks, vs);
-                const int sk = X % L::kKStages;
-                if (!(ok = wwait(bars.k_load(sk), (X / L::kKStages) & 1)))
-                    break;
-                convert_codes<D, L::kInPlace>(sbase + L::k_codes(sk), sbase + L::kK + sk * L::kTileBytes, lane, r0,
-                                              ks_j);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(bars.k_full(sk));
-                const int sv = X % L::kVStages;
-                if (!(ok = wwait(bars.v_load(sv), (X / L::kVStages) & 1)))
-                    break;
-                convert_codes<D, L::kInPlace>(sbase + L::v_codes(sv), sbase + L::kV + sv * L::kTileBytes, lane, r0,
-                                              vs_j);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(bars.v_full(sv)); // codes are finite and weights past the end 0: nothing to zero
-            }
-        }
-    } else if (warp >= 8) {
-        // warps 8-11 (copies, MMA issue; INT8 also Q conversion) need
-        // fewer registers and hand part of theirs to the softmax warpgroups (128 x
-        // (2 kSoftmaxRegs + kOtherRegs [+ kConvRegs]) = the launch's registers)
+    if (warp >= 8) {
+        // warps 8-11 (copies, MMA issue) need fewer registers and hand part of theirs
+        // to the softmax warpgroups (128 x (2 kSoftmaxRegs + kOtherRegs) = the launch's
+        // registers)
         ptx::reg_dealloc<kOtherRegs>();
         const int bs = p.block_size;
         const int box_rows = p.box_rows;
@@ -779,10 +484,10 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             const int phys = __ldg(bt + key / bs);
             return phys * bs + (key & (bs - 1));
         };
-        if (!I8 && warp == kLoaderWarp) {
+        if (warp == kLoaderWarp) {
             // ------------------------------------------------------------ bf16: Q producer
             ItemIter items(p.tiles, p.num_items, P);
-            zero_query_padding<D, I8>(sgen, G * P, lane);
+            zero_query_padding<D>(sgen, G * P, lane);
             if (lane == 0)
                 ptx::prefetch_tmap(&tm_q);
             bool ok = true;
@@ -796,12 +501,12 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                     if (w.ord > 0 && !(ok = wwait(bars.q_free(t), (w.ord - 1) & 1)))
                         break;
                     if (lane == 0)
-                        load_query_tile<D, I8>(&tm_q, bars, sbase, w, t, G, P);
+                        load_query_tile<D>(&tm_q, bars, sbase, w, t, G, P);
                     __syncwarp();
                 }
                 early = 0;
                 if (ok && lane == 0 && items.more())
-                    prefetch_query_tiles<D, I8>(&tm_q, items.peek(), G, P);
+                    prefetch_query_tiles<D>(&tm_q, items.peek(), G, P);
                 if (ok && p.fused) {
                     if (items.more()) {
                         // this item's rows, pass by pass; a query buffer that frees meanwhile is
@@ -814,7 +519,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                                 if (!(early >> t & 1u) && (t == 0 || early) &&
                                     __shfl_sync(0xffffffffu, (int)ptx::mbar_test_wait(bars.q_free(t), w.ord & 1), 0)) {
                                     if (lane == 0)
-                                        load_query_tile<D, I8>(&tm_q, bars, sbase, items.peek(), t, G, P);
+                                        load_query_tile<D>(&tm_q, bars, sbase, items.peek(), t, G, P);
                                     __syncwarp();
                                     early |= 1u << t;
                                 }
@@ -824,7 +529,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                     }
                 }
             }
-        } else if (!I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
+        } else if (warp == kKProducerWarp || warp == kVProducerWarp) {
             // ------------------------------------------------------------ bf16: K and V producers
             ItemIter items(p.tiles, p.num_items, P);
             const bool is_k = warp == kKProducerWarp;
@@ -898,84 +603,13 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
             // entry is still the iterator's last one)
             if (ok && p.fused && items.ord > 0)
                 store_item_rows<D>(p, items.decode(items.ord - 1), lane, is_k ? 1 : 2, 3);
-        } else if (I8 && warp == kLoaderWarp) {
-            // ------------------------------------------------------------ INT8: TMA loader (Q, K codes, V codes)
-            ItemIter items(p.tiles, p.num_items, P);
-            zero_query_padding<D, I8>(sgen, G * P, lane);
-            if (lane == 0) {
-                ptx::prefetch_tmap(&tm_k);
-                ptx::prefetch_tmap(&tm_v);
-                ptx::prefetch_tmap(&tm_q);
-            }
-            // raw codes of global key tile X (one box of D bytes x box_rows per block) into its staging slot
-            auto load = [&](bool is_k, int X, int cur, const Item &w) {
-                const int st = X % (is_k ? L::kKStages : L::kVStages);
-                const uint32_t bar = is_k ? bars.k_load(st) : bars.v_load(st);
-                const uint32_t dst = sbase + (is_k ? L::k_codes(st) : L::v_codes(st));
-                if (lane == 0)
-                    ptx::mbar_arrive_expect_tx(bar, (uint32_t)L::kCodeBytes);
-                if (lane < nsub)
-                    ptx::tma_load_3d(dst + lane * box_rows * D, is_k ? &tm_k : &tm_v, bar, 0, w.g, cur);
-                __syncwarp();
-            };
-            uint32_t starts = 0;
-            int X = 0;
-            bool ok = true;
-            while (ok && items.more()) {
-                const Item w = items.next();
-                for (int t = 0; t < 2; ++t) {
-                    if (w.ord > 0 && !(ok = wwait(bars.q_free(t), (w.ord - 1) & 1)))
-                        break;
-                    if (lane == 0)
-                        load_query_tile<D, I8>(&tm_q, bars, sbase, w, t, G, P);
-                    __syncwarp();
-                }
-                const int32_t *bt = p.block_tables + (size_t)w.b * p.max_blocks;
-                int next = sub_row(w, bt, 0);
-                for (int j = 0; ok && j < w.nkt; ++j, ++X) {
-                    const int cur = next;
-                    if (j + 1 < w.nkt)
-                        next = sub_row(w, bt, j + 1);
-                    starts = (starts << 1) | (j == 0 ? 1u : 0u);
-                    if (X >= L::kKStages) {
-                        const int e = release_event(X, L::kKStages, w.ord, starts, 0);
-                        if (!(ok = wwait(bars.released(e), (e / kIterRing) & 1)))
-                            break;
-                    }
-                    load(true, X, cur, w);
-                    if (X >= L::kVStages) {
-                        const int e = release_event(X, L::kVStages, w.ord, starts, 1);
-                        if (!(ok = wwait(bars.released(e), (e / kIterRing) & 1)))
-                            break;
-                    }
-                    load(false, X, cur, w);
-                }
-            }
-        } else if (I8 && (warp == kKProducerWarp || warp == kVProducerWarp)) {
-            // ------------------------------------------------------------ INT8: Q conversion
-            ItemIter items(p.tiles, p.num_items, P);
-            // warp 8: query tile 0; warp 10: query tile 1
-            const int tq = warp == kKProducerWarp ? 0 : 1;
-            bool ok = true;
-            while (ok && items.more()) {
-                const Item w = items.next();
-                if (!(ok = wwait(bars.q_full(tq), w.ord & 1)))
-                    break;
-                q_tile_to_f16<D>(sgen + L::kQ + tq * L::kTileBytes, lane);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(bars.q_ready(tq));
-            }
-        } else if (!I8 && warp == kMmaWarp) {
-            // ------------------------------------------------------------ MMA issuer (bf16: the whole
-            // warp, one elected lane issuing each MMA and commit; INT8: lane 0 alone, which measured
-            // faster with that kernel's 16 warps)
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA issuer (the whole warp,
+            // one elected lane issuing each MMA and commit)
 
             ItemIter items(p.tiles, p.num_items, P);
-            // INT8 cache: f16 operands (exact codes, f16 Q and P)
-            constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
-            constexpr uint32_t idesc_o = I8 ? ptx::idesc_f16(128, D, 1) : ptx::idesc_bf16(128, D, 1);
+            constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, 0);
+            constexpr uint32_t idesc_o = ptx::idesc_bf16(128, D, 1);
             // Shared-memory descriptors: a constant upper word and a lower word of base
             // address + the k step's offset.  The base passes through an empty asm so that
             // it is rebuilt at each use instead of hoisting all 16 k-step descriptors into
@@ -1013,7 +647,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 const Item w = items.next();
                 const uint32_t qpar = w.ord & 1;
                 const int jfix = straddle_tile(w, p.fused, box_rows);
-                ok = wwait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) && wwait(bars.k_full(ks), kph);
+                ok = wwait(bars.q_full(0), qpar) && wwait(bars.k_full(ks), kph);
                 if (ok && jfix == 0) { // key tile 0's straddling box patched
                     ok = wwait(bars.k_fix(ks), (fixpar >> ks) & 1u);
                     fixpar ^= 1u << ks;
@@ -1025,7 +659,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 ptx::mma_commit_warp(bars.s_full(0));
                 // query tile 1 is waited for only now (also when empty: its buffer is
                 // released below, and every load of it must be consumed first)
-                if (!(ok = wwait(I8 ? bars.q_ready(1) : bars.q_full(1), qpar)))
+                if (!(ok = wwait(bars.q_full(1), qpar)))
                     break;
                 if (w.nkt1 > 0) {
                     ptx::tc_fence_after();
@@ -1051,7 +685,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                         if (!v_ready) {
                             if (!(ok = wwait(bars.v_full(vs), vph)))
                                 return;
-                            if (!I8 && ((w.tail && j == w.nkt - 1) || j == jfix)) {
+                            if ((w.tail && j == w.nkt - 1) || j == jfix) {
                                 if (!(ok = wwait(bars.v_tail(vs), (tailpar >> vs) & 1u)))
                                     return;
                                 tailpar ^= 1u << vs;
@@ -1087,123 +721,6 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                     if (!ok)
                         break;
                     ptx::mma_commit_warp(bars.released(E + j + 1)); // V tile j and K tile j + 1 read
-                    if (++vs == L::kVStages) {
-                        vs = 0;
-                        vph ^= 1;
-                    }
-                    if (k_next && ++ks == L::kKStages) {
-                        ks = 0;
-                        kph ^= 1;
-                    }
-                }
-                E += w.nkt + 1;
-            }
-        } else if (I8 && warp == kMmaWarp && lane == 0) {
-            // ------------------------------------------------------------ INT8: MMA issuer (lane 0)
-            ItemIter items(p.tiles, p.num_items, P);
-            // INT8 cache: f16 operands (exact codes, f16 Q and P)
-            constexpr uint32_t idesc_s = I8 ? ptx::idesc_f16(128, 128, 0) : ptx::idesc_bf16(128, 128, 0);
-            constexpr uint32_t idesc_o = I8 ? ptx::idesc_f16(128, D, 1) : ptx::idesc_bf16(128, D, 1);
-            // Shared-memory descriptors: a constant upper word and a lower word of base
-            // address + the k step's offset.  The base passes through an empty asm so that
-            // it is rebuilt at each use instead of hoisting all 16 k-step descriptors into
-            // registers (this warpgroup runs on few).
-            const uint32_t hi_k = (uint32_t)(ptx::smem_desc(0, 16, 1024, ptx::kSwizzle128B) >> 32);
-            const uint32_t hi_v = (uint32_t)(ptx::smem_desc(0, L::kPanelBytes, 1024, ptx::kSwizzle128B) >> 32);
-            auto desc = [](uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; };
-            auto issue_s = [&](int t, int ks) {
-                uint32_t qa = (uint32_t)ptx::smem_desc(sbase + L::kQ + t * L::kTileBytes, 16, 1024, ptx::kSwizzle128B);
-                uint32_t kb = (uint32_t)ptx::smem_desc(sbase + L::kK + ks * L::kTileBytes, 16, 1024, ptx::kSwizzle128B);
-                asm volatile("" : "+r"(qa), "+r"(kb));
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = ((kk >> 2) * L::kPanelBytes + (kk & 3) * 32) >> 4;
-                    ptx::mma_bf16_ss(tmem + t * 256, desc(qa + o, hi_k), desc(kb + o, hi_k), idesc_s, kk > 0);
-                }
-            };
-            auto issue_pv = [&](int t, int vs, bool first) {
-                uint32_t vb = (uint32_t)ptx::smem_desc(sbase + L::kV + vs * L::kTileBytes, L::kPanelBytes, 1024,
-                                                       ptx::kSwizzle128B);
-                asm volatile("" : "+r"(vb));
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    ptx::mma_bf16_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8, desc(vb + kk * (2048 >> 4), hi_v),
-                                     idesc_o, (!first || kk > 0) ? 1u : 0u);
-            };
-            // ring positions kept as counters (no division in the issue loop)
-            int ks = 0, kph = 0, vs = 0, vph = 0;
-            uint32_t np = 0;       // bit t: parity of the P tiles of query tile t consumed so far
-            uint32_t tailpar = 0;  // bit s: parity of the tail tiles V slot s has held
-            int E = 0;             // first release event of the current item
-            bool ok = true;
-            while (ok && items.more()) {
-                const Item w = items.next();
-                const uint32_t qpar = w.ord & 1;
-                ok = wait(I8 ? bars.q_ready(0) : bars.q_full(0), qpar) && wait(bars.k_full(ks), kph);
-                if (!ok)
-                    break;
-                ptx::tc_fence_after();
-                issue_s(0, ks);
-                ptx::mma_commit(bars.s_full(0));
-                // query tile 1 is waited for only now (also when empty: its buffer is
-                // released below, and every load of it must be consumed first)
-                if (!(ok = wait(I8 ? bars.q_ready(1) : bars.q_full(1), qpar)))
-                    break;
-                if (w.nkt1 > 0) {
-                    ptx::tc_fence_after();
-                    issue_s(1, ks);
-                    ptx::mma_commit(bars.s_full(1));
-                }
-                ptx::mma_commit(bars.released(E)); // K tile 0 read by both score MMAs
-                if (w.nkt0 == 1)
-                    ptx::mma_commit(bars.q_free(0));
-                if (w.nkt1 <= 1)
-                    ptx::mma_commit(bars.q_free(1));
-                if (++ks == L::kKStages) {
-                    ks = 0;
-                    kph ^= 1;
-                }
-                for (int j = 0; ok && j < w.nkt; ++j) {
-                    bool v_ready = false, k_next = false;
-                    // one query tile: PV(t, j), then S(t, j + 1) into the same TMEM columns
-                    auto step = [&](const int t, const int ntk) {
-                        if (!(ok = wait(bars.p_full(t), (np >> t) & 1u)))
-                            return;
-                        np ^= 1u << t;
-                        if (!v_ready) {
-                            if (!(ok = wait(bars.v_full(vs), vph)))
-                                return;
-                            if (!I8 && w.tail && j == w.nkt - 1) {
-                                if (!(ok = wait(bars.v_tail(vs), (tailpar >> vs) & 1u)))
-                                    return;
-                                tailpar ^= 1u << vs;
-                            }
-                            v_ready = true;
-                        }
-                        ptx::tc_fence_after();
-                        issue_pv(t, vs, j == 0);
-                        if (j + 1 == ntk)
-                            ptx::mma_commit(bars.o_full(t)); // O_t final
-                        if (j + 1 < ntk) {
-                            if (!k_next) {
-                                if (!(ok = wait(bars.k_full(ks), kph)))
-                                    return;
-                                ptx::tc_fence_after();
-                                k_next = true;
-                            }
-                            issue_s(t, ks);
-                            ptx::mma_commit(bars.s_full(t));
-                            if (j + 2 == ntk)
-                                ptx::mma_commit(bars.q_free(t)); // that was the last read of Q_t
-                        }
-                    };
-                    if (j < w.nkt0)
-                        step(0, w.nkt0);
-                    if (ok && j < w.nkt1)
-                        step(1, w.nkt1);
-                    if (!ok)
-                        break;
-                    ptx::mma_commit(bars.released(E + j + 1)); // V tile j and K tile j + 1 read
                     if (++vs == L::kVStages) {
                         vs = 0;
                         vph ^= 1;
@@ -1307,7 +824,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                             ptx::f2_fma(ptx::f2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, negm2), x0, x1);
                         const float e0 = ptx::ex2(x0), e1 = ptx::ex2(x1); // masked columns: 2^-inf = 0
                         sum2[(c >> 1) & 3] = ptx::f2_add(sum2[(c >> 1) & 3], ptx::f2(e0, e1));
-                        pk[(c >> 1) & 31] = I8 ? ptx::pack_f16(e0, e1) : ptx::pack_bf16(e0, e1);
+                        pk[(c >> 1) & 31] = ptx::pack_bf16(e0, e1);
                     }
                     ptx::tmem_st32(s_col + 32 * h, pk);
                 }
@@ -1352,7 +869,7 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
                 p.out + ((size_t)(w.cq0 + w.q0 + t * P + rpos) * p.num_heads + (size_t)w.g * G + rhead) * D;
             // TMEM loads in batches of kBatch 32-column chunks, one wait per batch
             // (bf16: the whole row at once; the register budget allows it)
-            constexpr int kBatch = I8 ? 1 : D / 32;
+            constexpr int kBatch = D / 32;
 #pragma unroll
             for (int c0 = 0; c0 < D / 32; c0 += kBatch) {
                 uint32_t o[kBatch][32];
@@ -1395,26 +912,26 @@ __global__ void __launch_bounds__(kThreadsOf<I8>, 1)
     }
 }
 
-template <int D, bool I8>
+template <int D>
 int launch(const PrefillArgs &a, cudaStream_t stream)
 {
-    using L = PfLayout<D, I8>;
-    if (int rc = ensure_smem<prefill_kernel<D, I8>>(L::kSmemBytes, "prefill"))
+    using L = PfLayout<D>;
+    if (int rc = ensure_smem<prefill_kernel<D>>(L::kSmemBytes, "prefill"))
         return rc;
-    // The register hand-over inside the kernel assumes kLaunchRegsOf<I8> per thread
-    // at launch; with fewer the softmax warpgroups' request could never be granted.
+    // The register hand-over inside the kernel assumes kLaunchRegs per thread at
+    // launch; with fewer the softmax warpgroups' request could never be granted.
     static std::atomic<int> launch_regs{0};
     int nreg = launch_regs.load(std::memory_order_acquire);
     if (nreg == 0) {
         cudaFuncAttributes fa{};
-        const cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, I8>);
+        const cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
         if (e != cudaSuccess)
             return fail(PA_ERR_CUDA, "prefill kernel attributes: %s", cudaGetErrorString(e));
         launch_regs.store(nreg = fa.numRegs, std::memory_order_release);
     }
-    if (nreg != kLaunchRegsOf<I8>)
+    if (nreg != kLaunchRegs)
         return fail(PA_ERR_UNSUPPORTED, "prefill kernel built with %d registers per thread, needs %d", nreg,
-                    kLaunchRegsOf<I8>);
+                    kLaunchRegs);
     const pa_dims &d = a.dims;
     const int G = d.num_heads / d.num_kv_heads;
     const uint64_t rows = (uint64_t)d.num_blocks * d.block_size;
@@ -1429,26 +946,15 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     // One box per physical block (or per 128-key tile); for a fused store whose cached
     // prefixes end inside a box, boxes of 16 rows, so a straddling box has at most 15 new
     // rows for the producer to patch in.
-    const uint32_t box_rows = !I8 && a.k_in && a.small_boxes ? 16u : d.block_size < 128 ? (uint32_t)d.block_size : 128u;
-    if constexpr (I8) { // raw codes: one head's D bytes x box_rows rows, unswizzled
-        constexpr CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-        constexpr CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
-        if ((rc = encode_tmap_3d(&tk, u8, a.k_cache, D, d.num_kv_heads, rows, (uint64_t)D, (uint64_t)d.num_kv_heads * D,
-                                 D, 1, box_rows, none, "int8 k_cache")) != PA_OK)
-            return rc;
-        if ((rc = encode_tmap_3d(&tv, u8, a.v_cache, D, d.num_kv_heads, rows, (uint64_t)D, (uint64_t)d.num_kv_heads * D,
-                                 D, 1, box_rows, none, "int8 v_cache")) != PA_OK)
-            return rc;
-    } else {
-        if ((rc = encode_tmap_3d(&tk, bf16, a.k_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
-                                 (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "k_cache")) != PA_OK)
-            return rc;
-        if ((rc = encode_tmap_3d(&tv, bf16, a.v_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
-                                 (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "v_cache")) != PA_OK)
-            return rc;
-    }
+    const uint32_t box_rows = a.k_in && a.small_boxes ? 16u : d.block_size < 128 ? (uint32_t)d.block_size : 128u;
+    if ((rc = encode_tmap_3d(&tk, bf16, a.k_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
+                             (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "k_cache")) != PA_OK)
+        return rc;
+    if ((rc = encode_tmap_3d(&tv, bf16, a.v_cache, D, d.num_kv_heads, rows, (uint64_t)D * 2,
+                             (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "v_cache")) != PA_OK)
+        return rc;
     CUtensorMap tkin = tk, tvin = tv; // fused store: the new keys' inputs, same box as the cache's
-    if (!I8 && a.k_in) {
+    if (a.k_in) {
         if ((rc = encode_tmap_3d(&tkin, bf16, a.k_in, D, d.num_kv_heads, (uint64_t)a.total_q, (uint64_t)D * 2,
                                  (uint64_t)d.num_kv_heads * D * 2, 64, 1, box_rows, sw, "k")) != PA_OK)
             return rc;
@@ -1471,42 +977,21 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     p.max_blocks = a.max_blocks_per_seq;
     p.num_slots = (int32_t)rows;
     p.num_kv_heads = d.num_kv_heads;
-    p.k_scale = static_cast<const __half *>(a.k_scale);
-    p.v_scale = static_cast<const __half *>(a.v_scale);
     p.num_items = a.num_tiles;
     p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
-    p.fused = !I8 && a.k_in ? 1 : 0;
+    p.fused = a.k_in ? 1 : 0;
     p.slot_mapping = a.slot_mapping;
     p.k_in = static_cast<const uint4 *>(a.k_in);
     p.v_in = static_cast<const uint4 *>(a.v_in);
     p.k_cache = static_cast<uint4 *>(const_cast<void *>(a.k_cache));
     p.v_cache = static_cast<uint4 *>(const_cast<void *>(a.v_cache));
-    p.store8 = I8 && a.k_in ? 1 : 0;
-    p.total_q = a.total_q;
-    p.grid_sync = a.grid_sync;
     // persistent: one CTA per SM (shared memory and TMEM admit one), each walking its items
     int sms = 0;
     if (int rc2 = sm_count(&sms))
         return rc2;
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-    cudaError_t e;
-    if (p.store8) {
-        // the store pass ends in a grid barrier: every CTA must be resident at once
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(kThreadsOf<I8>);
-        cfg.dynamicSmemBytes = L::kSmemBytes;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, prefill_kernel<D, I8>, tq, tk, tv, tkin, tvin, p);
-    } else {
-        prefill_kernel<D, I8><<<(unsigned)grid, kThreadsOf<I8>, L::kSmemBytes, stream>>>(tq, tk, tv, tkin, tvin, p);
-        e = cudaGetLastError();
-    }
+    prefill_kernel<D><<<(unsigned)grid, kThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tkin, tvin, p);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
@@ -1519,13 +1004,7 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
 int launch_prefill(const PrefillArgs &a, void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return a.dims.head_dim == 128 ? launch<128, false>(a, s) : launch<64, false>(a, s);
-}
-
-int launch_prefill_int8(const PrefillArgs &a, void *stream)
-{
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return a.dims.head_dim == 128 ? launch<128, true>(a, s) : launch<64, true>(a, s);
+    return a.dims.head_dim == 128 ? launch<128>(a, s) : launch<64>(a, s);
 }
 
 int read_prefill_error(uint32_t *code)

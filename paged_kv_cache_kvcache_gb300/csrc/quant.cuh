@@ -18,6 +18,7 @@
 
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -59,11 +60,11 @@ __device__ __forceinline__ void load_row_part(const uint16_t *__restrict__ row, 
         p.v[i] = __ldcs(reinterpret_cast<const uint4 *>(row + 32 * h) + i);
 }
 
-// Quantises a loaded part into its 32 codes of the row (codes: the row's D int8
-// codes, 16-byte aligned); returns the row's fp32 scale (the caller stores its fp16
-// copy).  The kThreadsPerRow<D> threads of a row (adjacent lanes) call it together.
+// Quantises a loaded part into its 32 codes (c[w] holds codes 4w .. 4w + 3 of the part,
+// lowest byte first); returns the row's fp32 scale (the cache keeps its fp16 copy).  The
+// kThreadsPerRow<D> threads of a row (adjacent lanes) call it together.
 template <int D>
-__device__ __forceinline__ float quantise_row_part(const RowPart &p, int8_t *__restrict__ codes, int h)
+__device__ __forceinline__ float quantise_part(const RowPart &p, uint32_t (&c)[8])
 {
     auto word = [&](int e) { // the 32-bit word holding values 2e and 2e + 1
         const uint4 &u = p.v[e >> 2];
@@ -89,21 +90,58 @@ __device__ __forceinline__ float quantise_row_part(const RowPart &p, int8_t *__r
     const float scale = fmaxf(__fdiv_rn(a, 127.0f), 1e-8f);
     const float rcp = __frcp_rn(scale);
 #pragma unroll
-    for (int o = 0; o < 2; ++o) { // 16 codes per store
-        uint32_t c[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t w0 = word(8 * o + 2 * k), w1 = word(8 * o + 2 * k + 1);
-            const int c0 = code_of(__uint_as_float(w0 << 16), scale, rcp);
-            const int c1 = code_of(__uint_as_float(w0 & 0xffff0000u), scale, rcp);
-            const int c2 = code_of(__uint_as_float(w1 << 16), scale, rcp);
-            const int c3 = code_of(__uint_as_float(w1 & 0xffff0000u), scale, rcp);
-            c[k] = (uint32_t)(c0 & 0xff) | (uint32_t)(c1 & 0xff) << 8 | (uint32_t)(c2 & 0xff) << 16 |
-                   (uint32_t)(c3 & 0xff) << 24;
-        }
-        reinterpret_cast<uint4 *>(codes + 32 * h)[o] = make_uint4(c[0], c[1], c[2], c[3]);
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t w0 = word(2 * k), w1 = word(2 * k + 1);
+        const int c0 = code_of(__uint_as_float(w0 << 16), scale, rcp);
+        const int c1 = code_of(__uint_as_float(w0 & 0xffff0000u), scale, rcp);
+        const int c2 = code_of(__uint_as_float(w1 << 16), scale, rcp);
+        const int c3 = code_of(__uint_as_float(w1 & 0xffff0000u), scale, rcp);
+        c[k] = (uint32_t)(c0 & 0xff) | (uint32_t)(c1 & 0xff) << 8 | (uint32_t)(c2 & 0xff) << 16 |
+               (uint32_t)(c3 & 0xff) << 24;
     }
     return scale;
+}
+
+// quantise_part, with the 32 codes stored at codes + 32 h (codes: the row's D int8 codes,
+// 16-byte aligned).
+template <int D>
+__device__ __forceinline__ float quantise_row_part(const RowPart &p, int8_t *__restrict__ codes, int h)
+{
+    uint32_t c[8];
+    const float scale = quantise_part<D>(p, c);
+    uint4 *dst = reinterpret_cast<uint4 *>(codes + 32 * h);
+    dst[0] = make_uint4(c[0], c[1], c[2], c[3]);
+    dst[1] = make_uint4(c[4], c[5], c[6], c[7]);
+    return scale;
+}
+
+// Code j of the word (lowest byte first) as an exact fp32 value: the biased code
+// (code + 128, the byte xor 0x80) placed in the low mantissa bits of 2^23, minus
+// 2^23 + 128.
+__device__ __forceinline__ float code_value(uint32_t biased, int j)
+{
+    return __int_as_float((int)__byte_perm(biased, 0x4B000000u, 0x7540u | (uint32_t)j)) - 8388736.0f;
+}
+
+// The 32 codes of a part (as quantise_part returns them) dequantised to bf16:
+// RN(code * scale) with the product exact in fp32 (8-bit code, 11-bit fp16 scale),
+// i.e. one rounding of the exact value.  out[i] holds values 8i .. 8i + 7, lowest first.
+__device__ __forceinline__ void dequantise_part(const uint32_t (&c)[8], float scale, uint4 (&out)[4])
+{
+    uint32_t v[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t b = c[k] ^ 0x80808080u;
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+            const __nv_bfloat162 pair =
+                __floats2bfloat162_rn(code_value(b, j) * scale, code_value(b, j + 1) * scale);
+            v[2 * k + j / 2] = *reinterpret_cast<const uint32_t *>(&pair);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        out[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
 // Part h (loaded in p) of the K or V row of token t, KV head g, quantised into cache

@@ -109,6 +109,97 @@ int launch_store_kvcache_int8(const pa_dims &d, const void *k, const void *v, vo
     return PA_OK;
 }
 
+// INT8 prefill front end: the keys and values that a prefill batch attends over,
+// dequantised into a bf16 scratch cache of 128-token blocks, each sequence's keys
+// in consecutive blocks (the plan's scratch tables; scratch block sb holds keys
+// e[1] .. e[1] + 127 of sequence e[0], e = scratch_items[sb]).  "面试问答准备:
+// nano-vLLM 推理引擎优化", Q3, the prefill's dequantisation path: the values the
+// block table references, read as code x token scale in fp32 and rounded to the
+// model's dtype (bf16), feed the bf16 attention.  With `store`, the new tokens'
+// rows (positions from the cached prefix on) are first quantised from k_in/v_in
+// into the INT8 cache at their slots, as pa_store_kvcache_int8 does, and their
+// scratch rows dequantise those codes and the stored fp16 scale, so the scratch
+// holds what the cache then holds.
+//
+// Work unit: one (scratch row, tensor, KV head), handled by kThreadsPerRow<D>
+// adjacent threads (32 values each): unit u is row u / (2 Hkv), then K heads, then
+// V heads, so a warp reads and writes whole rows of K and of V (coalesced).  One
+// unit per thread group; HBM-bound: 3 bytes moved per value (1 read, 2 written).
+template <int D, bool kStore>
+__global__ void __launch_bounds__(256) int8_gather_kernel(const GatherArgs a)
+{
+    constexpr int TPR = quant::kThreadsPerRow<D>;
+    const uint32_t hkv = (uint32_t)a.num_kv_heads;
+    const uint32_t j = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t unit = j / TPR;
+    if (unit >= (uint32_t)a.scratch_blocks * 128u * 2u * hkv)
+        return;
+    const int h = (int)(j % TPR);
+    const uint32_t r = unit / (2u * hkv); // scratch row
+    const uint32_t c = unit - r * 2u * hkv;
+    const bool is_v = c >= hkv;
+    const int g = (int)(is_v ? c - hkv : c);
+    const int4 e = __ldg(reinterpret_cast<const int4 *>(a.scratch_items) + 2 * (r >> 7));
+    const int b = e.x, pos = e.y + (int)(r & 127), lk = e.z, cached = e.w;
+    if (pos >= lk)
+        return; // past the sequence end: the attention never reads this row's values
+    uint32_t code[8];
+    float sc;
+    if (kStore && pos >= cached) {
+        const int t = __ldg(a.scratch_items + 8 * (r >> 7) + 4) + pos; // packed row of the new token
+        const int32_t slot = __ldg(a.slot_mapping + t);
+        quant::RowPart part;
+        quant::load_row_part((is_v ? a.v_in : a.k_in) + ((size_t)t * hkv + g) * D, h, part);
+        const __half hs = __float2half_rn(quant::quantise_part<D>(part, code));
+        if (slot >= 0 && slot < a.num_slots) {
+            uint4 *dst = reinterpret_cast<uint4 *>((is_v ? a.v_codes_w : a.k_codes_w) + ((size_t)slot * hkv + g) * D +
+                                                   32 * h);
+            dst[0] = make_uint4(code[0], code[1], code[2], code[3]);
+            dst[1] = make_uint4(code[4], code[5], code[6], code[7]);
+            if (h == 0)
+                (is_v ? a.v_scale_w : a.k_scale_w)[((size_t)(slot / a.block_size) * hkv + g) * a.block_size +
+                                                   slot % a.block_size] = __half_as_ushort(hs);
+        } else if (slot != -1 && !is_v && g == 0 && h == 0) {
+            atomicOr(&g_store_error, 1u);
+        }
+        sc = __half2float(hs);
+    } else {
+        const int bs = a.block_size;
+        const int blk = __ldg(a.block_tables + (size_t)b * a.max_blocks + pos / bs);
+        const uint4 *src = reinterpret_cast<const uint4 *>((is_v ? a.v_codes : a.k_codes) +
+                                                           (((size_t)blk * bs + pos % bs) * hkv + g) * D + 32 * h);
+        const uint4 x0 = __ldcs(src), x1 = __ldcs(src + 1);
+        sc = __half2float(__ushort_as_half(__ldg((is_v ? a.v_scale : a.k_scale) + ((size_t)blk * hkv + g) * bs + pos % bs)));
+        code[0] = x0.x, code[1] = x0.y, code[2] = x0.z, code[3] = x0.w;
+        code[4] = x1.x, code[5] = x1.y, code[6] = x1.z, code[7] = x1.w;
+    }
+    uint4 o[4];
+    quant::dequantise_part(code, sc, o);
+    uint4 *dst = reinterpret_cast<uint4 *>((is_v ? a.v_out : a.k_out) + ((size_t)r * hkv + g) * D + 32 * h);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        dst[i] = o[i];
+}
+
+int launch_int8_gather(const GatherArgs &a, void *stream)
+{
+    const int threads = 256;
+    const int64_t n = (int64_t)a.scratch_blocks * 128 * 2 * a.num_kv_heads * (a.head_dim / 32);
+    if (n == 0)
+        return PA_OK;
+    if (n > INT32_MAX)
+        return fail(PA_ERR_UNSUPPORTED, "INT8 prefill scratch of %lld (row, tensor, head) units exceeds int32",
+                    (long long)(n / (a.head_dim / 32)));
+    const bool st = a.k_in != nullptr;
+    auto kern = a.head_dim == 128 ? (st ? int8_gather_kernel<128, true> : int8_gather_kernel<128, false>)
+                                  : (st ? int8_gather_kernel<64, true> : int8_gather_kernel<64, false>);
+    kern<<<(unsigned)((n + threads - 1) / threads), threads, 0, (cudaStream_t)stream>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "int8 gather launch: %s", cudaGetErrorString(e));
+    return PA_OK;
+}
+
 int read_store_error(uint32_t *code)
 {
     uint32_t v = 0, zero = 0;

@@ -41,7 +41,10 @@ class pa_prefill_meta(ctypes.Structure):
                 ("num_tiles", ctypes.c_int32), ("rows_per_tile", ctypes.c_int32), ("prefix_aligned", ctypes.c_int32),
                 ("off_cu_seqlens_q", ctypes.c_uint64), ("off_cu_seqlens_k", ctypes.c_uint64),
                 ("off_block_tables", ctypes.c_uint64), ("off_slot_mapping", ctypes.c_uint64),
-                ("off_tiles", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64), ("off_grid_sync", ctypes.c_uint64)]
+                ("off_tiles", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64),
+                ("off_scratch_tables", ctypes.c_uint64), ("off_scratch_items", ctypes.c_uint64),
+                ("workspace_bytes", ctypes.c_uint64), ("scratch_blocks", ctypes.c_int32),
+                ("scratch_pitch", ctypes.c_int32)]
 
 
 class pa_decode_meta(ctypes.Structure):
@@ -91,9 +94,8 @@ def lib() -> ctypes.CDLL:
                                                P]
             L.pa_store_kvcache_int8.argtypes = [P, P, P, P, P, P, P, P, I32, P]
             L.pa_decode_int8.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, SZ, P]
-            L.pa_prefill_varlen_int8.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P]
-            L.pa_prefill_varlen_int8_fused.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P,
-                                                       P, P]
+            L.pa_prefill_varlen_int8.argtypes = [P] * 11 + [ctypes.c_float] + [P] * 4 + [SZ, P]
+            L.pa_prefill_varlen_int8_fused.argtypes = [P] * 14 + [ctypes.c_float] + [P] * 4 + [SZ, P]
             L.pa_last_error_string.argtypes = []
             L.pa_last_error_string.restype = ctypes.c_char_p
             L.pa_read_device_error.argtypes = [P, P]
@@ -350,26 +352,51 @@ def pa_store_kvcache_int8(dims: pa_dims, k, v, k_cache, v_cache, k_scale, v_scal
            "pa_store_kvcache_int8")
 
 
+def prefill_workspace(plan: PrefillPlan, device="cuda") -> Optional[torch.Tensor]:
+    """The INT8 prefill's workspace (its bf16 scratch cache) for this plan."""
+    n = int(plan.meta.workspace_bytes)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def _call_workspace(plan: PrefillPlan, workspace, device, stream):
+    """The caller's workspace, or one allocated for this call (kept from reuse until the
+    call's stream has passed it)."""
+    if workspace is None:
+        workspace = prefill_workspace(plan, device)
+        if workspace is not None and stream is not None:
+            st = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream))
+            workspace.record_stream(st)
+    return workspace
+
+
 def pa_prefill_varlen_int8(dims: pa_dims, q, k_cache, v_cache, k_scale, v_scale, plan: PrefillPlan, scale: float,
-                           out, stream=None):
-    """pa_prefill_varlen over an INT8 cache (same plan as pa_prefill_varlen)."""
+                           out, workspace=None, stream=None):
+    """pa_prefill_varlen over an INT8 cache (same plan as pa_prefill_varlen; workspace of
+    plan.meta.workspace_bytes, allocated here when not given)."""
     m = plan.meta
+    workspace = _call_workspace(plan, workspace, q.device, stream)
+    ws_bytes = int(workspace.numel()) if isinstance(workspace, torch.Tensor) else 0
     _check(lib().pa_prefill_varlen_int8(ctypes.byref(dims), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                         _ptr(v_scale), plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
-                                        plan.dptr(m.off_block_tables), float(scale), _ptr(out), ctypes.byref(m),
-                                        plan.dptr(m.off_tiles), _stream(stream)), "pa_prefill_varlen_int8")
+                                        plan.dptr(m.off_block_tables), plan.dptr(m.off_scratch_tables),
+                                        plan.dptr(m.off_scratch_items), float(scale), _ptr(out), ctypes.byref(m),
+                                        plan.dptr(m.off_tiles), _ptr(workspace), ws_bytes, _stream(stream)),
+           "pa_prefill_varlen_int8")
 
 
 def pa_prefill_varlen_int8_fused(dims: pa_dims, q, k, v, k_cache, v_cache, k_scale, v_scale, plan: PrefillPlan,
-                                 scale: float, out, stream=None):
-    """pa_store_kvcache_int8 of the new tokens' k/v at the plan's slots + pa_prefill_varlen_int8, in one launch."""
+                                 scale: float, out, workspace=None, stream=None):
+    """pa_store_kvcache_int8 of the new tokens' k/v at the plan's slots + pa_prefill_varlen_int8, in one call."""
     m = plan.meta
+    workspace = _call_workspace(plan, workspace, q.device, stream)
+    ws_bytes = int(workspace.numel()) if isinstance(workspace, torch.Tensor) else 0
     _check(lib().pa_prefill_varlen_int8_fused(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache),
                                               _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                                               plan.dptr(m.off_cu_seqlens_q), plan.dptr(m.off_cu_seqlens_k),
                                               plan.dptr(m.off_block_tables), plan.dptr(m.off_slot_mapping),
+                                              plan.dptr(m.off_scratch_tables), plan.dptr(m.off_scratch_items),
                                               float(scale), _ptr(out), ctypes.byref(m), plan.dptr(m.off_tiles),
-                                              plan.dptr(m.off_grid_sync), _stream(stream)),
+                                              _ptr(workspace), ws_bytes, _stream(stream)),
            "pa_prefill_varlen_int8_fused")
 
 

@@ -23,12 +23,12 @@ def test_library_exports_every_declared_symbol():
     for name in declared:
         assert hasattr(lib, name), name
     assert set(pa.EXPORTS) == declared
-    assert pa.pa_version() == 0x000400
+    assert pa.pa_version() == 0x000500
 
 
 def test_struct_sizes_match_header_layout():
     assert ctypes.sizeof(pa.pa_dims) == 20
-    assert ctypes.sizeof(pa.pa_prefill_meta) == 8 * 4 + 7 * 8
+    assert ctypes.sizeof(pa.pa_prefill_meta) == 8 * 4 + 9 * 8 + 2 * 4
     # fields added after total_bytes leave the earlier offsets where they were
     assert pa.pa_prefill_meta.total_bytes.offset == 8 * 4 + 5 * 8
     assert ctypes.sizeof(pa.pa_decode_meta) == 6 * 4 + 7 * 8
@@ -275,10 +275,22 @@ def test_int8_fused_and_copy_calls_reject_bad_args_without_touching_the_gpu():
     bad = pa.make_dims(4, 16, 4, 2, 96)
     pm = pa.pa_prefill_meta()
     pm.num_tiles, pm.total_q, pm.num_seqs, pm.max_blocks_per_seq, pm.rows_per_tile = 1, 1, 1, 1, 64
-    assert L.pa_prefill_varlen_int8(ctypes.byref(bad), 16, 16, 16, 16, 16, 16, 16, 16, f(0.1), 16, ctypes.byref(pm),
-                                    16, None) == pa.PA_ERR_UNSUPPORTED
-    assert L.pa_prefill_varlen_int8(ctypes.byref(dims), 16, 16, 16, None, 16, 16, 16, 16, f(0.1), 16,
-                                    ctypes.byref(pm), 16, None) == pa.PA_ERR_INVALID_ARG
+    pm.scratch_blocks, pm.scratch_pitch = 1, 1
+    pm.workspace_bytes = 128 * 2 * 64 * 4  # dims: 2 KV heads, D 64
+
+    def int8_call(d=dims, ks=16, stab=16, ws=16, ws_bytes=pm.workspace_bytes):
+        return L.pa_prefill_varlen_int8(ctypes.byref(d), 16, 16, 16, ks, 16, 16, 16, 16, stab, 16, f(0.1), 16,
+                                        ctypes.byref(pm), 16, ws, ws_bytes, None)
+
+    assert int8_call(d=bad) == pa.PA_ERR_UNSUPPORTED
+    assert int8_call(ks=None) == pa.PA_ERR_INVALID_ARG                      # scales
+    assert int8_call(stab=None) == pa.PA_ERR_INVALID_ARG                    # scratch tables
+    assert int8_call(ws=None) == pa.PA_ERR_INVALID_ARG                      # workspace
+    assert int8_call(ws=24) == pa.PA_ERR_INVALID_ARG                        # misaligned workspace
+    assert int8_call(ws_bytes=pm.workspace_bytes - 16) == pa.PA_ERR_WORKSPACE
+    pm.workspace_bytes += 16  # not the scratch size of these dims
+    assert int8_call(ws_bytes=1 << 30) == pa.PA_ERR_INVALID_ARG
+    pm.workspace_bytes -= 16
     # fused decode: NULL new-token rows or slot mapping
     assert L.pa_decode_fused(ctypes.byref(dims), 16, None, 16, 16, 16, 16, 16, 16, f(0.1), 16, ctypes.byref(dm), 16,
                              16, None, 0, None) == pa.PA_ERR_INVALID_ARG
@@ -334,33 +346,57 @@ def test_prefill_int8_fused_rejects_bad_args_without_touching_the_gpu():
     L = pa.lib()
     pm = pa.pa_prefill_meta()
     pm.num_tiles, pm.total_q, pm.num_seqs, pm.max_blocks_per_seq, pm.rows_per_tile = 1, 1, 1, 1, 64
+    pm.scratch_blocks, pm.scratch_pitch, pm.workspace_bytes = 1, 1, 128 * 2 * 64 * 4
     f = ctypes.c_float
 
-    def call(q=16, k=16, v=16, kc=16, vc=16, ks=16, vs=16, slots=16, scale=0.1, sync=16):
-        return L.pa_prefill_varlen_int8_fused(ctypes.byref(dims), q, k, v, kc, vc, ks, vs, 16, 16, 16, slots,
-                                              f(scale), 16, ctypes.byref(pm), 16, sync, None)
+    def call(q=16, k=16, v=16, kc=16, vc=16, ks=16, vs=16, slots=16, scale=0.1, sseq=16, ws=16):
+        return L.pa_prefill_varlen_int8_fused(ctypes.byref(dims), q, k, v, kc, vc, ks, vs, 16, 16, 16, slots, 16,
+                                              sseq, f(scale), 16, ctypes.byref(pm), 16, ws, pm.workspace_bytes, None)
 
     assert call(k=None) == pa.PA_ERR_INVALID_ARG       # new-token rows
     assert call(vs=None) == pa.PA_ERR_INVALID_ARG      # scales
     assert call(slots=None) == pa.PA_ERR_INVALID_ARG   # slot mapping
-    assert call(sync=None) == pa.PA_ERR_INVALID_ARG    # the plan's barrier words
-    assert call(sync=18) == pa.PA_ERR_INVALID_ARG      # barrier words not 4-byte aligned
+    assert call(sseq=None) == pa.PA_ERR_INVALID_ARG    # the plan's scratch block owners
+    assert call(ws=None) == pa.PA_ERR_INVALID_ARG      # workspace
     assert call(v=24) == pa.PA_ERR_INVALID_ARG         # misaligned rows
     assert call(ks=40) == pa.PA_ERR_INVALID_ARG        # misaligned scales
     assert call(scale=-1.0) == pa.PA_ERR_INVALID_ARG
     pm.num_tiles = 0  # nothing to do: no launch, no error
     assert L.pa_prefill_varlen_int8_fused(ctypes.byref(dims), None, None, None, None, None, None, None, None, None,
-                                          None, None, f(0.1), None, ctypes.byref(pm), None, None,
+                                          None, None, None, None, f(0.1), None, ctypes.byref(pm), None, None, 0,
                                           None) == pa.PA_OK
 
 
-def test_pack_prefill_grid_sync_words_are_zero():
-    """The packed image carries the fused INT8 launch's two barrier words, zeroed, after the work list."""
-    dims = pa.make_dims(64, 16, 4, 2, 64)
-    lens, qlens = [40, 17], [8, 17]
-    blocks = [list(range(i * 8, i * 8 + -(-n // 16))) for i, n in enumerate(lens)]
+def test_pack_prefill_scratch_tables():
+    """The INT8 prefill's scratch cache: ceil(seq_len / 128) consecutive 128-token blocks for each
+    sequence with new tokens, in sequence order (none for a sequence without new tokens), the tables
+    -1 padded to the widest sequence, each scratch block's entry (sequence, first key, key count,
+    cached prefix, packed row of its new keys minus the prefix), and K + V bf16 bytes."""
+    dims = pa.make_dims(512, 16, 8, 2, 128)
+    lens, qlens = [300, 17, 128, 129, 1000], [8, 0, 128, 1, 5]
+    blocks, o = [], 0
+    for n in lens:
+        blocks.append(list(range(o, o + -(-n // 16))))
+        o += -(-n // 16)
     plan = pa.pa_pack_prefill(dims, lens, qlens, blocks, pin=False)
     m = plan.meta
-    assert m.off_grid_sync >= m.off_tiles + 4 * 8 * m.num_tiles
-    assert m.off_grid_sync % 4 == 0 and m.off_grid_sync + 8 <= m.total_bytes
-    assert list(plan.host_array(m.off_grid_sync, 2)) == [0, 0]
+    per = [-(-n // 128) if q > 0 else 0 for n, q in zip(lens, qlens)]   # 3, 0, 1, 2, 8
+    assert m.scratch_blocks == sum(per) == 14 and m.scratch_pitch == max(per) == 8
+    assert m.workspace_bytes == 14 * 128 * 2 * 128 * 2 * 2
+    tab = np.asarray(plan.host_array(m.off_scratch_tables, 5 * 8)).reshape(5, 8)
+    first = np.concatenate([[0], np.cumsum(per)[:-1]])
+    for b in range(5):
+        want = [first[b] + i if i < per[b] else -1 for i in range(8)]
+        assert list(tab[b]) == want, b
+    items = np.asarray(plan.host_array(m.off_scratch_items, 14 * 8)).reshape(14, 8)
+    cu_q = np.concatenate([[0], np.cumsum(qlens)])
+    want = []
+    for b in range(5):
+        for i in range(per[b]):
+            cached = lens[b] - qlens[b]
+            want.append([b, 128 * i, lens[b], cached, cu_q[b] - cached, 0, 0, 0])
+    assert items.tolist() == want
+    assert [w[0] for w in want] == [0, 0, 0, 2, 3, 3] + [4] * 8
+    assert m.off_scratch_tables >= m.off_tiles + 4 * 8 * m.num_tiles
+    assert m.off_scratch_items >= m.off_scratch_tables + 4 * 5 * 8 and m.off_scratch_items % 16 == 0
+    assert m.off_scratch_items + 4 * 8 * 14 <= m.total_bytes

@@ -1,10 +1,10 @@
 """INT8 prefill on the GPU against the oracle's attention over the dequantised cache.
 
 Method: "面试问答准备: nano-vLLM 推理引擎优化", Q3 — per-(token, KV head) INT8
-codes with fp16 scales, dequantised inside the kernel (each code tile turned
-once into fp16 code x token scale for the tensor cores; no floating copy of
-the cache).  Tolerances as for the bf16 path: max |err| <= 2e-2, relative
-RMS <= 1e-2.
+codes with fp16 scales; the prefill reads the keys and values its batch
+references as code x token scale rounded to bf16 (a gather launch into a
+scratch cache) and runs the bf16 attention over them.  Tolerances as for the
+bf16 path: max |err| <= 2e-2, relative RMS <= 1e-2.
 """
 import numpy as np
 import pytest
@@ -123,10 +123,10 @@ def test_int8_prefill_single_32k_sequence_sampled():
 
 
 def test_int8_prefill_and_decode_over_mixed_token_magnitudes():
-    """Tokens whose K/V magnitudes span 1e-4 .. 10^0.5 (scales down to ~1e-6, so that fp16
-    code x scale products fall in the subnormal range, and up to about 3x those of N(0, 1)
-    data) and all-zero tokens (scale 0): a prefill over them, then a decode of each
-    sequence's last token."""
+    """Tokens whose K/V magnitudes span 1e-4 .. 10^0.5 (scales down to ~1e-6, so that the
+    decode's fp16 code x scale products fall in the subnormal range, and up to about 3x
+    those of N(0, 1) data) and all-zero tokens (scale 0): a prefill over them, then a
+    decode of each sequence's last token."""
     hq, hkv, d, bs = 8, 2, 128, 16
     lens = np.array([300, 77, 129], np.int32)
     nb = int(sum(-(-l // bs) for l in lens)) + 3
