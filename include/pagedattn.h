@@ -518,12 +518,15 @@ int pa_selftest_bounded_wait(uint32_t timeout_us, int arrive_first, pa_stream_t 
  */
 int pa_stream_read(const void *src, size_t bytes, uint32_t *sink, pa_stream_t stream);
 
-/* Library version, e.g. 0x000400 for 0.4.0.  0.2.0 added pa_prefill_varlen_fused
+/* Library version, e.g. 0x000500 for 0.5.0.  0.2.0 added pa_prefill_varlen_fused
  * and gave pa_prefill_meta's spare field its meaning (prefix_aligned); 0.3.0
  * made pa_prefill_varlen_fused one launch for any cached prefix and added
- * pa_stream_read; 0.4.0 added pa_prefill_varlen_int8_fused and
- * pa_prefill_meta.off_grid_sync (a field after total_bytes: the earlier
- * fields keep their offsets). */
+ * pa_stream_read; 0.4.0 added pa_prefill_varlen_int8_fused; 0.5.0 made the
+ * INT8 prefill a bf16 gather into caller workspace followed by the bf16 kernel
+ * (pa_prefill_varlen_int8 and pa_prefill_varlen_int8_fused take the scratch
+ * tables, the scratch items and the workspace) and replaced pa_prefill_meta's
+ * barrier words with the scratch fields (after total_bytes: the earlier fields
+ * keep their offsets). */
 int pa_version(void);
 
 #ifdef __cplusplus
