@@ -43,9 +43,9 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 # of the 64 sequences, scaled by 4 (traffic grows with the sequences).  Must be
 # re-captured (or set to None) whenever one of these kernels changes.
 NCU_TRAFFIC = {"qwen25": {"prefill": 232.9e6, "decode": 4.334e9}}
-NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": None, "decode": 2.214e9}}
+NCU_TRAFFIC_INT8 = {"qwen25": {"prefill": 249.7e6, "decode": 2.214e9}}  # prefill: gather + prefill kernel
 NCU_TRAFFIC_FUSED_PREFILL = {"qwen25": 268.8e6}
-NCU_TRAFFIC_INT8_FUSED_PREFILL = {"qwen25": None}
+NCU_TRAFFIC_INT8_FUSED_PREFILL = {"qwen25": 267.5e6}  # quantising gather + prefill kernel
 NCU_TRAFFIC_COPY_BLOCKS = 488.3e6  # 268.5 MB read + 219.7 MB written (part of the writes still in L2 at exit)
 
 
