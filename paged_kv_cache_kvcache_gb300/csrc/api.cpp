@@ -226,6 +226,7 @@ static int prefill_int8(const char *fn, bool store, const pa_dims *dims, const v
     g.scratch_items = scratch_items;
     g.k_out = static_cast<uint16_t *>(workspace);
     g.v_out = g.k_out + half;
+    g.out_v8 = (reinterpret_cast<uintptr_t>(workspace) & 31u) == 0 ? 1 : 0;
     if (store) {
         g.k_in = static_cast<const uint16_t *>(k);
         g.v_in = static_cast<const uint16_t *>(v);

@@ -88,6 +88,7 @@ int launch_store_kvcache(const pa_dims &d, const void *k, const void *v, void *k
 struct GatherArgs {
     int32_t num_kv_heads, head_dim, block_size, max_blocks;
     int32_t scratch_blocks;
+    int32_t out_v8; // the scratch is 32-byte aligned: 32-byte stores
     int64_t num_slots;
     const int8_t *k_codes, *v_codes;      // INT8 cache
     const uint16_t *k_scale, *v_scale;    // fp16 bits

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "quant.cuh"
 
 namespace pa {
@@ -175,10 +176,16 @@ __global__ void __launch_bounds__(256) int8_gather_kernel(const GatherArgs a)
     }
     uint4 o[4];
     quant::dequantise_part(code, sc, o);
-    uint4 *dst = reinterpret_cast<uint4 *>((is_v ? a.v_out : a.k_out) + ((size_t)r * hkv + g) * D + 32 * h);
+    uint16_t *out = (is_v ? a.v_out : a.k_out) + ((size_t)r * hkv + g) * D + 32 * h;
+    if (a.out_v8) { // 32-byte stores: half the store instructions (the gather is bound by them)
+        ptx::st_global_v8(out, o[0].x, o[0].y, o[0].z, o[0].w, o[1].x, o[1].y, o[1].z, o[1].w);
+        ptx::st_global_v8(out + 16, o[2].x, o[2].y, o[2].z, o[2].w, o[3].x, o[3].y, o[3].z, o[3].w);
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(out);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        dst[i] = o[i];
+        for (int i = 0; i < 4; ++i)
+            dst[i] = o[i];
+    }
 }
 
 int launch_int8_gather(const GatherArgs &a, void *stream)
