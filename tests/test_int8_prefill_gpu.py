@@ -169,3 +169,47 @@ def test_int8_prefill_matches_int8_decode():
     torch.cuda.synchronize()
     a, b = out_p[-1].float(), out_d[0].float()
     assert (a - b).abs().max().item() < 1e-2
+
+
+@pytest.mark.parametrize("seed,bs,hkv,d", [(881, 16, 2, 128), (882, 256, 8, 128), (883, 32, 4, 64)])
+def test_int8_gather_scratch_is_code_times_scale_rounded_to_bf16(seed, bs, hkv, d):
+    """The gather's output, read back from the workspace: for every key of every sequence with
+    new tokens, the scratch row the plan's scratch tables give holds RN_bf16(code x fp16 scale)
+    of the cache row its block table names, bit for bit against the oracle's prefill reading
+    (a sequence without new tokens gets no scratch block)."""
+    w = workloads.random_case(seed, num_seqs=7, hq=2 * hkv, hkv=hkv, d=d, bs=bs, max_len=700, cached="random",
+                              device="cuda")
+    b0 = w.batches[0]
+    # sequence 2 without new tokens: its rows taken out of q/k/v
+    qlens = b0.query_lens.copy()
+    start = int(qlens[:2].sum())
+    keep = torch.cat([torch.arange(start), torch.arange(start + int(qlens[2]), int(qlens.sum()))]).to(b0.q.device)
+    qlens[2] = 0
+    batch = workloads.Batch("prefill", b0.seq_lens, qlens, b0.block_lists, b0.q[keep], b0.k[keep], b0.v[keep],
+                            b0.num_heads, b0.scale)
+    gpu, host = int8_pools(w, batch.num_heads)
+    out, plan = run_gpu_batch_int8(w, batch, gpu)
+    slots = oracle.slot_mapping(batch.seq_lens, batch.query_lens, batch.block_lists, bs)
+    oracle.store_kvcache_int8(*host, batch.k, batch.v, slots)
+    # the call above allocated its own workspace; run once more into a zeroed one this test keeps
+    ws = torch.zeros(int(plan.meta.workspace_bytes), dtype=torch.uint8, device="cuda")
+    pa.pa_prefill_varlen_int8(dims_of(w, batch), batch.q.cuda(), *gpu, plan, batch.scale, out, ws)
+    torch.cuda.synchronize()
+    assert pa.pa_read_device_error() == 0
+    int8_equal(gpu, host, what="gather case")
+    m = plan.meta
+    rows = m.scratch_blocks * 128
+    scratch = ws.view(torch.bfloat16).view(2, rows, hkv, d).float().cpu().numpy().astype(np.float64)
+    tab = plan.host_array(m.off_scratch_tables, len(batch.seq_lens) * m.scratch_pitch).reshape(-1, m.scratch_pitch)
+    written = np.zeros(rows, bool)
+    for b, (lk, lq) in enumerate(zip(batch.seq_lens, batch.query_lens)):
+        lk, lq = int(lk), int(lq)
+        if lq == 0:
+            assert (tab[b] == -1).all()
+            continue
+        idx = np.concatenate([np.arange(128) + 128 * int(s) for s in tab[b][: -(-lk // 128)]])[:lk]
+        written[idx] = True
+        for t, (codes, scales) in enumerate(((host[0], host[2]), (host[1], host[3]))):
+            want = oracle.gather_dense_int8(codes, scales, lk, batch.block_lists[b], bs, values="bf16")
+            np.testing.assert_array_equal(scratch[t, idx], want, err_msg=f"sequence {b} tensor {t}")
+    assert not scratch[:, ~written].any(), "rows past a sequence's end were written"
