@@ -85,7 +85,8 @@ typedef struct pa_prefill_meta {
     uint64_t off_slot_mapping;  /* int32 [total_q] */
     uint64_t off_tiles;         /* int32 [num_tiles][8] work list, longest first: sequence,
                                    first query row, KV head, key tiles, first packed
-                                   query row of the sequence, query length, key length, 0 */
+                                   query row of the sequence, query length, key length,
+                                   physical block holding key 0 */
     uint64_t total_bytes;       /* size of the image */
     uint64_t off_scratch_tables; /* int32 [num_seqs][scratch_pitch], -1 padded: the blocks
                                    of sequence b in the INT8 prefill's bf16 scratch cache

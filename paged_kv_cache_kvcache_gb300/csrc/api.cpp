@@ -244,6 +244,7 @@ static int prefill_int8(const char *fn, bool store, const pa_dims *dims, const v
     a.v_cache = g.v_out;
     a.block_tables = scratch_tables;
     a.max_blocks_per_seq = meta->scratch_pitch;
+    a.scratch_cache = true;
     return launch_prefill(a, stream);
 }
 

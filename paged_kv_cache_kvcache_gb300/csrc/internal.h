@@ -17,7 +17,7 @@ constexpr int kPrefillKeyTile = 128;
 constexpr int kPrefillRows = 128;
 constexpr int kPrefillTilesPerItem = 2; // query tiles per prefill work item
 // work-list entry: sequence, first query row, KV head, key tiles, first packed
-// query row of the sequence, query length, key length, 0
+// query row of the sequence, query length, key length, physical block of key 0
 constexpr int kPrefillItemInts = 8;
 // Keys per warp step of the decode kernel and per CTA step (4 warps).
 constexpr int kDecodeChunk = 16;
@@ -129,6 +129,9 @@ struct PrefillArgs {
     // fused store with a cached prefix that does not end on a box boundary: fetch keys in
     // boxes of 16 rows, so that the box straddling the prefix end has few rows to patch
     bool small_boxes;
+    // the cache is the INT8 prefill's scratch (block tables: the plan's scratch tables,
+    // so the work entries' block of key 0 does not apply)
+    bool scratch_cache;
 };
 int launch_prefill(const PrefillArgs &a, void *stream);
 

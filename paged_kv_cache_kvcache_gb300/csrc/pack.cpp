@@ -228,7 +228,7 @@ extern "C" int pa_pack_prefill(const pa_dims *dims, int32_t num_seqs, const int3
         e[4] = cu_q[b];       // first packed query row of the sequence
         e[5] = query_lens[b];
         e[6] = seq_lens[b];
-        e[7] = 0;
+        e[7] = block_ids[block_offsets[b]]; // physical block holding key 0
     }
     return PA_OK;
 }

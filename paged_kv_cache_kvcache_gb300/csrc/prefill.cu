@@ -181,6 +181,7 @@ struct Item {
     int npos0, npos1;       // valid positions of query tiles 0 and 1 (tile 1 may be empty)
     int nkt0, nkt1, nkt;    // key tiles of each query tile; nkt = max
     bool tail;              // the last key tile runs past the sequence end
+    int blk0;               // physical block holding key 0 (read by the short-batch kernel only)
 };
 
 // The items of this CTA: rounds of gridDim.x consecutive entries of the list
@@ -209,7 +210,7 @@ struct ItemIter {
         Item w;
         w.ord = o;
         w.b = a0.x, w.q0 = a0.y, w.g = a0.z;
-        w.cq0 = a1.x, w.lq = a1.y, w.lk = a1.z;
+        w.cq0 = a1.x, w.lq = a1.y, w.lk = a1.z, w.blk0 = a1.w;
         const int off = w.lk - w.lq; // absolute position of query row 0
         w.npos0 = min(P, w.lq - w.q0);
         w.npos1 = max(0, min(P, w.lq - w.q0 - P));
@@ -357,6 +358,56 @@ __device__ __forceinline__ void store_rows_pass(const PfParams &p, int row0, int
         }
 }
 
+// All new K/V rows of item w copied by the 256 threads of the softmax warpgroups (thread
+// tid: vectors tid, tid + 256, ...; 8 of K and 8 of V in flight per thread, slots checked as
+// in store_rows_pass).
+template <int D>
+__device__ __forceinline__ void store_item_rows_wide(const PfParams &p, const Item &w, int tid)
+{
+    constexpr int VPR = D / 8, kU = 8, kThreadsW = 256;
+    const size_t hkv = (size_t)p.num_kv_heads;
+    const int total = store_vectors<D>(w, 0, 1);
+    for (int i0 = tid; i0 < total; i0 += kThreadsW * kU) {
+        uint4 kx[kU], vx[kU];
+        int slot[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int i = i0 + kThreadsW * u;
+            slot[u] = -1;
+            if (i < total) {
+                const int row = w.cq0 + w.q0 + i / VPR;
+                const int s = __ldg(p.slot_mapping + row);
+                const size_t from = ((size_t)row * hkv + w.g) * VPR + i % VPR;
+                kx[u] = __ldg(p.k_in + from);
+                vx[u] = __ldg(p.v_in + from);
+                if (s >= 0 && s < p.num_slots)
+                    slot[u] = s;
+                else if (s != -1)
+                    atomicOr(&g_prefill_error, 2u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (slot[u] >= 0) {
+                const size_t to = ((size_t)slot[u] * hkv + w.g) * VPR + (i0 + kThreadsW * u) % VPR;
+                p.k_cache[to] = kx[u];
+                p.v_cache[to] = vx[u];
+            }
+    }
+}
+
+// a `first` past every item's positions: the call copies nothing
+constexpr int kNoRows = 1 << 20;
+
+// Short kernel, fused store: an item of at least 128 positions has its rows copied by the
+// softmax warps at its start (measured: 8 x 128 prompts 10.7 -> 9.8 us per launch); a
+// smaller one by the three loader warps as in the other kernel (8 x 32: 6.7 against 7.0).
+template <int D>
+__device__ __forceinline__ bool wide_copy(const Item &w)
+{
+    return store_vectors<D>(w, 0, 1) >= 128 * (D / 8);
+}
+
 template <int D>
 __device__ __forceinline__ void store_item_rows(const PfParams &p, const Item &w, int lane, int first = 0,
                                                 int step = 1)
@@ -409,7 +460,14 @@ __device__ __forceinline__ void prefetch_query_tiles(const CUtensorMap *tm_q, co
             ptx::tma_prefetch_3d(tm_q, pp * 64, w.g * G, w.cq0 + w.q0 + t * P);
 }
 
-template <int D>
+// kShort: the instantiation for batches of at most one work item per CTA (short
+// prompts, where each item's start-up latency is the launch's time): its loaders
+// fetch their tensor maps and the first work entry while the barriers are set up,
+// and the first key box comes from the block named in the work entry (so not used
+// over the INT8 prefill's scratch cache, whose blocks the entries do not name).  The large
+// batches keep the other instantiation, whose register allocation those additions
+// would disturb (measured 1.5-2 % slower there).
+template <int D, bool kShort>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kin,
@@ -431,6 +489,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const Waiter wait{abort_flag};
     const int G = p.group;
     const int P = p.rows_per_tile;
+
+    if constexpr (kShort) {
+        if (warp >= 8 && lane == 0) {
+            if (warp == kLoaderWarp) {
+                ptx::prefetch_tmap(&tm_q);
+                ptx::prefetch_l1(p.tiles + 2 * ItemIter::index(0));
+            } else if (warp == kKProducerWarp) {
+                ptx::prefetch_tmap(&tm_k);
+                if (p.fused)
+                    ptx::prefetch_tmap(&tm_kin);
+            } else if (warp == kVProducerWarp) {
+                ptx::prefetch_tmap(&tm_v);
+                if (p.fused)
+                    ptx::prefetch_tmap(&tm_vin);
+            }
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
@@ -481,14 +556,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int off = w.lk - w.lq; // cached prefix
             if (p.fused && key >= off)
                 return -(w.cq0 + key - off + 1);
-            const int phys = __ldg(bt + key / bs);
+            const int phys = kShort && key < bs ? w.blk0 : __ldg(bt + key / bs);
             return phys * bs + (key & (bs - 1));
         };
         if (warp == kLoaderWarp) {
             // ------------------------------------------------------------ bf16: Q producer
             ItemIter items(p.tiles, p.num_items, P);
             zero_query_padding<D>(sgen, G * P, lane);
-            if (lane == 0)
+            if (!kShort && lane == 0)
                 ptx::prefetch_tmap(&tm_q);
             bool ok = true;
             uint32_t early = 0; // bit t: query tile t of the current item was loaded during the previous item's copy
@@ -524,8 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     early |= 1u << t;
                                 }
                         }
-                    } else { // the CTA's last item: a third of its rows (the producers copy the rest)
-                        store_item_rows<D>(p, w, lane, 0, 3);
+                    } else { // the CTA's last item: a third of its rows (the producers copy the rest;
+                             // the short kernel's softmax warps copy all of them: no row here)
+                        store_item_rows<D>(p, w, lane, kShort && wide_copy<D>(w) ? kNoRows : 0, 3);
                     }
                 }
             }
@@ -537,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ring = sbase + (is_k ? L::kK : L::kV);
             const CUtensorMap *tm = is_k ? &tm_k : &tm_v;
             const CUtensorMap *tm_in = is_k ? &tm_kin : &tm_vin;
-            if (lane == 0) {
+            if (!kShort && lane == 0) {
                 ptx::prefetch_tmap(tm);
                 if (p.fused)
                     ptx::prefetch_tmap(tm_in);
@@ -601,8 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // fused store: this producer's third of the rows of the CTA's last item (its work
             // entry is still the iterator's last one)
-            if (ok && p.fused && items.ord > 0)
-                store_item_rows<D>(p, items.decode(items.ord - 1), lane, is_k ? 1 : 2, 3);
+            if (ok && p.fused && items.ord > 0) {
+                const Item last = items.decode(items.ord - 1);
+                store_item_rows<D>(p, last, lane, kShort && wide_copy<D>(last) ? kNoRows : (is_k ? 1 : 2), 3);
+            }
         } else if (warp == kMmaWarp) {
             // ------------------------------------------------------------ MMA issuer (the whole warp,
             // one elected lane issuing each MMA and commit)
@@ -748,6 +826,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.scale_log2;
         uint32_t ns = 0, no = 0; // S tiles and items of this query tile so far (parities)
         bool ok = true;
+        if constexpr (kShort) {
+            // fused store, one item per CTA: the eight softmax warps copy its new K/V rows
+            // while they wait for its first scores (one pass of 8 K and 8 V vectors per
+            // thread covers 64 KB of rows), if it has at least 128 positions
+            if (p.fused && items.more() && wide_copy<D>(items.peek()))
+                store_item_rows_wide<D>(p, items.peek(), (int)threadIdx.x);
+        }
 
         while (ok && items.more()) {
             const Item w = items.next(false);
@@ -912,11 +997,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
-int launch(const PrefillArgs &a, cudaStream_t stream)
+template <int D, bool kShort>
+int launch(const PrefillArgs &a, cudaStream_t stream, int sms)
 {
     using L = PfLayout<D>;
-    if (int rc = ensure_smem<prefill_kernel<D>>(L::kSmemBytes, "prefill"))
+    if (int rc = ensure_smem<prefill_kernel<D, kShort>>(L::kSmemBytes, "prefill"))
         return rc;
     // The register hand-over inside the kernel assumes kLaunchRegs per thread at
     // launch; with fewer the softmax warpgroups' request could never be granted.
@@ -924,7 +1009,7 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     int nreg = launch_regs.load(std::memory_order_acquire);
     if (nreg == 0) {
         cudaFuncAttributes fa{};
-        const cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+        const cudaError_t e = cudaFuncGetAttributes(&fa, prefill_kernel<D, kShort>);
         if (e != cudaSuccess)
             return fail(PA_ERR_CUDA, "prefill kernel attributes: %s", cudaGetErrorString(e));
         launch_regs.store(nreg = fa.numRegs, std::memory_order_release);
@@ -986,11 +1071,8 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
     p.k_cache = static_cast<uint4 *>(const_cast<void *>(a.k_cache));
     p.v_cache = static_cast<uint4 *>(const_cast<void *>(a.v_cache));
     // persistent: one CTA per SM (shared memory and TMEM admit one), each walking its items
-    int sms = 0;
-    if (int rc2 = sm_count(&sms))
-        return rc2;
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-    prefill_kernel<D><<<(unsigned)grid, kThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tkin, tvin, p);
+    prefill_kernel<D, kShort><<<(unsigned)grid, kThreads, L::kSmemBytes, stream>>>(tq, tk, tv, tkin, tvin, p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -1004,7 +1086,12 @@ int launch(const PrefillArgs &a, cudaStream_t stream)
 int launch_prefill(const PrefillArgs &a, void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return a.dims.head_dim == 128 ? launch<128>(a, s) : launch<64>(a, s);
+    int sms = 0;
+    if (int rc = sm_count(&sms))
+        return rc;
+    if (a.num_tiles <= sms && !a.scratch_cache) // at most one work item per CTA
+        return a.dims.head_dim == 128 ? launch<128, true>(a, s, sms) : launch<64, true>(a, s, sms);
+    return a.dims.head_dim == 128 ? launch<128, false>(a, s, sms) : launch<64, false>(a, s, sms);
 }
 
 int read_prefill_error(uint32_t *code)

@@ -129,9 +129,9 @@ def test_pack_prefill_matches_definitions(name):
         P = plan.meta.rows_per_tile
         assert P == 128 // G
         cover = {}
-        for s, q0, g, nkt, cq, lq_, lk_, zero in tiles.tolist():
+        for s, q0, g, nkt, cq, lq_, lk_, blk0 in tiles.tolist():
             lq, lk = int(batch.query_lens[s]), int(batch.seq_lens[s])
-            assert (cq, lq_, lk_, zero) == (int(cu_q[s]), lq, lk, 0)
+            assert (cq, lq_, lk_, blk0) == (int(cu_q[s]), lq, lk, int(batch.block_lists[s][0]))
             assert q0 % (2 * P) == 0
             last = min(q0 + 2 * P, lq) - 1
             assert nkt == -(-(lk - lq + last + 1) // 128)
