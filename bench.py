@@ -696,12 +696,12 @@ def main():
                    "decode": traffic.get("decode")}
     if int8:
         pk_name = ("pa_prefill_varlen_int8_fused (int8_gather_kernel<128,true>: quantising store of the new rows "
-                   "+ bf16 dequantisation into the scratch cache; then prefill_kernel<128>)" if step.prefill_fused else
+                   "+ bf16 dequantisation into the scratch cache; then prefill_kernel<128,false>)" if step.prefill_fused else
                    "pa_prefill_varlen_int8 (int8_gather_kernel<128,false>: bf16 dequantisation into the scratch "
-                   "cache; then prefill_kernel<128>)")
+                   "cache; then prefill_kernel<128,false>)")
     else:
-        pk_name = ("pa_prefill_varlen_fused (prefill_kernel<128>, store of the new K/V fused)"
-                   if step.prefill_fused else "pa_prefill_varlen (prefill_kernel<128>)")
+        pk_name = ("pa_prefill_varlen_fused (prefill_kernel<128,false>, store of the new K/V fused)"
+                   if step.prefill_fused else "pa_prefill_varlen (prefill_kernel<128,false>)")
     roof_p = {"kernel": pk_name,
               "bound": "tensor", "achieved": round(pk_tflops, 2),
               "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(pk_tflops / bf16_peak, 4),
@@ -743,7 +743,7 @@ def main():
         pf = prefill_flops(step.bp)
         t_low = (pf / (bf16_peak * 1e12) + dbytes / (hbm_peak * 1e9)) * 1e3
         gbs = dbytes / (t_prefill_kernel * 1e-3) / 1e9
-        roof_p = {"kernel": "pa_prefill_varlen (prefill_kernel<128>), prefill + decode rows", "bound": "hbm",
+        roof_p = {"kernel": "pa_prefill_varlen (prefill_kernel<128,false>), prefill + decode rows", "bound": "hbm",
                   "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(gbs / hbm_peak, 4),
                   "peak_source": f"{peak_src} hbm_gbs", "traffic": None, "work_per_launch": dbytes,
                   "ms_per_launch": round(t_prefill_kernel, 5)}
