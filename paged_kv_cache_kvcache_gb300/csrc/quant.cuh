@@ -1,5 +1,6 @@
-// INT8 KV quantiser, shared by the quantising store kernel and the store pass of
-// the fused INT8 prefill, so both write the same codes and scales bit for bit.
+// INT8 KV quantiser, shared by the quantising store kernel and the gather of the
+// fused INT8 prefill, so both write the same codes and scales bit for bit; and the
+// bf16 dequantiser of the INT8 prefill's gather.
 //
 // Source: "面试问答准备: nano-vLLM 推理引擎优化", Q3 (KV cache quantisation):
 // each (token, KV head) vector gets scale = max|x| / 127 (floored at 1e-8) and
