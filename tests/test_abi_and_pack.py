@@ -400,3 +400,17 @@ def test_pack_prefill_scratch_tables():
     assert m.off_scratch_tables >= m.off_tiles + 4 * 8 * m.num_tiles
     assert m.off_scratch_items >= m.off_scratch_tables + 4 * 5 * 8 and m.off_scratch_items % 16 == 0
     assert m.off_scratch_items + 4 * 8 * 14 <= m.total_bytes
+
+
+def test_pack_prefill_scratch_without_new_tokens():
+    """No sequence with new tokens: no scratch block, no workspace, tables all -1 (and no work)."""
+    dims = pa.make_dims(64, 16, 4, 2, 64)
+    plan = pa.pa_pack_prefill(dims, [40, 17], [0, 0], [[0, 1, 2], [3, 4]], pin=False)
+    m = plan.meta
+    assert (m.num_tiles, m.scratch_blocks, m.workspace_bytes, m.scratch_pitch) == (0, 0, 0, 1)
+    assert list(plan.host_array(m.off_scratch_tables, 2)) == [-1, -1]
+    # the INT8 prefill over such a plan launches nothing and needs no workspace
+    L = pa.lib()
+    f = ctypes.c_float
+    assert L.pa_prefill_varlen_int8(ctypes.byref(dims), None, None, None, None, None, None, None, None, None, None,
+                                    f(0.1), None, ctypes.byref(m), None, None, 0, None) == pa.PA_OK
