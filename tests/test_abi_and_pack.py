@@ -26,6 +26,21 @@ def test_library_exports_every_declared_symbol():
     assert pa.pa_version() == 0x000500
 
 
+def test_binding_argument_counts_match_the_header():
+    """Every declaration's parameter count equals the binding's ctypes argument list, so a
+    signature change in the header cannot leave the binding calling with the old layout."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    lib = pa.lib()
+    checked = 0
+    for name, params in re.findall(r"^(?:int|const char \*)\s*(pa_\w+)\s*\(([^)]*)\)\s*;", text, flags=re.M):
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        argtypes = getattr(lib, name).argtypes
+        assert argtypes is not None and len(argtypes) == n, (name, n, argtypes)
+        checked += 1
+    assert checked == len(pa.EXPORTS)
+
+
 def test_struct_sizes_match_header_layout():
     assert ctypes.sizeof(pa.pa_dims) == 20
     assert ctypes.sizeof(pa.pa_prefill_meta) == 8 * 4 + 9 * 8 + 2 * 4
